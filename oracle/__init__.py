@@ -1,0 +1,131 @@
+"""fp64 CPU oracle for fused BSHD attention (forward + backward).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may call this module; the product package never
+imports it.  It shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (plain loops over a fully materialised
+score matrix, one (batch, head) at a time).  This module only compiles it with
+gcc on first use and marshals numpy arrays through ctypes.
+
+Definitions followed (see ``oracle.c`` for the full statement):
+  * "Speed up attention on GPU with cuDNN and TransformerEngine", section "How
+    attention works" and steps 4 and 7 (naive attention, causal masking);
+  * "JAX: Single-GPU Attention with TransformerEngine", sections 1, 4 and
+    "Other attention knobs" (GQA, sliding window, MLA head dims, scale_factor,
+    sink softmax types);
+  * "[JAX] Add support for sink attention in JAX #2225", Greptile summaries and
+    the review thread on the off-by-one offset (vanilla / off-by-one / learnable).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+VANILLA, OFF_BY_ONE, LEARNABLE = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_oracle.so (gcc, OpenMP, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        i, d = ctypes.c_int, ctypes.c_double
+        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp,
+                                   dp, dp, dp, dp]
+        lib.oracle_fwd.restype = ctypes.c_int
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp,
+                                   dp, dp, dp, dp, dp]
+        lib.oracle_bwd.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_scale(d_qk: int) -> float:
+    """1/sqrt(d_qk): the codelab's 1/sqrt(d_k) (the Q/K head dim under MLA dims)."""
+    return 1.0 / np.sqrt(d_qk)
+
+
+def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
+                  offset=None, scale=None):
+    """O, LSE, p_sink, rowsum for BSHD q [B,Sq,Hq,dqk], k [B,Skv,Hkv,dqk], v [B,Skv,Hkv,dv].
+
+    Returns a dict of float64 arrays: o [B,Sq,Hq,dv]; lse, psink, rowsum [B,Hq,Sq].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, dqk = q.shape
+    _, Skv, Hkv, dv = v.shape
+    assert k.shape == (B, Skv, Hkv, dqk)
+    scale = default_scale(dqk) if scale is None else float(scale)
+    off = _f64(offset).reshape(-1) if offset is not None else None
+    o = np.zeros((B, Sq, Hq, dv))
+    lse = np.zeros((B, Hq, Sq))
+    psink = np.zeros((B, Hq, Sq))
+    rowsum = np.zeros((B, Hq, Sq))
+    rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, dqk, dv,
+                            scale, int(bool(causal)), int(window), int(softmax_type),
+                            _ptr(off), _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
+    if rc != 0:
+        raise ValueError("oracle_fwd rejected its arguments")
+    return {"o": o, "lse": lse, "psink": psink, "rowsum": rowsum}
+
+
+def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA,
+                  offset=None, scale=None):
+    """dq, dk, dv, d_offset [Hq], D [B,Hq,Sq] (= dO.O) for the same arguments as fwd."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Sq, Hq, dqk = q.shape
+    _, Skv, Hkv, dv = v.shape
+    assert dout.shape == (B, Sq, Hq, dv)
+    scale = default_scale(dqk) if scale is None else float(scale)
+    off = _f64(offset).reshape(-1) if offset is not None else None
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dvv = np.zeros_like(v)
+    doff = np.zeros(Hq)
+    D = np.zeros((B, Hq, Sq))
+    rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Sq, Skv, Hq, Hkv,
+                            dqk, dv, scale, int(bool(causal)), int(window),
+                            int(softmax_type), _ptr(off), _ptr(dq), _ptr(dk), _ptr(dvv),
+                            _ptr(doff), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_bwd rejected its arguments")
+    return {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}

@@ -1,0 +1,261 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for fused BSHD scaled-dot-product attention,
+ * forward and backward, with grouped-query heads, a causal left window, distinct
+ * Q/K and V head dims and the three sink softmax types.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: it exists so that the tests, the smoke check and the CPU baseline of
+ * the benchmark can check the CUDA kernels against an independent definition.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * What it computes, and where the definition comes from:
+ *   - "Speed up attention on GPU with cuDNN and TransformerEngine", section
+ *     "How attention works": Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V in
+ *     four steps (score, scale + softmax, attend, output of Q's shape).
+ *   - Same codelab, step 4 "Implement attention from scratch": the score matrix
+ *     is materialised in full, one (batch, head) at a time.  This file does the
+ *     same: every (b, h) gets its own S_q x S_kv score/probability matrix.
+ *   - Same codelab, step 7 "Add causal masking": query i sees keys j <= i.
+ *   - "JAX: Single-GPU Attention with TransformerEngine", section 1 (GQA + SWA
+ *     baseline: K/V heads are repeated for the query heads of a group; the causal
+ *     sliding-window mask is applied explicitly) and section "Other attention
+ *     knobs" (scale_factor overrides 1/sqrt(head_dim); sink softmax types).
+ *   - "[JAX] Add support for sink attention in JAX #2225", Greptile summaries
+ *     (sequence diagrams): vanilla exp(S_i)/sum exp(S); off-by-one
+ *     exp(S_i)/(1 + sum exp(S)); learnable exp(S_ji)/(exp(alpha_j) + sum_i exp(S_ji))
+ *     with one alpha per head, which receives a gradient in the backward.
+ *
+ * Readings taken where the pages are silent or at odds (each one is listed in the
+ * design notes of the repository):
+ *   - the sink is an extra logit c with no value vector: c = -inf (vanilla),
+ *     c = 0 (off-by-one: the review thread of PR 2225 settles 0, not 1, which
+ *     makes "+1" in the denominator), c = offset[h] (learnable, one per query head,
+ *     not multiplied by the scale);
+ *   - window w >= 0 with causal: query i sees keys i-w <= j <= i (top-left
+ *     diagonal); w < 0 means no window;
+ *   - kv head of query head h is h / (H_q / H_kv) (contiguous groups);
+ *   - LSE = M_i + ln Z_i includes the sink; a row with no visible key and no sink
+ *     gives O = 0, LSE = -inf, and contributes nothing to the backward.
+ *
+ * Backward (derived from the definition; the pages only name the outputs
+ * dq, dk, dv, d_softmax_offset):
+ *   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,   dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_{h in group} sum_i dS_ij q_i,
+ *   dV_j = sum_{h in group} sum_i P_ij dO_i,  d offset_h = -sum_{b,i} p_sink_i D_i.
+ *
+ * All tensors are contiguous BSHD (batch, sequence, head, head-dim) in double,
+ * except lse / psink / rowsum / D which are [B, H_q, S_q] and offset [H_q].
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_VANILLA 0
+#define ORACLE_OFF_BY_ONE 1
+#define ORACLE_LEARNABLE 2
+
+static size_t bshd(int b, int s, int h, int c, int S, int H, int D) {
+    return (((size_t)b * S + s) * H + h) * D + c;
+}
+
+/* Is key j visible to query i?  Causal: j <= i.  Window w >= 0: j >= i - w. */
+static int visible(int i, int j, int causal, int window) {
+    if (causal && j > i) return 0;
+    if (window >= 0 && j < i - window) return 0;
+    return 1;
+}
+
+/* The sink logit c of query head h (see the readings above). */
+static double sink_logit(int softmax_type, const double* offset, int h) {
+    if (softmax_type == ORACLE_OFF_BY_ONE) return 0.0;
+    if (softmax_type == ORACLE_LEARNABLE) return offset[h];
+    return -INFINITY;
+}
+
+/*
+ * Probabilities of one (b, h): P[i*Skv + j] for every visible pair, 0 elsewhere,
+ * plus LSE_i and p_sink_i.  Steps "score" and "scale + softmax" of the codelab,
+ * with the sink logit joining the max and the denominator.
+ */
+static void probs_one_head(const double* q, const double* k, int b, int h, int g,
+                           int Sq, int Skv, int Hq, int Hkv, int dqk,
+                           double scale, int causal, int window, double c,
+                           double* P, double* lse, double* psink) {
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Sq; i++) {
+        double* row = P + (size_t)i * Skv;
+        /* score: s_ij = scale * q_i . k_j, on visible pairs only */
+        double m = c; /* running max starts at the sink logit (-inf for vanilla) */
+        for (int j = 0; j < Skv; j++) {
+            if (!visible(i, j, causal, window)) { row[j] = -INFINITY; continue; }
+            double s = 0.0;
+            for (int t = 0; t < dqk; t++)
+                s += q[bshd(b, i, h, t, Sq, Hq, dqk)] * k[bshd(b, j, g, t, Skv, Hkv, dqk)];
+            s *= scale;
+            row[j] = s;
+            if (s > m) m = s;
+        }
+        double z = 0.0;
+        if (m == -INFINITY) { /* no visible key and no sink: empty row */
+            for (int j = 0; j < Skv; j++) row[j] = 0.0;
+            lse[i] = -INFINITY;
+            psink[i] = 0.0;
+            continue;
+        }
+        if (c != -INFINITY) z += exp(c - m);
+        for (int j = 0; j < Skv; j++)
+            if (row[j] != -INFINITY) z += exp(row[j] - m);
+        for (int j = 0; j < Skv; j++)
+            row[j] = (row[j] == -INFINITY) ? 0.0 : exp(row[j] - m) / z;
+        lse[i] = m + log(z);
+        psink[i] = (c == -INFINITY) ? 0.0 : exp(c - lse[i]);
+    }
+}
+
+/*
+ * Forward.  o: [B,Sq,Hq,dv]; lse, psink, rowsum: [B,Hq,Sq] (psink/rowsum may be
+ * NULL).  rowsum_i = sum_j P_ij (1 for vanilla, 1 - p_sink for the sink types).
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_fwd(const double* q, const double* k, const double* v,
+               int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
+               double scale, int causal, int window, int softmax_type, const double* offset,
+               double* o, double* lse, double* psink, double* rowsum) {
+    if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
+    int G = Hq / Hkv;
+    double* P = (double*)malloc(sizeof(double) * ((size_t)Sq * Skv + 1));
+    double* ps = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
+    if (!P || !ps) { free(P); free(ps); return -1; }
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < Hq; h++) {
+            int g = h / G;
+            double c = sink_logit(softmax_type, offset, h);
+            double* lrow = lse + ((size_t)b * Hq + h) * Sq;
+            probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
+                           P, lrow, ps);
+            /* attend: O_i = sum_j P_ij v_j */
+#pragma omp parallel for schedule(static)
+            for (int i = 0; i < Sq; i++) {
+                for (int t = 0; t < dv; t++) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Skv; j++)
+                        acc += P[(size_t)i * Skv + j] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
+                    o[bshd(b, i, h, t, Sq, Hq, dv)] = acc;
+                }
+                if (rowsum) {
+                    double r = 0.0;
+                    for (int j = 0; j < Skv; j++) r += P[(size_t)i * Skv + j];
+                    rowsum[((size_t)b * Hq + h) * Sq + i] = r;
+                }
+                if (psink) psink[((size_t)b * Hq + h) * Sq + i] = ps[i];
+            }
+        }
+    }
+    free(P);
+    free(ps);
+    return 0;
+}
+
+/*
+ * Backward.  Inputs q,k,v,dout (BSHD).  Outputs dq [B,Sq,Hq,dqk], dk [B,Skv,Hkv,dqk],
+ * dv [B,Skv,Hkv,dv], d_offset [Hq] (may be NULL unless learnable; written for
+ * every type, zero for vanilla / off-by-one since they have no parameter),
+ * Dout [B,Hq,Sq] = dO_i . O_i (may be NULL).  Recomputes P and O from scratch.
+ */
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
+               int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
+               double scale, int causal, int window, int softmax_type, const double* offset,
+               double* dq, double* dk, double* dvout, double* d_offset, double* Dout) {
+    if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
+    int G = Hq / Hkv;
+    size_t nP = (size_t)Sq * Skv + 1;
+    double* P = (double*)malloc(sizeof(double) * nP);
+    double* dS = (double*)malloc(sizeof(double) * nP);
+    double* O = (double*)malloc(sizeof(double) * ((size_t)Sq * dv + 1));
+    double* D = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
+    double* lse = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
+    double* ps = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
+    if (!P || !dS || !O || !D || !lse || !ps) {
+        free(P); free(dS); free(O); free(D); free(lse); free(ps);
+        return -1;
+    }
+    memset(dk, 0, sizeof(double) * (size_t)B * Skv * Hkv * dqk);
+    memset(dvout, 0, sizeof(double) * (size_t)B * Skv * Hkv * dv);
+    if (d_offset) for (int h = 0; h < Hq; h++) d_offset[h] = 0.0;
+
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < Hq; h++) {
+            int g = h / G;
+            double c = sink_logit(softmax_type, offset, h);
+            probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
+                           P, lse, ps);
+#pragma omp parallel for schedule(static)
+            for (int i = 0; i < Sq; i++) {
+                /* O_i = sum_j P_ij v_j, then D_i = dO_i . O_i */
+                double Di = 0.0;
+                for (int t = 0; t < dv; t++) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Skv; j++)
+                        acc += P[(size_t)i * Skv + j] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
+                    O[(size_t)i * dv + t] = acc;
+                    Di += dout[bshd(b, i, h, t, Sq, Hq, dv)] * acc;
+                }
+                D[i] = Di;
+                /* dP_ij = dO_i . v_j ; dS_ij = P_ij (dP_ij - D_i) */
+                for (int j = 0; j < Skv; j++) {
+                    double pij = P[(size_t)i * Skv + j];
+                    if (pij == 0.0) { dS[(size_t)i * Skv + j] = 0.0; continue; }
+                    double dp = 0.0;
+                    for (int t = 0; t < dv; t++)
+                        dp += dout[bshd(b, i, h, t, Sq, Hq, dv)] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
+                    dS[(size_t)i * Skv + j] = pij * (dp - Di);
+                }
+                /* dQ_i = scale sum_j dS_ij k_j */
+                for (int t = 0; t < dqk; t++) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Skv; j++)
+                        acc += dS[(size_t)i * Skv + j] * k[bshd(b, j, g, t, Skv, Hkv, dqk)];
+                    dq[bshd(b, i, h, t, Sq, Hq, dqk)] = scale * acc;
+                }
+            }
+            /* dK_j += scale sum_i dS_ij q_i ; dV_j += sum_i P_ij dO_i  (sum over the group) */
+#pragma omp parallel for schedule(static)
+            for (int j = 0; j < Skv; j++) {
+                for (int t = 0; t < dqk; t++) {
+                    double acc = 0.0;
+                    for (int i = 0; i < Sq; i++)
+                        acc += dS[(size_t)i * Skv + j] * q[bshd(b, i, h, t, Sq, Hq, dqk)];
+                    dk[bshd(b, j, g, t, Skv, Hkv, dqk)] += scale * acc;
+                }
+                for (int t = 0; t < dv; t++) {
+                    double acc = 0.0;
+                    for (int i = 0; i < Sq; i++)
+                        acc += P[(size_t)i * Skv + j] * dout[bshd(b, i, h, t, Sq, Hq, dv)];
+                    dvout[bshd(b, j, g, t, Skv, Hkv, dv)] += acc;
+                }
+            }
+            /* d offset_h = -sum_i p_sink_i D_i  (learnable only; a sum over b too) */
+            if (softmax_type == ORACLE_LEARNABLE && d_offset) {
+                double acc = 0.0;
+                for (int i = 0; i < Sq; i++) acc += ps[i] * D[i];
+                d_offset[h] -= acc;
+            }
+            if (Dout)
+                for (int i = 0; i < Sq; i++) Dout[((size_t)b * Hq + h) * Sq + i] = D[i];
+        }
+    }
+    free(P); free(dS); free(O); free(D); free(lse); free(ps);
+    return 0;
+}
+
+/* Number of OpenMP threads the oracle runs with (1 when built without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
