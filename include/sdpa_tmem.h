@@ -1,0 +1,119 @@
+/*
+ * sdpa_tmem.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product attention
+ * library libsdpa_tmem.so: forward and backward of
+ *
+ *     O = softmax(scale * Q K^T + mask) V      on BSHD tensors,
+ *
+ * with grouped-query heads, a causal mask with an optional left sliding window,
+ * distinct Q/K and V head dims, and three sink softmax types.
+ *
+ * Where each operation is defined:
+ *   - the attention itself: "Speed up attention on GPU with cuDNN and
+ *     TransformerEngine", section "How attention works" (score, scale + softmax,
+ *     attend, output of Q's shape), step 7 (causal: query i sees keys j <= i);
+ *   - BSHD layout, GQA (num_gqa_groups: each K/V head serves H_q/H_kv query
+ *     heads), causal sliding window, MLA head dims (Q/K dim != V dim, layout
+ *     bshd_bshd_bshd), scale_factor defaulting to 1/sqrt(head_dim), sink softmax
+ *     types and deterministic backward: "JAX: Single-GPU Attention with
+ *     TransformerEngine", sections 1, 2, 4 and "Other attention knobs";
+ *   - the sink softmax denominators and the learnable offset's gradient:
+ *     "[JAX] Add support for sink attention in JAX #2225", Greptile summaries
+ *     (vanilla exp(S_i)/sum exp(S); off-by-one exp(S_i)/(1 + sum exp(S));
+ *     learnable exp(S_ji)/(exp(alpha_j) + sum_i exp(S_ji)), the backward
+ *     returning grad_softmax_offset).
+ *
+ * Conventions shared by every call:
+ *   - All pointers are DEVICE pointers owned by the caller; the library allocates
+ *     no device memory.  Its only state is one device error word per GPU.
+ *   - Big tensors are contiguous BSHD bf16: Q [B,S_q,H_q,d_qk], K [B,S_kv,H_kv,d_qk],
+ *     V [B,S_kv,H_kv,d_v], O and dO [B,S_q,H_q,d_v]; their base addresses must be
+ *     16-byte aligned.  LSE is fp32 [B,H_q,S_q] (natural log, scaled-logit units,
+ *     the sink included); softmax_offset and d_offset are fp32 [H_q].
+ *   - Query head h uses K/V head h / (H_q / H_kv).
+ *   - Masking: key j is visible to query i iff j < S_kv, and (causal == 0 or
+ *     j <= i), and (window < 0 or j >= i - window).  A window needs causal != 0.
+ *     A row that sees no key gets O = 0 and LSE = sink logit (-inf for vanilla).
+ *   - scale <= 0 (or NaN) selects 1/sqrt(d_qk).
+ *   - softmax_type: ATTN_SOFTMAX_VANILLA (no sink), ATTN_SOFTMAX_OFF_BY_ONE (a sink
+ *     logit 0, i.e. +1 in the denominator), ATTN_SOFTMAX_LEARNABLE (sink logit
+ *     softmax_offset[h], not multiplied by scale; softmax_offset required).
+ *   - Supported head dims: d_qk in {64, 128, 192}, d_v in {64, 128}; H_q % H_kv == 0;
+ *     B, H_q <= 65535.  Anything else returns ATTN_ERR_UNSUPPORTED (no fallback).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Outputs are overwritten, never accumulated.  A status other than
+ *     ATTN_OK means nothing was launched, except ATTN_ERR_CUDA, which reports the
+ *     CUDA error of a launch.
+ *   - Kernels never trap.  A pipeline wait that does not complete within about a
+ *     second sets the device error word and the kernel exits; read it with
+ *     attn_last_device_error().
+ */
+#ifndef SDPA_TMEM_H
+#define SDPA_TMEM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ATTN_SOFTMAX_VANILLA = 0, ATTN_SOFTMAX_OFF_BY_ONE = 1, ATTN_SOFTMAX_LEARNABLE = 2 };
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, H_q % H_kv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head dims, window without causal, grid limits */
+  ATTN_ERR_MISALIGNED = 3,    /* a BSHD base address not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 5, /* reported by attn_last_device_error() */
+  ATTN_ERR_WORKSPACE = 6      /* workspace missing, too small or misaligned */
+};
+
+/*
+ * Forward.  Writes o [B,S_q,H_q,d_v] (bf16) and lse [B,H_q,S_q] (fp32).
+ * q, k, v: bf16 BSHD inputs.  softmax_offset: fp32 [H_q] for LEARNABLE, else
+ * ignored (may be NULL).  Empty problems (B == 0 or S_q == 0) return ATTN_OK
+ * without launching.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
+             int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+             const float* softmax_offset, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (256-byte aligned
+ * pointer required).  deterministic != 0 selects the recompute path for dQ, which
+ * needs no fp32 dQ accumulator.  Returns 0 for sizes that attn_bwd rejects.
+ */
+size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic);
+
+/*
+ * Backward of attn_fwd for the same arguments.  Inputs: q, k, v, o (the forward
+ * output), dout = dL/dO (bf16 BSHD) and lse (the forward's fp32 LSE).  Outputs:
+ * dq [B,S_q,H_q,d_qk], dk [B,S_kv,H_kv,d_qk], dv [B,S_kv,H_kv,d_v] (bf16, dK/dV
+ * summed over the query heads of each group) and, for LEARNABLE, d_offset [H_q]
+ * (fp32, summed over batch and rows; NULL is allowed for the other types and is
+ * then not written; for them a non-NULL d_offset receives zeros).
+ * deterministic != 0: bitwise-reproducible results (dQ by a query-stationary
+ * recompute pass); 0: dQ may be accumulated with fp32 atomics where supported.
+ * workspace: device scratch of at least attn_bwd_workspace_size() bytes.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk,
+             int d_v, float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error word:
+ * 0 when no kernel reported a failure, ATTN_ERR_DEVICE_TIMEOUT when a pipeline
+ * wait timed out (the site is written to *site if site != NULL), ATTN_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+int attn_last_device_error(void* stream, int* site);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_TMEM_H */

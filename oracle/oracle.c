@@ -53,6 +53,7 @@
 #define ORACLE_VANILLA 0
 #define ORACLE_OFF_BY_ONE 1
 #define ORACLE_LEARNABLE 2
+#define ORACLE_MAX_D 512 /* largest head dim the oracle accepts */
 
 static size_t bshd(int b, int s, int h, int c, int S, int H, int D) {
     return (((size_t)b * S + s) * H + h) * D + c;
@@ -123,6 +124,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                double* o, double* lse, double* psink, double* rowsum) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
+    if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
     int G = Hq / Hkv;
     double* P = (double*)malloc(sizeof(double) * ((size_t)Sq * Skv + 1));
     double* ps = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
@@ -137,12 +139,14 @@ int oracle_fwd(const double* q, const double* k, const double* v,
             /* attend: O_i = sum_j P_ij v_j */
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
-                for (int t = 0; t < dv; t++) {
-                    double acc = 0.0;
-                    for (int j = 0; j < Skv; j++)
-                        acc += P[(size_t)i * Skv + j] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
-                    o[bshd(b, i, h, t, Sq, Hq, dv)] = acc;
+                double acc[ORACLE_MAX_D];
+                for (int t = 0; t < dv; t++) acc[t] = 0.0;
+                for (int j = 0; j < Skv; j++) {
+                    double pij = P[(size_t)i * Skv + j];
+                    if (pij == 0.0) continue;
+                    for (int t = 0; t < dv; t++) acc[t] += pij * v[bshd(b, j, g, t, Skv, Hkv, dv)];
                 }
+                for (int t = 0; t < dv; t++) o[bshd(b, i, h, t, Sq, Hq, dv)] = acc[t];
                 if (rowsum) {
                     double r = 0.0;
                     for (int j = 0; j < Skv; j++) r += P[(size_t)i * Skv + j];
@@ -169,6 +173,7 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                double* dq, double* dk, double* dvout, double* d_offset, double* Dout) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
+    if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
     int G = Hq / Hkv;
     size_t nP = (size_t)Sq * Skv + 1;
     double* P = (double*)malloc(sizeof(double) * nP);
@@ -194,13 +199,17 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
                 /* O_i = sum_j P_ij v_j, then D_i = dO_i . O_i */
+                double acc[ORACLE_MAX_D];
+                for (int t = 0; t < dv; t++) acc[t] = 0.0;
+                for (int j = 0; j < Skv; j++) {
+                    double pij = P[(size_t)i * Skv + j];
+                    if (pij == 0.0) continue;
+                    for (int t = 0; t < dv; t++) acc[t] += pij * v[bshd(b, j, g, t, Skv, Hkv, dv)];
+                }
                 double Di = 0.0;
                 for (int t = 0; t < dv; t++) {
-                    double acc = 0.0;
-                    for (int j = 0; j < Skv; j++)
-                        acc += P[(size_t)i * Skv + j] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
-                    O[(size_t)i * dv + t] = acc;
-                    Di += dout[bshd(b, i, h, t, Sq, Hq, dv)] * acc;
+                    O[(size_t)i * dv + t] = acc[t];
+                    Di += dout[bshd(b, i, h, t, Sq, Hq, dv)] * acc[t];
                 }
                 D[i] = Di;
                 /* dP_ij = dO_i . v_j ; dS_ij = P_ij (dP_ij - D_i) */
@@ -213,28 +222,28 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                     dS[(size_t)i * Skv + j] = pij * (dp - Di);
                 }
                 /* dQ_i = scale sum_j dS_ij k_j */
-                for (int t = 0; t < dqk; t++) {
-                    double acc = 0.0;
-                    for (int j = 0; j < Skv; j++)
-                        acc += dS[(size_t)i * Skv + j] * k[bshd(b, j, g, t, Skv, Hkv, dqk)];
-                    dq[bshd(b, i, h, t, Sq, Hq, dqk)] = scale * acc;
+                for (int t = 0; t < dqk; t++) acc[t] = 0.0;
+                for (int j = 0; j < Skv; j++) {
+                    double dsij = dS[(size_t)i * Skv + j];
+                    if (dsij == 0.0) continue;
+                    for (int t = 0; t < dqk; t++) acc[t] += dsij * k[bshd(b, j, g, t, Skv, Hkv, dqk)];
                 }
+                for (int t = 0; t < dqk; t++) dq[bshd(b, i, h, t, Sq, Hq, dqk)] = scale * acc[t];
             }
             /* dK_j += scale sum_i dS_ij q_i ; dV_j += sum_i P_ij dO_i  (sum over the group) */
 #pragma omp parallel for schedule(static)
             for (int j = 0; j < Skv; j++) {
-                for (int t = 0; t < dqk; t++) {
-                    double acc = 0.0;
-                    for (int i = 0; i < Sq; i++)
-                        acc += dS[(size_t)i * Skv + j] * q[bshd(b, i, h, t, Sq, Hq, dqk)];
-                    dk[bshd(b, j, g, t, Skv, Hkv, dqk)] += scale * acc;
+                double ak[ORACLE_MAX_D], av[ORACLE_MAX_D];
+                for (int t = 0; t < dqk; t++) ak[t] = 0.0;
+                for (int t = 0; t < dv; t++) av[t] = 0.0;
+                for (int i = 0; i < Sq; i++) {
+                    double dsij = dS[(size_t)i * Skv + j], pij = P[(size_t)i * Skv + j];
+                    if (pij == 0.0) continue;
+                    for (int t = 0; t < dqk; t++) ak[t] += dsij * q[bshd(b, i, h, t, Sq, Hq, dqk)];
+                    for (int t = 0; t < dv; t++) av[t] += pij * dout[bshd(b, i, h, t, Sq, Hq, dv)];
                 }
-                for (int t = 0; t < dv; t++) {
-                    double acc = 0.0;
-                    for (int i = 0; i < Sq; i++)
-                        acc += P[(size_t)i * Skv + j] * dout[bshd(b, i, h, t, Sq, Hq, dv)];
-                    dvout[bshd(b, j, g, t, Skv, Hkv, dv)] += acc;
-                }
+                for (int t = 0; t < dqk; t++) dk[bshd(b, j, g, t, Skv, Hkv, dqk)] += scale * ak[t];
+                for (int t = 0; t < dv; t++) dvout[bshd(b, j, g, t, Skv, Hkv, dv)] += av[t];
             }
             /* d offset_h = -sum_i p_sink_i D_i  (learnable only; a sum over b too) */
             if (softmax_type == ORACLE_LEARNABLE && d_offset) {

@@ -1,0 +1,199 @@
+"""GB300 (sm_103a) fused scaled-dot-product attention, forward and backward.
+
+A thin Python binding over the C ABI of ``libsdpa_tmem.so`` (declared in
+``include/sdpa_tmem.h``): the functions below carry the same names and only
+marshal torch tensors into device pointers and the current CUDA stream.  Every
+step of the computation runs in the library's CUDA kernels; there is no other
+path.  Importing this package does not load the library; the first call does,
+and it raises if the library has not been built.
+
+    from scaled_dot_product_tmem_gb300 import sdpa_forward, sdpa_backward
+    o, lse = sdpa_forward(q, k, v, causal=True, window=1024)
+    dq, dk, dv, d_off = sdpa_backward(q, k, v, o, dout, lse, causal=True, window=1024)
+
+Tensors are BSHD bf16 on the GPU: q [B,S_q,H_q,d_qk], k [B,S_kv,H_kv,d_qk],
+v [B,S_kv,H_kv,d_v]; lse fp32 [B,H_q,S_q]; softmax_offset fp32 [H_q].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+VANILLA, OFF_BY_ONE, LEARNABLE = 0, 1, 2
+SOFTMAX_TYPES = {"vanilla": VANILLA, "off_by_one": OFF_BY_ONE, "learnable": LEARNABLE}
+ATTN_OK = 0
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdpa_tmem.so")
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} (status {status})")
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m scaled_dot_product_tmem_gb300.build`"
+                           " (or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, i, vp, sz,
+                             vp]
+    lib.attn_bwd.restype = i
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    lib.attn_last_device_error.restype = i
+    _lib = lib
+    return lib
+
+
+def library():
+    """The loaded ctypes library (loads it on first use)."""
+    return _load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, ndim):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _stype(softmax_type):
+    return SOFTMAX_TYPES[softmax_type] if isinstance(softmax_type, str) else int(softmax_type)
+
+
+# ----------------------------------------------------------------------------- C ABI, same names
+
+
+def attn_status_string(status: int) -> str:
+    return _load().attn_status_string(int(status)).decode()
+
+
+def attn_last_device_error(stream=None):
+    """Synchronise the stream; return (status, site) of the device error word and clear it."""
+    site = ctypes.c_int(0)
+    st = _load().attn_last_device_error(_stream(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
+             stream=None):
+    """Forward into preallocated o [B,S_q,H_q,d_v] bf16 and lse [B,H_q,S_q] fp32."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    if softmax_offset is not None:
+        _check(softmax_offset, "softmax_offset", torch.float32, 1)
+    B, S_q, H_q, d_qk = q.shape
+    _, S_kv, H_kv, d_v = v.shape
+    st = _load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d_qk, d_v,
+                          float(scale or 0.0), int(bool(causal)), int(window), _stype(softmax_type),
+                          _ptr(softmax_offset), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+
+
+def attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic=True) -> int:
+    return int(_load().attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, int(bool(deterministic))))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, window=-1, softmax_type=VANILLA,
+             softmax_offset=None, scale=0.0, deterministic=True, workspace=None, stream=None):
+    """Backward into preallocated dq, dk, dv (bf16) and d_offset (fp32 [H_q], learnable)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    B, S_q, H_q, d_qk = q.shape
+    _, S_kv, H_kv, d_v = v.shape
+    need = attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = _load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(d_offset), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
+                          int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset),
+                          int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+
+
+# ----------------------------------------------------------------------------- conveniences
+
+
+def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
+                 stream=None):
+    """Allocate O and LSE, run attn_fwd, return (o, lse)."""
+    B, S_q, H_q, _ = q.shape
+    d_v = v.shape[3]
+    o = torch.empty((B, S_q, H_q, d_v), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H_q, S_q), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, causal=causal, window=window, softmax_type=softmax_type,
+             softmax_offset=softmax_offset, scale=scale, stream=stream)
+    return o, lse
+
+
+def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None,
+                  scale=0.0, deterministic=True, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and d_offset for the learnable sink), run attn_bwd, return them."""
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    st = _stype(softmax_type)
+    d_off = torch.empty((q.shape[2],), dtype=torch.float32, device=q.device) if st == LEARNABLE else None
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_off, causal=causal, window=window, softmax_type=st,
+             softmax_offset=softmax_offset, scale=scale, deterministic=deterministic, workspace=workspace,
+             stream=stream)
+    return dq, dk, dv, d_off
+
+
+class SDPAFunction(torch.autograd.Function):
+    """autograd wrapper: forward/backward both run in the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, softmax_offset, causal, window, softmax_type, scale, deterministic):
+        o, lse = sdpa_forward(q, k, v, causal=causal, window=window, softmax_type=softmax_type,
+                              softmax_offset=softmax_offset, scale=scale)
+        ctx.save_for_backward(q, k, v, o, lse, softmax_offset)
+        ctx.cfg = (causal, window, softmax_type, scale, deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse, off = ctx.saved_tensors
+        causal, window, st, scale, det = ctx.cfg
+        dq, dk, dv, d_off = sdpa_backward(q, k, v, o, dout.contiguous(), lse, causal=causal, window=window,
+                                          softmax_type=st, softmax_offset=off, scale=scale, deterministic=det)
+        return dq, dk, dv, d_off, None, None, None, None, None
+
+
+def attention(q, k, v, softmax_offset=None, *, causal=True, window=-1, softmax_type=VANILLA, scale=0.0,
+              deterministic=True):
+    """Differentiable fused attention (q, k, v and the learnable offset receive gradients)."""
+    return SDPAFunction.apply(q, k, v, softmax_offset, causal, window, softmax_type, scale, deterministic)

@@ -1,0 +1,235 @@
+// api.cu -- the C ABI declared in include/sdpa_tmem.h: argument validation,
+// TMA tensor-map creation, workspace carving and kernel dispatch.  No compute.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/sdpa_tmem.h"
+#include "attn_kernels.h"
+#include "tmap.h"
+
+namespace {
+
+__device__ int g_device_error;  // one word per GPU: 0 or kErrTimeoutBase + site
+
+constexpr int kMaxDevices = 64;
+
+int* device_error_ptr() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_supported(int d_qk, int d_v) {
+  return (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
+}
+
+// Shared validation of sizes and flags.  Returns ATTN_OK or an error status.
+int check_common(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int causal, int window,
+                 int softmax_type, const float* softmax_offset) {
+  if (B < 0 || S_q < 0 || S_kv < 0 || H_q <= 0 || H_kv <= 0) return ATTN_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (softmax_type < ATTN_SOFTMAX_VANILLA || softmax_type > ATTN_SOFTMAX_LEARNABLE) return ATTN_ERR_INVALID_ARG;
+  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && softmax_offset == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!dims_supported(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (window >= 0 && !causal) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+float resolve_scale(float scale, int d_qk) {
+  if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(static_cast<float>(d_qk));
+  return scale;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t lse2, dsum, dq_acc, total;
+};
+
+WsLayout ws_layout(int B, int S_q, int H_q, int d_qk, bool need_dq_acc) {
+  const size_t s_pad = (static_cast<size_t>(S_q) + 127) / 128 * 128;
+  const size_t rows = static_cast<size_t>(B) * H_q * s_pad;
+  WsLayout w;
+  w.lse2 = 0;
+  w.dsum = round256(rows * sizeof(float));
+  w.dq_acc = w.dsum + round256(rows * sizeof(float));
+  w.total = w.dq_acc + (need_dq_acc ? round256(static_cast<size_t>(B) * S_q * H_q * d_qk * sizeof(float)) : 0);
+  return w;
+}
+
+bool use_fused_dq(int d_qk, int d_v, int deterministic) {
+  return !deterministic && sdpa::bwd_kv_supports_fused_dq(d_qk, d_v);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+int attn_last_device_error(void* stream, int* site) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* p = device_error_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (site) *site = v;
+  if (v == 0) return ATTN_OK;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
+             int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+             const float* softmax_offset, void* stream) {
+  int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || S_q == 0) return ATTN_OK;
+  if (!q || !o || !lse || (S_kv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  int* err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  // TMA maps need a non-empty tensor; with S_kv == 0 no kv tile is ever loaded.
+  const int skv_map = S_kv > 0 ? S_kv : 1;
+  const void* kk = S_kv > 0 ? k : q;
+  const void* vv = S_kv > 0 ? v : q;
+  CUtensorMap tq, tk, tv;
+  if (!sdpa::make_bshd_map(&tq, q, B, S_q, H_q, d_qk, 128) ||
+      !sdpa::make_bshd_map(&tk, kk, B, skv_map, S_kv > 0 ? H_kv : H_q, d_qk, 128) ||
+      !sdpa::make_bshd_map(&tv, vv, B, skv_map, S_kv > 0 ? H_kv : H_q, S_kv > 0 ? d_v : d_qk, 128))
+    return ATTN_ERR_CUDA;
+  sdpa::FwdParams p;
+  p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
+  p.scale_log2 = resolve_scale(scale, d_qk) * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.window = window < 0 ? -1 : window;
+  p.softmax_type = softmax_type;
+  p.offset = softmax_offset;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = err;
+  int rc = sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+  return rc == 0 ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic) {
+  if (check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, 1, -1, 0, nullptr) != ATTN_OK) return 0;
+  return ws_layout(B, S_q, H_q, d_qk, use_fused_dq(d_qk, d_v, deterministic)).total;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk,
+             int d_v, float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && !d_offset) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0 || (S_q == 0 && S_kv == 0)) {
+    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if ((S_q > 0 && (!q || !o || !dout || !lse || !dq)) || (S_kv > 0 && (!k || !v || !dk || !dv)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(d_offset) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const bool fused = use_fused_dq(d_qk, d_v, deterministic);
+  const WsLayout w = ws_layout(B, S_q, H_q, d_qk, fused);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  int* err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+
+  // No query rows: dK = dV = 0 (no key is seen); no key: dQ = 0.
+  if (S_q == 0) {
+    if (cudaMemsetAsync(dk, 0, (size_t)B * S_kv * H_kv * d_qk * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, (size_t)B * S_kv * H_kv * d_v * 2, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  sdpa::BwdParams p;
+  p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
+  p.scale = resolve_scale(scale, d_qk);
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.window = window < 0 ? -1 : window;
+  p.softmax_type = softmax_type;
+  p.S_pad = (S_q + 127) / 128 * 128;
+  p.offset = softmax_offset;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  p.Dsum = reinterpret_cast<float*>(ws + w.dsum);
+  p.d_offset = d_offset;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
+  p.err = err;
+
+  if (sdpa::launch_bwd_preprocess(d_v, p, s) != 0) return ATTN_ERR_CUDA;
+  if (fused && cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)B * S_q * H_q * d_qk, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (S_kv == 0) {
+    // Every row is empty: O = 0 so D = 0, dQ = 0, d_offset = 0 (written by preprocess).
+    if (cudaMemsetAsync(dq, 0, (size_t)B * S_q * H_q * d_qk * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  const int bq_rows = 64;  // query-tile rows of the kv-stationary kernel
+  if (!sdpa::make_bshd_map(&tq, q, B, S_q, H_q, d_qk, bq_rows) ||
+      !sdpa::make_bshd_map(&tdo, dout, B, S_q, H_q, d_v, bq_rows) ||
+      !sdpa::make_bshd_map(&tk, k, B, S_kv, H_kv, d_qk, 128) ||
+      !sdpa::make_bshd_map(&tv, v, B, S_kv, H_kv, d_v, 128))
+    return ATTN_ERR_CUDA;
+  int rc = sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, p, fused, s);
+  if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+  if (rc != 0) return ATTN_ERR_CUDA;
+  if (fused) {
+    if (sdpa::launch_bwd_dq_convert(d_qk, p, s) != 0) return ATTN_ERR_CUDA;
+  } else {
+    CUtensorMap tq128, tdo128;
+    if (!sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
+        !sdpa::make_bshd_map(&tdo128, dout, B, S_q, H_q, d_v, 128))
+      return ATTN_ERR_CUDA;
+    rc = sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);
+    if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+    if (rc != 0) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,773 @@
+// attn_bwd.cu -- fused BSHD attention backward for sm_103a.
+//
+// With P_ij = exp(scale * q_i.k_j - LSE_i) (the forward's probabilities, sink
+// included in LSE), dP_ij = dO_i.v_j, D_i = dO_i.O_i and dS_ij = P_ij (dP_ij - D_i):
+//   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_{h in group} sum_i dS_ij q_i,
+//   dV_j = sum_{h in group} sum_i P_ij dO_i,
+//   d offset_h = -sum_{b,i} exp(offset_h - LSE_i) D_i        (learnable sink).
+// The pages name these outputs ("[JAX] Add support for sink attention in JAX
+// #2225", Greptile sequence diagrams: the backward returns grad_q, grad_k,
+// grad_v, grad_bias, grad_softmax_offset); the formulas follow from the forward
+// definition ("Speed up attention on GPU with cuDNN and TransformerEngine",
+// section "How attention works").  The sink has no value vector, so D_i = dO_i.O_i
+// and the dS formula are unchanged by it.
+//
+// Kernels:
+//   bwd_preprocess   D and LSE*log2(e) into padded [B, H_q, S_pad] rows.
+//   bwd_doffset      deterministic per-head reduction for d offset.
+//   bwd_kv           kv-stationary: one CTA per (b, kv head, 128 keys) walks the
+//                    query heads of the group x 64-row query tiles that see those
+//                    keys; dK/dV accumulate in TMEM (the GQA head sum is free).
+//                    Optionally also dQ^T = K^T dS^T per step, drained with fp32
+//                    atomics by a fourth warpgroup (non-deterministic path).
+//   bwd_q            query-stationary deterministic dQ: recomputes S, P, dP, dS
+//                    for one 128-row query tile over its kv tiles.
+//   bwd_dq_convert   dQ = bf16(scale * fp32 accumulator).
+#include <cuda_runtime.h>
+
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+// =============================================================================
+// Preprocess: D = rowsum(dO * O) (fp32) and lse2 = LSE * log2(e).
+// Rows are padded to S_pad: D = 0 and lse2 = +inf there, so padded query rows get
+// P = exp2(s - inf) = 0 in the main kernels.
+// =============================================================================
+template <int D_V>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  constexpr int TPR = D_V / 8;  // threads per row, 8 bf16 (16 bytes) each
+  const long long rows = (long long)p.B * p.S_q * p.H_q;
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / TPR;
+  const int sub = threadIdx.x % TPR;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p.o + row * D_V + sub * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(p.dout + row * D_V + sub * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(a2[e]);
+      const float2 fg = __bfloat1622float2(g2[e]);
+      acc = fmaf(fa.x, fg.x, acc);
+      acc = fmaf(fa.y, fg.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
+    // row enumerates (b, i, h) in memory order
+    const int h = (int)(row % p.H_q);
+    const long long bi = row / p.H_q;
+    const int i = (int)(bi % p.S_q);
+    const int b = (int)(bi / p.S_q);
+    const size_t dst = ((size_t)b * p.H_q + h) * p.S_pad + i;
+    p.Dsum[dst] = acc;
+    p.lse2[dst] = p.lse[((size_t)b * p.H_q + h) * p.S_q + i] * kLog2e;
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_pad_kernel(const BwdParams p) {
+  const int pad = p.S_pad - p.S_q;
+  const long long n = (long long)p.B * p.H_q * pad;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
+    const long long bh = t / pad;
+    const int i = p.S_q + (int)(t % pad);
+    p.Dsum[bh * p.S_pad + i] = 0.f;
+    p.lse2[bh * p.S_pad + i] = INFINITY;
+  }
+}
+
+// d offset_h = -sum_{b,i} exp(offset_h - LSE_{b,h,i}) D_{b,h,i}.  One block per
+// head; fixed assignment of terms to threads and a fixed reduction tree, so the
+// result is bitwise reproducible.
+__global__ void __launch_bounds__(256) bwd_doffset_kernel(const BwdParams p) {
+  const int h = blockIdx.x;
+  const float c2 = p.offset[h] * kLog2e;
+  float acc = 0.f;
+  for (int b = 0; b < p.B; ++b) {
+    const float* l2 = p.lse2 + ((size_t)b * p.H_q + h) * p.S_pad;
+    const float* dd = p.Dsum + ((size_t)b * p.H_q + h) * p.S_pad;
+    for (int i = threadIdx.x; i < p.S_q; i += blockDim.x) acc = fmaf(ex2(c2 - l2[i]), dd[i], acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  __shared__ float part[8];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x / 32] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += part[w];
+    p.d_offset[h] = -s;
+  }
+}
+
+int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.S_q * p.H_q;
+  if (rows > 0) {
+    const int tpr = d_v / 8;
+    const long long threads = rows * tpr;
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (d_v == 64)
+      bwd_preprocess_kernel<64><<<blocks, 256, 0, stream>>>(p);
+    else if (d_v == 128)
+      bwd_preprocess_kernel<128><<<blocks, 256, 0, stream>>>(p);
+    else
+      return -2;
+  }
+  if (p.S_pad > p.S_q) bwd_pad_kernel<<<296, 256, 0, stream>>>(p);
+  if (p.softmax_type == 2)
+    bwd_doffset_kernel<<<p.H_q, 256, 0, stream>>>(p);
+  else if (p.d_offset)
+    cudaMemsetAsync(p.d_offset, 0, sizeof(float) * p.H_q, stream);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// =============================================================================
+// kv-stationary main kernel
+// =============================================================================
+template <int D_QK, int D_V, bool FUSE_DQ>
+struct KvCfg {
+  static constexpr int BN = 128;  // keys per CTA (TMEM lanes)
+  static constexpr int BQ = 64;   // query rows per step
+  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
+  static constexpr int KCHUNK = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr int QCHUNK = 64 * 128;   // 64 rows x 128 bytes
+  static constexpr int NQ = (D_QK == 64 && D_V == 64) ? 6 : 3;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + QCH * KCHUNK;
+  static constexpr int OFF_DS = OFF_V + VCH * KCHUNK;  // dS^T [128 keys x 64 q] bf16, swizzled
+  static constexpr int DS_BYTES = FUSE_DQ ? 128 * 128 : 0;
+  static constexpr int OFF_Q = OFF_DS + DS_BYTES;
+  static constexpr int Q_STAGE = QCH * QCHUNK;
+  static constexpr int OFF_DO = OFF_Q + NQ * Q_STAGE;
+  static constexpr int DO_STAGE = VCH * QCHUNK;
+  static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // lse2[64] + D[64] per stage
+  static constexpr int L_STAGE = 2 * BQ * 4;
+  static constexpr int OFF_BAR = OFF_L + NQ * L_STAGE;
+  // kv_full, q_full[NQ], q_empty[NQ], s_ready, dp_ready, p_ready, ds_ready, dq_ready, dq_free, mma_done
+  static constexpr int NBAR = 1 + 2 * NQ + 7;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
+  static constexpr int THREADS = FUSE_DQ ? 448 : 320;
+  // TMEM columns
+  static constexpr int COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
+  static_assert(COL_DQ + (FUSE_DQ ? 64 : 0) <= 512, "TMEM budget");
+  static_assert(!FUSE_DQ || D_QK == 128, "dQ^T = K^T dS^T needs M = d_qk = 128");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM > 116 * 1024, "one CTA per SM");
+};
+
+enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain };
+
+template <int D_QK, int D_V, bool FUSE_DQ>
+__global__ void __maxnreg__(FUSE_DQ ? 144 : 200)
+    attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const BwdParams p) {
+  using C = KvCfg<D_QK, D_V, FUSE_DQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::NQ;
+  uint64_t* s_ready = q_empty + C::NQ;
+  uint64_t* dp_ready = s_ready + 1;
+  uint64_t* p_ready = s_ready + 2;
+  uint64_t* ds_ready = s_ready + 3;
+  uint64_t* dq_ready = s_ready + 4;
+  uint64_t* dq_free = s_ready + 5;
+  uint64_t* mma_done = s_ready + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_tiles = gridDim.x;
+  const int nt = (int)(n_tiles - 1 - blockIdx.x);  // later keys (less work when causal) last
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const int n0 = (p.causal ? (int)blockIdx.x : nt) * C::BN;
+  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
+  int ilo = 0, ihi = -1;
+  const bool any_q = q_tile_range(mask, n0, min(n0 + C::BN - 1, p.S_kv - 1), C::BQ, &ilo, &ihi);
+  const int nq = any_q ? ihi - ilo + 1 : 0;
+  const int nsteps = nq * p.G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::NQ; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
+    mbar_init(s_ready, 1);
+    mbar_init(dp_ready, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(dq_ready, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc<512>(tmem_slot);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int* err = p.err;
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nsteps > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(kv_full, (C::QCH + C::VCH) * C::KCHUNK);
+      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_K + c * C::KCHUNK, &tmK, kv_full, c * 64, hk, n0, b);
+      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_V + c * C::KCHUNK, &tmV, kv_full, c * 64, hk, n0, b);
+      for (int s = 0; s < nsteps; ++s) {
+        const int st = s % C::NQ;
+        if (!mbar_wait(&q_empty[st], ((s / C::NQ) & 1) ^ 1, err, kKvQEmpty)) break;
+        const int h = hk * p.G + s / nq;
+        const int q0 = (ilo + s % nq) * C::BQ;
+        mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(smem + C::OFF_Q + st * C::Q_STAGE + c * C::QCHUNK, &tmQ, &q_full[st], c * 64, h, q0, b);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(smem + C::OFF_DO + st * C::DO_STAGE + c * C::QCHUNK, &tmDO, &q_full[st], c * 64, h, q0, b);
+        const size_t row = ((size_t)b * p.H_q + h) * p.S_pad + q0;
+        bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.lse2 + row, C::BQ * 4, &q_full[st]);
+        bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
+      }
+      mbar_wait(kv_full, 0, err, kKvDrain);
+      for (int s = 0; s < C::NQ && s < nsteps; ++s) {
+        const int last = s + ((nsteps - 1 - s) / C::NQ) * C::NQ;
+        mbar_wait(&q_full[s], (last / C::NQ) & 1, err, kKvDrain);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nsteps > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
+      constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
+      constexpr uint32_t idDK = idesc_bf16_f32(128, D_QK, false, true);
+      constexpr uint32_t idDQ = idesc_bf16_f32(128, C::BQ, true, true);
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+      auto issue_S_dP = [&](int st) {
+        const uint32_t qa = sQ + st * C::Q_STAGE, da = sDO + st * C::DO_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < D_QK / 16; ++kk)
+          mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
+                 smem_desc_sw128(qa + (kk / 4) * C::QCHUNK + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+        mma_commit(s_ready);
+#pragma unroll
+        for (int kk = 0; kk < D_V / 16; ++kk)
+          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
+                 smem_desc_sw128(da + (kk / 4) * C::QCHUNK + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+        mma_commit(dp_ready);
+      };
+      bool ok = mbar_wait(kv_full, 0, err, kKvFull) && mbar_wait(&q_full[0], 0, err, kKvQFull);
+      if (ok) {
+        tc_fence_after();
+        issue_S_dP(0);
+      }
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int st = s % C::NQ;
+        const uint32_t qa = sQ + st * C::Q_STAGE, da = sDO + st * C::DO_STAGE;
+        ok = mbar_wait(p_ready, s & 1, err, kKvP);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO   (P^T bf16 in TMEM: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + (kk / 2) * 32 + (kk % 2) * 8,
+                 smem_desc_sw128(da + kk * 2048, C::QCHUNK, 1024), idDV, (s > 0 || kk > 0) ? 1u : 0u);
+        ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
+        if (!ok) break;
+        tc_fence_after();
+        // dK += dS^T Q
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8,
+                 smem_desc_sw128(qa + kk * 2048, C::QCHUNK, 1024), idDK, (s > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (FUSE_DQ) {
+          ok = mbar_wait(dq_free, (s & 1) ^ 1, err, kKvDQFree);
+          if (!ok) break;
+          tc_fence_after();
+          // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sK + kk * 2048, C::KCHUNK, 1024),
+                   smem_desc_sw128(sDS + kk * 2048, C::KCHUNK, 1024), idDQ, kk > 0);
+          mma_commit(dq_ready);
+        }
+        mma_commit(&q_empty[st]);
+        if (s + 1 < nsteps) {
+          const int st1 = (s + 1) % C::NQ;
+          ok = mbar_wait(&q_full[st1], ((s + 1) / C::NQ) & 1, err, kKvQFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_S_dP(st1);
+        }
+      }
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, err, kKvDone);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ P / dS warpgroups
+    const int w = warp / 4;  // which 32 query columns of the 64
+    const int r = (warp % 4) * 32 + lane;
+    const int key = n0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int st = s % C::NQ;
+      const int q0 = (ilo + s % nq) * C::BQ;
+      const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
+      const float* dd = l2 + C::BQ;
+      ok = mbar_wait(s_ready, s & 1, err, kKvS);
+      if (!ok) break;
+      tc_fence_after();
+      float pr[32];
+      {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + C::COL_S + 32 * w, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -l2[c]));
+      }
+      if (!tile_fully_visible(mask, q0, C::BQ, n0, C::BN)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (!key_visible(mask, q0 + 32 * w + c, key)) pr[c] = 0.f;
+      }
+      {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        tmem_st16(lane_addr + C::COL_S + 32 * w, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      ok = mbar_wait(dp_ready, s & 1, err, kKvDP);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dsk[16];
+      {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a = pr[2 * c] * (__uint_as_float(rr[2 * c]) - dd[2 * c]);
+          const float bq = pr[2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - dd[2 * c + 1]);
+          dsk[c] = pack_bf16x2(a, bq);
+        }
+      }
+      tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
+      if constexpr (FUSE_DQ) {
+        // dS^T row r, query columns 32w..32w+31 -> 16-byte chunks 4w..4w+3 (128-byte swizzle)
+        uint8_t* rowp = smem + C::OFF_DS + r * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = (4 * w + k) ^ (r & 7);
+          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+              make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
+    bool have = false;
+    if (ok && nsteps > 0) {
+      have = mbar_wait(mma_done, 0, err, kKvDone);
+      tc_fence_after();
+    }
+    if (key < p.S_kv) {
+      const int ncols = w == 0 ? D_V : D_QK;
+      const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
+      const float mul = w == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst = w == 0 ? p.dv + (((size_t)b * p.S_kv + key) * p.H_kv + hk) * D_V
+                                  : p.dk + (((size_t)b * p.S_kv + key) * p.H_kv + hk) * D_QK;
+#pragma unroll 1
+      for (int c0 = 0; c0 < ncols; c0 += 32) {
+        uint32_t rr[32];
+        if (have) {
+          tmem_ld32(lane_addr + col0 + c0, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) rr[c] = 0u;
+        }
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * mul, __uint_as_float(rr[2 * c + 1]) * mul);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+      }
+    }
+  } else if (FUSE_DQ && warp >= 10 && warp < 14) {
+    // ------------------------------------------------------------ dQ drain: TMEM lane = head-dim index d
+    const int d = (warp % 4) * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    for (int s = 0; s < nsteps; ++s) {
+      if (!mbar_wait(dq_ready, s & 1, err, kKvDQReady)) break;
+      tc_fence_after();
+      const int h = hk * p.G + s / nq;
+      const int q0 = (ilo + s % nq) * C::BQ;
+      float* base = p.dq_acc + (((size_t)b * p.S_q + q0) * p.H_q + h) * D_QK + d;
+      const size_t qstride = (size_t)p.H_q * D_QK;
+#pragma unroll
+      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + C::COL_DQ + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (q0 + c0 + c < p.S_q) atomicAdd(base + (size_t)(c0 + c) * qstride, __uint_as_float(rr[c]));
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return d_qk == 128 && (d_v == 128 || d_v == 64); }
+
+template <int D_QK, int D_V, bool FUSE>
+static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdParams& p, cudaStream_t stream) {
+  using C = KvCfg<D_QK, D_V, FUSE>;
+  auto kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
+  dim3 grid((p.S_kv + C::BN - 1) / C::BN, p.H_kv, p.B);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const CUtensorMap& tdo, const BwdParams& p, bool fuse_dq, cudaStream_t stream) {
+  if (fuse_dq) {
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, p, stream);
+    if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, p, stream);
+    return -2;
+  }
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, p, stream);
+  return -2;
+}
+
+// =============================================================================
+// query-stationary deterministic dQ kernel
+// =============================================================================
+template <int D_QK, int D_V>
+struct QCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
+  static constexpr int CHUNK = 128 * 128;
+  static constexpr int NK = 2;
+  static constexpr int NV = (D_QK == 192 && D_V == 128) ? 1 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + QCH * CHUNK;
+  static constexpr int OFF_K = OFF_DO + VCH * CHUNK;
+  static constexpr int OFF_V = OFF_K + NK * QCH * CHUNK;
+  static constexpr int OFF_BAR = OFF_V + NV * VCH * CHUNK;
+  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready, ds_ready, mma_done
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 4;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
+  static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
+  static constexpr int THREADS = 320;
+  static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256;
+  static_assert(COL_DQ + D_QK <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain };
+
+template <int D_QK, int D_V>
+__global__ void __maxnreg__(200)
+    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      const BwdParams p) {
+  using C = QCfg<D_QK, D_V>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::NK;
+  uint64_t* v_full = k_empty + C::NK;
+  uint64_t* v_empty = v_full + C::NV;
+  uint64_t* s_ready = v_empty + C::NV;
+  uint64_t* dp_ready = s_ready + 1;
+  uint64_t* ds_ready = s_ready + 2;
+  uint64_t* mma_done = s_ready + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int qt = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
+  const int m0 = qt * C::BM;
+  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
+  int jlo = 1, jhi = 0;
+  const bool active = kv_tile_range(mask, m0, min(m0 + C::BM - 1, p.S_q - 1), C::BN, &jlo, &jhi);
+  const int nj = active ? jhi - jlo + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < C::NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    mbar_init(s_ready, 1);
+    mbar_init(dp_ready, 1);
+    mbar_init(ds_ready, 256);
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc<512>(tmem_slot);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int* err = p.err;
+
+  if (warp == 9) {
+    if (lane == 0 && nj > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(q_full, (C::QCH + C::VCH) * C::CHUNK);
+      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_Q + c * C::CHUNK, &tmQ, q_full, c * 64, h, m0, b);
+      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_DO + c * C::CHUNK, &tmDO, q_full, c * 64, h, m0, b);
+      for (int n = 0; n < nj; ++n) {
+        const int j = jlo + n;
+        const int sk = n % C::NK, sv = n % C::NV;
+        if (!mbar_wait(&k_empty[sk], ((n / C::NK) & 1) ^ 1, err, kQKEmpty)) break;
+        mbar_arrive_expect_tx(&k_full[sk], C::QCH * C::CHUNK);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(smem + C::OFF_K + (sk * C::QCH + c) * C::CHUNK, &tmK, &k_full[sk], c * 64, hk, j * C::BN, b);
+        if (!mbar_wait(&v_empty[sv], ((n / C::NV) & 1) ^ 1, err, kQVEmpty)) break;
+        mbar_arrive_expect_tx(&v_full[sv], C::VCH * C::CHUNK);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(smem + C::OFF_V + (sv * C::VCH + c) * C::CHUNK, &tmV, &v_full[sv], c * 64, hk, j * C::BN, b);
+      }
+      mbar_wait(q_full, 0, err, kQDrain);
+      for (int s = 0; s < C::NK && s < nj; ++s) {
+        const int last = s + ((nj - 1 - s) / C::NK) * C::NK;
+        mbar_wait(&k_full[s], (last / C::NK) & 1, err, kQDrain);
+      }
+      for (int s = 0; s < C::NV && s < nj; ++s) {
+        const int last = s + ((nj - 1 - s) / C::NV) * C::NV;
+        mbar_wait(&v_full[s], (last / C::NV) & 1, err, kQDrain);
+      }
+    }
+  } else if (warp == 8) {
+    if (lane == 0 && nj > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idDQ = idesc_bf16_f32(128, D_QK, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      bool ok = mbar_wait(q_full, 0, err, kQQ);
+      for (int n = 0; n < nj && ok; ++n) {
+        const int sk = n % C::NK, sv = n % C::NV;
+        const uint32_t ka = sK + sk * C::QCH * C::CHUNK, va = sV + sv * C::VCH * C::CHUNK;
+        ok = mbar_wait(&k_full[sk], (n / C::NK) & 1, err, kQKFull);
+        if (!ok) break;
+        tc_fence_after();
+        // S = Q K^T
+#pragma unroll
+        for (int kk = 0; kk < D_QK / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_ss(tmem + C::COL_S, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idS,
+                 kk > 0);
+        }
+        mma_commit(s_ready);
+        ok = mbar_wait(&v_full[sv], (n / C::NV) & 1, err, kQVFull);
+        if (!ok) break;
+        tc_fence_after();
+        // dP = dO V^T
+#pragma unroll
+        for (int kk = 0; kk < D_V / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sDO + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idS,
+                 kk > 0);
+        }
+        mma_commit(dp_ready);
+        mma_commit(&v_empty[sv]);
+        ok = mbar_wait(ds_ready, n & 1, err, kQDS);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS K   (dS bf16 in TMEM: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(tmem + C::COL_DQ, tmem + C::COL_S + (kk / 4) * 64 + (kk % 4) * 8,
+                 smem_desc_sw128(ka + kk * 2048, C::CHUNK, 1024), idDQ, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&k_empty[sk]);
+      }
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, err, kQDone);
+    }
+  } else {
+    // ------------------------------------------------------------ dS warpgroups: thread = query row
+    const int w = warp / 4;  // keys 64w .. 64w+63 of each kv tile
+    const int r = (warp % 4) * 32 + lane;
+    const int i = m0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float l2row = INFINITY, drow = 0.f;
+    if (i < p.S_q) {
+      const size_t ri = ((size_t)b * p.H_q + h) * p.S_pad + i;
+      l2row = p.lse2[ri];
+      drow = p.Dsum[ri];
+    }
+    bool ok = true;
+    for (int n = 0; n < nj && ok; ++n) {
+      const int k0 = (jlo + n) * C::BN + 64 * w;
+      ok = mbar_wait(s_ready, n & 1, err, kQS);
+      if (!ok) break;
+      tc_fence_after();
+      const bool full = tile_fully_visible(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
+      float pr[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + C::COL_S + 64 * w + c0, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pr[c0 + c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -l2row));
+      }
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!key_visible(mask, i, k0 + c)) pr[c] = 0.f;
+      }
+      ok = mbar_wait(dp_ready, n & 1, err, kQDP);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_addr + C::COL_DP + 64 * w + c0, rr);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a = pr[c0 + 2 * c] * (__uint_as_float(rr[2 * c]) - drow);
+          const float bq = pr[c0 + 2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - drow);
+          pk[c] = pack_bf16x2(a, bq);
+        }
+        tmem_st16(lane_addr + C::COL_S + 64 * w + c0 / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2)
+    bool have = false;
+    if (ok && nj > 0) {
+      have = mbar_wait(mma_done, 0, err, kQDone);
+      tc_fence_after();
+    }
+    if (i < p.S_q) {
+      __nv_bfloat16* dst = p.dq + (((size_t)b * p.S_q + i) * p.H_q + h) * D_QK;
+      constexpr int HALF = D_QK / 2;
+#pragma unroll 1
+      for (int c0 = w * HALF; c0 < (w + 1) * HALF; c0 += 32) {
+        uint32_t rr[32];
+        if (have) {
+          tmem_ld32(lane_addr + C::COL_DQ + c0, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) rr[c] = 0u;
+        }
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * p.scale, __uint_as_float(rr[2 * c + 1]) * p.scale);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+template <int D_QK, int D_V>
+static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                      const BwdParams& p, cudaStream_t stream) {
+  using C = QCfg<D_QK, D_V>;
+  auto kern = attn_bwd_q_kernel<D_QK, D_V>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
+  dim3 grid((p.S_q + C::BM - 1) / C::BM, p.H_q, p.B);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_q_t<128, 64>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_q_t<64, 128>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_q_t<192, 64>(tq, tk, tv, tdo, p, stream);
+  return -2;
+}
+
+// =============================================================================
+// dQ = bf16(scale * accumulator)
+// =============================================================================
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
+                                                             uint2* __restrict__ dq, size_t n4, float scale) {
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[t];
+    dq[t] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+  }
+}
+
+int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream) {
+  const size_t n = (size_t)p.B * p.S_q * p.H_q * d_qk;
+  const size_t n4 = n / 4;  // d_qk is a multiple of 64
+  const unsigned blocks = (unsigned)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
+  bwd_dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.dq_acc),
+                                                    reinterpret_cast<uint2*>(p.dq), n4, p.scale);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace sdpa

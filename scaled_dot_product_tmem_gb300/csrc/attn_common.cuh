@@ -1,0 +1,67 @@
+// attn_common.cuh -- index arithmetic shared by the forward and backward kernels:
+// which keys a query row sees, which kv tiles a block of query rows touches, and
+// which query tiles a block of keys is seen by.
+//
+// Masking rule (causal with an optional left window, top-left diagonal):
+//   key j is visible to query i  iff  j < S_kv  and (!causal or j <= i)
+//                                     and (window < 0 or j >= i - window).
+// ("JAX: Single-GPU Attention with TransformerEngine", sections 1-2: causal
+// mask plus sliding window; codelab "Speed up attention on GPU with cuDNN and
+// TransformerEngine", step 7: query i sees keys j <= i.)
+#pragma once
+#include <cstdint>
+
+namespace sdpa {
+
+struct MaskSpec {
+  int S_q, S_kv, causal, window;
+};
+
+__host__ __device__ __forceinline__ bool key_visible(const MaskSpec& m, int i, int j) {
+  return j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
+}
+
+// Inclusive range of kv tiles (size bn) touched by query rows [r0, r1]; returns
+// false when those rows see no key at all.
+__host__ __device__ __forceinline__ bool kv_tile_range(const MaskSpec& m, int r0, int r1, int bn, int* jlo,
+                                                       int* jhi) {
+  int lo = m.window >= 0 ? (r0 - m.window > 0 ? r0 - m.window : 0) : 0;
+  int hi = m.causal ? (r1 < m.S_kv - 1 ? r1 : m.S_kv - 1) : m.S_kv - 1;
+  if (hi < lo || m.S_kv <= 0) return false;
+  *jlo = lo / bn;
+  *jhi = hi / bn;
+  return true;
+}
+
+// Inclusive range of query tiles (size bm) that see at least one key of
+// [k0, k1]; returns false when none does.
+__host__ __device__ __forceinline__ bool q_tile_range(const MaskSpec& m, int k0, int k1, int bm, int* ilo,
+                                                      int* ihi) {
+  int lo = m.causal ? k0 : 0;
+  int hi = m.window >= 0 ? k1 + m.window : m.S_q - 1;
+  if (hi > m.S_q - 1) hi = m.S_q - 1;
+  if (hi < lo || m.S_q <= 0) return false;
+  *ilo = lo / bm;
+  *ihi = hi / bm;
+  return true;
+}
+
+// Is the whole (rows [r0, r0+bm), keys [k0, k0+bn)) tile visible?  Then the
+// per-element mask can be skipped.  Rows past S_q do not matter (never stored).
+__host__ __device__ __forceinline__ bool tile_fully_visible(const MaskSpec& m, int r0, int bm, int k0, int bn) {
+  int r1 = r0 + bm - 1;
+  int k1 = k0 + bn - 1;
+  if (k1 >= m.S_kv) return false;
+  if (m.causal && k1 > r0) return false;
+  if (m.window >= 0 && k0 < r1 - m.window) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace sdpa

@@ -1,0 +1,377 @@
+// attn_fwd.cu -- fused BSHD attention forward for sm_103a.
+//
+// Computes, per (batch b, query head h, kv head h / G):
+//   S = scale * Q K^T, masked (causal + left window), softmax with an optional sink
+//   logit c (off-by-one: c = 0; learnable: c = offset[h]), O = P V, and
+//   LSE = log(e^c + sum_j e^{S_j}) per row.
+// Sources: "Speed up attention on GPU with cuDNN and TransformerEngine", section
+// "How attention works" and step 7 (causal); "JAX: Single-GPU Attention with
+// TransformerEngine", sections 1, 2, 4 and "Other attention knobs" (GQA, sliding
+// window, MLA head dims, scale_factor, sink softmax); "[JAX] Add support for sink
+// attention in JAX #2225", Greptile sequence diagrams (the three denominators).
+//
+// One CTA owns two 128-row query tiles of one (b, h) and walks the kv tiles that
+// either of them can see.  Warp roles (320 threads):
+//   warps 0-3 / 4-7  softmax warpgroup of query tile 0 / 1: thread r owns row r
+//                    (TMEM lane r); online softmax in fp32 with the sink folded
+//                    into the running max/denominator; writes bf16 P into TMEM
+//                    over its own S columns; rescales O in TMEM only when the
+//                    running max grows by more than 2^8 (exact: the final
+//                    normalisation uses the same stale max); epilogue O/l, LSE.
+//   warp 8           one thread issues tcgen05.mma: S_t = Q_t K_j^T (both from
+//                    shared memory) and O_t += P_t V_j (P from TMEM, V from
+//                    shared memory, MN-major).
+//   warp 9           one thread issues the TMA loads: Q once, then K / V rings.
+// TMEM (512 columns): S_t / P_t at t*256, O_t at t*256 + 128.
+#include <cuda_runtime.h>
+
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+template <int D_QK, int D_V, int NK, int NV>
+struct FwdCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
+  static constexpr int CHUNK = 128 * 128;  // one 128-row x 64-col bf16 box
+  static constexpr int Q_TILE = QCH * CHUNK;
+  static constexpr int K_STAGE = QCH * CHUNK;
+  static constexpr int V_STAGE = VCH * CHUNK;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NK * K_STAGE;
+  static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
+  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready[2], p_ready[2], o_done[2], mma_done
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
+  static constexpr int THREADS = 320;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM > 116 * 1024, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
+};
+
+enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
+
+template <int D_QK, int D_V, int NK, int NV>
+__global__ void __maxnreg__(200)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D_QK, D_V, NK, NV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_ready = v_empty + NV;
+  uint64_t* p_ready = s_ready + 2;
+  uint64_t* o_done = p_ready + 2;
+  uint64_t* mma_done = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int qb = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
+  const int m0 = qb * 2 * C::BM;
+  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
+
+  // Per query tile: does it exist (rows < S_q) and which kv tiles does it see?
+  bool exists[2], active[2];
+  int jlo[2], jhi[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = m0 + t * C::BM;
+    exists[t] = r0 < p.S_q;
+    const int r1 = min(r0 + C::BM - 1, p.S_q - 1);
+    active[t] = exists[t] && kv_tile_range(mask, r0, r1, C::BN, &jlo[t], &jhi[t]);
+    if (!active[t]) { jlo[t] = 1; jhi[t] = 0; }
+  }
+  const bool any = active[0] || active[1];
+  const int J0 = active[0] ? (active[1] ? min(jlo[0], jlo[1]) : jlo[0]) : jlo[1];
+  const int J1 = active[1] ? (active[0] ? max(jhi[0], jhi[1]) : jhi[1]) : jhi[0];
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_ready[t], 1);
+      mbar_init(&p_ready[t], C::BM);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc<512>(tmem_slot);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int* err = p.err;
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && any) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t qbytes = (active[0] ? C::Q_TILE : 0) + (active[1] ? C::Q_TILE : 0);
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < 2; ++t)
+        if (active[t])
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(smem + C::OFF_Q + t * C::Q_TILE + c * C::CHUNK, &tmQ, q_full, c * 64, h, m0 + t * C::BM, b);
+      bool ok = true;
+      for (int j = J0; j <= J1 && ok; ++j) {
+        const int n = j - J0;
+        const int sk = n % NK, sv = n % NV;
+        ok = mbar_wait(&k_empty[sk], ((n / NK) & 1) ^ 1, err, kSiteKEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&k_full[sk], C::K_STAGE);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(smem + C::OFF_K + sk * C::K_STAGE + c * C::CHUNK, &tmK, &k_full[sk], c * 64, hk, j * C::BN, b);
+        ok = mbar_wait(&v_empty[sv], ((n / NV) & 1) ^ 1, err, kSiteVEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&v_full[sv], C::V_STAGE);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE + c * C::CHUNK, &tmV, &v_full[sv], c * 64, hk, j * C::BN, b);
+      }
+      // Drain: every load issued must have landed before the CTA can exit.
+      const int nj = J1 - J0 + 1;
+      mbar_wait(q_full, 0, err, kSiteDrain);
+      for (int s = 0; s < NK && s < nj; ++s) {
+        const int last = s + ((nj - 1 - s) / NK) * NK;
+        mbar_wait(&k_full[s], (last / NK) & 1, err, kSiteDrain);
+      }
+      for (int s = 0; s < NV && s < nj; ++s) {
+        const int last = s + ((nj - 1 - s) / NV) * NV;
+        mbar_wait(&v_full[s], (last / NV) & 1, err, kSiteDrain);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && any) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      auto issue_S = [&](int t, int stage) {
+        const uint32_t qa = sQ + t * C::Q_TILE, ka = sK + stage * C::K_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < D_QK / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_ss(tmem + t * 256, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idS,
+                 kk > 0);
+        }
+      };
+      auto issue_PV = [&](int t, int stage, bool acc) {
+        const uint32_t va = sV + stage * C::V_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, smem_desc_sw128(va + kk * 2048, C::CHUNK, 1024), idO,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, err, kSiteQ);
+      if (ok) ok = mbar_wait(&k_full[0], 0, err, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (active[t] && jlo[t] == J0) {
+            issue_S(t, 0);
+            mma_commit(&s_ready[t]);
+          }
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = J0; j <= J1 && ok; ++j) {
+        const int n = j - J0;
+        const bool need_k = j + 1 <= J1;
+        ok = mbar_wait(&v_full[n % NV], (n / NV) & 1, err, kSiteVFull);
+        if (ok && need_k) ok = mbar_wait(&k_full[(n + 1) % NK], ((n + 1) / NK) & 1, err, kSiteKFull);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (ok && active[t] && j >= jlo[t] && j <= jhi[t]) {
+            ok = mbar_wait(&p_ready[t], (j - jlo[t]) & 1, err, kSiteP);
+            if (ok) {
+              tc_fence_after();
+              issue_PV(t, n % NV, j > jlo[t]);
+              if (j == jhi[t]) mma_commit(&o_done[t]);
+            }
+          }
+          if (ok && active[t] && j + 1 >= jlo[t] && j + 1 <= jhi[t]) {
+            issue_S(t, (n + 1) % NK);
+            mma_commit(&s_ready[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&v_empty[n % NV]);
+        if (need_k) mma_commit(&k_empty[(n + 1) % NK]);
+      }
+      // Every MMA must be complete before TMEM is released.
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, err, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;
+    const bool my_active = t ? active[1] : active[0];
+    const bool my_exists = t ? exists[1] : exists[0];
+    const int my_jlo = t ? jlo[1] : jlo[0];
+    const int my_jhi = t ? jhi[1] : jhi[0];
+    const int r = (warp % 4) * 32 + lane;
+    const int i = m0 + t * C::BM + r;  // query row
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const uint32_t colS = t * 256, colO = t * 256 + 128;
+    const float sl2 = p.scale_log2;
+    // running max (in scaled log2 units) and denominator; the sink starts them
+    float m_run = -INFINITY, l = 0.f;
+    if (p.softmax_type == 1) { m_run = 0.f; l = 1.f; }
+    if (p.softmax_type == 2) { m_run = p.offset[h] * kLog2e; l = 1.f; }
+    bool ok = true;
+    if (my_active) {
+      for (int j = my_jlo; j <= my_jhi; ++j) {
+        const int it = j - my_jlo;
+        ok = mbar_wait(&s_ready[t], it & 1, err, kSiteS);
+        if (!ok) break;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(lane_addr + colS + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(rr[c]);
+        }
+        const int k0 = j * C::BN;
+        if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (!key_visible(mask, i, k0 + c)) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_tile = mx * sl2;
+        if (m_tile > m_run + 8.f) {
+          // grow the running max; rescale l and (after the first tile) O in TMEM
+          const float alpha = ex2(m_run - m_tile);
+          l *= alpha;
+          if (it > 0) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < D_V; c0 += 32) {
+              uint32_t rr[32];
+              tmem_ld32(lane_addr + colO + c0, rr);
+              tmem_ld_wait();
+              uint32_t w0[16], w1[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                w0[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+                w1[c] = __float_as_uint(__uint_as_float(rr[16 + c]) * alpha);
+              }
+              tmem_st16(lane_addr + colO + c0, w0);
+              tmem_st16(lane_addr + colO + c0 + 16, w1);
+            }
+          }
+          m_run = m_tile;
+        }
+        const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float a = ex2(fmaf(s[c0 + 2 * c], sl2, -m_sub));
+            const float bq = ex2(fmaf(s[c0 + 2 * c + 1], sl2, -m_sub));
+            lsum += a + bq;
+            pk[c] = pack_bf16x2(a, bq);
+          }
+          tmem_st16(lane_addr + colS + c0 / 2, pk);
+        }
+        l += lsum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_ready[t]);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    if (my_exists) {
+      bool have_o = false;
+      if (my_active && ok) {
+        have_o = mbar_wait(&o_done[t], 0, err, kSiteO);
+        tc_fence_after();
+      }
+      if (i < p.S_q) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.o + (((size_t)b * p.S_q + i) * p.H_q + h) * D_V;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D_V; c0 += 32) {
+          uint32_t rr[32];
+          if (have_o) {
+            tmem_ld32(lane_addr + colO + c0, rr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) rr[c] = 0u;
+          }
+          uint32_t pw[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * inv, __uint_as_float(rr[2 * c + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+        }
+        const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+        p.lse[((size_t)b * p.H_q + h) * p.S_q + i] = l > 0.f ? (m_sub + lg2(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+template <int D_QK, int D_V, int NK, int NV>
+static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                        cudaStream_t stream) {
+  using C = FwdCfg<D_QK, D_V, NK, NV>;
+  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
+    attr_set = true;
+  }
+  dim3 grid((p.S_q + 2 * C::BM - 1) / (2 * C::BM), p.H_q, p.B);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const FwdParams& p, cudaStream_t stream) {
+  if (d_qk == 128 && d_v == 128) return launch_fwd_t<128, 128, 2, 2>(tq, tk, tv, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_fwd_t<64, 64, 4, 4>(tq, tk, tv, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_fwd_t<192, 128, 2, 1>(tq, tk, tv, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_fwd_t<128, 64, 2, 3>(tq, tk, tv, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_fwd_t<64, 128, 3, 3>(tq, tk, tv, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_fwd_t<192, 64, 2, 2>(tq, tk, tv, p, stream);
+  return -2;
+}
+
+}  // namespace sdpa

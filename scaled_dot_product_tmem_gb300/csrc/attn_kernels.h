@@ -1,0 +1,53 @@
+// attn_kernels.h -- internal launch interface between the C-ABI layer (api.cu)
+// and the kernel translation units.  Not part of the public header.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace sdpa {
+
+struct FwdParams {
+  int B, S_q, S_kv, H_q, H_kv, G;
+  float scale_log2;  // scale * log2(e)
+  int causal, window, softmax_type;
+  const float* offset;  // [H_q], learnable only
+  __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
+  float* lse;           // [B, H_q, S_q]
+  int* err;             // device error word
+};
+
+// Returns 0 on a successful launch, -2 for an unsupported (d_qk, d_v), -1 on a
+// CUDA launch error.
+int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const FwdParams& p, cudaStream_t stream);
+
+struct BwdParams {
+  int B, S_q, S_kv, H_q, H_kv, G;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  int causal, window, softmax_type;
+  int S_pad;                  // S_q rounded up to 128: row length of lse2 / Dsum
+  const float* offset;        // [H_q]
+  const __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
+  const __nv_bfloat16* dout;  // [B, S_q, H_q, d_v]
+  const float* lse;           // [B, H_q, S_q] (natural log)
+  float* lse2;                // [B, H_q, S_pad] workspace: LSE * log2(e), +inf padding
+  float* Dsum;                // [B, H_q, S_pad] workspace: rowsum(dO * O), 0 padding
+  float* d_offset;            // [H_q] (learnable) or null
+  __nv_bfloat16* dq;          // [B, S_q, H_q, d_qk]
+  __nv_bfloat16* dk;          // [B, S_kv, H_kv, d_qk]
+  __nv_bfloat16* dv;          // [B, S_kv, H_kv, d_v]
+  float* dq_acc;              // [B, S_q, H_q, d_qk] fp32 workspace (atomic dQ path) or null
+  int* err;
+};
+
+int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
+int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const CUtensorMap& tdo, const BwdParams& p, bool fuse_dq, cudaStream_t stream);
+int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
+bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
+
+}  // namespace sdpa

@@ -1,0 +1,102 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, exports every
+function include/sdpa_tmem.h declares, and rejects bad arguments with the documented
+status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa_tmem.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from scaled_dot_product_tmem_gb300 import build
+    build.build()
+    import scaled_dot_product_tmem_gb300 as sdpa
+    return sdpa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string", "attn_last_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} is declared in sdpa_tmem.h but not exported"
+
+
+def test_status_strings(lib):
+    import scaled_dot_product_tmem_gb300 as sdpa
+    for st in range(7):
+        assert sdpa.attn_status_string(st) not in ("", "unknown status")
+    assert sdpa.attn_status_string(99) == "unknown status"
+
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, TIMEOUT, WORKSPACE = range(7)
+P = ctypes.c_void_p(0x10000)   # a fake, 16-byte aligned "device" address (never dereferenced)
+MIS = ctypes.c_void_p(0x10008)
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, Sq=64, Skv=64, Hq=4, Hkv=2, dqk=128, dv=128, scale=0.0,
+        causal=1, window=-1, st=0, off=None):
+    return lib.attn_fwd(q, k, v, o, lse, B, Sq, Skv, Hq, Hkv, dqk, dv, ctypes.c_float(scale), causal, window, st,
+                        off, None)
+
+
+def test_fwd_argument_validation(lib):
+    assert fwd(lib, Hq=3, Hkv=2) == INVALID
+    assert fwd(lib, Hkv=0) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, st=3) == INVALID
+    assert fwd(lib, st=2, off=None) == INVALID          # learnable needs the offset
+    assert fwd(lib, dqk=96) == UNSUPPORTED
+    assert fwd(lib, dv=192) == UNSUPPORTED
+    assert fwd(lib, causal=0, window=8) == UNSUPPORTED  # window only with causal
+    assert fwd(lib, B=70000) == UNSUPPORTED
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, q=MIS) == MISALIGNED
+    assert fwd(lib, o=MIS) == MISALIGNED
+    assert fwd(lib, B=0) == OK                          # empty: nothing to launch
+    assert fwd(lib, Sq=0) == OK
+
+
+def test_bwd_workspace_and_validation(lib):
+    import scaled_dot_product_tmem_gb300 as sdpa
+    det = sdpa.attn_bwd_workspace_size(4, 2048, 2048, 32, 8, 128, 128, True)
+    atom = sdpa.attn_bwd_workspace_size(4, 2048, 2048, 32, 8, 128, 128, False)
+    rows = 4 * 32 * 2048
+    assert det == 2 * rows * 4                          # lse2 + D, fp32
+    assert atom == det + 4 * 2048 * 32 * 128 * 4        # + fp32 dQ accumulator
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 3, 64, 64, True) == 0
+
+    def bwd(ws=P, ws_bytes=1 << 30, q=P, Hq=4, Hkv=2, st=0, doff=None, off=None, window=-1, causal=1):
+        return lib.attn_bwd(q, P, P, P, P, P, P, P, P, doff, 1, 64, 64, Hq, Hkv, 128, 128, ctypes.c_float(0.0),
+                            causal, window, st, off, 1, ws, ctypes.c_size_t(ws_bytes), None)
+
+    assert bwd(Hq=5) == INVALID
+    assert bwd(st=2, off=P, doff=None) == INVALID       # learnable needs d_offset
+    assert bwd(causal=0, window=3) == UNSUPPORTED
+    assert bwd(q=MIS) == MISALIGNED
+    assert bwd(ws=None) == WORKSPACE
+    assert bwd(ws_bytes=16) == WORKSPACE
+    assert bwd(ws=ctypes.c_void_p(0x10010)) == WORKSPACE  # needs 256-byte alignment
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import scaled_dot_product_tmem_gb300 as sdpa
+    monkeypatch.setattr(sdpa, "_lib", None)
+    monkeypatch.setattr(sdpa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        sdpa.library()

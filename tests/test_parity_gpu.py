@@ -1,0 +1,125 @@
+"""CUDA path vs the fp64 oracle, element by element, on sizes the oracle finishes in
+seconds that still span several 128-row tiles and a ragged tail; every feature
+(GQA/MQA, causal + window, MLA dims, the three softmax types, scale) and the edge
+cases (empty and key-less rows, S_q != S_kv, window 0, no keys at all)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
+from parity_util import Shape, compare, gpu_run, make_inputs, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+# (name, shape, causal, window, softmax_type, scale)
+CASES = [
+    ("tiny_gqa_swa", Shape(1, 128, 128, 4, 2, 64, 64), True, 32, VANILLA, 0.125),
+    ("mqa_ragged_d128", Shape(2, 300, 300, 4, 1, 128, 128), True, -1, VANILLA, None),
+    ("gqa_window_obo", Shape(1, 333, 333, 4, 2, 128, 128), True, 100, OFF_BY_ONE, None),
+    ("mla_learnable", Shape(1, 257, 257, 2, 2, 192, 128), True, -1, LEARNABLE, 1 / math.sqrt(192)),
+    ("d64_window_learnable", Shape(2, 200, 200, 4, 2, 64, 64), True, 64, LEARNABLE, None),
+    ("noncausal_rect", Shape(1, 150, 290, 2, 1, 128, 64), False, -1, VANILLA, 0.3),
+    ("causal_sq_gt_skv", Shape(1, 300, 170, 2, 2, 64, 128), True, -1, OFF_BY_ONE, None),
+    ("keyless_rows_vanilla", Shape(1, 400, 130, 2, 1, 128, 128), True, 50, VANILLA, None),
+    ("keyless_rows_learnable", Shape(1, 400, 130, 2, 1, 128, 128), True, 50, LEARNABLE, None),
+    ("window0", Shape(1, 200, 200, 2, 2, 64, 64), True, 0, VANILLA, None),
+    ("d192_64", Shape(1, 190, 190, 4, 1, 192, 64), True, 70, VANILLA, None),
+    ("d128_64_obo", Shape(2, 260, 260, 2, 1, 128, 64), True, -1, OFF_BY_ONE, None),
+    ("long_window_multi_tile", Shape(1, 700, 700, 2, 1, 128, 128), True, 300, LEARNABLE, 0.09),
+    ("large_logits_obo", Shape(1, 260, 260, 2, 1, 64, 64), True, -1, OFF_BY_ONE, 1.0),
+]
+
+
+@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fwd_bwd_matches_oracle(case, deterministic):
+    name, shape, causal, window, st, scale = case
+    x = make_inputs(shape, 100 + CASES.index(case), learnable_offset=True)
+    kw = dict(causal=causal, window=window, softmax_type=st, scale=scale)
+    ref = oracle_run(x, **kw)
+    gpu = gpu_run(x, deterministic=deterministic, **kw)
+    compare(gpu, ref, name)
+
+
+def test_tiny_config_exact_recipe():
+    """The tiny oracle case: B=1, S=128, H_q=4, H_kv=2, d=64, causal window 32,
+    vanilla, scale 1/8, Q/K/V/dO N(0,1) from seed 0 rounded to bf16."""
+    x = make_inputs(Shape(1, 128, 128, 4, 2, 64, 64), 0)
+    kw = dict(causal=True, window=32, softmax_type=VANILLA, scale=0.125)
+    errs = compare(gpu_run(x, **kw), oracle_run(x, **kw), "tiny")
+    assert errs["o"] < 1e-2
+
+
+def test_no_keys_at_all():
+    """S_kv = 0: every row is empty: O = 0, LSE = sink logit (-inf for vanilla); dQ = 0."""
+    for st in (VANILLA, LEARNABLE):
+        x = make_inputs(Shape(1, 70, 0, 2, 1, 64, 64), 5, learnable_offset=True)
+        kw = dict(causal=True, window=-1, softmax_type=st, scale=None)
+        gpu = gpu_run(x, **kw)
+        assert np.all(gpu["o"] == 0) and np.all(gpu["dq"] == 0)
+        if st == VANILLA:
+            assert np.all(np.isneginf(gpu["lse"]))
+        else:
+            np.testing.assert_allclose(gpu["lse"], np.broadcast_to(x["offset"].numpy()[None, :, None], (1, 2, 70)),
+                                       atol=1e-6)
+
+
+def test_empty_problem_is_a_noop():
+    import scaled_dot_product_tmem_gb300 as sdpa
+    q = torch.zeros((0, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = sdpa.sdpa_forward(q, q[:, :, :1], q[:, :, :1])
+    assert o.shape == (0, 16, 2, 64) and lse.shape == (0, 2, 16)
+    q = torch.zeros((1, 0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.randn((1, 9, 1, 64), device="cuda").to(torch.bfloat16)
+    o, lse = sdpa.sdpa_forward(q, k, k)
+    dq, dk, dv, _ = sdpa.sdpa_backward(q, k, k, o, o, lse)
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0) and torch.all(dv == 0)
+
+
+def test_deterministic_bwd_is_bitwise_reproducible():
+    import scaled_dot_product_tmem_gb300 as sdpa
+    x = make_inputs(Shape(2, 333, 333, 8, 2, 128, 128), 7, learnable_offset=True)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = x["offset"].to(dev)
+    kw = dict(causal=True, window=150, softmax_type=LEARNABLE, softmax_offset=off)
+    o, lse = sdpa.sdpa_forward(q, k, v, **kw)
+    a = sdpa.sdpa_backward(q, k, v, o, do, lse, deterministic=True, **kw)
+    b = sdpa.sdpa_backward(q, k, v, o, do, lse, deterministic=True, **kw)
+    torch.cuda.synchronize()
+    for ta, tb in zip(a, b):
+        assert torch.equal(ta, tb)
+
+
+def test_outputs_do_not_spill_past_their_buffers():
+    """Guard bands around every output stay untouched (ragged sizes, all paths)."""
+    import scaled_dot_product_tmem_gb300 as sdpa
+    shape = Shape(1, 201, 201, 4, 2, 128, 128)
+    x = make_inputs(shape, 9, learnable_offset=True)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = x["offset"].to(dev)
+    G = 4096
+
+    def guarded(shape_, dtype):
+        n = int(np.prod(shape_))
+        buf = torch.full((n + 2 * G,), 7.0, dtype=dtype, device=dev)
+        return buf, buf[G:G + n].view(shape_)
+
+    for det in (True, False):
+        ob, o = guarded((1, 201, 4, 128), torch.bfloat16)
+        lb, lse = guarded((1, 4, 201), torch.float32)
+        sdpa.attn_fwd(q, k, v, o, lse, causal=True, window=90, softmax_type=LEARNABLE, softmax_offset=off)
+        qb, dq = guarded(tuple(q.shape), torch.bfloat16)
+        kb, dk = guarded(tuple(k.shape), torch.bfloat16)
+        vb, dvv = guarded(tuple(v.shape), torch.bfloat16)
+        fb, dof = guarded((4,), torch.float32)
+        sdpa.attn_bwd(q, k, v, o, do, lse, dq, dk, dvv, dof, causal=True, window=90, softmax_type=LEARNABLE,
+                      softmax_offset=off, deterministic=det)
+        torch.cuda.synchronize()
+        for buf in (ob, lb, qb, kb, vb, fb):
+            assert torch.all(buf[:G] == 7.0) and torch.all(buf[-G:] == 7.0)
