@@ -104,6 +104,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
 /* Human-readable name of a status code (static storage). */
 const char* attn_status_string(int status);
 
+/* Description of the last failure this thread saw inside the library (which call
+   failed and CUDA's message), or "" (thread-local storage, valid until the next call). */
+const char* attn_last_error_message(void);
+
 /*
  * Synchronises `stream`, then returns and clears the current device's error word:
  * 0 when no kernel reported a failure, ATTN_ERR_DEVICE_TIMEOUT when a pipeline
@@ -111,6 +115,25 @@ const char* attn_status_string(int status);
  * the synchronisation itself failed.
  */
 int attn_last_device_error(void* stream, int* site);
+
+/*
+ * Measurement aid (off by default).  While enabled, attn_fwd and attn_bwd record
+ * a pair of CUDA events on their launch stream around each class of kernel they
+ * enqueue.  attn_timing_read() waits for those events, writes per class the
+ * summed milliseconds (ms[k]) and the number of kernels launched (launches[k])
+ * for k < n, discards the records and returns ATTN_OK (or ATTN_ERR_CUDA).
+ * Classes: the ATTN_KERNEL_* values below.  Either output pointer may be NULL.
+ */
+enum {
+  ATTN_KERNEL_FWD = 0,             /* forward kernel */
+  ATTN_KERNEL_BWD_PREPROCESS = 1,  /* D = rowsum(dO*O), LSE rescale, d_offset */
+  ATTN_KERNEL_BWD_KV = 2,          /* kv-stationary dK/dV (+ atomic dQ) kernel */
+  ATTN_KERNEL_BWD_Q = 3,           /* query-stationary deterministic dQ kernel */
+  ATTN_KERNEL_BWD_DQ_CONVERT = 4,  /* fp32 dQ accumulator -> bf16 */
+  ATTN_KERNEL_CLASSES = 5
+};
+int attn_timing_enable(int on);
+int attn_timing_read(double* ms, int* launches, int n);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,8 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {attn_status_string(status)} (status {status})")
+        detail = attn_last_error_message()
+        super().__init__(f"{what}: {attn_status_string(status)} (status {status})" + (f" [{detail}]" if detail else ""))
 
 
 def _load():
@@ -54,6 +55,12 @@ def _load():
     lib.attn_bwd.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_last_error_message.argtypes = []
+    lib.attn_last_error_message.restype = ctypes.c_char_p
+    lib.attn_timing_enable.argtypes = [i]
+    lib.attn_timing_enable.restype = i
+    lib.attn_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i]
+    lib.attn_timing_read.restype = i
     lib.attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.attn_last_device_error.restype = i
     _lib = lib
@@ -95,6 +102,10 @@ def _stype(softmax_type):
 
 def attn_status_string(status: int) -> str:
     return _load().attn_status_string(int(status)).decode()
+
+
+def attn_last_error_message() -> str:
+    return _load().attn_last_error_message().decode()
 
 
 def attn_last_device_error(stream=None):
@@ -142,6 +153,24 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, w
                           int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+
+
+KERNEL_CLASSES = ("fwd", "bwd_preprocess", "bwd_kv", "bwd_q", "bwd_dq_convert")
+
+
+def attn_timing_enable(on: bool = True) -> None:
+    _load().attn_timing_enable(int(bool(on)))
+
+
+def attn_timing_read():
+    """{class: (milliseconds, kernel launches)} accumulated since the last read."""
+    n = len(KERNEL_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    st = _load().attn_timing_read(ms, cnt, n)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_timing_read")
+    return {name: (ms[k], cnt[k]) for k, name in enumerate(KERNEL_CLASSES)}
 
 
 # ----------------------------------------------------------------------------- conveniences

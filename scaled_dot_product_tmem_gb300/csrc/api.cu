@@ -5,13 +5,24 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "../../include/sdpa_tmem.h"
 #include "attn_kernels.h"
 #include "tmap.h"
 
 namespace {
+
+// Text of the last failure seen by this thread (which call, and CUDA's message).
+thread_local char g_last_error[256] = "";
+
+void set_error(const char* what, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+}
+void set_error(const char* what) { snprintf(g_last_error, sizeof(g_last_error), "%s", what); }
 
 __device__ int g_device_error;  // one word per GPU: 0 or kErrTimeoutBase + site
 
@@ -20,10 +31,18 @@ constexpr int kMaxDevices = 64;
 int* device_error_ptr() {
   static int* ptrs[kMaxDevices] = {nullptr};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    set_error("cudaGetDevice", e);
+    return nullptr;
+  }
   if (!ptrs[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) {
+      set_error("cudaGetSymbolAddress(device error word)", e);
+      return nullptr;
+    }
     ptrs[dev] = static_cast<int*>(p);
   }
   return ptrs[dev];
@@ -74,9 +93,42 @@ bool use_fused_dq(int d_qk, int d_v, int deterministic) {
   return !deterministic && sdpa::bwd_kv_supports_fused_dq(d_qk, d_v);
 }
 
+// ---------------------------------------------------------------------------
+// Optional timing of every kernel launch (CUDA events on the launch stream).
+// ---------------------------------------------------------------------------
+struct TimingRec {
+  cudaEvent_t a, b;
+  int kind, launches;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimingRec> g_timing;
+
+// Runs `launch` (which enqueues `nlaunch` kernels of class `kind` on stream s);
+// brackets it with events when timing is on.
+template <class F>
+int timed(int kind, int nlaunch, cudaStream_t s, F&& launch) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> g(g_timing_mu);
+    on = g_timing_on;
+  }
+  if (!on) return launch();
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return -1;
+  cudaEventRecord(a, s);
+  const int rc = launch();
+  cudaEventRecord(b, s);
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  g_timing.push_back({a, b, kind, nlaunch});
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
+
+const char* attn_last_error_message(void) { return g_last_error; }
 
 const char* attn_status_string(int status) {
   switch (status) {
@@ -122,8 +174,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   CUtensorMap tq, tk, tv;
   if (!sdpa::make_bshd_map(&tq, q, B, S_q, H_q, d_qk, 128) ||
       !sdpa::make_bshd_map(&tk, kk, B, skv_map, S_kv > 0 ? H_kv : H_q, d_qk, 128) ||
-      !sdpa::make_bshd_map(&tv, vv, B, skv_map, S_kv > 0 ? H_kv : H_q, S_kv > 0 ? d_v : d_qk, 128))
+      !sdpa::make_bshd_map(&tv, vv, B, skv_map, S_kv > 0 ? H_kv : H_q, S_kv > 0 ? d_v : d_qk, 128)) {
+    set_error("cuTensorMapEncodeTiled (forward operands)");
     return ATTN_ERR_CUDA;
+  }
   sdpa::FwdParams p;
   p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
   p.scale_log2 = resolve_scale(scale, d_qk) * 1.4426950408889634f;
@@ -134,9 +188,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.err = err;
-  int rc = sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] { return sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s); });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
-  return rc == 0 ? ATTN_OK : ATTN_ERR_CUDA;
+  if (rc != 0) {
+    set_error("forward kernel launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
 }
 
 size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic) {
@@ -200,7 +259,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
   p.err = err;
 
-  if (sdpa::launch_bwd_preprocess(d_v, p, s) != 0) return ATTN_ERR_CUDA;
+  const int n_pre = 1 + (p.S_pad > S_q ? 1 : 0) + (softmax_type == ATTN_SOFTMAX_LEARNABLE ? 1 : 0);
+  if (timed(ATTN_KERNEL_BWD_PREPROCESS, n_pre, s, [&] { return sdpa::launch_bwd_preprocess(d_v, p, s); }) != 0) {
+    set_error("backward preprocess launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
   if (fused && cudaMemsetAsync(p.dq_acc, 0, sizeof(float) * (size_t)B * S_q * H_q * d_qk, s) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (S_kv == 0) {
@@ -213,23 +276,67 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (!sdpa::make_bshd_map(&tq, q, B, S_q, H_q, d_qk, bq_rows) ||
       !sdpa::make_bshd_map(&tdo, dout, B, S_q, H_q, d_v, bq_rows) ||
       !sdpa::make_bshd_map(&tk, k, B, S_kv, H_kv, d_qk, 128) ||
-      !sdpa::make_bshd_map(&tv, v, B, S_kv, H_kv, d_v, 128))
+      !sdpa::make_bshd_map(&tv, v, B, S_kv, H_kv, d_v, 128)) {
+    set_error("cuTensorMapEncodeTiled (backward operands)");
     return ATTN_ERR_CUDA;
-  int rc = sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, p, fused, s);
+  }
+  int rc = timed(ATTN_KERNEL_BWD_KV, 1, s,
+                 [&] { return sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, p, fused, s); });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
-  if (rc != 0) return ATTN_ERR_CUDA;
+  if (rc != 0) {
+    set_error("backward kv kernel launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
   if (fused) {
-    if (sdpa::launch_bwd_dq_convert(d_qk, p, s) != 0) return ATTN_ERR_CUDA;
+    if (timed(ATTN_KERNEL_BWD_DQ_CONVERT, 1, s, [&] { return sdpa::launch_bwd_dq_convert(d_qk, p, s); }) != 0) {
+      set_error("dQ convert launch", cudaGetLastError());
+      return ATTN_ERR_CUDA;
+    }
   } else {
     CUtensorMap tq128, tdo128;
     if (!sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
         !sdpa::make_bshd_map(&tdo128, dout, B, S_q, H_q, d_v, 128))
       return ATTN_ERR_CUDA;
-    rc = sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);
+    rc = timed(ATTN_KERNEL_BWD_Q, 1, s,
+               [&] { return sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s); });
     if (rc == -2) return ATTN_ERR_UNSUPPORTED;
-    if (rc != 0) return ATTN_ERR_CUDA;
+    if (rc != 0) {
+      set_error("backward dQ kernel launch", cudaGetLastError());
+      return ATTN_ERR_CUDA;
+    }
   }
   return ATTN_OK;
+}
+
+int attn_timing_enable(int on) {
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  g_timing_on = on != 0;
+  return ATTN_OK;
+}
+
+int attn_timing_read(double* ms, int* launches, int n) {
+  std::vector<TimingRec> recs;
+  {
+    std::lock_guard<std::mutex> g(g_timing_mu);
+    recs.swap(g_timing);
+  }
+  for (int k = 0; k < n; ++k) {
+    if (ms) ms[k] = 0.0;
+    if (launches) launches[k] = 0;
+  }
+  int status = ATTN_OK;
+  for (const TimingRec& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      status = ATTN_ERR_CUDA;
+    if (r.kind >= 0 && r.kind < n) {
+      if (ms) ms[r.kind] += t;
+      if (launches) launches[r.kind] += r.launches;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  return status;
 }
 
 }  // extern "C"

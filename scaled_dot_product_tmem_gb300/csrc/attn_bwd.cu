@@ -123,7 +123,7 @@ int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream) {
     bwd_doffset_kernel<<<p.H_q, 256, 0, stream>>>(p);
   else if (p.d_offset)
     cudaMemsetAsync(p.d_offset, 0, sizeof(float) * p.H_q, stream);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 // =============================================================================
@@ -164,7 +164,7 @@ struct KvCfg {
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain };
 
 template <int D_QK, int D_V, bool FUSE_DQ>
-__global__ void __maxnreg__(FUSE_DQ ? 144 : 200)
+__global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
@@ -461,7 +461,7 @@ static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   dim3 grid((p.S_kv + C::BN - 1) / C::BN, p.H_kv, p.B);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -509,7 +509,7 @@ struct QCfg {
 enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain };
 
 template <int D_QK, int D_V>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const BwdParams p) {
@@ -736,7 +736,7 @@ static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   dim3 grid((p.S_q + C::BM - 1) / C::BM, p.H_q, p.B);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -767,7 +767,7 @@ int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream) {
   const unsigned blocks = (unsigned)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
   bwd_dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.dq_acc),
                                                     reinterpret_cast<uint2*>(p.dq), n4, p.scale);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace sdpa

@@ -55,7 +55,7 @@ struct FwdCfg {
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
 
 template <int D_QK, int D_V, int NK, int NV>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D_QK, D_V, NK, NV>;
@@ -360,7 +360,7 @@ static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   }
   dim3 grid((p.S_q + 2 * C::BM - 1) / (2 * C::BM), p.H_q, p.B);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
