@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark: fused attention forward + backward on GB300, in unmasked-FLOP TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = attn_fwd + attn_bwd (every step of the hot path) over one batch of
+synthetic BSHD bf16 inputs already resident in HBM.  The default workload is the
+GQA + sliding-window training shape (B=4, S=2048, H_q=32, H_kv=8, d=128, causal,
+left window 1024, vanilla softmax).  FLOPs count only unmasked (query, key)
+pairs: forward 2(d_qk + d_v) per pair, backward 2(3 d_qk + 2 d_v) per pair.
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own copy of the
+workload (independent problems, no collective on the data path: weak scaling).
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
+workload instead (the only other place this script runs the oracle is the
+``cpu_baseline`` leg of the default arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, unmasked FLOPs) and % of GB300 BF16 peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc):
+    return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
+                scale=scale, seed=seed, desc=desc)
+
+
+WORKLOADS = {
+    "gqa_swa_b4_s2048": _w("gqa_swa_b4_s2048", 4, 2048, 32, 8, 128, 128, True, 1024, 0, None, 1,
+                           "BSHD GQA + SWA training shape: B=4, S=2048, H_q=32, H_kv=8, d_qk=d_v=128, causal, "
+                           "left window 1024, vanilla softmax"),
+    "mla_b2_s4096": _w("mla_b2_s4096", 2, 4096, 16, 16, 192, 128, True, -1, 0, 1 / math.sqrt(192), 2,
+                       "MLA head dims: B=2, S=4096, H=16, d_qk=192, d_v=128, causal, scale 1/sqrt(192)"),
+    "sink_obo_b2_s4096": _w("sink_obo_b2_s4096", 2, 4096, 32, 8, 64, 64, True, -1, 1, None, 3,
+                            "sink attention, off-by-one: B=2, S=4096, H_q=32, H_kv=8, d=64, causal"),
+    "sink_learnable_b2_s4096": _w("sink_learnable_b2_s4096", 2, 4096, 32, 8, 64, 64, True, -1, 2, None, 3,
+                                  "sink attention, learnable offset [32]: B=2, S=4096, H_q=32, H_kv=8, d=64, causal"),
+}
+for _S in (512, 1024, 2048, 4096, 8192, 16384):
+    for _H in (32, 8, 1):
+        _n = f"sweep_s{_S}_hkv{_H}"
+        WORKLOADS[_n] = _w(_n, 32768 // _S, _S, 32, _H, 128, 128, True, -1, 0, None, 1000 + _S + _H,
+                           f"32768-token sweep: B={32768 // _S}, S={_S}, H_q=32, H_kv={_H}, d=128, causal")
+DEFAULT = "gqa_swa_b4_s2048"
+HEADLINE = "sweep_s8192_hkv8"
+
+
+def n_pairs(S, causal, window):
+    """Unmasked (query, key) pairs of one (batch, head) with S_q = S_kv = S."""
+    if not causal:
+        return S * S
+    if window < 0 or window >= S - 1:
+        return S * (S + 1) // 2
+    w = window
+    return (w + 1) * (w + 2) // 2 + (S - w - 1) * (w + 1)
+
+
+def flops(wl, part="total"):
+    n = wl["B"] * wl["Hq"] * n_pairs(wl["S"], wl["causal"], wl["window"])
+    fwd = n * 2 * (wl["dqk"] + wl["dv"])
+    bwd = n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}[part]
+
+
+def kernel_flops(wl, cls, fused):
+    """Algorithmic FLOPs one launch of a kernel class performs (see the design notes)."""
+    n = wl["B"] * wl["Hq"] * n_pairs(wl["S"], wl["causal"], wl["window"])
+    d, e = wl["dqk"], wl["dv"]
+    return {"fwd": n * 2 * (d + e),
+            "bwd_kv": n * 2 * ((3 * d + 2 * e) if fused else (2 * d + 2 * e)),
+            "bwd_q": n * 2 * d}.get(cls, 0)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "MEASURED_PEAKS.json"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle samples
+
+
+def oracle_units(wl):
+    """(b, query head) units of the workload, in a fixed order."""
+    return [(b, h) for b in range(wl["B"]) for h in range(wl["Hq"])]
+
+
+def run_oracle_unit(wl, x, b, h):
+    import oracle
+    G = wl["Hq"] // wl["Hkv"]
+    g = h // G
+    q = x["q"][b:b + 1, :, h:h + 1].double().numpy()
+    k = x["k"][b:b + 1, :, g:g + 1].double().numpy()
+    v = x["v"][b:b + 1, :, g:g + 1].double().numpy()
+    do = x["dout"][b:b + 1, :, h:h + 1].double().numpy()
+    off = x["offset"][h:h + 1].double().numpy() if wl["st"] == 2 else None
+    kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], offset=off, scale=wl["scale"])
+    oracle.attention_fwd(q, k, v, **kw)
+    oracle.attention_bwd(q, k, v, do, **kw)
+
+
+def unit_flops(wl):
+    return flops(wl) / (wl["B"] * wl["Hq"])
+
+
+def make_cpu_inputs(wl, rank=0):
+    from scaled_dot_product_tmem_gb300.inputs import Shape, make_inputs
+    shape = Shape(wl["B"], wl["S"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"], wl["dv"])
+    return make_inputs(shape, wl["seed"] + 7919 * rank, learnable_offset=(wl["st"] == 2))
+
+
+def cpu_baseline(wl, x, budget_s=12.0):
+    """The oracle, as it stands, on whole (batch, query head) units until ~budget_s."""
+    import oracle
+    units = oracle_units(wl)
+    done, t0 = 0, time.perf_counter()
+    for b, h in units:
+        run_oracle_unit(wl, x, b, h)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done * unit_flops(wl) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} of {len(units)} (batch, query head) units of the workload, fwd+bwd in fp64 "
+                      f"({dt:.1f} s); TFLOP/s counts the same unmasked FLOPs as the GPU number"}
+
+
+# ----------------------------------------------------------------------------- arms
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def reference_arm(args, wl, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    x = make_cpu_inputs(wl)
+    units = oracle_units(wl)
+    for i in range(args.warmup):
+        run_oracle_unit(wl, x, *units[i % len(units)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run_oracle_unit(wl, x, *units[(args.warmup + i) % len(units)])
+    dt = time.perf_counter() - t0
+    value = args.steps * unit_flops(wl) / dt / 1e12
+    sample = (f"each step = one (batch, query head) unit of the workload, fwd+bwd in fp64 "
+              f"({unit_flops(wl) / 1e9:.2f} GFLOP)")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["desc"], "seq_len": wl["S"], "global_batch": wl["B"]},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _step_fns(sdpa, wl, dev, det, x):
+    import torch
+    B, S, Hq, Hkv, dqk, dv = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"], wl["dv"]
+    t = {n: x[n].to(dev) for n in ("q", "k", "v", "dout")}
+    off = x["offset"].to(dev) if wl["st"] == 2 else None
+    o = torch.empty((B, S, Hq, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(t["q"])
+    dk = torch.empty_like(t["k"])
+    dvv = torch.empty_like(t["v"])
+    doff = torch.empty((Hq,), dtype=torch.float32, device=dev) if wl["st"] == 2 else None
+    ws = torch.empty(max(sdpa.attn_bwd_workspace_size(B, S, S, Hq, Hkv, dqk, dv, det), 256), dtype=torch.uint8,
+                     device=dev)
+    kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], softmax_offset=off,
+              scale=wl["scale"] or 0.0)
+
+    def step():
+        sdpa.attn_fwd(t["q"], t["k"], t["v"], o, lse, **kw)
+        sdpa.attn_bwd(t["q"], t["k"], t["v"], o, t["dout"], lse, dq, dk, dvv, doff, deterministic=det,
+                      workspace=ws, **kw)
+
+    return step, t, (o, dq, dk, dvv)
+
+
+def measure(sdpa, wl, dev, det, x, steps, warmup, sampler=None):
+    """Device time of `steps` fwd+bwd steps on resident inputs (L2 flushed between steps)."""
+    import torch
+    step, t, outs = _step_fns(sdpa, wl, dev, det, x)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    st, site = sdpa.attn_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} site {site:#x} during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sdpa.attn_timing_read()
+    sdpa.attn_timing_enable(True)
+    if sampler:
+        sampler.start()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))  # evict the previous step's data from L2 (outside the timed span)
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    sdpa.attn_timing_enable(False)
+    kt = sdpa.attn_timing_read()
+    st, site = sdpa.attn_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} site {site:#x}")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    return ms, kt, clocks
+
+
+def measure_e2e(sdpa, wl, dev, det, x, steps, warmup):
+    """Same step through the C ABI from pinned HOST buffers: H2D of q/k/v/dO and D2H of
+    O/dQ/dK/dV inside the timed span."""
+    import torch
+    step, t, outs = _step_fns(sdpa, wl, dev, det, x)
+    host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "dout")}
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+    def e2e_step():
+        for n in ("q", "k", "v", "dout"):
+            t[n].copy_(host_in[n], non_blocking=True)
+        step()
+        for ho, o in zip(host_out, outs):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b), h2d, d2h
+
+
+def _max_over_ranks(val, world, dev):
+    if world == 1:
+        return val
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([val], dtype=torch.float64, device=dev)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def ours_arm(args, wl, world, rank, local):
+    import torch
+    import scaled_dot_product_tmem_gb300 as sdpa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sdpa.library()
+    fused_ok = wl["dqk"] == 128
+    det = bool(args.deterministic) or not fused_ok
+    x = make_cpu_inputs(wl, rank)
+    ms, kt, clocks = measure(sdpa, wl, dev, det, x, args.steps, args.warmup, ClockSampler(local))
+    total_flops = flops(wl)
+    ms_max = _max_over_ranks(ms, world, dev)
+    value = world * total_flops * args.steps / (ms_max / 1e3) / 1e12
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms, h2d, d2h = measure_e2e(sdpa, wl, dev, det, x, e2e_steps, 2)
+    e2e_ms = _max_over_ranks(e2e_ms, world, dev)
+    e2e_value = world * total_flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    dom = max(kt, key=lambda k: kt[k][0])
+    dms, dn = kt[dom]
+    dflops = kernel_flops(wl, dom, fused=not det)
+    achieved = dflops / (dms / dn / 1e3) / 1e12 if dn else 0.0
+    peak = float(peaks["bf16_tflops"])
+    launches = sum(v[1] for v in kt.values())
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps,
+                   "share": v[0] / sum(u[0] for u in kt.values())}
+               for k, v in kt.items() if v[1]}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
+                       "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
+                       "bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ",
+                       "l2": "flushed between timed steps (258 MB write outside the timed span)"},
+            "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            "fwd_tflop": flops(wl, "fwd") / 1e12, "bwd_tflop": flops(wl, "bwd") / 1e12,
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": f"bf16_tflops (burst) from {peak_src}",
+                         "traffic": None},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clocks}
+    if args.headline and wl["name"] != HEADLINE and world == 1:
+        hw = WORKLOADS[HEADLINE]
+        hx = make_cpu_inputs(hw)
+        hsteps = min(args.steps, 10)
+        hms, hkt, _ = measure(sdpa, hw, dev, False, hx, hsteps, 3)
+        hv = flops(hw) * hsteps / (hms / 1e3) / 1e12
+        line["headline_causal_gqa_s8192"] = {
+            "workload": hw["desc"], "value": hv, "unit": "TFLOP/s",
+            "pct_of_nominal_bf16_peak": 100 * hv / NOMINAL_BF16_TFLOPS, "frac_of_measured_peak": hv / peak,
+            "kernels": {k: v[0] / v[1] for k, v in hkt.items() if v[1]}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, x)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--deterministic", action="store_true", help="deterministic backward (recompute dQ)")
+    ap.add_argument("--headline", action="store_true", help="also time the causal GQA S=8192 sweep point")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, wl, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+    world, rank, local = dist_setup()
+    return ours_arm(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
