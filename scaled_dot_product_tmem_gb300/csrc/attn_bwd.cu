@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       const int q0 = (ilo + s % nq) * C::BQ;
       const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
       const float* dd = l2 + C::BQ;
-      ok = mbar_wait(s_ready, s & 1, err, kKvS);
+      ok = mbar_wait_warp(s_ready, s & 1, err, kKvS);
       if (!ok) break;
       tc_fence_after();
       float pr[32];
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       }
       tc_fence_before();
       mbar_arrive(p_ready);
-      ok = mbar_wait(dp_ready, s & 1, err, kKvDP);
+      ok = mbar_wait_warp(dp_ready, s & 1, err, kKvDP);
       if (!ok) break;
       tc_fence_after();
       uint32_t dsk[16];
@@ -389,15 +389,17 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
     bool have = false;
     if (ok && nsteps > 0) {
-      have = mbar_wait(mma_done, 0, err, kKvDone);
+      have = mbar_wait_warp(mma_done, 0, err, kKvDone);
       tc_fence_after();
     }
-    if (key < p.S_kv) {
+    {
+      const bool row_ok = key < p.S_kv;  // all lanes load TMEM; only real keys store
+      const int krow = row_ok ? key : 0;
       const int ncols = w == 0 ? D_V : D_QK;
       const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
       const float mul = w == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst = w == 0 ? p.dv + (((size_t)b * p.S_kv + key) * p.H_kv + hk) * D_V
-                                  : p.dk + (((size_t)b * p.S_kv + key) * p.H_kv + hk) * D_QK;
+      __nv_bfloat16* dst = w == 0 ? p.dv + (((size_t)b * p.S_kv + krow) * p.H_kv + hk) * D_V
+                                  : p.dk + (((size_t)b * p.S_kv + krow) * p.H_kv + hk) * D_QK;
 #pragma unroll 1
       for (int c0 = 0; c0 < ncols; c0 += 32) {
         uint32_t rr[32];
@@ -412,9 +414,11 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * mul, __uint_as_float(rr[2 * c + 1]) * mul);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+        }
       }
     }
   } else if (FUSE_DQ && warp >= 10 && warp < 14) {
@@ -422,7 +426,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     const int d = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     for (int s = 0; s < nsteps; ++s) {
-      if (!mbar_wait(dq_ready, s & 1, err, kKvDQReady)) break;
+      if (!mbar_wait_warp(dq_ready, s & 1, err, kKvDQReady)) break;
       tc_fence_after();
       const int h = hk * p.G + s / nq;
       const int q0 = (ilo + s % nq) * C::BQ;
@@ -650,7 +654,7 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int n = 0; n < nj && ok; ++n) {
       const int k0 = (jlo + n) * C::BN + 64 * w;
-      ok = mbar_wait(s_ready, n & 1, err, kQS);
+      ok = mbar_wait_warp(s_ready, n & 1, err, kQS);
       if (!ok) break;
       tc_fence_after();
       const bool full = tile_fully_visible(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
@@ -668,7 +672,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 64; ++c)
           if (!key_visible(mask, i, k0 + c)) pr[c] = 0.f;
       }
-      ok = mbar_wait(dp_ready, n & 1, err, kQDP);
+      ok = mbar_wait_warp(dp_ready, n & 1, err, kQDP);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -692,11 +696,12 @@ __global__ void __launch_bounds__(320, 1)
     // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2)
     bool have = false;
     if (ok && nj > 0) {
-      have = mbar_wait(mma_done, 0, err, kQDone);
+      have = mbar_wait_warp(mma_done, 0, err, kQDone);
       tc_fence_after();
     }
-    if (i < p.S_q) {
-      __nv_bfloat16* dst = p.dq + (((size_t)b * p.S_q + i) * p.H_q + h) * D_QK;
+    {
+      const bool row_ok = i < p.S_q;  // all lanes load TMEM; only real rows store
+      __nv_bfloat16* dst = p.dq + (((size_t)b * p.S_q + (row_ok ? i : 0)) * p.H_q + h) * D_QK;
       constexpr int HALF = D_QK / 2;
 #pragma unroll 1
       for (int c0 = w * HALF; c0 < (w + 1) * HALF; c0 += 32) {
@@ -712,9 +717,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * p.scale, __uint_as_float(rr[2 * c + 1]) * p.scale);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+        }
       }
     }
   }

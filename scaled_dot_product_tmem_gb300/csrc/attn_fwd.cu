@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(320, 1)
     if (my_active) {
       for (int j = my_jlo; j <= my_jhi; ++j) {
         const int it = j - my_jlo;
-        ok = mbar_wait(&s_ready[t], it & 1, err, kSiteS);
+        ok = mbar_wait_warp(&s_ready[t], it & 1, err, kSiteS);
         if (!ok) break;
         tc_fence_after();
         float s[128];
@@ -263,9 +263,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
         const float m_tile = mx * sl2;
-        if (m_tile > m_run + 8.f) {
-          // grow the running max; rescale l and (after the first tile) O in TMEM
-          const float alpha = ex2(m_run - m_tile);
+        // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
+        // when any row's max grew by more than 2^8, every row of the warp moves to
+        // its new max (alpha = 1 for rows whose max did not change).
+        if (__any_sync(0xffffffffu, m_tile > m_run + 8.f)) {
+          const float m_new = fmaxf(m_run, m_tile);
+          const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
           l *= alpha;
           if (it > 0) {
 #pragma unroll 1
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(320, 1)
               tmem_st16(lane_addr + colO + c0 + 16, w1);
             }
           }
-          m_run = m_tile;
+          m_run = m_new;
         }
         const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
         float lsum = 0.f;
@@ -308,31 +311,34 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ epilogue
     if (my_exists) {
       bool have_o = false;
-      if (my_active && ok) {
-        have_o = mbar_wait(&o_done[t], 0, err, kSiteO);
+      if (my_active && ok) {  // warp-uniform
+        have_o = mbar_wait_warp(&o_done[t], 0, err, kSiteO);
         tc_fence_after();
       }
-      if (i < p.S_q) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + (((size_t)b * p.S_q + i) * p.H_q + h) * D_V;
+      const bool row_ok = i < p.S_q;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.o + (((size_t)b * p.S_q + (row_ok ? i : 0)) * p.H_q + h) * D_V;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D_V; c0 += 32) {
-          uint32_t rr[32];
-          if (have_o) {
-            tmem_ld32(lane_addr + colO + c0, rr);
-            tmem_ld_wait();
-          } else {
+      for (int c0 = 0; c0 < D_V; c0 += 32) {
+        uint32_t rr[32];
+        if (have_o) {  // all lanes load; only rows < S_q store
+          tmem_ld32(lane_addr + colO + c0, rr);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) rr[c] = 0u;
-          }
-          uint32_t pw[16];
+          for (int c = 0; c < 32; ++c) rr[c] = 0u;
+        }
+        uint32_t pw[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * inv, __uint_as_float(rr[2 * c + 1]) * inv);
+        for (int c = 0; c < 16; ++c)
+          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * inv, __uint_as_float(rr[2 * c + 1]) * inv);
+        if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
         }
+      }
+      if (row_ok) {
         const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
         p.lse[((size_t)b * p.H_q + h) * p.S_q + i] = l > 0.f ? (m_sub + lg2(l)) * kLn2 : -INFINITY;
       }

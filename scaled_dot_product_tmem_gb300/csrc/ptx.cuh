@@ -89,6 +89,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Warp-uniform wait: every lane waits, and the result is true only if every lane
+// saw the phase complete.  Call sites that follow with warp-collective tcgen05
+// instructions (.sync.aligned) need this: a lane that skipped them would leave
+// the rest of its warp waiting forever.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err, int site) {
+  const bool ok = mbar_wait(bar, parity, err, site);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ---------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------
@@ -214,7 +223,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // ---------------------------------------------------------------------------
 // tcgen05.ld / st, shape 32x32b: lane i of the warp <-> TMEM lane (base + i),
 // .xN = N consecutive 32-bit columns per lane.  A warp may only touch the 32
-// TMEM lanes of its sub-partition (warp id % 4).
+// TMEM lanes of its sub-partition (warp id % 4).  These (and the waits below)
+// are warp-collective: all 32 lanes must execute them, never under a per-lane
+// condition.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
