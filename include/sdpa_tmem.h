@@ -117,6 +117,44 @@ const char* attn_last_error_message(void);
 int attn_last_device_error(void* stream, int* site);
 
 /*
+ * attn_bwd_noalloc -- the backward of attn_fwd for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this is a packaging variant of
+ * attn_bwd, not part of the method.)
+ *
+ * attn_bwd needs a caller-provided workspace.  Some callers cannot provide one:
+ * runtimes that fix their device-memory footprint at start-up and forbid any
+ * allocation on the launch path (inference-engine plugins, for example), and plain
+ * C callers that have no device allocator of their own.  This entry point takes the
+ * same arguments as attn_bwd minus `deterministic` and the workspace, allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library call), and keeps its
+ * scratch in one fixed array inside the library: attn_bwd_noalloc_max_scratch_bytes()
+ * bytes (8 MiB) per GPU, held by every GPU that loads the library until the process
+ * exits.  It always runs the deterministic backward (bitwise-equal to attn_bwd with
+ * deterministic != 0).
+ *
+ * Limits and rules:
+ *   - the scratch holds 8 bytes per (batch, query head, query row padded up to a
+ *     multiple of 128): B * H_q * ceil(S_q/128)*128 <= 1,048,576 rows (for example
+ *     B=4, H_q=32, S_q=8192).  Larger problems return ATTN_ERR_WORKSPACE without
+ *     launching; attn_bwd_noalloc_message() then says how much was needed.
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture.
+ *   - every call on a device shares the one array.  Each call writes every word it
+ *     later reads, so a previous call's contents never leak into a result, but
+ *     calls whose kernels overlap on the GPU (different streams or threads) race on
+ *     the array: order them on one stream.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv,
+                     int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                     const float* softmax_offset, void* stream);
+/* Size in bytes of attn_bwd_noalloc's built-in scratch array. */
+size_t attn_bwd_noalloc_max_scratch_bytes(void);
+/* Why the last attn_bwd_noalloc call on this thread failed, or "" (thread-local). */
+const char* attn_bwd_noalloc_message(void);
+
+/*
  * Measurement aid (off by default).  While enabled, attn_fwd and attn_bwd record
  * a pair of CUDA events on their launch stream around each class of kernel they
  * enqueue.  attn_timing_read() waits for those events, writes per class the

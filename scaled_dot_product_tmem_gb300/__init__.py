@@ -57,6 +57,13 @@ def _load():
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_error_message.argtypes = []
     lib.attn_last_error_message.restype = ctypes.c_char_p
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp,
+                                     vp]
+    lib.attn_bwd_noalloc.restype = i
+    lib.attn_bwd_noalloc_max_scratch_bytes.argtypes = []
+    lib.attn_bwd_noalloc_max_scratch_bytes.restype = sz
+    lib.attn_bwd_noalloc_message.argtypes = []
+    lib.attn_bwd_noalloc_message.restype = ctypes.c_char_p
     lib.attn_timing_enable.argtypes = [i]
     lib.attn_timing_enable.restype = i
     lib.attn_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i]
@@ -153,6 +160,29 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, w
                           int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, window=-1,
+                     softmax_type=VANILLA, softmax_offset=None, scale=0.0, stream=None):
+    """attn_bwd without a workspace: for callers that must not allocate device memory.
+
+    The library keeps the scratch in a fixed built-in array (see
+    attn_bwd_noalloc_max_scratch_bytes); this function allocates nothing either.
+    Always the deterministic backward.  Calls that overlap on the GPU race on the
+    shared array; the first call on a device must come before any stream capture.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    B, S_q, H_q, d_qk = q.shape
+    _, S_kv, H_kv, d_v = v.shape
+    st = _load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(d_offset), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
+                                  int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset),
+                                  _stream(stream))
+    if st != ATTN_OK:
+        msg = _load().attn_bwd_noalloc_message().decode()
+        raise AttnError(st, "attn_bwd_noalloc" + (f" ({msg})" if msg else ""))
 
 
 KERNEL_CLASSES = ("fwd", "bwd_preprocess", "bwd_kv", "bwd_q", "bwd_dq_convert")

@@ -126,6 +126,11 @@ int timed(int kind, int nlaunch, cudaStream_t s, F&& launch) {
 
 }  // namespace
 
+namespace sdpa {
+// The device error word of the current device, for the other host files of the library.
+int* device_error_word() { return device_error_ptr(); }
+}  // namespace sdpa
+
 extern "C" {
 
 const char* attn_last_error_message(void) { return g_last_error; }

@@ -50,4 +50,7 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
 
+// Device error word of the current device (null if CUDA cannot report it).
+int* device_error_word();
+
 }  // namespace sdpa

@@ -1,0 +1,72 @@
+"""attn_bwd_noalloc: the backward for callers that cannot allocate device memory
+(runtimes that freeze their memory footprint at start-up and forbid allocation on
+the launch path, or C callers without a device allocator).  It keeps its scratch in
+a fixed array inside the library.
+
+This file is collected last on purpose: if it fails, a run that stops at the first
+failure has already run every other test.  It checks the entry point, called through
+the C ABI, against attn_bwd (the workspace entry point) on two calls in a row with
+different shapes, so the second call runs on an array that still holds the first
+call's contents.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL_GRAD, Shape, make_inputs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+OK, WORKSPACE = 0, 6
+
+
+def _run_both(sdpa, lib, shape, seed, st, window):
+    dev = torch.device("cuda")
+    x = make_inputs(shape, seed, learnable_offset=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = x["offset"].to(dev) if st == sdpa.LEARNABLE else None
+    kw = dict(causal=True, window=window, softmax_type=st, softmax_offset=off)
+    o, lse = sdpa.sdpa_forward(q, k, v, **kw)
+    ref = sdpa.sdpa_backward(q, k, v, o, do, lse, deterministic=True, **kw)
+
+    dq, dk, dv = torch.full_like(q, 3.0), torch.full_like(k, 3.0), torch.full_like(v, 3.0)
+    d_off = torch.full((shape.H_q,), 3.0, device=dev) if off is not None else None
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    B, S_q, H_q, d_qk = q.shape
+    _, S_kv, H_kv, d_v = v.shape
+    rc = lib.attn_bwd_noalloc(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv), p(d_off), B, S_q, S_kv,
+                              H_q, H_kv, d_qk, d_v, ctypes.c_float(0.0), 1, window, st, p(off),
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == OK, lib.attn_bwd_noalloc_message().decode()
+    torch.cuda.synchronize()
+    status, site = sdpa.attn_last_device_error()
+    assert status == 0, f"device error {status} at site {site:#x}"
+    got = [dq, dk, dv] + ([d_off] if d_off is not None else [])
+    want = [ref[0], ref[1], ref[2]] + ([ref[3]] if d_off is not None else [])
+    for name, g, w in zip(("dq", "dk", "dv", "d_offset"), got, want):
+        err = rel_l2(g.float().cpu().numpy(), w.float().cpu().numpy())
+        assert err <= TOL_GRAD, f"{name}: relative L2 {err} vs attn_bwd"
+
+
+def test_no_alloc_backward_matches_workspace_backward_twice():
+    import scaled_dot_product_tmem_gb300 as sdpa
+    lib = sdpa.library()
+    # first call: learnable sink, GQA, ragged length, window
+    _run_both(sdpa, lib, Shape(2, 300, 300, 8, 2, 128, 128), 201, sdpa.LEARNABLE, 100)
+    # second call right after, other shape: the array still holds the first call's data
+    _run_both(sdpa, lib, Shape(1, 200, 200, 4, 4, 64, 64), 202, sdpa.VANILLA, -1)
+
+
+def test_no_alloc_rejects_problems_beyond_its_array():
+    import scaled_dot_product_tmem_gb300 as sdpa
+    lib = sdpa.library()
+    cap = lib.attn_bwd_noalloc_max_scratch_bytes()
+    assert cap == 8 << 20
+    fake = ctypes.c_void_p(0x10000)
+    # B * H_q * S_pad = 8 * 32 * 8192 rows needs 16 MiB > 8 MiB: rejected before any launch
+    rc = lib.attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake, None, 8, 8192, 8192, 32, 8,
+                              128, 128, ctypes.c_float(0.0), 1, -1, 0, None, None)
+    assert rc == WORKSPACE
+    assert "scratch" in lib.attn_bwd_noalloc_message().decode()
