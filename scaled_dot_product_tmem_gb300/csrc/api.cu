@@ -285,8 +285,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     set_error("cuTensorMapEncodeTiled (backward operands)");
     return ATTN_ERR_CUDA;
   }
+  CUtensorMap tdq = tq;
+  if (fused && !sdpa::make_f32_bshd_map(&tdq, p.dq_acc, B, S_q, H_q, d_qk, bq_rows)) {
+    set_error("cuTensorMapEncodeTiled (dQ accumulator)");
+    return ATTN_ERR_CUDA;
+  }
   int rc = timed(ATTN_KERNEL_BWD_KV, 1, s,
-                 [&] { return sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, p, fused, s); });
+                 [&] { return sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s); });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("backward kv kernel launch", cudaGetLastError());

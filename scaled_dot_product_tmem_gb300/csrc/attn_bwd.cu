@@ -18,8 +18,8 @@
 //   bwd_kv           kv-stationary: one CTA per (b, kv head, 128 keys) walks the
 //                    query heads of the group x 64-row query tiles that see those
 //                    keys; dK/dV accumulate in TMEM (the GQA head sum is free).
-//                    Optionally also dQ^T = K^T dS^T per step, drained with fp32
-//                    atomics by a fourth warpgroup (non-deterministic path).
+//                    Optionally also dQ^T = K^T dS^T per step, added into an fp32
+//                    accumulator by TMA bulk reductions (non-deterministic path).
 //   bwd_q            query-stationary deterministic dQ: recomputes S, P, dP, dS
 //                    for one 128-row query tile over its kv tiles.
 //   bwd_dq_convert   dQ = bf16(scale * fp32 accumulator).
@@ -147,7 +147,9 @@ struct KvCfg {
   static constexpr int DO_STAGE = VCH * QCHUNK;
   static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // lse2[64] + D[64] per stage
   static constexpr int L_STAGE = 2 * BQ * 4;
-  static constexpr int OFF_BAR = OFF_L + NQ * L_STAGE;
+  static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
+  static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, q_full[NQ], q_empty[NQ], s_ready, dp_ready, p_ready, ds_ready, dq_ready, dq_free, mma_done
   static constexpr int NBAR = 1 + 2 * NQ + 7;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
@@ -167,7 +169,7 @@ template <int D_QK, int D_V, bool FUSE_DQ>
 __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = KvCfg<D_QK, D_V, FUSE_DQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -257,13 +259,16 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      auto issue_S_dP = [&](int st) {
-        const uint32_t qa = sQ + st * C::Q_STAGE, da = sDO + st * C::DO_STAGE;
+      auto issue_S = [&](int st) {
+        const uint32_t qa = sQ + st * C::Q_STAGE;
 #pragma unroll
         for (int kk = 0; kk < D_QK / 16; ++kk)
           mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
                  smem_desc_sw128(qa + (kk / 4) * C::QCHUNK + (kk % 4) * 32, 16, 1024), idS, kk > 0);
         mma_commit(s_ready);
+      };
+      auto issue_dP = [&](int st) {
+        const uint32_t da = sDO + st * C::DO_STAGE;
 #pragma unroll
         for (int kk = 0; kk < D_V / 16; ++kk)
           mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
@@ -273,10 +278,17 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       bool ok = mbar_wait(kv_full, 0, err, kKvFull) && mbar_wait(&q_full[0], 0, err, kKvQFull);
       if (ok) {
         tc_fence_after();
-        issue_S_dP(0);
+        issue_S(0);
+        issue_dP(0);
       }
+      // Issue order per step s: dV(s), S(s+1), dK(s), [dQ^T(s)], dP(s+1).  The next
+      // step's scores are computed while the P/dS warps finish step s, and each
+      // write into the S or dP columns comes after the MMA that last read them
+      // (tcgen05 MMAs of one thread execute in issue order).
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % C::NQ;
+        const int st1 = (s + 1) % C::NQ;
+        const bool more = s + 1 < nsteps;
         const uint32_t qa = sQ + st * C::Q_STAGE, da = sDO + st * C::DO_STAGE;
         ok = mbar_wait(p_ready, s & 1, err, kKvP);
         if (!ok) break;
@@ -286,6 +298,12 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
         for (int kk = 0; kk < C::BQ / 16; ++kk)
           mma_ts(tmem + C::COL_DV, tmem + C::COL_S + (kk / 2) * 32 + (kk % 2) * 8,
                  smem_desc_sw128(da + kk * 2048, C::QCHUNK, 1024), idDV, (s > 0 || kk > 0) ? 1u : 0u);
+        if (more) {
+          ok = mbar_wait(&q_full[st1], ((s + 1) / C::NQ) & 1, err, kKvQFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_S(st1);
+        }
         ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
         if (!ok) break;
         tc_fence_after();
@@ -306,13 +324,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
           mma_commit(dq_ready);
         }
         mma_commit(&q_empty[st]);
-        if (s + 1 < nsteps) {
-          const int st1 = (s + 1) % C::NQ;
-          ok = mbar_wait(&q_full[st1], ((s + 1) / C::NQ) & 1, err, kKvQFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_S_dP(st1);
-        }
+        if (more) issue_dP(st1);
       }
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, err, kKvDone);
@@ -337,9 +349,12 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       {
         uint32_t rr[32];
         tmem_ld32(lane_addr + C::COL_S + 32 * w, rr);
+        float lv[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -l2[c]));
+        for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -lv[c]));
       }
       if (!tile_fully_visible(mask, q0, C::BQ, n0, C::BN)) {
 #pragma unroll
@@ -362,11 +377,14 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       {
         uint32_t rr[32];
         tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
+        float dv4[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a = pr[2 * c] * (__uint_as_float(rr[2 * c]) - dd[2 * c]);
-          const float bq = pr[2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - dd[2 * c + 1]);
+          const float a = pr[2 * c] * (__uint_as_float(rr[2 * c]) - dv4[2 * c]);
+          const float bq = pr[2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - dv4[2 * c + 1]);
           dsk[c] = pack_bf16x2(a, bq);
         }
       }
@@ -423,27 +441,41 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     }
   } else if (FUSE_DQ && warp >= 10 && warp < 14) {
     // ------------------------------------------------------------ dQ drain: TMEM lane = head-dim index d
+    // dQ^T of each step goes TMEM -> registers -> shared memory as [q][d] fp32, and
+    // one thread adds the whole 64 x d_qk tile into the fp32 accumulator with a
+    // TMA bulk reduction (rows past S_q are skipped by the TMA unit).
     const int d = (warp % 4) * 32 + lane;
+    const int tid_d = threadIdx.x - 320;  // 0..127 over the four drain warps
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_DQS);
+    if (tid_d == 0) tma_prefetch_desc(&tmDQ);
     for (int s = 0; s < nsteps; ++s) {
-      if (!mbar_wait_warp(dq_ready, s & 1, err, kKvDQReady)) break;
+      const bool got = mbar_wait(dq_ready, s & 1, err, kKvDQReady);
+      if (!bar_red_and(1, 128, got)) break;  // uniform over the 128 drain threads
       tc_fence_after();
       const int h = hk * p.G + s / nq;
       const int q0 = (ilo + s % nq) * C::BQ;
-      float* base = p.dq_acc + (((size_t)b * p.S_q + q0) * p.H_q + h) * D_QK + d;
-      const size_t qstride = (size_t)p.H_q * D_QK;
-#pragma unroll
-      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DQ + c0, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (q0 + c0 + c < p.S_q) atomicAdd(base + (size_t)(c0 + c) * qstride, __uint_as_float(rr[c]));
-      }
+      uint32_t ra[32], rb[32];
+      tmem_ld32(lane_addr + C::COL_DQ, ra);
+      tmem_ld32(lane_addr + C::COL_DQ + 32, rb);
+      tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(dq_free);
+      mbar_arrive(dq_free);  // the TMEM columns may be overwritten now
+      if (tid_d == 0) bulk_wait_read_all();  // previous tile has left shared memory
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        stage[c * D_QK + d] = __uint_as_float(ra[c]);
+        stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid_d == 0) {
+        tma_reduce_add_4d(&tmDQ, stage, 0, h, q0, b);
+        bulk_commit_group();
+      }
     }
+    if (tid_d == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -459,28 +491,29 @@ bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return d_qk == 128 && (d_v ==
 
 template <int D_QK, int D_V, bool FUSE>
 static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using C = KvCfg<D_QK, D_V, FUSE>;
   auto kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   dim3 grid((p.S_kv + C::BN - 1) / C::BN, p.H_kv, p.B);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const BwdParams& p, bool fuse_dq, cudaStream_t stream) {
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
+                  cudaStream_t stream) {
   if (fuse_dq) {
-    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, p, stream);
-    if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, p, stream);
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
     return -2;
   }
-  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, false>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
   return -2;
 }
 

@@ -272,18 +272,13 @@ __global__ void __launch_bounds__(320, 1)
           l *= alpha;
           if (it > 0) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D_V; c0 += 32) {
-              uint32_t rr[32];
-              tmem_ld32(lane_addr + colO + c0, rr);
+            for (int c0 = 0; c0 < D_V; c0 += 16) {
+              uint32_t rr[16];
+              tmem_ld16(lane_addr + colO + c0, rr);
               tmem_ld_wait();
-              uint32_t w0[16], w1[16];
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                w0[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-                w1[c] = __float_as_uint(__uint_as_float(rr[16 + c]) * alpha);
-              }
-              tmem_st16(lane_addr + colO + c0, w0);
-              tmem_st16(lane_addr + colO + c0 + 16, w1);
+              for (int c = 0; c < 16; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+              tmem_st16(lane_addr + colO + c0, rr);
             }
           }
           m_run = m_new;

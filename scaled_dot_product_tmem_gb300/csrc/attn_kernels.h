@@ -43,8 +43,10 @@ struct BwdParams {
 };
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
+// tdq: fp32 map of dq_acc (box d_qk x 64 rows) when fuse_dq, else any valid map (unused).
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const BwdParams& p, bool fuse_dq, cudaStream_t stream);
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
+                  cudaStream_t stream);
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);

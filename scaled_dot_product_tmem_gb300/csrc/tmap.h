@@ -40,6 +40,21 @@ inline bool make_bshd_map(CUtensorMap* m, const void* base, int B, int S, int H,
   return r == CUDA_SUCCESS;
 }
 
+// An fp32 BSHD tensor [B, S, H, D] (D <= 256) as a 4-D TMA tensor with a box of
+// D x 1 head x `box_rows` rows x 1 batch, no swizzle (used for bulk reductions).
+inline bool make_f32_bshd_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int box_rows) {
+  PFN_encodeTiled enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4, (cuuint64_t)S * H * D * 4};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A row-major bf16 matrix [rows, cols] as a 2-D TMA tensor with a 64 x box_rows
 // box and 128-byte swizzle.
 inline bool make_2d_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
