@@ -150,11 +150,13 @@ struct KvCfg {
   static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  // kv_full, q_full[NQ], q_empty[NQ], s_ready, dp_ready, p_ready, ds_ready, dq_ready, dq_free, mma_done
-  static constexpr int NBAR = 1 + 2 * NQ + 7;
+  // kv_full, q_full[NQ], q_empty[NQ], s_ready, dp_ready, p_ready, ds_ready, dq_ready, dq_free, mma_done,
+  // dv_done, dk_done
+  static constexpr int NBAR = 1 + 2 * NQ + 9;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
-  static constexpr int THREADS = FUSE_DQ ? 448 : 320;
+  static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
+  static constexpr int THREADS = FUSE_DQ ? 480 : 352;
   // TMEM columns
   static constexpr int COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
   static_assert(COL_DQ + (FUSE_DQ ? 64 : 0) <= 512, "TMEM budget");
@@ -163,10 +165,11 @@ struct KvCfg {
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
 };
 
-enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain };
+enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
+              kKvDvDone, kKvDkDone };
 
 template <int D_QK, int D_V, bool FUSE_DQ>
-__global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
+__global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -184,6 +187,8 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
   uint64_t* dq_ready = s_ready + 4;
   uint64_t* dq_free = s_ready + 5;
   uint64_t* mma_done = s_ready + 6;
+  uint64_t* dv_done = s_ready + 7;
+  uint64_t* dk_done = s_ready + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -206,7 +211,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
     mbar_init(ds_ready, 256);
     mbar_init(dq_ready, 1);
     mbar_init(dq_free, 128);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);
+    mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -249,8 +256,15 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
         mbar_wait(&q_full[s], (last / C::NQ) & 1, err, kKvDrain);
       }
     }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 8 || warp == C::MMA_B_WARP) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads, because one cannot issue tcgen05.mma fast enough to
+    // keep the tensor core busy with these 64-wide tiles:
+    //   A (warp 8):  S^T(s) = K Q_s^T, dP^T(s) = V dO_s^T
+    //   B:           dV += P^T(s) dO_s, dK += dS^T(s) Q_s, [dQ^T(s) = K^T dS^T(s)]
+    // MMAs of different threads are not ordered, so A waits for B's dv_done(s-1)
+    // before S(s) overwrites the columns that held P(s-1), and for B's dk_done(s-1)
+    // before dP(s) overwrites the columns that held dS(s-1).
     if (lane == 0 && nsteps > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
       constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
@@ -259,73 +273,72 @@ __global__ void __launch_bounds__(FUSE_DQ ? 448 : 320, 1)
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      auto issue_S = [&](int st) {
-        const uint32_t qa = sQ + st * C::Q_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < D_QK / 16; ++kk)
-          mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
-                 smem_desc_sw128(qa + (kk / 4) * C::QCHUNK + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-        mma_commit(s_ready);
-      };
-      auto issue_dP = [&](int st) {
-        const uint32_t da = sDO + st * C::DO_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < D_V / 16; ++kk)
-          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + (kk / 4) * C::KCHUNK + (kk % 4) * 32, 16, 1024),
-                 smem_desc_sw128(da + (kk / 4) * C::QCHUNK + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-        mma_commit(dp_ready);
-      };
-      bool ok = mbar_wait(kv_full, 0, err, kKvFull) && mbar_wait(&q_full[0], 0, err, kKvQFull);
-      if (ok) {
-        tc_fence_after();
-        issue_S(0);
-        issue_dP(0);
-      }
-      // Issue order per step s: dV(s), S(s+1), dK(s), [dQ^T(s)], dP(s+1).  The next
-      // step's scores are computed while the P/dS warps finish step s, and each
-      // write into the S or dP columns comes after the MMA that last read them
-      // (tcgen05 MMAs of one thread execute in issue order).
-      for (int s = 0; s < nsteps && ok; ++s) {
-        const int st = s % C::NQ;
-        const int st1 = (s + 1) % C::NQ;
-        const bool more = s + 1 < nsteps;
-        const uint32_t qa = sQ + st * C::Q_STAGE, da = sDO + st * C::DO_STAGE;
-        ok = mbar_wait(p_ready, s & 1, err, kKvP);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO   (P^T bf16 in TMEM: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + (kk / 2) * 32 + (kk % 2) * 8,
-                 smem_desc_sw128(da + kk * 2048, C::QCHUNK, 1024), idDV, (s > 0 || kk > 0) ? 1u : 0u);
-        if (more) {
-          ok = mbar_wait(&q_full[st1], ((s + 1) / C::NQ) & 1, err, kKvQFull);
+      bool ok = mbar_wait(kv_full, 0, err, kKvFull);
+      if (warp == 8) {
+        const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);  // K as K-major A of S^T
+        const uint64_t dV0 = smem_desc_sw128(sV, 16, 1024);  // V as K-major A of dP^T
+        for (int s = 0; s < nsteps && ok; ++s) {
+          const int st = s % C::NQ;
+          ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
+          if (ok && s > 0) ok = mbar_wait(dv_done, (s - 1) & 1, err, kKvDvDone);
           if (!ok) break;
           tc_fence_after();
-          issue_S(st1);
-        }
-        ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
-        if (!ok) break;
-        tc_fence_after();
-        // dK += dS^T Q
+          const uint64_t dq = smem_desc_sw128(sQ + st * C::Q_STAGE, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8,
-                 smem_desc_sw128(qa + kk * 2048, C::QCHUNK, 1024), idDK, (s > 0 || kk > 0) ? 1u : 0u);
-        if constexpr (FUSE_DQ) {
-          ok = mbar_wait(dq_free, (s & 1) ^ 1, err, kKvDQFree);
+          for (int kk = 0; kk < D_QK / 16; ++kk)
+            mma_ss(tmem + C::COL_S, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
+                   desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
+          mma_commit(s_ready);
+          if (s > 0) ok = mbar_wait(dk_done, (s - 1) & 1, err, kKvDkDone);
           if (!ok) break;
           tc_fence_after();
-          // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
+          const uint64_t ddo = smem_desc_sw128(sDO + st * C::DO_STAGE, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sK + kk * 2048, C::KCHUNK, 1024),
-                   smem_desc_sw128(sDS + kk * 2048, C::KCHUNK, 1024), idDQ, kk > 0);
-          mma_commit(dq_ready);
+          for (int kk = 0; kk < D_V / 16; ++kk)
+            mma_ss(tmem + C::COL_DP, desc_add(dV0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
+                   desc_add(ddo, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
+          mma_commit(dp_ready);
         }
-        mma_commit(&q_empty[st]);
-        if (more) issue_dP(st1);
+      } else {
+        const uint64_t dKt0 = smem_desc_sw128(sK, C::KCHUNK, 1024);   // K as MN-major A of dQ^T
+        const uint64_t dDS0 = smem_desc_sw128(sDS, C::KCHUNK, 1024);  // dS^T as MN-major B of dQ^T
+        for (int s = 0; s < nsteps && ok; ++s) {
+          const int st = s % C::NQ;
+          const uint64_t ddo_mn = smem_desc_sw128(sDO + st * C::DO_STAGE, C::QCHUNK, 1024);  // dO, MN-major B of dV
+          const uint64_t dq_mn = smem_desc_sw128(sQ + st * C::Q_STAGE, C::QCHUNK, 1024);     // Q, MN-major B of dK
+          ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait(p_ready, s & 1, err, kKvP);
+          if (!ok) break;
+          tc_fence_after();
+          // dV += P^T dO   (P^T bf16 in TMEM: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_S + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048),
+                   idDV, (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(dv_done);
+          ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
+          if (!ok) break;
+          tc_fence_after();
+          // dK += dS^T Q
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
+                   idDK, (s > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (FUSE_DQ) {
+            ok = mbar_wait(dq_free, (s & 1) ^ 1, err, kKvDQFree);
+            if (!ok) break;
+            tc_fence_after();
+            // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+              mma_ss(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS0, kk * 2048), idDQ, kk > 0);
+            mma_commit(dq_ready);
+          }
+          // The stage's S/dP MMAs (issuer A) completed before P(s)/dS(s) existed.
+          mma_commit(dk_done);
+          mma_commit(&q_empty[st]);
+        }
       }
+      // Every MMA of both issuers must be complete before TMEM is released.
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, err, kKvDone);
     }
@@ -635,6 +648,9 @@ __global__ void __launch_bounds__(320, 1)
       for (int n = 0; n < nj && ok; ++n) {
         const int sk = n % C::NK, sv = n % C::NV;
         const uint32_t ka = sK + sk * C::QCH * C::CHUNK, va = sV + sv * C::VCH * C::CHUNK;
+        const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dKa = smem_desc_sw128(ka, 16, 1024);
+        const uint64_t dDO0 = smem_desc_sw128(sDO, 16, 1024), dVa = smem_desc_sw128(va, 16, 1024);
+        const uint64_t dKmn = smem_desc_sw128(ka, C::CHUNK, 1024);
         ok = mbar_wait(&k_full[sk], (n / C::NK) & 1, err, kQKFull);
         if (!ok) break;
         tc_fence_after();
@@ -642,7 +658,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D_QK / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::COL_S, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idS,
+          mma_ss(tmem + C::COL_S, desc_add(dQ0, off), desc_add(dKa, off), idS,
                  kk > 0);
         }
         mma_commit(s_ready);
@@ -653,7 +669,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D_V / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sDO + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idS,
+          mma_ss(tmem + C::COL_DP, desc_add(dDO0, off), desc_add(dVa, off), idS,
                  kk > 0);
         }
         mma_commit(dp_ready);
@@ -665,7 +681,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           mma_ts(tmem + C::COL_DQ, tmem + C::COL_S + (kk / 4) * 64 + (kk % 4) * 8,
-                 smem_desc_sw128(ka + kk * 2048, C::CHUNK, 1024), idDQ, (n > 0 || kk > 0) ? 1u : 0u);
+                 desc_add(dKmn, kk * 2048), idDQ, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&k_empty[sk]);
       }
       mma_commit(mma_done);

@@ -157,6 +157,8 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues for both query tiles in the order PV_0(j), S_0(j+1),
+    // PV_1(j), S_1(j+1): each tile's softmax overlaps the other tile's GEMMs.
     if (lane == 0 && any) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
@@ -164,19 +166,19 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
       auto issue_S = [&](int t, int stage) {
-        const uint32_t qa = sQ + t * C::Q_TILE, ka = sK + stage * C::K_STAGE;
+        const uint64_t dq = smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D_QK / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + t * 256, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idS,
-                 kk > 0);
+          mma_ss(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
         }
       };
       auto issue_PV = [&](int t, int stage, bool acc) {
-        const uint32_t va = sV + stage * C::V_STAGE;
+        const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, smem_desc_sw128(va + kk * 2048, C::CHUNK, 1024), idO,
+          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
                  (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, err, kSiteQ);
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, err, kSiteDrain);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     const int t = warp / 4;
     const bool my_active = t ? active[1] : active[0];

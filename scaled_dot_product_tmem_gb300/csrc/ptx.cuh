@@ -207,6 +207,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Move a descriptor's start address by `bytes` (a multiple of 16).  The address
+// field holds shared-memory offsets >> 4, which stay below 2^14, so the add never
+// carries into the next field.  Building a descriptor once per tile and advancing it
+// with constant adds keeps the MMA-issuing thread's instruction chain short: a full
+// rebuild per MMA is a serial chain of 64-bit integer ops that costs more cycles
+// than a small MMA takes to execute.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // Bits: D format [4,6) = 1 (f32); A format [7,10) = 1 (bf16); B format [10,13)
 // = 1 (bf16); A major bit 15, B major bit 16 (0 = K-major, 1 = MN-major);
