@@ -139,8 +139,9 @@ struct KvCfg {
   static constexpr int NQ = (D_QK == 64 && D_V == 64) ? 6 : 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + QCH * KCHUNK;
-  static constexpr int OFF_DS = OFF_V + VCH * KCHUNK;  // dS^T [128 keys x 64 q] bf16, swizzled
-  static constexpr int DS_BYTES = FUSE_DQ ? 128 * 128 : 0;
+  static constexpr int OFF_DS = OFF_V + VCH * KCHUNK;  // 2 x dS^T [128 keys x 64 q] bf16, swizzled
+  static constexpr int DS_BUF = 128 * 128;
+  static constexpr int DS_BYTES = FUSE_DQ ? 2 * DS_BUF : 0;
   static constexpr int OFF_Q = OFF_DS + DS_BYTES;
   static constexpr int Q_STAGE = QCH * QCHUNK;
   static constexpr int OFF_DO = OFF_Q + NQ * Q_STAGE;
@@ -150,16 +151,19 @@ struct KvCfg {
   static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  // kv_full, q_full[NQ], q_empty[NQ], s_ready, dp_ready, p_ready, ds_ready, dq_ready, dq_free, mma_done,
-  // dv_done, dk_done
-  static constexpr int NBAR = 1 + 2 * NQ + 9;
+  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready, ds_ready, dq_ready, dq_free,
+  // mma_done, dv_done[2], dk_done
+  static constexpr int NBAR = 1 + 2 * NQ + 11;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
   static constexpr int THREADS = FUSE_DQ ? 480 : 352;
   // TMEM columns
-  static constexpr int COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
-  static_assert(COL_DQ + (FUSE_DQ ? 64 : 0) <= 512, "TMEM budget");
+  // S^T/P^T is double-buffered (slots COL_S0 / COL_S1, step s uses slot s & 1) so the
+  // next step's scores can be computed while the current P^T still feeds dV.
+  static constexpr int COL_S0 = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
+  static constexpr int COL_S1 = COL_DQ + (FUSE_DQ ? 64 : 0);
+  static_assert(COL_S1 + 64 <= 512, "TMEM budget");
   static_assert(!FUSE_DQ || D_QK == 128, "dQ^T = K^T dS^T needs M = d_qk = 128");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
@@ -180,15 +184,15 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NQ;
-  uint64_t* s_ready = q_empty + C::NQ;
-  uint64_t* dp_ready = s_ready + 1;
-  uint64_t* p_ready = s_ready + 2;
-  uint64_t* ds_ready = s_ready + 3;
-  uint64_t* dq_ready = s_ready + 4;
-  uint64_t* dq_free = s_ready + 5;
-  uint64_t* mma_done = s_ready + 6;
-  uint64_t* dv_done = s_ready + 7;
-  uint64_t* dk_done = s_ready + 8;
+  uint64_t* s_ready = q_empty + C::NQ;  // [2], per S slot
+  uint64_t* dp_ready = s_ready + 2;
+  uint64_t* p_ready = s_ready + 3;
+  uint64_t* ds_ready = s_ready + 4;
+  uint64_t* dq_ready = s_ready + 5;
+  uint64_t* dq_free = s_ready + 6;
+  uint64_t* mma_done = s_ready + 7;
+  uint64_t* dv_done = s_ready + 8;  // [2], per S slot
+  uint64_t* dk_done = s_ready + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -205,14 +209,16 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NQ; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
-    mbar_init(s_ready, 1);
+    mbar_init(&s_ready[0], 1);
+    mbar_init(&s_ready[1], 1);
     mbar_init(dp_ready, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_ready, 1);
     mbar_init(dq_free, 128);
     mbar_init(mma_done, 2);
-    mbar_init(dv_done, 1);
+    mbar_init(&dv_done[0], 1);
+    mbar_init(&dv_done[1], 1);
     mbar_init(dk_done, 1);
     fence_barrier_init();
   }
@@ -279,16 +285,19 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         const uint64_t dV0 = smem_desc_sw128(sV, 16, 1024);  // V as K-major A of dP^T
         for (int s = 0; s < nsteps && ok; ++s) {
           const int st = s % C::NQ;
+          const int slot = s & 1;
           ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
-          if (ok && s > 0) ok = mbar_wait(dv_done, (s - 1) & 1, err, kKvDvDone);
+          // slot reuse: P^T(s-2) in this slot must have been read by dV(s-2)
+          if (ok && s >= 2) ok = mbar_wait(&dv_done[slot], ((s >> 1) - 1) & 1, err, kKvDvDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dq = smem_desc_sw128(sQ + st * C::Q_STAGE, 16, 1024);
+          const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
 #pragma unroll
           for (int kk = 0; kk < D_QK / 16; ++kk)
-            mma_ss(tmem + C::COL_S, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
+            mma_ss(colS, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
                    desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
-          mma_commit(s_ready);
+          mma_commit(&s_ready[slot]);
           if (s > 0) ok = mbar_wait(dk_done, (s - 1) & 1, err, kKvDkDone);
           if (!ok) break;
           tc_fence_after();
@@ -309,12 +318,14 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait(p_ready, s & 1, err, kKvP);
           if (!ok) break;
           tc_fence_after();
-          // dV += P^T dO   (P^T bf16 in TMEM: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
+          const int slot = s & 1;
+          const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
+          // dV += P^T dO   (P^T bf16 in the slot: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts(tmem + C::COL_DV, tmem + C::COL_S + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048),
-                   idDV, (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(dv_done);
+            mma_ts(tmem + C::COL_DV, colS + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048), idDV,
+                   (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&dv_done[slot]);
           ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
           if (!ok) break;
           tc_fence_after();
@@ -323,18 +334,21 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           for (int kk = 0; kk < C::BQ / 16; ++kk)
             mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
                    idDK, (s > 0 || kk > 0) ? 1u : 0u);
+          // dS^T(s) in TMEM is consumed once dK(s) completes: issuer A may write dP(s+1).
+          // (dQ^T reads dS^T from shared memory, double-buffered, so it does not gate dP.)
+          mma_commit(dk_done);
           if constexpr (FUSE_DQ) {
             ok = mbar_wait(dq_free, (s & 1) ^ 1, err, kKvDQFree);
             if (!ok) break;
             tc_fence_after();
             // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
+            const uint64_t dDS = desc_add(dDS0, slot * C::DS_BUF);
 #pragma unroll
             for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ss(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS0, kk * 2048), idDQ, kk > 0);
+              mma_ss(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS, kk * 2048), idDQ, kk > 0);
             mma_commit(dq_ready);
           }
           // The stage's S/dP MMAs (issuer A) completed before P(s)/dS(s) existed.
-          mma_commit(dk_done);
           mma_commit(&q_empty[st]);
         }
       }
@@ -355,13 +369,15 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       const int q0 = (ilo + s % nq) * C::BQ;
       const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
       const float* dd = l2 + C::BQ;
-      ok = mbar_wait_warp(s_ready, s & 1, err, kKvS);
+      const int slot = s & 1;
+      const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
+      ok = mbar_wait_warp(&s_ready[slot], (s >> 1) & 1, err, kKvS);
       if (!ok) break;
       tc_fence_after();
       float pr[32];
       {
         uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_S + 32 * w, rr);
+        tmem_ld32(lane_addr + colS + 32 * w, rr);
         float lv[32];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
@@ -378,7 +394,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
-        tmem_st16(lane_addr + C::COL_S + 32 * w, pk);
+        tmem_st16(lane_addr + colS + 32 * w, pk);
         tmem_st_wait();
       }
       tc_fence_before();
@@ -404,7 +420,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
       if constexpr (FUSE_DQ) {
         // dS^T row r, query columns 32w..32w+31 -> 16-byte chunks 4w..4w+3 (128-byte swizzle)
-        uint8_t* rowp = smem + C::OFF_DS + r * 128;
+        uint8_t* rowp = smem + C::OFF_DS + slot * C::DS_BUF + r * 128;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int chunk = (4 * w + k) ^ (r & 7);
