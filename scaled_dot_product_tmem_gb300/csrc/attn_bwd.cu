@@ -151,9 +151,11 @@ struct KvCfg {
   static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready, ds_ready, dq_ready, dq_free,
-  // mma_done, dv_done[2], dk_done
-  static constexpr int NBAR = 1 + 2 * NQ + 11;
+  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, dq_ready, dq_free,
+  // mma_done, dv_done[2], dk_done.  Barriers of the double-buffered S slot are per slot: with
+  // two slots the P/dS warps can finish step s+1's P before issuer B has waited for step s's,
+  // and a single barrier would then complete two phases before B looks.
+  static constexpr int NBAR = 1 + 2 * NQ + 12;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
@@ -186,13 +188,13 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   uint64_t* q_empty = q_full + C::NQ;
   uint64_t* s_ready = q_empty + C::NQ;  // [2], per S slot
   uint64_t* dp_ready = s_ready + 2;
-  uint64_t* p_ready = s_ready + 3;
-  uint64_t* ds_ready = s_ready + 4;
-  uint64_t* dq_ready = s_ready + 5;
-  uint64_t* dq_free = s_ready + 6;
-  uint64_t* mma_done = s_ready + 7;
-  uint64_t* dv_done = s_ready + 8;  // [2], per S slot
-  uint64_t* dk_done = s_ready + 10;
+  uint64_t* p_ready = s_ready + 3;      // [2], per S slot
+  uint64_t* ds_ready = s_ready + 5;
+  uint64_t* dq_ready = s_ready + 6;
+  uint64_t* dq_free = s_ready + 7;
+  uint64_t* mma_done = s_ready + 8;
+  uint64_t* dv_done = s_ready + 9;      // [2], per S slot
+  uint64_t* dk_done = s_ready + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     mbar_init(&s_ready[0], 1);
     mbar_init(&s_ready[1], 1);
     mbar_init(dp_ready, 1);
-    mbar_init(p_ready, 256);
+    mbar_init(&p_ready[0], 256);
+    mbar_init(&p_ready[1], 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_ready, 1);
     mbar_init(dq_free, 128);
@@ -264,14 +267,14 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     }
   } else if (warp == 8 || warp == C::MMA_B_WARP) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads, because one cannot issue tcgen05.mma fast enough to
+    // Two issuing warps, because one cannot issue tcgen05.mma fast enough to
     // keep the tensor core busy with these 64-wide tiles:
     //   A (warp 8):  S^T(s) = K Q_s^T, dP^T(s) = V dO_s^T
     //   B:           dV += P^T(s) dO_s, dK += dS^T(s) Q_s, [dQ^T(s) = K^T dS^T(s)]
-    // MMAs of different threads are not ordered, so A waits for B's dv_done(s-1)
+    // MMAs of different warps are not ordered, so A waits for B's dv_done
     // before S(s) overwrites the columns that held P(s-1), and for B's dk_done(s-1)
     // before dP(s) overwrites the columns that held dS(s-1).
-    if (lane == 0 && nsteps > 0) {
+    if (nsteps > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
       constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
       constexpr uint32_t idDK = idesc_bf16_f32(128, D_QK, false, true);
@@ -279,34 +282,34 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait(kv_full, 0, err, kKvFull);
+      bool ok = mbar_wait_warp(kv_full, 0, err, kKvFull);
       if (warp == 8) {
         const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);  // K as K-major A of S^T
         const uint64_t dV0 = smem_desc_sw128(sV, 16, 1024);  // V as K-major A of dP^T
         for (int s = 0; s < nsteps && ok; ++s) {
           const int st = s % C::NQ;
           const int slot = s & 1;
-          ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
+          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
           // slot reuse: P^T(s-2) in this slot must have been read by dV(s-2)
-          if (ok && s >= 2) ok = mbar_wait(&dv_done[slot], ((s >> 1) - 1) & 1, err, kKvDvDone);
+          if (ok && s >= 2) ok = mbar_wait_warp(&dv_done[slot], ((s >> 1) - 1) & 1, err, kKvDvDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dq = smem_desc_sw128(sQ + st * C::Q_STAGE, 16, 1024);
           const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
 #pragma unroll
           for (int kk = 0; kk < D_QK / 16; ++kk)
-            mma_ss(colS, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
+            mma_ss_warp(colS, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
                    desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
-          mma_commit(&s_ready[slot]);
-          if (s > 0) ok = mbar_wait(dk_done, (s - 1) & 1, err, kKvDkDone);
+          mma_commit_warp(&s_ready[slot]);
+          if (s > 0) ok = mbar_wait_warp(dk_done, (s - 1) & 1, err, kKvDkDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t ddo = smem_desc_sw128(sDO + st * C::DO_STAGE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D_V / 16; ++kk)
-            mma_ss(tmem + C::COL_DP, desc_add(dV0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
+            mma_ss_warp(tmem + C::COL_DP, desc_add(dV0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
                    desc_add(ddo, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
-          mma_commit(dp_ready);
+          mma_commit_warp(dp_ready);
         }
       } else {
         const uint64_t dKt0 = smem_desc_sw128(sK, C::KCHUNK, 1024);   // K as MN-major A of dQ^T
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           const int st = s % C::NQ;
           const uint64_t ddo_mn = smem_desc_sw128(sDO + st * C::DO_STAGE, C::QCHUNK, 1024);  // dO, MN-major B of dV
           const uint64_t dq_mn = smem_desc_sw128(sQ + st * C::Q_STAGE, C::QCHUNK, 1024);     // Q, MN-major B of dK
-          ok = mbar_wait(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait(p_ready, s & 1, err, kKvP);
+          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait_warp(&p_ready[s & 1], (s >> 1) & 1, err, kKvP);
           if (!ok) break;
           tc_fence_after();
           const int slot = s & 1;
@@ -323,38 +326,38 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           // dV += P^T dO   (P^T bf16 in the slot: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts(tmem + C::COL_DV, colS + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048), idDV,
+            mma_ts_warp(tmem + C::COL_DV, colS + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048), idDV,
                    (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&dv_done[slot]);
-          ok = mbar_wait(ds_ready, s & 1, err, kKvDS);
+          mma_commit_warp(&dv_done[slot]);
+          ok = mbar_wait_warp(ds_ready, s & 1, err, kKvDS);
           if (!ok) break;
           tc_fence_after();
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
+            mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
                    idDK, (s > 0 || kk > 0) ? 1u : 0u);
           // dS^T(s) in TMEM is consumed once dK(s) completes: issuer A may write dP(s+1).
           // (dQ^T reads dS^T from shared memory, double-buffered, so it does not gate dP.)
-          mma_commit(dk_done);
+          mma_commit_warp(dk_done);
           if constexpr (FUSE_DQ) {
-            ok = mbar_wait(dq_free, (s & 1) ^ 1, err, kKvDQFree);
+            ok = mbar_wait_warp(dq_free, (s & 1) ^ 1, err, kKvDQFree);
             if (!ok) break;
             tc_fence_after();
             // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
             const uint64_t dDS = desc_add(dDS0, slot * C::DS_BUF);
 #pragma unroll
             for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ss(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS, kk * 2048), idDQ, kk > 0);
-            mma_commit(dq_ready);
+              mma_ss_warp(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS, kk * 2048), idDQ, kk > 0);
+            mma_commit_warp(dq_ready);
           }
           // The stage's S/dP MMAs (issuer A) completed before P(s)/dS(s) existed.
-          mma_commit(&q_empty[st]);
+          mma_commit_warp(&q_empty[st]);
         }
       }
       // Every MMA of both issuers must be complete before TMEM is released.
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, err, kKvDone);
+      mma_commit_warp(mma_done);
+      mbar_wait_warp(mma_done, 0, err, kKvDone);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ P / dS warpgroups
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[slot]);
       ok = mbar_wait_warp(dp_ready, s & 1, err, kKvDP);
       if (!ok) break;
       tc_fence_after();
@@ -561,21 +564,24 @@ struct QCfg {
   static constexpr int OFF_K = OFF_DO + VCH * CHUNK;
   static constexpr int OFF_V = OFF_K + NK * QCH * CHUNK;
   static constexpr int OFF_BAR = OFF_V + NV * VCH * CHUNK;
-  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready, ds_ready, mma_done
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 4;
+  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready, ds_ready, mma_done,
+  // s_free, dq_done
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 6;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
+  // dS (bf16) is written over the dP columns, so the next S can be computed as soon
+  // as the dS warps have loaded the current S.
   static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256;
   static_assert(COL_DQ + D_QK <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain };
+enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone };
 
 template <int D_QK, int D_V>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const BwdParams p) {
@@ -592,6 +598,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* dp_ready = s_ready + 1;
   uint64_t* ds_ready = s_ready + 2;
   uint64_t* mma_done = s_ready + 3;
+  uint64_t* s_free = s_ready + 4;
+  uint64_t* dq_done = s_ready + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -610,7 +618,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(s_ready, 1);
     mbar_init(dp_ready, 1);
     mbar_init(ds_ready, 256);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);
+    mbar_init(s_free, 256);
+    mbar_init(dq_done, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -654,56 +664,66 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait(&v_full[s], (last / C::NV) & 1, err, kQDrain);
       }
     }
-  } else if (warp == 8) {
-    if (lane == 0 && nj > 0) {
+  } else if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    //   A (warp 8):  S(n) = Q K_n^T, dP(n) = dO V_n^T
+    //   B (warp 10): dQ += dS(n) K_n
+    // S(n+1) waits for the dS warps to have loaded S(n) (s_free); dP(n+1) waits
+    // for dQ(n), which reads dS(n) from the dP columns (dq_done).
+    if (nj > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idDQ = idesc_bf16_f32(128, D_QK, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      bool ok = mbar_wait(q_full, 0, err, kQQ);
-      for (int n = 0; n < nj && ok; ++n) {
-        const int sk = n % C::NK, sv = n % C::NV;
-        const uint32_t ka = sK + sk * C::QCH * C::CHUNK, va = sV + sv * C::VCH * C::CHUNK;
-        const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dKa = smem_desc_sw128(ka, 16, 1024);
-        const uint64_t dDO0 = smem_desc_sw128(sDO, 16, 1024), dVa = smem_desc_sw128(va, 16, 1024);
-        const uint64_t dKmn = smem_desc_sw128(ka, C::CHUNK, 1024);
-        ok = mbar_wait(&k_full[sk], (n / C::NK) & 1, err, kQKFull);
-        if (!ok) break;
-        tc_fence_after();
-        // S = Q K^T
+      bool ok = mbar_wait_warp(q_full, 0, err, kQQ);
+      if (warp == 8) {
+        const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
+        for (int n = 0; n < nj && ok; ++n) {
+          const int sk = n % C::NK, sv = n % C::NV;
+          const uint64_t dKa = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, 16, 1024);
+          const uint64_t dVa = smem_desc_sw128(sV + sv * C::VCH * C::CHUNK, 16, 1024);
+          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull);
+          if (ok && n > 0) ok = mbar_wait_warp(s_free, (n - 1) & 1, err, kQSFree);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D_QK / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::COL_S, desc_add(dQ0, off), desc_add(dKa, off), idS,
-                 kk > 0);
+          for (int kk = 0; kk < D_QK / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+            mma_ss_warp(tmem + C::COL_S, desc_add(dQ0, off), desc_add(dKa, off), idS, kk > 0);
+          }
+          mma_commit_warp(s_ready);
+          ok = mbar_wait_warp(&v_full[sv], (n / C::NV) & 1, err, kQVFull);
+          if (ok && n > 0) ok = mbar_wait_warp(dq_done, (n - 1) & 1, err, kQDqDone);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D_V / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+            mma_ss_warp(tmem + C::COL_DP, desc_add(dDO0, off), desc_add(dVa, off), idS, kk > 0);
+          }
+          mma_commit_warp(dp_ready);
+          mma_commit_warp(&v_empty[sv]);
         }
-        mma_commit(s_ready);
-        ok = mbar_wait(&v_full[sv], (n / C::NV) & 1, err, kQVFull);
-        if (!ok) break;
-        tc_fence_after();
-        // dP = dO V^T
+      } else {
+        for (int n = 0; n < nj && ok; ++n) {
+          const int sk = n % C::NK;
+          const uint64_t dKmn = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, C::CHUNK, 1024);
+          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull) && mbar_wait_warp(ds_ready, n & 1, err, kQDS);
+          if (!ok) break;
+          tc_fence_after();
+          // dQ += dS K   (dS bf16 over the dP columns: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
 #pragma unroll
-        for (int kk = 0; kk < D_V / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::COL_DP, desc_add(dDO0, off), desc_add(dVa, off), idS,
-                 kk > 0);
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts_warp(tmem + C::COL_DQ, tmem + C::COL_DP + (kk / 4) * 64 + (kk % 4) * 8, desc_add(dKmn, kk * 2048),
+                   idDQ, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_warp(dq_done);
+          mma_commit_warp(&k_empty[sk]);  // S(n) (issuer A) completed before dS(n) existed
         }
-        mma_commit(dp_ready);
-        mma_commit(&v_empty[sv]);
-        ok = mbar_wait(ds_ready, n & 1, err, kQDS);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ += dS K   (dS bf16 in TMEM: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::COL_DQ, tmem + C::COL_S + (kk / 4) * 64 + (kk % 4) * 8,
-                 desc_add(dKmn, kk * 2048), idDQ, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&k_empty[sk]);
       }
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, err, kQDone);
+      mma_commit_warp(mma_done);
+      mbar_wait_warp(mma_done, 0, err, kQDone);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ dS warpgroups: thread = query row
     const int w = warp / 4;  // keys 64w .. 64w+63 of each kv tile
     const int r = (warp % 4) * 32 + lane;
@@ -724,13 +744,18 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const bool full = tile_fully_visible(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
       float pr[64];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_S + 64 * w + c0, rr);
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(lane_addr + C::COL_S + 64 * w, ra);
+        tmem_ld32(lane_addr + C::COL_S + 64 * w + 32, rb);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(s_free);  // S is in registers: the next S may be written
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c0 + c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -l2row));
+        for (int c = 0; c < 32; ++c) {
+          pr[c] = ex2(fmaf(__uint_as_float(ra[c]), sl2, -l2row));
+          pr[32 + c] = ex2(fmaf(__uint_as_float(rb[c]), sl2, -l2row));
+        }
       }
       if (!full) {
 #pragma unroll
@@ -752,7 +777,7 @@ __global__ void __launch_bounds__(320, 1)
           const float bq = pr[c0 + 2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - drow);
           pk[c] = pack_bf16x2(a, bq);
         }
-        tmem_st16(lane_addr + C::COL_S + 64 * w + c0 / 2, pk);
+        tmem_st16(lane_addr + C::COL_DP + 64 * w + c0 / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();

@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues for both query tiles in the order PV_0(j), S_0(j+1),
+    // One warp issues for both query tiles in the order PV_0(j), S_0(j+1),
     // PV_1(j), S_1(j+1): each tile's softmax overlaps the other tile's GEMMs.
-    if (lane == 0 && any) {
+    if (any) {  // the whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
@@ -171,57 +171,57 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D_QK / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
+          mma_ss_warp(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
         }
       };
       auto issue_PV = [&](int t, int stage, bool acc) {
         const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
+          mma_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(q_full, 0, err, kSiteQ);
-      if (ok) ok = mbar_wait(&k_full[0], 0, err, kSiteKFull);
+      bool ok = mbar_wait_warp(q_full, 0, err, kSiteQ);
+      if (ok) ok = mbar_wait_warp(&k_full[0], 0, err, kSiteKFull);
       if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (active[t] && jlo[t] == J0) {
             issue_S(t, 0);
-            mma_commit(&s_ready[t]);
+            mma_commit_warp(&s_ready[t]);
           }
-        mma_commit(&k_empty[0]);
+        mma_commit_warp(&k_empty[0]);
       }
       for (int j = J0; j <= J1 && ok; ++j) {
         const int n = j - J0;
         const bool need_k = j + 1 <= J1;
-        ok = mbar_wait(&v_full[n % NV], (n / NV) & 1, err, kSiteVFull);
-        if (ok && need_k) ok = mbar_wait(&k_full[(n + 1) % NK], ((n + 1) / NK) & 1, err, kSiteKFull);
+        ok = mbar_wait_warp(&v_full[n % NV], (n / NV) & 1, err, kSiteVFull);
+        if (ok && need_k) ok = mbar_wait_warp(&k_full[(n + 1) % NK], ((n + 1) / NK) & 1, err, kSiteKFull);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (ok && active[t] && j >= jlo[t] && j <= jhi[t]) {
-            ok = mbar_wait(&p_ready[t], (j - jlo[t]) & 1, err, kSiteP);
+            ok = mbar_wait_warp(&p_ready[t], (j - jlo[t]) & 1, err, kSiteP);
             if (ok) {
               tc_fence_after();
               issue_PV(t, n % NV, j > jlo[t]);
-              if (j == jhi[t]) mma_commit(&o_done[t]);
+              if (j == jhi[t]) mma_commit_warp(&o_done[t]);
             }
           }
           if (ok && active[t] && j + 1 >= jlo[t] && j + 1 <= jhi[t]) {
             issue_S(t, (n + 1) % NK);
-            mma_commit(&s_ready[t]);
+            mma_commit_warp(&s_ready[t]);
           }
         }
         if (!ok) break;
-        mma_commit(&v_empty[n % NV]);
-        if (need_k) mma_commit(&k_empty[(n + 1) % NK]);
+        mma_commit_warp(&v_empty[n % NV]);
+        if (need_k) mma_commit_warp(&k_empty[(n + 1) % NK]);
       }
       // Every MMA must be complete before TMEM is released.
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, err, kSiteDrain);
+      mma_commit_warp(mma_done);
+      mbar_wait_warp(mma_done, 0, err, kSiteDrain);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
