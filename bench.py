@@ -87,6 +87,27 @@ def kernel_flops(wl, cls, fused):
             "bwd_q": n * 2 * d}.get(cls, 0)
 
 
+def recorded_traffic(wl, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
+    that summary is for another workload or the kernel sources changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("workload") != wl["name"] or kernel not in d.get("kernels", {}):
+        return None
+    h = hashlib.sha256()
+    for s in d["sources"]:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d["sources_sha256"]:
+        return None
+    k = d["kernels"][kernel]
+    return k["dram_bytes_read"] + k["dram_bytes_write"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -378,7 +399,7 @@ def ours_arm(args, wl, world, rank, local):
             "fwd_tflop": flops(wl, "fwd") / 1e12, "bwd_tflop": flops(wl, "bwd") / 1e12,
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": f"bf16_tflops (burst) from {peak_src}",
-                         "traffic": None},
+                         "traffic": recorded_traffic(wl, dom), "traffic_unit": "bytes per launch (ncu DRAM read+write)"},
             "kernels": kernels,
             "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
