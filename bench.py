@@ -42,6 +42,8 @@ def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc):
 
 
 WORKLOADS = {
+    "tiny_gqa_swa": _w("tiny_gqa_swa", 1, 128, 4, 2, 64, 64, True, 32, 0, 0.125, 0,
+                       "tiny case: B=1, S=128, H_q=4, H_kv=2, d=64, causal, left window 32, vanilla, scale 1/8"),
     "gqa_swa_b4_s2048": _w("gqa_swa_b4_s2048", 4, 2048, 32, 8, 128, 128, True, 1024, 0, None, 1,
                            "BSHD GQA + SWA training shape: B=4, S=2048, H_q=32, H_kv=8, d_qk=d_v=128, causal, "
                            "left window 1024, vanilla softmax"),

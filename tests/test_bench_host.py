@@ -1,0 +1,72 @@
+"""Host-side checks of bench.py (no GPU): the unmasked-pair count behind every TFLOP/s
+figure, the reference arm (the fp64 oracle) end to end, and the max-over-ranks timing
+reduction of the multi-process path on two gloo ranks."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 64, 130])
+@pytest.mark.parametrize("causal,window", [(True, -1), (True, 0), (True, 5), (True, 129), (False, -1)])
+def test_n_pairs_matches_brute_force(S, causal, window):
+    brute = sum(1 for i in range(S) for j in range(S)
+                if (not causal or j <= i) and (window < 0 or j >= i - window))
+    assert bench.n_pairs(S, causal, window) == brute
+
+
+def test_flops_counts():
+    wl = bench.WORKLOADS["sweep_s8192_hkv8"]
+    n = 4 * 32 * 8192 * 8193 // 2
+    assert bench.flops(wl, "fwd") == n * 2 * 256
+    assert bench.flops(wl, "bwd") == n * 2 * (3 * 128 + 2 * 128)
+    assert abs(bench.flops(wl) / 1e12 - 7.698) < 1e-3   # the 7.698 TFLOP of the S=8192 GQA point
+
+
+def test_traffic_only_for_its_workload():
+    assert bench.recorded_traffic(bench.WORKLOADS["mla_b2_s4096"], "bwd_kv") is None
+
+
+def test_reference_arm_prints_one_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny_gqa_swa", "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["dtype"] == "f64"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench._max_over_ranks(float(10 + rank), world, torch.device("cpu"))
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 2000
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 11.0, 1: 11.0}
