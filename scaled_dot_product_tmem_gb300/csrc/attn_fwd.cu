@@ -246,14 +246,16 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait_warp(&s_ready[t], it & 1, err, kSiteS);
         if (!ok) break;
         tc_fence_after();
+        // the whole 128-key row in one batch of TMEM loads, one wait
         float s[128];
+        {
+          uint32_t rr[128];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(lane_addr + colS + c0, rr);
+          for (int c0 = 0; c0 < 128; c0 += 32)
+            tmem_ld32(lane_addr + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(&rr[c0]));
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(rr[c]);
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
         }
         const int k0 = j * C::BN;
         if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
@@ -261,9 +263,16 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (!key_visible(mask, i, k0 + c)) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row max: eight independent chains of three-input max, then a small tree
+        float mp[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < 8; ++k) {
+          float a = s[k];
+#pragma unroll
+          for (int c = k + 8; c + 8 < 128; c += 16) a = fmax3(a, s[c], s[c + 8]);
+          mp[k] = fmaxf(a, s[k + 120]);
+        }
+        const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
         const float m_tile = mx * sl2;
         // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
         // when any row's max grew by more than 2^8, every row of the warp moves to
@@ -286,20 +295,31 @@ __global__ void __launch_bounds__(320, 1)
           m_run = m_new;
         }
         const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-        float lsum = 0.f;
+        // p = 2^(s * scale * log2e - m), paired: one f32x2 FMA per two keys; the row sum
+        // is kept in four paired partial sums so no long add chain forms
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float a = ex2(fmaf(s[c0 + 2 * c], sl2, -m_sub));
-            const float bq = ex2(fmaf(s[c0 + 2 * c + 1], sl2, -m_sub));
-            lsum += a + bq;
+            float xa, xb;
+            f2_unpack(f2_fma(f2_pack(s[c0 + 2 * c], s[c0 + 2 * c + 1]), sl2x2, negm2), xa, xb);
+            const float a = ex2(xa), bq = ex2(xb);
+            ls2[c % 4] = f2_add(ls2[c % 4], f2_pack(a, bq));
             pk[c] = pack_bf16x2(a, bq);
           }
           tmem_st16(lane_addr + colS + c0 / 2, pk);
         }
-        l += lsum;
+        {
+          float s0, s1, s2, s3, s4, s5, s6, s7;
+          f2_unpack(ls2[0], s0, s1);
+          f2_unpack(ls2[1], s2, s3);
+          f2_unpack(ls2[2], s4, s5);
+          f2_unpack(ls2[3], s6, s7);
+          l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_ready[t]);
