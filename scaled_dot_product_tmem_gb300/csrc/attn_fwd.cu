@@ -246,13 +246,15 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait_warp(&s_ready[t], it & 1, err, kSiteS);
         if (!ok) break;
         tc_fence_after();
-        // the whole 128-key row in one batch of TMEM loads, one wait
-        float s[128];
+        // The whole 128-key row in one batch of TMEM loads, one wait; each load also
+        // yields the max of its 32 columns.  Where a 32-key chunk is only partly visible
+        // to this row, the chunk's max is retaken over its visible keys after masking.
+        float s[128], cmax[4];
         {
           uint32_t rr[128];
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 32)
-            tmem_ld32(lane_addr + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(&rr[c0]));
+            tmem_ld32_max(lane_addr + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(&rr[c0]), cmax[c0 / 32]);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
@@ -260,19 +262,21 @@ __global__ void __launch_bounds__(320, 1)
         const int k0 = j * C::BN;
         if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (!key_visible(mask, i, k0 + c)) s[c] = -INFINITY;
-        }
-        // row max: eight independent chains of three-input max, then a small tree
-        float mp[8];
+          for (int q = 0; q < 4; ++q) {
+            const bool first = key_visible(mask, i, k0 + 32 * q), last = key_visible(mask, i, k0 + 32 * q + 31);
+            // visible keys of a row form one interval, so a chunk whose two ends are
+            // visible is fully visible
+            if (first && last) continue;
+            float m = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float a = s[k];
-#pragma unroll
-          for (int c = k + 8; c + 8 < 128; c += 16) a = fmax3(a, s[c], s[c + 8]);
-          mp[k] = fmaxf(a, s[k + 120]);
+            for (int c = 0; c < 32; ++c) {
+              if (!key_visible(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
+              m = fmaxf(m, s[32 * q + c]);
+            }
+            cmax[q] = m;
+          }
         }
-        const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+        const float mx = fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
         const float m_tile = mx * sl2;
         // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
         // when any row's max grew by more than 2^8, every row of the warp moves to
