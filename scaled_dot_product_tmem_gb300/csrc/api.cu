@@ -75,14 +75,14 @@ float resolve_scale(float scale, int d_qk) {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t lse2, dsum, dq_acc, total;
+  size_t nlse2, dsum, dq_acc, total;
 };
 
 WsLayout ws_layout(int B, int S_q, int H_q, int d_qk, bool need_dq_acc) {
   const size_t s_pad = (static_cast<size_t>(S_q) + 127) / 128 * 128;
   const size_t rows = static_cast<size_t>(B) * H_q * s_pad;
   WsLayout w;
-  w.lse2 = 0;
+  w.nlse2 = 0;
   w.dsum = round256(rows * sizeof(float));
   w.dq_acc = w.dsum + round256(rows * sizeof(float));
   w.total = w.dq_acc + (need_dq_acc ? round256(static_cast<size_t>(B) * S_q * H_q * d_qk * sizeof(float)) : 0);
@@ -255,7 +255,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.o = static_cast<const __nv_bfloat16*>(o);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
-  p.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  p.nlse2 = reinterpret_cast<float*>(ws + w.nlse2);
   p.Dsum = reinterpret_cast<float*>(ws + w.dsum);
   p.d_offset = d_offset;
   p.dq = static_cast<__nv_bfloat16*>(dq);
@@ -264,7 +264,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
   p.err = err;
 
-  const int n_pre = 1 + (p.S_pad > S_q ? 1 : 0) + (softmax_type == ATTN_SOFTMAX_LEARNABLE ? 1 : 0);
+  const int n_pre = 1 + (softmax_type == ATTN_SOFTMAX_LEARNABLE ? 1 : 0);
   if (timed(ATTN_KERNEL_BWD_PREPROCESS, n_pre, s, [&] { return sdpa::launch_bwd_preprocess(d_v, p, s); }) != 0) {
     set_error("backward preprocess launch", cudaGetLastError());
     return ATTN_ERR_CUDA;

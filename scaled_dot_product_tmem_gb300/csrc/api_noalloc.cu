@@ -138,7 +138,7 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   p.o = static_cast<const __nv_bfloat16*>(o);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
-  p.lse2 = reinterpret_cast<float*>(scratch);
+  p.nlse2 = reinterpret_cast<float*>(scratch);
   p.Dsum = reinterpret_cast<float*>(scratch + round256(rows * sizeof(float)));
   p.d_offset = d_offset;
   p.dq = static_cast<__nv_bfloat16*>(dq);

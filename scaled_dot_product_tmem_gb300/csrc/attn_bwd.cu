@@ -32,52 +32,49 @@
 namespace sdpa {
 
 // =============================================================================
-// Preprocess: D = rowsum(dO * O) (fp32) and lse2 = LSE * log2(e).
-// Rows are padded to S_pad: D = 0 and lse2 = +inf there, so padded query rows get
-// P = exp2(s - inf) = 0 in the main kernels.
+// Preprocess: D = rowsum(dO * O) (fp32) and nlse2 = -LSE * log2(e), one block per
+// (64 query rows, head, batch) so the per-row values are read and written as
+// contiguous runs.  Rows are padded to S_pad: D = 0 and nlse2 = -inf there, so
+// padded query rows get P = exp2(s + nlse2) = 0 in the main kernels.
 // =============================================================================
 template <int D_V>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
-  constexpr int TPR = D_V / 8;  // threads per row, 8 bf16 (16 bytes) each
-  const long long rows = (long long)p.B * p.S_q * p.H_q;
-  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / TPR;
+  constexpr int TPR = D_V / 8;     // threads per row, 8 bf16 (16 bytes) each
+  constexpr int RPP = 256 / TPR;   // rows per pass of the block
+  constexpr int TILE = 64;
+  __shared__ float dsum[TILE];
+  const int i0 = blockIdx.x * TILE, h = blockIdx.y, b = blockIdx.z;
   const int sub = threadIdx.x % TPR;
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p.o + row * D_V + sub * 8);
-    const uint4 g = *reinterpret_cast<const uint4*>(p.dout + row * D_V + sub * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 fa = __bfloat1622float2(a2[e]);
-      const float2 fg = __bfloat1622float2(g2[e]);
-      acc = fmaf(fa.x, fg.x, acc);
-      acc = fmaf(fa.y, fg.y, acc);
+  for (int r = threadIdx.x / TPR; r < TILE; r += RPP) {
+    const int i = i0 + r;
+    float acc = 0.f;
+    if (i < p.S_q) {
+      const size_t off = (((size_t)b * p.S_q + i) * p.H_q + h) * D_V + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
+      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a2[e]);
+        const float2 fg = __bfloat1622float2(g2[e]);
+        acc = fmaf(fa.x, fg.x, acc);
+        acc = fmaf(fa.y, fg.y, acc);
+      }
     }
-  }
+    // the TPR lanes of a row are consecutive lanes of one warp
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && sub == 0) {
-    // row enumerates (b, i, h) in memory order
-    const int h = (int)(row % p.H_q);
-    const long long bi = row / p.H_q;
-    const int i = (int)(bi % p.S_q);
-    const int b = (int)(bi / p.S_q);
-    const size_t dst = ((size_t)b * p.H_q + h) * p.S_pad + i;
-    p.Dsum[dst] = acc;
-    p.lse2[dst] = p.lse[((size_t)b * p.H_q + h) * p.S_q + i] * kLog2e;
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0) dsum[r] = acc;
   }
-}
-
-__global__ void __launch_bounds__(256) bwd_pad_kernel(const BwdParams p) {
-  const int pad = p.S_pad - p.S_q;
-  const long long n = (long long)p.B * p.H_q * pad;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
-    const long long bh = t / pad;
-    const int i = p.S_q + (int)(t % pad);
-    p.Dsum[bh * p.S_pad + i] = 0.f;
-    p.lse2[bh * p.S_pad + i] = INFINITY;
+  __syncthreads();
+  if (threadIdx.x < TILE) {
+    const int i = i0 + threadIdx.x;
+    const size_t bh = (size_t)b * p.H_q + h;
+    const bool real = i < p.S_q;
+    p.Dsum[bh * p.S_pad + i] = real ? dsum[threadIdx.x] : 0.f;
+    p.nlse2[bh * p.S_pad + i] = real ? -p.lse[bh * p.S_q + i] * kLog2e : -INFINITY;
   }
 }
 
@@ -89,9 +86,9 @@ __global__ void __launch_bounds__(256) bwd_doffset_kernel(const BwdParams p) {
   const float c2 = p.offset[h] * kLog2e;
   float acc = 0.f;
   for (int b = 0; b < p.B; ++b) {
-    const float* l2 = p.lse2 + ((size_t)b * p.H_q + h) * p.S_pad;
+    const float* nl2 = p.nlse2 + ((size_t)b * p.H_q + h) * p.S_pad;
     const float* dd = p.Dsum + ((size_t)b * p.H_q + h) * p.S_pad;
-    for (int i = threadIdx.x; i < p.S_q; i += blockDim.x) acc = fmaf(ex2(c2 - l2[i]), dd[i], acc);
+    for (int i = threadIdx.x; i < p.S_q; i += blockDim.x) acc = fmaf(ex2(c2 + nl2[i]), dd[i], acc);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -106,19 +103,15 @@ __global__ void __launch_bounds__(256) bwd_doffset_kernel(const BwdParams p) {
 }
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.S_q * p.H_q;
-  if (rows > 0) {
-    const int tpr = d_v / 8;
-    const long long threads = rows * tpr;
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if ((long long)p.B * p.S_q * p.H_q > 0) {
+    const dim3 grid(p.S_pad / 64, p.H_q, p.B);
     if (d_v == 64)
-      bwd_preprocess_kernel<64><<<blocks, 256, 0, stream>>>(p);
+      bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(p);
     else if (d_v == 128)
-      bwd_preprocess_kernel<128><<<blocks, 256, 0, stream>>>(p);
+      bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(p);
     else
       return -2;
   }
-  if (p.S_pad > p.S_q) bwd_pad_kernel<<<296, 256, 0, stream>>>(p);
   if (p.softmax_type == 2)
     bwd_doffset_kernel<<<p.H_q, 256, 0, stream>>>(p);
   else if (p.d_offset)
@@ -146,7 +139,7 @@ struct KvCfg {
   static constexpr int Q_STAGE = QCH * QCHUNK;
   static constexpr int OFF_DO = OFF_Q + NQ * Q_STAGE;
   static constexpr int DO_STAGE = VCH * QCHUNK;
-  static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // lse2[64] + D[64] per stage
+  static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // nlse2[64] + D[64] per stage
   static constexpr int L_STAGE = 2 * BQ * 4;
   static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
@@ -256,7 +249,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         for (int c = 0; c < C::VCH; ++c)
           tma_load_4d(smem + C::OFF_DO + st * C::DO_STAGE + c * C::QCHUNK, &tmDO, &q_full[st], c * 64, h, q0, b);
         const size_t row = ((size_t)b * p.H_q + h) * p.S_pad + q0;
-        bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.lse2 + row, C::BQ * 4, &q_full[st]);
+        bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.nlse2 + row, C::BQ * 4, &q_full[st]);
         bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
       }
       mbar_wait(kv_full, 0, err, kKvDrain);
@@ -381,12 +374,19 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       {
         uint32_t rr[32];
         tmem_ld32(lane_addr + colS + 32 * w, rr);
-        float lv[32];
+        float lv[32];  // -LSE * log2(e) of the 32 queries
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
         tmem_ld_wait();
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, -lv[c]));
+        for (int c = 0; c < 32; c += 2) {
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2, f2_pack(lv[c], lv[c + 1])),
+                    xa, xb);
+          pr[c] = ex2(xa);
+          pr[c + 1] = ex2(xb);
+        }
       }
       if (!tile_fully_visible(mask, q0, C::BQ, n0, C::BN)) {
 #pragma unroll
@@ -415,8 +415,12 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a = pr[2 * c] * (__uint_as_float(rr[2 * c]) - dv4[2 * c]);
-          const float bq = pr[2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - dv4[2 * c + 1]);
+          // dS = P (dP - D), paired
+          float a, bq;
+          f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
+                           f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
+                                  f2_pack(dv4[2 * c], dv4[2 * c + 1]))),
+                    a, bq);
           dsk[c] = pack_bf16x2(a, bq);
         }
       }
@@ -730,10 +734,10 @@ __global__ void __launch_bounds__(352, 1)
     const int i = m0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2;
-    float l2row = INFINITY, drow = 0.f;
+    float nl2row = -INFINITY, drow = 0.f;
     if (i < p.S_q) {
       const size_t ri = ((size_t)b * p.H_q + h) * p.S_pad + i;
-      l2row = p.lse2[ri];
+      nl2row = p.nlse2[ri];
       drow = p.Dsum[ri];
     }
     bool ok = true;
@@ -753,8 +757,8 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive(s_free);  // S is in registers: the next S may be written
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          pr[c] = ex2(fmaf(__uint_as_float(ra[c]), sl2, -l2row));
-          pr[32 + c] = ex2(fmaf(__uint_as_float(rb[c]), sl2, -l2row));
+          pr[c] = ex2(fmaf(__uint_as_float(ra[c]), sl2, nl2row));
+          pr[32 + c] = ex2(fmaf(__uint_as_float(rb[c]), sl2, nl2row));
         }
       }
       if (!full) {

@@ -27,12 +27,12 @@ struct BwdParams {
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   int causal, window, softmax_type;
-  int S_pad;                  // S_q rounded up to 128: row length of lse2 / Dsum
+  int S_pad;                  // S_q rounded up to 128: row length of nlse2 / Dsum
   const float* offset;        // [H_q]
   const __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
   const __nv_bfloat16* dout;  // [B, S_q, H_q, d_v]
   const float* lse;           // [B, H_q, S_q] (natural log)
-  float* lse2;                // [B, H_q, S_pad] workspace: LSE * log2(e), +inf padding
+  float* nlse2;               // [B, H_q, S_pad] workspace: -LSE * log2(e), -inf padding
   float* Dsum;                // [B, H_q, S_pad] workspace: rowsum(dO * O), 0 padding
   float* d_offset;            // [H_q] (learnable) or null
   __nv_bfloat16* dq;          // [B, S_q, H_q, d_qk]
