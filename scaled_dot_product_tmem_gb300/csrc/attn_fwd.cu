@@ -10,8 +10,10 @@
 // window, MLA head dims, scale_factor, sink softmax); "[JAX] Add support for sink
 // attention in JAX #2225", Greptile sequence diagrams (the three denominators).
 //
-// One CTA owns two 128-row query tiles of one (b, h) and walks the kv tiles that
-// either of them can see.  Warp roles (320 threads):
+// A work tile is two 128-row query tiles of one (b, h); its CTA walks the kv tiles
+// that either of them can see.  CTAs are persistent (one per SM), each taking every
+// gridDim-th work tile, heaviest causal query blocks first, so one tile's output
+// epilogue overlaps the next tile's loads and first GEMM.  Warp roles (320 threads):
 //   warps 0-3 / 4-7  softmax warpgroup of query tile 0 / 1: thread r owns row r
 //                    (TMEM lane r); online softmax in fp32 with the sink folded
 //                    into the running max/denominator; writes bf16 P into TMEM
@@ -43,14 +45,48 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
   static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
-  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready[2], p_ready[2], o_done[2], mma_done
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
+  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready[2], p_ready[2], o_done[2], mma_done,
+  // q_empty
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 8;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int THREADS = 320;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SMEM > 116 * 1024, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
 };
+
+// One work tile: two 128-row query tiles of one (b, h).  For each query tile: does it
+// exist (rows < S_q), does it see any key, and which kv tiles [jlo, jhi] it sees;
+// [J0, J1] is the union.  Causal work is ordered heaviest query block first.
+struct FwdTile {
+  int h, b, hk, m0, J0, J1;
+  int jlo[2], jhi[2];
+  bool exists[2], active[2], any;
+};
+
+template <int BM, int BN>
+__device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, const MaskSpec& mask, int nqb, int wi) {
+  FwdTile T;
+  const int hb = wi % (p.H_q * p.B);
+  const int q = wi / (p.H_q * p.B);
+  const int qb = p.causal ? nqb - 1 - q : q;
+  T.h = hb % p.H_q;
+  T.b = hb / p.H_q;
+  T.hk = T.h / p.G;
+  T.m0 = qb * 2 * BM;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = T.m0 + t * BM;
+    T.exists[t] = r0 < p.S_q;
+    const int r1 = min(r0 + BM - 1, p.S_q - 1);
+    T.active[t] = T.exists[t] && kv_tile_range(mask, r0, r1, BN, &T.jlo[t], &T.jhi[t]);
+    if (!T.active[t]) { T.jlo[t] = 1; T.jhi[t] = 0; }
+  }
+  T.any = T.active[0] || T.active[1];
+  T.J0 = T.active[0] ? (T.active[1] ? min(T.jlo[0], T.jlo[1]) : T.jlo[0]) : T.jlo[1];
+  T.J1 = T.active[1] ? (T.active[0] ? max(T.jhi[0], T.jhi[1]) : T.jhi[1]) : T.jhi[0];
+  return T;
+}
 
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
 
@@ -71,31 +107,17 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_ready = s_ready + 2;
   uint64_t* o_done = p_ready + 2;
   uint64_t* mma_done = o_done + 2;
+  uint64_t* q_empty = mma_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qb = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
-  const int m0 = qb * 2 * C::BM;
   const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
-
-  // Per query tile: does it exist (rows < S_q) and which kv tiles does it see?
-  bool exists[2], active[2];
-  int jlo[2], jhi[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int r0 = m0 + t * C::BM;
-    exists[t] = r0 < p.S_q;
-    const int r1 = min(r0 + C::BM - 1, p.S_q - 1);
-    active[t] = exists[t] && kv_tile_range(mask, r0, r1, C::BN, &jlo[t], &jhi[t]);
-    if (!active[t]) { jlo[t] = 1; jhi[t] = 0; }
-  }
-  const bool any = active[0] || active[1];
-  const int J0 = active[0] ? (active[1] ? min(jlo[0], jlo[1]) : jlo[0]) : jlo[1];
-  const int J1 = active[1] ? (active[0] ? max(jhi[0], jhi[1]) : jhi[1]) : jhi[0];
+  const int nqb = (p.S_q + 2 * C::BM - 1) / (2 * C::BM);
+  const int n_work = nqb * p.H_q * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     for (int t = 0; t < 2; ++t) {
@@ -116,101 +138,122 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   int* err = p.err;
 
+  // The CTA is persistent: it takes work tiles wi = blockIdx.x, blockIdx.x + gridDim.x,
+  // ...; every role walks the same sequence and counts barrier phases across tiles.
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && any) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t qbytes = (active[0] ? C::Q_TILE : 0) + (active[1] ? C::Q_TILE : 0);
-      mbar_arrive_expect_tx(q_full, qbytes);
-      for (int t = 0; t < 2; ++t)
-        if (active[t])
-          for (int c = 0; c < C::QCH; ++c)
-            tma_load_4d(smem + C::OFF_Q + t * C::Q_TILE + c * C::CHUNK, &tmQ, q_full, c * 64, h, m0 + t * C::BM, b);
+      int n = 0, nw = 0;  // kv stages loaded, Q tiles loaded
       bool ok = true;
-      for (int j = J0; j <= J1 && ok; ++j) {
-        const int n = j - J0;
-        const int sk = n % NK, sv = n % NV;
-        ok = mbar_wait(&k_empty[sk], ((n / NK) & 1) ^ 1, err, kSiteKEmpty);
+      for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
+        const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+        if (!T.any) continue;
+        // Q of the previous tile must have been read by that tile's last S MMAs
+        if (nw > 0) ok = mbar_wait(q_empty, (nw - 1) & 1, err, kSiteQ);
         if (!ok) break;
-        mbar_arrive_expect_tx(&k_full[sk], C::K_STAGE);
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(smem + C::OFF_K + sk * C::K_STAGE + c * C::CHUNK, &tmK, &k_full[sk], c * 64, hk, j * C::BN, b);
-        ok = mbar_wait(&v_empty[sv], ((n / NV) & 1) ^ 1, err, kSiteVEmpty);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&v_full[sv], C::V_STAGE);
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE + c * C::CHUNK, &tmV, &v_full[sv], c * 64, hk, j * C::BN, b);
+        const uint32_t qbytes = (T.active[0] ? C::Q_TILE : 0) + (T.active[1] ? C::Q_TILE : 0);
+        mbar_arrive_expect_tx(q_full, qbytes);
+        for (int t = 0; t < 2; ++t)
+          if (T.active[t])
+            for (int c = 0; c < C::QCH; ++c)
+              tma_load_4d(smem + C::OFF_Q + t * C::Q_TILE + c * C::CHUNK, &tmQ, q_full, c * 64, T.h,
+                          T.m0 + t * C::BM, T.b);
+        ++nw;
+        for (int j = T.J0; j <= T.J1 && ok; ++j, ++n) {
+          const int sk = n % NK, sv = n % NV;
+          ok = mbar_wait(&k_empty[sk], ((n / NK) & 1) ^ 1, err, kSiteKEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&k_full[sk], C::K_STAGE);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(smem + C::OFF_K + sk * C::K_STAGE + c * C::CHUNK, &tmK, &k_full[sk], c * 64, T.hk,
+                        j * C::BN, T.b);
+          ok = mbar_wait(&v_empty[sv], ((n / NV) & 1) ^ 1, err, kSiteVEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&v_full[sv], C::V_STAGE);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE + c * C::CHUNK, &tmV, &v_full[sv], c * 64, T.hk,
+                        j * C::BN, T.b);
+        }
       }
       // Drain: every load issued must have landed before the CTA can exit.
-      const int nj = J1 - J0 + 1;
-      mbar_wait(q_full, 0, err, kSiteDrain);
-      for (int s = 0; s < NK && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / NK) * NK;
+      if (nw > 0) mbar_wait(q_full, (nw - 1) & 1, err, kSiteDrain);
+      for (int s = 0; s < NK && s < n; ++s) {
+        const int last = s + ((n - 1 - s) / NK) * NK;
         mbar_wait(&k_full[s], (last / NK) & 1, err, kSiteDrain);
       }
-      for (int s = 0; s < NV && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / NV) * NV;
+      for (int s = 0; s < NV && s < n; ++s) {
+        const int last = s + ((n - 1 - s) / NV) * NV;
         mbar_wait(&v_full[s], (last / NV) & 1, err, kSiteDrain);
       }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // One warp issues for both query tiles in the order PV_0(j), S_0(j+1),
-    // PV_1(j), S_1(j+1): each tile's softmax overlaps the other tile's GEMMs.
-    if (any) {  // the whole warp runs the loop; elect.sync picks the issuing lane
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      const uint32_t sK = smem_u32(smem + C::OFF_K);
-      const uint32_t sV = smem_u32(smem + C::OFF_V);
-      auto issue_S = [&](int t, int stage) {
-        const uint64_t dq = smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024);
-        const uint64_t dk = smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024);
+    // PV_1(j), S_1(j+1): each tile's softmax overlaps the other tile's GEMMs.  The
+    // first S of the next work tile follows the last PV of this one, so it runs
+    // while the softmax warps write this tile's output.
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+    const uint32_t sK = smem_u32(smem + C::OFF_K);
+    const uint32_t sV = smem_u32(smem + C::OFF_V);
+    auto issue_S = [&](int t, int stage) {
+      const uint64_t dq = smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D_QK / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss_warp(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
-        }
-      };
-      auto issue_PV = [&](int t, int stage, bool acc) {
-        const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
-                 (acc || kk > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait_warp(q_full, 0, err, kSiteQ);
-      if (ok) ok = mbar_wait_warp(&k_full[0], 0, err, kSiteKFull);
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (active[t] && jlo[t] == J0) {
-            issue_S(t, 0);
-            mma_commit_warp(&s_ready[t]);
-          }
-        mma_commit_warp(&k_empty[0]);
+      for (int kk = 0; kk < D_QK / 16; ++kk) {
+        const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+        mma_ss_warp(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
       }
-      for (int j = J0; j <= J1 && ok; ++j) {
-        const int n = j - J0;
-        const bool need_k = j + 1 <= J1;
+    };
+    auto issue_PV = [&](int t, int stage, bool acc) {
+      const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
+                    (acc || kk > 0) ? 1u : 0u);
+    };
+    int n = 0, nw = 0;      // kv stages consumed, Q tiles consumed
+    int pc[2] = {0, 0};     // p_ready phases consumed per query tile
+    bool ok = true, issued = false;
+    for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
+      const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+      if (!T.any) continue;
+      issued = true;
+      ok = mbar_wait_warp(q_full, nw & 1, err, kSiteQ);
+      ++nw;
+      if (ok) ok = mbar_wait_warp(&k_full[n % NK], (n / NK) & 1, err, kSiteKFull);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (T.active[t] && T.jlo[t] == T.J0) {
+          issue_S(t, n % NK);
+          mma_commit_warp(&s_ready[t]);
+        }
+      mma_commit_warp(&k_empty[n % NK]);
+      if (T.J0 == T.J1) mma_commit_warp(q_empty);  // every S of the tile is issued
+      for (int j = T.J0; j <= T.J1 && ok; ++j, ++n) {
+        const bool need_k = j + 1 <= T.J1;
         ok = mbar_wait_warp(&v_full[n % NV], (n / NV) & 1, err, kSiteVFull);
         if (ok && need_k) ok = mbar_wait_warp(&k_full[(n + 1) % NK], ((n + 1) / NK) & 1, err, kSiteKFull);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (ok && active[t] && j >= jlo[t] && j <= jhi[t]) {
-            ok = mbar_wait_warp(&p_ready[t], (j - jlo[t]) & 1, err, kSiteP);
+          if (ok && T.active[t] && j >= T.jlo[t] && j <= T.jhi[t]) {
+            ok = mbar_wait_warp(&p_ready[t], pc[t] & 1, err, kSiteP);
+            ++pc[t];
             if (ok) {
               tc_fence_after();
-              issue_PV(t, n % NV, j > jlo[t]);
-              if (j == jhi[t]) mma_commit_warp(&o_done[t]);
+              issue_PV(t, n % NV, j > T.jlo[t]);
+              if (j == T.jhi[t]) mma_commit_warp(&o_done[t]);
             }
           }
-          if (ok && active[t] && j + 1 >= jlo[t] && j + 1 <= jhi[t]) {
+          if (ok && T.active[t] && j + 1 >= T.jlo[t] && j + 1 <= T.jhi[t]) {
             issue_S(t, (n + 1) % NK);
             mma_commit_warp(&s_ready[t]);
           }
@@ -218,122 +261,127 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         mma_commit_warp(&v_empty[n % NV]);
         if (need_k) mma_commit_warp(&k_empty[(n + 1) % NK]);
+        if (j + 1 == T.J1) mma_commit_warp(q_empty);  // the tile's last S MMAs were just issued
       }
-      // Every MMA must be complete before TMEM is released.
+    }
+    // Every MMA must be complete before TMEM is released.
+    if (issued) {
       mma_commit_warp(mma_done);
       mbar_wait_warp(mma_done, 0, err, kSiteDrain);
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------------ softmax + epilogue
     const int t = warp / 4;
-    const bool my_active = t ? active[1] : active[0];
-    const bool my_exists = t ? exists[1] : exists[0];
-    const int my_jlo = t ? jlo[1] : jlo[0];
-    const int my_jhi = t ? jhi[1] : jhi[0];
     const int r = (warp % 4) * 32 + lane;
-    const int i = m0 + t * C::BM + r;  // query row
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const uint32_t colS = t * 256, colO = t * 256 + 128;
     const float sl2 = p.scale_log2;
-    // running max (in scaled log2 units) and denominator; the sink starts them
-    float m_run = -INFINITY, l = 0.f;
-    if (p.softmax_type == 1) { m_run = 0.f; l = 1.f; }
-    if (p.softmax_type == 2) { m_run = p.offset[h] * kLog2e; l = 1.f; }
+    int sc = 0, od = 0;  // s_ready / o_done phases consumed
     bool ok = true;
-    if (my_active) {
-      for (int j = my_jlo; j <= my_jhi; ++j) {
-        const int it = j - my_jlo;
-        ok = mbar_wait_warp(&s_ready[t], it & 1, err, kSiteS);
-        if (!ok) break;
-        tc_fence_after();
-        // The whole 128-key row in one batch of TMEM loads, one wait; each load also
-        // yields the max of its 32 columns.  Where a 32-key chunk is only partly visible
-        // to this row, the chunk's max is retaken over its visible keys after masking.
-        float s[128], cmax[4];
-        {
-          uint32_t rr[128];
+    for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
+      const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+      if (!T.exists[t]) continue;
+      const int m0 = T.m0, h = T.h, b = T.b;
+      const int i = m0 + t * C::BM + r;  // query row
+      // running max (in scaled log2 units) and denominator; the sink starts them
+      float m_run = -INFINITY, l = 0.f;
+      if (p.softmax_type == 1) { m_run = 0.f; l = 1.f; }
+      if (p.softmax_type == 2) { m_run = p.offset[h] * kLog2e; l = 1.f; }
+      if (T.active[t]) {
+        for (int j = T.jlo[t]; j <= T.jhi[t]; ++j) {
+          const int it = j - T.jlo[t];
+          ok = mbar_wait_warp(&s_ready[t], sc & 1, err, kSiteS);
+          ++sc;
+          if (!ok) break;
+          tc_fence_after();
+          // The whole 128-key row in one batch of TMEM loads, one wait; each load also
+          // yields the max of its 32 columns.  Where a 32-key chunk is only partly visible
+          // to this row, the chunk's max is retaken over its visible keys after masking.
+          float s[128], cmax[4];
+          {
+            uint32_t rr[128];
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32)
-            tmem_ld32_max(lane_addr + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(&rr[c0]), cmax[c0 / 32]);
-          tmem_ld_wait();
+            for (int c0 = 0; c0 < 128; c0 += 32)
+              tmem_ld32_max(lane_addr + colS + c0, *reinterpret_cast<uint32_t(*)[32]>(&rr[c0]), cmax[c0 / 32]);
+            tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
-        }
-        const int k0 = j * C::BN;
-        if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const bool first = key_visible(mask, i, k0 + 32 * q), last = key_visible(mask, i, k0 + 32 * q + 31);
-            // visible keys of a row form one interval, so a chunk whose two ends are
-            // visible is fully visible
-            if (first && last) continue;
-            float m = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (!key_visible(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
-              m = fmaxf(m, s[32 * q + c]);
-            }
-            cmax[q] = m;
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
           }
-        }
-        const float mx = fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
-        const float m_tile = mx * sl2;
-        // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
-        // when any row's max grew by more than 2^8, every row of the warp moves to
-        // its new max (alpha = 1 for rows whose max did not change).
-        if (__any_sync(0xffffffffu, m_tile > m_run + 8.f)) {
-          const float m_new = fmaxf(m_run, m_tile);
-          const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
-          l *= alpha;
-          if (it > 0) {
+          const int k0 = j * C::BN;
+          if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool first = key_visible(mask, i, k0 + 32 * q), last = key_visible(mask, i, k0 + 32 * q + 31);
+              // visible keys of a row form one interval, so a chunk whose two ends are
+              // visible is fully visible
+              if (first && last) continue;
+              float m = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                if (!key_visible(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
+                m = fmaxf(m, s[32 * q + c]);
+              }
+              cmax[q] = m;
+            }
+          }
+          const float mx = fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
+          const float m_tile = mx * sl2;
+          // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
+          // when any row's max grew by more than 2^8, every row of the warp moves to
+          // its new max (alpha = 1 for rows whose max did not change).
+          if (__any_sync(0xffffffffu, m_tile > m_run + 8.f)) {
+            const float m_new = fmaxf(m_run, m_tile);
+            const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+            l *= alpha;
+            if (it > 0) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D_V; c0 += 16) {
-              uint32_t rr[16];
-              tmem_ld16(lane_addr + colO + c0, rr);
-              tmem_ld_wait();
+              for (int c0 = 0; c0 < D_V; c0 += 16) {
+                uint32_t rr[16];
+                tmem_ld16(lane_addr + colO + c0, rr);
+                tmem_ld_wait();
 #pragma unroll
-              for (int c = 0; c < 16; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-              tmem_st16(lane_addr + colO + c0, rr);
+                for (int c = 0; c < 16; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+                tmem_st16(lane_addr + colO + c0, rr);
+              }
             }
+            m_run = m_new;
           }
-          m_run = m_new;
-        }
-        const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-        // p = 2^(s * scale * log2e - m), paired: one f32x2 FMA per two keys; the row sum
-        // is kept in four paired partial sums so no long add chain forms
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
-        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+          const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+          // p = 2^(s * scale * log2e - m), paired: one f32x2 FMA per two keys; the row sum
+          // is kept in four paired partial sums so no long add chain forms
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+          uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t pk[16];
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float xa, xb;
-            f2_unpack(f2_fma(f2_pack(s[c0 + 2 * c], s[c0 + 2 * c + 1]), sl2x2, negm2), xa, xb);
-            const float a = ex2(xa), bq = ex2(xb);
-            ls2[c % 4] = f2_add(ls2[c % 4], f2_pack(a, bq));
-            pk[c] = pack_bf16x2(a, bq);
+            for (int c = 0; c < 16; ++c) {
+              float xa, xb;
+              f2_unpack(f2_fma(f2_pack(s[c0 + 2 * c], s[c0 + 2 * c + 1]), sl2x2, negm2), xa, xb);
+              const float a = ex2(xa), bq = ex2(xb);
+              ls2[c % 4] = f2_add(ls2[c % 4], f2_pack(a, bq));
+              pk[c] = pack_bf16x2(a, bq);
+            }
+            tmem_st16(lane_addr + colS + c0 / 2, pk);
           }
-          tmem_st16(lane_addr + colS + c0 / 2, pk);
+          {
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            f2_unpack(ls2[0], s0, s1);
+            f2_unpack(ls2[1], s2, s3);
+            f2_unpack(ls2[2], s4, s5);
+            f2_unpack(ls2[3], s6, s7);
+            l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_ready[t]);
         }
-        {
-          float s0, s1, s2, s3, s4, s5, s6, s7;
-          f2_unpack(ls2[0], s0, s1);
-          f2_unpack(ls2[1], s2, s3);
-          f2_unpack(ls2[2], s4, s5);
-          f2_unpack(ls2[3], s6, s7);
-          l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_ready[t]);
       }
-    }
-    // ------------------------------------------------------------ epilogue
-    if (my_exists) {
+      // ------------------------------------------------------------ epilogue
       bool have_o = false;
-      if (my_active && ok) {  // warp-uniform
-        have_o = mbar_wait_warp(&o_done[t], 0, err, kSiteO);
+      if (T.active[t] && ok) {  // warp-uniform
+        have_o = mbar_wait_warp(&o_done[t], od & 1, err, kSiteO);
+        ++od;
         tc_fence_after();
       }
       const bool row_ok = i < p.S_q;
@@ -385,7 +433,16 @@ static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
     attr_set = true;
   }
-  dim3 grid((p.S_q + 2 * C::BM - 1) / (2 * C::BM), p.H_q, p.B);
+  // persistent: one CTA per SM (at most one work tile per CTA when there are fewer)
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+      return -1;
+  }
+  const long long n_work = (long long)((p.S_q + 2 * C::BM - 1) / (2 * C::BM)) * p.H_q * p.B;
+  const unsigned grid = (unsigned)(n_work < n_sm ? n_work : n_sm);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
