@@ -45,16 +45,25 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   __shared__ float dsum[TILE];
   const int i0 = blockIdx.x * TILE, h = blockIdx.y, b = blockIdx.z;
   const int sub = threadIdx.x % TPR;
+  constexpr int NR = TILE / RPP;  // rows per thread
+  uint4 a[NR], g[NR];
 #pragma unroll
-  for (int r = threadIdx.x / TPR; r < TILE; r += RPP) {
-    const int i = i0 + r;
-    float acc = 0.f;
+  for (int k = 0; k < NR; ++k) {  // every load of this thread first, then the math
+    const int i = i0 + threadIdx.x / TPR + k * RPP;
+    a[k] = g[k] = make_uint4(0u, 0u, 0u, 0u);
     if (i < p.S_q) {
       const size_t off = (((size_t)b * p.S_q + i) * p.H_q + h) * D_V + sub * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
-      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+      a[k] = __ldcs(reinterpret_cast<const uint4*>(p.o + off));
+      g[k] = __ldcs(reinterpret_cast<const uint4*>(p.dout + off));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    const int r = threadIdx.x / TPR + k * RPP;
+    float acc = 0.f;
+    {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[k]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fa = __bfloat1622float2(a2[e]);
@@ -855,19 +864,21 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
 // dQ = bf16(scale * accumulator)
 // =============================================================================
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
-                                                             uint2* __restrict__ dq, size_t n4, float scale) {
-  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = acc[t];
-    dq[t] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+                                                             uint4* __restrict__ dq, size_t n8, float scale) {
+  // one thread: 8 consecutive floats -> one 16-byte store
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < n8) {
+    const float4 a0 = __ldcs(acc + 2 * t), a1 = __ldcs(acc + 2 * t + 1);
+    dq[t] = make_uint4(pack_bf16x2(a0.x * scale, a0.y * scale), pack_bf16x2(a0.z * scale, a0.w * scale),
+                       pack_bf16x2(a1.x * scale, a1.y * scale), pack_bf16x2(a1.z * scale, a1.w * scale));
   }
 }
 
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream) {
-  const size_t n = (size_t)p.B * p.S_q * p.H_q * d_qk;
-  const size_t n4 = n / 4;  // d_qk is a multiple of 64
-  const unsigned blocks = (unsigned)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
-  bwd_dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.dq_acc),
-                                                    reinterpret_cast<uint2*>(p.dq), n4, p.scale);
+  const size_t n8 = (size_t)p.B * p.S_q * p.H_q * d_qk / 8;  // d_qk is a multiple of 64
+  if (n8 == 0) return 0;
+  bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(p.dq_acc),
+                                                                          reinterpret_cast<uint4*>(p.dq), n8, p.scale);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
