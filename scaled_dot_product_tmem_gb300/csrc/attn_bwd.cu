@@ -173,6 +173,8 @@ struct KvCfg {
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
 };
 
+constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's block order
+
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
               kKvDvDone, kKvDkDone };
 
@@ -200,10 +202,18 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_tiles = gridDim.x;
-  const int nt = (int)(n_tiles - 1 - blockIdx.x);  // later keys (less work when causal) last
-  const int hk = blockIdx.y, b = blockIdx.z;
-  const int n0 = (p.causal ? (int)blockIdx.x : nt) * C::BN;
+  // Block order: groups (b, kv head) in chunks of kKvChunk; within a chunk, kv tile
+  // by kv tile (tile 0, the most work when causal, first) and group by group.  Blocks
+  // start in index order, so the long blocks of every chunk start early while the
+  // chunk's queries stay few enough to be shared in L2.
+  const int n_kv = (p.S_kv + C::BN - 1) / C::BN;
+  const int n_gr = p.H_kv * p.B;
+  const int per_chunk = kKvChunk * n_kv;
+  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
+  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
+  const int g = chunk * kKvChunk + within % csize;
+  const int hk = g % p.H_kv, b = g / p.H_kv;
+  const int n0 = (within / csize) * C::BN;
   const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
   int ilo = 0, ihi = -1;
   const bool any_q = q_tile_range(mask, n0, min(n0 + C::BN - 1, p.S_kv - 1), C::BQ, &ilo, &ihi);
@@ -540,8 +550,9 @@ static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   using C = KvCfg<D_QK, D_V, FUSE>;
   auto kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  dim3 grid((p.S_kv + C::BN - 1) / C::BN, p.H_kv, p.B);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+  const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B;
+  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -616,8 +627,17 @@ __global__ void __launch_bounds__(352, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qt = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
+  // Block order as in the kv kernel: (b, head) groups in chunks of kKvChunk (heads of a
+  // chunk share K and V in L2), within a chunk query tile by query tile, the tile with
+  // the most kv tiles (the last one when causal) first.
+  const int n_qt = (p.S_q + C::BM - 1) / C::BM;
+  const int n_gr = p.H_q * p.B;
+  const int per_chunk = kKvChunk * n_qt;
+  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
+  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
+  const int g = chunk * kKvChunk + within % csize;
+  const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
+  const int h = g % p.H_q, b = g / p.H_q, hk = h / p.G;
   const int m0 = qt * C::BM;
   const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
   int jlo = 1, jhi = 0;
@@ -844,8 +864,9 @@ static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   using C = QCfg<D_QK, D_V>;
   auto kern = attn_bwd_q_kernel<D_QK, D_V>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  dim3 grid((p.S_q + C::BM - 1) / C::BM, p.H_q, p.B);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
+  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
