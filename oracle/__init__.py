@@ -129,3 +129,78 @@ def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}
+
+
+# ----------------------------------------------------------------------------- padded batches
+def _lens(seq_lens, B: int, S: int):
+    """Per-entry lengths clamped to [0, S]; None means every entry is full length."""
+    if seq_lens is None:
+        return [S] * B
+    lens = np.asarray(seq_lens).reshape(-1)
+    assert lens.shape == (B,), "one length per batch entry"
+    return [int(min(max(int(x), 0), S)) for x in lens]
+
+
+def _sink_logit(softmax_type, off, h):
+    if softmax_type == OFF_BY_ONE:
+        return 0.0
+    if softmax_type == LEARNABLE:
+        return float(off[h])
+    return -np.inf
+
+
+def attention_fwd_varlen(q, k, v, *, seq_lens_q=None, seq_lens_kv=None, causal=True, window=-1,
+                         softmax_type=VANILLA, offset=None, scale=None):
+    """Padded batch: entry b holds its Lq[b] queries and Lkv[b] keys at the front of
+    its rows.  Its result is attention_fwd on those rows alone; a padded query row
+    sees no key, so O = 0, LSE = the sink logit c (-inf for vanilla), p_sink = 1
+    with a sink (0 without) and rowsum = 0.  Lengths are clamped to [0, S].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, dqk = q.shape
+    _, Skv, Hkv, dv = v.shape
+    Lq, Lkv = _lens(seq_lens_q, B, Sq), _lens(seq_lens_kv, B, Skv)
+    off = _f64(offset).reshape(-1) if offset is not None else None
+    o = np.zeros((B, Sq, Hq, dv))
+    lse = np.empty((B, Hq, Sq))
+    psink = np.empty((B, Hq, Sq))
+    rowsum = np.zeros((B, Hq, Sq))
+    for h in range(Hq):  # padded rows first; valid rows are overwritten below
+        c = _sink_logit(softmax_type, off, h)
+        lse[:, h, :] = c
+        psink[:, h, :] = 0.0 if softmax_type == VANILLA else 1.0
+    for b in range(B):
+        if Lq[b] == 0 or Lkv[b] == 0:
+            continue  # every row of the entry sees no key
+        r = attention_fwd(q[b:b + 1, :Lq[b]], k[b:b + 1, :Lkv[b]], v[b:b + 1, :Lkv[b]], causal=causal,
+                          window=window, softmax_type=softmax_type, offset=offset, scale=scale)
+        o[b, :Lq[b]] = r["o"][0]
+        lse[b, :, :Lq[b]] = r["lse"][0]
+        psink[b, :, :Lq[b]] = r["psink"][0]
+        rowsum[b, :, :Lq[b]] = r["rowsum"][0]
+    return {"o": o, "lse": lse, "psink": psink, "rowsum": rowsum}
+
+
+def attention_bwd_varlen(q, k, v, dout, *, seq_lens_q=None, seq_lens_kv=None, causal=True, window=-1,
+                         softmax_type=VANILLA, offset=None, scale=None):
+    """Gradients for attention_fwd_varlen: padded query rows and padded keys get zero
+    gradients (dO of a padded row is ignored), and d_offset sums the valid rows of
+    every entry."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Sq, Hq, dqk = q.shape
+    _, Skv, Hkv, dv = v.shape
+    Lq, Lkv = _lens(seq_lens_q, B, Sq), _lens(seq_lens_kv, B, Skv)
+    dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    doff = np.zeros(Hq)
+    D = np.zeros((B, Hq, Sq))
+    for b in range(B):
+        if Lq[b] == 0 or Lkv[b] == 0:
+            continue  # O = 0 on every row of the entry: nothing flows back
+        r = attention_bwd(q[b:b + 1, :Lq[b]], k[b:b + 1, :Lkv[b]], v[b:b + 1, :Lkv[b]], dout[b:b + 1, :Lq[b]],
+                          causal=causal, window=window, softmax_type=softmax_type, offset=offset, scale=scale)
+        dq[b, :Lq[b]] = r["dq"][0]
+        dk[b, :Lkv[b]] = r["dk"][0]
+        dvv[b, :Lkv[b]] = r["dv"][0]
+        D[b, :, :Lq[b]] = r["D"][0]
+        doff += r["d_offset"]
+    return {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}

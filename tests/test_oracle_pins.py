@@ -224,7 +224,7 @@ def test_causal_last_row_matches_full():
 # (learnable).  Gradients, d_offset included, come from torch autograd.
 # ---------------------------------------------------------------------------
 
-def _torch_reference(x, causal, window, st, scale):
+def _torch_reference(x, causal, window, st, scale, lens_q=None, lens_kv=None):
     q = torch.tensor(x["q"]).permute(0, 2, 1, 3).requires_grad_(True)   # B,Hq,Sq,d
     k = torch.tensor(x["k"]).permute(0, 2, 1, 3).requires_grad_(True)
     v = torch.tensor(x["v"]).permute(0, 2, 1, 3).requires_grad_(True)
@@ -240,8 +240,16 @@ def _torch_reference(x, causal, window, st, scale):
         allowed &= j <= i
     if window >= 0:
         allowed &= j >= i - window
-    mask = torch.zeros(Sq, Skv, dtype=torch.float64).masked_fill(~allowed, float("-inf"))
-    mask = mask.expand(B, Hq, Sq, Skv)
+    allowed = allowed.expand(B, Sq, Skv).clone()
+    if lens_q is not None:
+        # padded batch: keys past Lkv are masked; a padded query row keeps key 0 only
+        # (its output is not compared and its dO is zero, so it adds no gradient)
+        for b in range(B):
+            allowed[b, :, lens_kv[b]:] = False
+            allowed[b, lens_q[b]:, :] = False
+            allowed[b, lens_q[b]:, 0] = True
+    mask = torch.zeros(B, Sq, Skv, dtype=torch.float64).masked_fill(~allowed, float("-inf"))
+    mask = mask[:, None].expand(B, Hq, Sq, Skv)
     off = None
     if st != VANILLA:
         kk = torch.cat([kk, torch.zeros(B, Hq, 1, dqk, dtype=torch.float64)], dim=2)
@@ -253,7 +261,10 @@ def _torch_reference(x, causal, window, st, scale):
             col = torch.zeros(B, Hq, Sq, 1, dtype=torch.float64)
         mask = torch.cat([mask, col], dim=3)
     o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask, scale=scale)
-    do = torch.tensor(x["dout"]).permute(0, 2, 1, 3)
+    do = torch.tensor(x["dout"]).permute(0, 2, 1, 3).clone()
+    if lens_q is not None:
+        for b in range(B):
+            do[b, :, lens_q[b]:] = 0
     (o * do).sum().backward()
     res = {"o": o.detach().permute(0, 2, 1, 3).numpy(),
            "dq": q.grad.permute(0, 2, 1, 3).numpy(),
@@ -361,3 +372,64 @@ def test_empty_and_keyless_rows():
                              offset=x["offset"])
     np.testing.assert_allclose(f["lse"][0, 0, 4:], x["offset"][0], atol=0)
     np.testing.assert_allclose(f["psink"][0, 0, 4:], 1.0, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# Padded batches (per-entry lengths): the oracle runs each entry on its valid
+# rows alone; torch gets the full padded tensors with the padding masked instead.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("st", [VANILLA, OFF_BY_ONE, LEARNABLE])
+@pytest.mark.parametrize("causal,window", [(True, -1), (True, 5), (False, -1)])
+def test_varlen_matches_torch_sdpa_fp64(st, causal, window):
+    s = Shape(4, 21, 26, 4, 2, 16, 8)
+    x = _inp(s, 31, learnable=True)
+    lq, lkv = [21, 9, 1, 14], [26, 12, 7, 3]
+    scale = 0.29
+    off = x["offset"] if st == LEARNABLE else None
+    kw = dict(seq_lens_q=lq, seq_lens_kv=lkv, causal=causal, window=window, softmax_type=st, offset=off,
+              scale=scale)
+    f = oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], **kw)
+    g = oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dout"], **kw)
+    ref = _torch_reference(x, causal, window, st, scale, lq, lkv)
+    for b in range(4):
+        # valid rows that see at least one key (with causal top-left, rows >= Lkv see keys < Lkv)
+        np.testing.assert_allclose(f["o"][b, :lq[b]], ref["o"][b, :lq[b]], atol=1e-12)
+    for key in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(g[key], ref[key], atol=1e-11)
+    if st == LEARNABLE:
+        np.testing.assert_allclose(g["d_offset"], ref["d_offset"], atol=1e-11)
+
+
+def test_varlen_padding_and_full_lengths():
+    s = Shape(3, 12, 10, 2, 1, 8, 8)
+    x = _inp(s, 37, learnable=True)
+    # full lengths reproduce the plain oracle exactly
+    kw = dict(causal=True, window=4, softmax_type=LEARNABLE, offset=x["offset"])
+    f0 = oracle.attention_fwd(x["q"], x["k"], x["v"], **kw)
+    f1 = oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], seq_lens_q=[12, 12, 12], seq_lens_kv=[10, 10, 10], **kw)
+    g0 = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dout"], **kw)
+    g1 = oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dout"], seq_lens_q=None, seq_lens_kv=[10] * 3, **kw)
+    for key in ("o", "lse"):
+        assert np.array_equal(f0[key], f1[key])
+    for key in ("dq", "dk", "dv", "d_offset"):
+        assert np.array_equal(g0[key], g1[key])
+    # padded rows: O = 0 and LSE = the sink logit; padded keys and rows get no gradient;
+    # an entry with no key (Lkv = 0) is all padding; lengths past S are clamped
+    lq, lkv = [5, 12, 30], [0, 4, 10]
+    for st in (VANILLA, OFF_BY_ONE, LEARNABLE):
+        kw = dict(seq_lens_q=lq, seq_lens_kv=lkv, causal=True, softmax_type=st, offset=x["offset"])
+        f = oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], **kw)
+        g = oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dout"], **kw)
+        c = {VANILLA: -np.inf, OFF_BY_ONE: 0.0, LEARNABLE: None}[st]
+        for b, (a, kk) in enumerate(zip([5, 12, 12], [0, 4, 10])):
+            assert np.all(f["o"][b, a:] == 0) and np.all(g["dq"][b, a:] == 0)
+            assert np.all(g["dk"][b, kk:] == 0) and np.all(g["dv"][b, kk:] == 0)
+            for h in range(2):
+                want = x["offset"][h] if st == LEARNABLE else c
+                assert np.all(f["lse"][b, h, a:] == want)
+        assert np.all(f["o"][0] == 0) and np.all(g["dq"][0] == 0)
+        # a valid entry is the plain oracle on its own rows
+        r = oracle.attention_fwd(x["q"][1:2, :12], x["k"][1:2, :4], x["v"][1:2, :4], causal=True, softmax_type=st,
+                                 offset=x["offset"])
+        assert np.array_equal(f["o"][1], r["o"][0])
