@@ -101,6 +101,29 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int d_v, float scale, int causal, int window, int softmax_type, const float* softmax_offset,
              int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Padded batches ("JAX: Single-GPU Attention with TransformerEngine", section 1:
+ * the sequence descriptor gives each sequence's length and its padding).  Same as
+ * attn_fwd / attn_bwd, plus seq_lens_q and seq_lens_kv: device int32 arrays [B]
+ * (4-byte aligned, read by the kernels, owned by the caller) holding how many of
+ * entry b's S_q query rows and S_kv key rows are real; they sit at the front of the
+ * entry's rows and the rest is padding.  Values are clamped to [0, S_q] and
+ * [0, S_kv].  NULL means every entry is full length (then these calls are exactly
+ * attn_fwd / attn_bwd).  Entry b computes as if its tensors held only its real
+ * rows; a padded query row sees no key, so o = 0 and lse = the sink logit (-inf
+ * for VANILLA, 0 for OFF_BY_ONE, offset[h] for LEARNABLE) there; padded rows and
+ * padded keys get zero dq / dk / dv and add nothing to d_offset.  Work outside
+ * each entry's lengths is skipped.  Same workspace as attn_bwd.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+                    int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, void* stream);
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
+                    int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* attn_status_string(int status);
 

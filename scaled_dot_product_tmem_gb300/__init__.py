@@ -53,6 +53,11 @@ def _load():
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, i, vp, sz,
                              vp]
     lib.attn_bwd.restype = i
+    lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, vp, vp, vp]
+    lib.attn_fwd_varlen.restype = i
+    lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, vp,
+                                    vp, i, vp, sz, vp]
+    lib.attn_bwd_varlen.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_error_message.argtypes = []
@@ -122,9 +127,20 @@ def attn_last_device_error(stream=None):
     return st, site.value
 
 
+def _check_lens(t, name, B):
+    if t is not None:
+        _check(t, name, torch.int32, 1)
+        if t.shape[0] != B:
+            raise ValueError(f"{name}: one length per batch entry ({B}), got {t.shape[0]}")
+
+
 def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-             stream=None):
-    """Forward into preallocated o [B,S_q,H_q,d_v] bf16 and lse [B,H_q,S_q] fp32."""
+             seq_lens_q=None, seq_lens_kv=None, stream=None):
+    """Forward into preallocated o [B,S_q,H_q,d_v] bf16 and lse [B,H_q,S_q] fp32.
+
+    seq_lens_q / seq_lens_kv: optional int32 [B] device tensors for a padded batch
+    (attn_fwd_varlen); None means full length.
+    """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, n, torch.bfloat16, 4)
     _check(lse, "lse", torch.float32, 3)
@@ -132,9 +148,14 @@ def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, s
         _check(softmax_offset, "softmax_offset", torch.float32, 1)
     B, S_q, H_q, d_qk = q.shape
     _, S_kv, H_kv, d_v = v.shape
-    st = _load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d_qk, d_v,
-                          float(scale or 0.0), int(bool(causal)), int(window), _stype(softmax_type),
-                          _ptr(softmax_offset), _stream(stream))
+    _check_lens(seq_lens_q, "seq_lens_q", B)
+    _check_lens(seq_lens_kv, "seq_lens_kv", B)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
+            int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset))
+    if seq_lens_q is None and seq_lens_kv is None:
+        st = _load().attn_fwd(*args, _stream(stream))
+    else:
+        st = _load().attn_fwd_varlen(*args, _ptr(seq_lens_q), _ptr(seq_lens_kv), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
 
@@ -144,20 +165,30 @@ def attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic=Tr
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, window=-1, softmax_type=VANILLA,
-             softmax_offset=None, scale=0.0, deterministic=True, workspace=None, stream=None):
-    """Backward into preallocated dq, dk, dv (bf16) and d_offset (fp32 [H_q], learnable)."""
+             softmax_offset=None, scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None,
+             stream=None):
+    """Backward into preallocated dq, dk, dv (bf16) and d_offset (fp32 [H_q], learnable).
+
+    seq_lens_q / seq_lens_kv as for attn_fwd (attn_bwd_varlen).
+    """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16, 4)
     _check(lse, "lse", torch.float32, 3)
     B, S_q, H_q, d_qk = q.shape
     _, S_kv, H_kv, d_v = v.shape
+    _check_lens(seq_lens_q, "seq_lens_q", B)
+    _check_lens(seq_lens_kv, "seq_lens_kv", B)
     need = attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = _load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(d_offset), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
-                          int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset),
-                          int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(d_offset),
+            B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0), int(bool(causal)), int(window),
+            _stype(softmax_type), _ptr(softmax_offset))
+    tail = (int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
+    if seq_lens_q is None and seq_lens_kv is None:
+        st = _load().attn_bwd(*args, *tail)
+    else:
+        st = _load().attn_bwd_varlen(*args, _ptr(seq_lens_q), _ptr(seq_lens_kv), *tail)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
 
@@ -207,19 +238,20 @@ def attn_timing_read():
 
 
 def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-                 stream=None):
+                 seq_lens_q=None, seq_lens_kv=None, stream=None):
     """Allocate O and LSE, run attn_fwd, return (o, lse)."""
     B, S_q, H_q, _ = q.shape
     d_v = v.shape[3]
     o = torch.empty((B, S_q, H_q, d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H_q, S_q), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, o, lse, causal=causal, window=window, softmax_type=softmax_type,
-             softmax_offset=softmax_offset, scale=scale, stream=stream)
+             softmax_offset=softmax_offset, scale=scale, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv,
+             stream=stream)
     return o, lse
 
 
 def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None,
-                  scale=0.0, deterministic=True, workspace=None, stream=None):
+                  scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None, stream=None):
     """Allocate dQ, dK, dV (and d_offset for the learnable sink), run attn_bwd, return them."""
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
@@ -228,7 +260,7 @@ def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type
     d_off = torch.empty((q.shape[2],), dtype=torch.float32, device=q.device) if st == LEARNABLE else None
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_off, causal=causal, window=window, softmax_type=st,
              softmax_offset=softmax_offset, scale=scale, deterministic=deterministic, workspace=workspace,
-             stream=stream)
+             seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, stream=stream)
     return dq, dk, dv, d_off
 
 

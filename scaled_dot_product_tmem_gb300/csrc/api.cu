@@ -161,14 +161,15 @@ int attn_last_device_error(void* stream, int* site) {
   return ATTN_ERR_DEVICE_TIMEOUT;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
-             int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
-             const float* softmax_offset, void* stream) {
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+                    int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, void* stream) {
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
   if (st != ATTN_OK) return st;
   if (B == 0 || S_q == 0) return ATTN_OK;
   if (!q || !o || !lse || (S_kv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens_q) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens_kv) & 3u))
     return ATTN_ERR_MISALIGNED;
   int* err = device_error_ptr();
   if (!err) return ATTN_ERR_CUDA;
@@ -190,6 +191,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.window = window < 0 ? -1 : window;
   p.softmax_type = softmax_type;
   p.offset = softmax_offset;
+  p.seq_q = seq_lens_q;
+  p.seq_kv = seq_lens_kv;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.err = err;
@@ -203,15 +206,25 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ATTN_OK;
 }
 
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
+             int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+             const float* softmax_offset, void* stream) {
+  return attn_fwd_varlen(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
+                         softmax_offset, nullptr, nullptr, stream);
+}
+
 size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic) {
   if (check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, 1, -1, 0, nullptr) != ATTN_OK) return 0;
   return ws_layout(B, S_q, H_q, d_qk, use_fused_dq(d_qk, d_v, deterministic)).total;
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-             void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk,
-             int d_v, float scale, int causal, int window, int softmax_type, const float* softmax_offset,
-             int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
+                    int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if ((reinterpret_cast<uintptr_t>(seq_lens_q) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens_kv) & 3u))
+    return ATTN_ERR_MISALIGNED;
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
   if (st != ATTN_OK) return st;
   if (softmax_type == ATTN_SOFTMAX_LEARNABLE && !d_offset) return ATTN_ERR_INVALID_ARG;
@@ -252,6 +265,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.softmax_type = softmax_type;
   p.S_pad = (S_q + 127) / 128 * 128;
   p.offset = softmax_offset;
+  p.seq_q = seq_lens_q;
+  p.seq_kv = seq_lens_kv;
   p.o = static_cast<const __nv_bfloat16*>(o);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
@@ -316,6 +331,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     }
   }
   return ATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk,
+             int d_v, float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+             int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale,
+                         causal, window, softmax_type, softmax_offset, nullptr, nullptr, deterministic, workspace,
+                         workspace_bytes, stream);
 }
 
 int attn_timing_enable(int on) {

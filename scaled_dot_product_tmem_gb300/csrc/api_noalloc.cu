@@ -145,6 +145,8 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = nullptr;
+  p.seq_q = nullptr;
+  p.seq_kv = nullptr;
   p.err = err;
 
   if (sdpa::launch_bwd_preprocess(d_v, p, s) != 0) return ATTN_ERR_CUDA;

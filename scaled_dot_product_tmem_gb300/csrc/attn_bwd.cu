@@ -35,7 +35,8 @@ namespace sdpa {
 // Preprocess: D = rowsum(dO * O) (fp32) and nlse2 = -LSE * log2(e), one block per
 // (64 query rows, head, batch) so the per-row values are read and written as
 // contiguous runs.  Rows are padded to S_pad: D = 0 and nlse2 = -inf there, so
-// padded query rows get P = exp2(s + nlse2) = 0 in the main kernels.
+// padded query rows get P = exp2(s + nlse2) = 0 in the main kernels.  In a padded
+// batch, an entry's rows past its own query length are padding in the same way.
 // =============================================================================
 template <int D_V>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   constexpr int TILE = 64;
   __shared__ float dsum[TILE];
   const int i0 = blockIdx.x * TILE, h = blockIdx.y, b = blockIdx.z;
+  const int Lq = entry_len(p.seq_q, b, p.S_q);  // rows past it are padding, like rows past S_q
   const int sub = threadIdx.x % TPR;
   constexpr int NR = TILE / RPP;  // rows per thread
   uint4 a[NR], g[NR];
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   for (int k = 0; k < NR; ++k) {  // every load of this thread first, then the math
     const int i = i0 + threadIdx.x / TPR + k * RPP;
     a[k] = g[k] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < p.S_q) {
+    if (i < Lq) {
       const size_t off = (((size_t)b * p.S_q + i) * p.H_q + h) * D_V + sub * 8;
       a[k] = __ldcs(reinterpret_cast<const uint4*>(p.o + off));
       g[k] = __ldcs(reinterpret_cast<const uint4*>(p.dout + off));
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   if (threadIdx.x < TILE) {
     const int i = i0 + threadIdx.x;
     const size_t bh = (size_t)b * p.H_q + h;
-    const bool real = i < p.S_q;
+    const bool real = i < Lq;
     p.Dsum[bh * p.S_pad + i] = real ? dsum[threadIdx.x] : 0.f;
     p.nlse2[bh * p.S_pad + i] = real ? -p.lse[bh * p.S_q + i] * kLog2e : -INFINITY;
   }
@@ -214,9 +216,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   const int g = chunk * kKvChunk + within % csize;
   const int hk = g % p.H_kv, b = g / p.H_kv;
   const int n0 = (within / csize) * C::BN;
-  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
+  const MaskSpec mask{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal, p.window};
   int ilo = 0, ihi = -1;
-  const bool any_q = q_tile_range(mask, n0, min(n0 + C::BN - 1, p.S_kv - 1), C::BQ, &ilo, &ihi);
+  const bool any_q = q_tile_range(mask, n0, n0 + C::BN - 1, C::BQ, &ilo, &ihi);
   const int nq = any_q ? ihi - ilo + 1 : 0;
   const int nsteps = nq * p.G;
 
@@ -639,9 +641,9 @@ __global__ void __launch_bounds__(352, 1)
   const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
   const int h = g % p.H_q, b = g / p.H_q, hk = h / p.G;
   const int m0 = qt * C::BM;
-  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
+  const MaskSpec mask{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal, p.window};
   int jlo = 1, jhi = 0;
-  const bool active = kv_tile_range(mask, m0, min(m0 + C::BM - 1, p.S_q - 1), C::BN, &jlo, &jhi);
+  const bool active = kv_tile_range(mask, m0, m0 + C::BM - 1, C::BN, &jlo, &jhi);
   const int nj = active ? jhi - jlo + 1 : 0;
 
   if (threadIdx.x == 0) {

@@ -3,8 +3,10 @@
 // which query tiles a block of keys is seen by.
 //
 // Masking rule (causal with an optional left window, top-left diagonal):
-//   key j is visible to query i  iff  j < S_kv  and (!causal or j <= i)
+//   key j is visible to query i  iff  i < S_q and j < S_kv and (!causal or j <= i)
 //                                     and (window < 0 or j >= i - window).
+// In a padded batch S_q and S_kv are the entry's own lengths, so its padded query
+// rows see no key and its padded keys are seen by no query.
 // ("JAX: Single-GPU Attention with TransformerEngine", sections 1-2: causal
 // mask plus sliding window; codelab "Speed up attention on GPU with cuDNN and
 // TransformerEngine", step 7: query i sees keys j <= i.)
@@ -18,13 +20,22 @@ struct MaskSpec {
 };
 
 __host__ __device__ __forceinline__ bool key_visible(const MaskSpec& m, int i, int j) {
-  return j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
+  return i < m.S_q && j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
+}
+
+// Length of batch entry b: lens[b] clamped to [0, S], or S without a length array.
+__host__ __device__ __forceinline__ int entry_len(const int* lens, int b, int S) {
+  if (!lens) return S;
+  const int l = lens[b];
+  return l < 0 ? 0 : (l > S ? S : l);
 }
 
 // Inclusive range of kv tiles (size bn) touched by query rows [r0, r1]; returns
 // false when those rows see no key at all.
 __host__ __device__ __forceinline__ bool kv_tile_range(const MaskSpec& m, int r0, int r1, int bn, int* jlo,
                                                        int* jhi) {
+  if (r1 > m.S_q - 1) r1 = m.S_q - 1;
+  if (r1 < r0) return false;
   int lo = m.window >= 0 ? (r0 - m.window > 0 ? r0 - m.window : 0) : 0;
   int hi = m.causal ? (r1 < m.S_kv - 1 ? r1 : m.S_kv - 1) : m.S_kv - 1;
   if (hi < lo || m.S_kv <= 0) return false;
@@ -37,6 +48,8 @@ __host__ __device__ __forceinline__ bool kv_tile_range(const MaskSpec& m, int r0
 // [k0, k1]; returns false when none does.
 __host__ __device__ __forceinline__ bool q_tile_range(const MaskSpec& m, int k0, int k1, int bm, int* ilo,
                                                       int* ihi) {
+  if (k1 > m.S_kv - 1) k1 = m.S_kv - 1;
+  if (k1 < k0) return false;
   int lo = m.causal ? k0 : 0;
   int hi = m.window >= 0 ? k1 + m.window : m.S_q - 1;
   if (hi > m.S_q - 1) hi = m.S_q - 1;
@@ -47,11 +60,11 @@ __host__ __device__ __forceinline__ bool q_tile_range(const MaskSpec& m, int k0,
 }
 
 // Is the whole (rows [r0, r0+bm), keys [k0, k0+bn)) tile visible?  Then the
-// per-element mask can be skipped.  Rows past S_q do not matter (never stored).
+// per-element mask can be skipped.
 __host__ __device__ __forceinline__ bool tile_fully_visible(const MaskSpec& m, int r0, int bm, int k0, int bn) {
   int r1 = r0 + bm - 1;
   int k1 = k0 + bn - 1;
-  if (k1 >= m.S_kv) return false;
+  if (k1 >= m.S_kv || r1 >= m.S_q) return false;
   if (m.causal && k1 > r0) return false;
   if (m.window >= 0 && k0 < r1 - m.window) return false;
   return true;

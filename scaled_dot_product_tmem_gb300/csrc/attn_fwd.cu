@@ -62,10 +62,11 @@ struct FwdTile {
   int h, b, hk, m0, J0, J1;
   int jlo[2], jhi[2];
   bool exists[2], active[2], any;
+  MaskSpec mask;  // with the entry's own lengths
 };
 
 template <int BM, int BN>
-__device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, const MaskSpec& mask, int nqb, int wi) {
+__device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi) {
   FwdTile T;
   const int hb = wi % (p.H_q * p.B);
   const int q = wi / (p.H_q * p.B);
@@ -74,12 +75,12 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, const MaskSpec& 
   T.b = hb / p.H_q;
   T.hk = T.h / p.G;
   T.m0 = qb * 2 * BM;
+  T.mask = MaskSpec{entry_len(p.seq_q, T.b, p.S_q), entry_len(p.seq_kv, T.b, p.S_kv), p.causal, p.window};
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = T.m0 + t * BM;
-    T.exists[t] = r0 < p.S_q;
-    const int r1 = min(r0 + BM - 1, p.S_q - 1);
-    T.active[t] = T.exists[t] && kv_tile_range(mask, r0, r1, BN, &T.jlo[t], &T.jhi[t]);
+    T.exists[t] = r0 < p.S_q;  // rows of the padded tensor: they get an output either way
+    T.active[t] = T.exists[t] && kv_tile_range(T.mask, r0, r0 + BM - 1, BN, &T.jlo[t], &T.jhi[t]);
     if (!T.active[t]) { T.jlo[t] = 1; T.jhi[t] = 0; }
   }
   T.any = T.active[0] || T.active[1];
@@ -111,7 +112,6 @@ __global__ void __launch_bounds__(320, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const MaskSpec mask{p.S_q, p.S_kv, p.causal, p.window};
   const int nqb = (p.S_q + 2 * C::BM - 1) / (2 * C::BM);
   const int n_work = nqb * p.H_q * p.B;
 
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(320, 1)
       int n = 0, nw = 0;  // kv stages loaded, Q tiles loaded
       bool ok = true;
       for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-        const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+        const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
         if (!T.any) continue;
         // Q of the previous tile must have been read by that tile's last S MMAs
         if (nw > 0) ok = mbar_wait(q_empty, (nw - 1) & 1, err, kSiteQ);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(320, 1)
     int pc[2] = {0, 0};     // p_ready phases consumed per query tile
     bool ok = true, issued = false;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-      const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+      const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
       if (!T.any) continue;
       issued = true;
       ok = mbar_wait_warp(q_full, nw & 1, err, kSiteQ);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(320, 1)
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
     bool ok = true;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-      const FwdTile T = fwd_tile<C::BM, C::BN>(p, mask, nqb, wi);
+      const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
       if (!T.exists[t]) continue;
       const int m0 = T.m0, h = T.h, b = T.b;
       const int i = m0 + t * C::BM + r;  // query row
@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
           }
           const int k0 = j * C::BN;
+          const MaskSpec& mask = T.mask;
           if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

@@ -12,6 +12,8 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal, window, softmax_type;
   const float* offset;  // [H_q], learnable only
+  const int* seq_q;     // [B] query lengths of a padded batch, or null (all S_q)
+  const int* seq_kv;    // [B] key lengths of a padded batch, or null (all S_kv)
   __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
   float* lse;           // [B, H_q, S_q]
   int* err;             // device error word
@@ -29,6 +31,8 @@ struct BwdParams {
   int causal, window, softmax_type;
   int S_pad;                  // S_q rounded up to 128: row length of nlse2 / Dsum
   const float* offset;        // [H_q]
+  const int* seq_q;           // [B] query lengths of a padded batch, or null (all S_q)
+  const int* seq_kv;          // [B] key lengths of a padded batch, or null (all S_kv)
   const __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
   const __nv_bfloat16* dout;  // [B, S_q, H_q, d_v]
   const float* lse;           // [B, H_q, S_q] (natural log)

@@ -15,12 +15,15 @@ TOL_LSE = 1e-3
 TOL_GRAD = 1e-2
 
 
-def gpu_run(x, *, causal, window, softmax_type, scale, deterministic=True, bwd=True):
+def gpu_run(x, *, causal, window, softmax_type, scale, deterministic=True, bwd=True, lens_q=None, lens_kv=None):
     import scaled_dot_product_tmem_gb300 as sdpa
     dev = torch.device("cuda")
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     off = x["offset"].to(dev) if softmax_type == oracle.LEARNABLE else None
     kw = dict(causal=causal, window=window, softmax_type=softmax_type, softmax_offset=off, scale=scale)
+    if lens_q is not None or lens_kv is not None:
+        kw["seq_lens_q"] = None if lens_q is None else torch.tensor(lens_q, dtype=torch.int32, device=dev)
+        kw["seq_lens_kv"] = None if lens_kv is None else torch.tensor(lens_kv, dtype=torch.int32, device=dev)
     o, lse = sdpa.sdpa_forward(q, k, v, **kw)
     res = {"o": o, "lse": lse}
     if bwd:
@@ -35,14 +38,19 @@ def gpu_run(x, *, causal, window, softmax_type, scale, deterministic=True, bwd=T
     return {n: t.float().cpu().numpy() for n, t in res.items()}
 
 
-def oracle_run(x, *, causal, window, softmax_type, scale, bwd=True):
+def oracle_run(x, *, causal, window, softmax_type, scale, bwd=True, lens_q=None, lens_kv=None):
     xd = {n: t.double().numpy() for n, t in x.items()}
     off = xd.get("offset") if softmax_type == oracle.LEARNABLE else None
     kw = dict(causal=causal, window=window, softmax_type=softmax_type, offset=off, scale=scale)
-    f = oracle.attention_fwd(xd["q"], xd["k"], xd["v"], **kw)
+    varlen = lens_q is not None or lens_kv is not None
+    fwd, bwd_fn = (oracle.attention_fwd_varlen, oracle.attention_bwd_varlen) if varlen else \
+        (oracle.attention_fwd, oracle.attention_bwd)
+    if varlen:
+        kw.update(seq_lens_q=lens_q, seq_lens_kv=lens_kv)
+    f = fwd(xd["q"], xd["k"], xd["v"], **kw)
     res = {"o": f["o"], "lse": f["lse"]}
     if bwd:
-        g = oracle.attention_bwd(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
+        g = bwd_fn(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
         res.update(dq=g["dq"], dk=g["dk"], dv=g["dv"])
         if softmax_type == oracle.LEARNABLE:
             res["d_offset"] = g["d_offset"]
