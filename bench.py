@@ -36,9 +36,11 @@ NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc):
+def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None):
+    """A workload; `lens` (one length per batch entry, same for queries and keys) makes
+    it a padded batch run through the varlen entry points."""
     return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
-                scale=scale, seed=seed, desc=desc)
+                scale=scale, seed=seed, desc=desc, lens=lens)
 
 
 WORKLOADS = {
@@ -59,6 +61,11 @@ for _S in (512, 1024, 2048, 4096, 8192, 16384):
         _n = f"sweep_s{_S}_hkv{_H}"
         WORKLOADS[_n] = _w(_n, 32768 // _S, _S, 32, _H, 128, 128, True, -1, 0, None, 1000 + _S + _H,
                            f"32768-token sweep: B={32768 // _S}, S={_S}, H_q=32, H_kv={_H}, d=128, causal")
+# Padded batch: B=8 entries padded to S=4096, lengths spread evenly from 512 to 4096.
+WORKLOADS["varlen_gqa_b8_s4096"] = _w(
+    "varlen_gqa_b8_s4096", 8, 4096, 32, 8, 128, 128, True, -1, 0, None, 5,
+    "padded batch: B=8 padded to S=4096, lengths 4096, 3584, ..., 512, H_q=32, H_kv=8, d=128, causal",
+    lens=[4096 - 512 * i for i in range(8)])
 DEFAULT = "gqa_swa_b4_s2048"
 HEADLINE = "sweep_s8192_hkv8"
 
@@ -73,8 +80,16 @@ def n_pairs(S, causal, window):
     return (w + 1) * (w + 2) // 2 + (S - w - 1) * (w + 1)
 
 
+def total_pairs(wl):
+    """Unmasked pairs of one query head summed over the batch (each entry over its own
+    length in a padded batch)."""
+    if wl.get("lens"):
+        return sum(n_pairs(L, wl["causal"], wl["window"]) for L in wl["lens"])
+    return wl["B"] * n_pairs(wl["S"], wl["causal"], wl["window"])
+
+
 def flops(wl, part="total"):
-    n = wl["B"] * wl["Hq"] * n_pairs(wl["S"], wl["causal"], wl["window"])
+    n = wl["Hq"] * total_pairs(wl)
     fwd = n * 2 * (wl["dqk"] + wl["dv"])
     bwd = n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}[part]
@@ -82,7 +97,7 @@ def flops(wl, part="total"):
 
 def kernel_flops(wl, cls, fused):
     """Algorithmic FLOPs one launch of a kernel class performs (see the design notes)."""
-    n = wl["B"] * wl["Hq"] * n_pairs(wl["S"], wl["causal"], wl["window"])
+    n = wl["Hq"] * total_pairs(wl)
     d, e = wl["dqk"], wl["dv"]
     return {"fwd": n * 2 * (d + e),
             "bwd_kv": n * 2 * ((3 * d + 2 * e) if fused else (2 * d + 2 * e)),
@@ -184,17 +199,22 @@ def run_oracle_unit(wl, x, b, h):
     import oracle
     G = wl["Hq"] // wl["Hkv"]
     g = h // G
-    q = x["q"][b:b + 1, :, h:h + 1].double().numpy()
-    k = x["k"][b:b + 1, :, g:g + 1].double().numpy()
-    v = x["v"][b:b + 1, :, g:g + 1].double().numpy()
-    do = x["dout"][b:b + 1, :, h:h + 1].double().numpy()
+    L = wl["lens"][b] if wl.get("lens") else wl["S"]  # a padded entry computes on its own rows
+    q = x["q"][b:b + 1, :L, h:h + 1].double().numpy()
+    k = x["k"][b:b + 1, :L, g:g + 1].double().numpy()
+    v = x["v"][b:b + 1, :L, g:g + 1].double().numpy()
+    do = x["dout"][b:b + 1, :L, h:h + 1].double().numpy()
     off = x["offset"][h:h + 1].double().numpy() if wl["st"] == 2 else None
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], offset=off, scale=wl["scale"])
     oracle.attention_fwd(q, k, v, **kw)
     oracle.attention_bwd(q, k, v, do, **kw)
 
 
-def unit_flops(wl):
+def unit_flops(wl, b=None):
+    """FLOPs of one (batch, query head) unit: of entry b, or the workload's average."""
+    if b is not None and wl.get("lens"):
+        per = 2 * (wl["dqk"] + wl["dv"]) + 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+        return n_pairs(wl["lens"][b], wl["causal"], wl["window"]) * per
     return flops(wl) / (wl["B"] * wl["Hq"])
 
 
@@ -208,14 +228,15 @@ def cpu_baseline(wl, x, budget_s=12.0):
     """The oracle, as it stands, on whole (batch, query head) units until ~budget_s."""
     import oracle
     units = oracle_units(wl)
-    done, t0 = 0, time.perf_counter()
+    done, work, t0 = 0, 0.0, time.perf_counter()
     for b, h in units:
         run_oracle_unit(wl, x, b, h)
         done += 1
+        work += unit_flops(wl, b)
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": done * unit_flops(wl) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    return {"value": work / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{done} of {len(units)} (batch, query head) units of the workload, fwd+bwd in fp64 "
                       f"({dt:.1f} s); TFLOP/s counts the same unmasked FLOPs as the GPU number"}
@@ -245,11 +266,13 @@ def reference_arm(args, wl, world, rank):
     units = oracle_units(wl)
     for i in range(args.warmup):
         run_oracle_unit(wl, x, *units[i % len(units)])
-    t0 = time.perf_counter()
+    t0, work = time.perf_counter(), 0.0
     for i in range(args.steps):
-        run_oracle_unit(wl, x, *units[(args.warmup + i) % len(units)])
+        u = units[(args.warmup + i) % len(units)]
+        run_oracle_unit(wl, x, *u)
+        work += unit_flops(wl, u[0])
     dt = time.perf_counter() - t0
-    value = args.steps * unit_flops(wl) / dt / 1e12
+    value = work / dt / 1e12
     sample = (f"each step = one (batch, query head) unit of the workload, fwd+bwd in fp64 "
               f"({unit_flops(wl) / 1e9:.2f} GFLOP)")
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
@@ -279,6 +302,9 @@ def _step_fns(sdpa, wl, dev, det, x):
                      device=dev)
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], softmax_offset=off,
               scale=wl["scale"] or 0.0)
+    if wl.get("lens"):
+        lens = torch.tensor(wl["lens"], dtype=torch.int32, device=dev)
+        kw.update(seq_lens_q=lens, seq_lens_kv=lens)
 
     def step():
         sdpa.attn_fwd(t["q"], t["k"], t["v"], o, lse, **kw)
@@ -396,7 +422,8 @@ def ours_arm(args, wl, world, rank, local):
             "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
                        "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
                        "bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ",
-                       "l2": "flushed between timed steps (258 MB write outside the timed span)"},
+                       "l2": "flushed between timed steps (258 MB write outside the timed span)",
+                       **({"seq_lens": wl["lens"]} if wl.get("lens") else {})},
             "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             "fwd_tflop": flops(wl, "fwd") / 1e12, "bwd_tflop": flops(wl, "bwd") / 1e12,
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -70,3 +70,16 @@ def test_max_over_ranks_gloo_two_ranks():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == {0: 11.0, 1: 11.0}
+
+
+def test_padded_batch_workload_counts_each_entry_on_its_own_length():
+    import bench
+    wl = bench.WORKLOADS["varlen_gqa_b8_s4096"]
+    assert len(wl["lens"]) == wl["B"] and max(wl["lens"]) <= wl["S"]
+    per_pair = 2 * (wl["dqk"] + wl["dv"]) + 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+    want = wl["Hq"] * sum(L * (L + 1) // 2 for L in wl["lens"]) * per_pair
+    assert bench.flops(wl) == want
+    assert sum(bench.unit_flops(wl, b) for b in range(wl["B"])) * wl["Hq"] == want
+    # a padded batch whose lengths are all S counts like the plain workload
+    full = dict(wl, lens=[wl["S"]] * wl["B"])
+    assert bench.flops(full) == bench.flops(dict(wl, lens=None))
