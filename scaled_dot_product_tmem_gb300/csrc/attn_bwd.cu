@@ -180,7 +180,7 @@ constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
               kKvDvDone, kKvDkDone };
 
-template <int D_QK, int D_V, bool FUSE_DQ>
+template <int D_QK, int D_V, bool FUSE_DQ, bool VL>
 __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   const int g = chunk * kKvChunk + within % csize;
   const int hk = g % p.H_kv, b = g / p.H_kv;
   const int n0 = (within / csize) * C::BN;
-  const MaskSpec mask{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal, p.window};
+  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
+                                      p.window}
+                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
   int ilo = 0, ihi = -1;
   const bool any_q = q_tile_range(mask, n0, n0 + C::BN - 1, C::BQ, &ilo, &ihi);
   const int nq = any_q ? ihi - ilo + 1 : 0;
@@ -409,10 +411,10 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           pr[c + 1] = ex2(xb);
         }
       }
-      if (!tile_fully_visible(mask, q0, C::BQ, n0, C::BN)) {
+      if (!tile_fully_visible<VL>(mask, q0, C::BQ, n0, C::BN)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (!key_visible(mask, q0 + 32 * w + c, key)) pr[c] = 0.f;
+          if (!key_visible<VL>(mask, q0 + 32 * w + c, key)) pr[c] = 0.f;
       }
       {
         uint32_t pk[16];
@@ -550,7 +552,9 @@ template <int D_QK, int D_V, bool FUSE>
 static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using C = KvCfg<D_QK, D_V, FUSE>;
-  auto kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE>;
+  // padded batches get the instantiation with the per-entry lengths and row tests
+  auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true>
+                                    : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
@@ -606,7 +610,7 @@ struct QCfg {
 
 enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone };
 
-template <int D_QK, int D_V>
+template <int D_QK, int D_V, bool VL>
 __global__ void __launch_bounds__(352, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -641,7 +645,9 @@ __global__ void __launch_bounds__(352, 1)
   const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
   const int h = g % p.H_q, b = g / p.H_q, hk = h / p.G;
   const int m0 = qt * C::BM;
-  const MaskSpec mask{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal, p.window};
+  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
+                                      p.window}
+                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
   int jlo = 1, jhi = 0;
   const bool active = kv_tile_range(mask, m0, m0 + C::BM - 1, C::BN, &jlo, &jhi);
   const int nj = active ? jhi - jlo + 1 : 0;
@@ -777,7 +783,7 @@ __global__ void __launch_bounds__(352, 1)
       ok = mbar_wait_warp(s_ready, n & 1, err, kQS);
       if (!ok) break;
       tc_fence_after();
-      const bool full = tile_fully_visible(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
+      const bool full = tile_fully_visible<VL>(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
       float pr[64];
       {
         uint32_t ra[32], rb[32];
@@ -795,7 +801,7 @@ __global__ void __launch_bounds__(352, 1)
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (!key_visible(mask, i, k0 + c)) pr[c] = 0.f;
+          if (!key_visible<VL>(mask, i, k0 + c)) pr[c] = 0.f;
       }
       ok = mbar_wait_warp(dp_ready, n & 1, err, kQDP);
       if (!ok) break;
@@ -864,7 +870,8 @@ template <int D_QK, int D_V>
 static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const BwdParams& p, cudaStream_t stream) {
   using C = QCfg<D_QK, D_V>;
-  auto kern = attn_bwd_q_kernel<D_QK, D_V>;
+  // padded batches get the instantiation with the per-entry lengths and row tests
+  auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;

@@ -19,8 +19,11 @@ struct MaskSpec {
   int S_q, S_kv, causal, window;
 };
 
+// VL: the batch is padded (S_q is the entry's own length and rows past it exist);
+// without it every row the kernels look at is below S_q and the row test is dropped.
+template <bool VL>
 __host__ __device__ __forceinline__ bool key_visible(const MaskSpec& m, int i, int j) {
-  return i < m.S_q && j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
+  return (!VL || i < m.S_q) && j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
 }
 
 // Length of batch entry b: lens[b] clamped to [0, S], or S without a length array.
@@ -60,11 +63,12 @@ __host__ __device__ __forceinline__ bool q_tile_range(const MaskSpec& m, int k0,
 }
 
 // Is the whole (rows [r0, r0+bm), keys [k0, k0+bn)) tile visible?  Then the
-// per-element mask can be skipped.
+// per-element mask can be skipped.  (Without VL, rows past S_q are never stored.)
+template <bool VL>
 __host__ __device__ __forceinline__ bool tile_fully_visible(const MaskSpec& m, int r0, int bm, int k0, int bn) {
   int r1 = r0 + bm - 1;
   int k1 = k0 + bn - 1;
-  if (k1 >= m.S_kv || r1 >= m.S_q) return false;
+  if (k1 >= m.S_kv || (VL && r1 >= m.S_q)) return false;
   if (m.causal && k1 > r0) return false;
   if (m.window >= 0 && k0 < r1 - m.window) return false;
   return true;

@@ -65,7 +65,7 @@ struct FwdTile {
   MaskSpec mask;  // with the entry's own lengths
 };
 
-template <int BM, int BN>
+template <int BM, int BN, bool VL>
 __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi) {
   FwdTile T;
   const int hb = wi % (p.H_q * p.B);
@@ -75,7 +75,8 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi)
   T.b = hb / p.H_q;
   T.hk = T.h / p.G;
   T.m0 = qb * 2 * BM;
-  T.mask = MaskSpec{entry_len(p.seq_q, T.b, p.S_q), entry_len(p.seq_kv, T.b, p.S_kv), p.causal, p.window};
+  T.mask = VL ? MaskSpec{entry_len(p.seq_q, T.b, p.S_q), entry_len(p.seq_kv, T.b, p.S_kv), p.causal, p.window}
+              : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = T.m0 + t * BM;
@@ -91,7 +92,7 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi)
 
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
 
-template <int D_QK, int D_V, int NK, int NV>
+template <int D_QK, int D_V, int NK, int NV, bool VL>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(320, 1)
       int n = 0, nw = 0;  // kv stages loaded, Q tiles loaded
       bool ok = true;
       for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-        const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
+        const FwdTile T = fwd_tile<C::BM, C::BN, VL>(p, nqb, wi);
         if (!T.any) continue;
         // Q of the previous tile must have been read by that tile's last S MMAs
         if (nw > 0) ok = mbar_wait(q_empty, (nw - 1) & 1, err, kSiteQ);
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(320, 1)
     int pc[2] = {0, 0};     // p_ready phases consumed per query tile
     bool ok = true, issued = false;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-      const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
+      const FwdTile T = fwd_tile<C::BM, C::BN, VL>(p, nqb, wi);
       if (!T.any) continue;
       issued = true;
       ok = mbar_wait_warp(q_full, nw & 1, err, kSiteQ);
@@ -279,17 +280,23 @@ __global__ void __launch_bounds__(320, 1)
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
     bool ok = true;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
-      const FwdTile T = fwd_tile<C::BM, C::BN>(p, nqb, wi);
-      if (!T.exists[t]) continue;
+      const FwdTile T = fwd_tile<C::BM, C::BN, VL>(p, nqb, wi);
+      // this warpgroup's query tile, selected without a run-time index into T (which
+      // would move T to local memory)
+      const bool my_exists = t ? T.exists[1] : T.exists[0];
+      if (!my_exists) continue;
       const int m0 = T.m0, h = T.h, b = T.b;
+      const MaskSpec mask = T.mask;
+      const bool my_active = t ? T.active[1] : T.active[0];
+      const int my_jlo = t ? T.jlo[1] : T.jlo[0], my_jhi = t ? T.jhi[1] : T.jhi[0];
       const int i = m0 + t * C::BM + r;  // query row
       // running max (in scaled log2 units) and denominator; the sink starts them
       float m_run = -INFINITY, l = 0.f;
       if (p.softmax_type == 1) { m_run = 0.f; l = 1.f; }
       if (p.softmax_type == 2) { m_run = p.offset[h] * kLog2e; l = 1.f; }
-      if (T.active[t]) {
-        for (int j = T.jlo[t]; j <= T.jhi[t]; ++j) {
-          const int it = j - T.jlo[t];
+      if (my_active) {
+        for (int j = my_jlo; j <= my_jhi; ++j) {
+          const int it = j - my_jlo;
           ok = mbar_wait_warp(&s_ready[t], sc & 1, err, kSiteS);
           ++sc;
           if (!ok) break;
@@ -308,18 +315,17 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
           }
           const int k0 = j * C::BN;
-          const MaskSpec& mask = T.mask;
-          if (!tile_fully_visible(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
+          if (!tile_fully_visible<VL>(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const bool first = key_visible(mask, i, k0 + 32 * q), last = key_visible(mask, i, k0 + 32 * q + 31);
+              const bool first = key_visible<VL>(mask, i, k0 + 32 * q), last = key_visible<VL>(mask, i, k0 + 32 * q + 31);
               // visible keys of a row form one interval, so a chunk whose two ends are
               // visible is fully visible
               if (first && last) continue;
               float m = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                if (!key_visible(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
+                if (!key_visible<VL>(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
                 m = fmaxf(m, s[32 * q + c]);
               }
               cmax[q] = m;
@@ -380,7 +386,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       // ------------------------------------------------------------ epilogue
       bool have_o = false;
-      if (T.active[t] && ok) {  // warp-uniform
+      if (my_active && ok) {  // warp-uniform
         have_o = mbar_wait_warp(&o_done[t], od & 1, err, kSiteO);
         ++od;
         tc_fence_after();
@@ -424,11 +430,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D_QK, int D_V, int NK, int NV>
+template <int D_QK, int D_V, int NK, int NV, bool VL>
 static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                         cudaStream_t stream) {
   using C = FwdCfg<D_QK, D_V, NK, NV>;
-  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV>;
+  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
@@ -448,15 +454,23 @@ static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
+template <bool VL>
+static int launch_attn_fwd_vl(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdParams& p, cudaStream_t stream) {
+  if (d_qk == 128 && d_v == 128) return launch_fwd_t<128, 128, 2, 2, VL>(tq, tk, tv, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_fwd_t<64, 64, 4, 4, VL>(tq, tk, tv, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_fwd_t<192, 128, 2, 1, VL>(tq, tk, tv, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_fwd_t<128, 64, 2, 3, VL>(tq, tk, tv, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_fwd_t<64, 128, 3, 3, VL>(tq, tk, tv, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_fwd_t<192, 64, 2, 2, VL>(tq, tk, tv, p, stream);
+  return -2;
+}
+
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                     const FwdParams& p, cudaStream_t stream) {
-  if (d_qk == 128 && d_v == 128) return launch_fwd_t<128, 128, 2, 2>(tq, tk, tv, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_fwd_t<64, 64, 4, 4>(tq, tk, tv, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_fwd_t<192, 128, 2, 1>(tq, tk, tv, p, stream);
-  if (d_qk == 128 && d_v == 64) return launch_fwd_t<128, 64, 2, 3>(tq, tk, tv, p, stream);
-  if (d_qk == 64 && d_v == 128) return launch_fwd_t<64, 128, 3, 3>(tq, tk, tv, p, stream);
-  if (d_qk == 192 && d_v == 64) return launch_fwd_t<192, 64, 2, 2>(tq, tk, tv, p, stream);
-  return -2;
+  // padded batches get the instantiation with the per-entry lengths and row tests
+  return (p.seq_q || p.seq_kv) ? launch_attn_fwd_vl<true>(d_qk, d_v, tq, tk, tv, p, stream)
+                               : launch_attn_fwd_vl<false>(d_qk, d_v, tq, tk, tv, p, stream);
 }
 
 }  // namespace sdpa
