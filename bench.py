@@ -395,7 +395,7 @@ def ours_arm(args, wl, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sdpa.library()
-    fused_ok = wl["dqk"] == 128
+    fused_ok = wl["dqk"] in (64, 128) and wl["dv"] in (64, 128)  # the library's fused-dQ head dims
     det = bool(args.deterministic) or not fused_ok
     x = make_cpu_inputs(wl, rank)
     ms, kt, clocks = measure(sdpa, wl, dev, det, x, args.steps, args.warmup, ClockSampler(local))

@@ -170,7 +170,9 @@ struct KvCfg {
   static constexpr int COL_S0 = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
   static constexpr int COL_S1 = COL_DQ + (FUSE_DQ ? 64 : 0);
   static_assert(COL_S1 + 64 <= 512, "TMEM budget");
-  static_assert(!FUSE_DQ || D_QK == 128, "dQ^T = K^T dS^T needs M = d_qk = 128");
+  // dQ^T = K^T dS^T is issued with M = 128 head-dim rows; with d_qk = 64 its rows 64-127
+  // read the next 64 columns of shared memory (the V tile) and are never drained.
+  static_assert(!FUSE_DQ || D_QK == 128 || D_QK == 64, "fused dQ for d_qk in {64, 128}");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
 };
@@ -522,10 +524,12 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       mbar_arrive(dq_free);  // the TMEM columns may be overwritten now
       if (tid_d == 0) bulk_wait_read_all();  // previous tile has left shared memory
       named_bar_sync(1, 128);
+      if (d < D_QK) {  // lanes past d_qk hold the unused rows of the M = 128 product
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        stage[c * D_QK + d] = __uint_as_float(ra[c]);
-        stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
+        for (int c = 0; c < 32; ++c) {
+          stage[c * D_QK + d] = __uint_as_float(ra[c]);
+          stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
+        }
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
@@ -546,7 +550,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   }
 }
 
-bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return d_qk == 128 && (d_v == 128 || d_v == 64); }
+bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return (d_qk == 128 || d_qk == 64) && (d_v == 128 || d_v == 64); }
 
 template <int D_QK, int D_V, bool FUSE>
 static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
@@ -568,6 +572,8 @@ int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& t
   if (fuse_dq) {
     if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
     if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
     return -2;
   }
   if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
