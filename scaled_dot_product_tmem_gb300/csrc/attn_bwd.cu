@@ -414,9 +414,13 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         }
       }
       if (!tile_fully_visible<VL>(mask, q0, C::BQ, n0, C::BN)) {
+        int vlo, vhi;  // the query rows that see this thread's key
+        visible_rows<VL>(mask, key, &vlo, &vhi);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (!key_visible<VL>(mask, q0 + 32 * w + c, key)) pr[c] = 0.f;
+        for (int c = 0; c < 32; ++c) {
+          const int qq = q0 + 32 * w + c;
+          pr[c] = (qq >= vlo && qq <= vhi) ? pr[c] : 0.f;
+        }
       }
       {
         uint32_t pk[16];

@@ -26,6 +26,27 @@ __host__ __device__ __forceinline__ bool key_visible(const MaskSpec& m, int i, i
   return (!VL || i < m.S_q) && j < m.S_kv && (!m.causal || j <= i) && (m.window < 0 || j >= i - m.window);
 }
 
+// The keys query row i sees form one interval [*lo, *hi] (empty when lo > hi):
+// the same set key_visible<VL> describes, as two bounds a mask loop can compare with.
+template <bool VL>
+__host__ __device__ __forceinline__ void visible_keys(const MaskSpec& m, int i, int* lo, int* hi) {
+  int a = m.window >= 0 ? i - m.window : 0;
+  int z = m.causal ? i : m.S_kv - 1;
+  if (z > m.S_kv - 1) z = m.S_kv - 1;
+  *lo = a < 0 ? 0 : a;
+  *hi = (VL && i >= m.S_q) ? -1 : z;
+}
+
+// The query rows that see key j form one interval [*lo, *hi] (empty when lo > hi).
+template <bool VL>
+__host__ __device__ __forceinline__ void visible_rows(const MaskSpec& m, int j, int* lo, int* hi) {
+  int a = m.causal ? j : 0;
+  int z = m.window >= 0 ? j + m.window : 0x7fffffff - 1;
+  if (VL && z > m.S_q - 1) z = m.S_q - 1;
+  *lo = a;
+  *hi = j < m.S_kv ? z : -1;
+}
+
 // Length of batch entry b: lens[b] clamped to [0, S], or S without a length array.
 __host__ __device__ __forceinline__ int entry_len(const int* lens, int b, int S) {
   if (!lens) return S;
