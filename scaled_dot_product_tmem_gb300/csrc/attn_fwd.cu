@@ -316,16 +316,18 @@ __global__ void __launch_bounds__(320, 1)
           }
           const int k0 = j * C::BN;
           if (!tile_fully_visible<VL>(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
+            // the keys this row sees form one interval [vlo, vhi], so a chunk whose two
+            // ends are inside it is fully visible
+            int vlo, vhi;
+            visible_keys<VL>(mask, i, &vlo, &vhi);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const bool first = key_visible<VL>(mask, i, k0 + 32 * q), last = key_visible<VL>(mask, i, k0 + 32 * q + 31);
-              // visible keys of a row form one interval, so a chunk whose two ends are
-              // visible is fully visible
-              if (first && last) continue;
+              const int c0 = k0 + 32 * q;
+              if (c0 >= vlo && c0 + 31 <= vhi) continue;
               float m = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                if (!key_visible<VL>(mask, i, k0 + 32 * q + c)) s[32 * q + c] = -INFINITY;
+                if (c0 + c < vlo || c0 + c > vhi) s[32 * q + c] = -INFINITY;
                 m = fmaxf(m, s[32 * q + c]);
               }
               cmax[q] = m;
