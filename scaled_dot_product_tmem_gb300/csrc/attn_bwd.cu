@@ -802,20 +802,29 @@ __global__ void __launch_bounds__(352, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(s_free);  // S is in registers: the next S may be written
+        // P = exp2(S * scale * log2(e) - LSE * log2(e)), one f32x2 FMA per key pair
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2row, nl2row);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pr[c] = ex2(fmaf(__uint_as_float(ra[c]), sl2, nl2row));
-          pr[32 + c] = ex2(fmaf(__uint_as_float(rb[c]), sl2, nl2row));
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1, y0, y1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2x2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, nl2x2), y0, y1);
+          pr[c] = ex2(x0);
+          pr[c + 1] = ex2(x1);
+          pr[32 + c] = ex2(y0);
+          pr[32 + c + 1] = ex2(y1);
         }
       }
-      if (!full) {
+      if (!full) {  // this row sees keys [vlo, vhi]: two compares per key
+        int vlo, vhi;
+        visible_keys<VL>(mask, i, &vlo, &vhi);
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (!key_visible<VL>(mask, i, k0 + c)) pr[c] = 0.f;
+        for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
       }
       ok = mbar_wait_warp(dp_ready, n & 1, err, kQDP);
       if (!ok) break;
       tc_fence_after();
+      const uint64_t drow2 = f2_pack(drow, drow);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t rr[32];
@@ -823,9 +832,11 @@ __global__ void __launch_bounds__(352, 1)
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a = pr[c0 + 2 * c] * (__uint_as_float(rr[2 * c]) - drow);
-          const float bq = pr[c0 + 2 * c + 1] * (__uint_as_float(rr[2 * c + 1]) - drow);
+        for (int c = 0; c < 16; ++c) {  // dS = P (dP - D), paired
+          float a, bq;
+          f2_unpack(f2_mul(f2_pack(pr[c0 + 2 * c], pr[c0 + 2 * c + 1]),
+                           f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])), drow2)),
+                    a, bq);
           pk[c] = pack_bf16x2(a, bq);
         }
         tmem_st16(lane_addr + C::COL_DP + 64 * w + c0 / 2, pk);
