@@ -81,7 +81,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 /*
  * Bytes of device workspace attn_bwd needs for these sizes (256-byte aligned
  * pointer required).  deterministic != 0 selects the recompute path for dQ, which
- * needs no fp32 dQ accumulator.  Returns 0 for sizes that attn_bwd rejects.
+ * needs no fp32 dQ accumulator.  When the kv-stationary grid would be small (few
+ * kv heads, as with MQA) the query heads of a group are split across several CTAs
+ * and the workspace also holds their fp32 partial dK/dV; the combine that sums
+ * them is fixed-order, so results stay reproducible.  Returns 0 for sizes that
+ * attn_bwd rejects.
  */
 size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic);
 
@@ -190,7 +194,7 @@ enum {
   ATTN_KERNEL_BWD_PREPROCESS = 1,  /* D = rowsum(dO*O), LSE rescale, d_offset */
   ATTN_KERNEL_BWD_KV = 2,          /* kv-stationary dK/dV (+ atomic dQ) kernel */
   ATTN_KERNEL_BWD_Q = 3,           /* query-stationary deterministic dQ kernel */
-  ATTN_KERNEL_BWD_DQ_CONVERT = 4,  /* fp32 dQ accumulator -> bf16 */
+  ATTN_KERNEL_BWD_DQ_CONVERT = 4,  /* fp32 dQ accumulator -> bf16; split dK/dV combine */
   ATTN_KERNEL_CLASSES = 5
 };
 int attn_timing_enable(int on);

@@ -75,17 +75,22 @@ float resolve_scale(float scale, int d_qk) {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t nlse2, dsum, dq_acc, total;
+  size_t nlse2, dsum, dq_acc, dk_part, dv_part, total;
+  int ns;  // query-head splits of the kv kernel
 };
 
-WsLayout ws_layout(int B, int S_q, int H_q, int d_qk, bool need_dq_acc) {
+WsLayout ws_layout(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, bool need_dq_acc) {
   const size_t s_pad = (static_cast<size_t>(S_q) + 127) / 128 * 128;
   const size_t rows = static_cast<size_t>(B) * H_q * s_pad;
   WsLayout w;
   w.nlse2 = 0;
   w.dsum = round256(rows * sizeof(float));
   w.dq_acc = w.dsum + round256(rows * sizeof(float));
-  w.total = w.dq_acc + (need_dq_acc ? round256(static_cast<size_t>(B) * S_q * H_q * d_qk * sizeof(float)) : 0);
+  w.dk_part = w.dq_acc + (need_dq_acc ? round256(static_cast<size_t>(B) * S_q * H_q * d_qk * sizeof(float)) : 0);
+  w.ns = S_q > 0 && S_kv > 0 ? sdpa::bwd_kv_head_splits(B, S_kv, H_kv, H_q / H_kv) : 1;
+  const size_t kv_rows = static_cast<size_t>(w.ns > 1 ? w.ns : 0) * B * S_kv * H_kv;
+  w.dv_part = w.dk_part + round256(kv_rows * d_qk * sizeof(float));
+  w.total = w.dv_part + round256(kv_rows * d_v * sizeof(float));
   return w;
 }
 
@@ -215,7 +220,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int deterministic) {
   if (check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, 1, -1, 0, nullptr) != ATTN_OK) return 0;
-  return ws_layout(B, S_q, H_q, d_qk, use_fused_dq(d_qk, d_v, deterministic)).total;
+  return ws_layout(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, use_fused_dq(d_qk, d_v, deterministic)).total;
 }
 
 int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -240,7 +245,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
       (reinterpret_cast<uintptr_t>(d_offset) & 3u))
     return ATTN_ERR_MISALIGNED;
   const bool fused = use_fused_dq(d_qk, d_v, deterministic);
-  const WsLayout w = ws_layout(B, S_q, H_q, d_qk, fused);
+  const WsLayout w = ws_layout(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, fused);
   if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_WORKSPACE;
   int* err = device_error_ptr();
@@ -277,6 +282,9 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
+  p.ns = w.ns;
+  p.dk_part = w.ns > 1 ? reinterpret_cast<float*>(ws + w.dk_part) : nullptr;
+  p.dv_part = w.ns > 1 ? reinterpret_cast<float*>(ws + w.dv_part) : nullptr;
   p.err = err;
 
   const int n_pre = 1 + (softmax_type == ATTN_SOFTMAX_LEARNABLE ? 1 : 0);
@@ -310,6 +318,11 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("backward kv kernel launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  if (p.ns > 1 &&
+      timed(ATTN_KERNEL_BWD_DQ_CONVERT, 1, s, [&] { return sdpa::launch_bwd_kv_combine(d_qk, d_v, p, s); }) != 0) {
+    set_error("dK/dV split combine launch", cudaGetLastError());
     return ATTN_ERR_CUDA;
   }
   if (fused) {

@@ -145,6 +145,8 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = nullptr;
+  p.ns = 1;  // no scratch for split partials: one CTA per (kv tile, kv head)
+  p.dk_part = p.dv_part = nullptr;
   p.seq_q = nullptr;
   p.seq_kv = nullptr;
   p.err = err;

@@ -211,12 +211,14 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   // start in index order, so the long blocks of every chunk start early while the
   // chunk's queries stay few enough to be shared in L2.
   const int n_kv = (p.S_kv + C::BN - 1) / C::BN;
-  const int n_gr = p.H_kv * p.B;
+  const int n_gr = p.H_kv * p.B * p.ns;  // group = (b, kv head, head split)
   const int per_chunk = kKvChunk * n_kv;
   const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
   const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
   const int g = chunk * kKvChunk + within % csize;
-  const int hk = g % p.H_kv, b = g / p.H_kv;
+  const int split = g % p.ns, hk = (g / p.ns) % p.H_kv, b = g / (p.ns * p.H_kv);
+  const int Gs = p.G / p.ns;               // query heads this CTA walks
+  const int h0 = hk * p.G + split * Gs;    // the first of them
   const int n0 = (within / csize) * C::BN;
   const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
                                       p.window}
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   int ilo = 0, ihi = -1;
   const bool any_q = q_tile_range(mask, n0, n0 + C::BN - 1, C::BQ, &ilo, &ihi);
   const int nq = any_q ? ihi - ilo + 1 : 0;
-  const int nsteps = nq * p.G;
+  const int nsteps = nq * Gs;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       for (int s = 0; s < nsteps; ++s) {
         const int st = s % C::NQ;
         if (!mbar_wait(&q_empty[st], ((s / C::NQ) & 1) ^ 1, err, kKvQEmpty)) break;
-        const int h = hk * p.G + s / nq;
+        const int h = h0 + s / nq;
         const int q0 = (ilo + s % nq) * C::BQ;
         mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE);
         for (int c = 0; c < C::QCH; ++c)
@@ -481,8 +483,12 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       const int ncols = w == 0 ? D_V : D_QK;
       const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
       const float mul = w == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst = w == 0 ? p.dv + (((size_t)b * p.S_kv + krow) * p.H_kv + hk) * D_V
-                                  : p.dk + (((size_t)b * p.S_kv + krow) * p.H_kv + hk) * D_QK;
+      const size_t row = ((size_t)b * p.S_kv + krow) * p.H_kv + hk;
+      __nv_bfloat16* dst = w == 0 ? p.dv + row * D_V : p.dk + row * D_QK;
+      // with head splits this CTA's sum is one fp32 partial slice
+      float* part = p.ns == 1 ? nullptr
+                              : (w == 0 ? p.dv_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_V
+                                        : p.dk_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_QK);
 #pragma unroll 1
       for (int c0 = 0; c0 < ncols; c0 += 32) {
         uint32_t rr[32];
@@ -492,6 +498,16 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) rr[c] = 0u;
+        }
+        if (part) {
+          if (row_ok) {
+            float4* f4 = reinterpret_cast<float4*>(part + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              f4[q] = make_float4(__uint_as_float(rr[4 * q]) * mul, __uint_as_float(rr[4 * q + 1]) * mul,
+                                  __uint_as_float(rr[4 * q + 2]) * mul, __uint_as_float(rr[4 * q + 3]) * mul);
+          }
+          continue;
         }
         uint32_t pw[16];
 #pragma unroll
@@ -518,7 +534,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       const bool got = mbar_wait(dq_ready, s & 1, err, kKvDQReady);
       if (!bar_red_and(1, 128, got)) break;  // uniform over the 128 drain threads
       tc_fence_after();
-      const int h = hk * p.G + s / nq;
+      const int h = h0 + s / nq;
       const int q0 = (ilo + s % nq) * C::BQ;
       uint32_t ra[32], rb[32];
       tmem_ld32(lane_addr + C::COL_DQ, ra);
@@ -564,7 +580,7 @@ static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true>
                                     : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B;
+  const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
   kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
@@ -909,6 +925,39 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
   if (d_qk == 64 && d_v == 128) return launch_q_t<64, 128>(tq, tk, tv, tdo, p, stream);
   if (d_qk == 192 && d_v == 64) return launch_q_t<192, 64>(tq, tk, tv, tdo, p, stream);
   return -2;
+}
+
+int bwd_kv_head_splits(int B, int S_kv, int H_kv, int G) {
+  const long long ctas = (long long)((S_kv + 127) / 128) * H_kv * B;
+  int ns = 1;
+  while (2 * ns <= G && G % (2 * ns) == 0 && ctas * ns < 1024) ns *= 2;
+  return ns;
+}
+
+// dK, dV = bf16(sum over the head splits of the fp32 partial slices), slice 0 first.
+__global__ void __launch_bounds__(256) bwd_kv_combine_kernel(const float4* __restrict__ part,
+                                                             uint2* __restrict__ out, size_t n4, int ns) {
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (size_t)gridDim.x * blockDim.x) {
+    float4 a = part[t];
+    for (int s = 1; s < ns; ++s) {
+      const float4 b = part[(size_t)s * n4 + t];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    out[t] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+  }
+}
+
+int launch_bwd_kv_combine(int d_qk, int d_v, const BwdParams& p, cudaStream_t stream) {
+  const size_t rows = (size_t)p.B * p.S_kv * p.H_kv;
+  for (int w = 0; w < 2; ++w) {
+    const size_t n4 = rows * (w == 0 ? d_qk : d_v) / 4;
+    if (n4 == 0) continue;
+    const unsigned blocks = (unsigned)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
+    bwd_kv_combine_kernel<<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(w == 0 ? p.dk_part : p.dv_part),
+        reinterpret_cast<uint2*>(w == 0 ? p.dk : p.dv), n4, p.ns);
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 // =============================================================================

@@ -42,6 +42,9 @@ struct BwdParams {
   __nv_bfloat16* dq;          // [B, S_q, H_q, d_qk]
   __nv_bfloat16* dk;          // [B, S_kv, H_kv, d_qk]
   __nv_bfloat16* dv;          // [B, S_kv, H_kv, d_v]
+  int ns;                     // query-head splits of the kv kernel (1: a CTA walks every head of its group)
+  float* dk_part;             // ns > 1: [ns, B, S_kv, H_kv, d_qk] fp32 partial dK (scaled), one slice per split
+  float* dv_part;             // ns > 1: [ns, B, S_kv, H_kv, d_v] fp32 partial dV
   float* dq_acc;              // [B, S_q, H_q, d_qk] fp32 workspace (atomic dQ path) or null
   int* err;
 };
@@ -51,6 +54,12 @@ int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
                   cudaStream_t stream);
+// Query-head splits of the kv kernel for these sizes: halves each CTA's head loop
+// while the grid has fewer than 1024 CTAs (few kv heads, as with MQA), so that no
+// single CTA outlasts the rest; 1 = no split.
+int bwd_kv_head_splits(int B, int S_kv, int H_kv, int G);
+// ns > 1: dK, dV (bf16) = the sum of the ns fp32 partial slices, in slice order.
+int launch_bwd_kv_combine(int d_qk, int d_v, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);

@@ -78,7 +78,12 @@ def test_bwd_workspace_and_validation(lib):
     rows = 4 * 32 * 2048
     assert det == 2 * rows * 4                          # lse2 + D, fp32
     assert atom == det + 4 * 2048 * 32 * 128 * 4        # + fp32 dQ accumulator
-    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4
+    # B=1, S=100, H_kv=2: 2 kv CTAs, so the 2 query heads of each group go to 2 CTAs
+    # and the workspace adds 2 fp32 partial slices of dK and dV
+    part = 2 * 1 * 100 * 2 * 64 * 4
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4 + 2 * part
+    # MHA has no head loop to split
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 4, 64, 64, True) == 2 * 4 * 128 * 4
     assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 3, 64, 64, True) == 0
 
     def bwd(ws=P, ws_bytes=1 << 30, q=P, Hq=4, Hkv=2, st=0, doff=None, off=None, window=-1, causal=1):

@@ -30,6 +30,8 @@ CASES = [
     ("d128_64_obo", Shape(2, 260, 260, 2, 1, 128, 64), True, -1, OFF_BY_ONE, None),
     ("long_window_multi_tile", Shape(1, 700, 700, 2, 1, 128, 128), True, 300, LEARNABLE, 0.09),
     ("large_logits_obo", Shape(1, 260, 260, 2, 1, 64, 64), True, -1, OFF_BY_ONE, 1.0),
+    # 32 query heads on one kv head, 3 kv tiles: each CTA walks a single head
+    ("mqa_g32_one_head_per_cta", Shape(1, 300, 300, 32, 1, 64, 64), True, -1, LEARNABLE, None),
 ]
 
 
