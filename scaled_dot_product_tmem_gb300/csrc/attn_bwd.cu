@@ -928,9 +928,11 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
 }
 
 int bwd_kv_head_splits(int B, int S_kv, int H_kv, int G) {
+  constexpr long long kSms = 152;  // GB300
   const long long ctas = (long long)((S_kv + 127) / 128) * H_kv * B;
   int ns = 1;
-  while (2 * ns <= G && G % (2 * ns) == 0 && ctas * ns < 1024) ns *= 2;
+  if (ctas >= 3 * kSms) return ns;  // enough CTAs: the split's fp32 partials cost more than they balance
+  while (2 * ns <= G && G % (2 * ns) == 0 && ctas * ns < 6 * kSms) ns *= 2;
   return ns;
 }
 

@@ -54,9 +54,9 @@ int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
                   cudaStream_t stream);
-// Query-head splits of the kv kernel for these sizes: halves each CTA's head loop
-// while the grid has fewer than 1024 CTAs (few kv heads, as with MQA), so that no
-// single CTA outlasts the rest; 1 = no split.
+// Query-head splits of the kv kernel for these sizes: a grid of fewer than 3 CTAs
+// per SM (few kv heads, as with MQA) is bound by its longest CTA, so each CTA's
+// head loop is halved until the grid has 6 CTAs per SM; 1 = no split.
 int bwd_kv_head_splits(int B, int S_kv, int H_kv, int G);
 // ns > 1: dK, dV (bf16) = the sum of the ns fp32 partial slices, in slice order.
 int launch_bwd_kv_combine(int d_qk, int d_v, const BwdParams& p, cudaStream_t stream);

@@ -82,6 +82,10 @@ def test_bwd_workspace_and_validation(lib):
     # and the workspace adds 2 fp32 partial slices of dK and dV
     part = 2 * 1 * 100 * 2 * 64 * 4
     assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4 + 2 * part
+    # MQA at 32,768 tokens: 256 kv CTAs (under 3 per SM) -> 4 splits, 1024 CTAs
+    mqa = sdpa.attn_bwd_workspace_size(4, 8192, 8192, 32, 1, 128, 128, True)
+    assert mqa == 2 * 4 * 32 * 8192 * 4 + 2 * 4 * (4 * 8192 * 1 * 128 * 4)
+    # GQA B=4 S=2048 H_kv=8: 512 CTAs, no split (checked above: det has no partials)
     # MHA has no head loop to split
     assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 4, 64, 64, True) == 2 * 4 * 128 * 4
     assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 3, 64, 64, True) == 0
