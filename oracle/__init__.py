@@ -16,6 +16,9 @@ Definitions followed (see ``oracle.c`` for the full statement):
     sink softmax types);
   * "[JAX] Add support for sink attention in JAX #2225", Greptile summaries and
     the review thread on the off-by-one offset (vanilla / off-by-one / learnable).
+
+``oracle.fp8`` adds the E4M3 codec, per-tensor quantisation and the FP8 forward
+(codelab step 10, "Inspect the FP8 path") in numpy.
 """
 from __future__ import annotations
 
