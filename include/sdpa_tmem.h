@@ -182,7 +182,49 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void);
 const char* attn_bwd_noalloc_message(void);
 
 /*
- * Measurement aid (off by default).  While enabled, attn_fwd and attn_bwd record
+ * FP8 (E4M3) forward.  Source: "Speed up attention on GPU with cuDNN and
+ * TransformerEngine", step 10 ("Benchmark NVIDIA TransformerEngine and FP8"),
+ * section "Inspect the FP8 path": the forward runs on E4M3 tensors (4 exponent,
+ * 3 mantissa bits) with per-tensor scaling factors from the absolute maximum
+ * (DelayedScaling, margin 0); the output stays bf16.
+ *
+ * E4M3 here is the OCP 8-bit float: bias 7, no infinities, largest finite 448;
+ * conversions round to nearest even and saturate to +-448.  All scalars below
+ * (amax, descale) are single fp32 values in DEVICE memory, so a step needs no
+ * host synchronisation.
+ *
+ * attn_fp8_amax: amax[0] = max |x| over n bf16 values at x (16-byte aligned).
+ *   A caller with an amax history writes the history's max into amax instead.
+ * attn_fp8_quantize: scale = 448 / amax[0] (1 when amax is 0 or not finite);
+ *   x8 = E4M3(fp32(x) * scale) and descale[0] = 1 / scale (fp32, correctly
+ *   rounded).  x is bf16 BSHD [B, S, H, d].  transpose = 0: x8 has the same
+ *   layout; transpose = 1 (d = 64 or 128): x8 is [B, H, d, S_pad], keys
+ *   innermost, S_pad = attn_fp8_vt_row_bytes(S), zeros past S — the layout
+ *   attn_fwd_fp8 takes V in.  x and x8 16-byte aligned.
+ * attn_fwd_fp8: O (bf16 BSHD [B, S_q, H_q, d]) and LSE (fp32 [B, H_q, S_q]) of
+ *   softmax(scale * Q K^T) V over the dequantised tensors Q = q8 * descale_q,
+ *   K = k8 * descale_k, V = vt8 * descale_v, with the same masks, grouped heads
+ *   and sink types as attn_fwd.  q8 [B, S_q, H_q, d], k8 [B, S_kv, H_kv, d]
+ *   E4M3 BSHD; vt8 [B, H_kv, d, S_pad] from attn_fp8_quantize(transpose = 1).
+ *   d = d_qk = d_v in {64, 128}.  The kernel rounds the softmax numerators to
+ *   E4M3 for the P.V product while the normaliser and the LSE use their fp32
+ *   values; the departure from the exact O this causes is bounded per row by
+ *   2^-4 * sum_j P_j |v_j| + sum_j min(2^-10 * e^(M - LSE), P_j) |v_j|
+ *   (P_j the probabilities, M the row's largest logit or sink).
+ * Errors as attn_fwd; d outside {64, 128} is ATTN_ERR_UNSUPPORTED.
+ */
+int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream);
+int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                      float* descale, void* stream);
+/* Row length in bytes of the transposed E4M3 V: S rounded up to a multiple of 16. */
+int attn_fp8_vt_row_bytes(int S);
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,
+                 const float* descale_v, void* o, float* lse, int B, int S_q, int S_kv, int H_q, int H_kv, int d,
+                 float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* stream);
+
+/*
+ * Measurement aid (off by default).  While enabled, the attn_fwd*, attn_bwd* and
+ * attn_fp8_* calls record
  * a pair of CUDA events on their launch stream around each class of kernel they
  * enqueue.  attn_timing_read() waits for those events, writes per class the
  * summed milliseconds (ms[k]) and the number of kernels launched (launches[k])
@@ -195,7 +237,8 @@ enum {
   ATTN_KERNEL_BWD_KV = 2,          /* kv-stationary dK/dV (+ atomic dQ) kernel */
   ATTN_KERNEL_BWD_Q = 3,           /* query-stationary deterministic dQ kernel */
   ATTN_KERNEL_BWD_DQ_CONVERT = 4,  /* fp32 dQ accumulator -> bf16; split dK/dV combine */
-  ATTN_KERNEL_CLASSES = 5
+  ATTN_KERNEL_FP8_QUANT = 5,       /* E4M3 amax and quantisation */
+  ATTN_KERNEL_CLASSES = 6
 };
 int attn_timing_enable(int on);
 int attn_timing_read(double* ms, int* launches, int n);

@@ -109,7 +109,7 @@ def attention_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, *, causal=Tru
 
 
 def p_rounding_bound(q, k, v, lse, *, causal=True, window=-1, scale=None, softmax_type=VANILLA,
-                     offset=None):
+                     offset=None, rows=None):
     """Per-row bound [B,Hq,Sq] on |O_rounded - O| when the softmax numerators are
     rounded to E4M3 before the P.V product while the denominator keeps them exact.
 
@@ -120,7 +120,8 @@ def p_rounding_bound(q, k, v, lse, *, causal=True, window=-1, scale=None, softma
     rounds to 0).  Divided by l', per output element that is at most
         2^-4 * sum_j P_j |v_j| + sum_j min(2^-10 * exp(M - lse), P_j) |v_j|
     with P_j = exp(s_j - lse) the exact probabilities of the visible keys.  The
-    bound is returned per row as the max over the head dim.
+    bound is returned per row as the max over the head dim; ``rows`` (query indices)
+    restricts it to those rows, in that order.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -129,14 +130,17 @@ def p_rounding_bound(q, k, v, lse, *, causal=True, window=-1, scale=None, softma
     _, Skv, Hkv, dv = v.shape
     G = Hq // Hkv
     sc = (1.0 / np.sqrt(dqk)) if scale is None else float(scale)
-    i = np.arange(Sq)[:, None]  # query i sees keys j <= i (causal), j >= i - window
+    rows = np.arange(Sq) if rows is None else np.asarray(rows)
+    q = q[:, rows]
+    lse = np.asarray(lse)[:, :, rows]
+    i = rows[:, None]  # query i sees keys j <= i (causal), j >= i - window
     j = np.arange(Skv)[None, :]
-    vis = np.ones((Sq, Skv), dtype=bool)
+    vis = np.ones((len(rows), Skv), dtype=bool)
     if causal:
         vis &= j <= i
     if window >= 0:
         vis &= j >= i - window
-    out = np.zeros((B, Hq, Sq))
+    out = np.zeros((B, Hq, len(rows)))
     for b in range(B):
         for h in range(Hq):
             s = np.where(vis, sc * q[b, :, h, :] @ k[b, :, h // G, :].T, -np.inf)

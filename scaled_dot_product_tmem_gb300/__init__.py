@@ -75,6 +75,14 @@ def _load():
     lib.attn_timing_read.restype = i
     lib.attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.attn_last_device_error.restype = i
+    lib.attn_fp8_amax.argtypes = [vp, sz, vp, vp]
+    lib.attn_fp8_amax.restype = i
+    lib.attn_fp8_quantize.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp]
+    lib.attn_fp8_quantize.restype = i
+    lib.attn_fp8_vt_row_bytes.argtypes = [i]
+    lib.attn_fp8_vt_row_bytes.restype = i
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp, vp]
+    lib.attn_fwd_fp8.restype = i
     _lib = lib
     return lib
 
@@ -216,7 +224,7 @@ def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal
         raise AttnError(st, "attn_bwd_noalloc" + (f" ({msg})" if msg else ""))
 
 
-KERNEL_CLASSES = ("fwd", "bwd_preprocess", "bwd_kv", "bwd_q", "bwd_dq_convert")
+KERNEL_CLASSES = ("fwd", "bwd_preprocess", "bwd_kv", "bwd_q", "bwd_dq_convert", "fp8_quantize")
 
 
 def attn_timing_enable(on: bool = True) -> None:
@@ -232,6 +240,98 @@ def attn_timing_read():
     if st != ATTN_OK:
         raise AttnError(st, "attn_timing_read")
     return {name: (ms[k], cnt[k]) for k, name in enumerate(KERNEL_CLASSES)}
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) forward
+
+
+def attn_fp8_vt_row_bytes(S: int) -> int:
+    return int(_load().attn_fp8_vt_row_bytes(int(S)))
+
+
+def attn_fp8_amax(x, amax, *, stream=None):
+    """amax (fp32 [1], device) = max |x| over the bf16 tensor x."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
+        raise TypeError("x must be a contiguous bf16 CUDA tensor")
+    _check(amax, "amax", torch.float32, 1)
+    st = _load().attn_fp8_amax(_ptr(x), x.numel(), _ptr(amax), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fp8_amax")
+
+
+def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, stream=None):
+    """x8 (uint8 E4M3) = E4M3(x * 448 / amax); descale (fp32 [1]) = amax / 448 as 1 / scale.
+
+    x bf16 BSHD [B,S,H,d]; x8 the same shape, or [B,H,d,S_pad] with transpose=True."""
+    _check(x, "x", torch.bfloat16, 4)
+    _check(x8, "x8", torch.uint8, 4)
+    _check(amax, "amax", torch.float32, 1)
+    _check(descale, "descale", torch.float32, 1)
+    B, S, H, d = x.shape
+    want = (B, H, d, attn_fp8_vt_row_bytes(S)) if transpose else (B, S, H, d)
+    if tuple(x8.shape) != want:
+        raise ValueError(f"x8 must have shape {want}, got {tuple(x8.shape)}")
+    st = _load().attn_fp8_quantize(_ptr(x), _ptr(x8), B, S, H, d, int(bool(transpose)), _ptr(amax), _ptr(descale),
+                                   _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fp8_quantize")
+
+
+def attn_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, *, causal=True, window=-1,
+                 softmax_type=VANILLA, softmax_offset=None, scale=0.0, stream=None):
+    """E4M3 forward into preallocated o [B,S_q,H_q,d] bf16 and lse [B,H_q,S_q] fp32.
+
+    q8 [B,S_q,H_q,d], k8 [B,S_kv,H_kv,d] uint8 E4M3 BSHD; vt8 [B,H_kv,d,S_pad] from
+    attn_fp8_quantize(transpose=True); descale_* fp32 [1] device tensors."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        _check(t, n, torch.uint8, 4)
+    for t, n in ((descale_q, "descale_q"), (descale_k, "descale_k"), (descale_v, "descale_v")):
+        _check(t, n, torch.float32, 1)
+    _check(o, "o", torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    if softmax_offset is not None:
+        _check(softmax_offset, "softmax_offset", torch.float32, 1)
+    B, S_q, H_q, d = q8.shape
+    _, S_kv, H_kv, _ = k8.shape
+    if tuple(vt8.shape) != (B, H_kv, d, attn_fp8_vt_row_bytes(S_kv)):
+        raise ValueError(f"vt8 must have shape {(B, H_kv, d, attn_fp8_vt_row_bytes(S_kv))}, got {tuple(vt8.shape)}")
+    st = _load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(descale_q), _ptr(descale_k), _ptr(descale_v),
+                              _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d, float(scale or 0.0),
+                              int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset),
+                              _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
+
+
+def fp8_quantize(x, *, transpose=False, amax=None, stream=None):
+    """Per-tensor E4M3 quantisation of a bf16 BSHD tensor: returns (x8, amax, descale).
+
+    amax: an fp32 [1] device tensor holding the scaling statistic (for example the
+    max of an amax history); None computes this tensor's own amax."""
+    B, S, H, d = x.shape
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+        attn_fp8_amax(x, amax, stream=stream)
+    shape = (B, H, d, attn_fp8_vt_row_bytes(S)) if transpose else (B, S, H, d)
+    x8 = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    attn_fp8_quantize(x, x8, amax, descale, transpose=transpose, stream=stream)
+    return x8, amax, descale
+
+
+def sdpa_forward_fp8(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
+                     stream=None):
+    """bf16 in, bf16 out through the E4M3 forward: quantise Q, K (BSHD) and V
+    (transposed) with their own amax, then run attn_fwd_fp8.  Returns (o, lse)."""
+    q8, _, dq = fp8_quantize(q, stream=stream)
+    k8, _, dk = fp8_quantize(k, stream=stream)
+    vt8, _, dv = fp8_quantize(v, transpose=True, stream=stream)
+    B, S_q, H_q, d = q.shape
+    o = torch.empty((B, S_q, H_q, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H_q, S_q), dtype=torch.float32, device=q.device)
+    attn_fwd_fp8(q8, k8, vt8, dq, dk, dv, o, lse, causal=causal, window=window, softmax_type=softmax_type,
+                 softmax_offset=softmax_offset, scale=scale, stream=stream)
+    return o, lse
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -355,6 +355,97 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
                          workspace_bytes, stream);
 }
 
+int attn_fp8_vt_row_bytes(int S) { return S <= 0 ? 0 : (S + 15) / 16 * 16; }
+
+int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream) {
+  if (!amax || (n > 0 && !x)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax) & 3u)) return ATTN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (timed(ATTN_KERNEL_FP8_QUANT, n > 0 ? 1 : 0, s, [&] {
+        return sdpa::launch_fp8_amax(static_cast<const __nv_bfloat16*>(x), n, amax, s);
+      }) != 0) {
+    set_error("fp8 amax launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                      float* descale, void* stream) {
+  if (B < 0 || S < 0 || H <= 0 || d <= 0 || d % 8 != 0 || !amax || !descale) return ATTN_ERR_INVALID_ARG;
+  if (transpose && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((size_t)B * S * H * d > 0 && (!x || !x8)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
+      (reinterpret_cast<uintptr_t>(descale) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  if ((size_t)B * S * H * d == 0) return ATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = timed(ATTN_KERNEL_FP8_QUANT, 1, s, [&] {
+    return sdpa::launch_fp8_quantize(static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(x8), B, S, H, d,
+                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, s);
+  });
+  if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+  if (rc != 0) {
+    set_error("fp8 quantize launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,
+                 const float* descale_v, void* o, float* lse, int B, int S_q, int S_kv, int H_q, int H_kv, int d,
+                 float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* stream) {
+  int st = check_common(B, S_q, S_kv, H_q, H_kv, d, d, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || S_q == 0) return ATTN_OK;
+  if (!q8 || !o || !lse || !descale_q || !descale_k || !descale_v || (S_kv > 0 && (!k8 || !vt8)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(descale_q) & 3u) ||
+      (reinterpret_cast<uintptr_t>(descale_k) & 3u) || (reinterpret_cast<uintptr_t>(descale_v) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  int* err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  // TMA maps need a non-empty tensor; with S_kv == 0 no kv tile is ever loaded.
+  const int skv_map = S_kv > 0 ? S_kv : 1;
+  const void* kk = S_kv > 0 ? k8 : q8;
+  CUtensorMap tq, tk, tv;
+  bool ok = sdpa::make_bshd_map_e4m3(&tq, q8, B, S_q, H_q, d, 128) &&
+            sdpa::make_bshd_map_e4m3(&tk, kk, B, skv_map, S_kv > 0 ? H_kv : H_q, d, 128);
+  if (S_kv > 0)
+    ok = ok && sdpa::make_vt_map_e4m3(&tv, vt8, B, S_kv, attn_fp8_vt_row_bytes(S_kv), H_kv, d);
+  else
+    tv = tk;
+  if (!ok) {
+    set_error("cuTensorMapEncodeTiled (fp8 forward operands)");
+    return ATTN_ERR_CUDA;
+  }
+  sdpa::FwdParams p;
+  p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
+  p.scale_log2 = resolve_scale(scale, d) * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.window = window < 0 ? -1 : window;
+  p.softmax_type = softmax_type;
+  p.offset = softmax_offset;
+  p.seq_q = nullptr;
+  p.seq_kv = nullptr;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = err;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] { return sdpa::launch_attn_fwd_fp8(d, tq, tk, tv, p, s); });
+  if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+  if (rc != 0) {
+    set_error("fp8 forward kernel launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
 int attn_timing_enable(int on) {
   std::lock_guard<std::mutex> g(g_timing_mu);
   g_timing_on = on != 0;

@@ -25,6 +25,15 @@
 //                    shared memory, MN-major).
 //   warp 9           one thread issues the TMA loads: Q once, then K / V rings.
 // TMEM (512 columns): S_t / P_t at t*256, O_t at t*256 + 128.
+//
+// E4M3 instantiation (F8): Q, K and V arrive as per-tensor-scaled E4M3 bytes (V
+// transposed to [B, H_kv, d, S], keys innermost, so both GEMMs read K-major
+// operands); S and P.V run as tcgen05.mma kind::f8f6f4 (K = 32 per instruction).
+// The scores are rescaled by descale_q * descale_k with the softmax scale; P is
+// rounded to E4M3 (values <= 2^8 under the lazy rescale, inside E4M3's range)
+// while the row sum keeps the fp32 values; O is multiplied by descale_v / l.
+// Source for the FP8 forward: "Speed up attention on GPU with cuDNN and
+// TransformerEngine", step 10, section "Inspect the FP8 path".
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
@@ -33,14 +42,17 @@
 
 namespace sdpa {
 
-template <int D_QK, int D_V, int NK, int NV>
+template <int D_QK, int D_V, int NK, int NV, bool F8 = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
-  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
-  static constexpr int CHUNK = 128 * 128;  // one 128-row x 64-col bf16 box
+  // bf16: boxes of 64 head dims (one 128-byte swizzle row each); E4M3: one box of
+  // the whole head dim (64 or 128 bytes per row), and V^T boxes of d rows x 128 keys
+  static constexpr int QCH = F8 ? 1 : D_QK / 64, VCH = F8 ? 1 : D_V / 64;
+  static constexpr int CHUNK = F8 ? 128 * D_QK : 128 * 128;
   static constexpr int Q_TILE = QCH * CHUNK;
   static constexpr int K_STAGE = QCH * CHUNK;
-  static constexpr int V_STAGE = VCH * CHUNK;
+  static constexpr int V_STAGE = F8 ? D_V * 128 : VCH * CHUNK;
+  static_assert(!F8 || (D_QK == D_V && (D_QK == 64 || D_QK == 128)), "E4M3 head dims");
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
@@ -49,7 +61,9 @@ struct FwdCfg {
   // q_empty
   static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 8;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
+  static constexpr int SMEM_USED = OFF_TMEM_SLOT + 16 + 1024;
+  // at least 117 KB so that one CTA per SM holds the 512 TMEM columns
+  static constexpr int SMEM = SMEM_USED > 117 * 1024 ? SMEM_USED : 117 * 1024;
   static constexpr int THREADS = 320;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SMEM > 116 * 1024, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
@@ -92,11 +106,11 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi)
 
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
 
-template <int D_QK, int D_V, int NK, int NV, bool VL>
+template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D_QK, D_V, NK, NV>;
+  using C = FwdCfg<D_QK, D_V, NK, NV, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -174,9 +188,13 @@ __global__ void __launch_bounds__(320, 1)
           ok = mbar_wait(&v_empty[sv], ((n / NV) & 1) ^ 1, err, kSiteVEmpty);
           if (!ok) break;
           mbar_arrive_expect_tx(&v_full[sv], C::V_STAGE);
-          for (int c = 0; c < C::VCH; ++c)
-            tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE + c * C::CHUNK, &tmV, &v_full[sv], c * 64, T.hk,
-                        j * C::BN, T.b);
+          if constexpr (F8) {  // V^T: keys innermost
+            tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE, &tmV, &v_full[sv], j * C::BN, 0, T.hk, T.b);
+          } else {
+            for (int c = 0; c < C::VCH; ++c)
+              tma_load_4d(smem + C::OFF_V + sv * C::V_STAGE + c * C::CHUNK, &tmV, &v_full[sv], c * 64, T.hk,
+                          j * C::BN, T.b);
+          }
         }
       }
       // Drain: every load issued must have landed before the CTA can exit.
@@ -196,26 +214,47 @@ __global__ void __launch_bounds__(320, 1)
     // PV_1(j), S_1(j+1): each tile's softmax overlaps the other tile's GEMMs.  The
     // first S of the next work tile follows the last PV of this one, so it runs
     // while the softmax warps write this tile's output.
-    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idO = idesc_bf16_f32(128, D_V, false, true);
+    constexpr uint32_t idS = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idO = F8 ? idesc_e4m3_f32(128, D_V) : idesc_bf16_f32(128, D_V, false, true);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
     auto issue_S = [&](int t, int stage) {
-      const uint64_t dq = smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024);
-      const uint64_t dk = smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024);
+      if constexpr (F8) {
+        // rows of D_QK bytes: 128-byte swizzle for d = 128, 64-byte for d = 64
+        const uint64_t dq = D_QK == 128 ? smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024)
+                                        : smem_desc_sw64(sQ + t * C::Q_TILE, 16, 512);
+        const uint64_t dk = D_QK == 128 ? smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024)
+                                        : smem_desc_sw64(sK + stage * C::K_STAGE, 16, 512);
 #pragma unroll
-      for (int kk = 0; kk < D_QK / 16; ++kk) {
-        const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-        mma_ss_warp(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
+        for (int kk = 0; kk < D_QK / 32; ++kk)
+          mma_ss_f8_warp(tmem + t * 256, desc_add(dq, kk * 32), desc_add(dk, kk * 32), idS, kk > 0);
+      } else {
+        const uint64_t dq = smem_desc_sw128(sQ + t * C::Q_TILE, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(sK + stage * C::K_STAGE, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D_QK / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_ss_warp(tmem + t * 256, desc_add(dq, off), desc_add(dk, off), idS, kk > 0);
+        }
       }
     };
     auto issue_PV = [&](int t, int stage, bool acc) {
-      const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
+      if constexpr (F8) {
+        // P: 4 E4M3 per TMEM column (32 keys = 8 columns per MMA); V^T: K-major rows of
+        // 128 keys
+        const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < C::BN / 16; ++kk)
-        mma_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
-                    (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BN / 32; ++kk)
+          mma_ts_f8_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 32), idO,
+                         (acc || kk > 0) ? 1u : 0u);
+      } else {
+        const uint64_t dv = smem_desc_sw128(sV + stage * C::V_STAGE, C::CHUNK, 1024);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc_add(dv, kk * 2048), idO,
+                      (acc || kk > 0) ? 1u : 0u);
+      }
     };
     int n = 0, nw = 0;      // kv stages consumed, Q tiles consumed
     int pc[2] = {0, 0};     // p_ready phases consumed per query tile
@@ -276,7 +315,10 @@ __global__ void __launch_bounds__(320, 1)
     const int r = (warp % 4) * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const uint32_t colS = t * 256, colO = t * 256 + 128;
-    const float sl2 = p.scale_log2;
+    // E4M3: the MMA sums products of the stored codes; the per-tensor descales
+    // bring the scores and O back to the real values
+    const float sl2 = F8 ? p.scale_log2 * (*p.descale_q) * (*p.descale_k) : p.scale_log2;
+    const float o_mul = F8 ? *p.descale_v : 1.f;
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
     bool ok = true;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
@@ -363,15 +405,28 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t pk[16];
+            float pf[32];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               float xa, xb;
               f2_unpack(f2_fma(f2_pack(s[c0 + 2 * c], s[c0 + 2 * c + 1]), sl2x2, negm2), xa, xb);
               const float a = ex2(xa), bq = ex2(xb);
               ls2[c % 4] = f2_add(ls2[c % 4], f2_pack(a, bq));
-              pk[c] = pack_bf16x2(a, bq);
+              if constexpr (F8) {
+                pf[2 * c] = a;
+                pf[2 * c + 1] = bq;
+              } else {
+                pk[c] = pack_bf16x2(a, bq);
+              }
             }
-            tmem_st16(lane_addr + colS + c0 / 2, pk);
+            if constexpr (F8) {
+              uint32_t p8[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) p8[q] = pack_e4m3x4(pf[4 * q], pf[4 * q + 1], pf[4 * q + 2], pf[4 * q + 3]);
+              tmem_st8(lane_addr + colS + c0 / 4, p8);
+            } else {
+              tmem_st16(lane_addr + colS + c0 / 2, pk);
+            }
           }
           {
             float s0, s1, s2, s3, s4, s5, s6, s7;
@@ -394,7 +449,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
       }
       const bool row_ok = i < p.S_q;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? o_mul / l : 0.f;
       __nv_bfloat16* orow = p.o + (((size_t)b * p.S_q + (row_ok ? i : 0)) * p.H_q + h) * D_V;
 #pragma unroll 1
       for (int c0 = 0; c0 < D_V; c0 += 32) {
@@ -432,11 +487,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D_QK, int D_V, int NK, int NV, bool VL>
+template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false>
 static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                         cudaStream_t stream) {
-  using C = FwdCfg<D_QK, D_V, NK, NV>;
-  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL>;
+  using C = FwdCfg<D_QK, D_V, NK, NV, F8>;
+  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL, F8>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
@@ -473,6 +528,13 @@ int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap&
   // padded batches get the instantiation with the per-entry lengths and row tests
   return (p.seq_q || p.seq_kv) ? launch_attn_fwd_vl<true>(d_qk, d_v, tq, tk, tv, p, stream)
                                : launch_attn_fwd_vl<false>(d_qk, d_v, tq, tk, tv, p, stream);
+}
+
+int launch_attn_fwd_fp8(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                        const FwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_t<128, 128, 3, 3, false, true>(tq, tk, tvt, p, stream);
+  if (d == 64) return launch_fwd_t<64, 64, 6, 6, false, true>(tq, tk, tvt, p, stream);
+  return -2;
 }
 
 }  // namespace sdpa

@@ -17,12 +17,25 @@ struct FwdParams {
   __nv_bfloat16* o;     // [B, S_q, H_q, d_v]
   float* lse;           // [B, H_q, S_q]
   int* err;             // device error word
+  // E4M3 forward only: device scalars that undo the per-tensor scaling of Q, K, V
+  const float* descale_q = nullptr;
+  const float* descale_k = nullptr;
+  const float* descale_v = nullptr;
 };
 
 // Returns 0 on a successful launch, -2 for an unsupported (d_qk, d_v), -1 on a
 // CUDA launch error.
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                     const FwdParams& p, cudaStream_t stream);
+// E4M3 forward, d_qk = d_v = d in {64, 128}; tvt maps V^T [B, H_kv, d, S_kv_pad].
+int launch_attn_fwd_fp8(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                        const FwdParams& p, cudaStream_t stream);
+// amax[0] = max |x| over n bf16 values (amax must be zeroed first).
+int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t stream);
+// x8 = E4M3(x * scale), scale = 448 / amax[0] (1 if amax is 0 or not finite),
+// descale[0] = 1 / scale.  transpose: x [B, S, H, d] -> x8 [B, H, d, S_pad].
+int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
+                        const float* amax, float* descale, cudaStream_t stream);
 
 struct BwdParams {
   int B, S_q, S_kv, H_q, H_kv, G;

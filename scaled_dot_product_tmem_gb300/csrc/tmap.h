@@ -55,6 +55,38 @@ inline bool make_f32_bshd_map(CUtensorMap* m, const void* base, int B, int S, in
   return r == CUDA_SUCCESS;
 }
 
+// An E4M3 BSHD tensor [B, S, H, D] (D = 64 or 128 bytes per row) as a 4-D TMA
+// tensor (d, h, s, b) with a box of the whole head dim x 1 head x `box_rows` rows
+// x 1 batch, swizzled by the row length (128-byte or 64-byte swizzle).
+inline bool make_bshd_map_e4m3(CUtensorMap* m, const void* base, int B, int S, int H, int D, int box_rows) {
+  PFN_encodeTiled enc = get_encode_tiled();
+  if (!enc || (D != 64 && D != 128)) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)H * D, (cuuint64_t)S * H * D};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The transposed E4M3 V [B, H, D, S_pad] (keys innermost, rows S_pad bytes apart)
+// as (s, d, h, b) with a box of 128 keys x D rows x 1 x 1, 128-byte swizzle; keys
+// at or past S read as zeros.
+inline bool make_vt_map_e4m3(CUtensorMap* m, const void* base, int B, int S, int S_pad, int H, int D) {
+  PFN_encodeTiled enc = get_encode_tiled();
+  if (!enc || S_pad % 16 != 0 || S_pad < S) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)S, (cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)S_pad, (cuuint64_t)D * S_pad, (cuuint64_t)H * D * S_pad};
+  cuuint32_t box[4] = {128, (cuuint32_t)D, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A row-major bf16 matrix [rows, cols] as a 2-D TMA tensor with a 64 x box_rows
 // box and 128-byte swizzle.
 inline bool make_2d_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {

@@ -109,3 +109,32 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(sdpa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         sdpa.library()
+
+
+def test_fp8_argument_validation(lib):
+    assert lib.attn_fp8_vt_row_bytes(1) == 16 and lib.attn_fp8_vt_row_bytes(16) == 16
+    assert lib.attn_fp8_vt_row_bytes(2049) == 2064 and lib.attn_fp8_vt_row_bytes(0) == 0
+
+    def f8(q=P, k=P, vt=P, dq=P, dk=P, dv=P, o=P, lse=P, B=1, Sq=64, Skv=64, Hq=4, Hkv=2, d=128, causal=1,
+           window=-1, st=0, off=None):
+        return lib.attn_fwd_fp8(q, k, vt, dq, dk, dv, o, lse, B, Sq, Skv, Hq, Hkv, d, ctypes.c_float(0.0), causal,
+                                window, st, off, None)
+
+    assert f8(d=96) == UNSUPPORTED                      # E4M3 head dims: 64 and 128
+    assert f8(d=192) == UNSUPPORTED
+    assert f8(Hq=3) == INVALID
+    assert f8(dq=None) == INVALID                       # descales are required
+    assert f8(vt=MIS) == MISALIGNED
+    assert f8(dv=ctypes.c_void_p(0x10002)) == MISALIGNED
+    assert f8(B=0) == OK and f8(Sq=0) == OK             # nothing to launch
+
+    def qz(x=P, x8=P, B=1, S=64, H=2, d=128, t=0, amax=P, desc=P):
+        return lib.attn_fp8_quantize(x, x8, B, S, H, d, t, amax, desc, None)
+
+    assert qz(d=96, t=1) == UNSUPPORTED                 # the transposed form: d = 64 or 128
+    assert qz(d=12) == INVALID                          # rows of whole 16-byte chunks
+    assert qz(amax=None) == INVALID
+    assert qz(x8=MIS) == MISALIGNED
+    assert qz(B=0) == OK
+    assert lib.attn_fp8_amax(P, ctypes.c_size_t(8), None, None) == INVALID
+    assert lib.attn_fp8_amax(MIS, ctypes.c_size_t(8), P, None) == MISALIGNED
