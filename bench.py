@@ -4,7 +4,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = attn_fwd + attn_bwd (every step of the hot path) over one batch of
-synthetic BSHD bf16 inputs already resident in HBM.  The default workload is the
+synthetic BSHD bf16 inputs already resident in HBM.  The ``fp8_fwd_*`` workloads
+time the E4M3 forward instead: one step = the per-tensor E4M3 casts of Q, K and V
+(delayed scaling: the scale from the previous step's amax, this step's amax
+recorded during the cast) + attn_fwd_fp8, counted in forward FLOPs.  The default workload is the
 GQA + sliding-window training shape (B=4, S=2048, H_q=32, H_kv=8, d=128, causal,
 left window 1024, vanilla softmax).  FLOPs count only unmasked (query, key)
 pairs: forward 2(d_qk + d_v) per pair, backward 2(3 d_qk + 2 d_v) per pair.
@@ -32,15 +35,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, unmasked FLOPs) and % of GB300 BF16 peak"
+METRIC_FP8 = "attention fwd TFLOP/s (E4M3 Q/K/V with per-tensor scales, bf16 O; unmasked FLOPs)"
+FP8_PER_BF16 = 2.0  # nominal dense E4M3 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s)
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None):
+def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False):
     """A workload; `lens` (one length per batch entry, same for queries and keys) makes
-    it a padded batch run through the varlen entry points."""
+    it a padded batch run through the varlen entry points; `fp8` makes it the E4M3
+    forward."""
     return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
-                scale=scale, seed=seed, desc=desc, lens=lens)
+                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8)
 
 
 WORKLOADS = {
@@ -66,6 +72,13 @@ WORKLOADS["varlen_gqa_b8_s4096"] = _w(
     "varlen_gqa_b8_s4096", 8, 4096, 32, 8, 128, 128, True, -1, 0, None, 5,
     "padded batch: B=8 padded to S=4096, lengths 4096, 3584, ..., 512, H_q=32, H_kv=8, d=128, causal",
     lens=[4096 - 512 * i for i in range(8)])
+# E4M3 forward: the pages' FP8 example shape, and the causal GQA S=8192 point.
+WORKLOADS["fp8_fwd_mha_b4_s2048_d64"] = _w(
+    "fp8_fwd_mha_b4_s2048_d64", 4, 2048, 8, 8, 64, 64, True, -1, 0, None, 41,
+    "E4M3 forward: B=4, S=2048, H=8 (MHA), d=64, causal (the FP8 example's shape)", fp8=True)
+WORKLOADS["fp8_fwd_gqa_b4_s8192_d128"] = _w(
+    "fp8_fwd_gqa_b4_s8192_d128", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 42,
+    "E4M3 forward: B=4, S=8192, H_q=32, H_kv=8, d=128, causal", fp8=True)
 DEFAULT = "gqa_swa_b4_s2048"
 HEADLINE = "sweep_s8192_hkv8"
 
@@ -91,7 +104,7 @@ def total_pairs(wl):
 def flops(wl, part="total"):
     n = wl["Hq"] * total_pairs(wl)
     fwd = n * 2 * (wl["dqk"] + wl["dv"])
-    bwd = n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+    bwd = 0 if wl.get("fp8") else n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}[part]
 
 
@@ -104,6 +117,15 @@ def kernel_flops(wl, cls, fused):
             "bwd_q": n * 2 * d}.get(cls, 0)
 
 
+def fp8_cast_bytes(wl):
+    """Bytes the three E4M3 casts of one step must move: read bf16 Q, K, V (2 B per
+    element) and write their E4M3 codes (1 B; V's rows padded to 16 keys)."""
+    B, S, Hq, Hkv, d = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"]
+    nq, nk = B * S * Hq * d, B * S * Hkv * d
+    nv_out = B * Hkv * d * ((S + 15) // 16 * 16)
+    return 2 * (nq + 2 * nk) + nq + nk + nv_out
+
+
 def recorded_traffic(wl, kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
     that summary is for another workload or the kernel sources changed since."""
@@ -113,7 +135,9 @@ def recorded_traffic(wl, kernel):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("workload") != wl["name"] or kernel not in d.get("kernels", {}):
+    kernels = d.get("kernels", {}) if d.get("workload") == wl["name"] else \
+        d.get("other_workloads", {}).get(wl["name"], {})
+    if kernel not in kernels:
         return None
     h = hashlib.sha256()
     for s in d["sources"]:
@@ -121,7 +145,7 @@ def recorded_traffic(wl, kernel):
             h.update(f.read())
     if h.hexdigest() != d["sources_sha256"]:
         return None
-    k = d["kernels"][kernel]
+    k = kernels[kernel]
     return k["dram_bytes_read"] + k["dram_bytes_write"]
 
 
@@ -199,6 +223,16 @@ def run_oracle_unit(wl, x, b, h):
     import oracle
     G = wl["Hq"] // wl["Hkv"]
     g = h // G
+    if wl.get("fp8"):
+        import numpy as np
+        from oracle import fp8
+        amax = x.setdefault("_amax", {n: np.float32(x[n].float().abs().max()) for n in ("q", "k", "v")})
+        q8, _, dq = fp8.quantize(x["q"][b:b + 1, :, h:h + 1].float().numpy(), amax=amax["q"])
+        k8, _, dk = fp8.quantize(x["k"][b:b + 1, :, g:g + 1].float().numpy(), amax=amax["k"])
+        v8, _, dv = fp8.quantize(x["v"][b:b + 1, :, g:g + 1].float().numpy(), amax=amax["v"])
+        fp8.attention_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=wl["causal"], window=wl["window"],
+                              softmax_type=wl["st"], scale=wl["scale"])
+        return
     L = wl["lens"][b] if wl.get("lens") else wl["S"]  # a padded entry computes on its own rows
     q = x["q"][b:b + 1, :L, h:h + 1].double().numpy()
     k = x["k"][b:b + 1, :L, g:g + 1].double().numpy()
@@ -213,7 +247,7 @@ def run_oracle_unit(wl, x, b, h):
 def unit_flops(wl, b=None):
     """FLOPs of one (batch, query head) unit: of entry b, or the workload's average."""
     if b is not None and wl.get("lens"):
-        per = 2 * (wl["dqk"] + wl["dv"]) + 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+        per = 2 * (wl["dqk"] + wl["dv"]) + (0 if wl.get("fp8") else 2 * (3 * wl["dqk"] + 2 * wl["dv"]))
         return n_pairs(wl["lens"][b], wl["causal"], wl["window"]) * per
     return flops(wl) / (wl["B"] * wl["Hq"])
 
@@ -238,7 +272,8 @@ def cpu_baseline(wl, x, budget_s=12.0):
     dt = time.perf_counter() - t0
     return {"value": work / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{done} of {len(units)} (batch, query head) units of the workload, fwd+bwd in fp64 "
+            "sample": f"{done} of {len(units)} (batch, query head) units of the workload, "
+                      f"{'E4M3 quantisation + fwd' if wl.get('fp8') else 'fwd+bwd'} in fp64 "
                       f"({dt:.1f} s); TFLOP/s counts the same unmasked FLOPs as the GPU number"}
 
 
@@ -273,9 +308,10 @@ def reference_arm(args, wl, world, rank):
         work += unit_flops(wl, u[0])
     dt = time.perf_counter() - t0
     value = work / dt / 1e12
-    sample = (f"each step = one (batch, query head) unit of the workload, fwd+bwd in fp64 "
+    sample = (f"each step = one (batch, query head) unit of the workload, "
+              f"{'E4M3 quantisation + fwd' if wl.get('fp8') else 'fwd+bwd'} in fp64 "
               f"({unit_flops(wl) / 1e9:.2f} GFLOP)")
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+    line = {"metric": METRIC_FP8 if wl.get("fp8") else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl["desc"], "seq_len": wl["S"], "global_batch": wl["B"]},
@@ -287,8 +323,37 @@ def reference_arm(args, wl, world, rank):
     return 0
 
 
+def _step_fns_fp8(sdpa, wl, dev, x):
+    """E4M3 forward step: cast Q, K (BSHD) and V (transposed) with the scales of the
+    previous step's amax while recording this step's, then attn_fwd_fp8."""
+    import torch
+    B, S, Hq, Hkv, d = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"]
+    t = {n: x[n].to(dev) for n in ("q", "k", "v")}
+    f32 = lambda: torch.empty(1, dtype=torch.float32, device=dev)
+    amax = {n: [f32(), f32()] for n in t}          # [previous step's, this step's]
+    desc = {n: f32() for n in t}
+    for n in t:
+        sdpa.attn_fp8_amax(t[n], amax[n][0])      # the history before the first step
+    x8 = {"q": torch.empty((B, S, Hq, d), dtype=torch.uint8, device=dev),
+          "k": torch.empty((B, S, Hkv, d), dtype=torch.uint8, device=dev),
+          "v": torch.empty((B, Hkv, d, sdpa.attn_fp8_vt_row_bytes(S)), dtype=torch.uint8, device=dev)}
+    o = torch.empty((B, S, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], scale=wl["scale"] or 0.0)
+
+    def step():
+        for n in ("q", "k", "v"):
+            sdpa.attn_fp8_quantize(t[n], x8[n], amax[n][0], desc[n], transpose=(n == "v"), amax_out=amax[n][1])
+            amax[n].reverse()                      # this step's amax scales the next step
+        sdpa.attn_fwd_fp8(x8["q"], x8["k"], x8["v"], desc["q"], desc["k"], desc["v"], o, lse, **kw)
+
+    return step, t, (o,)
+
+
 def _step_fns(sdpa, wl, dev, det, x):
     import torch
+    if wl.get("fp8"):
+        return _step_fns_fp8(sdpa, wl, dev, x)
     B, S, Hq, Hkv, dqk, dv = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"], wl["dv"]
     t = {n: x[n].to(dev) for n in ("q", "k", "v", "dout")}
     off = x["offset"].to(dev) if wl["st"] == 2 else None
@@ -356,8 +421,8 @@ def measure_e2e(sdpa, wl, dev, det, x, steps, warmup):
     download overlap step i's kernels; events order each copy against the kernels that
     produce or consume its buffers."""
     import torch
-    host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "dout")}
     sets = [_step_fns(sdpa, wl, dev, det, x) for _ in range(2)]
+    host_in = {n: x[n].pin_memory() for n in sets[0][1]}
     host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs] for _, _, outs in sets]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(o.numel() * o.element_size() for o in host_out[0])
@@ -374,7 +439,7 @@ def measure_e2e(sdpa, wl, dev, det, x, steps, warmup):
             with torch.cuda.stream(up):
                 if started[k]:
                     up.wait_event(computed[k])      # the kernels of step i-2 read these inputs
-                for nm in ("q", "k", "v", "dout"):
+                for nm in host_in:
                     t[nm].copy_(host_in[nm], non_blocking=True)
                 uploaded[k].record(up)
             comp.wait_event(uploaded[k])
@@ -421,6 +486,7 @@ def ours_arm(args, wl, world, rank, local):
     sdpa.library()
     fused_ok = wl["dqk"] in (64, 128) and wl["dv"] in (64, 128)  # the library's fused-dQ head dims
     det = bool(args.deterministic) or not fused_ok
+    fp8 = bool(wl.get("fp8"))
     x = make_cpu_inputs(wl, rank)
     ms, kt, clocks = measure(sdpa, wl, dev, det, x, args.steps, args.warmup, ClockSampler(local))
     total_flops = flops(wl)
@@ -433,25 +499,39 @@ def ours_arm(args, wl, world, rank, local):
     peaks, peak_src = load_peaks()
     dom = max(kt, key=lambda k: kt[k][0])
     dms, dn = kt[dom]
-    dflops = kernel_flops(wl, dom, fused=not det)
-    achieved = dflops / (dms / dn / 1e3) / 1e12 if dn else 0.0
-    peak = float(peaks["bf16_tflops"])
+    if dom == "fp8_quantize":  # a stream: bytes, against the measured copy bandwidth
+        bound, unit = "hbm", "GB/s"
+        achieved = fp8_cast_bytes(wl) / 3 / (dms / dn / 1e3) / 1e9 if dn else 0.0
+        peak = float(peaks["hbm_gbs"])
+        peak_desc = f"hbm_gbs from {peak_src}"
+    else:
+        bound, unit = "tensor", "TFLOP/s"
+        dflops = kernel_flops(wl, dom, fused=not det)
+        achieved = dflops / (dms / dn / 1e3) / 1e12 if dn else 0.0
+        peak = float(peaks["bf16_tflops"]) * (FP8_PER_BF16 if fp8 else 1.0)
+        peak_desc = (f"bf16_tflops (burst) from {peak_src} x {FP8_PER_BF16} (nominal E4M3/bf16 ratio)"
+                     if fp8 else f"bf16_tflops (burst) from {peak_src}")
     launches = sum(v[1] for v in kt.values())
     kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps,
                    "share": v[0] / sum(u[0] for u in kt.values())}
                for k, v in kt.items() if v[1]}
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    line = {"metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
                        "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
-                       "bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ",
+                       **({"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + "
+                                   "attn_fwd_fp8"} if fp8 else
+                          {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
                        "l2": "flushed between timed steps (258 MB write outside the timed span)",
                        **({"seq_lens": wl["lens"]} if wl.get("lens") else {})},
             "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            **({"pct_of_nominal_fp8_peak": 100.0 * value / world / (FP8_PER_BF16 * NOMINAL_BF16_TFLOPS)}
+               if fp8 else {}),
             "fwd_tflop": flops(wl, "fwd") / 1e12, "bwd_tflop": flops(wl, "bwd") / 1e12,
-            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": f"bf16_tflops (burst) from {peak_src}",
+            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak, "peak_source": peak_desc,
                          "traffic": recorded_traffic(wl, dom), "traffic_unit": "bytes per launch (ncu DRAM read+write)"},
             "kernels": kernels,
             "gpu_launches": launches,

@@ -197,7 +197,10 @@ const char* attn_bwd_noalloc_message(void);
  *   A caller with an amax history writes the history's max into amax instead.
  * attn_fp8_quantize: scale = 448 / amax[0] (1 when amax is 0 or not finite);
  *   x8 = E4M3(fp32(x) * scale) and descale[0] = 1 / scale (fp32, correctly
- *   rounded).  x is bf16 BSHD [B, S, H, d].  transpose = 0: x8 has the same
+ *   rounded).  amax_out, when not NULL, receives max |x| of this tensor, taken
+ *   during the same pass (delayed scaling: amax holds the history's max from
+ *   earlier steps, amax_out records this step's; it must not alias amax or
+ *   descale).  x is bf16 BSHD [B, S, H, d].  transpose = 0: x8 has the same
  *   layout; transpose = 1 (d = 64 or 128): x8 is [B, H, d, S_pad], keys
  *   innermost, S_pad = attn_fp8_vt_row_bytes(S), zeros past S — the layout
  *   attn_fwd_fp8 takes V in.  x and x8 16-byte aligned.
@@ -215,7 +218,7 @@ const char* attn_bwd_noalloc_message(void);
  */
 int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream);
 int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
-                      float* descale, void* stream);
+                      float* descale, float* amax_out, void* stream);
 /* Row length in bytes of the transposed E4M3 V: S rounded up to a multiple of 16. */
 int attn_fp8_vt_row_bytes(int S);
 int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,

@@ -77,7 +77,7 @@ def _load():
     lib.attn_last_device_error.restype = i
     lib.attn_fp8_amax.argtypes = [vp, sz, vp, vp]
     lib.attn_fp8_amax.restype = i
-    lib.attn_fp8_quantize.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp]
+    lib.attn_fp8_quantize.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.attn_fp8_quantize.restype = i
     lib.attn_fp8_vt_row_bytes.argtypes = [i]
     lib.attn_fp8_vt_row_bytes.restype = i
@@ -259,10 +259,11 @@ def attn_fp8_amax(x, amax, *, stream=None):
         raise AttnError(st, "attn_fp8_amax")
 
 
-def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, stream=None):
+def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, amax_out=None, stream=None):
     """x8 (uint8 E4M3) = E4M3(x * 448 / amax); descale (fp32 [1]) = amax / 448 as 1 / scale.
 
-    x bf16 BSHD [B,S,H,d]; x8 the same shape, or [B,H,d,S_pad] with transpose=True."""
+    x bf16 BSHD [B,S,H,d]; x8 the same shape, or [B,H,d,S_pad] with transpose=True.
+    amax_out (fp32 [1], optional): records max |x| during the same pass."""
     _check(x, "x", torch.bfloat16, 4)
     _check(x8, "x8", torch.uint8, 4)
     _check(amax, "amax", torch.float32, 1)
@@ -271,8 +272,10 @@ def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, stream=None):
     want = (B, H, d, attn_fp8_vt_row_bytes(S)) if transpose else (B, S, H, d)
     if tuple(x8.shape) != want:
         raise ValueError(f"x8 must have shape {want}, got {tuple(x8.shape)}")
+    if amax_out is not None:
+        _check(amax_out, "amax_out", torch.float32, 1)
     st = _load().attn_fp8_quantize(_ptr(x), _ptr(x8), B, S, H, d, int(bool(transpose)), _ptr(amax), _ptr(descale),
-                                   _stream(stream))
+                                   _ptr(amax_out), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fp8_quantize")
 
@@ -303,11 +306,13 @@ def attn_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, *, causal
         raise AttnError(st, "attn_fwd_fp8")
 
 
-def fp8_quantize(x, *, transpose=False, amax=None, stream=None):
+def fp8_quantize(x, *, transpose=False, amax=None, amax_out=None, stream=None):
     """Per-tensor E4M3 quantisation of a bf16 BSHD tensor: returns (x8, amax, descale).
 
     amax: an fp32 [1] device tensor holding the scaling statistic (for example the
-    max of an amax history); None computes this tensor's own amax."""
+    max of an amax history); None computes this tensor's own amax first (a second
+    pass).  amax_out: optional fp32 [1] device tensor that records this tensor's
+    amax during the cast (delayed scaling)."""
     B, S, H, d = x.shape
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
@@ -315,7 +320,7 @@ def fp8_quantize(x, *, transpose=False, amax=None, stream=None):
     shape = (B, H, d, attn_fp8_vt_row_bytes(S)) if transpose else (B, S, H, d)
     x8 = torch.empty(shape, dtype=torch.uint8, device=x.device)
     descale = torch.empty(1, dtype=torch.float32, device=x.device)
-    attn_fp8_quantize(x, x8, amax, descale, transpose=transpose, stream=stream)
+    attn_fp8_quantize(x, x8, amax, descale, transpose=transpose, amax_out=amax_out, stream=stream)
     return x8, amax, descale
 
 

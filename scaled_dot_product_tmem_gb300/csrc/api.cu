@@ -371,18 +371,19 @@ int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream) {
 }
 
 int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
-                      float* descale, void* stream) {
+                      float* descale, float* amax_out, void* stream) {
   if (B < 0 || S < 0 || H <= 0 || d <= 0 || d % 8 != 0 || !amax || !descale) return ATTN_ERR_INVALID_ARG;
   if (transpose && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((size_t)B * S * H * d > 0 && (!x || !x8)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
-      (reinterpret_cast<uintptr_t>(descale) & 3u))
+      (reinterpret_cast<uintptr_t>(descale) & 3u) || (reinterpret_cast<uintptr_t>(amax_out) & 3u))
     return ATTN_ERR_MISALIGNED;
+  if (amax_out && (amax_out == amax || amax_out == descale)) return ATTN_ERR_INVALID_ARG;
   if ((size_t)B * S * H * d == 0) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int rc = timed(ATTN_KERNEL_FP8_QUANT, 1, s, [&] {
     return sdpa::launch_fp8_quantize(static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(x8), B, S, H, d,
-                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, s);
+                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, amax_out, s);
   });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {

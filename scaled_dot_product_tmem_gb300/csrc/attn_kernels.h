@@ -34,8 +34,9 @@ int launch_attn_fwd_fp8(int d, const CUtensorMap& tq, const CUtensorMap& tk, con
 int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t stream);
 // x8 = E4M3(x * scale), scale = 448 / amax[0] (1 if amax is 0 or not finite),
 // descale[0] = 1 / scale.  transpose: x [B, S, H, d] -> x8 [B, H, d, S_pad].
+// amax_out (may be null): receives max |x| of this tensor, recorded during the cast.
 int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, cudaStream_t stream);
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream);
 
 struct BwdParams {
   int B, S_q, S_kv, H_q, H_kv, G;

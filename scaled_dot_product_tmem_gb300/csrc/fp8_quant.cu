@@ -6,6 +6,8 @@
 //   amax   = max |x|                       (fp8_amax_kernel)
 //   scale  = 448 / amax  (1 if amax is 0 or not finite), descale = 1 / scale
 //   x8     = E4M3(x * scale), round to nearest even, saturating to +-448
+// With delayed scaling the scale comes from earlier steps' amax and the cast also
+// records this tensor's amax (amax_out), so a step reads each tensor once.
 // Both kernels are HBM-bound streams: 16-byte loads, grid-stride loops sized to a
 // few CTAs per SM.  The transposing form writes V as [B, H, d, S_pad] (keys
 // innermost, rows padded to 16 bytes with zeros), the layout in which the forward's
@@ -24,6 +26,21 @@ constexpr unsigned kGridCap = 152 * 8;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Block-wide max of `m` into *out (skipped when out is null); every thread calls it.
+__device__ __forceinline__ void block_amax(unsigned m, unsigned* out) {
+  if (!out) return;
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ unsigned wm[32];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x / 32); ++w) m = max(m, wm[w]);
+    atomicMax(out, m);
+  }
+}
+
+__device__ __forceinline__ unsigned abs_bits(float v) { return __float_as_uint(fabsf(v)); }
+
 // |x| of non-negative floats orders like their bit patterns, so an unsigned max
 // over the bits is a float max (a NaN input ends up above every finite value).
 __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ x8, const __nv_bfloat16* __restrict__ x,
@@ -34,21 +51,11 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__
     const uint4 w = __ldcs(x8 + t);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      m = max(m, __float_as_uint(fabsf(bf16_lo(ws[q]))));
-      m = max(m, __float_as_uint(fabsf(bf16_hi(ws[q]))));
-    }
+    for (int q = 0; q < 4; ++q) m = max(m, max(abs_bits(bf16_lo(ws[q])), abs_bits(bf16_hi(ws[q]))));
   }
   if (blockIdx.x == 0)
-    for (size_t t = n8 * 8 + threadIdx.x; t < n; t += blockDim.x) m = max(m, __float_as_uint(fabsf(__bfloat162float(x[t]))));
-  m = __reduce_max_sync(0xffffffffu, m);
-  __shared__ unsigned wm[8];
-  if ((threadIdx.x & 31) == 0) wm[threadIdx.x / 32] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < (int)(blockDim.x / 32); ++w) m = max(m, wm[w]);
-    atomicMax(amax_bits, m);
-  }
+    for (size_t t = n8 * 8 + threadIdx.x; t < n; t += blockDim.x) m = max(m, abs_bits(__bfloat162float(x[t])));
+  block_amax(m, amax_bits);
 }
 
 __device__ __forceinline__ float scale_of(const float* amax) {
@@ -58,12 +65,19 @@ __device__ __forceinline__ float scale_of(const float* amax) {
 
 __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict__ x8, const __nv_bfloat16* __restrict__ x,
                                                         uint2* __restrict__ out8, uint8_t* __restrict__ out, size_t n,
-                                                        const float* __restrict__ amax, float* __restrict__ descale) {
+                                                        const float* __restrict__ amax, float* __restrict__ descale,
+                                                        unsigned* __restrict__ amax_out) {
   const float sc = scale_of(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
   const size_t n8 = n / 8;
+  unsigned m = 0;
   for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += (size_t)gridDim.x * blockDim.x) {
     const uint4 w = __ldcs(x8 + t);
+    if (amax_out) {
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m = max(m, max(abs_bits(bf16_lo(ws[q])), abs_bits(bf16_hi(ws[q]))));
+    }
     const uint32_t lo = pack_e4m3x4(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
                                     __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
     const uint32_t hi = pack_e4m3x4(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
@@ -72,9 +86,11 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
   }
   if (blockIdx.x == 0)
     for (size_t t = n8 * 8 + threadIdx.x; t < n; t += blockDim.x) {
-      const float v = __fmul_rn(__bfloat162float(x[t]), sc);
-      out[t] = (uint8_t)(pack_e4m3x4(v, 0.f, 0.f, 0.f) & 0xFFu);
+      const float xv = __bfloat162float(x[t]);
+      m = max(m, abs_bits(xv));
+      out[t] = (uint8_t)(pack_e4m3x4(__fmul_rn(xv, sc), 0.f, 0.f, 0.f) & 0xFFu);
     }
+  block_amax(m, amax_out);
 }
 
 // One block per (b, h, 64-key tile): the tile's 64 x d bf16 values are read as
@@ -84,7 +100,7 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
 template <int D>
 __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ out,
                                                           int S, int H, int S_pad, const float* __restrict__ amax,
-                                                          float* __restrict__ descale) {
+                                                          float* __restrict__ descale, unsigned* __restrict__ amax_out) {
   __shared__ __align__(16) uint8_t tile[D][64 + 16];
   const float sc = scale_of(amax);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
@@ -93,6 +109,7 @@ __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* _
   const int h = bh % H, b = bh / H;
   const int k0 = kt * 64;
   constexpr int CPR = D / 8;  // 16-byte chunks per key row
+  unsigned m = 0;
   for (int c = threadIdx.x; c < 64 * CPR; c += blockDim.x) {
     const int kk = c / CPR, d0 = (c % CPR) * 8;
     const int key = k0 + kk;
@@ -101,11 +118,13 @@ __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* _
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+      m = max(m, max(abs_bits(bf16_lo(ws[q])), abs_bits(bf16_hi(ws[q]))));
       const uint32_t e = pack_e4m3x4(__fmul_rn(bf16_lo(ws[q]), sc), __fmul_rn(bf16_hi(ws[q]), sc), 0.f, 0.f);
       tile[d0 + 2 * q][kk] = (uint8_t)(e & 0xFFu);
       tile[d0 + 2 * q + 1][kk] = (uint8_t)((e >> 8) & 0xFFu);
     }
   }
+  block_amax(m, amax_out);  // (its barrier also publishes the tile)
   __syncthreads();
   for (int c = threadIdx.x; c < D * 4; c += blockDim.x) {
     const int dd = c / 4, q = c % 4;
@@ -132,18 +151,20 @@ int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t 
 }
 
 int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, cudaStream_t stream) {
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream) {
   const size_t n = (size_t)B * S * H * d;
+  unsigned* ao = reinterpret_cast<unsigned*>(amax_out);
+  if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return -1;
   if (!transpose) {
     fp8_quant_kernel<<<grid_for(n / 8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), x,
-                                                          reinterpret_cast<uint2*>(x8), x8, n, amax, descale);
+                                                          reinterpret_cast<uint2*>(x8), x8, n, amax, descale, ao);
   } else {
     const long long blocks = (long long)((S_pad + 63) / 64) * H * B;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
     if (d == 128)
-      fp8_quant_t_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale);
+      fp8_quant_t_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
     else if (d == 64)
-      fp8_quant_t_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale);
+      fp8_quant_t_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
     else
       return -2;
   }

@@ -128,13 +128,15 @@ def test_fp8_argument_validation(lib):
     assert f8(dv=ctypes.c_void_p(0x10002)) == MISALIGNED
     assert f8(B=0) == OK and f8(Sq=0) == OK             # nothing to launch
 
-    def qz(x=P, x8=P, B=1, S=64, H=2, d=128, t=0, amax=P, desc=P):
-        return lib.attn_fp8_quantize(x, x8, B, S, H, d, t, amax, desc, None)
+    def qz(x=P, x8=P, B=1, S=64, H=2, d=128, t=0, amax=P, desc=P, aout=None):
+        return lib.attn_fp8_quantize(x, x8, B, S, H, d, t, amax, desc, aout, None)
 
     assert qz(d=96, t=1) == UNSUPPORTED                 # the transposed form: d = 64 or 128
     assert qz(d=12) == INVALID                          # rows of whole 16-byte chunks
     assert qz(amax=None) == INVALID
     assert qz(x8=MIS) == MISALIGNED
     assert qz(B=0) == OK
+    assert qz(aout=P) == INVALID                        # amax_out may not alias amax
+    assert qz(aout=ctypes.c_void_p(0x10022)) == MISALIGNED
     assert lib.attn_fp8_amax(P, ctypes.c_size_t(8), None, None) == INVALID
     assert lib.attn_fp8_amax(MIS, ctypes.c_size_t(8), P, None) == MISALIGNED

@@ -83,3 +83,23 @@ def test_padded_batch_workload_counts_each_entry_on_its_own_length():
     # a padded batch whose lengths are all S counts like the plain workload
     full = dict(wl, lens=[wl["S"]] * wl["B"])
     assert bench.flops(full) == bench.flops(dict(wl, lens=None))
+
+
+def test_fp8_workloads_count_forward_flops_and_cast_bytes():
+    import bench
+    wl = bench.WORKLOADS["fp8_fwd_mha_b4_s2048_d64"]
+    n = 4 * 8 * 2048 * 2049 // 2
+    assert bench.flops(wl) == bench.flops(wl, "fwd") == n * 2 * (64 + 64)
+    assert bench.flops(wl, "bwd") == 0
+    elems = 4 * 2048 * 8 * 64
+    assert bench.fp8_cast_bytes(wl) == 3 * (2 * elems + elems)   # bf16 in, E4M3 out, S a multiple of 16
+
+
+def test_reference_arm_runs_the_fp8_oracle():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "fp8_fwd_mha_b4_s2048_d64", "--steps", "3", "--warmup", "3"], capture_output=True,
+                         text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip()][0])
+    assert d["metric"] == bench.METRIC_FP8 and d["value"] > 0
+    assert "E4M3" in d["cpu_baseline"]["sample"]

@@ -56,18 +56,24 @@ def test_quantize_bit_exact(shape, transpose):
     assert np.array_equal(got, codes)
 
 
-def test_quantize_with_a_given_amax_and_saturation():
+@pytest.mark.parametrize("transpose", [False, True], ids=["bshd", "vt"])
+def test_quantize_with_a_given_amax_and_saturation(transpose):
     """A caller's amax (an amax history's max) sets the scale; values above it
-    saturate to +-448 instead of overflowing."""
+    saturate to +-448 instead of overflowing; amax_out records the tensor's own amax
+    in the same pass."""
     sdpa = _sdpa()
-    x = make_inputs(Shape(1, 64, 64, 2, 2, 64, 64), 12)["k"]
+    x = make_inputs(Shape(2, 100, 100, 3, 3, 64, 64), 12)["k"]
     a = torch.tensor([0.5], dtype=torch.float32, device="cuda")  # below the true amax
-    x8, _, descale = sdpa.fp8_quantize(x.cuda(), amax=a)
+    rec = torch.full((1,), 123.0, dtype=torch.float32, device="cuda")  # overwritten
+    x8, _, descale = sdpa.fp8_quantize(x.cuda(), amax=a, amax_out=rec, transpose=transpose)
     torch.cuda.synchronize()
-    codes, _, d_ref = fp8.quantize(x.float().numpy(), amax=np.float32(0.5))
+    _check_device()
+    codes, _, d_ref = fp8.quantize(x.float().numpy(), amax=np.float32(0.5), transpose=transpose)
     assert descale.item() == d_ref
-    assert np.array_equal(x8.cpu().numpy(), codes)
+    got = x8.cpu().numpy()
+    assert np.array_equal(got[..., :100] if transpose else got, codes)
     assert (np.abs(fp8.e4m3_decode(codes)) == 448.0).sum() > 10
+    assert rec.item() == float(np.abs(x.float().numpy()).max())
 
 
 def _oracle_fp8(x, *, causal, window, softmax_type, scale, rows=None):
