@@ -8,8 +8,7 @@
 //   x8     = E4M3(x * scale), round to nearest even, saturating to +-448
 // With delayed scaling the scale comes from earlier steps' amax and the cast also
 // records this tensor's amax (amax_out), so a step reads each tensor once.
-// Both kernels are HBM-bound streams: 16-byte loads, grid-stride loops sized to a
-// few CTAs per SM.  The transposing form writes V as [B, H, d, S_pad] (keys
+// Both kernels are HBM-bound streams of 16-byte loads and stores.  The transposing form writes V as [B, H, d, S_pad] (keys
 // innermost, rows padded to 16 bytes with zeros), the layout in which the forward's
 // P.V product reads V as a K-major operand.
 #include <cuda_runtime.h>
@@ -93,45 +92,65 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
   block_amax(m, amax_out);
 }
 
-// One block per (b, h, 64-key tile): the tile's 64 x d bf16 values are read as
-// 16-byte rows, converted, transposed through shared memory and written as d rows
-// of 64 E4M3 bytes (16-byte stores; keys past S are zeros, keys past S_pad are not
-// written).
+// One block per (b, h, 128-key tile).  Phase 1 reads the tile's 128 x d bf16 values
+// as 16-byte chunks (coalesced along d), converts them and stores the codes row by
+// row (key-major) in shared memory.  Phase 2 gives each thread 4 head dims x 16 keys:
+// sixteen 4-byte reads, 4 x 4 byte transposes with byte permutes, and one 16-byte
+// store per head dim into V^T (keys past S are zeros; keys past S_pad are not written).
 template <int D>
 __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ out,
                                                           int S, int H, int S_pad, const float* __restrict__ amax,
                                                           float* __restrict__ descale, unsigned* __restrict__ amax_out) {
-  __shared__ __align__(16) uint8_t tile[D][64 + 16];
+  constexpr int KT = 128;          // keys per tile
+  constexpr int ROW = D + 4;       // bytes per key row in shared memory (4-byte aligned, skews the banks)
+  __shared__ __align__(16) uint8_t tile[KT * ROW];
   const float sc = scale_of(amax);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
-  const int n_tiles = (S_pad + 63) / 64;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
+  const int n_tiles = (S_pad + KT - 1) / KT;
   const int kt = blockIdx.x % n_tiles, bh = blockIdx.x / n_tiles;
   const int h = bh % H, b = bh / H;
-  const int k0 = kt * 64;
+  const int k0 = kt * KT;
   constexpr int CPR = D / 8;  // 16-byte chunks per key row
   unsigned m = 0;
-  for (int c = threadIdx.x; c < 64 * CPR; c += blockDim.x) {
+  for (int c = threadIdx.x; c < KT * CPR; c += blockDim.x) {
     const int kk = c / CPR, d0 = (c % CPR) * 8;
     const int key = k0 + kk;
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (key < S) w = __ldcs(reinterpret_cast<const uint4*>(x + (((size_t)b * S + key) * H + h) * D + d0));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    m = max(m, max(max(abs_bits(bf16_lo(w.x)), abs_bits(bf16_hi(w.x))), max(abs_bits(bf16_lo(w.y)), abs_bits(bf16_hi(w.y)))));
+    m = max(m, max(max(abs_bits(bf16_lo(w.z)), abs_bits(bf16_hi(w.z))), max(abs_bits(bf16_lo(w.w)), abs_bits(bf16_hi(w.w)))));
+    const uint32_t lo = pack_e4m3x4(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
+                                    __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
+    const uint32_t hi = pack_e4m3x4(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
+                                    __fmul_rn(bf16_lo(w.w), sc), __fmul_rn(bf16_hi(w.w), sc));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tile + kk * ROW + d0);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
+  block_amax(m, amax_out);
+  __syncthreads();
+  constexpr int DG = D / 4;  // groups of 4 head dims
+  for (int t = threadIdx.x; t < DG * (KT / 16); t += blockDim.x) {
+    const int dg = t % DG, kg = t / DG;
+    const int key = k0 + kg * 16;
+    if (key >= S_pad) continue;
+    uint32_t o[4][4];  // o[e][q]: head dim 4*dg+e, keys 4q .. 4q+3 of the group
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      m = max(m, max(abs_bits(bf16_lo(ws[q])), abs_bits(bf16_hi(ws[q]))));
-      const uint32_t e = pack_e4m3x4(__fmul_rn(bf16_lo(ws[q]), sc), __fmul_rn(bf16_hi(ws[q]), sc), 0.f, 0.f);
-      tile[d0 + 2 * q][kk] = (uint8_t)(e & 0xFFu);
-      tile[d0 + 2 * q + 1][kk] = (uint8_t)((e >> 8) & 0xFFu);
+      uint32_t w[4];  // key kg*16 + 4q + r: its codes of head dims 4*dg .. 4*dg+3
+#pragma unroll
+      for (int r = 0; r < 4; ++r) w[r] = *reinterpret_cast<const uint32_t*>(tile + (kg * 16 + 4 * q + r) * ROW + 4 * dg);
+      const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140), t1 = __byte_perm(w[0], w[1], 0x7362);
+      const uint32_t t2 = __byte_perm(w[2], w[3], 0x5140), t3 = __byte_perm(w[2], w[3], 0x7362);
+      o[0][q] = __byte_perm(t0, t2, 0x5410);
+      o[1][q] = __byte_perm(t0, t2, 0x7632);
+      o[2][q] = __byte_perm(t1, t3, 0x5410);
+      o[3][q] = __byte_perm(t1, t3, 0x7632);
     }
-  }
-  block_amax(m, amax_out);  // (its barrier also publishes the tile)
-  __syncthreads();
-  for (int c = threadIdx.x; c < D * 4; c += blockDim.x) {
-    const int dd = c / 4, q = c % 4;
-    const int key = k0 + q * 16;
-    if (key >= S_pad) continue;
-    *reinterpret_cast<uint4*>(out + (((size_t)b * H + h) * D + dd) * S_pad + key) =
-        *reinterpret_cast<const uint4*>(&tile[dd][q * 16]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint4*>(out + (((size_t)b * H + h) * D + 4 * dg + e) * S_pad + key) =
+          make_uint4(o[e][0], o[e][1], o[e][2], o[e][3]);
   }
 }
 
@@ -159,7 +178,7 @@ int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H
     fp8_quant_kernel<<<grid_for(n / 8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), x,
                                                           reinterpret_cast<uint2*>(x8), x8, n, amax, descale, ao);
   } else {
-    const long long blocks = (long long)((S_pad + 63) / 64) * H * B;
+    const long long blocks = (long long)((S_pad + 127) / 128) * H * B;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
     if (d == 128)
       fp8_quant_t_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
