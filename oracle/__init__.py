@@ -56,11 +56,11 @@ def _load():
         lib = ctypes.CDLL(build())
         dp = ctypes.POINTER(ctypes.c_double)
         i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp,
+        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i,
                                    dp, dp, dp, dp]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp,
-                                   dp, dp, dp, dp, dp]
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i,
+                                   dp, dp, dp, dp, dp, dp]
         lib.oracle_bwd.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -87,10 +87,20 @@ def default_scale(d_qk: int) -> float:
     return 1.0 / np.sqrt(d_qk)
 
 
+def _bias_args(bias, B, Hq, Sq, Skv):
+    if bias is None:
+        return None, 1, 1
+    bias = _f64(bias)
+    Bb, Hb = bias.shape[0], bias.shape[1]
+    assert bias.shape == (Bb, Hb, Sq, Skv) and Bb in (1, B) and Hb in (1, Hq), bias.shape
+    return bias, Bb, Hb
+
+
 def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None):
+                  offset=None, scale=None, bias=None):
     """O, LSE, p_sink, rowsum for BSHD q [B,Sq,Hq,dqk], k [B,Skv,Hkv,dqk], v [B,Skv,Hkv,dv].
 
+    bias: optional [Bb,Hb,Sq,Skv] (Bb in {1,B}, Hb in {1,Hq}) added to the scaled scores.
     Returns a dict of float64 arrays: o [B,Sq,Hq,dv]; lse, psink, rowsum [B,Hq,Sq].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -99,39 +109,46 @@ def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
     assert k.shape == (B, Skv, Hkv, dqk)
     scale = default_scale(dqk) if scale is None else float(scale)
     off = _f64(offset).reshape(-1) if offset is not None else None
+    bias, Bb, Hb = _bias_args(bias, B, Hq, Sq, Skv)
     o = np.zeros((B, Sq, Hq, dv))
     lse = np.zeros((B, Hq, Sq))
     psink = np.zeros((B, Hq, Sq))
     rowsum = np.zeros((B, Hq, Sq))
     rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, dqk, dv,
                             scale, int(bool(causal)), int(window), int(softmax_type),
-                            _ptr(off), _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
+                            _ptr(off), _ptr(bias), Bb, Hb, _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     return {"o": o, "lse": lse, "psink": psink, "rowsum": rowsum}
 
 
 def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None):
-    """dq, dk, dv, d_offset [Hq], D [B,Hq,Sq] (= dO.O) for the same arguments as fwd."""
+                  offset=None, scale=None, bias=None):
+    """dq, dk, dv, d_offset [Hq], D [B,Hq,Sq] (= dO.O) and, with a bias, dbias (its
+    shape) for the same arguments as fwd."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Sq, Hq, dqk = q.shape
     _, Skv, Hkv, dv = v.shape
     assert dout.shape == (B, Sq, Hq, dv)
     scale = default_scale(dqk) if scale is None else float(scale)
     off = _f64(offset).reshape(-1) if offset is not None else None
+    bias, Bb, Hb = _bias_args(bias, B, Hq, Sq, Skv)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dvv = np.zeros_like(v)
     doff = np.zeros(Hq)
     D = np.zeros((B, Hq, Sq))
+    dbias = np.zeros_like(bias) if bias is not None else None
     rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Sq, Skv, Hq, Hkv,
                             dqk, dv, scale, int(bool(causal)), int(window),
-                            int(softmax_type), _ptr(off), _ptr(dq), _ptr(dk), _ptr(dvv),
-                            _ptr(doff), _ptr(D))
+                            int(softmax_type), _ptr(off), _ptr(bias), Bb, Hb, _ptr(dq), _ptr(dk),
+                            _ptr(dvv), _ptr(doff), _ptr(D), _ptr(dbias))
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
-    return {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}
+    out = {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}
+    if dbias is not None:
+        out["dbias"] = dbias
+    return out
 
 
 # ----------------------------------------------------------------------------- padded batches

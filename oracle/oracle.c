@@ -37,6 +37,14 @@
  *   - LSE = M_i + ln Z_i includes the sink; a row with no visible key and no sink
  *     gives O = 0, LSE = -inf, and contributes nothing to the backward.
  *
+ * Additive bias ("JAX: Single-GPU Attention with TransformerEngine", section "Other
+ * attention knobs": pass `bias` with an `attn_bias_type`; the sequence diagrams of
+ * PR 2225 pass it to the fused kernels and get grad_bias back).  Reading: the bias
+ * is added to the scaled scores, s_ij = scale q_i . k_j + bias_ij (post-scale), before
+ * the masks; it is a [Bb, Hb, S_q, S_kv] tensor with Bb in {1, B} and Hb in {1, H_q}
+ * broadcast over batch / heads; a -inf bias entry removes that key like a mask.
+ * dbias_ij = sum over the (b, h) that share the entry of dS_ij.
+ *
  * Backward (derived from the definition; the pages only name the outputs
  * dq, dk, dv, d_softmax_offset):
  *   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,   dS_ij = P_ij (dP_ij - D_i),
@@ -66,6 +74,12 @@ static int visible(int i, int j, int causal, int window) {
     return 1;
 }
 
+/* The [S_q, S_kv] bias plane that batch b, query head h reads, or NULL. */
+static const double* bias_plane(const double* bias, int Bb, int Hb, int b, int h, int Sq, int Skv) {
+    if (!bias) return NULL;
+    return bias + ((size_t)(Bb == 1 ? 0 : b) * Hb + (Hb == 1 ? 0 : h)) * Sq * Skv;
+}
+
 /* The sink logit c of query head h (see the readings above). */
 static double sink_logit(int softmax_type, const double* offset, int h) {
     if (softmax_type == ORACLE_OFF_BY_ONE) return 0.0;
@@ -80,7 +94,7 @@ static double sink_logit(int softmax_type, const double* offset, int h) {
  */
 static void probs_one_head(const double* q, const double* k, int b, int h, int g,
                            int Sq, int Skv, int Hq, int Hkv, int dqk,
-                           double scale, int causal, int window, double c,
+                           double scale, int causal, int window, double c, const double* bias,
                            double* P, double* lse, double* psink) {
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < Sq; i++) {
@@ -93,11 +107,12 @@ static void probs_one_head(const double* q, const double* k, int b, int h, int g
             for (int t = 0; t < dqk; t++)
                 s += q[bshd(b, i, h, t, Sq, Hq, dqk)] * k[bshd(b, j, g, t, Skv, Hkv, dqk)];
             s *= scale;
+            if (bias) s += bias[(size_t)i * Skv + j]; /* this (b, h)'s bias plane, or NULL */
             row[j] = s;
             if (s > m) m = s;
         }
         double z = 0.0;
-        if (m == -INFINITY) { /* no visible key and no sink: empty row */
+        if (m == -INFINITY) { /* no visible key (or all biased to -inf) and no sink: empty row */
             for (int j = 0; j < Skv; j++) row[j] = 0.0;
             lse[i] = -INFINITY;
             psink[i] = 0.0;
@@ -121,8 +136,10 @@ static void probs_one_head(const double* q, const double* k, int b, int h, int g
 int oracle_fwd(const double* q, const double* k, const double* v,
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
+               const double* bias, int Bb, int Hb,
                double* o, double* lse, double* psink, double* rowsum) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
     int G = Hq / Hkv;
@@ -135,7 +152,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
             double c = sink_logit(softmax_type, offset, h);
             double* lrow = lse + ((size_t)b * Hq + h) * Sq;
             probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
-                           P, lrow, ps);
+                           bias_plane(bias, Bb, Hb, b, h, Sq, Skv), P, lrow, ps);
             /* attend: O_i = sum_j P_ij v_j */
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
@@ -170,8 +187,10 @@ int oracle_fwd(const double* q, const double* k, const double* v,
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
-               double* dq, double* dk, double* dvout, double* d_offset, double* Dout) {
+               const double* bias, int Bb, int Hb,
+               double* dq, double* dk, double* dvout, double* d_offset, double* Dout, double* dbias) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
     int G = Hq / Hkv;
@@ -189,13 +208,14 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
     memset(dk, 0, sizeof(double) * (size_t)B * Skv * Hkv * dqk);
     memset(dvout, 0, sizeof(double) * (size_t)B * Skv * Hkv * dv);
     if (d_offset) for (int h = 0; h < Hq; h++) d_offset[h] = 0.0;
+    if (bias && dbias) memset(dbias, 0, sizeof(double) * (size_t)Bb * Hb * Sq * Skv);
 
     for (int b = 0; b < B; b++) {
         for (int h = 0; h < Hq; h++) {
             int g = h / G;
             double c = sink_logit(softmax_type, offset, h);
             probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
-                           P, lse, ps);
+                           bias_plane(bias, Bb, Hb, b, h, Sq, Skv), P, lse, ps);
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
                 /* O_i = sum_j P_ij v_j, then D_i = dO_i . O_i */
@@ -244,6 +264,13 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                 }
                 for (int t = 0; t < dqk; t++) dk[bshd(b, j, g, t, Skv, Hkv, dqk)] += scale * ak[t];
                 for (int t = 0; t < dv; t++) dvout[bshd(b, j, g, t, Skv, Hkv, dv)] += av[t];
+            }
+            /* dbias_ij += dS_ij (the scores' gradient, summed over the (b, h) sharing it) */
+            if (bias && dbias) {
+                double* plane = (double*)bias_plane(dbias, Bb, Hb, b, h, Sq, Skv);
+#pragma omp parallel for schedule(static)
+                for (int i = 0; i < Sq; i++)
+                    for (int j = 0; j < Skv; j++) plane[(size_t)i * Skv + j] += dS[(size_t)i * Skv + j];
             }
             /* d offset_h = -sum_i p_sink_i D_i  (learnable only; a sum over b too) */
             if (softmax_type == ORACLE_LEARNABLE && d_offset) {
