@@ -41,12 +41,13 @@ NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False):
+def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False, bias=None):
     """A workload; `lens` (one length per batch entry, same for queries and keys) makes
     it a padded batch run through the varlen entry points; `fp8` makes it the E4M3
-    forward."""
+    forward; `bias` = (Bb, Hb) adds a bf16 [Bb, Hb, S, S] bias (attn_fwd_bias /
+    attn_bwd_bias, with dbias)."""
     return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
-                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8)
+                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8, bias=bias)
 
 
 WORKLOADS = {
@@ -79,6 +80,11 @@ WORKLOADS["fp8_fwd_mha_b4_s2048_d64"] = _w(
 WORKLOADS["fp8_fwd_gqa_b4_s8192_d128"] = _w(
     "fp8_fwd_gqa_b4_s8192_d128", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 42,
     "E4M3 forward: B=4, S=8192, H_q=32, H_kv=8, d=128, causal", fp8=True)
+# Additive bias, one [S, S] plane per query head shared by the batch (dbias sums the batch).
+WORKLOADS["bias_gqa_b2_s4096"] = _w(
+    "bias_gqa_b2_s4096", 2, 4096, 32, 8, 128, 128, True, -1, 0, None, 8,
+    "additive bias [1, 32, S, S] (bf16, N(0,1)) with dbias: B=2, S=4096, H_q=32, H_kv=8, d=128, causal",
+    bias=(1, 32))
 DEFAULT = "gqa_swa_b4_s2048"
 HEADLINE = "sweep_s8192_hkv8"
 
@@ -240,6 +246,10 @@ def run_oracle_unit(wl, x, b, h):
     do = x["dout"][b:b + 1, :L, h:h + 1].double().numpy()
     off = x["offset"][h:h + 1].double().numpy() if wl["st"] == 2 else None
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], offset=off, scale=wl["scale"])
+    if wl.get("bias"):
+        Bb, Hb = wl["bias"]
+        kw["bias"] = x["bias"][b if Bb > 1 else 0:(b if Bb > 1 else 0) + 1,
+                               h if Hb > 1 else 0:(h if Hb > 1 else 0) + 1, :L, :L].double().numpy()
     oracle.attention_fwd(q, k, v, **kw)
     oracle.attention_bwd(q, k, v, do, **kw)
 
@@ -253,9 +263,12 @@ def unit_flops(wl, b=None):
 
 
 def make_cpu_inputs(wl, rank=0):
-    from scaled_dot_product_tmem_gb300.inputs import Shape, make_inputs
+    from scaled_dot_product_tmem_gb300.inputs import Shape, make_bias, make_inputs
     shape = Shape(wl["B"], wl["S"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"], wl["dv"])
-    return make_inputs(shape, wl["seed"] + 7919 * rank, learnable_offset=(wl["st"] == 2))
+    x = make_inputs(shape, wl["seed"] + 7919 * rank, learnable_offset=(wl["st"] == 2))
+    if wl.get("bias"):
+        x["bias"] = make_bias((*wl["bias"], wl["S"], wl["S"]), wl["seed"] + 1 + 7919 * rank)
+    return x
 
 
 def cpu_baseline(wl, x, budget_s=12.0):
@@ -370,13 +383,19 @@ def _step_fns(sdpa, wl, dev, det, x):
     if wl.get("lens"):
         lens = torch.tensor(wl["lens"], dtype=torch.int32, device=dev)
         kw.update(seq_lens_q=lens, seq_lens_kv=lens)
+    bkw, outs = {}, (o, dq, dk, dvv)
+    if wl.get("bias"):
+        t["bias"] = x["bias"].to(dev)
+        dbias = torch.empty(t["bias"].shape, dtype=torch.float32, device=dev)
+        bkw, outs = {"dbias": dbias}, (o, dq, dk, dvv, dbias)
 
     def step():
-        sdpa.attn_fwd(t["q"], t["k"], t["v"], o, lse, **kw)
+        b = t.get("bias")
+        sdpa.attn_fwd(t["q"], t["k"], t["v"], o, lse, bias=b, **kw)
         sdpa.attn_bwd(t["q"], t["k"], t["v"], o, t["dout"], lse, dq, dk, dvv, doff, deterministic=det,
-                      workspace=ws, **kw)
+                      workspace=ws, bias=b, **bkw, **kw)
 
-    return step, t, (o, dq, dk, dvv)
+    return step, t, outs
 
 
 def measure(sdpa, wl, dev, det, x, steps, warmup, sampler=None):
@@ -525,7 +544,9 @@ def ours_arm(args, wl, world, rank, local):
                                    "attn_fwd_fp8"} if fp8 else
                           {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
                        "l2": "flushed between timed steps (258 MB write outside the timed span)",
-                       **({"seq_lens": wl["lens"]} if wl.get("lens") else {})},
+                       **({"seq_lens": wl["lens"]} if wl.get("lens") else {}),
+                       **({"bias": f"bf16 {list(wl['bias']) + [wl['S'], wl['S']]}, dbias fp32"}
+                          if wl.get("bias") else {})},
             "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             **({"pct_of_nominal_fp8_peak": 100.0 * value / world / (FP8_PER_BF16 * NOMINAL_BF16_TFLOPS)}
                if fp8 else {}),

@@ -182,6 +182,35 @@ size_t attn_bwd_noalloc_max_scratch_bytes(void);
 const char* attn_bwd_noalloc_message(void);
 
 /*
+ * Additive attention bias.  Source: "JAX: Single-GPU Attention with
+ * TransformerEngine", section "Other attention knobs" (pass `bias` with an
+ * `attn_bias_type`), and the sequence diagrams of "[JAX] Add support for sink
+ * attention in JAX #2225" (the fused forward takes the bias, the fused backward
+ * returns grad_bias next to dq, dk, dv).
+ *
+ * bias: bf16 [bias_B, bias_H, S_q, S_kv], contiguous, 16-byte aligned, with
+ *   bias_B in {1, B} and bias_H in {1, H_q} (1 = broadcast over that dim).  It is
+ *   added to the scaled scores before the masks and the softmax (post-scale):
+ *   s_ij = scale * q_i . k_j + bias[b][h][i][j]; a -inf entry removes that key.
+ * attn_fwd_bias: otherwise as attn_fwd.  attn_bwd_bias: as attn_bwd, plus
+ *   dbias: fp32, the bias's shape (NULL: not computed) = dL/ds summed over the
+ *   (b, h) that share each entry; the call zeroes it and accumulates it with fp32
+ *   atomics, so with a broadcast bias (bias_B = 1 < B or bias_H = 1 < H_q) dbias is
+ *   not bitwise reproducible and deterministic != 0 is rejected
+ *   (ATTN_ERR_UNSUPPORTED).  Same workspace as attn_bwd.
+ * Supported: full-length batches with d_qk = d_v in {64, 128}; other head dims
+ * return ATTN_ERR_UNSUPPORTED.
+ */
+int attn_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, const void* bias, int bias_B,
+                  int bias_H, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale, int causal,
+                  int window, int softmax_type, const float* softmax_offset, void* stream);
+int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, float* d_offset, const void* bias, int bias_B, int bias_H,
+                  float* dbias, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale,
+                  int causal, int window, int softmax_type, const float* softmax_offset, int deterministic,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * FP8 (E4M3) forward.  Source: "Speed up attention on GPU with cuDNN and
  * TransformerEngine", step 10 ("Benchmark NVIDIA TransformerEngine and FP8"),
  * section "Inspect the FP8 path": the forward runs on E4M3 tensors (4 exponent,

@@ -75,6 +75,11 @@ def _load():
     lib.attn_timing_read.restype = i
     lib.attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.attn_last_device_error.restype = i
+    lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, vp]
+    lib.attn_fwd_bias.restype = i
+    lib.attn_bwd_bias.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, i, i, i, i, i, i, i, f, i, i,
+                                  i, vp, i, vp, sz, vp]
+    lib.attn_bwd_bias.restype = i
     lib.attn_fp8_amax.argtypes = [vp, sz, vp, vp]
     lib.attn_fp8_amax.restype = i
     lib.attn_fp8_quantize.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp, vp]
@@ -142,12 +147,22 @@ def _check_lens(t, name, B):
             raise ValueError(f"{name}: one length per batch entry ({B}), got {t.shape[0]}")
 
 
+def _check_bias(bias, B, H_q, S_q, S_kv):
+    _check(bias, "bias", torch.bfloat16, 4)
+    Bb, Hb = bias.shape[0], bias.shape[1]
+    if tuple(bias.shape[2:]) != (S_q, S_kv) or Bb not in (1, B) or Hb not in (1, H_q):
+        raise ValueError(f"bias must be [1 or {B}, 1 or {H_q}, {S_q}, {S_kv}], got {tuple(bias.shape)}")
+    return Bb, Hb
+
+
 def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-             seq_lens_q=None, seq_lens_kv=None, stream=None):
+             seq_lens_q=None, seq_lens_kv=None, bias=None, stream=None):
     """Forward into preallocated o [B,S_q,H_q,d_v] bf16 and lse [B,H_q,S_q] fp32.
 
     seq_lens_q / seq_lens_kv: optional int32 [B] device tensors for a padded batch
     (attn_fwd_varlen); None means full length.
+    bias: optional bf16 [1 or B, 1 or H_q, S_q, S_kv] added to the scaled scores
+    (attn_fwd_bias).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, n, torch.bfloat16, 4)
@@ -160,7 +175,12 @@ def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, s
     _check_lens(seq_lens_kv, "seq_lens_kv", B)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
             int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset))
-    if seq_lens_q is None and seq_lens_kv is None:
+    if bias is not None:
+        if seq_lens_q is not None or seq_lens_kv is not None:
+            raise ValueError("bias with padded batches is not supported")
+        Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
+        st = _load().attn_fwd_bias(*args[:5], _ptr(bias), Bb, Hb, *args[5:], _stream(stream))
+    elif seq_lens_q is None and seq_lens_kv is None:
         st = _load().attn_fwd(*args, _stream(stream))
     else:
         st = _load().attn_fwd_varlen(*args, _ptr(seq_lens_q), _ptr(seq_lens_kv), _stream(stream))
@@ -174,10 +194,12 @@ def attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic=Tr
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, window=-1, softmax_type=VANILLA,
              softmax_offset=None, scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None,
-             stream=None):
+             bias=None, dbias=None, stream=None):
     """Backward into preallocated dq, dk, dv (bf16) and d_offset (fp32 [H_q], learnable).
 
-    seq_lens_q / seq_lens_kv as for attn_fwd (attn_bwd_varlen).
+    seq_lens_q / seq_lens_kv as for attn_fwd (attn_bwd_varlen).  bias as for attn_fwd,
+    with dbias an optional preallocated fp32 tensor of the bias's shape
+    (attn_bwd_bias).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16, 4)
@@ -193,7 +215,16 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, w
             B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0), int(bool(causal)), int(window),
             _stype(softmax_type), _ptr(softmax_offset))
     tail = (int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
-    if seq_lens_q is None and seq_lens_kv is None:
+    if bias is not None:
+        if seq_lens_q is not None or seq_lens_kv is not None:
+            raise ValueError("bias with padded batches is not supported")
+        Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
+        if dbias is not None:
+            _check(dbias, "dbias", torch.float32, 4)
+            if dbias.shape != bias.shape:
+                raise ValueError("dbias must have the bias's shape")
+        st = _load().attn_bwd_bias(*args[:10], _ptr(bias), Bb, Hb, _ptr(dbias), *args[10:], *tail)
+    elif seq_lens_q is None and seq_lens_kv is None:
         st = _load().attn_bwd(*args, *tail)
     else:
         st = _load().attn_bwd_varlen(*args, _ptr(seq_lens_q), _ptr(seq_lens_kv), *tail)
@@ -343,7 +374,7 @@ def sdpa_forward_fp8(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, s
 
 
 def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-                 seq_lens_q=None, seq_lens_kv=None, stream=None):
+                 seq_lens_q=None, seq_lens_kv=None, bias=None, stream=None):
     """Allocate O and LSE, run attn_fwd, return (o, lse)."""
     B, S_q, H_q, _ = q.shape
     d_v = v.shape[3]
@@ -351,22 +382,25 @@ def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softm
     lse = torch.empty((B, H_q, S_q), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, o, lse, causal=causal, window=window, softmax_type=softmax_type,
              softmax_offset=softmax_offset, scale=scale, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv,
-             stream=stream)
+             bias=bias, stream=stream)
     return o, lse
 
 
 def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None,
-                  scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None, stream=None):
-    """Allocate dQ, dK, dV (and d_offset for the learnable sink), run attn_bwd, return them."""
+                  scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None, bias=None,
+                  stream=None):
+    """Allocate dQ, dK, dV (and d_offset for the learnable sink), run attn_bwd, return them;
+    with a bias, also dbias (fp32, the bias's shape) as a fifth output."""
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     st = _stype(softmax_type)
     d_off = torch.empty((q.shape[2],), dtype=torch.float32, device=q.device) if st == LEARNABLE else None
+    dbias = torch.empty(bias.shape, dtype=torch.float32, device=q.device) if bias is not None else None
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_off, causal=causal, window=window, softmax_type=st,
              softmax_offset=softmax_offset, scale=scale, deterministic=deterministic, workspace=workspace,
-             seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, stream=stream)
-    return dq, dk, dv, d_off
+             seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, bias=bias, dbias=dbias, stream=stream)
+    return (dq, dk, dv, d_off) if bias is None else (dq, dk, dv, d_off, dbias)
 
 
 class SDPAFunction(torch.autograd.Function):

@@ -166,11 +166,29 @@ int attn_last_device_error(void* stream, int* site) {
   return ATTN_ERR_DEVICE_TIMEOUT;
 }
 
-int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+// Checks of an additive bias [bias_B, bias_H, S_q, S_kv] (bf16, 16-byte aligned) and
+// its element strides (0 along a broadcast dim).
+static int check_bias(const void* bias, int bias_B, int bias_H, int B, int H_q, int d_qk, int d_v, long long* sb,
+                      long long* sh, int S_q, int S_kv) {
+  if (!bias || (bias_B != 1 && bias_B != B) || (bias_H != 1 && bias_H != H_q)) return ATTN_ERR_INVALID_ARG;
+  if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(bias)) return ATTN_ERR_MISALIGNED;
+  *sh = bias_H == 1 ? 0 : (long long)S_q * S_kv;
+  *sb = bias_B == 1 ? 0 : (long long)bias_H * S_q * S_kv;
+  return ATTN_OK;
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
                     int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
-                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, void* stream) {
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, const void* bias,
+                    int bias_B, int bias_H, void* stream) {
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
   if (st != ATTN_OK) return st;
+  long long bsb = 0, bsh = 0;
+  if (bias) {
+    st = check_bias(bias, bias_B, bias_H, B, H_q, d_qk, d_v, &bsb, &bsh, S_q, S_kv);
+    if (st != ATTN_OK) return st;
+  }
   if (B == 0 || S_q == 0) return ATTN_OK;
   if (!q || !o || !lse || (S_kv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
@@ -201,6 +219,9 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.err = err;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.bias_sb = bsb;
+  p.bias_sh = bsh;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] { return sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s); });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
@@ -209,6 +230,21 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
     return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+                    int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
+                  softmax_offset, seq_lens_q, seq_lens_kv, nullptr, 1, 1, stream);
+}
+
+int attn_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, const void* bias, int bias_B,
+                  int bias_H, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale, int causal,
+                  int window, int softmax_type, const float* softmax_offset, void* stream) {
+  if (!bias) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
+                  softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
@@ -223,21 +259,33 @@ size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int 
   return ws_layout(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, use_fused_dq(d_qk, d_v, deterministic)).total;
 }
 
-int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                     void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
                     int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
-                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, int deterministic,
-                    void* workspace, size_t workspace_bytes, void* stream) {
-  if ((reinterpret_cast<uintptr_t>(seq_lens_q) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens_kv) & 3u))
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, const void* bias,
+                    int bias_B, int bias_H, float* dbias, int deterministic, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if ((reinterpret_cast<uintptr_t>(seq_lens_q) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens_kv) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dbias) & 3u))
     return ATTN_ERR_MISALIGNED;
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
   if (st != ATTN_OK) return st;
+  long long bsb = 0, bsh = 0;
+  if (bias) {
+    st = check_bias(bias, bias_B, bias_H, B, H_q, d_qk, d_v, &bsb, &bsh, S_q, S_kv);
+    if (st != ATTN_OK) return st;
+    // a broadcast dbias sums several (b, h) with fp32 atomics: not bitwise reproducible
+    if (deterministic && dbias && ((bias_B == 1 && B > 1) || (bias_H == 1 && H_q > 1))) return ATTN_ERR_UNSUPPORTED;
+  }
+  const size_t dbias_bytes = bias && dbias ? sizeof(float) * (size_t)bias_B * bias_H * S_q * S_kv : 0;
   if (softmax_type == ATTN_SOFTMAX_LEARNABLE && !d_offset) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (B == 0 || (S_q == 0 && S_kv == 0)) {
     if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
+  // dbias accumulates with atomics from zero (no visible pair: it stays zero)
+  if (dbias_bytes && cudaMemsetAsync(dbias, 0, dbias_bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
   if ((S_q > 0 && (!q || !o || !dout || !lse || !dq)) || (S_kv > 0 && (!k || !v || !dk || !dv)))
     return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
@@ -282,6 +330,10 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.bias_sb = bsb;
+  p.bias_sh = bsh;
+  p.dbias = bias ? dbias : nullptr;
   p.ns = w.ns;
   p.dk_part = w.ns > 1 ? reinterpret_cast<float*>(ws + w.dk_part) : nullptr;
   p.dv_part = w.ns > 1 ? reinterpret_cast<float*>(ws + w.dv_part) : nullptr;
@@ -344,6 +396,27 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
     }
   }
   return ATTN_OK;
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
+                    int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                    const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, int deterministic,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
+                  window, softmax_type, softmax_offset, seq_lens_q, seq_lens_kv, nullptr, 1, 1, nullptr,
+                  deterministic, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, float* d_offset, const void* bias, int bias_B, int bias_H,
+                  float* dbias, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale,
+                  int causal, int window, int softmax_type, const float* softmax_offset, int deterministic,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!bias) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
+                  window, softmax_type, softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, dbias,
+                  deterministic, workspace, workspace_bytes, stream);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

@@ -85,7 +85,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
     const size_t bh = (size_t)b * p.H_q + h;
     const bool real = i < Lq;
     p.Dsum[bh * p.S_pad + i] = real ? dsum[threadIdx.x] : 0.f;
-    p.nlse2[bh * p.S_pad + i] = real ? -p.lse[bh * p.S_q + i] * kLog2e : -INFINITY;
+    // a row with no probability mass (LSE = -inf: no visible key, or a bias of -inf on
+    // every key) gets -inf too, so every P of it is exp2(-inf) = 0 without a NaN
+    const float l = real ? p.lse[bh * p.S_q + i] : -INFINITY;
+    p.nlse2[bh * p.S_pad + i] = l == -INFINITY ? -INFINITY : -l * kLog2e;
   }
 }
 
@@ -182,7 +185,7 @@ constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
               kKvDvDone, kKvDkDone };
 
-template <int D_QK, int D_V, bool FUSE_DQ, bool VL>
+template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false>
 __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -386,10 +389,13 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     const int key = n0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2;
+    // bias: this thread's key column of the bias plane (keys past S_kv read key 0; their P is 0)
+    const int bkey = key < p.S_kv ? key : 0;
     bool ok = true;
     for (int s = 0; s < nsteps && ok; ++s) {
       const int st = s % C::NQ;
       const int q0 = (ilo + s % nq) * C::BQ;
+      [[maybe_unused]] const long long bplane = BIAS ? b * p.bias_sb + (h0 + s / nq) * p.bias_sh : 0;
       const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
       const float* dd = l2 + C::BQ;
       const int slot = s & 1;
@@ -404,6 +410,15 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         float lv[32];  // -LSE * log2(e) of the 32 queries
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
+        if constexpr (BIAS) {  // + bias * log2(e) (queries past S_q read 0; their P is 0)
+          const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int qq = q0 + 32 * w + c;
+            const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
+            lv[c] = fmaf(bv, kLog2e, lv[c]);
+          }
+        }
         tmem_ld_wait();
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -453,6 +468,14 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
                                   f2_pack(dv4[2 * c], dv4[2 * c + 1]))),
                     a, bq);
           dsk[c] = pack_bf16x2(a, bq);
+          if constexpr (BIAS) {  // dbias = dS, summed with fp32 atomics over the (b, h) sharing it
+            if (p.dbias && key < p.S_kv) {
+              const int qq = q0 + 32 * w + 2 * c;
+              float* dcol = p.dbias + bplane + key;
+              if (qq < p.S_q) atomicAdd(dcol + (size_t)qq * p.S_kv, a);
+              if (qq + 1 < p.S_q) atomicAdd(dcol + (size_t)(qq + 1) * p.S_kv, bq);
+            }
+          }
         }
       }
       tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
@@ -579,6 +602,14 @@ static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   // padded batches get the instantiation with the per-entry lengths and row tests
   auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true>
                                     : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
+  if (p.bias) {  // bias instantiations: full-length batches, d_qk = d_v in {64, 128}
+    if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
+      if (p.seq_q || p.seq_kv) return -2;
+      kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, true>;
+    } else {
+      return -2;
+    }
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
@@ -636,7 +667,7 @@ struct QCfg {
 
 enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone };
 
-template <int D_QK, int D_V, bool VL>
+template <int D_QK, int D_V, bool VL, bool BIAS = false>
 __global__ void __launch_bounds__(352, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -803,6 +834,10 @@ __global__ void __launch_bounds__(352, 1)
       nl2row = p.nlse2[ri];
       drow = p.Dsum[ri];
     }
+    // bias: this row of the bias plane (rows past S_q read row S_q - 1; their P is 0)
+    [[maybe_unused]] const __nv_bfloat16* brow =
+        BIAS ? p.bias + b * p.bias_sb + h * p.bias_sh + (size_t)min(i, p.S_q - 1) * p.S_kv : nullptr;
+    [[maybe_unused]] const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
     bool ok = true;
     for (int n = 0; n < nj && ok; ++n) {
       const int k0 = (jlo + n) * C::BN + 64 * w;
@@ -820,15 +855,35 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive(s_free);  // S is in registers: the next S may be written
         // P = exp2(S * scale * log2(e) - LSE * log2(e)), one f32x2 FMA per key pair
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2row, nl2row);
+        if constexpr (BIAS) {  // (+ bias * log2(e)): the bias enters through the addend
+          const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1, y0, y1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2x2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, nl2x2), y0, y1);
-          pr[c] = ex2(x0);
-          pr[c + 1] = ex2(x1);
-          pr[32 + c] = ex2(y0);
-          pr[32 + c + 1] = ex2(y1);
+          for (int c8 = 0; c8 < 64; c8 += 8) {
+            float bv[8];
+            load_bias8(brow, k0 + c8, p.S_kv, bias_vec, bv);
+            const uint32_t* src = c8 < 32 ? ra : rb;
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const int c = (c8 % 32) + e;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(src[c]), __uint_as_float(src[c + 1])), sl2x2,
+                               f2_fma(f2_pack(bv[e], bv[e + 1]), l2e2, nl2x2)),
+                        x0, x1);
+              pr[c8 + e] = ex2(x0);
+              pr[c8 + e + 1] = ex2(x1);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1, y0, y1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2x2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, nl2x2), y0, y1);
+            pr[c] = ex2(x0);
+            pr[c + 1] = ex2(x1);
+            pr[32 + c] = ex2(y0);
+            pr[32 + c + 1] = ex2(y1);
+          }
         }
       }
       if (!full) {  // this row sees keys [vlo, vhi]: two compares per key
@@ -909,6 +964,14 @@ static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   using C = QCfg<D_QK, D_V>;
   // padded batches get the instantiation with the per-entry lengths and row tests
   auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
+  if (p.bias) {
+    if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
+      if (p.seq_q || p.seq_kv) return -2;
+      kern = attn_bwd_q_kernel<D_QK, D_V, false, true>;
+    } else {
+      return -2;
+    }
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;

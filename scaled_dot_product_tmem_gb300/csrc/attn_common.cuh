@@ -11,6 +11,8 @@
 // mask plus sliding window; codelab "Speed up attention on GPU with cuDNN and
 // TransformerEngine", step 7: query i sees keys j <= i.)
 #pragma once
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 namespace sdpa {
@@ -101,5 +103,31 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Additive bias ("JAX: Single-GPU Attention with TransformerEngine", section "Other
+// attention knobs": `bias` with an `attn_bias_type`): a bf16 [Bb, Hb, S_q, S_kv] tensor
+// added to the scaled scores; Bb in {1, B} and Hb in {1, H_q} broadcast, expressed as
+// element strides that are 0 along a broadcast dim.
+__device__ __forceinline__ float bf16_bits_to_float(unsigned short u) { return __uint_as_float((uint32_t)u << 16); }
+
+// 8 consecutive bias values of one row, starting at key k (0 for keys >= S_kv).  vec:
+// S_kv is a multiple of 8 and k of 8, so one 16-byte load covers them (all or none
+// below S_kv).
+__device__ __forceinline__ void load_bias8(const __nv_bfloat16* row, int k, int S_kv, bool vec, float (&out)[8]) {
+  if (vec) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (k < S_kv) w = __ldg(reinterpret_cast<const uint4*>(row + k));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      out[2 * q] = __uint_as_float(ws[q] << 16);
+      out[2 * q + 1] = __uint_as_float(ws[q] & 0xFFFF0000u);
+    }
+  } else {
+    const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[e] = (k + e < S_kv) ? bf16_bits_to_float(__ldg(r + k + e)) : 0.f;
+  }
+}
 
 }  // namespace sdpa

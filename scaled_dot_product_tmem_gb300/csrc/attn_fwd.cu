@@ -34,6 +34,10 @@
 // while the row sum keeps the fp32 values; O is multiplied by descale_v / l.
 // Source for the FP8 forward: "Speed up attention on GPU with cuDNN and
 // TransformerEngine", step 10, section "Inspect the FP8 path".
+//
+// Bias instantiation (BIAS): each softmax thread reads its row of the bf16 bias for
+// the 128 keys of a tile and forms t = s * scale * log2(e) + bias * log2(e); the
+// chunk maxima are retaken over t, and the exponent is t - max.
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
@@ -106,7 +110,7 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi)
 
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
 
-template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false>
+template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false, bool BIAS = false>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -319,6 +323,10 @@ __global__ void __launch_bounds__(320, 1)
     // bring the scores and O back to the real values
     const float sl2 = F8 ? p.scale_log2 * (*p.descale_q) * (*p.descale_k) : p.scale_log2;
     const float o_mul = F8 ? *p.descale_v : 1.f;
+    // with a bias the scores are turned into log2-unit logits before the max, so the
+    // max and the exponent then take them as they are
+    const float sx = BIAS ? 1.f : sl2;
+    const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
     bool ok = true;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
@@ -332,6 +340,8 @@ __global__ void __launch_bounds__(320, 1)
       const bool my_active = t ? T.active[1] : T.active[0];
       const int my_jlo = t ? T.jlo[1] : T.jlo[0], my_jhi = t ? T.jhi[1] : T.jhi[0];
       const int i = m0 + t * C::BM + r;  // query row
+      const __nv_bfloat16* brow = nullptr;  // this row of the bias (rows past S_q read row S_q - 1)
+      if constexpr (BIAS) brow = p.bias + b * p.bias_sb + h * p.bias_sh + (size_t)min(i, p.S_q - 1) * p.S_kv;
       // running max (in scaled log2 units) and denominator; the sink starts them
       float m_run = -INFINITY, l = 0.f;
       if (p.softmax_type == 1) { m_run = 0.f; l = 1.f; }
@@ -357,6 +367,24 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
           }
           const int k0 = j * C::BN;
+          if constexpr (BIAS) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float m = -INFINITY;
+#pragma unroll
+              for (int e8 = 0; e8 < 4; ++e8) {
+                float bv[8];
+                load_bias8(brow, k0 + 32 * q + 8 * e8, p.S_kv, bias_vec, bv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  float& x = s[32 * q + 8 * e8 + e];
+                  x = fmaf(bv[e], kLog2e, x * sl2);
+                  m = fmaxf(m, x);
+                }
+              }
+              cmax[q] = m;
+            }
+          }
           if (!tile_fully_visible<VL>(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
             // the keys this row sees form one interval [vlo, vhi], so a chunk whose two
             // ends are inside it is fully visible
@@ -376,7 +404,7 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
           const float mx = fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
-          const float m_tile = mx * sl2;
+          const float m_tile = mx * sx;
           // Lazy rescale, decided per warp (the TMEM loads/stores are warp-collective):
           // when any row's max grew by more than 2^8, every row of the warp moves to
           // its new max (alpha = 1 for rows whose max did not change).
@@ -400,7 +428,7 @@ __global__ void __launch_bounds__(320, 1)
           const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
           // p = 2^(s * scale * log2e - m), paired: one f32x2 FMA per two keys; the row sum
           // is kept in four paired partial sums so no long add chain forms
-          const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+          const uint64_t sl2x2 = f2_pack(sx, sx), negm2 = f2_pack(-m_sub, -m_sub);
           uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -487,11 +515,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false>
+template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false, bool BIAS = false>
 static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                         cudaStream_t stream) {
   using C = FwdCfg<D_QK, D_V, NK, NV, F8>;
-  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL, F8>;
+  auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL, F8, BIAS>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
@@ -525,6 +553,12 @@ static int launch_attn_fwd_vl(int d_qk, int d_v, const CUtensorMap& tq, const CU
 
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                     const FwdParams& p, cudaStream_t stream) {
+  if (p.bias) {  // bias instantiations: full-length batches, d_qk = d_v in {64, 128}
+    if (p.seq_q || p.seq_kv) return -2;
+    if (d_qk == 128 && d_v == 128) return launch_fwd_t<128, 128, 2, 2, false, false, true>(tq, tk, tv, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_fwd_t<64, 64, 4, 4, false, false, true>(tq, tk, tv, p, stream);
+    return -2;
+  }
   // padded batches get the instantiation with the per-entry lengths and row tests
   return (p.seq_q || p.seq_kv) ? launch_attn_fwd_vl<true>(d_qk, d_v, tq, tk, tv, p, stream)
                                : launch_attn_fwd_vl<false>(d_qk, d_v, tq, tk, tv, p, stream);

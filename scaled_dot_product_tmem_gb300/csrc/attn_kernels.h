@@ -21,6 +21,10 @@ struct FwdParams {
   const float* descale_q = nullptr;
   const float* descale_k = nullptr;
   const float* descale_v = nullptr;
+  // additive bias [Bb, Hb, S_q, S_kv] (bf16) or null; element strides of batch and head
+  // (0 along a broadcast dim)
+  const __nv_bfloat16* bias = nullptr;
+  long long bias_sb = 0, bias_sh = 0;
 };
 
 // Returns 0 on a successful launch, -2 for an unsupported (d_qk, d_v), -1 on a
@@ -61,6 +65,12 @@ struct BwdParams {
   float* dv_part;             // ns > 1: [ns, B, S_kv, H_kv, d_v] fp32 partial dV
   float* dq_acc;              // [B, S_q, H_q, d_qk] fp32 workspace (atomic dQ path) or null
   int* err;
+  // additive bias [Bb, Hb, S_q, S_kv] (bf16) or null, with the element strides of batch
+  // and head (0 along a broadcast dim); dbias: fp32, same shape and strides, zeroed by
+  // the caller, accumulated with fp32 atomics (null: not wanted)
+  const __nv_bfloat16* bias = nullptr;
+  long long bias_sb = 0, bias_sh = 0;
+  float* dbias = nullptr;
 };
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);

@@ -47,3 +47,11 @@ def make_inputs(shape: Shape, seed: int, *, with_dout: bool = True,
     if learnable_offset:
         out["offset"] = torch.randn((s.H_q,), generator=g, dtype=torch.float32)
     return out
+
+
+def make_bias(shape, seed: int, dtype=torch.bfloat16):
+    """An additive attention bias of `shape` ([Bb, Hb, S_q, S_kv]): fp32 N(0, 1) from
+    its own CPU generator (seeded `seed`), rounded to bf16."""
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed))
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(dtype)

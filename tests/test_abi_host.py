@@ -140,3 +140,23 @@ def test_fp8_argument_validation(lib):
     assert qz(aout=ctypes.c_void_p(0x10022)) == MISALIGNED
     assert lib.attn_fp8_amax(P, ctypes.c_size_t(8), None, None) == INVALID
     assert lib.attn_fp8_amax(MIS, ctypes.c_size_t(8), P, None) == MISALIGNED
+
+
+def test_bias_argument_validation(lib):
+    def fb(bias=P, Bb=1, Hb=4, B=2, Hq=4, Hkv=2, d=128, dv=None):
+        return lib.attn_fwd_bias(P, P, P, P, P, bias, Bb, Hb, B, 64, 64, Hq, Hkv, d, d if dv is None else dv,
+                                 ctypes.c_float(0.0), 1, -1, 0, None, None)
+
+    assert fb(bias=None) == INVALID
+    assert fb(Bb=3) == INVALID and fb(Hb=2) == INVALID   # broadcast dims are 1 or the full size
+    assert fb(d=192, dv=128) == UNSUPPORTED              # bias kernels: d_qk = d_v in {64, 128}
+    assert fb(bias=MIS) == MISALIGNED
+    assert fb(B=0, Bb=1) == OK
+
+    def bb(Bb=1, Hb=4, dbias=P, det=1, bias=P):
+        return lib.attn_bwd_bias(P, P, P, P, P, P, P, P, P, None, bias, Bb, Hb, dbias, 2, 64, 64, 4, 2, 128, 128,
+                                 ctypes.c_float(0.0), 1, -1, 0, None, det, P, ctypes.c_size_t(1 << 30), None)
+
+    assert bb() == UNSUPPORTED                           # broadcast dbias is summed with atomics
+    assert bb(Bb=2, Hb=4, dbias=ctypes.c_void_p(0x10002)) == MISALIGNED
+    assert bb(bias=None) == INVALID

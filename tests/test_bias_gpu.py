@@ -1,0 +1,156 @@
+"""Additive attention bias on the GPU (attn_fwd_bias / attn_bwd_bias) against the fp64
+oracle: O, LSE, dQ, dK, dV, d_offset and dbias with the tolerances of the bf16 path
+(dbias is a gradient: relative L2 <= 1e-2), for broadcast and per-(b, h) biases,
+-inf entries, head splits (MQA) and both dQ paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
+from parity_util import TOL_GRAD, TOL_LSE, TOL_O, rel_l2
+from scaled_dot_product_tmem_gb300.inputs import Shape, make_bias, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _sdpa():
+    import scaled_dot_product_tmem_gb300 as sdpa
+    return sdpa
+
+
+def _run(x, bias, *, causal, window, st, scale, deterministic):
+    sdpa = _sdpa()
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    off = x["offset"].to(dev) if st == LEARNABLE else None
+    kw = dict(causal=causal, window=window, softmax_type=st, softmax_offset=off, scale=scale or 0.0)
+    bg = bias.to(dev)
+    o, lse = sdpa.sdpa_forward(q, k, v, bias=bg, **kw)
+    dq, dk, dv, d_off, dbias = sdpa.sdpa_backward(q, k, v, o, do, lse, bias=bg, deterministic=deterministic, **kw)
+    torch.cuda.synchronize()
+    st_, site = sdpa.attn_last_device_error()
+    assert st_ == 0, f"device error {st_} site {site:#x}"
+    out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dbias": dbias}
+    if d_off is not None:
+        out["d_offset"] = d_off
+    return {n: t.float().cpu().numpy() for n, t in out.items()}
+
+
+def _ref(x, bias, *, causal, window, st, scale):
+    xd = {n: t.double().numpy() for n, t in x.items()}
+    kw = dict(causal=causal, window=window, softmax_type=st, scale=scale, bias=bias.double().numpy(),
+              offset=xd["offset"] if st == LEARNABLE else None)
+    f = oracle.attention_fwd(xd["q"], xd["k"], xd["v"], **kw)
+    g = oracle.attention_bwd(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
+    out = {"o": f["o"], "lse": f["lse"], "dq": g["dq"], "dk": g["dk"], "dv": g["dv"], "dbias": g["dbias"]}
+    if st == LEARNABLE:
+        out["d_offset"] = g["d_offset"]
+    return out
+
+
+def _compare(gpu, ref, what):
+    e = float(np.abs(gpu["o"] - ref["o"]).max())
+    assert e <= TOL_O, f"{what}: O max-abs {e}"
+    fin = np.isfinite(ref["lse"])
+    assert np.array_equal(fin, np.isfinite(gpu["lse"])), f"{what}: LSE finiteness"
+    if fin.any():
+        e = float(np.abs(gpu["lse"][fin] - ref["lse"][fin]).max())
+        assert e <= TOL_LSE, f"{what}: LSE max-abs {e}"
+    for n in ("dq", "dk", "dv", "d_offset", "dbias"):
+        if n in ref:
+            e = rel_l2(gpu[n], ref[n])
+            assert e <= TOL_GRAD, f"{what}: {n} relative L2 {e}"
+
+
+CASES = [
+    # name, shape, causal, window, softmax type, scale, bias (Bb, Hb), deterministic
+    ("gqa_batch_broadcast", Shape(2, 300, 300, 4, 2, 128, 128), True, -1, VANILLA, None, (1, 4), False),
+    ("d64_window_obo", Shape(1, 256, 256, 4, 1, 64, 64), True, 100, OFF_BY_ONE, None, (1, 4), False),
+    # (learnable here makes d_offset ~1 % of sum |p_sink D|: a cancellation that bf16 O alone
+    # moves by 0.4 %; the learnable sink is covered by the causal ragged case below)
+    ("noncausal_rect_head_broadcast", Shape(2, 200, 333, 2, 2, 64, 64), False, -1, OFF_BY_ONE, 0.2, (2, 1), False),
+    ("per_bh_deterministic", Shape(2, 256, 256, 4, 2, 128, 128), True, -1, VANILLA, None, (2, 4), True),
+    ("mqa_head_splits_full_broadcast", Shape(1, 300, 300, 8, 1, 128, 128), True, -1, VANILLA, None, (1, 1), False),
+    ("ragged_det_d64", Shape(1, 77, 77, 2, 2, 64, 64), True, 10, LEARNABLE, None, (1, 2), True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_bias_parity(case):
+    name, shape, causal, window, st, scale, (Bb, Hb), det = case
+    x = make_inputs(shape, 500 + len(name), learnable_offset=(st == LEARNABLE))
+    bias = make_bias((Bb, Hb, shape.S_q, shape.S_kv), 600 + len(name))
+    kw = dict(causal=causal, window=window, st=st, scale=scale)
+    gpu = _run(x, bias, deterministic=det, **kw)
+    _compare(gpu, _ref(x, bias, **kw), name)
+    if det:  # one contributor per dbias entry: bitwise reproducible
+        again = _run(x, bias, deterministic=det, **kw)
+        for n in gpu:
+            assert np.array_equal(gpu[n], again[n]), n
+
+
+def test_minus_inf_bias_masks_keys_and_whole_rows():
+    shape = Shape(1, 200, 200, 2, 1, 64, 64)
+    x = make_inputs(shape, 71)
+    bias = make_bias((1, 2, 200, 200), 72).float()
+    bias[:, :, :, 50:90] = float("-inf")      # a band of keys removed for every row
+    bias[:, 1, 120:130, :] = float("-inf")    # whole rows of head 1: no key left
+    bias = bias.to(torch.bfloat16)
+    kw = dict(causal=True, window=-1, st=VANILLA, scale=None)
+    gpu = _run(x, bias, deterministic=False, **kw)
+    ref = _ref(x, bias, **kw)
+    assert np.all(gpu["o"][0, 120:130, 1] == 0) and np.all(np.isneginf(gpu["lse"][0, 1, 120:130]))
+    assert np.all(gpu["dbias"][..., 50:90] == 0)
+    _compare(gpu, ref, "-inf bias")
+
+
+def test_zero_bias_equals_no_bias():
+    sdpa = _sdpa()
+    shape = Shape(1, 256, 256, 4, 2, 128, 128)
+    x = make_inputs(shape, 81)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    z = torch.zeros((1, 1, 256, 256), dtype=torch.bfloat16, device="cuda")
+    o0, l0 = sdpa.sdpa_forward(q, k, v, causal=True)
+    o1, l1 = sdpa.sdpa_forward(q, k, v, causal=True, bias=z)
+    torch.cuda.synchronize()
+    assert float((o0.float() - o1.float()).abs().max()) <= 2e-3
+    assert float((l0 - l1).abs().max()) <= 1e-5
+
+
+def test_bias_rejections():
+    sdpa = _sdpa()
+    shape = Shape(2, 64, 64, 4, 2, 128, 128)
+    x = make_inputs(shape, 91)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    b = torch.zeros((1, 4, 64, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = sdpa.sdpa_forward(q, k, v, bias=b)
+    with pytest.raises(sdpa.AttnError, match="unsupported"):   # broadcast dbias + deterministic
+        sdpa.sdpa_backward(q, k, v, o, do, lse, bias=b, deterministic=True)
+    q3 = torch.zeros((2, 64, 4, 192), dtype=torch.bfloat16, device="cuda")
+    k3 = torch.zeros((2, 64, 2, 192), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sdpa.AttnError, match="unsupported"):   # MLA dims have no bias kernel
+        sdpa.sdpa_forward(q3, k3, v, bias=b)
+
+
+def test_bias_full_size_sampled():
+    """The bias workload of bench.py (B=2, S=4096, H_q=32, H_kv=8, d=128, causal, bias
+    [1, 32, S, S]): the oracle runs kv-head group 3 for both batch entries; dbias of
+    those heads is the sum of the two entries' dS."""
+    shape = Shape(2, 4096, 4096, 32, 8, 128, 128)
+    x = make_inputs(shape, 8)
+    bias = make_bias((1, 32, 4096, 4096), 9)
+    gpu = _run(x, bias, causal=True, window=-1, st=VANILLA, scale=None, deterministic=False)
+    G, g = 4, 3
+    hs = slice(g * G, (g + 1) * G)
+    dbias = 0
+    for b in range(2):
+        xs = {"q": x["q"][b:b + 1, :, hs], "k": x["k"][b:b + 1, :, g:g + 1], "v": x["v"][b:b + 1, :, g:g + 1],
+              "dout": x["dout"][b:b + 1, :, hs]}
+        ref = _ref(xs, bias[:, hs], causal=True, window=-1, st=VANILLA, scale=None)
+        dbias = dbias + ref.pop("dbias")
+        unit = {"o": gpu["o"][b:b + 1, :, hs], "lse": gpu["lse"][b:b + 1, hs], "dq": gpu["dq"][b:b + 1, :, hs],
+                "dk": gpu["dk"][b:b + 1, :, g:g + 1], "dv": gpu["dv"][b:b + 1, :, g:g + 1]}
+        _compare(unit, ref, f"bias unit b={b}")
+    e = rel_l2(gpu["dbias"][:, hs], dbias)
+    assert e <= TOL_GRAD, f"dbias of heads {hs}: relative L2 {e}"
