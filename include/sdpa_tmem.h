@@ -255,6 +255,19 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* d
                  float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* stream);
 
 /*
+ * Failure-path self-test.  Every pipeline wait in the kernels is bounded (about one
+ * second); on expiry the kernel stores 0x100 + a site code in a per-GPU device error
+ * word, every other wait gives up at once, in-flight copies and MMAs are drained with
+ * bounded waits, TMEM is freed and the kernel returns, so the CUDA context stays
+ * usable and attn_last_device_error() reports ATTN_ERR_DEVICE_TIMEOUT with the site.
+ * attn_selftest_wait_timeout enqueues one warp that waits on a barrier nobody
+ * arrives at, through that same bounded wait, so the path can be checked without a
+ * fault: after it, attn_last_device_error() returns ATTN_ERR_DEVICE_TIMEOUT with
+ * site 0x100 + `site` (0..255) and clears the word.
+ */
+int attn_selftest_wait_timeout(int site, void* stream);
+
+/*
  * Measurement aid (off by default).  While enabled, the attn_fwd*, attn_bwd* and
  * attn_fp8_* calls record
  * a pair of CUDA events on their launch stream around each class of kernel they

@@ -75,6 +75,8 @@ def _load():
     lib.attn_timing_read.restype = i
     lib.attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.attn_last_device_error.restype = i
+    lib.attn_selftest_wait_timeout.argtypes = [i, vp]
+    lib.attn_selftest_wait_timeout.restype = i
     lib.attn_fwd_bias.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, vp]
     lib.attn_fwd_bias.restype = i
     lib.attn_bwd_bias.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, i, i, i, i, i, i, i, f, i, i,
@@ -138,6 +140,13 @@ def attn_last_device_error(stream=None):
     site = ctypes.c_int(0)
     st = _load().attn_last_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def attn_selftest_wait_timeout(site: int, stream=None) -> None:
+    """Enqueue the failure-path self-test (a bounded wait that runs out; no fault)."""
+    st = _load().attn_selftest_wait_timeout(int(site), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_selftest_wait_timeout")
 
 
 def _check_lens(t, name, B):

@@ -520,6 +520,17 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* d
   return ATTN_OK;
 }
 
+int attn_selftest_wait_timeout(int site, void* stream) {
+  if (site < 0 || site > 0xFF) return ATTN_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  if (sdpa::launch_selftest_wait(err, site, static_cast<cudaStream_t>(stream)) != 0) {
+    set_error("self-test launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
 int attn_timing_enable(int on) {
   std::lock_guard<std::mutex> g(g_timing_mu);
   g_timing_on = on != 0;

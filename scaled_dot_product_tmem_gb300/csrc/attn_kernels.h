@@ -89,6 +89,10 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
 
+// One warp waits on an mbarrier nobody arrives at: after the wait limit it records
+// kErrTimeoutBase + site in *err and returns (the failure path, without a fault).
+int launch_selftest_wait(int* err, int site, cudaStream_t stream);
+
 // Device error word of the current device (null if CUDA cannot report it).
 int* device_error_word();
 
