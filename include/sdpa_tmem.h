@@ -5,7 +5,10 @@
  *     O = softmax(scale * Q K^T + mask) V      on BSHD tensors,
  *
  * with grouped-query heads, a causal mask with an optional left sliding window,
- * distinct Q/K and V head dims, and three sink softmax types.
+ * distinct Q/K and V head dims, and three sink softmax types; plus padded batches
+ * with per-entry lengths (attn_fwd_varlen / attn_bwd_varlen), an additive bias with
+ * its gradient (attn_fwd_bias / attn_bwd_bias) and an E4M3 forward with per-tensor
+ * scaling (attn_fp8_amax, attn_fp8_quantize, attn_fwd_fp8).
  *
  * Where each operation is defined:
  *   - the attention itself: "Speed up attention on GPU with cuDNN and
