@@ -264,6 +264,34 @@ def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal
         raise AttnError(st, "attn_bwd_noalloc" + (f" ({msg})" if msg else ""))
 
 
+def attn_bwd_noalloc_max_scratch_bytes() -> int:
+    return int(_load().attn_bwd_noalloc_max_scratch_bytes())
+
+
+def attn_bwd_noalloc_message() -> str:
+    return _load().attn_bwd_noalloc_message().decode()
+
+
+def attn_fwd_varlen(q, k, v, o, lse, seq_lens_q, seq_lens_kv, **kw):
+    """attn_fwd on a padded batch: int32 [B] device tensors of query / key lengths."""
+    attn_fwd(q, k, v, o, lse, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, **kw)
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q, seq_lens_kv, **kw):
+    """attn_bwd on a padded batch (lengths as for attn_fwd_varlen)."""
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, **kw)
+
+
+def attn_fwd_bias(q, k, v, o, lse, bias, **kw):
+    """attn_fwd with an additive bf16 bias [1 or B, 1 or H_q, S_q, S_kv]."""
+    attn_fwd(q, k, v, o, lse, bias=bias, **kw)
+
+
+def attn_bwd_bias(q, k, v, o, dout, lse, dq, dk, dv, d_offset, bias, dbias, **kw):
+    """attn_bwd with an additive bias; dbias: fp32 tensor of the bias's shape, or None."""
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, bias=bias, dbias=dbias, **kw)
+
+
 KERNEL_CLASSES = ("fwd", "bwd_preprocess", "bwd_kv", "bwd_q", "bwd_dq_convert", "fp8_quantize")
 
 

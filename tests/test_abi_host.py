@@ -160,3 +160,10 @@ def test_bias_argument_validation(lib):
     assert bb() == UNSUPPORTED                           # broadcast dbias is summed with atomics
     assert bb(Bb=2, Hb=4, dbias=ctypes.c_void_p(0x10002)) == MISALIGNED
     assert bb(bias=None) == INVALID
+
+
+def test_binding_has_every_boundary_name():
+    """The Python binding exposes each C-ABI function under the same name."""
+    import scaled_dot_product_tmem_gb300 as sdpa
+    for n in declared_functions():
+        assert callable(getattr(sdpa, n, None)), f"{n} has no binding of the same name"
