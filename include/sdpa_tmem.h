@@ -159,8 +159,13 @@ int attn_last_device_error(void* stream, int* site);
  * nothing (no cudaMalloc, no cudaFree, no allocating library call), and keeps its
  * scratch in one fixed array inside the library: attn_bwd_noalloc_max_scratch_bytes()
  * bytes (8 MiB) per GPU, held by every GPU that loads the library until the process
- * exits.  It always runs the deterministic backward (bitwise-equal to attn_bwd with
- * deterministic != 0).
+ * exits.  It always runs the deterministic backward (query-stationary dQ), and it
+ * is itself bitwise reproducible.  Its results match attn_bwd with deterministic != 0
+ * within the gradient tolerance.  They are bitwise equal to it whenever attn_bwd walks
+ * every query head of a kv group in one CTA.  attn_bwd instead splits the group's heads
+ * across CTAs when its kv grid has fewer than 456 CTAs (3 per SM) and the group has
+ * more than one query head.  The split sums partial dK/dV slices in another fp32
+ * order; this entry point has no scratch for those slices and never splits.
  *
  * Limits and rules:
  *   - the scratch holds 8 bytes per (batch, query head, query row padded up to a

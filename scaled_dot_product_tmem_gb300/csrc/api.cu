@@ -30,12 +30,18 @@ constexpr int kMaxDevices = 64;
 
 int* device_error_ptr() {
   static int* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;  // first calls on one device from several threads fill its entry once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     set_error("cudaGetDevice", e);
     return nullptr;
   }
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device index out of the library's range (64 devices)");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> g(mu);
   if (!ptrs[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
@@ -49,28 +55,6 @@ int* device_error_ptr() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool dims_supported(int d_qk, int d_v) {
-  return (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
-}
-
-// Shared validation of sizes and flags.  Returns ATTN_OK or an error status.
-int check_common(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int causal, int window,
-                 int softmax_type, const float* softmax_offset) {
-  if (B < 0 || S_q < 0 || S_kv < 0 || H_q <= 0 || H_kv <= 0) return ATTN_ERR_INVALID_ARG;
-  if (H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (softmax_type < ATTN_SOFTMAX_VANILLA || softmax_type > ATTN_SOFTMAX_LEARNABLE) return ATTN_ERR_INVALID_ARG;
-  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && softmax_offset == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!dims_supported(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
-  if (window >= 0 && !causal) return ATTN_ERR_UNSUPPORTED;
-  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
-  return ATTN_OK;
-}
-
-float resolve_scale(float scale, int d_qk) {
-  if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(static_cast<float>(d_qk));
-  return scale;
-}
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -100,6 +84,8 @@ bool use_fused_dq(int d_qk, int d_v, int deterministic) {
 
 // ---------------------------------------------------------------------------
 // Optional timing of every kernel launch (CUDA events on the launch stream).
+// Events come from a pool that attn_timing_read refills, so after the first
+// timed steps a launch costs two event records and no event creation.
 // ---------------------------------------------------------------------------
 struct TimingRec {
   cudaEvent_t a, b;
@@ -108,19 +94,35 @@ struct TimingRec {
 std::mutex g_timing_mu;
 bool g_timing_on = false;
 std::vector<TimingRec> g_timing;
+std::vector<cudaEvent_t> g_event_pool;
+
+// An event from the pool, or a new one (null if CUDA cannot make one).  Caller holds g_timing_mu.
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
 
 // Runs `launch` (which enqueues `nlaunch` kernels of class `kind` on stream s);
 // brackets it with events when timing is on.
 template <class F>
 int timed(int kind, int nlaunch, cudaStream_t s, F&& launch) {
-  bool on;
+  cudaEvent_t a = nullptr, b = nullptr;
   {
     std::lock_guard<std::mutex> g(g_timing_mu);
-    on = g_timing_on;
+    if (!g_timing_on) return launch();
+    a = pooled_event();
+    b = pooled_event();
+    if (!a || !b) {
+      if (a) g_event_pool.push_back(a);
+      if (b) g_event_pool.push_back(b);
+      return -1;
+    }
   }
-  if (!on) return launch();
-  cudaEvent_t a = nullptr, b = nullptr;
-  if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return -1;
   cudaEventRecord(a, s);
   const int rc = launch();
   cudaEventRecord(b, s);
@@ -134,7 +136,32 @@ int timed(int kind, int nlaunch, cudaStream_t s, F&& launch) {
 namespace sdpa {
 // The device error word of the current device, for the other host files of the library.
 int* device_error_word() { return device_error_ptr(); }
+
+bool dims_supported(int d_qk, int d_v) {
+  return (d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128);
+}
+
+// Shared validation of sizes and flags.  Returns ATTN_OK or an error status.
+int check_common(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int causal, int window,
+                 int softmax_type, const float* softmax_offset) {
+  if (B < 0 || S_q < 0 || S_kv < 0 || H_q <= 0 || H_kv <= 0) return ATTN_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (softmax_type < ATTN_SOFTMAX_VANILLA || softmax_type > ATTN_SOFTMAX_LEARNABLE) return ATTN_ERR_INVALID_ARG;
+  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && softmax_offset == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!dims_supported(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED;
+  if (window >= 0 && !causal) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+float resolve_scale(float scale, int d_qk) {
+  if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(static_cast<float>(d_qk));
+  return scale;
+}
 }  // namespace sdpa
+
+using sdpa::check_common;
+using sdpa::resolve_scale;
 
 extern "C" {
 
@@ -556,8 +583,11 @@ int attn_timing_read(double* ms, int* launches, int n) {
       if (ms) ms[r.kind] += t;
       if (launches) launches[r.kind] += r.launches;
     }
-    cudaEventDestroy(r.a);
-    cudaEventDestroy(r.b);
+  }
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  for (const TimingRec& r : recs) {  // back to the pool for the next timed launches
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
   }
   return status;
 }

@@ -44,8 +44,14 @@ thread_local char g_msg[256] = "";
 unsigned char* scratch_ptr(int* status) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     snprintf(g_msg, sizeof(g_msg), "attn_bwd_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
+    *status = ATTN_ERR_CUDA;
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(g_msg, sizeof(g_msg), "attn_bwd_noalloc: device %d is past the %d devices the library tracks", dev,
+             kMaxDevices);
     *status = ATTN_ERR_CUDA;
     return nullptr;
   }
@@ -67,6 +73,20 @@ unsigned char* scratch_ptr(int* status) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Records which CUDA call failed and why; returns ATTN_ERR_CUDA.
+int cuda_failed(const char* what, cudaError_t e) {
+  snprintf(g_msg, sizeof(g_msg), "attn_bwd_noalloc: %s failed: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  return ATTN_ERR_CUDA;
+}
+// The same for a kernel launch (the reason is CUDA's last error).
+int launch_failed(const char* what) { return cuda_failed(what, cudaGetLastError()); }
+
+// cudaMemsetAsync(dst, 0, bytes) on s; ATTN_OK or ATTN_ERR_CUDA with the message set.
+int zero_async(void* dst, size_t bytes, cudaStream_t s) {
+  const cudaError_t e = cudaMemsetAsync(dst, 0, bytes, s);
+  return e == cudaSuccess ? ATTN_OK : cuda_failed("cudaMemsetAsync", e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -80,13 +100,11 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
                      const float* softmax_offset, void* stream) {
   g_msg[0] = '\0';
-  // Same argument rules as attn_bwd.
-  if (B < 0 || S_q < 0 || S_kv < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (softmax_type < ATTN_SOFTMAX_VANILLA || softmax_type > ATTN_SOFTMAX_LEARNABLE) return ATTN_ERR_INVALID_ARG;
-  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && (!softmax_offset || !d_offset)) return ATTN_ERR_INVALID_ARG;
-  if (!((d_qk == 64 || d_qk == 128 || d_qk == 192) && (d_v == 64 || d_v == 128))) return ATTN_ERR_UNSUPPORTED;
-  if (window >= 0 && !causal) return ATTN_ERR_UNSUPPORTED;
-  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  // The argument rules of attn_bwd (the same checks, shared with the other entry points).
+  const int st = sdpa::check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type,
+                                    softmax_offset);
+  if (st != ATTN_OK) return st;
+  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && !d_offset) return ATTN_ERR_INVALID_ARG;
   const size_t s_pad = (static_cast<size_t>(S_q) + 127) / 128 * 128;
   const size_t rows = static_cast<size_t>(B) * H_q * s_pad;
   const size_t need = 2 * round256(rows * sizeof(float));
@@ -98,10 +116,7 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
     return ATTN_ERR_WORKSPACE;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (B == 0 || (S_q == 0 && S_kv == 0)) {
-    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
-  }
+  if (B == 0 || (S_q == 0 && S_kv == 0)) return d_offset ? zero_async(d_offset, sizeof(float) * H_q, s) : ATTN_OK;
   if ((S_q > 0 && (!q || !o || !dout || !lse || !dq)) || (S_kv > 0 && (!k || !v || !dk || !dv)))
     return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
@@ -109,26 +124,29 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
       (reinterpret_cast<uintptr_t>(d_offset) & 3u))
     return ATTN_ERR_MISALIGNED;
   if (S_q == 0) {
-    if (cudaMemsetAsync(dk, 0, (size_t)B * S_kv * H_kv * d_qk * 2, s) != cudaSuccess ||
-        cudaMemsetAsync(dv, 0, (size_t)B * S_kv * H_kv * d_v * 2, s) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
+    int rc = zero_async(dk, (size_t)B * S_kv * H_kv * d_qk * 2, s);
+    if (rc == ATTN_OK) rc = zero_async(dv, (size_t)B * S_kv * H_kv * d_v * 2, s);
+    if (rc == ATTN_OK && d_offset) rc = zero_async(d_offset, sizeof(float) * H_q, s);
+    return rc;
   }
   int status = ATTN_OK;
   unsigned char* scratch = scratch_ptr(&status);
   if (!scratch) return status;
   int* err = sdpa::device_error_word();
-  if (!err) return ATTN_ERR_CUDA;
+  if (!err) {
+    snprintf(g_msg, sizeof(g_msg), "attn_bwd_noalloc: the device error word is unavailable (%s)",
+             attn_last_error_message());
+    return ATTN_ERR_CUDA;
+  }
 
   // Every word of the scratch that the kernels read is written earlier in the
-  // same call (real rows by the preprocess kernel, padding rows by the pad
-  // kernel), so nothing left by a previous call is ever read and nothing needs
-  // clearing.  Calls that overlap on the GPU (other streams, other threads)
-  // share the array and race.
+  // same call: the preprocess kernel writes both arrays for every real row and
+  // every padding row (D = 0, LSE * log2 e = -inf past S_q), so nothing left by a
+  // previous call is ever read and nothing needs clearing.  Calls that overlap on
+  // the GPU (other streams, other threads) share the array and race.
   sdpa::BwdParams p;
   p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
-  p.scale = (scale > 0.f && scale < 3.0e38f) ? scale : 1.0f / sqrtf(static_cast<float>(d_qk));
+  p.scale = sdpa::resolve_scale(scale, d_qk);
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
   p.window = window < 0 ? -1 : window;
@@ -151,11 +169,8 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   p.seq_kv = nullptr;
   p.err = err;
 
-  if (sdpa::launch_bwd_preprocess(d_v, p, s) != 0) return ATTN_ERR_CUDA;
-  if (S_kv == 0) {
-    if (cudaMemsetAsync(dq, 0, (size_t)B * S_q * H_q * d_qk * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
-  }
+  if (sdpa::launch_bwd_preprocess(d_v, p, s) != 0) return launch_failed("backward preprocess launch");
+  if (S_kv == 0) return zero_async(dq, (size_t)B * S_q * H_q * d_qk * 2, s);
   CUtensorMap tq64, tdo64, tq128, tdo128, tk, tv;
   if (!sdpa::make_bshd_map(&tq64, q, B, S_q, H_q, d_qk, 64) || !sdpa::make_bshd_map(&tdo64, dout, B, S_q, H_q, d_v, 64) ||
       !sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
@@ -166,10 +181,11 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   }
   int rc = sdpa::launch_bwd_kv(d_qk, d_v, tq64, tk, tv, tdo64, tq64, p, false, s);
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
-  if (rc != 0) return ATTN_ERR_CUDA;
+  if (rc != 0) return launch_failed("backward kv kernel launch");
   rc = sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
-  return rc == 0 ? ATTN_OK : ATTN_ERR_CUDA;
+  if (rc != 0) return launch_failed("backward dQ kernel launch");
+  return ATTN_OK;
 }
 
 }  // extern "C"

@@ -96,4 +96,11 @@ int launch_selftest_wait(int* err, int site, cudaStream_t stream);
 // Device error word of the current device (null if CUDA cannot report it).
 int* device_error_word();
 
+// Argument rules shared by every entry point (sizes, flags, head dims): ATTN_OK or an
+// error status of the public header.
+int check_common(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, int causal, int window,
+                 int softmax_type, const float* softmax_offset);
+// The softmax scale to use: `scale` when finite and positive, else 1 / sqrt(d_qk).
+float resolve_scale(float scale, int d_qk);
+
 }  // namespace sdpa

@@ -4,10 +4,15 @@ the launch path, or C callers without a device allocator).  It keeps its scratch
 a fixed array inside the library.
 
 This file is collected last on purpose: if it fails, a run that stops at the first
-failure has already run every other test.  It checks the entry point, called through
-the C ABI, against attn_bwd (the workspace entry point) on two calls in a row with
-different shapes, so the second call runs on an array that still holds the first
-call's contents.
+failure has already run every other test.  It calls the entry point through the C
+ABI three times in a row with different shapes, so each later call runs on an array
+that still holds the previous call's contents, and checks:
+  * against attn_bwd with deterministic != 0: bitwise equal where attn_bwd also walks
+    every query head of a kv group in one CTA (no head split: the same kernels on the
+    same inputs), within the gradient tolerance where attn_bwd splits the heads (its
+    partial dK/dV slices add in another fp32 order);
+  * against the fp64 oracle on the first shape, with the tolerances of every other
+    parity test.
 """
 import ctypes
 
@@ -15,11 +20,18 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL_GRAD, Shape, make_inputs, rel_l2
+from parity_util import TOL_GRAD, Shape, compare, make_inputs, oracle_run, rel_l2
 
 pytestmark = pytest.mark.gpu
 
 OK, WORKSPACE = 0, 6
+NUM_SMS = 152  # attn_bwd splits a group's query heads when its kv grid has < 3 CTAs per SM
+
+
+def _splits(shape):
+    """Whether attn_bwd splits the query heads of a kv group for this shape."""
+    ctas = -(-shape.S_kv // 128) * shape.H_kv * shape.B
+    return ctas < 3 * NUM_SMS and shape.H_q // shape.H_kv > 1
 
 
 def _run_both(sdpa, lib, shape, seed, st, window):
@@ -45,18 +57,36 @@ def _run_both(sdpa, lib, shape, seed, st, window):
     assert status == 0, f"device error {status} at site {site:#x}"
     got = [dq, dk, dv] + ([d_off] if d_off is not None else [])
     want = [ref[0], ref[1], ref[2]] + ([ref[3]] if d_off is not None else [])
-    for name, g, w in zip(("dq", "dk", "dv", "d_offset"), got, want):
-        err = rel_l2(g.float().cpu().numpy(), w.float().cpu().numpy())
-        assert err <= TOL_GRAD, f"{name}: relative L2 {err} vs attn_bwd"
+    names = ("dq", "dk", "dv", "d_offset")
+    if _splits(shape):
+        for name, g, w in zip(names, got, want):
+            err = rel_l2(g.float().cpu().numpy(), w.float().cpu().numpy())
+            assert err <= TOL_GRAD, f"{name}: relative L2 {err} vs attn_bwd"
+    else:
+        for name, g, w in zip(names, got, want):
+            assert torch.equal(g, w), f"{name}: not bitwise equal to attn_bwd (deterministic)"
+    res = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    if d_off is not None:
+        res["d_offset"] = d_off
+    return x, {n: t.float().cpu().numpy() for n, t in res.items()}
 
 
-def test_no_alloc_backward_matches_workspace_backward_twice():
+def test_no_alloc_backward_three_calls_in_a_row():
     import scaled_dot_product_tmem_gb300 as sdpa
     lib = sdpa.library()
-    # first call: learnable sink, GQA, ragged length, window
-    _run_both(sdpa, lib, Shape(2, 300, 300, 8, 2, 128, 128), 201, sdpa.LEARNABLE, 100)
-    # second call right after, other shape: the array still holds the first call's data
-    _run_both(sdpa, lib, Shape(1, 200, 200, 4, 4, 64, 64), 202, sdpa.VANILLA, -1)
+    # first call: learnable sink, GQA (attn_bwd splits the group's heads), ragged, window
+    shape = Shape(2, 300, 300, 8, 2, 128, 128)
+    assert _splits(shape)
+    x, gpu = _run_both(sdpa, lib, shape, 201, sdpa.LEARNABLE, 100)
+    compare(gpu, oracle_run(x, causal=True, window=100, softmax_type=sdpa.LEARNABLE, scale=None), "noalloc vs oracle")
+    # second call right after, other shape (MHA: no split): bitwise equal to attn_bwd
+    shape = Shape(1, 200, 200, 4, 4, 64, 64)
+    assert not _splits(shape)
+    _run_both(sdpa, lib, shape, 202, sdpa.VANILLA, -1)
+    # third call: GQA with 512 kv CTAs (no split), off-by-one sink: bitwise equal to attn_bwd
+    shape = Shape(16, 512, 512, 16, 8, 64, 64)
+    assert not _splits(shape)
+    _run_both(sdpa, lib, shape, 203, sdpa.OFF_BY_ONE, -1)
 
 
 def test_no_alloc_rejects_problems_beyond_its_array():
