@@ -82,6 +82,86 @@ def compare(gpu, ref, what=""):
     return errs
 
 
+BF16_U = 2.0 ** -8  # unit roundoff of bf16 (8 significant bits)
+
+
+def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0):
+    """Tolerance for the learnable sink's d_offset, from the rounding the design imposes.
+
+    d_offset_h = -sum_{b,i} p_i D_i, with p_i = exp(o_h - LSE_i) and D_i = dO_i . O_i.
+    The terms have both signs, and the sum can be a small fraction of sum |p_i D_i|.
+    A fused backward has only the forward's stored bf16 output O^, so it forms
+    D^_i = dO_i . O^_i.  O^ carries two roundings to bf16 (unit roundoff u = 2^-8):
+    P is rounded before P.V, and O is rounded on output.  Each rounding moves its value
+    by at most u|value|; with the absolute error spread over +-half an ulp, its variance
+    is at most u^2 value^2 / 3.  Rounding errors of different elements are independent,
+    and dO is independent of them.  So, to first order,
+      Var(O^_id - O_id) <= u^2/3 (O_id^2 + sum_j P_ij^2 v_jd^2),
+      Var(D^_i - D_i)   = sum_d dO_id^2 Var(O^_id - O_id),
+      Var(d^_h - d_h)   = sum_{b,i} p_i^2 Var(D^_i - D_i).
+    The tolerance is `sigmas` standard deviations of that, plus three deterministic
+    terms, none of which comes from rounding O:
+      * r sum p |D^|, where r = e^e_LSE - 1 and e_LSE is the measured LSE error
+        (p^ is within r of p, relative);
+      * the fp32 dot of D^ over d_v terms: d_v 2^-24 sum_i p_i sum_d |dO_id O^_id|;
+      * the fp32 sum of n = B*S_q terms per head, one thread per 256th of them then
+        a 256-wide tree: (n/256 + 16) 2^-24 sum p |D^|.
+    sum_j P_ij^2 v_jd^2 comes from the oracle: its forward with every logit doubled
+    (scale, offset and bias times 2) on v^2 gives sum_j P'_ij v_jd^2, with
+    P'_ij = P_ij^2 e^{2 LSE_i - LSE'_i}.
+
+    `gpu` holds the kernel's stored O ("o") and LSE ("lse").  Returns
+      (exact d_offset, tolerance, the formula in fp64 on the stored O, kernel tolerance).
+    The kernel tolerance is the deterministic part alone.  The last two isolate the
+    kernel's own arithmetic from the rounding of O.
+    """
+    xd = {n: t.double().numpy() for n, t in x.items()}
+    sc = oracle.default_scale(xd["q"].shape[-1]) if scale is None else float(scale)
+    kw = dict(causal=causal, window=window, softmax_type=oracle.LEARNABLE, offset=xd["offset"], scale=sc)
+    kw2 = dict(kw, offset=2.0 * xd["offset"], scale=2.0 * sc)
+    if bias is not None:
+        kw["bias"] = bias
+        kw2["bias"] = 2.0 * bias
+    f = oracle.attention_fwd(xd["q"], xd["k"], xd["v"], **kw)
+    g = oracle.attention_bwd(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
+    f2 = oracle.attention_fwd(xd["q"], xd["k"], xd["v"] ** 2, **kw2)
+    with np.errstate(invalid="ignore"):
+        w = np.exp(f2["lse"] - 2.0 * f["lse"])                       # [B, H_q, S_q]
+    w = np.where(np.isfinite(w), w, 0.0)
+    p2v2 = f2["o"] * np.transpose(w, (0, 2, 1))[..., None]          # sum_j P_ij^2 v_jd^2
+    var_o = BF16_U ** 2 / 3.0 * (f["o"] ** 2 + p2v2)
+    dO = xd["dout"]
+    var_d = np.einsum("bshd,bshd->bhs", dO ** 2, var_o)
+    p = f["psink"]
+    sigma = np.sqrt(np.sum(p ** 2 * var_d, axis=(0, 2)))
+    o_gpu = np.asarray(gpu["o"], dtype=np.float64)
+    D_gpu = np.einsum("bshd,bshd->bhs", dO, o_gpu)
+    fin = np.isfinite(f["lse"])
+    e_lse = float(np.abs(np.asarray(gpu["lse"], np.float64)[fin] - f["lse"][fin]).max()) if fin.any() else 0.0
+    r = np.expm1(e_lse)
+    n = p.shape[0] * p.shape[2]
+    summation = (n / 256 + 16) * 2.0 ** -24 * np.sum(p * np.abs(D_gpu), axis=(0, 2))
+    dot = dO.shape[-1] * 2.0 ** -24 * np.einsum("bshd,bshd->bhs", np.abs(dO), np.abs(o_gpu))
+    kernel_tol = np.sum(p * (r * np.abs(D_gpu) + dot), axis=(0, 2)) + summation
+    on_gpu_o = -np.sum(p * D_gpu, axis=(0, 2))
+    return g["d_offset"], sigmas * sigma + kernel_tol, on_gpu_o, kernel_tol
+
+
+def check_d_offset_bound(x, gpu, what, **kw):
+    """Assert the derived per-head d_offset tolerance (d_offset_bound).  Also assert
+    that the kernel's reduction reproduces the fp64 formula on its own stored O within
+    the deterministic part.  Returns (relative L2 error vs exact, relative L2 error vs
+    the formula on the GPU's O)."""
+    exact, tol, on_gpu_o, kernel_tol = d_offset_bound(x, gpu, **kw)
+    got = np.asarray(gpu["d_offset"], dtype=np.float64)
+    err = np.abs(got - exact)
+    assert np.all(err <= tol), f"{what}: d_offset error {err} above the derived tolerance {tol}"
+    kern = np.abs(got - on_gpu_o)
+    assert np.all(kern <= kernel_tol), \
+        f"{what}: d_offset differs from the formula on its own O by {kern} (tolerance {kernel_tol})"
+    return float(rel_l2(got, exact)), float(rel_l2(got, on_gpu_o))
+
+
 def slice_group(x, b, g, G):
     """The inputs of one (batch b, kv head g) unit: query heads g*G..g*G+G-1 with kv head g."""
     out = {}
@@ -105,4 +185,5 @@ def gpu_slice(res, b, g, G):
     return out
 
 
-__all__ = ["Shape", "make_inputs", "gpu_run", "oracle_run", "compare", "slice_group", "gpu_slice", "rel_l2"]
+__all__ = ["Shape", "make_inputs", "gpu_run", "oracle_run", "compare", "slice_group", "gpu_slice", "rel_l2",
+           "d_offset_bound", "check_d_offset_bound"]

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
-from parity_util import TOL_GRAD, TOL_LSE, TOL_O, rel_l2
+from parity_util import TOL_GRAD, TOL_LSE, TOL_O, check_d_offset_bound, rel_l2
 from scaled_dot_product_tmem_gb300.inputs import Shape, make_bias, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -49,7 +49,9 @@ def _ref(x, bias, *, causal, window, st, scale):
     return out
 
 
-def _compare(gpu, ref, what):
+def _compare(gpu, ref, what, d_offset_stated=True):
+    """Every output within the stated tolerances; d_offset_stated=False leaves d_offset
+    to the derived bound (parity_util.d_offset_bound), for cases where its terms cancel."""
     e = float(np.abs(gpu["o"] - ref["o"]).max())
     assert e <= TOL_O, f"{what}: O max-abs {e}"
     fin = np.isfinite(ref["lse"])
@@ -58,32 +60,40 @@ def _compare(gpu, ref, what):
         e = float(np.abs(gpu["lse"][fin] - ref["lse"][fin]).max())
         assert e <= TOL_LSE, f"{what}: LSE max-abs {e}"
     for n in ("dq", "dk", "dv", "d_offset", "dbias"):
+        if n == "d_offset" and not d_offset_stated:
+            continue
         if n in ref:
             e = rel_l2(gpu[n], ref[n])
             assert e <= TOL_GRAD, f"{what}: {n} relative L2 {e}"
 
 
 CASES = [
-    # name, shape, causal, window, softmax type, scale, bias (Bb, Hb), deterministic
-    ("gqa_batch_broadcast", Shape(2, 300, 300, 4, 2, 128, 128), True, -1, VANILLA, None, (1, 4), False),
-    ("d64_window_obo", Shape(1, 256, 256, 4, 1, 64, 64), True, 100, OFF_BY_ONE, None, (1, 4), False),
-    # (learnable here makes d_offset ~1 % of sum |p_sink D|: a cancellation that bf16 O alone
-    # moves by 0.4 %; the learnable sink is covered by the causal ragged case below)
-    ("noncausal_rect_head_broadcast", Shape(2, 200, 333, 2, 2, 64, 64), False, -1, OFF_BY_ONE, 0.2, (2, 1), False),
-    ("per_bh_deterministic", Shape(2, 256, 256, 4, 2, 128, 128), True, -1, VANILLA, None, (2, 4), True),
-    ("mqa_head_splits_full_broadcast", Shape(1, 300, 300, 8, 1, 128, 128), True, -1, VANILLA, None, (1, 1), False),
-    ("ragged_det_d64", Shape(1, 77, 77, 2, 2, 64, 64), True, 10, LEARNABLE, None, (1, 2), True),
+    # name, shape, causal, window, softmax type, scale, bias (Bb, Hb), deterministic, d_offset check
+    ("gqa_batch_broadcast", Shape(2, 300, 300, 4, 2, 128, 128), True, -1, VANILLA, None, (1, 4), False, "stated"),
+    ("d64_window_obo", Shape(1, 256, 256, 4, 1, 64, 64), True, 100, OFF_BY_ONE, None, (1, 4), False, "stated"),
+    # non-causal with an N(0,1) bias: d_offset is about 1 % of sum |p_sink D|, so the
+    # bf16 rounding of the stored O (which D must be formed from) moves it by more than
+    # 1e-2 relative; it is held to the bound derived from that rounding instead
+    ("noncausal_rect_head_broadcast", Shape(2, 200, 333, 2, 2, 64, 64), False, -1, LEARNABLE, 0.2, (2, 1), False,
+     "bound"),
+    ("per_bh_deterministic", Shape(2, 256, 256, 4, 2, 128, 128), True, -1, VANILLA, None, (2, 4), True, "stated"),
+    ("mqa_head_splits_full_broadcast", Shape(1, 300, 300, 8, 1, 128, 128), True, -1, VANILLA, None, (1, 1), False,
+     "stated"),
+    ("ragged_det_d64", Shape(1, 77, 77, 2, 2, 64, 64), True, 10, LEARNABLE, None, (1, 2), True, "stated"),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_bias_parity(case):
-    name, shape, causal, window, st, scale, (Bb, Hb), det = case
+    name, shape, causal, window, st, scale, (Bb, Hb), det, doff = case
     x = make_inputs(shape, 500 + len(name), learnable_offset=(st == LEARNABLE))
     bias = make_bias((Bb, Hb, shape.S_q, shape.S_kv), 600 + len(name))
     kw = dict(causal=causal, window=window, st=st, scale=scale)
     gpu = _run(x, bias, deterministic=det, **kw)
-    _compare(gpu, _ref(x, bias, **kw), name)
+    _compare(gpu, _ref(x, bias, **kw), name, d_offset_stated=(doff == "stated"))
+    if st == LEARNABLE:  # the derived bound holds in every learnable case
+        check_d_offset_bound(x, gpu, name, causal=causal, window=window, scale=scale,
+                             bias=bias.double().numpy())
     if det:  # one contributor per dbias entry: bitwise reproducible
         again = _run(x, bias, deterministic=det, **kw)
         for n in gpu:

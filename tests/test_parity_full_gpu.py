@@ -28,6 +28,8 @@ FULL = [
     ("sweep_s2048_gqa", Shape(16, 2048, 2048, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 2048 + 8,
      [(15, 2)]),
     ("sweep_s8192_gqa", Shape(4, 8192, 8192, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 8192 + 8, [(1, 5)]),
+    ("sweep_s16384_gqa", Shape(2, 16384, 16384, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 16384 + 8,
+     [(1, 6)]),
 ]
 
 
@@ -44,13 +46,15 @@ def test_full_size_sampled_units(case, deterministic):
         compare(gpu_slice(gpu, b, g, G), ref, f"{name} unit (b={b}, g={g})")
 
 
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused_dq", "det"])
 @pytest.mark.parametrize("st", [OFF_BY_ONE, LEARNABLE], ids=["off_by_one", "learnable"])
-def test_sink_config_full_size(st):
-    """B=2, S=4096, H_q=32, H_kv=8, d=64, causal; learnable offset [32] N(0,1) with gradient."""
+def test_sink_config_full_size(st, deterministic):
+    """B=2, S=4096, H_q=32, H_kv=8, d=64, causal; learnable offset [32] N(0,1) with gradient.
+    deterministic=False is the path bench.py times: the kv kernel with the fused dQ."""
     shape = Shape(2, 4096, 4096, 32, 8, 64, 64)
     x = make_inputs(shape, 3, learnable_offset=True)
     kw = dict(causal=True, window=-1, softmax_type=st, scale=None)
-    gpu = gpu_run(x, **kw)
+    gpu = gpu_run(x, deterministic=deterministic, **kw)
     G, g = 4, 6
     d_off = np.zeros(G)
     for b in range(2):

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
-from parity_util import Shape, compare, gpu_run, make_inputs, oracle_run
+from parity_util import Shape, check_d_offset_bound, compare, gpu_run, make_inputs, oracle_run
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,34 @@ def test_fwd_bwd_matches_oracle(case, deterministic):
     ref = oracle_run(x, **kw)
     gpu = gpu_run(x, deterministic=deterministic, **kw)
     compare(gpu, ref, name)
+    if st == LEARNABLE:  # the derived d_offset bound holds wherever the stated tolerance does
+        check_d_offset_bound(x, gpu, name, causal=causal, window=window, scale=scale)
+
+
+# Non-causal learnable sink with mixed-sign D, no bias: every output but d_offset at the
+# stated tolerances; d_offset (whose terms cancel) at the bound derived from the bf16
+# rounding of the stored O that D is formed from (parity_util.d_offset_bound).
+NONCAUSAL_LEARNABLE = [
+    ("noncausal_square", Shape(2, 256, 256, 4, 2, 128, 128), 0.08),
+    ("noncausal_rect_d64", Shape(2, 200, 333, 2, 2, 64, 64), 0.2),
+    ("noncausal_mqa_ragged", Shape(1, 301, 129, 8, 1, 128, 128), None),
+]
+
+
+@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("case", NONCAUSAL_LEARNABLE, ids=[c[0] for c in NONCAUSAL_LEARNABLE])
+def test_noncausal_learnable_d_offset(case, deterministic):
+    name, shape, scale = case
+    x = make_inputs(shape, 300 + NONCAUSAL_LEARNABLE.index(case), learnable_offset=True)
+    kw = dict(causal=False, window=-1, softmax_type=LEARNABLE, scale=scale)
+    ref = oracle_run(x, **kw)
+    gpu = gpu_run(x, deterministic=deterministic, **kw)
+    D = oracle.attention_bwd(*(x[n].double().numpy() for n in ("q", "k", "v", "dout")), causal=False,
+                             softmax_type=LEARNABLE, offset=x["offset"].double().numpy(), scale=scale)["D"]
+    assert (D > 0).any() and (D < 0).any(), "the case should have D of both signs"
+    ref.pop("d_offset")
+    compare(gpu, ref, name)
+    check_d_offset_bound(x, gpu, name, causal=False, window=-1, scale=scale)
 
 
 def test_tiny_config_exact_recipe():
