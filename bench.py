@@ -7,10 +7,15 @@ One step = attn_fwd + attn_bwd (every step of the hot path) over one batch of
 synthetic BSHD bf16 inputs already resident in HBM.  The ``fp8_fwd_*`` workloads
 time the E4M3 forward instead: one step = the per-tensor E4M3 casts of Q, K and V
 (delayed scaling: the scale from the previous step's amax, this step's amax
-recorded during the cast) + attn_fwd_fp8, counted in forward FLOPs.  The default workload is the
-GQA + sliding-window training shape (B=4, S=2048, H_q=32, H_kv=8, d=128, causal,
-left window 1024, vanilla softmax).  FLOPs count only unmasked (query, key)
-pairs: forward 2(d_qk + d_v) per pair, backward 2(3 d_qk + 2 d_v) per pair.
+recorded during the cast) + attn_fwd_fp8, counted in forward FLOPs.  The default
+workload is causal GQA at S=8192 (B=4, H_q=32, H_kv=8, d=128, vanilla softmax),
+the point at which the method's target is stated.  FLOPs count only unmasked
+(query, key) pairs: forward 2(d_qk + d_v) per pair, backward 2(3 d_qk + 2 d_v) per
+pair.
+
+The headline value comes from a pass with no per-kernel instrumentation; the
+per-kernel split and the roofline come from a second pass of the same steps with
+CUDA events around every launch.
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own copy of the
 workload (independent problems, no collective on the data path: weak scaling).
@@ -85,8 +90,7 @@ WORKLOADS["bias_gqa_b2_s4096"] = _w(
     "bias_gqa_b2_s4096", 2, 4096, 32, 8, 128, 128, True, -1, 0, None, 8,
     "additive bias [1, 32, S, S] (bf16, N(0,1)) with dbias: B=2, S=4096, H_q=32, H_kv=8, d=128, causal",
     bias=(1, 32))
-DEFAULT = "gqa_swa_b4_s2048"
-HEADLINE = "sweep_s8192_hkv8"
+DEFAULT = "sweep_s8192_hkv8"
 
 
 def n_pairs(S, causal, window):
@@ -306,6 +310,25 @@ def dist_setup():
     return world, rank, local
 
 
+def bench_config(wl, world, det):
+    """The `config` object of the JSON line, the same for both arms."""
+    fp8 = bool(wl.get("fp8"))
+    return {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
+            "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
+            **({"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + attn_fwd_fp8"}
+               if fp8 else {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
+            "l2": "flushed between timed steps (258 MB write outside the timed span)",
+            **({"seq_lens": wl["lens"]} if wl.get("lens") else {}),
+            **({"bias": f"bf16 {list(wl['bias']) + [wl['S'], wl['S']]}, dbias fp32"} if wl.get("bias") else {})}
+
+
+def uses_deterministic(wl, args):
+    """The backward path bench.py runs: deterministic when asked for, or when the head
+    dims have no fused dQ in the library (d_qk = 192)."""
+    fused_ok = wl["dqk"] in (64, 128) and wl["dv"] in (64, 128)
+    return bool(args.deterministic) or not fused_ok
+
+
 def reference_arm(args, wl, world, rank):
     if rank != 0:
         return 0
@@ -327,7 +350,7 @@ def reference_arm(args, wl, world, rank):
     line = {"metric": METRIC_FP8 if wl.get("fp8") else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl["desc"], "seq_len": wl["S"], "global_batch": wl["B"]},
+            "config": bench_config(wl, 1, uses_deterministic(wl, args)),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
@@ -398,8 +421,10 @@ def _step_fns(sdpa, wl, dev, det, x):
     return step, t, outs
 
 
-def measure(sdpa, wl, dev, det, x, steps, warmup, sampler=None):
-    """Device time of `steps` fwd+bwd steps on resident inputs (L2 flushed between steps)."""
+def measure(sdpa, wl, dev, det, x, steps, warmup, sampler=None, split_steps=10):
+    """Device time of `steps` fwd+bwd steps on resident inputs (L2 flushed between
+    steps), taken with per-kernel timing off; then `split_steps` more steps with CUDA
+    events around every launch for the per-kernel split."""
     import torch
     step, t, outs = _step_fns(sdpa, wl, dev, det, x)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -409,26 +434,31 @@ def measure(sdpa, wl, dev, det, x, steps, warmup, sampler=None):
     st, site = sdpa.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st} site {site:#x} during warm-up")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    sdpa.attn_timing_read()
-    sdpa.attn_timing_enable(True)
+
+    def timed_steps(n, per_kernel):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        sdpa.attn_timing_read()
+        sdpa.attn_timing_enable(per_kernel)
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.fill_(float(i))  # evict the previous step's data from L2 (outside the timed span)
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+        sdpa.attn_timing_enable(False)
+        kt = sdpa.attn_timing_read()
+        return sum(a.elapsed_time(b) for a, b in zip(starts, ends)), kt
+
     if sampler:
         sampler.start()
-    torch.cuda.synchronize()
-    for i in range(steps):
-        flush.fill_(float(i))  # evict the previous step's data from L2 (outside the timed span)
-        starts[i].record()
-        step()
-        ends[i].record()
-    torch.cuda.synchronize()
+    ms, _ = timed_steps(steps, False)
     clocks = sampler.stop() if sampler else None
-    sdpa.attn_timing_enable(False)
-    kt = sdpa.attn_timing_read()
+    _, kt = timed_steps(split_steps, True)
     st, site = sdpa.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st} site {site:#x}")
-    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
     return ms, kt, clocks
 
 
@@ -503,18 +533,23 @@ def ours_arm(args, wl, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sdpa.library()
-    fused_ok = wl["dqk"] in (64, 128) and wl["dv"] in (64, 128)  # the library's fused-dQ head dims
-    det = bool(args.deterministic) or not fused_ok
+    det = uses_deterministic(wl, args)
     fp8 = bool(wl.get("fp8"))
     x = make_cpu_inputs(wl, rank)
-    ms, kt, clocks = measure(sdpa, wl, dev, det, x, args.steps, args.warmup, ClockSampler(local))
+    ms, kt, clocks = measure(sdpa, wl, dev, det, x, args.steps, args.warmup, ClockSampler(local),
+                             split_steps=min(args.steps, 10))
     total_flops = flops(wl)
     ms_max = _max_over_ranks(ms, world, dev)
     value = world * total_flops * args.steps / (ms_max / 1e3) / 1e12
-    e2e_steps = max(3, min(args.steps, 20))
-    e2e_ms, h2d, d2h = measure_e2e(sdpa, wl, dev, det, x, e2e_steps, 2)
-    e2e_ms = _max_over_ranks(e2e_ms, world, dev)
-    e2e_value = world * total_flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        e2e_ms, h2d, d2h = measure_e2e(sdpa, wl, dev, det, x, e2e_steps, 2)
+        e2e_ms = _max_over_ranks(e2e_ms, world, dev)
+        e2e = {"value": world * total_flops * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "copies": "pinned host buffers; two device buffer sets, uploads and downloads on their own "
+                         "streams overlapping the neighbouring steps' kernels"}
     peaks, peak_src = load_peaks()
     dom = max(kt, key=lambda k: kt[k][0])
     dms, dn = kt[dom]
@@ -538,15 +573,7 @@ def ours_arm(args, wl, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
-            "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
-                       "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
-                       **({"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + "
-                                   "attn_fwd_fp8"} if fp8 else
-                          {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
-                       "l2": "flushed between timed steps (258 MB write outside the timed span)",
-                       **({"seq_lens": wl["lens"]} if wl.get("lens") else {}),
-                       **({"bias": f"bf16 {list(wl['bias']) + [wl['S'], wl['S']]}, dbias fp32"}
-                          if wl.get("bias") else {})},
+            "config": bench_config(wl, world, det),
             "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             **({"pct_of_nominal_fp8_peak": 100.0 * value / world / (FP8_PER_BF16 * NOMINAL_BF16_TFLOPS)}
                if fp8 else {}),
@@ -555,21 +582,10 @@ def ours_arm(args, wl, world, rank, local):
                          "frac": achieved / peak, "peak_source": peak_desc,
                          "traffic": recorded_traffic(wl, dom), "traffic_unit": "bytes per launch (ncu DRAM read+write)"},
             "kernels": kernels,
+            "kernel_split": f"a second pass of {min(args.steps, 10)} steps with CUDA events around every launch",
             "gpu_launches": launches,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "copies": "pinned host buffers; two device buffer sets, uploads and downloads on their own "
-                              "streams overlapping the neighbouring steps' kernels"},
+            **({"e2e": e2e} if e2e else {}),
             "clocks": clocks}
-    if args.headline and wl["name"] != HEADLINE and world == 1:
-        hw = WORKLOADS[HEADLINE]
-        hx = make_cpu_inputs(hw)
-        hsteps = min(args.steps, 10)
-        hms, hkt, _ = measure(sdpa, hw, dev, False, hx, hsteps, 3)
-        hv = flops(hw) * hsteps / (hms / 1e3) / 1e12
-        line["headline_causal_gqa_s8192"] = {
-            "workload": hw["desc"], "value": hv, "unit": "TFLOP/s",
-            "pct_of_nominal_bf16_peak": 100 * hv / NOMINAL_BF16_TFLOPS, "frac_of_measured_peak": hv / peak,
-            "kernels": {k: v[0] / v[1] for k, v in hkt.items() if v[1]}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, x)
     if rank == 0:
@@ -585,8 +601,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--deterministic", action="store_true", help="deterministic backward (recompute dQ)")
-    ap.add_argument("--headline", action="store_true", help="also time the causal GQA S=8192 sweep point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (keeps the device footprint to one step's buffers, for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
