@@ -56,12 +56,17 @@ def _load():
         lib = ctypes.CDLL(build())
         dp = ctypes.POINTER(ctypes.c_double)
         i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i,
+        u64 = ctypes.c_uint64
+        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64,
                                    dp, dp, dp, dp]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i,
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64,
                                    dp, dp, dp, dp, dp, dp]
         lib.oracle_bwd.restype = ctypes.c_int
+        lib.oracle_philox4x64_10.argtypes = [ctypes.POINTER(u64), ctypes.POINTER(u64), ctypes.POINTER(u64)]
+        lib.oracle_philox4x64_10.restype = None
+        lib.oracle_dropout_keep.argtypes = [i, i, i, i, i, u64, u64, ctypes.POINTER(ctypes.c_ubyte)]
+        lib.oracle_dropout_keep.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -87,6 +92,45 @@ def default_scale(d_qk: int) -> float:
     return 1.0 / np.sqrt(d_qk)
 
 
+def dropout_threshold(p: float) -> int:
+    """The drop threshold t of probability p: pairs whose 16-bit uniform is below t are
+    dropped, so p is realised as t / 65536 (t = floor(p * 65536 + 1/2))."""
+    p = float(p)
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    t = int(np.floor(p * 65536.0 + 0.5))
+    if t > 65535:
+        raise ValueError("dropout probability rounds to 1")
+    return t
+
+
+def philox4x64_10(counter, key):
+    """Philox4x64-10 of one 4 x 64-bit counter under a 2 x 64-bit key (four uint64 words)."""
+    c = (ctypes.c_uint64 * 4)(*[int(x) & (2 ** 64 - 1) for x in counter])
+    k = (ctypes.c_uint64 * 2)(*[int(x) & (2 ** 64 - 1) for x in key])
+    out = (ctypes.c_uint64 * 4)()
+    _load().oracle_philox4x64_10(c, k, out)
+    return np.array(list(out), dtype=np.uint64)
+
+
+def dropout_keep(b, h, Sq, Skv, p, rng_state):
+    """Keep decisions [Sq, Skv] (bool) of batch b, query head h for drop probability p
+    and rng_state = (seed, offset)."""
+    keep = np.zeros((Sq, Skv), dtype=np.uint8)
+    rc = _load().oracle_dropout_keep(int(b), int(h), int(Sq), int(Skv), dropout_threshold(p),
+                                     int(rng_state[0]), int(rng_state[1]),
+                                     keep.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)))
+    if rc != 0:
+        raise ValueError("oracle_dropout_keep rejected its arguments")
+    return keep.astype(bool)
+
+
+def _drop_args(dropout_p, rng_state):
+    t = dropout_threshold(dropout_p)
+    seed, off = (0, 0) if rng_state is None else (int(rng_state[0]), int(rng_state[1]))
+    return t, seed, off
+
+
 def _bias_args(bias, B, Hq, Sq, Skv):
     if bias is None:
         return None, 1, 1
@@ -97,10 +141,12 @@ def _bias_args(bias, B, Hq, Sq, Skv):
 
 
 def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None, bias=None):
+                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None):
     """O, LSE, p_sink, rowsum for BSHD q [B,Sq,Hq,dqk], k [B,Skv,Hkv,dqk], v [B,Skv,Hkv,dv].
 
     bias: optional [Bb,Hb,Sq,Skv] (Bb in {1,B}, Hb in {1,Hq}) added to the scaled scores.
+    dropout_p, rng_state = (seed, offset): attention dropout (see oracle.c); rowsum,
+    LSE and p_sink are those of the undropped probabilities.
     Returns a dict of float64 arrays: o [B,Sq,Hq,dv]; lse, psink, rowsum [B,Hq,Sq].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -114,16 +160,18 @@ def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
     lse = np.zeros((B, Hq, Sq))
     psink = np.zeros((B, Hq, Sq))
     rowsum = np.zeros((B, Hq, Sq))
+    t, seed, roff = _drop_args(dropout_p, rng_state)
     rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, dqk, dv,
                             scale, int(bool(causal)), int(window), int(softmax_type),
-                            _ptr(off), _ptr(bias), Bb, Hb, _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
+                            _ptr(off), _ptr(bias), Bb, Hb, t, seed, roff,
+                            _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
     return {"o": o, "lse": lse, "psink": psink, "rowsum": rowsum}
 
 
 def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None, bias=None):
+                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None):
     """dq, dk, dv, d_offset [Hq], D [B,Hq,Sq] (= dO.O) and, with a bias, dbias (its
     shape) for the same arguments as fwd."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -139,10 +187,11 @@ def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA
     doff = np.zeros(Hq)
     D = np.zeros((B, Hq, Sq))
     dbias = np.zeros_like(bias) if bias is not None else None
+    t, seed, roff = _drop_args(dropout_p, rng_state)
     rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Sq, Skv, Hq, Hkv,
                             dqk, dv, scale, int(bool(causal)), int(window),
-                            int(softmax_type), _ptr(off), _ptr(bias), Bb, Hb, _ptr(dq), _ptr(dk),
-                            _ptr(dvv), _ptr(doff), _ptr(D), _ptr(dbias))
+                            int(softmax_type), _ptr(off), _ptr(bias), Bb, Hb, t, seed, roff,
+                            _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(doff), _ptr(D), _ptr(dbias))
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     out = {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}

@@ -51,10 +51,32 @@
  *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_{h in group} sum_i dS_ij q_i,
  *   dV_j = sum_{h in group} sum_i P_ij dO_i,  d offset_h = -sum_{b,i} p_sink_i D_i.
  *
+ * Attention dropout ("JAX: Single-GPU Attention with TransformerEngine", section
+ * "Other attention knobs": `attention_dropout`; the sequence diagrams of PR 2225: the
+ * fused forward returns an rng_state that the fused backward takes).  Reading: each
+ * probability P_ij (after the softmax, sink included in the normaliser) is kept with
+ * probability 1 - p and scaled by 1/(1 - p), or dropped to 0; the normaliser, LSE and
+ * p_sink are those of the undropped softmax.  The keep decisions come from a
+ * counter-based generator, so the backward regenerates them from the same state:
+ *   - Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ *     as 1, 2, 3", SC'11): ten rounds on a 4 x 64-bit counter with a 2 x 64-bit key;
+ *   - key = (seed, offset) = the rng_state; counter of pair (b, h, i, j) =
+ *     (j / 4, i / 4, h, b);
+ *   - the call yields four 64-bit words; pair (i, j) takes word i % 4 and, within it,
+ *     the 16-bit field j % 4 (bits 16 (j % 4) .. 16 (j % 4) + 15), a uniform u in
+ *     [0, 65536);
+ *   - the drop probability is realised as t / 65536 with t = floor(p * 65536 + 1/2);
+ *     the pair is kept iff u >= t, and a kept P is multiplied by 65536 / (65536 - t).
+ * With M_ij = keep_ij * 65536 / (65536 - t) the forward is O_i = sum_j P_ij M_ij v_j
+ * and the backward is (dP~_ij = dO_i . v_j):
+ *   D_i = dO_i . O_i = sum_j P_ij M_ij dP~_ij,   dS_ij = P_ij (M_ij dP~_ij - D_i),
+ *   dV_j = sum_{h in group} sum_i P_ij M_ij dO_i,   dQ, dK, d offset as above.
+ *
  * All tensors are contiguous BSHD (batch, sequence, head, head-dim) in double,
  * except lse / psink / rowsum / D which are [B, H_q, S_q] and offset [H_q].
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -78,6 +100,56 @@ static int visible(int i, int j, int causal, int window) {
 static const double* bias_plane(const double* bias, int Bb, int Hb, int b, int h, int Sq, int Skv) {
     if (!bias) return NULL;
     return bias + ((size_t)(Bb == 1 ? 0 : b) * Hb + (Hb == 1 ? 0 : h)) * Sq * Skv;
+}
+
+/*
+ * Philox4x64-10 (SC'11 paper cited above).  One round maps the counter
+ * (c0, c1, c2, c3) with key (k0, k1) to
+ *   (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)),
+ * hi/lo the upper/lower 64 bits of the 128-bit product; between rounds the key is
+ * bumped by the Weyl constants (W0, W1).  Ten rounds, the first with the key itself.
+ */
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; r++) {
+        if (r > 0) { k0 += W0; k1 += W1; }
+        unsigned __int128 p0 = (unsigned __int128)M0 * c0, p1 = (unsigned __int128)M1 * c2;
+        uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k0, n1 = (uint64_t)p1;
+        uint64_t n2 = (uint64_t)(p0 >> 64) ^ c3 ^ k1, n3 = (uint64_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Dropout state: drop threshold t (0: no dropout) and the Philox key (seed, offset). */
+typedef struct { int t; uint64_t seed, offset; } dropout_t;
+
+/* The 16-bit uniform of pair (b, h, i, j) (see the header). */
+static unsigned dropout_u16(const dropout_t* d, int b, int h, int i, int j) {
+    uint64_t ctr[4] = {(uint64_t)(j / 4), (uint64_t)(i / 4), (uint64_t)h, (uint64_t)b};
+    uint64_t key[2] = {d->seed, d->offset}, w[4];
+    oracle_philox4x64_10(ctr, key, w);
+    return (unsigned)((w[i % 4] >> (16 * (j % 4))) & 0xFFFFu);
+}
+
+/* M_ij: 65536 / (65536 - t) if the pair is kept, 0 if dropped; 1 without dropout. */
+static double dropout_mult(const dropout_t* d, int b, int h, int i, int j) {
+    if (!d || d->t == 0) return 1.0;
+    return dropout_u16(d, b, h, i, j) >= (unsigned)d->t ? 65536.0 / (65536.0 - d->t) : 0.0;
+}
+
+/* The keep decisions of one (b, h) as bytes [Sq * Skv] (1 kept, 0 dropped), for tests. */
+int oracle_dropout_keep(int b, int h, int Sq, int Skv, int t, uint64_t seed, uint64_t offset,
+                        unsigned char* keep) {
+    if (t < 0 || t > 65535) return -1;
+    dropout_t d = {t, seed, offset};
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Sq; i++)
+        for (int j = 0; j < Skv; j++)
+            keep[(size_t)i * Skv + j] = dropout_u16(&d, b, h, i, j) >= (unsigned)t;
+    return 0;
 }
 
 /* The sink logit c of query head h (see the readings above). */
@@ -136,9 +208,11 @@ static void probs_one_head(const double* q, const double* k, int b, int h, int g
 int oracle_fwd(const double* q, const double* k, const double* v,
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
-               const double* bias, int Bb, int Hb,
+               const double* bias, int Bb, int Hb, int drop_t, uint64_t seed, uint64_t offset_rng,
                double* o, double* lse, double* psink, double* rowsum) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (drop_t < 0 || drop_t > 65535) return -1;
+    dropout_t drop = {drop_t, seed, offset_rng};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
@@ -153,7 +227,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
             double* lrow = lse + ((size_t)b * Hq + h) * Sq;
             probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
                            bias_plane(bias, Bb, Hb, b, h, Sq, Skv), P, lrow, ps);
-            /* attend: O_i = sum_j P_ij v_j */
+            /* attend: O_i = sum_j P_ij M_ij v_j  (M = 1 without dropout) */
 #pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
                 double acc[ORACLE_MAX_D];
@@ -161,6 +235,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                 for (int j = 0; j < Skv; j++) {
                     double pij = P[(size_t)i * Skv + j];
                     if (pij == 0.0) continue;
+                    pij *= dropout_mult(&drop, b, h, i, j);
                     for (int t = 0; t < dv; t++) acc[t] += pij * v[bshd(b, j, g, t, Skv, Hkv, dv)];
                 }
                 for (int t = 0; t < dv; t++) o[bshd(b, i, h, t, Sq, Hq, dv)] = acc[t];
@@ -187,9 +262,11 @@ int oracle_fwd(const double* q, const double* k, const double* v,
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
-               const double* bias, int Bb, int Hb,
+               const double* bias, int Bb, int Hb, int drop_t, uint64_t seed, uint64_t offset_rng,
                double* dq, double* dk, double* dvout, double* d_offset, double* Dout, double* dbias) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
+    if (drop_t < 0 || drop_t > 65535) return -1;
+    dropout_t drop = {drop_t, seed, offset_rng};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
@@ -197,12 +274,13 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
     size_t nP = (size_t)Sq * Skv + 1;
     double* P = (double*)malloc(sizeof(double) * nP);
     double* dS = (double*)malloc(sizeof(double) * nP);
+    double* Mk = (double*)malloc(sizeof(double) * nP); /* M_ij of the current (b, h) */
     double* O = (double*)malloc(sizeof(double) * ((size_t)Sq * dv + 1));
     double* D = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
     double* lse = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
     double* ps = (double*)malloc(sizeof(double) * ((size_t)Sq + 1));
-    if (!P || !dS || !O || !D || !lse || !ps) {
-        free(P); free(dS); free(O); free(D); free(lse); free(ps);
+    if (!P || !dS || !Mk || !O || !D || !lse || !ps) {
+        free(P); free(dS); free(Mk); free(O); free(D); free(lse); free(ps);
         return -1;
     }
     memset(dk, 0, sizeof(double) * (size_t)B * Skv * Hkv * dqk);
@@ -217,12 +295,15 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
             probs_one_head(q, k, b, h, g, Sq, Skv, Hq, Hkv, dqk, scale, causal, window, c,
                            bias_plane(bias, Bb, Hb, b, h, Sq, Skv), P, lse, ps);
 #pragma omp parallel for schedule(static)
+            for (int i = 0; i < Sq; i++)
+                for (int j = 0; j < Skv; j++) Mk[(size_t)i * Skv + j] = dropout_mult(&drop, b, h, i, j);
+#pragma omp parallel for schedule(static)
             for (int i = 0; i < Sq; i++) {
-                /* O_i = sum_j P_ij v_j, then D_i = dO_i . O_i */
+                /* O_i = sum_j P_ij M_ij v_j, then D_i = dO_i . O_i */
                 double acc[ORACLE_MAX_D];
                 for (int t = 0; t < dv; t++) acc[t] = 0.0;
                 for (int j = 0; j < Skv; j++) {
-                    double pij = P[(size_t)i * Skv + j];
+                    double pij = P[(size_t)i * Skv + j] * Mk[(size_t)i * Skv + j];
                     if (pij == 0.0) continue;
                     for (int t = 0; t < dv; t++) acc[t] += pij * v[bshd(b, j, g, t, Skv, Hkv, dv)];
                 }
@@ -232,14 +313,14 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                     Di += dout[bshd(b, i, h, t, Sq, Hq, dv)] * acc[t];
                 }
                 D[i] = Di;
-                /* dP_ij = dO_i . v_j ; dS_ij = P_ij (dP_ij - D_i) */
+                /* dP~_ij = dO_i . v_j ; dS_ij = P_ij (M_ij dP~_ij - D_i) */
                 for (int j = 0; j < Skv; j++) {
                     double pij = P[(size_t)i * Skv + j];
                     if (pij == 0.0) { dS[(size_t)i * Skv + j] = 0.0; continue; }
                     double dp = 0.0;
                     for (int t = 0; t < dv; t++)
                         dp += dout[bshd(b, i, h, t, Sq, Hq, dv)] * v[bshd(b, j, g, t, Skv, Hkv, dv)];
-                    dS[(size_t)i * Skv + j] = pij * (dp - Di);
+                    dS[(size_t)i * Skv + j] = pij * (Mk[(size_t)i * Skv + j] * dp - Di);
                 }
                 /* dQ_i = scale sum_j dS_ij k_j */
                 for (int t = 0; t < dqk; t++) acc[t] = 0.0;
@@ -250,7 +331,7 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                 }
                 for (int t = 0; t < dqk; t++) dq[bshd(b, i, h, t, Sq, Hq, dqk)] = scale * acc[t];
             }
-            /* dK_j += scale sum_i dS_ij q_i ; dV_j += sum_i P_ij dO_i  (sum over the group) */
+            /* dK_j += scale sum_i dS_ij q_i ; dV_j += sum_i P_ij M_ij dO_i  (sum over the group) */
 #pragma omp parallel for schedule(static)
             for (int j = 0; j < Skv; j++) {
                 double ak[ORACLE_MAX_D], av[ORACLE_MAX_D];
@@ -259,8 +340,9 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                 for (int i = 0; i < Sq; i++) {
                     double dsij = dS[(size_t)i * Skv + j], pij = P[(size_t)i * Skv + j];
                     if (pij == 0.0) continue;
+                    double pm = pij * Mk[(size_t)i * Skv + j];
                     for (int t = 0; t < dqk; t++) ak[t] += dsij * q[bshd(b, i, h, t, Sq, Hq, dqk)];
-                    for (int t = 0; t < dv; t++) av[t] += pij * dout[bshd(b, i, h, t, Sq, Hq, dv)];
+                    for (int t = 0; t < dv; t++) av[t] += pm * dout[bshd(b, i, h, t, Sq, Hq, dv)];
                 }
                 for (int t = 0; t < dqk; t++) dk[bshd(b, j, g, t, Skv, Hkv, dqk)] += scale * ak[t];
                 for (int t = 0; t < dv; t++) dvout[bshd(b, j, g, t, Skv, Hkv, dv)] += av[t];
@@ -282,7 +364,7 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                 for (int i = 0; i < Sq; i++) Dout[((size_t)b * Hq + h) * Sq + i] = D[i];
         }
     }
-    free(P); free(dS); free(O); free(D); free(lse); free(ps);
+    free(P); free(dS); free(Mk); free(O); free(D); free(lse); free(ps);
     return 0;
 }
 
