@@ -46,13 +46,18 @@ NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False, bias=None):
+def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False, bias=None,
+       dropout=0.0):
     """A workload; `lens` (one length per batch entry, same for queries and keys) makes
     it a padded batch run through the varlen entry points; `fp8` makes it the E4M3
     forward; `bias` = (Bb, Hb) adds a bf16 [Bb, Hb, S, S] bias (attn_fwd_bias /
-    attn_bwd_bias, with dbias)."""
+    attn_bwd_bias, with dbias); `dropout` = p runs attn_fwd_dropout / attn_bwd_dropout
+    with the rng state DROPOUT_RNG."""
     return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
-                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8, bias=bias)
+                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8, bias=bias, dropout=dropout)
+
+
+DROPOUT_RNG = (0x5EED_2024_0001, 0)  # (seed, offset) of the dropout workloads
 
 
 WORKLOADS = {
@@ -90,6 +95,14 @@ WORKLOADS["bias_gqa_b2_s4096"] = _w(
     "bias_gqa_b2_s4096", 2, 4096, 32, 8, 128, 128, True, -1, 0, None, 8,
     "additive bias [1, 32, S, S] (bf16, N(0,1)) with dbias: B=2, S=4096, H_q=32, H_kv=8, d=128, causal",
     bias=(1, 32))
+# Attention dropout p = 0.1 on the target point and on the GQA + SWA training shape.
+WORKLOADS["dropout_gqa_b4_s8192"] = _w(
+    "dropout_gqa_b4_s8192", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 1000 + 8192 + 8,
+    "attention dropout p=0.1 (Philox4x64-10 decisions): B=4, S=8192, H_q=32, H_kv=8, d=128, causal", dropout=0.1)
+WORKLOADS["dropout_gqa_swa_b4_s2048"] = _w(
+    "dropout_gqa_swa_b4_s2048", 4, 2048, 32, 8, 128, 128, True, 1024, 0, None, 1,
+    "attention dropout p=0.1 on the GQA + SWA training shape: B=4, S=2048, H_q=32, H_kv=8, d=128, causal, "
+    "left window 1024", dropout=0.1)
 DEFAULT = "sweep_s8192_hkv8"
 
 
@@ -250,6 +263,8 @@ def run_oracle_unit(wl, x, b, h):
     do = x["dout"][b:b + 1, :L, h:h + 1].double().numpy()
     off = x["offset"][h:h + 1].double().numpy() if wl["st"] == 2 else None
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], offset=off, scale=wl["scale"])
+    if wl.get("dropout"):  # the unit takes the decisions of its (b, h) in the full problem
+        kw.update(dropout_p=wl["dropout"], rng_state=DROPOUT_RNG, dropout_origin=(b, h))
     if wl.get("bias"):
         Bb, Hb = wl["bias"]
         kw["bias"] = x["bias"][b if Bb > 1 else 0:(b if Bb > 1 else 0) + 1,
@@ -319,7 +334,8 @@ def bench_config(wl, world, det):
                if fp8 else {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
             "l2": "flushed between timed steps (258 MB write outside the timed span)",
             **({"seq_lens": wl["lens"]} if wl.get("lens") else {}),
-            **({"bias": f"bf16 {list(wl['bias']) + [wl['S'], wl['S']]}, dbias fp32"} if wl.get("bias") else {})}
+            **({"bias": f"bf16 {list(wl['bias']) + [wl['S'], wl['S']]}, dbias fp32"} if wl.get("bias") else {}),
+            **({"dropout": f"p={wl['dropout']}, rng_state {list(DROPOUT_RNG)}"} if wl.get("dropout") else {})}
 
 
 def uses_deterministic(wl, args):
@@ -403,6 +419,8 @@ def _step_fns(sdpa, wl, dev, det, x):
                      device=dev)
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], softmax_offset=off,
               scale=wl["scale"] or 0.0)
+    if wl.get("dropout"):
+        kw.update(dropout_p=wl["dropout"], rng_state=torch.tensor(list(DROPOUT_RNG), dtype=torch.int64, device=dev))
     if wl.get("lens"):
         lens = torch.tensor(wl["lens"], dtype=torch.int32, device=dev)
         kw.update(seq_lens_q=lens, seq_lens_kv=lens)

@@ -7,8 +7,9 @@
  * with grouped-query heads, a causal mask with an optional left sliding window,
  * distinct Q/K and V head dims, and three sink softmax types; plus padded batches
  * with per-entry lengths (attn_fwd_varlen / attn_bwd_varlen), an additive bias with
- * its gradient (attn_fwd_bias / attn_bwd_bias) and an E4M3 forward with per-tensor
- * scaling (attn_fp8_amax, attn_fp8_quantize, attn_fwd_fp8).
+ * its gradient (attn_fwd_bias / attn_bwd_bias), attention dropout (attn_fwd_dropout /
+ * attn_bwd_dropout) and an E4M3 forward with per-tensor scaling (attn_fp8_amax,
+ * attn_fp8_quantize, attn_fwd_fp8).
  *
  * Where each operation is defined:
  *   - the attention itself: "Speed up attention on GPU with cuDNN and
@@ -188,6 +189,42 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
 size_t attn_bwd_noalloc_max_scratch_bytes(void);
 /* Why the last attn_bwd_noalloc call on this thread failed, or "" (thread-local). */
 const char* attn_bwd_noalloc_message(void);
+
+/*
+ * Attention dropout.  Source: "JAX: Single-GPU Attention with TransformerEngine",
+ * section "Other attention knobs" (`attention_dropout`); the sequence diagrams of
+ * "[JAX] Add support for sink attention in JAX #2225" (the fused forward returns an
+ * rng_state that the fused backward takes).
+ *
+ * Each probability P_ij after the softmax (sink included in the normaliser) is
+ * dropped or kept; a kept one is scaled by 1/(1 - p):
+ *   O_i = sum_j P_ij M_ij v_j,   M_ij = keep_ij * 65536 / (65536 - t),
+ * while LSE (and p_sink) are those of the undropped softmax.  The backward uses
+ *   dS_ij = P_ij (M_ij dO_i . v_j - D_i),   D_i = dO_i . O_i,   dV_j = sum_i P_ij M_ij dO_i.
+ * The decisions come from a counter-based generator, so the backward regenerates
+ * them: Philox4x64-10 (Salmon et al., SC'11) keyed by rng_state = (seed, offset);
+ * pair (b, h, i, j) uses the counter (j / 4, i / 4, h, b), output word i % 4, 16-bit
+ * field j % 4 as a uniform u in [0, 65536), and is kept iff u >= t.
+ *
+ * dropout_p: drop probability in [0, 1), realised as t / 65536 with
+ *   t = floor(dropout_p * 65536 + 1/2) (from the float value); t = 0 runs the plain
+ *   kernels; a value outside [0, 1), or one that rounds to t = 65536, returns
+ *   ATTN_ERR_INVALID_ARG.
+ * rng_state: DEVICE pointer to two uint64 values, seed then offset, 8-byte aligned,
+ *   read by the kernels when they run (so a caller can advance the offset in place
+ *   between steps).  Pass the same state to the forward and the backward of a step.
+ * Otherwise as attn_fwd / attn_bwd (same workspace as attn_bwd).  Supported: full-length
+ * batches, no bias, (d_qk, d_v) in {(64, 64), (128, 128), (192, 128)}; other head dims
+ * return ATTN_ERR_UNSUPPORTED.
+ */
+int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+                     int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                     const float* softmax_offset, float dropout_p, const unsigned long long* rng_state, void* stream);
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
+                     int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                     const float* softmax_offset, float dropout_p, const unsigned long long* rng_state,
+                     int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Additive attention bias.  Source: "JAX: Single-GPU Attention with

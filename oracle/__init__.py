@@ -57,10 +57,10 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         i, d = ctypes.c_int, ctypes.c_double
         u64 = ctypes.c_uint64
-        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64,
+        lib.oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64, i, i,
                                    dp, dp, dp, dp]
         lib.oracle_fwd.restype = ctypes.c_int
-        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64,
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64, i, i,
                                    dp, dp, dp, dp, dp, dp]
         lib.oracle_bwd.restype = ctypes.c_int
         lib.oracle_philox4x64_10.argtypes = [ctypes.POINTER(u64), ctypes.POINTER(u64), ctypes.POINTER(u64)]
@@ -141,12 +141,14 @@ def _bias_args(bias, B, Hq, Sq, Skv):
 
 
 def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None):
+                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None, dropout_origin=(0, 0)):
     """O, LSE, p_sink, rowsum for BSHD q [B,Sq,Hq,dqk], k [B,Skv,Hkv,dqk], v [B,Skv,Hkv,dv].
 
     bias: optional [Bb,Hb,Sq,Skv] (Bb in {1,B}, Hb in {1,Hq}) added to the scaled scores.
     dropout_p, rng_state = (seed, offset): attention dropout (see oracle.c); rowsum,
-    LSE and p_sink are those of the undropped probabilities.
+    LSE and p_sink are those of the undropped probabilities.  dropout_origin = (b0, h0):
+    the arrays are batch entries b0.. and query heads h0.. of a bigger problem, whose
+    decisions they take.
     Returns a dict of float64 arrays: o [B,Sq,Hq,dv]; lse, psink, rowsum [B,Hq,Sq].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -164,6 +166,7 @@ def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
     rc = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, Hq, Hkv, dqk, dv,
                             scale, int(bool(causal)), int(window), int(softmax_type),
                             _ptr(off), _ptr(bias), Bb, Hb, t, seed, roff,
+                            int(dropout_origin[0]), int(dropout_origin[1]),
                             _ptr(o), _ptr(lse), _ptr(psink), _ptr(rowsum))
     if rc != 0:
         raise ValueError("oracle_fwd rejected its arguments")
@@ -171,7 +174,7 @@ def attention_fwd(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA,
 
 
 def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA,
-                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None):
+                  offset=None, scale=None, bias=None, dropout_p=0.0, rng_state=None, dropout_origin=(0, 0)):
     """dq, dk, dv, d_offset [Hq], D [B,Hq,Sq] (= dO.O) and, with a bias, dbias (its
     shape) for the same arguments as fwd."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -191,6 +194,7 @@ def attention_bwd(q, k, v, dout, *, causal=True, window=-1, softmax_type=VANILLA
     rc = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Sq, Skv, Hq, Hkv,
                             dqk, dv, scale, int(bool(causal)), int(window),
                             int(softmax_type), _ptr(off), _ptr(bias), Bb, Hb, t, seed, roff,
+                            int(dropout_origin[0]), int(dropout_origin[1]),
                             _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(doff), _ptr(D), _ptr(dbias))
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")

@@ -123,8 +123,10 @@ void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Dropout state: drop threshold t (0: no dropout) and the Philox key (seed, offset). */
-typedef struct { int t; uint64_t seed, offset; } dropout_t;
+/* Dropout state: drop threshold t (0: no dropout), the Philox key (seed, offset), and the
+ * batch / query-head index of the arrays' first entry / head in the problem they were cut
+ * from (0 for a whole problem): the decisions are those of (b + b0, h + h0). */
+typedef struct { int t; uint64_t seed, offset; int b0, h0; } dropout_t;
 
 /* The 16-bit uniform of pair (b, h, i, j) (see the header). */
 static unsigned dropout_u16(const dropout_t* d, int b, int h, int i, int j) {
@@ -137,14 +139,14 @@ static unsigned dropout_u16(const dropout_t* d, int b, int h, int i, int j) {
 /* M_ij: 65536 / (65536 - t) if the pair is kept, 0 if dropped; 1 without dropout. */
 static double dropout_mult(const dropout_t* d, int b, int h, int i, int j) {
     if (!d || d->t == 0) return 1.0;
-    return dropout_u16(d, b, h, i, j) >= (unsigned)d->t ? 65536.0 / (65536.0 - d->t) : 0.0;
+    return dropout_u16(d, b + d->b0, h + d->h0, i, j) >= (unsigned)d->t ? 65536.0 / (65536.0 - d->t) : 0.0;
 }
 
 /* The keep decisions of one (b, h) as bytes [Sq * Skv] (1 kept, 0 dropped), for tests. */
 int oracle_dropout_keep(int b, int h, int Sq, int Skv, int t, uint64_t seed, uint64_t offset,
                         unsigned char* keep) {
     if (t < 0 || t > 65535) return -1;
-    dropout_t d = {t, seed, offset};
+    dropout_t d = {t, seed, offset, 0, 0};
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < Sq; i++)
         for (int j = 0; j < Skv; j++)
@@ -209,10 +211,11 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
                const double* bias, int Bb, int Hb, int drop_t, uint64_t seed, uint64_t offset_rng,
+               int drop_b0, int drop_h0,
                double* o, double* lse, double* psink, double* rowsum) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
-    if (drop_t < 0 || drop_t > 65535) return -1;
-    dropout_t drop = {drop_t, seed, offset_rng};
+    if (drop_t < 0 || drop_t > 65535 || drop_b0 < 0 || drop_h0 < 0) return -1;
+    dropout_t drop = {drop_t, seed, offset_rng, drop_b0, drop_h0};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;
@@ -263,10 +266,11 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                int B, int Sq, int Skv, int Hq, int Hkv, int dqk, int dv,
                double scale, int causal, int window, int softmax_type, const double* offset,
                const double* bias, int Bb, int Hb, int drop_t, uint64_t seed, uint64_t offset_rng,
+               int drop_b0, int drop_h0,
                double* dq, double* dk, double* dvout, double* d_offset, double* Dout, double* dbias) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
-    if (drop_t < 0 || drop_t > 65535) return -1;
-    dropout_t drop = {drop_t, seed, offset_rng};
+    if (drop_t < 0 || drop_t > 65535 || drop_b0 < 0 || drop_h0 < 0) return -1;
+    dropout_t drop = {drop_t, seed, offset_rng, drop_b0, drop_h0};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
     if (dqk > ORACLE_MAX_D || dv > ORACLE_MAX_D) return -1;

@@ -90,6 +90,11 @@ def _load():
     lib.attn_fp8_vt_row_bytes.restype = i
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp, vp]
     lib.attn_fwd_fp8.restype = i
+    lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, f, vp, vp]
+    lib.attn_fwd_dropout.restype = i
+    lib.attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, f,
+                                     vp, i, vp, sz, vp]
+    lib.attn_bwd_dropout.restype = i
     _lib = lib
     return lib
 
@@ -164,14 +169,26 @@ def _check_bias(bias, B, H_q, S_q, S_kv):
     return Bb, Hb
 
 
+def _check_rng(rng_state):
+    """rng_state: a CUDA int64 (or uint64) tensor of two values, seed then offset."""
+    if rng_state is None:
+        raise ValueError("dropout needs rng_state: a CUDA int64 tensor [seed, offset]")
+    if rng_state.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)):
+        raise TypeError(f"rng_state must be int64 or uint64, got {rng_state.dtype}")
+    if tuple(rng_state.shape) != (2,) or not rng_state.is_contiguous() or not rng_state.is_cuda:
+        raise ValueError("rng_state must be a contiguous CUDA tensor of shape [2] (seed, offset)")
+
+
 def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-             seq_lens_q=None, seq_lens_kv=None, bias=None, stream=None):
+             seq_lens_q=None, seq_lens_kv=None, bias=None, dropout_p=0.0, rng_state=None, stream=None):
     """Forward into preallocated o [B,S_q,H_q,d_v] bf16 and lse [B,H_q,S_q] fp32.
 
     seq_lens_q / seq_lens_kv: optional int32 [B] device tensors for a padded batch
     (attn_fwd_varlen); None means full length.
     bias: optional bf16 [1 or B, 1 or H_q, S_q, S_kv] added to the scaled scores
     (attn_fwd_bias).
+    dropout_p, rng_state: attention dropout (attn_fwd_dropout); rng_state is a CUDA
+    int64 tensor [seed, offset], to be passed to the backward of the same step too.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, n, torch.bfloat16, 4)
@@ -184,7 +201,12 @@ def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, s
     _check_lens(seq_lens_kv, "seq_lens_kv", B)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0),
             int(bool(causal)), int(window), _stype(softmax_type), _ptr(softmax_offset))
-    if bias is not None:
+    if dropout_p:
+        if bias is not None or seq_lens_q is not None or seq_lens_kv is not None:
+            raise ValueError("dropout with a bias or padded batches is not supported")
+        _check_rng(rng_state)
+        st = _load().attn_fwd_dropout(*args, float(dropout_p), _ptr(rng_state), _stream(stream))
+    elif bias is not None:
         if seq_lens_q is not None or seq_lens_kv is not None:
             raise ValueError("bias with padded batches is not supported")
         Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
@@ -203,12 +225,13 @@ def attn_bwd_workspace_size(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, deterministic=Tr
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, window=-1, softmax_type=VANILLA,
              softmax_offset=None, scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None,
-             bias=None, dbias=None, stream=None):
+             bias=None, dbias=None, dropout_p=0.0, rng_state=None, stream=None):
     """Backward into preallocated dq, dk, dv (bf16) and d_offset (fp32 [H_q], learnable).
 
     seq_lens_q / seq_lens_kv as for attn_fwd (attn_bwd_varlen).  bias as for attn_fwd,
     with dbias an optional preallocated fp32 tensor of the bias's shape
-    (attn_bwd_bias).
+    (attn_bwd_bias).  dropout_p / rng_state as for attn_fwd (attn_bwd_dropout; the
+    forward's values).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16, 4)
@@ -224,7 +247,12 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, w
             B, S_q, S_kv, H_q, H_kv, d_qk, d_v, float(scale or 0.0), int(bool(causal)), int(window),
             _stype(softmax_type), _ptr(softmax_offset))
     tail = (int(bool(deterministic)), _ptr(workspace), workspace.numel(), _stream(stream))
-    if bias is not None:
+    if dropout_p:
+        if bias is not None or seq_lens_q is not None or seq_lens_kv is not None:
+            raise ValueError("dropout with a bias or padded batches is not supported")
+        _check_rng(rng_state)
+        st = _load().attn_bwd_dropout(*args, float(dropout_p), _ptr(rng_state), *tail)
+    elif bias is not None:
         if seq_lens_q is not None or seq_lens_kv is not None:
             raise ValueError("bias with padded batches is not supported")
         Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
@@ -280,6 +308,17 @@ def attn_fwd_varlen(q, k, v, o, lse, seq_lens_q, seq_lens_kv, **kw):
 def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q, seq_lens_kv, **kw):
     """attn_bwd on a padded batch (lengths as for attn_fwd_varlen)."""
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, **kw)
+
+
+def attn_fwd_dropout(q, k, v, o, lse, dropout_p, rng_state, **kw):
+    """attn_fwd with attention dropout: probability dropout_p, rng_state a CUDA int64
+    tensor [seed, offset]."""
+    attn_fwd(q, k, v, o, lse, dropout_p=dropout_p, rng_state=rng_state, **kw)
+
+
+def attn_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, d_offset, dropout_p, rng_state, **kw):
+    """attn_bwd of a forward with attention dropout (the forward's dropout_p and rng_state)."""
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, dropout_p=dropout_p, rng_state=rng_state, **kw)
 
 
 def attn_fwd_bias(q, k, v, o, lse, bias, **kw):
@@ -411,7 +450,7 @@ def sdpa_forward_fp8(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, s
 
 
 def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None, scale=0.0,
-                 seq_lens_q=None, seq_lens_kv=None, bias=None, stream=None):
+                 seq_lens_q=None, seq_lens_kv=None, bias=None, dropout_p=0.0, rng_state=None, stream=None):
     """Allocate O and LSE, run attn_fwd, return (o, lse)."""
     B, S_q, H_q, _ = q.shape
     d_v = v.shape[3]
@@ -419,13 +458,13 @@ def sdpa_forward(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, softm
     lse = torch.empty((B, H_q, S_q), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, v, o, lse, causal=causal, window=window, softmax_type=softmax_type,
              softmax_offset=softmax_offset, scale=scale, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv,
-             bias=bias, stream=stream)
+             bias=bias, dropout_p=dropout_p, rng_state=rng_state, stream=stream)
     return o, lse
 
 
 def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type=VANILLA, softmax_offset=None,
                   scale=0.0, deterministic=True, workspace=None, seq_lens_q=None, seq_lens_kv=None, bias=None,
-                  stream=None):
+                  dropout_p=0.0, rng_state=None, stream=None):
     """Allocate dQ, dK, dV (and d_offset for the learnable sink), run attn_bwd, return them;
     with a bias, also dbias (fp32, the bias's shape) as a fifth output."""
     dq = torch.empty_like(q)
@@ -436,7 +475,8 @@ def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type
     dbias = torch.empty(bias.shape, dtype=torch.float32, device=q.device) if bias is not None else None
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_off, causal=causal, window=window, softmax_type=st,
              softmax_offset=softmax_offset, scale=scale, deterministic=deterministic, workspace=workspace,
-             seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, bias=bias, dbias=dbias, stream=stream)
+             seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, bias=bias, dbias=dbias, dropout_p=dropout_p,
+             rng_state=rng_state, stream=stream)
     return (dq, dk, dv, d_off) if bias is None else (dq, dk, dv, d_off, dbias)
 
 

@@ -163,6 +163,28 @@ float resolve_scale(float scale, int d_qk) {
 using sdpa::check_common;
 using sdpa::resolve_scale;
 
+// The drop threshold t of dropout probability p: 16-bit uniforms below t are dropped,
+// so p is realised as t / 65536 with t = floor(p * 65536 + 1/2).  -1 when p is not in
+// [0, 1) or rounds to 1.
+static int drop_threshold(float p) {
+  if (!(p >= 0.f) || !(p < 1.f)) return -1;
+  const double t = std::floor(static_cast<double>(p) * 65536.0 + 0.5);
+  return t > 65535.0 ? -1 : static_cast<int>(t);
+}
+
+// Dropout arguments into the kernel parameters: ATTN_OK, or an error status.
+template <class P>
+static int set_dropout(P& prm, float dropout_p, const unsigned long long* rng_state) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return ATTN_ERR_INVALID_ARG;
+  prm.drop_t = static_cast<unsigned>(t);
+  prm.drop_scale = t > 0 ? static_cast<float>(65536.0 / (65536.0 - t)) : 1.f;
+  prm.rng = t > 0 ? rng_state : nullptr;
+  if (t > 0 && !rng_state) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(rng_state) & 7u) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
 extern "C" {
 
 const char* attn_last_error_message(void) { return g_last_error; }
@@ -208,8 +230,12 @@ static int check_bias(const void* bias, int bias_B, int bias_H, int B, int H_q, 
 static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
                     int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
                     const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, const void* bias,
-                    int bias_B, int bias_H, void* stream) {
+                    int bias_B, int bias_H, void* stream, float dropout_p = 0.f,
+                    const unsigned long long* rng_state = nullptr) {
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  sdpa::FwdParams p;
+  st = set_dropout(p, dropout_p, rng_state);
   if (st != ATTN_OK) return st;
   long long bsb = 0, bsh = 0;
   if (bias) {
@@ -234,7 +260,6 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
     set_error("cuTensorMapEncodeTiled (forward operands)");
     return ATTN_ERR_CUDA;
   }
-  sdpa::FwdParams p;
   p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
   p.scale_log2 = resolve_scale(scale, d_qk) * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
@@ -250,7 +275,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.bias_sb = bsb;
   p.bias_sh = bsh;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] { return sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s); });
+  int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] {
+    return p.drop_t ? sdpa::launch_attn_fwd_dropout(d_qk, d_v, tq, tk, tv, p, s)
+                    : sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s);
+  });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("forward kernel launch", cudaGetLastError());
@@ -274,6 +302,13 @@ int attn_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
                   softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, stream);
 }
 
+int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
+                     int H_q, int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                     const float* softmax_offset, float dropout_p, const unsigned long long* rng_state, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
+                  softmax_offset, nullptr, nullptr, nullptr, 1, 1, stream, dropout_p, rng_state);
+}
+
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv, int H_q,
              int H_kv, int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
              const float* softmax_offset, void* stream) {
@@ -291,11 +326,14 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
                     int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
                     const float* softmax_offset, const int* seq_lens_q, const int* seq_lens_kv, const void* bias,
                     int bias_B, int bias_H, float* dbias, int deterministic, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    void* stream, float dropout_p = 0.f, const unsigned long long* rng_state = nullptr) {
   if ((reinterpret_cast<uintptr_t>(seq_lens_q) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens_kv) & 3u) ||
       (reinterpret_cast<uintptr_t>(dbias) & 3u))
     return ATTN_ERR_MISALIGNED;
   int st = check_common(B, S_q, S_kv, H_q, H_kv, d_qk, d_v, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  sdpa::BwdParams p;
+  st = set_dropout(p, dropout_p, rng_state);
   if (st != ATTN_OK) return st;
   long long bsb = 0, bsh = 0;
   if (bias) {
@@ -336,7 +374,6 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  sdpa::BwdParams p;
   p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
   p.scale = resolve_scale(scale, d_qk);
   p.scale_log2 = p.scale * 1.4426950408889634f;
@@ -392,8 +429,10 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     set_error("cuTensorMapEncodeTiled (dQ accumulator)");
     return ATTN_ERR_CUDA;
   }
-  int rc = timed(ATTN_KERNEL_BWD_KV, 1, s,
-                 [&] { return sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s); });
+  int rc = timed(ATTN_KERNEL_BWD_KV, 1, s, [&] {
+    return p.drop_t ? sdpa::launch_bwd_kv_dropout(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s)
+                    : sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s);
+  });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("backward kv kernel launch", cudaGetLastError());
@@ -414,8 +453,10 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     if (!sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
         !sdpa::make_bshd_map(&tdo128, dout, B, S_q, H_q, d_v, 128))
       return ATTN_ERR_CUDA;
-    rc = timed(ATTN_KERNEL_BWD_Q, 1, s,
-               [&] { return sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s); });
+    rc = timed(ATTN_KERNEL_BWD_Q, 1, s, [&] {
+      return p.drop_t ? sdpa::launch_bwd_q_dropout(d_qk, d_v, tq128, tk, tv, tdo128, p, s)
+                      : sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);
+    });
     if (rc == -2) return ATTN_ERR_UNSUPPORTED;
     if (rc != 0) {
       set_error("backward dQ kernel launch", cudaGetLastError());
@@ -444,6 +485,16 @@ int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
                   window, softmax_type, softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, dbias,
                   deterministic, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv,
+                     int d_qk, int d_v, float scale, int causal, int window, int softmax_type,
+                     const float* softmax_offset, float dropout_p, const unsigned long long* rng_state,
+                     int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
+                  window, softmax_type, softmax_offset, nullptr, nullptr, nullptr, 1, 1, nullptr, deterministic,
+                  workspace, workspace_bytes, stream, dropout_p, rng_state);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

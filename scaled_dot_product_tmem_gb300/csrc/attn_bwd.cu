@@ -25,9 +25,7 @@
 //   bwd_dq_convert   dQ = bf16(scale * fp32 accumulator).
 #include <cuda_runtime.h>
 
-#include "attn_common.cuh"
-#include "attn_kernels.h"
-#include "ptx.cuh"
+#include "attn_bwd_kernels.cuh"
 
 namespace sdpa {
 
@@ -133,489 +131,7 @@ int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream) {
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-// =============================================================================
-// kv-stationary main kernel
-// =============================================================================
-template <int D_QK, int D_V, bool FUSE_DQ>
-struct KvCfg {
-  static constexpr int BN = 128;  // keys per CTA (TMEM lanes)
-  static constexpr int BQ = 64;   // query rows per step
-  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
-  static constexpr int KCHUNK = 128 * 128;  // 128 rows x 128 bytes
-  static constexpr int QCHUNK = 64 * 128;   // 64 rows x 128 bytes
-  static constexpr int NQ = (D_QK == 64 && D_V == 64) ? 6 : 3;
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + QCH * KCHUNK;
-  static constexpr int OFF_DS = OFF_V + VCH * KCHUNK;  // 2 x dS^T [128 keys x 64 q] bf16, swizzled
-  static constexpr int DS_BUF = 128 * 128;
-  static constexpr int DS_BYTES = FUSE_DQ ? 2 * DS_BUF : 0;
-  static constexpr int OFF_Q = OFF_DS + DS_BYTES;
-  static constexpr int Q_STAGE = QCH * QCHUNK;
-  static constexpr int OFF_DO = OFF_Q + NQ * Q_STAGE;
-  static constexpr int DO_STAGE = VCH * QCHUNK;
-  static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // nlse2[64] + D[64] per stage
-  static constexpr int L_STAGE = 2 * BQ * 4;
-  static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
-  static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, dq_ready, dq_free,
-  // mma_done, dv_done[2], dk_done.  Barriers of the double-buffered S slot are per slot: with
-  // two slots the P/dS warps can finish step s+1's P before issuer B has waited for step s's,
-  // and a single barrier would then complete two phases before B looks.
-  static constexpr int NBAR = 1 + 2 * NQ + 12;
-  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
-  static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
-  static constexpr int THREADS = FUSE_DQ ? 480 : 352;
-  // TMEM columns
-  // S^T/P^T is double-buffered (slots COL_S0 / COL_S1, step s uses slot s & 1) so the
-  // next step's scores can be computed while the current P^T still feeds dV.
-  static constexpr int COL_S0 = 0, COL_DP = 64, COL_DV = 128, COL_DK = 128 + D_V, COL_DQ = 128 + D_V + D_QK;
-  static constexpr int COL_S1 = COL_DQ + (FUSE_DQ ? 64 : 0);
-  static_assert(COL_S1 + 64 <= 512, "TMEM budget");
-  // dQ^T = K^T dS^T is issued with M = 128 head-dim rows; with d_qk = 64 its rows 64-127
-  // read the next 64 columns of shared memory (the V tile) and are never drained.
-  static_assert(!FUSE_DQ || D_QK == 128 || D_QK == 64, "fused dQ for d_qk in {64, 128}");
-  static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(SMEM > 116 * 1024, "one CTA per SM");
-};
-
-constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's block order
-
-enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
-              kKvDvDone, kKvDkDone };
-
-template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false>
-__global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
-    attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
-  using C = KvCfg<D_QK, D_V, FUSE_DQ>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = q_full + C::NQ;
-  uint64_t* s_ready = q_empty + C::NQ;  // [2], per S slot
-  uint64_t* dp_ready = s_ready + 2;
-  uint64_t* p_ready = s_ready + 3;      // [2], per S slot
-  uint64_t* ds_ready = s_ready + 5;
-  uint64_t* dq_ready = s_ready + 6;
-  uint64_t* dq_free = s_ready + 7;
-  uint64_t* mma_done = s_ready + 8;
-  uint64_t* dv_done = s_ready + 9;      // [2], per S slot
-  uint64_t* dk_done = s_ready + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order: groups (b, kv head) in chunks of kKvChunk; within a chunk, kv tile
-  // by kv tile (tile 0, the most work when causal, first) and group by group.  Blocks
-  // start in index order, so the long blocks of every chunk start early while the
-  // chunk's queries stay few enough to be shared in L2.
-  const int n_kv = (p.S_kv + C::BN - 1) / C::BN;
-  const int n_gr = p.H_kv * p.B * p.ns;  // group = (b, kv head, head split)
-  const int per_chunk = kKvChunk * n_kv;
-  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
-  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
-  const int g = chunk * kKvChunk + within % csize;
-  const int split = g % p.ns, hk = (g / p.ns) % p.H_kv, b = g / (p.ns * p.H_kv);
-  const int Gs = p.G / p.ns;               // query heads this CTA walks
-  const int h0 = hk * p.G + split * Gs;    // the first of them
-  const int n0 = (within / csize) * C::BN;
-  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
-                                      p.window}
-                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
-  int ilo = 0, ihi = -1;
-  const bool any_q = q_tile_range(mask, n0, n0 + C::BN - 1, C::BQ, &ilo, &ihi);
-  const int nq = any_q ? ihi - ilo + 1 : 0;
-  const int nsteps = nq * Gs;
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < C::NQ; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
-    mbar_init(&s_ready[0], 1);
-    mbar_init(&s_ready[1], 1);
-    mbar_init(dp_ready, 1);
-    mbar_init(&p_ready[0], 256);
-    mbar_init(&p_ready[1], 256);
-    mbar_init(ds_ready, 256);
-    mbar_init(dq_ready, 1);
-    mbar_init(dq_free, 128);
-    mbar_init(mma_done, 2);
-    mbar_init(&dv_done[0], 1);
-    mbar_init(&dv_done[1], 1);
-    mbar_init(dk_done, 1);
-    fence_barrier_init();
-  }
-  if (warp == 8) {
-    tmem_alloc<512>(tmem_slot);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  int* err = p.err;
-
-  if (warp == 9) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nsteps > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(kv_full, (C::QCH + C::VCH) * C::KCHUNK);
-      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_K + c * C::KCHUNK, &tmK, kv_full, c * 64, hk, n0, b);
-      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_V + c * C::KCHUNK, &tmV, kv_full, c * 64, hk, n0, b);
-      for (int s = 0; s < nsteps; ++s) {
-        const int st = s % C::NQ;
-        if (!mbar_wait(&q_empty[st], ((s / C::NQ) & 1) ^ 1, err, kKvQEmpty)) break;
-        const int h = h0 + s / nq;
-        const int q0 = (ilo + s % nq) * C::BQ;
-        mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE);
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(smem + C::OFF_Q + st * C::Q_STAGE + c * C::QCHUNK, &tmQ, &q_full[st], c * 64, h, q0, b);
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::OFF_DO + st * C::DO_STAGE + c * C::QCHUNK, &tmDO, &q_full[st], c * 64, h, q0, b);
-        const size_t row = ((size_t)b * p.H_q + h) * p.S_pad + q0;
-        bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.nlse2 + row, C::BQ * 4, &q_full[st]);
-        bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
-      }
-      mbar_wait(kv_full, 0, err, kKvDrain);
-      for (int s = 0; s < C::NQ && s < nsteps; ++s) {
-        const int last = s + ((nsteps - 1 - s) / C::NQ) * C::NQ;
-        mbar_wait(&q_full[s], (last / C::NQ) & 1, err, kKvDrain);
-      }
-    }
-  } else if (warp == 8 || warp == C::MMA_B_WARP) {
-    // ------------------------------------------------------------ MMA issuers
-    // Two issuing warps, because one cannot issue tcgen05.mma fast enough to
-    // keep the tensor core busy with these 64-wide tiles:
-    //   A (warp 8):  S^T(s) = K Q_s^T, dP^T(s) = V dO_s^T
-    //   B:           dV += P^T(s) dO_s, dK += dS^T(s) Q_s, [dQ^T(s) = K^T dS^T(s)]
-    // MMAs of different warps are not ordered, so A waits for B's dv_done
-    // before S(s) overwrites the columns that held P(s-1), and for B's dk_done(s-1)
-    // before dP(s) overwrites the columns that held dS(s-1).
-    if (nsteps > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
-      constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
-      constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
-      constexpr uint32_t idDK = idesc_bf16_f32(128, D_QK, false, true);
-      constexpr uint32_t idDQ = idesc_bf16_f32(128, C::BQ, true, true);
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait_warp(kv_full, 0, err, kKvFull);
-      if (warp == 8) {
-        const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);  // K as K-major A of S^T
-        const uint64_t dV0 = smem_desc_sw128(sV, 16, 1024);  // V as K-major A of dP^T
-        for (int s = 0; s < nsteps && ok; ++s) {
-          const int st = s % C::NQ;
-          const int slot = s & 1;
-          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
-          // slot reuse: P^T(s-2) in this slot must have been read by dV(s-2)
-          if (ok && s >= 2) ok = mbar_wait_warp(&dv_done[slot], ((s >> 1) - 1) & 1, err, kKvDvDone);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dq = smem_desc_sw128(sQ + st * C::Q_STAGE, 16, 1024);
-          const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
-#pragma unroll
-          for (int kk = 0; kk < D_QK / 16; ++kk)
-            mma_ss_warp(colS, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
-                   desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
-          mma_commit_warp(&s_ready[slot]);
-          if (s > 0) ok = mbar_wait_warp(dk_done, (s - 1) & 1, err, kKvDkDone);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t ddo = smem_desc_sw128(sDO + st * C::DO_STAGE, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D_V / 16; ++kk)
-            mma_ss_warp(tmem + C::COL_DP, desc_add(dV0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
-                   desc_add(ddo, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
-          mma_commit_warp(dp_ready);
-        }
-      } else {
-        const uint64_t dKt0 = smem_desc_sw128(sK, C::KCHUNK, 1024);   // K as MN-major A of dQ^T
-        const uint64_t dDS0 = smem_desc_sw128(sDS, C::KCHUNK, 1024);  // dS^T as MN-major B of dQ^T
-        for (int s = 0; s < nsteps && ok; ++s) {
-          const int st = s % C::NQ;
-          const uint64_t ddo_mn = smem_desc_sw128(sDO + st * C::DO_STAGE, C::QCHUNK, 1024);  // dO, MN-major B of dV
-          const uint64_t dq_mn = smem_desc_sw128(sQ + st * C::Q_STAGE, C::QCHUNK, 1024);     // Q, MN-major B of dK
-          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait_warp(&p_ready[s & 1], (s >> 1) & 1, err, kKvP);
-          if (!ok) break;
-          tc_fence_after();
-          const int slot = s & 1;
-          const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
-          // dV += P^T dO   (P^T bf16 in the slot: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
-#pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts_warp(tmem + C::COL_DV, colS + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048), idDV,
-                   (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_warp(&dv_done[slot]);
-          ok = mbar_wait_warp(ds_ready, s & 1, err, kKvDS);
-          if (!ok) break;
-          tc_fence_after();
-          // dK += dS^T Q
-#pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
-                   idDK, (s > 0 || kk > 0) ? 1u : 0u);
-          // dS^T(s) in TMEM is consumed once dK(s) completes: issuer A may write dP(s+1).
-          // (dQ^T reads dS^T from shared memory, double-buffered, so it does not gate dP.)
-          mma_commit_warp(dk_done);
-          if constexpr (FUSE_DQ) {
-            ok = mbar_wait_warp(dq_free, (s & 1) ^ 1, err, kKvDQFree);
-            if (!ok) break;
-            tc_fence_after();
-            // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
-            const uint64_t dDS = desc_add(dDS0, slot * C::DS_BUF);
-#pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ss_warp(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS, kk * 2048), idDQ, kk > 0);
-            mma_commit_warp(dq_ready);
-          }
-          // The stage's S/dP MMAs (issuer A) completed before P(s)/dS(s) existed.
-          mma_commit_warp(&q_empty[st]);
-        }
-      }
-      // Every MMA of both issuers must be complete before TMEM is released.
-      mma_commit_warp(mma_done);
-      mbar_wait_warp(mma_done, 0, err, kKvDone);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ P / dS warpgroups
-    const int w = warp / 4;  // which 32 query columns of the 64
-    const int r = (warp % 4) * 32 + lane;
-    const int key = n0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-    const float sl2 = p.scale_log2;
-    // bias: this thread's key column of the bias plane (keys past S_kv read key 0; their P is 0)
-    const int bkey = key < p.S_kv ? key : 0;
-    bool ok = true;
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int st = s % C::NQ;
-      const int q0 = (ilo + s % nq) * C::BQ;
-      [[maybe_unused]] const long long bplane = BIAS ? b * p.bias_sb + (h0 + s / nq) * p.bias_sh : 0;
-      const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
-      const float* dd = l2 + C::BQ;
-      const int slot = s & 1;
-      const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
-      ok = mbar_wait_warp(&s_ready[slot], (s >> 1) & 1, err, kKvS);
-      if (!ok) break;
-      tc_fence_after();
-      float pr[32];
-      {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + colS + 32 * w, rr);
-        float lv[32];  // -LSE * log2(e) of the 32 queries
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
-        if constexpr (BIAS) {  // + bias * log2(e) (queries past S_q read 0; their P is 0)
-          const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int qq = q0 + 32 * w + c;
-            const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
-            lv[c] = fmaf(bv, kLog2e, lv[c]);
-          }
-        }
-        tmem_ld_wait();
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float xa, xb;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2, f2_pack(lv[c], lv[c + 1])),
-                    xa, xb);
-          pr[c] = ex2(xa);
-          pr[c + 1] = ex2(xb);
-        }
-      }
-      if (!tile_fully_visible<VL>(mask, q0, C::BQ, n0, C::BN)) {
-        int vlo, vhi;  // the query rows that see this thread's key
-        visible_rows<VL>(mask, key, &vlo, &vhi);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int qq = q0 + 32 * w + c;
-          pr[c] = (qq >= vlo && qq <= vhi) ? pr[c] : 0.f;
-        }
-      }
-      {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
-        tmem_st16(lane_addr + colS + 32 * w, pk);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(&p_ready[slot]);
-      ok = mbar_wait_warp(dp_ready, s & 1, err, kKvDP);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dsk[16];
-      {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
-        float dv4[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          // dS = P (dP - D), paired
-          float a, bq;
-          f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
-                           f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
-                                  f2_pack(dv4[2 * c], dv4[2 * c + 1]))),
-                    a, bq);
-          dsk[c] = pack_bf16x2(a, bq);
-          if constexpr (BIAS) {  // dbias = dS, summed with fp32 atomics over the (b, h) sharing it
-            if (p.dbias && key < p.S_kv) {
-              const int qq = q0 + 32 * w + 2 * c;
-              float* dcol = p.dbias + bplane + key;
-              if (qq < p.S_q) atomicAdd(dcol + (size_t)qq * p.S_kv, a);
-              if (qq + 1 < p.S_q) atomicAdd(dcol + (size_t)(qq + 1) * p.S_kv, bq);
-            }
-          }
-        }
-      }
-      tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
-      if constexpr (FUSE_DQ) {
-        // dS^T row r, query columns 32w..32w+31 -> 16-byte chunks 4w..4w+3 (128-byte swizzle)
-        uint8_t* rowp = smem + C::OFF_DS + slot * C::DS_BUF + r * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = (4 * w + k) ^ (r & 7);
-          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-              make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_ready);
-    }
-    // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
-    bool have = false;
-    if (ok && nsteps > 0) {
-      have = mbar_wait_warp(mma_done, 0, err, kKvDone);
-      tc_fence_after();
-    }
-    {
-      const bool row_ok = key < p.S_kv;  // all lanes load TMEM; only real keys store
-      const int krow = row_ok ? key : 0;
-      const int ncols = w == 0 ? D_V : D_QK;
-      const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
-      const float mul = w == 0 ? 1.f : p.scale;
-      const size_t row = ((size_t)b * p.S_kv + krow) * p.H_kv + hk;
-      __nv_bfloat16* dst = w == 0 ? p.dv + row * D_V : p.dk + row * D_QK;
-      // with head splits this CTA's sum is one fp32 partial slice
-      float* part = p.ns == 1 ? nullptr
-                              : (w == 0 ? p.dv_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_V
-                                        : p.dk_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_QK);
-#pragma unroll 1
-      for (int c0 = 0; c0 < ncols; c0 += 32) {
-        uint32_t rr[32];
-        if (have) {
-          tmem_ld32(lane_addr + col0 + c0, rr);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) rr[c] = 0u;
-        }
-        if (part) {
-          if (row_ok) {
-            float4* f4 = reinterpret_cast<float4*>(part + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              f4[q] = make_float4(__uint_as_float(rr[4 * q]) * mul, __uint_as_float(rr[4 * q + 1]) * mul,
-                                  __uint_as_float(rr[4 * q + 2]) * mul, __uint_as_float(rr[4 * q + 3]) * mul);
-          }
-          continue;
-        }
-        uint32_t pw[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * mul, __uint_as_float(rr[2 * c + 1]) * mul);
-        if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-        }
-      }
-    }
-  } else if (FUSE_DQ && warp >= 10 && warp < 14) {
-    // ------------------------------------------------------------ dQ drain: TMEM lane = head-dim index d
-    // dQ^T of each step goes TMEM -> registers -> shared memory as [q][d] fp32, and
-    // one thread adds the whole 64 x d_qk tile into the fp32 accumulator with a
-    // TMA bulk reduction (rows past S_q are skipped by the TMA unit).
-    const int d = (warp % 4) * 32 + lane;
-    const int tid_d = threadIdx.x - 320;  // 0..127 over the four drain warps
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-    float* stage = reinterpret_cast<float*>(smem + C::OFF_DQS);
-    if (tid_d == 0) tma_prefetch_desc(&tmDQ);
-    for (int s = 0; s < nsteps; ++s) {
-      const bool got = mbar_wait(dq_ready, s & 1, err, kKvDQReady);
-      if (!bar_red_and(1, 128, got)) break;  // uniform over the 128 drain threads
-      tc_fence_after();
-      const int h = h0 + s / nq;
-      const int q0 = (ilo + s % nq) * C::BQ;
-      uint32_t ra[32], rb[32];
-      tmem_ld32(lane_addr + C::COL_DQ, ra);
-      tmem_ld32(lane_addr + C::COL_DQ + 32, rb);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(dq_free);  // the TMEM columns may be overwritten now
-      if (tid_d == 0) bulk_wait_read_all();  // previous tile has left shared memory
-      named_bar_sync(1, 128);
-      if (d < D_QK) {  // lanes past d_qk hold the unused rows of the M = 128 product
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          stage[c * D_QK + d] = __uint_as_float(ra[c]);
-          stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tid_d == 0) {
-        tma_reduce_add_4d(&tmDQ, stage, 0, h, q0, b);
-        bulk_commit_group();
-      }
-    }
-    if (tid_d == 0) bulk_wait_all();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 8) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc<512>(tmem);
-  }
-}
-
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return (d_qk == 128 || d_qk == 64) && (d_v == 128 || d_v == 64); }
-
-template <int D_QK, int D_V, bool FUSE>
-static int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
-  using C = KvCfg<D_QK, D_V, FUSE>;
-  // padded batches get the instantiation with the per-entry lengths and row tests
-  auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true>
-                                    : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
-  if (p.bias) {  // bias instantiations: full-length batches, d_qk = d_v in {64, 128}
-    if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
-      if (p.seq_q || p.seq_kv) return -2;
-      kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, true>;
-    } else {
-      return -2;
-    }
-  }
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
-  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
-}
 
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
@@ -634,349 +150,6 @@ int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& t
   if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
   if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
   return -2;
-}
-
-// =============================================================================
-// query-stationary deterministic dQ kernel
-// =============================================================================
-template <int D_QK, int D_V>
-struct QCfg {
-  static constexpr int BM = 128, BN = 128;
-  static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
-  static constexpr int CHUNK = 128 * 128;
-  static constexpr int NK = 2;
-  static constexpr int NV = (D_QK == 192 && D_V == 128) ? 1 : 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + QCH * CHUNK;
-  static constexpr int OFF_K = OFF_DO + VCH * CHUNK;
-  static constexpr int OFF_V = OFF_K + NK * QCH * CHUNK;
-  static constexpr int OFF_BAR = OFF_V + NV * VCH * CHUNK;
-  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready, ds_ready, mma_done,
-  // s_free, dq_done
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 6;
-  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
-  static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
-  static constexpr int THREADS = 352;
-  // dS (bf16) is written over the dP columns, so the next S can be computed as soon
-  // as the dS warps have loaded the current S.
-  static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256;
-  static_assert(COL_DQ + D_QK <= 512, "TMEM budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
-};
-
-enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone };
-
-template <int D_QK, int D_V, bool VL, bool BIAS = false>
-__global__ void __launch_bounds__(352, 1)
-    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                      const BwdParams p) {
-  using C = QCfg<D_QK, D_V>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + C::NK;
-  uint64_t* v_full = k_empty + C::NK;
-  uint64_t* v_empty = v_full + C::NV;
-  uint64_t* s_ready = v_empty + C::NV;
-  uint64_t* dp_ready = s_ready + 1;
-  uint64_t* ds_ready = s_ready + 2;
-  uint64_t* mma_done = s_ready + 3;
-  uint64_t* s_free = s_ready + 4;
-  uint64_t* dq_done = s_ready + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order as in the kv kernel: (b, head) groups in chunks of kKvChunk (heads of a
-  // chunk share K and V in L2), within a chunk query tile by query tile, the tile with
-  // the most kv tiles (the last one when causal) first.
-  const int n_qt = (p.S_q + C::BM - 1) / C::BM;
-  const int n_gr = p.H_q * p.B;
-  const int per_chunk = kKvChunk * n_qt;
-  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
-  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
-  const int g = chunk * kKvChunk + within % csize;
-  const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
-  const int h = g % p.H_q, b = g / p.H_q, hk = h / p.G;
-  const int m0 = qt * C::BM;
-  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
-                                      p.window}
-                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
-  int jlo = 1, jhi = 0;
-  const bool active = kv_tile_range(mask, m0, m0 + C::BM - 1, C::BN, &jlo, &jhi);
-  const int nj = active ? jhi - jlo + 1 : 0;
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
-    for (int s = 0; s < C::NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
-    mbar_init(s_ready, 1);
-    mbar_init(dp_ready, 1);
-    mbar_init(ds_ready, 256);
-    mbar_init(mma_done, 2);
-    mbar_init(s_free, 256);
-    mbar_init(dq_done, 1);
-    fence_barrier_init();
-  }
-  if (warp == 8) {
-    tmem_alloc<512>(tmem_slot);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  int* err = p.err;
-
-  if (warp == 9) {
-    if (lane == 0 && nj > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(q_full, (C::QCH + C::VCH) * C::CHUNK);
-      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_Q + c * C::CHUNK, &tmQ, q_full, c * 64, h, m0, b);
-      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_DO + c * C::CHUNK, &tmDO, q_full, c * 64, h, m0, b);
-      for (int n = 0; n < nj; ++n) {
-        const int j = jlo + n;
-        const int sk = n % C::NK, sv = n % C::NV;
-        if (!mbar_wait(&k_empty[sk], ((n / C::NK) & 1) ^ 1, err, kQKEmpty)) break;
-        mbar_arrive_expect_tx(&k_full[sk], C::QCH * C::CHUNK);
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(smem + C::OFF_K + (sk * C::QCH + c) * C::CHUNK, &tmK, &k_full[sk], c * 64, hk, j * C::BN, b);
-        if (!mbar_wait(&v_empty[sv], ((n / C::NV) & 1) ^ 1, err, kQVEmpty)) break;
-        mbar_arrive_expect_tx(&v_full[sv], C::VCH * C::CHUNK);
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::OFF_V + (sv * C::VCH + c) * C::CHUNK, &tmV, &v_full[sv], c * 64, hk, j * C::BN, b);
-      }
-      mbar_wait(q_full, 0, err, kQDrain);
-      for (int s = 0; s < C::NK && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / C::NK) * C::NK;
-        mbar_wait(&k_full[s], (last / C::NK) & 1, err, kQDrain);
-      }
-      for (int s = 0; s < C::NV && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / C::NV) * C::NV;
-        mbar_wait(&v_full[s], (last / C::NV) & 1, err, kQDrain);
-      }
-    }
-  } else if (warp == 8 || warp == 10) {
-    // ------------------------------------------------------------ MMA issuers
-    //   A (warp 8):  S(n) = Q K_n^T, dP(n) = dO V_n^T
-    //   B (warp 10): dQ += dS(n) K_n
-    // S(n+1) waits for the dS warps to have loaded S(n) (s_free); dP(n+1) waits
-    // for dQ(n), which reads dS(n) from the dP columns (dq_done).
-    if (nj > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idDQ = idesc_bf16_f32(128, D_QK, false, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      bool ok = mbar_wait_warp(q_full, 0, err, kQQ);
-      if (warp == 8) {
-        const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
-        for (int n = 0; n < nj && ok; ++n) {
-          const int sk = n % C::NK, sv = n % C::NV;
-          const uint64_t dKa = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, 16, 1024);
-          const uint64_t dVa = smem_desc_sw128(sV + sv * C::VCH * C::CHUNK, 16, 1024);
-          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull);
-          if (ok && n > 0) ok = mbar_wait_warp(s_free, (n - 1) & 1, err, kQSFree);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D_QK / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-            mma_ss_warp(tmem + C::COL_S, desc_add(dQ0, off), desc_add(dKa, off), idS, kk > 0);
-          }
-          mma_commit_warp(s_ready);
-          ok = mbar_wait_warp(&v_full[sv], (n / C::NV) & 1, err, kQVFull);
-          if (ok && n > 0) ok = mbar_wait_warp(dq_done, (n - 1) & 1, err, kQDqDone);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D_V / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-            mma_ss_warp(tmem + C::COL_DP, desc_add(dDO0, off), desc_add(dVa, off), idS, kk > 0);
-          }
-          mma_commit_warp(dp_ready);
-          mma_commit_warp(&v_empty[sv]);
-        }
-      } else {
-        for (int n = 0; n < nj && ok; ++n) {
-          const int sk = n % C::NK;
-          const uint64_t dKmn = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, C::CHUNK, 1024);
-          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull) && mbar_wait_warp(ds_ready, n & 1, err, kQDS);
-          if (!ok) break;
-          tc_fence_after();
-          // dQ += dS K   (dS bf16 over the dP columns: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts_warp(tmem + C::COL_DQ, tmem + C::COL_DP + (kk / 4) * 64 + (kk % 4) * 8, desc_add(dKmn, kk * 2048),
-                   idDQ, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_warp(dq_done);
-          mma_commit_warp(&k_empty[sk]);  // S(n) (issuer A) completed before dS(n) existed
-        }
-      }
-      mma_commit_warp(mma_done);
-      mbar_wait_warp(mma_done, 0, err, kQDone);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dS warpgroups: thread = query row
-    const int w = warp / 4;  // keys 64w .. 64w+63 of each kv tile
-    const int r = (warp % 4) * 32 + lane;
-    const int i = m0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-    const float sl2 = p.scale_log2;
-    float nl2row = -INFINITY, drow = 0.f;
-    if (i < p.S_q) {
-      const size_t ri = ((size_t)b * p.H_q + h) * p.S_pad + i;
-      nl2row = p.nlse2[ri];
-      drow = p.Dsum[ri];
-    }
-    // bias: this row of the bias plane (rows past S_q read row S_q - 1; their P is 0)
-    [[maybe_unused]] const __nv_bfloat16* brow =
-        BIAS ? p.bias + b * p.bias_sb + h * p.bias_sh + (size_t)min(i, p.S_q - 1) * p.S_kv : nullptr;
-    [[maybe_unused]] const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
-    bool ok = true;
-    for (int n = 0; n < nj && ok; ++n) {
-      const int k0 = (jlo + n) * C::BN + 64 * w;
-      ok = mbar_wait_warp(s_ready, n & 1, err, kQS);
-      if (!ok) break;
-      tc_fence_after();
-      const bool full = tile_fully_visible<VL>(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
-      float pr[64];
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(lane_addr + C::COL_S + 64 * w, ra);
-        tmem_ld32(lane_addr + C::COL_S + 64 * w + 32, rb);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(s_free);  // S is in registers: the next S may be written
-        // P = exp2(S * scale * log2(e) - LSE * log2(e)), one f32x2 FMA per key pair
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2row, nl2row);
-        if constexpr (BIAS) {  // (+ bias * log2(e)): the bias enters through the addend
-          const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
-#pragma unroll
-          for (int c8 = 0; c8 < 64; c8 += 8) {
-            float bv[8];
-            load_bias8(brow, k0 + c8, p.S_kv, bias_vec, bv);
-            const uint32_t* src = c8 < 32 ? ra : rb;
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const int c = (c8 % 32) + e;
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(src[c]), __uint_as_float(src[c + 1])), sl2x2,
-                               f2_fma(f2_pack(bv[e], bv[e + 1]), l2e2, nl2x2)),
-                        x0, x1);
-              pr[c8 + e] = ex2(x0);
-              pr[c8 + e + 1] = ex2(x1);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float x0, x1, y0, y1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2x2), x0, x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, nl2x2), y0, y1);
-            pr[c] = ex2(x0);
-            pr[c + 1] = ex2(x1);
-            pr[32 + c] = ex2(y0);
-            pr[32 + c + 1] = ex2(y1);
-          }
-        }
-      }
-      if (!full) {  // this row sees keys [vlo, vhi]: two compares per key
-        int vlo, vhi;
-        visible_keys<VL>(mask, i, &vlo, &vhi);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
-      }
-      ok = mbar_wait_warp(dp_ready, n & 1, err, kQDP);
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t drow2 = f2_pack(drow, drow);
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 64 * w + c0, rr);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {  // dS = P (dP - D), paired
-          float a, bq;
-          f2_unpack(f2_mul(f2_pack(pr[c0 + 2 * c], pr[c0 + 2 * c + 1]),
-                           f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])), drow2)),
-                    a, bq);
-          pk[c] = pack_bf16x2(a, bq);
-        }
-        tmem_st16(lane_addr + C::COL_DP + 64 * w + c0 / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_ready);
-    }
-    // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2)
-    bool have = false;
-    if (ok && nj > 0) {
-      have = mbar_wait_warp(mma_done, 0, err, kQDone);
-      tc_fence_after();
-    }
-    {
-      const bool row_ok = i < p.S_q;  // all lanes load TMEM; only real rows store
-      __nv_bfloat16* dst = p.dq + (((size_t)b * p.S_q + (row_ok ? i : 0)) * p.H_q + h) * D_QK;
-      constexpr int HALF = D_QK / 2;
-#pragma unroll 1
-      for (int c0 = w * HALF; c0 < (w + 1) * HALF; c0 += 32) {
-        uint32_t rr[32];
-        if (have) {
-          tmem_ld32(lane_addr + C::COL_DQ + c0, rr);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) rr[c] = 0u;
-        }
-        uint32_t pw[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * p.scale, __uint_as_float(rr[2 * c + 1]) * p.scale);
-        if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 8) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc<512>(tmem);
-  }
-}
-
-template <int D_QK, int D_V>
-static int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const BwdParams& p, cudaStream_t stream) {
-  using C = QCfg<D_QK, D_V>;
-  // padded batches get the instantiation with the per-entry lengths and row tests
-  auto kern = (p.seq_q || p.seq_kv) ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
-  if (p.bias) {
-    if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
-      if (p.seq_q || p.seq_kv) return -2;
-      kern = attn_bwd_q_kernel<D_QK, D_V, false, true>;
-    } else {
-      return -2;
-    }
-  }
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
-  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -25,6 +25,11 @@ struct FwdParams {
   // (0 along a broadcast dim)
   const __nv_bfloat16* bias = nullptr;
   long long bias_sb = 0, bias_sh = 0;
+  // attention dropout (drop_t > 0): rng = device [seed, offset] (the Philox key), drop
+  // threshold t (16-bit uniforms below it are dropped), kept values scaled by drop_scale
+  const unsigned long long* rng = nullptr;
+  unsigned drop_t = 0;
+  float drop_scale = 1.f;
 };
 
 // Returns 0 on a successful launch, -2 for an unsupported (d_qk, d_v), -1 on a
@@ -71,6 +76,10 @@ struct BwdParams {
   const __nv_bfloat16* bias = nullptr;
   long long bias_sb = 0, bias_sh = 0;
   float* dbias = nullptr;
+  // attention dropout, as in FwdParams (the same rng state regenerates the forward's decisions)
+  const unsigned long long* rng = nullptr;
+  unsigned drop_t = 0;
+  float drop_scale = 1.f;
 };
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
@@ -88,6 +97,16 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
                  const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
+
+// Dropout instantiations (full-length batches, bf16, no bias; (d_qk, d_v) in
+// {(64, 64), (128, 128), (192, 128)}): the same contracts as the launchers above.
+int launch_attn_fwd_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, cudaStream_t stream);
+int launch_bwd_kv_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
+                          cudaStream_t stream);
+int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 
 // One warp waits on an mbarrier nobody arrives at: after the wait limit it records
 // kErrTimeoutBase + site in *err and returns (the failure path, without a fault).

@@ -167,3 +167,26 @@ def test_binding_has_every_boundary_name():
     import scaled_dot_product_tmem_gb300 as sdpa
     for n in declared_functions():
         assert callable(getattr(sdpa, n, None)), f"{n} has no binding of the same name"
+
+
+def test_dropout_argument_validation(lib):
+    """attn_fwd_dropout / attn_bwd_dropout reject a probability outside [0, 1) (or one
+    that rounds to t = 65536), a missing rng_state and a misaligned one, before any
+    device work."""
+    f = ctypes.c_float
+    MIS4 = ctypes.c_void_p(0x10004)
+
+    def fwd_d(p, rng):
+        return lib.attn_fwd_dropout(P, P, P, P, P, 1, 64, 64, 4, 2, 128, 128, f(0.0), 1, -1, 0, None, f(p), rng, None)
+
+    def bwd_d(p, rng):
+        return lib.attn_bwd_dropout(P, P, P, P, P, P, P, P, P, None, 1, 64, 64, 4, 2, 128, 128, f(0.0), 1, -1, 0,
+                                    None, f(p), rng, 1, P, 1 << 20, None)
+
+    for call in (fwd_d, bwd_d):
+        assert call(-0.1, P) == INVALID
+        assert call(1.0, P) == INVALID
+        assert call(float("nan"), P) == INVALID
+        assert call(1.0 - 2.0 ** -18, P) == INVALID   # rounds to t = 65536: everything dropped
+        assert call(0.1, None) == INVALID             # a drop probability needs the rng state
+        assert call(0.1, MIS4) == MISALIGNED

@@ -176,3 +176,21 @@ def test_dropout_central_differences():
             mm = base.copy(); mm[idx] -= eps
             num[idx] = (loss(key, pp) - loss(key, mm)) / (2 * eps)
         np.testing.assert_allclose(g[gkey], num, atol=2e-8, rtol=1e-6, err_msg=gkey)
+
+
+def test_dropout_origin_takes_the_decisions_of_the_bigger_problem():
+    """A slice (batch entry 1, query heads 2..3 with kv head 1) computed on its own with
+    dropout_origin = (1, 2) equals that slice of the whole problem."""
+    s = Shape(2, 20, 20, 4, 2, 8, 8)
+    x = _inp(s, 45)
+    kw = dict(causal=True, softmax_type=VANILLA, scale=0.5, dropout_p=0.5, rng_state=(3, 4))
+    f = oracle.attention_fwd(x["q"], x["k"], x["v"], **kw)
+    g = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dout"], **kw)
+    sl = lambda a, hs: a[1:2, :, hs].copy()
+    fu = oracle.attention_fwd(sl(x["q"], slice(2, 4)), sl(x["k"], slice(1, 2)), sl(x["v"], slice(1, 2)),
+                              dropout_origin=(1, 2), **kw)
+    gu = oracle.attention_bwd(sl(x["q"], slice(2, 4)), sl(x["k"], slice(1, 2)), sl(x["v"], slice(1, 2)),
+                              sl(x["dout"], slice(2, 4)), dropout_origin=(1, 2), **kw)
+    np.testing.assert_array_equal(fu["o"], f["o"][1:2, :, 2:4])
+    np.testing.assert_array_equal(gu["dq"], g["dq"][1:2, :, 2:4])
+    np.testing.assert_allclose(gu["dk"], g["dk"][1:2, :, 1:2], atol=1e-14)
