@@ -243,8 +243,12 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
  *   atomics, so with a broadcast bias (bias_B = 1 < B or bias_H = 1 < H_q) dbias is
  *   not bitwise reproducible and deterministic != 0 is rejected
  *   (ATTN_ERR_UNSUPPORTED).  Same workspace as attn_bwd.
- * Supported: full-length batches with d_qk = d_v in {64, 128}; other head dims
- * return ATTN_ERR_UNSUPPORTED.
+ * attn_fwd_varlen_bias / attn_bwd_varlen_bias: the same on a padded batch (per-entry
+ *   lengths as for attn_fwd_varlen).  The bias keeps the padded shape [bias_B, bias_H,
+ *   S_q, S_kv]; entry b uses the top-left [Lq[b], Lkv[b]] corner of its planes, and dbias
+ *   is zero outside those corners.
+ * Supported head dims: (d_qk, d_v) in {(64, 64), (128, 128), (192, 128)}; others return
+ * ATTN_ERR_UNSUPPORTED.
  */
 int attn_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, const void* bias, int bias_B,
                   int bias_H, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale, int causal,
@@ -254,6 +258,16 @@ int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
                   float* dbias, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v, float scale,
                   int causal, int window, int softmax_type, const float* softmax_offset, int deterministic,
                   void* workspace, size_t workspace_bytes, void* stream);
+int attn_fwd_varlen_bias(const void* q, const void* k, const void* v, void* o, float* lse, const void* bias,
+                         int bias_B, int bias_H, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v,
+                         float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+                         const int* seq_lens_q, const int* seq_lens_kv, void* stream);
+int attn_bwd_varlen_bias(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, float* d_offset, const void* bias, int bias_B,
+                         int bias_H, float* dbias, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v,
+                         float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+                         const int* seq_lens_q, const int* seq_lens_kv, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * FP8 (E4M3) forward.  Source: "Speed up attention on GPU with cuDNN and

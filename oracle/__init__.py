@@ -222,12 +222,22 @@ def _sink_logit(softmax_type, off, h):
     return -np.inf
 
 
+def _entry_bias(bias, b, lq, lkv):
+    """The bias planes entry b of a padded batch sees, cropped to its own rows and keys."""
+    if bias is None:
+        return None
+    bias = np.asarray(bias)
+    return bias[(b if bias.shape[0] > 1 else 0):][:1, :, :lq, :lkv]
+
+
 def attention_fwd_varlen(q, k, v, *, seq_lens_q=None, seq_lens_kv=None, causal=True, window=-1,
-                         softmax_type=VANILLA, offset=None, scale=None):
+                         softmax_type=VANILLA, offset=None, scale=None, bias=None):
     """Padded batch: entry b holds its Lq[b] queries and Lkv[b] keys at the front of
     its rows.  Its result is attention_fwd on those rows alone; a padded query row
     sees no key, so O = 0, LSE = the sink logit c (-inf for vanilla), p_sink = 1
     with a sink (0 without) and rowsum = 0.  Lengths are clamped to [0, S].
+    bias: optional [Bb, Hb, S_q, S_kv] over the padded shape; an entry uses the top-left
+    [Lq, Lkv] corner of its planes.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, Hq, dqk = q.shape
@@ -246,7 +256,8 @@ def attention_fwd_varlen(q, k, v, *, seq_lens_q=None, seq_lens_kv=None, causal=T
         if Lq[b] == 0 or Lkv[b] == 0:
             continue  # every row of the entry sees no key
         r = attention_fwd(q[b:b + 1, :Lq[b]], k[b:b + 1, :Lkv[b]], v[b:b + 1, :Lkv[b]], causal=causal,
-                          window=window, softmax_type=softmax_type, offset=offset, scale=scale)
+                          window=window, softmax_type=softmax_type, offset=offset, scale=scale,
+                          bias=_entry_bias(bias, b, Lq[b], Lkv[b]))
         o[b, :Lq[b]] = r["o"][0]
         lse[b, :, :Lq[b]] = r["lse"][0]
         psink[b, :, :Lq[b]] = r["psink"][0]
@@ -255,10 +266,11 @@ def attention_fwd_varlen(q, k, v, *, seq_lens_q=None, seq_lens_kv=None, causal=T
 
 
 def attention_bwd_varlen(q, k, v, dout, *, seq_lens_q=None, seq_lens_kv=None, causal=True, window=-1,
-                         softmax_type=VANILLA, offset=None, scale=None):
+                         softmax_type=VANILLA, offset=None, scale=None, bias=None):
     """Gradients for attention_fwd_varlen: padded query rows and padded keys get zero
     gradients (dO of a padded row is ignored), and d_offset sums the valid rows of
-    every entry."""
+    every entry.  With a bias, also dbias (the bias's shape): each entry's dS added into
+    the corner of its planes, zero elsewhere."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Sq, Hq, dqk = q.shape
     _, Skv, Hkv, dv = v.shape
@@ -266,14 +278,21 @@ def attention_bwd_varlen(q, k, v, dout, *, seq_lens_q=None, seq_lens_kv=None, ca
     dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     doff = np.zeros(Hq)
     D = np.zeros((B, Hq, Sq))
+    dbias = None if bias is None else np.zeros(np.asarray(bias).shape)
     for b in range(B):
         if Lq[b] == 0 or Lkv[b] == 0:
             continue  # O = 0 on every row of the entry: nothing flows back
         r = attention_bwd(q[b:b + 1, :Lq[b]], k[b:b + 1, :Lkv[b]], v[b:b + 1, :Lkv[b]], dout[b:b + 1, :Lq[b]],
-                          causal=causal, window=window, softmax_type=softmax_type, offset=offset, scale=scale)
+                          causal=causal, window=window, softmax_type=softmax_type, offset=offset, scale=scale,
+                          bias=_entry_bias(bias, b, Lq[b], Lkv[b]))
         dq[b, :Lq[b]] = r["dq"][0]
         dk[b, :Lkv[b]] = r["dk"][0]
         dvv[b, :Lkv[b]] = r["dv"][0]
         D[b, :, :Lq[b]] = r["D"][0]
         doff += r["d_offset"]
-    return {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}
+        if dbias is not None:
+            dbias[(b if dbias.shape[0] > 1 else 0), :, :Lq[b], :Lkv[b]] += r["dbias"][0]
+    out = {"dq": dq, "dk": dk, "dv": dvv, "d_offset": doff, "D": D}
+    if dbias is not None:
+        out["dbias"] = dbias
+    return out

@@ -90,6 +90,12 @@ def _load():
     lib.attn_fp8_vt_row_bytes.restype = i
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp, vp]
     lib.attn_fwd_fp8.restype = i
+    lib.attn_fwd_varlen_bias.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, vp, vp,
+                                         vp]
+    lib.attn_fwd_varlen_bias.restype = i
+    lib.attn_bwd_varlen_bias.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, i, i, i, i, i, i, i, f,
+                                         i, i, i, vp, vp, vp, i, vp, sz, vp]
+    lib.attn_bwd_varlen_bias.restype = i
     lib.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, f, vp, vp]
     lib.attn_fwd_dropout.restype = i
     lib.attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, f,
@@ -207,10 +213,12 @@ def attn_fwd(q, k, v, o, lse, *, causal=True, window=-1, softmax_type=VANILLA, s
         _check_rng(rng_state)
         st = _load().attn_fwd_dropout(*args, float(dropout_p), _ptr(rng_state), _stream(stream))
     elif bias is not None:
-        if seq_lens_q is not None or seq_lens_kv is not None:
-            raise ValueError("bias with padded batches is not supported")
         Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
-        st = _load().attn_fwd_bias(*args[:5], _ptr(bias), Bb, Hb, *args[5:], _stream(stream))
+        if seq_lens_q is None and seq_lens_kv is None:
+            st = _load().attn_fwd_bias(*args[:5], _ptr(bias), Bb, Hb, *args[5:], _stream(stream))
+        else:
+            st = _load().attn_fwd_varlen_bias(*args[:5], _ptr(bias), Bb, Hb, *args[5:], _ptr(seq_lens_q),
+                                              _ptr(seq_lens_kv), _stream(stream))
     elif seq_lens_q is None and seq_lens_kv is None:
         st = _load().attn_fwd(*args, _stream(stream))
     else:
@@ -253,14 +261,16 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset=None, *, causal=True, w
         _check_rng(rng_state)
         st = _load().attn_bwd_dropout(*args, float(dropout_p), _ptr(rng_state), *tail)
     elif bias is not None:
-        if seq_lens_q is not None or seq_lens_kv is not None:
-            raise ValueError("bias with padded batches is not supported")
         Bb, Hb = _check_bias(bias, B, H_q, S_q, S_kv)
         if dbias is not None:
             _check(dbias, "dbias", torch.float32, 4)
             if dbias.shape != bias.shape:
                 raise ValueError("dbias must have the bias's shape")
-        st = _load().attn_bwd_bias(*args[:10], _ptr(bias), Bb, Hb, _ptr(dbias), *args[10:], *tail)
+        if seq_lens_q is None and seq_lens_kv is None:
+            st = _load().attn_bwd_bias(*args[:10], _ptr(bias), Bb, Hb, _ptr(dbias), *args[10:], *tail)
+        else:
+            st = _load().attn_bwd_varlen_bias(*args[:10], _ptr(bias), Bb, Hb, _ptr(dbias), *args[10:],
+                                              _ptr(seq_lens_q), _ptr(seq_lens_kv), *tail)
     elif seq_lens_q is None and seq_lens_kv is None:
         st = _load().attn_bwd(*args, *tail)
     else:
@@ -308,6 +318,19 @@ def attn_fwd_varlen(q, k, v, o, lse, seq_lens_q, seq_lens_kv, **kw):
 def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q, seq_lens_kv, **kw):
     """attn_bwd on a padded batch (lengths as for attn_fwd_varlen)."""
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, **kw)
+
+
+def attn_fwd_varlen_bias(q, k, v, o, lse, bias, seq_lens_q, seq_lens_kv, **kw):
+    """attn_fwd with an additive bias on a padded batch (entry b uses the top-left
+    [Lq[b], Lkv[b]] corner of its bias planes)."""
+    attn_fwd(q, k, v, o, lse, bias=bias, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, **kw)
+
+
+def attn_bwd_varlen_bias(q, k, v, o, dout, lse, dq, dk, dv, d_offset, bias, dbias, seq_lens_q, seq_lens_kv, **kw):
+    """attn_bwd with an additive bias on a padded batch; dbias is zero outside each
+    entry's corner."""
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, d_offset, bias=bias, dbias=dbias, seq_lens_q=seq_lens_q,
+             seq_lens_kv=seq_lens_kv, **kw)
 
 
 def attn_fwd_dropout(q, k, v, o, lse, dropout_p, rng_state, **kw):

@@ -220,7 +220,7 @@ int attn_last_device_error(void* stream, int* site) {
 static int check_bias(const void* bias, int bias_B, int bias_H, int B, int H_q, int d_qk, int d_v, long long* sb,
                       long long* sh, int S_q, int S_kv) {
   if (!bias || (bias_B != 1 && bias_B != B) || (bias_H != 1 && bias_H != H_q)) return ATTN_ERR_INVALID_ARG;
-  if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!((d_qk == d_v && (d_qk == 64 || d_qk == 128)) || (d_qk == 192 && d_v == 128))) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(bias)) return ATTN_ERR_MISALIGNED;
   *sh = bias_H == 1 ? 0 : (long long)S_q * S_kv;
   *sb = bias_B == 1 ? 0 : (long long)bias_H * S_q * S_kv;
@@ -300,6 +300,15 @@ int attn_fwd_bias(const void* q, const void* k, const void* v, void* o, float* l
   if (!bias) return ATTN_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
                   softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, stream);
+}
+
+int attn_fwd_varlen_bias(const void* q, const void* k, const void* v, void* o, float* lse, const void* bias,
+                         int bias_B, int bias_H, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v,
+                         float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+                         const int* seq_lens_q, const int* seq_lens_kv, void* stream) {
+  if (!bias) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal, window, softmax_type,
+                  softmax_offset, seq_lens_q, seq_lens_kv, bias, bias_B, bias_H, stream);
 }
 
 int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q, int S_kv,
@@ -484,6 +493,18 @@ int attn_bwd_bias(const void* q, const void* k, const void* v, const void* o, co
   if (!bias) return ATTN_ERR_INVALID_ARG;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
                   window, softmax_type, softmax_offset, nullptr, nullptr, bias, bias_B, bias_H, dbias,
+                  deterministic, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_varlen_bias(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, float* d_offset, const void* bias, int bias_B,
+                         int bias_H, float* dbias, int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_v,
+                         float scale, int causal, int window, int softmax_type, const float* softmax_offset,
+                         const int* seq_lens_q, const int* seq_lens_kv, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!bias) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, d_offset, B, S_q, S_kv, H_q, H_kv, d_qk, d_v, scale, causal,
+                  window, softmax_type, softmax_offset, seq_lens_q, seq_lens_kv, bias, bias_B, bias_H, dbias,
                   deterministic, workspace, workspace_bytes, stream);
 }
 

@@ -136,6 +136,7 @@ bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return (d_qk == 128 || d_qk =
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
                   cudaStream_t stream) {
+  if (p.bias) return launch_bwd_kv_bias(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fuse_dq, stream);
   if (fuse_dq) {
     if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
     if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
@@ -154,6 +155,7 @@ int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& t
 
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  if (p.bias) return launch_bwd_q_bias(d_qk, d_v, tq, tk, tv, tdo, p, stream);
   if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128>(tq, tk, tv, tdo, p, stream);
   if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64>(tq, tk, tv, tdo, p, stream);
   if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128>(tq, tk, tv, tdo, p, stream);

@@ -519,26 +519,26 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   }
 }
 
-template <int D_QK, int D_V, bool FUSE, bool DROP = false>
+// Which instantiation family a launcher picks: the plain kernels (full-length or
+// padded batches), the bias ones (full-length or padded), or the dropout ones
+// (full-length).  Each family is instantiated by its own translation unit.
+enum class KernVariant { kPlain, kBias, kDrop };
+
+template <int D_QK, int D_V, bool FUSE, KernVariant KV = KernVariant::kPlain>
 inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using C = KvCfg<D_QK, D_V, FUSE>;
+  const bool vl = p.seq_q || p.seq_kv;  // padded batches: per-entry lengths and row tests
   decltype(&attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>) kern;
-  if constexpr (DROP) {  // dropout: full-length batches without a bias
-    if (p.seq_q || p.seq_kv || p.bias) return -2;
+  if constexpr (KV == KernVariant::kDrop) {  // dropout: full-length batches without a bias
+    if (vl || p.bias) return -2;
     kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, false, true>;
+  } else if constexpr (KV == KernVariant::kBias) {
+    if (!p.bias) return -2;
+    kern = vl ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true, true> : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, true>;
   } else {
-    // padded batches get the instantiation with the per-entry lengths and row tests
-    kern = (p.seq_q || p.seq_kv) ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true>
-                                 : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
-    if (p.bias) {  // bias instantiations: full-length batches, d_qk = d_v in {64, 128}
-      if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
-        if (p.seq_q || p.seq_kv) return -2;
-        kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, true>;
-      } else {
-        return -2;
-      }
-    }
+    if (p.bias) return -2;
+    kern = vl ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true> : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
   }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
@@ -890,25 +890,21 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D_QK, int D_V, bool DROP = false>
+template <int D_QK, int D_V, KernVariant KV = KernVariant::kPlain>
 inline int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const BwdParams& p, cudaStream_t stream) {
   using C = QCfg<D_QK, D_V>;
+  const bool vl = p.seq_q || p.seq_kv;  // padded batches: per-entry lengths and row tests
   decltype(&attn_bwd_q_kernel<D_QK, D_V, false>) kern;
-  if constexpr (DROP) {  // dropout: full-length batches without a bias
-    if (p.seq_q || p.seq_kv || p.bias) return -2;
+  if constexpr (KV == KernVariant::kDrop) {  // dropout: full-length batches without a bias
+    if (vl || p.bias) return -2;
     kern = attn_bwd_q_kernel<D_QK, D_V, false, false, true>;
+  } else if constexpr (KV == KernVariant::kBias) {
+    if (!p.bias) return -2;
+    kern = vl ? attn_bwd_q_kernel<D_QK, D_V, true, true> : attn_bwd_q_kernel<D_QK, D_V, false, true>;
   } else {
-    // padded batches get the instantiation with the per-entry lengths and row tests
-    kern = (p.seq_q || p.seq_kv) ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
-    if (p.bias) {
-      if constexpr ((D_QK == 128 || D_QK == 64) && D_V == D_QK) {
-        if (p.seq_q || p.seq_kv) return -2;
-        kern = attn_bwd_q_kernel<D_QK, D_V, false, true>;
-      } else {
-        return -2;
-      }
-    }
+    if (p.bias) return -2;
+    kern = vl ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
   }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;

@@ -21,21 +21,21 @@ int launch_bwd_kv_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtens
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
                           cudaStream_t stream) {
   if (fuse_dq) {
-    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, true>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, true>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
     return -2;
   }
-  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, true>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, true>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, true>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
   return -2;
 }
 
 int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-  if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128, true>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64, true>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128, true>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
   return -2;
 }
 

@@ -18,12 +18,7 @@ static int launch_attn_fwd_vl(int d_qk, int d_v, const CUtensorMap& tq, const CU
 
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                     const FwdParams& p, cudaStream_t stream) {
-  if (p.bias) {  // bias instantiations: full-length batches, d_qk = d_v in {64, 128}
-    if (p.seq_q || p.seq_kv) return -2;
-    if (d_qk == 128 && d_v == 128) return launch_fwd_t<128, 128, 2, 2, false, false, true>(tq, tk, tv, p, stream);
-    if (d_qk == 64 && d_v == 64) return launch_fwd_t<64, 64, 4, 4, false, false, true>(tq, tk, tv, p, stream);
-    return -2;
-  }
+  if (p.bias) return launch_attn_fwd_bias(d_qk, d_v, tq, tk, tv, p, stream);  // attn_bias.cu
   // padded batches get the instantiation with the per-entry lengths and row tests
   return (p.seq_q || p.seq_kv) ? launch_attn_fwd_vl<true>(d_qk, d_v, tq, tk, tv, p, stream)
                                : launch_attn_fwd_vl<false>(d_qk, d_v, tq, tk, tv, p, stream);

@@ -98,6 +98,16 @@ int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
 
+// Bias instantiations (full-length or padded batches, bf16; (d_qk, d_v) in {(64, 64),
+// (128, 128), (192, 128)}; the fused dQ for 64 and 128): the same contracts as above.
+int launch_attn_fwd_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t stream);
+int launch_bwd_kv_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
+                       cudaStream_t stream);
+int launch_bwd_q_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+
 // Dropout instantiations (full-length batches, bf16, no bias; (d_qk, d_v) in
 // {(64, 64), (128, 128), (192, 128)}): the same contracts as the launchers above.
 int launch_attn_fwd_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -149,7 +149,8 @@ def test_bias_argument_validation(lib):
 
     assert fb(bias=None) == INVALID
     assert fb(Bb=3) == INVALID and fb(Hb=2) == INVALID   # broadcast dims are 1 or the full size
-    assert fb(d=192, dv=128) == UNSUPPORTED              # bias kernels: d_qk = d_v in {64, 128}
+    assert fb(d=128, dv=64) == UNSUPPORTED               # bias kernels: (64, 64), (128, 128), (192, 128)
+    assert fb(d=192, dv=64) == UNSUPPORTED
     assert fb(bias=MIS) == MISALIGNED
     assert fb(B=0, Bb=1) == OK
 

@@ -19,12 +19,15 @@ def _sdpa():
     return sdpa
 
 
-def _run(x, bias, *, causal, window, st, scale, deterministic):
+def _run(x, bias, *, causal, window, st, scale, deterministic, lens=None):
     sdpa = _sdpa()
     dev = torch.device("cuda")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     off = x["offset"].to(dev) if st == LEARNABLE else None
     kw = dict(causal=causal, window=window, softmax_type=st, softmax_offset=off, scale=scale or 0.0)
+    if lens is not None:
+        kw.update(seq_lens_q=torch.tensor(lens[0], dtype=torch.int32, device=dev),
+                  seq_lens_kv=torch.tensor(lens[1], dtype=torch.int32, device=dev))
     bg = bias.to(dev)
     o, lse = sdpa.sdpa_forward(q, k, v, bias=bg, **kw)
     dq, dk, dv, d_off, dbias = sdpa.sdpa_backward(q, k, v, o, do, lse, bias=bg, deterministic=deterministic, **kw)
@@ -37,12 +40,17 @@ def _run(x, bias, *, causal, window, st, scale, deterministic):
     return {n: t.float().cpu().numpy() for n, t in out.items()}
 
 
-def _ref(x, bias, *, causal, window, st, scale):
+def _ref(x, bias, *, causal, window, st, scale, lens=None):
     xd = {n: t.double().numpy() for n, t in x.items()}
     kw = dict(causal=causal, window=window, softmax_type=st, scale=scale, bias=bias.double().numpy(),
               offset=xd["offset"] if st == LEARNABLE else None)
-    f = oracle.attention_fwd(xd["q"], xd["k"], xd["v"], **kw)
-    g = oracle.attention_bwd(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
+    if lens is None:
+        f = oracle.attention_fwd(xd["q"], xd["k"], xd["v"], **kw)
+        g = oracle.attention_bwd(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
+    else:
+        kw.update(seq_lens_q=lens[0], seq_lens_kv=lens[1])
+        f = oracle.attention_fwd_varlen(xd["q"], xd["k"], xd["v"], **kw)
+        g = oracle.attention_bwd_varlen(xd["q"], xd["k"], xd["v"], xd["dout"], **kw)
     out = {"o": f["o"], "lse": f["lse"], "dq": g["dq"], "dk": g["dk"], "dv": g["dv"], "dbias": g["dbias"]}
     if st == LEARNABLE:
         out["d_offset"] = g["d_offset"]
@@ -80,6 +88,10 @@ CASES = [
     ("mqa_head_splits_full_broadcast", Shape(1, 300, 300, 8, 1, 128, 128), True, -1, VANILLA, None, (1, 1), False,
      "stated"),
     ("ragged_det_d64", Shape(1, 77, 77, 2, 2, 64, 64), True, 10, LEARNABLE, None, (1, 2), True, "stated"),
+    # MLA head dims (192 / 128): the query-stationary dQ path
+    ("mla_learnable", Shape(1, 257, 257, 2, 2, 192, 128), True, -1, LEARNABLE, 1 / np.sqrt(192), (1, 2), False,
+     "stated"),
+    ("mla_window_per_bh_det", Shape(2, 200, 200, 4, 2, 192, 128), True, 70, VANILLA, None, (2, 4), True, "stated"),
 ]
 
 
@@ -98,6 +110,35 @@ def test_bias_parity(case):
         again = _run(x, bias, deterministic=det, **kw)
         for n in gpu:
             assert np.array_equal(gpu[n], again[n]), n
+
+
+# Padded batches with a bias: entry b uses the top-left [Lq[b], Lkv[b]] corner of its bias
+# planes; dbias is zero outside the corners.
+VARLEN = [
+    # name, shape, causal, window, softmax type, (lens_q, lens_kv), bias (Bb, Hb), deterministic
+    ("gqa_batch_broadcast", Shape(3, 300, 300, 4, 2, 128, 128), True, -1, VANILLA,
+     ([300, 129, 0], [300, 129, 0]), (1, 4), False),
+    ("d64_learnable_head_broadcast", Shape(2, 260, 260, 4, 1, 64, 64), True, 90, LEARNABLE,
+     ([200, 260], [200, 260]), (2, 1), False),
+    ("d64_per_bh_det", Shape(2, 260, 260, 4, 1, 64, 64), True, -1, OFF_BY_ONE, ([260, 131], [260, 131]), (2, 4),
+     True),
+    ("noncausal_unequal_lengths", Shape(2, 200, 333, 2, 2, 128, 128), False, -1, OFF_BY_ONE, ([150, 200], [333, 64]),
+     (2, 2), False),
+    ("mla_varlen", Shape(2, 257, 257, 2, 2, 192, 128), True, -1, VANILLA, ([257, 100], [257, 100]), (1, 2), False),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[c[0] for c in VARLEN])
+def test_bias_with_padded_batches(case):
+    name, shape, causal, window, st, lens, (Bb, Hb), det = case
+    x = make_inputs(shape, 700 + len(name), learnable_offset=(st == LEARNABLE))
+    bias = make_bias((Bb, Hb, shape.S_q, shape.S_kv), 800 + len(name))
+    kw = dict(causal=causal, window=window, st=st, scale=None)
+    gpu = _run(x, bias, deterministic=det, lens=lens, **kw)
+    ref = _ref(x, bias, lens=lens, **kw)
+    for b in range(shape.B):  # padded query rows: O = 0 (the sink logit as LSE)
+        assert np.all(gpu["o"][b, lens[0][b]:] == 0)
+    _compare(gpu, ref, name)
 
 
 def test_minus_inf_bias_masks_keys_and_whole_rows():
@@ -137,10 +178,9 @@ def test_bias_rejections():
     o, lse = sdpa.sdpa_forward(q, k, v, bias=b)
     with pytest.raises(sdpa.AttnError, match="unsupported"):   # broadcast dbias + deterministic
         sdpa.sdpa_backward(q, k, v, o, do, lse, bias=b, deterministic=True)
-    q3 = torch.zeros((2, 64, 4, 192), dtype=torch.bfloat16, device="cuda")
-    k3 = torch.zeros((2, 64, 2, 192), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(sdpa.AttnError, match="unsupported"):   # MLA dims have no bias kernel
-        sdpa.sdpa_forward(q3, k3, v, bias=b)
+    v64 = torch.zeros((2, 64, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sdpa.AttnError, match="unsupported"):   # (128, 64) has no bias kernel
+        sdpa.sdpa_forward(q, k, v64, bias=b)
 
 
 def test_bias_full_size_sampled():

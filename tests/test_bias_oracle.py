@@ -115,3 +115,61 @@ def test_zero_bias_and_minus_inf_bias_special_cases():
     np.testing.assert_allclose(r["lse"], plain["lse"] + np.arange(S)[None, None], rtol=0, atol=1e-12)
     gr = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=True, window=4, bias=rowc)
     np.testing.assert_allclose(gr["dbias"].sum(axis=3), 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("st,causal,window,bias_bh", [(VANILLA, True, -1, (1, 4)), (LEARNABLE, True, 3, (2, 1)),
+                                                      (OFF_BY_ONE, False, -1, (2, 4))])
+def test_bias_with_padded_batches_matches_torch(st, causal, window, bias_bh):
+    """A padded batch with a bias: each entry uses the top-left [Lq, Lkv] corner of its
+    bias planes.  Torch gets the full padded tensors with the padding masked, the bias
+    in the additive mask, and dO = 0 on padded rows (a padded row keeps key 0 so that
+    its softmax is defined; it adds nothing); dbias comes from autograd and is zero
+    outside each entry's corner."""
+    B, S, Hq, Hkv, d = 2, 10, 4, 2, 8
+    lq, lkv = [7, 10], [10, 6] if not causal else [7, 10]
+    x = _inputs(B, S, S, Hq, Hkv, d, 11, st, (*bias_bh, S, S))
+    for b in range(B):
+        x["dout"][b, lq[b]:] = 0.0
+    kw = dict(causal=causal, window=window, softmax_type=st, scale=0.4, bias=x["bias"],
+              offset=x["offset"] if st == LEARNABLE else None, seq_lens_q=lq, seq_lens_kv=lkv)
+    f = oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], **kw)
+    g = oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dout"], **kw)
+    # torch: the padding as -inf in the additive mask, through a bias of the padded shape
+    pad = np.zeros((B, 1, S, S))
+    for b in range(B):
+        pad[b, :, :, lkv[b]:] = -np.inf
+        pad[b, :, lq[b]:, :] = -np.inf
+        pad[b, :, lq[b]:, 0] = 0.0
+    bias_t = torch.tensor(x["bias"]).requires_grad_(True)
+    q = torch.tensor(x["q"]).permute(0, 2, 1, 3).requires_grad_(True)
+    k = torch.tensor(x["k"]).permute(0, 2, 1, 3).requires_grad_(True)
+    v = torch.tensor(x["v"]).permute(0, 2, 1, 3).requires_grad_(True)
+    G = Hq // Hkv
+    kk, vv = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
+    i, j = torch.arange(S)[:, None], torch.arange(S)[None, :]
+    allowed = torch.ones(S, S, dtype=torch.bool)
+    if causal:
+        allowed &= j <= i
+    if window >= 0:
+        allowed &= j >= i - window
+    mask = (bias_t.expand(B, Hq, S, S) + torch.tensor(pad)
+            + torch.zeros(S, S, dtype=torch.float64).masked_fill(~allowed, float("-inf")))
+    for b in range(B):  # a padded row keeps key 0 whatever the causal mask says
+        mask = mask.clone()
+        mask[b, :, lq[b]:, 0] = bias_t.expand(B, Hq, S, S)[b, :, lq[b]:, 0]
+    if st != VANILLA:
+        kk = torch.cat([kk, torch.zeros(B, Hq, 1, d, dtype=torch.float64)], dim=2)
+        vv = torch.cat([vv, torch.zeros(B, Hq, 1, d, dtype=torch.float64)], dim=2)
+        c = torch.tensor(x["offset"]) if st == LEARNABLE else torch.zeros(Hq, dtype=torch.float64)
+        mask = torch.cat([mask, c[None, :, None, None].expand(B, Hq, S, 1)], dim=3)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask, scale=0.4)
+    (o * torch.tensor(x["dout"]).permute(0, 2, 1, 3)).sum().backward()
+    o = o.detach().permute(0, 2, 1, 3).numpy()
+    for b in range(B):
+        np.testing.assert_allclose(f["o"][b, :lq[b]], o[b, :lq[b]], rtol=0, atol=1e-12)
+        assert np.all(f["o"][b, lq[b]:] == 0)
+    np.testing.assert_allclose(g["dq"], q.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g["dk"], k.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g["dv"], v.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g["dbias"], bias_t.grad.numpy(), rtol=0, atol=1e-11)
+    assert g["dbias"].shape == x["bias"].shape
