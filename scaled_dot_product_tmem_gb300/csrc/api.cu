@@ -438,9 +438,17 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     set_error("cuTensorMapEncodeTiled (dQ accumulator)");
     return ATTN_ERR_CUDA;
   }
+  // the kv kernel stages its bias tiles (64 query rows x 128 keys) by TMA when the rows
+  // are a multiple of 16 bytes long; otherwise each thread loads its key's column itself
+  CUtensorMap tb = tq;
+  p.bias_tma = bias && S_kv % 8 == 0 ? 1 : 0;
+  if (p.bias_tma && !sdpa::make_bias_map(&tb, bias, bias_B, bias_H, S_q, S_kv, bq_rows, 128)) {
+    set_error("cuTensorMapEncodeTiled (bias)");
+    return ATTN_ERR_CUDA;
+  }
   int rc = timed(ATTN_KERNEL_BWD_KV, 1, s, [&] {
-    return p.drop_t ? sdpa::launch_bwd_kv_dropout(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s)
-                    : sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fused, s);
+    return p.drop_t ? sdpa::launch_bwd_kv_dropout(d_qk, d_v, tq, tk, tv, tdo, tdq, tb, p, fused, s)
+                    : sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, tb, p, fused, s);
   });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {

@@ -23,17 +23,17 @@ int launch_attn_fwd_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtenso
 }
 
 int launch_bwd_kv_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                       bool fuse_dq, cudaStream_t stream) {
   constexpr KernVariant B = KernVariant::kBias;
   if (fuse_dq) {
-    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, B>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, B>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, B>(tq, tk, tv, tdo, tdq, tb, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, B>(tq, tk, tv, tdo, tdq, tb, p, stream);
     return -2;
   }
-  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, B>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, B>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, B>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, B>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, B>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, B>(tq, tk, tv, tdo, tdq, tb, p, stream);
   return -2;
 }
 

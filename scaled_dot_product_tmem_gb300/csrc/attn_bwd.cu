@@ -134,22 +134,22 @@ int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream) {
 bool bwd_kv_supports_fused_dq(int d_qk, int d_v) { return (d_qk == 128 || d_qk == 64) && (d_v == 128 || d_v == 64); }
 
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                  cudaStream_t stream) {
-  if (p.bias) return launch_bwd_kv_bias(d_qk, d_v, tq, tk, tv, tdo, tdq, p, fuse_dq, stream);
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                  bool fuse_dq, cudaStream_t stream) {
+  if (p.bias) return launch_bwd_kv_bias(d_qk, d_v, tq, tk, tv, tdo, tdq, tb, p, fuse_dq, stream);
   if (fuse_dq) {
-    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, true>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true>(tq, tk, tv, tdo, tdq, tb, p, stream);
+    if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, true>(tq, tk, tv, tdo, tdq, tb, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true>(tq, tk, tv, tdo, tdq, tb, p, stream);
+    if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, true>(tq, tk, tv, tdo, tdq, tb, p, stream);
     return -2;
   }
-  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 128 && d_v == 64) return launch_kv_t<128, 64, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 64 && d_v == 128) return launch_kv_t<64, 128, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 192 && d_v == 64) return launch_kv_t<192, 64, false>(tq, tk, tv, tdo, tdq, tb, p, stream);
   return -2;
 }
 

@@ -38,14 +38,16 @@ namespace sdpa {
 // =============================================================================
 // kv-stationary main kernel
 // =============================================================================
-template <int D_QK, int D_V, bool FUSE_DQ>
+template <int D_QK, int D_V, bool FUSE_DQ, bool BIAS = false>
 struct KvCfg {
   static constexpr int BN = 128;  // keys per CTA (TMEM lanes)
   static constexpr int BQ = 64;   // query rows per step
   static constexpr int QCH = D_QK / 64, VCH = D_V / 64;
   static constexpr int KCHUNK = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int QCHUNK = 64 * 128;   // 64 rows x 128 bytes
-  static constexpr int NQ = (D_QK == 64 && D_V == 64) ? 6 : 3;
+  // Q/dO stages; with a bias each stage also holds the step's bias tile, so there are fewer
+  static constexpr int NQ = !BIAS ? ((D_QK == 64 && D_V == 64) ? 6 : 3)
+                                  : ((D_QK == 64 && D_V == 64) ? 4 : ((FUSE_DQ || D_QK == 192) ? 2 : 3));
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + QCH * KCHUNK;
   static constexpr int OFF_DS = OFF_V + VCH * KCHUNK;  // 2 x dS^T [128 keys x 64 q] bf16, swizzled
@@ -57,7 +59,9 @@ struct KvCfg {
   static constexpr int DO_STAGE = VCH * QCHUNK;
   static constexpr int OFF_L = OFF_DO + NQ * DO_STAGE;  // nlse2[64] + D[64] per stage
   static constexpr int L_STAGE = 2 * BQ * 4;
-  static constexpr int OFF_DQS = OFF_L + NQ * L_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
+  static constexpr int OFF_B = OFF_L + NQ * L_STAGE;    // bias tile [64 q][128 keys] bf16 per stage
+  static constexpr int B_STAGE = BIAS ? BQ * BN * 2 : 0;
+  static constexpr int OFF_DQS = OFF_B + NQ * B_STAGE;  // fp32 dQ tile [64 q][d_qk] staged for the TMA reduce
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, dq_ready, dq_free,
@@ -91,8 +95,9 @@ template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false, bool DROP
 __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
-  using C = KvCfg<D_QK, D_V, FUSE_DQ>;
+                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmB,
+                       const BwdParams p) {
+  using C = KvCfg<D_QK, D_V, FUSE_DQ, BIAS>;
   static_assert(!DROP || (!BIAS && !VL), "dropout: full-length batches without a bias");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -168,6 +173,8 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
+      const bool btma = BIAS && p.bias_tma;  // this stage also brings the step's bias tile
+      if (btma) tma_prefetch_desc(&tmB);
       mbar_arrive_expect_tx(kv_full, (C::QCH + C::VCH) * C::KCHUNK);
       for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_K + c * C::KCHUNK, &tmK, kv_full, c * 64, hk, n0, b);
       for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_V + c * C::KCHUNK, &tmV, kv_full, c * 64, hk, n0, b);
@@ -176,7 +183,10 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         if (!mbar_wait(&q_empty[st], ((s / C::NQ) & 1) ^ 1, err, kKvQEmpty)) break;
         const int h = h0 + s / nq;
         const int q0 = (ilo + s % nq) * C::BQ;
-        mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE);
+        mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE + (btma ? C::B_STAGE : 0));
+        if (btma)  // rows past S_q and keys past S_kv come in as zeros
+          tma_load_4d(smem + C::OFF_B + st * C::B_STAGE, &tmB, &q_full[st], n0, q0, p.bias_sh ? h : 0,
+                      p.bias_sb ? b : 0);
         for (int c = 0; c < C::QCH; ++c)
           tma_load_4d(smem + C::OFF_Q + st * C::Q_STAGE + c * C::QCHUNK, &tmQ, &q_full[st], c * 64, h, q0, b);
         for (int c = 0; c < C::VCH; ++c)
@@ -322,12 +332,19 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
         if constexpr (BIAS) {  // + bias * log2(e) (queries past S_q read 0; their P is 0)
-          const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
+          if (p.bias_tma) {  // this thread's key column of the staged tile [64 q][128 keys]
+            const unsigned short* bt =
+                reinterpret_cast<const unsigned short*>(smem + C::OFF_B + st * C::B_STAGE) + 32 * w * C::BN + r;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int qq = q0 + 32 * w + c;
-            const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
-            lv[c] = fmaf(bv, kLog2e, lv[c]);
+            for (int c = 0; c < 32; ++c) lv[c] = fmaf(bf16_bits_to_float(bt[c * C::BN]), kLog2e, lv[c]);
+          } else {
+            const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int qq = q0 + 32 * w + c;
+              const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
+              lv[c] = fmaf(bv, kLog2e, lv[c]);
+            }
           }
         }
         tmem_ld_wait();
@@ -526,8 +543,8 @@ enum class KernVariant { kPlain, kBias, kDrop };
 
 template <int D_QK, int D_V, bool FUSE, KernVariant KV = KernVariant::kPlain>
 inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
-  using C = KvCfg<D_QK, D_V, FUSE>;
+                       const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p, cudaStream_t stream) {
+  using C = KvCfg<D_QK, D_V, FUSE, KV == KernVariant::kBias>;
   const bool vl = p.seq_q || p.seq_kv;  // padded batches: per-entry lengths and row tests
   decltype(&attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>) kern;
   if constexpr (KV == KernVariant::kDrop) {  // dropout: full-length batches without a bias
@@ -543,7 +560,7 @@ inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
   const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tb, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

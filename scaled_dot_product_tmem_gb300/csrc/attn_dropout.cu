@@ -18,24 +18,26 @@ int launch_attn_fwd_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 }
 
 int launch_bwd_kv_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                          bool fuse_dq, cudaStream_t stream) {
+  constexpr KernVariant D = KernVariant::kDrop;
   if (fuse_dq) {
-    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
-    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
+    if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, true, D>(tq, tk, tv, tdo, tdq, tb, p, stream);
+    if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, true, D>(tq, tk, tv, tdo, tdq, tb, p, stream);
     return -2;
   }
-  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, KernVariant::kDrop>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d_qk == 128 && d_v == 128) return launch_kv_t<128, 128, false, D>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_kv_t<64, 64, false, D>(tq, tk, tv, tdo, tdq, tb, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_kv_t<192, 128, false, D>(tq, tk, tv, tdo, tdq, tb, p, stream);
   return -2;
 }
 
 int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-  if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
-  if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128, KernVariant::kDrop>(tq, tk, tv, tdo, p, stream);
+  constexpr KernVariant D = KernVariant::kDrop;
+  if (d_qk == 128 && d_v == 128) return launch_q_t<128, 128, D>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 64 && d_v == 64) return launch_q_t<64, 64, D>(tq, tk, tv, tdo, p, stream);
+  if (d_qk == 192 && d_v == 128) return launch_q_t<192, 128, D>(tq, tk, tv, tdo, p, stream);
   return -2;
 }
 

@@ -76,6 +76,7 @@ struct BwdParams {
   const __nv_bfloat16* bias = nullptr;
   long long bias_sb = 0, bias_sh = 0;
   float* dbias = nullptr;
+  int bias_tma = 0;  // the kv kernel stages its bias tiles by TMA (S_kv % 8 == 0), else loads them itself
   // attention dropout, as in FwdParams (the same rng state regenerates the forward's decisions)
   const unsigned long long* rng = nullptr;
   unsigned drop_t = 0;
@@ -84,9 +85,10 @@ struct BwdParams {
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
 // tdq: fp32 map of dq_acc (box d_qk x 64 rows) when fuse_dq, else any valid map (unused).
+// tb: the bias map (box 128 keys x 64 rows) when p.bias_tma, else any valid map (unused).
 int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                  cudaStream_t stream);
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                  bool fuse_dq, cudaStream_t stream);
 // Query-head splits of the kv kernel for these sizes: a grid of fewer than 3 CTAs
 // per SM (few kv heads, as with MQA) is bound by its longest CTA, so each CTA's
 // head loop is halved until the grid has 6 CTAs per SM; 1 = no split.
@@ -103,8 +105,8 @@ bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
 int launch_attn_fwd_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream);
 int launch_bwd_kv_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                       cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                       bool fuse_dq, cudaStream_t stream);
 int launch_bwd_q_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 
@@ -113,8 +115,8 @@ int launch_bwd_q_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMa
 int launch_attn_fwd_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream);
 int launch_bwd_kv_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool fuse_dq,
-                          cudaStream_t stream);
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
+                          bool fuse_dq, cudaStream_t stream);
 int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 
