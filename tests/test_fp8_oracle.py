@@ -147,3 +147,121 @@ def test_p_rounding_bound_covers_an_emulated_kernel(st):
             assert np.all(err <= bound[0, h] * (1 + 1e-9) + 1e-12)
             worst = max(worst, float((err / bound[0, h]).max()))
     assert worst > 0.3             # and it is tight: some element reaches 30 % of it
+
+
+# ----------------------------------------------------------------------------- E5M2 and the FP8 backward
+
+def test_e5m2_decode_closed_forms_and_torch():
+    d = fp8.e5m2_decode
+    assert d(0x7B) == 57344.0                    # S.11110.11: largest finite
+    assert d(0x01) == 2.0 ** -16                 # smallest subnormal
+    assert d(0x04) == 2.0 ** -14                 # smallest normal
+    assert d(0x3C) == 1.0 and d(0xBC) == -1.0    # exponent field 15 = bias
+    assert d(0x3D) == 1.25 and d(0x3F) == 1.75
+    assert d(0x7C) == np.inf and d(0xFC) == -np.inf
+    assert np.isnan(d(0x7D)) and np.isnan(d(0x7F))
+    codes = np.arange(256, dtype=np.uint8)
+    ours = d(codes)
+    theirs = torch.tensor(codes).view(torch.float8_e5m2).double().numpy()
+    same = (ours == theirs) | (np.isnan(ours) & np.isnan(theirs))
+    assert same.all()
+
+
+def test_e5m2_encode_round_trip_ties_saturation_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = fp8.e5m2_decode(codes)
+    fin = np.isfinite(vals)
+    assert np.array_equal(fp8.e5m2_encode(vals[fin]), codes[fin])
+    e = fp8.e5m2_encode
+    assert e(1.125) == 0x3C                       # tie 1 | 1.25 -> even code 0x3C
+    assert e(1.375) == 0x3E                       # tie 1.25 | 1.5 -> even code 0x3E
+    assert e(70000.0) == 0x7B and e(-1e30) == 0xFB and e(np.inf) == 0x7B   # satfinite
+    assert e(np.nan) == 0x7F
+    x = np.random.default_rng(5).normal(0, 100, 20000) * np.exp2(np.random.default_rng(6).integers(-20, 8, 20000))
+    x = x[np.abs(x) <= 57344.0]
+    theirs = torch.tensor(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(e(x), theirs)
+
+
+def test_e5m2_quantize_properties():
+    x = np.random.default_rng(7).normal(size=(2, 40, 3, 64)).astype(np.float32)
+    codes, amax, descale = fp8.quantize(x, fmt="e5m2")
+    assert amax == np.float32(np.abs(x).max())
+    back = fp8.dequantize(codes, descale, "e5m2")
+    assert np.abs(back).max() == pytest.approx(amax, rel=2 ** -3)
+    rel = np.abs(back - x) / np.maximum(np.abs(x), 2.0 ** -14 * float(descale))
+    assert rel.max() <= 2.0 ** -3 + 1e-6          # half an E5M2 step (2 mantissa bits)
+    t, _, _ = fp8.quantize(x, fmt="e5m2", transpose=True)
+    assert np.array_equal(t, codes.transpose(0, 2, 3, 1))
+
+
+def _fp8_bwd_case(seed, causal=True, window=-1, st=VANILLA, Sq=37, Skv=37, Hq=4, Hkv=2, d=16):
+    rng = np.random.default_rng(seed)
+    bf = lambda a: torch.tensor(a, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    q, k, v, do = (bf(rng.normal(size=s)) for s in ((2, Sq, Hq, d), (2, Skv, Hkv, d), (2, Skv, Hkv, d), (2, Sq, Hq, d)))
+    off = rng.normal(size=Hq)
+    q8, _, dq_ = fp8.quantize(q)
+    k8, _, dk_ = fp8.quantize(k)
+    v8, _, dv_ = fp8.quantize(v)
+    do8, _, ddo = fp8.quantize(do, fmt="e5m2")
+    kw = dict(causal=causal, window=window, softmax_type=st, offset=off if st == LEARNABLE else None, scale=0.3)
+    deq = dict(q=fp8.dequantize(q8, dq_), k=fp8.dequantize(k8, dk_), v=fp8.dequantize(v8, dv_),
+               do=fp8.dequantize(do8, ddo, "e5m2"))
+    f = oracle.attention_fwd(deq["q"], deq["k"], deq["v"], **kw)
+    return (q8, k8, v8, do8, dq_, dk_, dv_, ddo), deq, f, kw
+
+
+@pytest.mark.parametrize("st,causal,window", [(VANILLA, True, -1), (LEARNABLE, True, 5), (OFF_BY_ONE, False, -1)])
+def test_fp8_backward_without_roundings_is_the_exact_backward(st, causal, window):
+    """With both roundings off, the FP8 backward's steps are the backward of the
+    dequantised inputs: the C oracle's, computed on its own."""
+    codes, deq, f, kw = _fp8_bwd_case(11, causal, window, st)
+    got = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], 1.0, round_p=False, round_ds=False, **kw)
+    ref = oracle.attention_bwd(deq["q"], deq["k"], deq["v"], deq["do"], **kw)
+    for n in ("dq", "dk", "dv", "d_offset"):
+        np.testing.assert_allclose(got[n], ref[n], rtol=0, atol=1e-10, err_msg=n)
+
+
+def test_fp8_backward_roundings_match_torchs_casts():
+    """The two roundings written with torch's own float8 casts: P as E4M3(256 P) / 256
+    in dV, dS as E5M2(s dS) / s in dK and dQ."""
+    codes, deq, f, kw = _fp8_bwd_case(13, True, -1, VANILLA)
+    stat = 4.0  # covers this step's max |dS| (3.64), so nothing saturates (torch's cast would give inf)
+    got = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], stat, **kw)
+    s = float(np.float32(57344.0) / np.float32(stat))
+    q, k, v, do = (torch.tensor(deq[n]) for n in ("q", "k", "v", "do"))
+    o = torch.tensor(f["o"])
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    mask = torch.tril(torch.ones(Sq, Skv, dtype=torch.bool))
+    dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            S = 0.3 * q[b, :, h] @ k[b, :, g].T
+            P = torch.where(mask, torch.exp(S - torch.tensor(f["lse"][b, h])[:, None]), torch.zeros(()))
+            Pr = (P * 256).to(torch.float8_e4m3fn).double() / 256
+            dP = do[b, :, h] @ v[b, :, g].T
+            D = (do[b, :, h] * o[b, :, h]).sum(1)
+            dS = P * (dP - D[:, None])
+            dSr = (dS * s).to(torch.float8_e5m2).double() / s
+            dv[b, :, g] += Pr.T @ do[b, :, h]
+            dk[b, :, g] += 0.3 * dSr.T @ q[b, :, h]
+            dq[b, :, h] = 0.3 * dSr @ k[b, :, g]
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got[n], t.numpy(), rtol=0, atol=1e-12, err_msg=n)
+    assert got["amax_ds"] < stat
+
+
+def test_fp8_backward_roundings_move_the_gradients_by_their_size():
+    """The roundings are real but bounded: E4M3 P (3 bits) and E5M2 dS (2 bits) move
+    the gradients by at most a few per cent in relative L2, and not at all when off."""
+    codes, deq, f, kw = _fp8_bwd_case(17)
+    exact = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], 1.0, round_p=False, round_ds=False, **kw)
+    amax = exact["amax_ds"]
+    r = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], amax, **kw)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 1e-4 < rel(r["dv"], exact["dv"]) < 2 ** -5
+    for n in ("dq", "dk"):
+        assert 1e-3 < rel(r[n], exact[n]) < 2 ** -3
