@@ -229,13 +229,19 @@ P_SCALE = 256.0  # the fixed power-of-two scale of P in the FP8 backward's dV pr
 
 def attention_bwd_fp8(q8, k8, v8, do8, descale_q, descale_k, descale_v, descale_do, o, lse, ds_amax, *,
                       causal=True, window=-1, softmax_type=VANILLA, offset=None, scale=None,
-                      round_p=True, round_ds=True):
+                      round_p=True, round_ds=True, q_idx=None, k_idx=None):
     """The FP8 backward's steps (module docstring) on BSHD codes: q8, k8, v8 E4M3, do8
     E5M2, all in BSHD; o the forward's output (bf16 values), lse [B,Hq,Sq] its LSE;
     ds_amax the dS scaling statistic (s = 57344 / ds_amax).  round_p / round_ds
     switch the two roundings off (then this is the exact backward of the dequantised
     inputs, with D from the given O).  Returns a dict of float64 dq, dk, dv,
-    d_offset [Hq] and amax_ds = max |dS| (fp64)."""
+    d_offset [Hq] and amax_ds = max |dS| (fp64).
+
+    q_idx / k_idx (sorted absolute positions, default all) restrict the sums to those
+    query rows and keys, the masks still taken at the absolute positions: dq is then
+    [B, len(q_idx), Hq, d] summed over the keys k_idx, dk and dv [B, len(k_idx), Hkv, d]
+    summed over the rows q_idx, d_offset and amax_ds over the rows q_idx.  With
+    k_idx = all keys the dq rows are exact, with q_idx = all rows the dk, dv rows are."""
     q = dequantize(q8, descale_q)
     k = dequantize(k8, descale_k)
     v = dequantize(v8, descale_v)
@@ -245,11 +251,15 @@ def attention_bwd_fp8(q8, k8, v8, do8, descale_q, descale_k, descale_v, descale_
     B, Sq, Hq, dqk = q.shape
     _, Skv, Hkv, dv = v.shape
     G = Hq // Hkv
+    qi = np.arange(Sq) if q_idx is None else np.asarray(q_idx)
+    kj = np.arange(Skv) if k_idx is None else np.asarray(k_idx)
+    q, do, o, lse = q[:, qi], do[:, qi], o[:, qi], lse[:, :, qi]
+    k, v = k[:, kj], v[:, kj]
     sc = (1.0 / np.sqrt(dqk)) if scale is None else float(scale)
     s_ds = np.float64(scale_from_amax(ds_amax, "e5m2"))
-    i = np.arange(Sq)[:, None]
-    j = np.arange(Skv)[None, :]
-    vis = np.ones((Sq, Skv), dtype=bool)
+    i = qi[:, None]
+    j = kj[None, :]
+    vis = np.ones((len(qi), len(kj)), dtype=bool)
     if causal:
         vis &= j <= i
     if window >= 0:

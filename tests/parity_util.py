@@ -162,6 +162,140 @@ def check_d_offset_bound(x, gpu, what, **kw):
     return float(rel_l2(got, exact)), float(rel_l2(got, on_gpu_o))
 
 
+# Accumulation allowance of a tensor-core product of 8-bit operands over n terms: each
+# K = 32 block summed with at least 14 significant bits (an assumed floor: the
+# hardware's internal accumulation width is not documented), the blocks added in fp32.
+def fp8_acc_rel(n):
+    return 2.0 ** -13 + np.ceil(n / 32.0) * 2.0 ** -24
+
+
+def fp8_bwd_bounds(q8, k8, v8, do8, descale_q, descale_k, descale_v, descale_do, o, lse, ds_amax, *, causal,
+                   window, softmax_type, offset, scale, q_idx=None, k_idx=None):
+    """Per-element tolerances of the FP8 backward against oracle.fp8.attention_bwd_fp8
+    (with its roundings on), derived from the kernel's arithmetic.
+
+    Both sides round the same two matrices, P~ = E4M3(2^8 P) / 2^8 and
+    dS~ = E5M2(s dS) / s, and agree exactly wherever the kernel's fp32 value of 2^8 P
+    (or s dS) rounds to the same code as the exact one.  The kernel's value lies in
+    [x - e, x + e] around the exact x, with e from its error model below; rounding is
+    monotone, so its code lies between the codes of x - e and x + e, and the rounded
+    value may move by at most the larger of their distances from round(x) (zero where
+    both ends round alike).  Error model (fp32 unit roundoff 2^-24):
+      S     = scale q.k:  fp8_acc_rel(d) scale sum_d |q k| + 2^-22 |S|  (descale product)
+      exponent (natural units): e_S + 2^-23 (|S| + |LSE|), then ex2: 2^-21 relative,
+            so e_P = P (e_exp + 2^-21) 1.01;
+      dP    = dO.v:  fp8_acc_rel(d) sum_d |dO v| + 2^-22 |dP|;
+      D     = dO.O in fp32 over d terms:  d 2^-24 sum_d |dO O| + 2^-23 |D|;
+      dS    = P (dP - D):  |dP - D| e_P + P (e_dP + e_D) + 2^-23 |dS|.
+    The outputs are sums of the rounded matrices with fp32 tensor-core accumulation
+    over n terms (n = the rows, or keys, of every head summed), then one bf16 rounding
+    (u = 2^-8):
+      dV_jd: t = sum_i gapP_ij |dO_id| + fp8_acc_rel(n) sum_i P~_ij |dO_id|,
+      dK_jd: t = scale (sum_i gapS_ij |q_id| + fp8_acc_rel(n) sum_i |dS~_ij q_id|),
+      dQ_id: t = scale (sum_j gapS_ij |k_jd| + fp8_acc_rel(n) sum_j |dS~_ij k_jd|),
+      tolerance = t + 2^-8 (|exact| + t).
+    amax: max |dS| moves by at most max e_dS.  d_offset_h = -sum_i w_i D_i with
+    w = exp(c - LSE) taken by ex2 in fp32: sum_i w_i (e_D + (2^-21 + 2^-23 (|c| +
+    |LSE|)) |D|) + (n / 256 + 16) 2^-24 sum |w D| (a 256-wide fixed-order sum).
+
+    q_idx / k_idx as in attention_bwd_fp8.  Returns a dict of tolerances shaped like
+    its outputs (dq, dk, dv, d_offset) and amax_ds, plus "flips": the fraction of
+    (P, dS) elements whose code may differ."""
+    from oracle import fp8
+    q = fp8.dequantize(q8, descale_q)
+    k = fp8.dequantize(k8, descale_k)
+    v = fp8.dequantize(v8, descale_v)
+    do = fp8.dequantize(do8, descale_do, "e5m2")
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    B, Sq, Hq, d = q.shape
+    _, Skv, Hkv, _ = v.shape
+    G = Hq // Hkv
+    qi = np.arange(Sq) if q_idx is None else np.asarray(q_idx)
+    kj = np.arange(Skv) if k_idx is None else np.asarray(k_idx)
+    q, do, o, lse = q[:, qi], do[:, qi], o[:, qi], lse[:, :, qi]
+    k, v = k[:, kj], v[:, kj]
+    sc = (1.0 / np.sqrt(d)) if scale is None else float(scale)
+    s_ds = np.float64(fp8.scale_from_amax(ds_amax, "e5m2"))
+    vis = np.ones((len(qi), len(kj)), dtype=bool)
+    if causal:
+        vis &= kj[None, :] <= qi[:, None]
+    if window >= 0:
+        vis &= kj[None, :] >= qi[:, None] - window
+    acc_d = fp8_acc_rel(d)
+    acc_kv = fp8_acc_rel(len(qi) * G)      # dK, dV: every row of the group
+    acc_q = fp8_acc_rel(len(kj))           # dQ: every key
+    r4 = lambda x: fp8.e4m3_decode(fp8.e4m3_encode(x))
+    r5 = lambda x: fp8.e5m2_decode(fp8.e5m2_encode(x))
+    t_dq, t_dk, t_dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    t_doff = np.zeros(Hq)
+    amax_tol = 0.0
+    flips, total = 0, 0
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            L = lse[b, h][:, None]
+            ok = np.isfinite(L)
+            Lf = np.where(ok, L, 0.0)
+            S = sc * q[b, :, h, :] @ k[b, :, g, :].T
+            Sabs = sc * np.abs(q[b, :, h, :]) @ np.abs(k[b, :, g, :]).T
+            m = vis & ok
+            P = np.where(m, np.exp(np.where(m, S, 0.0) - Lf), 0.0)
+            e_exp = acc_d * Sabs + 2.0 ** -22 * np.abs(S) + 2.0 ** -23 * (np.abs(S) + np.abs(Lf))
+            e_P = np.where(m, P * (e_exp + 2.0 ** -21) * 1.01, 0.0)
+            x = P * fp8.P_SCALE
+            ex = e_P * fp8.P_SCALE
+            Pr = r4(x)
+            gapP = np.maximum(np.abs(r4(x + ex) - Pr), np.abs(r4(np.maximum(x - ex, 0.0)) - Pr)) / fp8.P_SCALE
+            dP = do[b, :, h, :] @ v[b, :, g, :].T
+            dPabs = np.abs(do[b, :, h, :]) @ np.abs(v[b, :, g, :]).T
+            D = np.sum(do[b, :, h, :] * o[b, :, h, :], axis=1)
+            Dabs = np.sum(np.abs(do[b, :, h, :] * o[b, :, h, :]), axis=1)
+            e_D = d * 2.0 ** -24 * Dabs + 2.0 ** -23 * np.abs(D)
+            e_dP = acc_d * dPabs + 2.0 ** -22 * np.abs(dP)
+            dS = P * (dP - D[:, None])
+            e_dS = np.where(m, np.abs(dP - D[:, None]) * e_P + P * (e_dP + e_D[:, None]) + 2.0 ** -23 * np.abs(dS),
+                            0.0)
+            amax_tol = max(amax_tol, float(e_dS.max()) if e_dS.size else 0.0)
+            y = dS * s_ds
+            ey = e_dS * s_ds + 2.0 ** -24 * np.abs(y)
+            Sr = r5(y)
+            gapS = np.maximum(np.abs(r5(y + ey) - Sr), np.abs(r5(y - ey) - Sr)) / s_ds
+            Pt = Pr / fp8.P_SCALE
+            dSt = Sr / s_ds
+            flips += int(np.count_nonzero(gapP) + np.count_nonzero(gapS))
+            total += 2 * int(m.sum())
+            ado, aq, ak = np.abs(do[b, :, h, :]), np.abs(q[b, :, h, :]), np.abs(k[b, :, g, :])
+            t_dv[b, :, g, :] += gapP.T @ ado + acc_kv * (Pt.T @ ado)
+            t_dk[b, :, g, :] += sc * (gapS.T @ aq + acc_kv * (np.abs(dSt).T @ aq))
+            t_dq[b, :, h, :] = sc * (gapS @ ak + acc_q * (np.abs(dSt) @ ak))
+            if softmax_type == 2:
+                c = float(np.asarray(offset).reshape(-1)[h])
+                w = np.where(ok[:, 0], np.exp(c - Lf[:, 0]), 0.0)
+                n = B * len(qi)
+                t_doff[h] += float(np.sum(w * (e_D + (2.0 ** -21 + 2.0 ** -23 * (abs(c) + np.abs(Lf[:, 0])))
+                                               * np.abs(D))) + (n / 256 + 16) * 2.0 ** -24 * np.sum(np.abs(w * D)))
+    return {"t_dq": t_dq, "t_dk": t_dk, "t_dv": t_dv, "d_offset": t_doff, "amax_ds": amax_tol,
+            "flips": flips / max(total, 1)}
+
+
+def check_fp8_bwd(got, ref, bounds, what, names=("dq", "dk", "dv")):
+    """Assert |got - exact| <= t + 2^-8 (|exact| + t) per element (fp8_bwd_bounds);
+    return the largest ratio of error to tolerance per output."""
+    ratios = {}
+    for n in names:
+        g = np.asarray(got[n], dtype=np.float64)
+        r = ref[n]
+        t = bounds["t_" + n]
+        tol = t + BF16_U * (np.abs(r) + t)
+        err = np.abs(g - r)
+        bad = err > tol
+        assert not bad.any(), (f"{what}: {n} off at {int(bad.sum())} elements, worst {float((err - tol).max()):.3g} "
+                               f"beyond the bound (first at {np.argwhere(bad)[0].tolist()})")
+        ratios[n] = float((err / np.maximum(tol, 1e-30)).max()) if err.size else 0.0
+    return ratios
+
+
 def slice_group(x, b, g, G):
     """The inputs of one (batch b, kv head g) unit: query heads g*G..g*G+G-1 with kv head g."""
     out = {}
@@ -186,4 +320,5 @@ def gpu_slice(res, b, g, G):
 
 
 __all__ = ["Shape", "make_inputs", "gpu_run", "oracle_run", "compare", "slice_group", "gpu_slice", "rel_l2",
-           "d_offset_bound", "check_d_offset_bound"]
+           "d_offset_bound", "check_d_offset_bound", "fp8_acc_rel",
+           "fp8_bwd_bounds", "check_fp8_bwd"]

@@ -265,3 +265,88 @@ def test_fp8_backward_roundings_move_the_gradients_by_their_size():
     assert 1e-4 < rel(r["dv"], exact["dv"]) < 2 ** -5
     for n in ("dq", "dk"):
         assert 1e-3 < rel(r[n], exact[n]) < 2 ** -3
+
+
+@pytest.mark.parametrize("causal,window", [(True, -1), (True, 40), (False, -1)])
+def test_fp8_backward_sampled_positions_match_the_full_result(causal, window):
+    """q_idx / k_idx only restrict which rows and keys are summed, at their absolute
+    positions: with all keys the dq rows, with all rows the dk / dv rows equal the
+    full result's."""
+    codes, deq, f, kw = _fp8_bwd_case(19, causal, window)
+    kw.pop("offset"), kw.pop("softmax_type")
+    full = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], 2.0, **kw)
+    Sq, Skv = codes[0].shape[1], codes[1].shape[1]
+    rows = np.array([0, 3, Sq // 2, Sq - 1])
+    keys = np.array([1, Skv // 3, Skv - 2])
+    a = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], 2.0, q_idx=rows, **kw)
+    b = fp8.attention_bwd_fp8(*codes, f["o"], f["lse"], 2.0, k_idx=keys, **kw)
+    np.testing.assert_array_equal(a["dq"], full["dq"][:, rows])
+    np.testing.assert_allclose(b["dk"], full["dk"][:, keys], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(b["dv"], full["dv"][:, keys], rtol=0, atol=1e-13)
+
+
+def _emulate_fp8_bwd_kernel(codes, o, lse, ds_amax, causal, window, scale):
+    """The FP8 backward in the kernel's fp32 arithmetic: S and dP as fp32 sums of the
+    codes' products, P = 2^(S sl2 - LSE log2 e) in fp32, D = fp32 sum of dO8 O times
+    descale, dS = P (dP dsc - D), the two roundings of the fp32 values, the output
+    sums scaled by the descales and rounded to bf16."""
+    f32 = np.float32
+    q8, k8, v8, do8, dsq, dsk, dsv, dsdo = codes
+    q, k, v = (fp8.e4m3_decode(c).astype(f32) for c in (q8, k8, v8))
+    do = fp8.e5m2_decode(do8).astype(f32)
+    B, Sq, Hq, d = q.shape
+    Skv, G = k.shape[1], Hq // k.shape[2]
+    sc = f32(scale)
+    log2e = f32(1.4426950408889634)
+    sl2 = f32(f32(f32(sc * log2e) * f32(dsq)) * f32(dsk))
+    dsc = f32(f32(dsdo) * f32(dsv))
+    s_ds = fp8.scale_from_amax(ds_amax, "e5m2")
+    i, j = np.arange(Sq)[:, None], np.arange(Skv)[None, :]
+    vis = np.ones((Sq, Skv), dtype=bool)
+    if causal:
+        vis &= j <= i
+    if window >= 0:
+        vis &= j >= i - window
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            nl2 = (-np.asarray(lse[b, h], dtype=f32) * log2e).astype(f32)[:, None]
+            P = np.exp2(((q[b, :, h] @ k[b, :, g].T).astype(f32) * sl2 + nl2).astype(f32)).astype(f32)
+            P = np.where(vis, P, f32(0))
+            Pt = fp8.e4m3_decode(fp8.e4m3_encode((P * f32(256)).astype(f32)))
+            D = (np.sum(do[b, :, h] * np.asarray(o[b, :, h], dtype=f32), axis=1, dtype=f32) * f32(dsdo)).astype(f32)
+            dS = (P * ((do[b, :, h] @ v[b, :, g].T).astype(f32) * dsc - D[:, None])).astype(f32)
+            St = fp8.e5m2_decode(fp8.e5m2_encode((dS * s_ds).astype(f32)))
+            dv[b, :, g] += (Pt.T @ do[b, :, h]) * float(dsdo) / 256
+            dk[b, :, g] += (St.T @ q[b, :, h]) * float(sc * dsq / s_ds)
+            dq[b, :, h] = (St @ k[b, :, g]) * float(sc * dsk / s_ds)
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16).double().numpy()
+    return {"dq": bf(dq), "dk": bf(dk), "dv": bf(dv)}
+
+
+@pytest.mark.parametrize("causal,window,seed", [(True, -1, 23), (True, 6, 29), (False, -1, 31)])
+def test_fp8_backward_bound_covers_the_kernel_arithmetic_and_catches_missing_roundings(causal, window, seed):
+    """The GPU tests' per-element FP8 backward tolerance (parity_util.fp8_bwd_bounds):
+    an fp32 emulation of the kernel's arithmetic stays inside it, while the backward
+    without either rounding leaves it on a large share of the elements."""
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    import parity_util as pu
+    codes, deq, f, kw = _fp8_bwd_case(seed, causal, window)
+    o = torch.from_numpy(f["o"]).to(torch.bfloat16).double().numpy()
+    lse = f["lse"].astype(np.float32).astype(np.float64)
+    kw = dict(causal=causal, window=window, scale=0.3)
+    amax = np.float32(fp8.attention_bwd_fp8(*codes, o, lse, 1.0, **kw)["amax_ds"])
+    ref = fp8.attention_bwd_fp8(*codes, o, lse, amax, **kw)
+    bnd = pu.fp8_bwd_bounds(*codes, o, lse, amax, softmax_type=VANILLA, offset=None, **kw)
+    ratios = pu.check_fp8_bwd(_emulate_fp8_bwd_kernel(codes, o, lse, amax, causal, window, 0.3), ref, bnd, "emu")
+    assert max(ratios.values()) < 1.0
+    assert bnd["flips"] < 0.1
+    for variant in (dict(round_p=False), dict(round_ds=False)):
+        wrong = fp8.attention_bwd_fp8(*codes, o, lse, amax, **variant, **kw)
+        names = ("dv",) if "round_p" in variant else ("dq", "dk")
+        for n in names:
+            t = bnd["t_" + n]
+            beyond = np.abs(wrong[n] - ref[n]) > t + pu.BF16_U * (np.abs(ref[n]) + t)
+            assert beyond.mean() > 0.2, (variant, n, beyond.mean())
