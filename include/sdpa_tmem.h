@@ -8,8 +8,9 @@
  * distinct Q/K and V head dims, and three sink softmax types; plus padded batches
  * with per-entry lengths (attn_fwd_varlen / attn_bwd_varlen), an additive bias with
  * its gradient (attn_fwd_bias / attn_bwd_bias), attention dropout (attn_fwd_dropout /
- * attn_bwd_dropout) and an E4M3 forward with per-tensor scaling (attn_fp8_amax,
- * attn_fp8_quantize, attn_fwd_fp8).
+ * attn_bwd_dropout), an E4M3 forward with per-tensor scaling (attn_fp8_amax,
+ * attn_fp8_quantize, attn_fwd_fp8) and its FP8 backward (attn_fp8_quantize_e5m2,
+ * attn_bwd_fp8).
  *
  * Where each operation is defined:
  *   - the attention itself: "Speed up attention on GPU with cuDNN and
@@ -312,6 +313,49 @@ int attn_fp8_vt_row_bytes(int S);
 int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,
                  const float* descale_v, void* o, float* lse, int B, int S_q, int S_kv, int H_q, int H_kv, int d,
                  float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* stream);
+
+/*
+ * FP8 backward (E4M3 Q, K, V; E5M2 dO).  Source: "Speed up attention on GPU with
+ * cuDNN and TransformerEngine", step 10, section "Inspect the FP8 path": the hybrid
+ * recipe keeps the forward's tensors in E4M3 and takes gradients in E5M2 (5 exponent,
+ * 2 mantissa bits, the wider range), each with a per-tensor scale from its absolute
+ * maximum (DelayedScaling, margin 0).
+ *
+ * E5M2 here is the OCP 8-bit float: bias 15, largest finite 57344; conversions round
+ * to nearest even and saturate to +-57344.
+ *
+ * attn_fp8_quantize_e5m2: attn_fp8_quantize with E5M2 codes and scale = 57344 /
+ *   amax[0] (1 when amax is 0 or not finite); the same layouts, alignment and errors.
+ * attn_bwd_fp8_workspace_size: bytes of device workspace attn_bwd_fp8 needs (256-byte
+ *   aligned; two fp32 rows per (b, h) of S_q rounded up to 128).
+ * attn_bwd_fp8: dQ, dK, dV (bf16 BSHD, as attn_bwd) and d_offset of the attention
+ *   whose forward attn_fwd_fp8 computed (o, lse its outputs), over the dequantised
+ *   Q = q8 descale_q, K = k8 descale_k, V = v8 descale_v and dO = do8 descale_do.
+ *   Per (b, h) with P = exp(scale Q K^T - LSE) masked as in the forward:
+ *     D = rowsum(dO * O); dP = dO V^T; dS = P (dP - D) (fp32);
+ *     P~ = E4M3(2^8 P) / 2^8 and dS~ = E5M2(s dS) / s with s = 57344 / ds_amax[0]
+ *       (1 when ds_amax[0] is 0 or not finite: delayed scaling from earlier steps);
+ *     dV = P~^T dO, dK = scale dS~^T Q, dQ = scale dS~ K (fp32 accumulation), summed
+ *       over the query heads of a group for dK, dV; d_offset as attn_bwd.
+ *   Operands: q8 [B, S_q, H_q, d], k8, v8 [B, S_kv, H_kv, d] E4M3 BSHD; do8 [B, S_q,
+ *   H_q, d] E5M2 BSHD; qt8, dot8 [B, H_q, d, attn_fp8_vt_row_bytes(S_q)] and kt8 [B,
+ *   H_kv, d, attn_fp8_vt_row_bytes(S_kv)], the same codes transposed (quantize calls
+ *   with transpose = 1 and the same amax); o bf16 BSHD; lse fp32 [B, H_q, S_q].  All
+ *   scalars are fp32 in device memory.  ds_amax_out, when not NULL, receives max |dS|
+ *   (before rounding) over the whole call, for the next step's ds_amax; it must not
+ *   alias ds_amax.  d = d_qk = d_v in {64, 128}; full-length batches, no bias or
+ *   dropout.  The results are deterministic (no atomics in dQ, dK, dV).
+ *   Errors as attn_bwd; d outside {64, 128} is ATTN_ERR_UNSUPPORTED.
+ */
+int attn_fp8_quantize_e5m2(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                           float* descale, float* amax_out, void* stream);
+size_t attn_bwd_fp8_workspace_size(int B, int S_q, int H_q);
+int attn_bwd_fp8(const void* q8, const void* k8, const void* v8, const void* do8, const void* qt8, const void* kt8,
+                 const void* dot8, const float* descale_q, const float* descale_k, const float* descale_v,
+                 const float* descale_do, const void* o, const float* lse, const float* ds_amax, float* ds_amax_out,
+                 void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d,
+                 float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* workspace,
+                 size_t workspace_bytes, void* stream);
 
 /*
  * Failure-path self-test.  Every pipeline wait in the kernels is bounded (about one

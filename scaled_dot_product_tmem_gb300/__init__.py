@@ -101,6 +101,13 @@ def _load():
     lib.attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp, f,
                                      vp, i, vp, sz, vp]
     lib.attn_bwd_dropout.restype = i
+    lib.attn_fp8_quantize_e5m2.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.attn_fp8_quantize_e5m2.restype = i
+    lib.attn_bwd_fp8_workspace_size.argtypes = [i, i, i]
+    lib.attn_bwd_fp8_workspace_size.restype = sz
+    lib.attn_bwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
+                                 i, i, i, f, i, i, i, vp, vp, sz, vp]
+    lib.attn_bwd_fp8.restype = i
     _lib = lib
     return lib
 
@@ -389,11 +396,7 @@ def attn_fp8_amax(x, amax, *, stream=None):
         raise AttnError(st, "attn_fp8_amax")
 
 
-def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, amax_out=None, stream=None):
-    """x8 (uint8 E4M3) = E4M3(x * 448 / amax); descale (fp32 [1]) = amax / 448 as 1 / scale.
-
-    x bf16 BSHD [B,S,H,d]; x8 the same shape, or [B,H,d,S_pad] with transpose=True.
-    amax_out (fp32 [1], optional): records max |x| during the same pass."""
+def _fp8_quantize(name, x, x8, amax, descale, transpose, amax_out, stream):
     _check(x, "x", torch.bfloat16, 4)
     _check(x8, "x8", torch.uint8, 4)
     _check(amax, "amax", torch.float32, 1)
@@ -404,10 +407,23 @@ def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, amax_out=None, s
         raise ValueError(f"x8 must have shape {want}, got {tuple(x8.shape)}")
     if amax_out is not None:
         _check(amax_out, "amax_out", torch.float32, 1)
-    st = _load().attn_fp8_quantize(_ptr(x), _ptr(x8), B, S, H, d, int(bool(transpose)), _ptr(amax), _ptr(descale),
-                                   _ptr(amax_out), _stream(stream))
+    st = getattr(_load(), name)(_ptr(x), _ptr(x8), B, S, H, d, int(bool(transpose)), _ptr(amax), _ptr(descale),
+                                _ptr(amax_out), _stream(stream))
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fp8_quantize")
+        raise AttnError(st, name)
+
+
+def attn_fp8_quantize(x, x8, amax, descale, *, transpose=False, amax_out=None, stream=None):
+    """x8 (uint8 E4M3) = E4M3(x * 448 / amax); descale (fp32 [1]) = amax / 448 as 1 / scale.
+
+    x bf16 BSHD [B,S,H,d]; x8 the same shape, or [B,H,d,S_pad] with transpose=True.
+    amax_out (fp32 [1], optional): records max |x| during the same pass."""
+    _fp8_quantize("attn_fp8_quantize", x, x8, amax, descale, transpose, amax_out, stream)
+
+
+def attn_fp8_quantize_e5m2(x, x8, amax, descale, *, transpose=False, amax_out=None, stream=None):
+    """attn_fp8_quantize with E5M2 codes: x8 = E5M2(x * 57344 / amax)."""
+    _fp8_quantize("attn_fp8_quantize_e5m2", x, x8, amax, descale, transpose, amax_out, stream)
 
 
 def attn_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, *, causal=True, window=-1,
@@ -436,13 +452,16 @@ def attn_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, *, causal
         raise AttnError(st, "attn_fwd_fp8")
 
 
-def fp8_quantize(x, *, transpose=False, amax=None, amax_out=None, stream=None):
-    """Per-tensor E4M3 quantisation of a bf16 BSHD tensor: returns (x8, amax, descale).
+def fp8_quantize(x, *, transpose=False, amax=None, amax_out=None, fmt="e4m3", stream=None):
+    """Per-tensor E4M3 (fmt="e5m2": E5M2) quantisation of a bf16 BSHD tensor: returns
+    (x8, amax, descale).
 
     amax: an fp32 [1] device tensor holding the scaling statistic (for example the
     max of an amax history); None computes this tensor's own amax first (a second
     pass).  amax_out: optional fp32 [1] device tensor that records this tensor's
     amax during the cast (delayed scaling)."""
+    if fmt not in ("e4m3", "e5m2"):
+        raise ValueError(f"fmt must be 'e4m3' or 'e5m2', got {fmt!r}")
     B, S, H, d = x.shape
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
@@ -450,7 +469,8 @@ def fp8_quantize(x, *, transpose=False, amax=None, amax_out=None, stream=None):
     shape = (B, H, d, attn_fp8_vt_row_bytes(S)) if transpose else (B, S, H, d)
     x8 = torch.empty(shape, dtype=torch.uint8, device=x.device)
     descale = torch.empty(1, dtype=torch.float32, device=x.device)
-    attn_fp8_quantize(x, x8, amax, descale, transpose=transpose, amax_out=amax_out, stream=stream)
+    quant = attn_fp8_quantize_e5m2 if fmt == "e5m2" else attn_fp8_quantize
+    quant(x, x8, amax, descale, transpose=transpose, amax_out=amax_out, stream=stream)
     return x8, amax, descale
 
 
@@ -467,6 +487,87 @@ def sdpa_forward_fp8(q, k, v, *, causal=True, window=-1, softmax_type=VANILLA, s
     attn_fwd_fp8(q8, k8, vt8, dq, dk, dv, o, lse, causal=causal, window=window, softmax_type=softmax_type,
                  softmax_offset=softmax_offset, scale=scale, stream=stream)
     return o, lse
+
+
+def attn_bwd_fp8_workspace_size(B, S_q, H_q) -> int:
+    return int(_load().attn_bwd_fp8_workspace_size(int(B), int(S_q), int(H_q)))
+
+
+def attn_bwd_fp8(q8, k8, v8, do8, qt8, kt8, dot8, descale_q, descale_k, descale_v, descale_do, o, lse, ds_amax,
+                 dq, dk, dv, d_offset=None, *, ds_amax_out=None, causal=True, window=-1, softmax_type=VANILLA,
+                 softmax_offset=None, scale=0.0, workspace=None, stream=None):
+    """FP8 backward into preallocated bf16 dq, dk, dv (BSHD) and d_offset (fp32 [H_q],
+    learnable sinks).  q8, k8, v8 uint8 E4M3 BSHD; do8 uint8 E5M2 BSHD; qt8, dot8
+    [B,H_q,d,S_pad(S_q)] and kt8 [B,H_kv,d,S_pad(S_kv)] the same codes transposed;
+    o, lse the forward's outputs; descale_*, ds_amax (s = 57344 / ds_amax for dS) and
+    ds_amax_out (receives max |dS|) fp32 [1] device tensors."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8"), (do8, "do8"), (qt8, "qt8"), (kt8, "kt8"), (dot8, "dot8")):
+        _check(t, n, torch.uint8, 4)
+    for t, n in ((descale_q, "descale_q"), (descale_k, "descale_k"), (descale_v, "descale_v"),
+                 (descale_do, "descale_do"), (ds_amax, "ds_amax")):
+        _check(t, n, torch.float32, 1)
+    if ds_amax_out is not None:
+        _check(ds_amax_out, "ds_amax_out", torch.float32, 1)
+    for t, n in ((o, "o"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    if softmax_offset is not None:
+        _check(softmax_offset, "softmax_offset", torch.float32, 1)
+    if d_offset is not None:
+        _check(d_offset, "d_offset", torch.float32, 1)
+    B, S_q, H_q, d = q8.shape
+    _, S_kv, H_kv, _ = k8.shape
+    want = {"qt8": (B, H_q, d, attn_fp8_vt_row_bytes(S_q)), "dot8": (B, H_q, d, attn_fp8_vt_row_bytes(S_q)),
+            "kt8": (B, H_kv, d, attn_fp8_vt_row_bytes(S_kv))}
+    for t, n in ((qt8, "qt8"), (dot8, "dot8"), (kt8, "kt8")):
+        if tuple(t.shape) != want[n]:
+            raise ValueError(f"{n} must have shape {want[n]}, got {tuple(t.shape)}")
+    for t, n, shp in ((v8, "v8", k8.shape), (do8, "do8", q8.shape), (o, "o", q8.shape), (dq, "dq", q8.shape),
+                      (dk, "dk", k8.shape), (dv, "dv", k8.shape)):
+        if tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{n} must have shape {tuple(shp)}, got {tuple(t.shape)}")
+    need = attn_bwd_fp8_workspace_size(B, S_q, H_q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
+    st = _load().attn_bwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(do8), _ptr(qt8), _ptr(kt8), _ptr(dot8),
+                              _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), _ptr(descale_do), _ptr(o), _ptr(lse),
+                              _ptr(ds_amax), _ptr(ds_amax_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(d_offset), B, S_q,
+                              S_kv, H_q, H_kv, d, float(scale or 0.0), int(bool(causal)), int(window),
+                              _stype(softmax_type), _ptr(softmax_offset), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_fp8")
+
+
+def sdpa_backward_fp8(q, k, v, o, dout, lse, *, ds_amax=None, ds_amax_out=None, causal=True, window=-1,
+                      softmax_type=VANILLA, softmax_offset=None, scale=0.0, stream=None):
+    """bf16 in, bf16 out through the FP8 backward: quantise Q, K, V (E4M3) and dO (E5M2)
+    with their own amax, natural and transposed, then run attn_bwd_fp8.  ds_amax: the
+    dS scaling statistic (fp32 [1] device tensor, e.g. the max of an amax history);
+    None runs the backward twice, the first time only to record this step's max |dS|.
+    Returns (dq, dk, dv, d_offset)."""
+    q8, aq, sq = fp8_quantize(q, stream=stream)
+    k8, ak, sk = fp8_quantize(k, stream=stream)
+    v8, _, sv = fp8_quantize(v, stream=stream)
+    do8, ado, sdo = fp8_quantize(dout, fmt="e5m2", stream=stream)
+    qt8, _, _ = fp8_quantize(q, transpose=True, amax=aq, stream=stream)
+    kt8, _, _ = fp8_quantize(k, transpose=True, amax=ak, stream=stream)
+    dot8, _, _ = fp8_quantize(dout, transpose=True, amax=ado, fmt="e5m2", stream=stream)
+    B, S_q, H_q, d = q.shape
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    d_offset = torch.empty(H_q, dtype=torch.float32, device=q.device)
+    kw = dict(causal=causal, window=window, softmax_type=softmax_type, softmax_offset=softmax_offset, scale=scale,
+              stream=stream)
+    if ds_amax is None:
+        ds_amax = torch.empty(1, dtype=torch.float32, device=q.device)
+        first = torch.ones(1, dtype=torch.float32, device=q.device)
+        attn_bwd_fp8(q8, k8, v8, do8, qt8, kt8, dot8, sq, sk, sv, sdo, o, lse, first, dq, dk, dv, d_offset,
+                     ds_amax_out=ds_amax, **kw)
+    attn_bwd_fp8(q8, k8, v8, do8, qt8, kt8, dot8, sq, sk, sv, sdo, o, lse, ds_amax, dq, dk, dv, d_offset,
+                 ds_amax_out=ds_amax_out, **kw)
+    return dq, dk, dv, d_offset
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -550,8 +550,8 @@ int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream) {
   return ATTN_OK;
 }
 
-int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
-                      float* descale, float* amax_out, void* stream) {
+static int fp8_quantize_impl(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                             float* descale, float* amax_out, void* stream, bool e5m2) {
   if (B < 0 || S < 0 || H <= 0 || d <= 0 || d % 8 != 0 || !amax || !descale) return ATTN_ERR_INVALID_ARG;
   if (transpose && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((size_t)B * S * H * d > 0 && (!x || !x8)) return ATTN_ERR_INVALID_ARG;
@@ -563,7 +563,7 @@ int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int rc = timed(ATTN_KERNEL_FP8_QUANT, 1, s, [&] {
     return sdpa::launch_fp8_quantize(static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(x8), B, S, H, d,
-                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, amax_out, s);
+                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, amax_out, s, e5m2);
   });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
@@ -571,6 +571,16 @@ int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int t
     return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
+}
+
+int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                      float* descale, float* amax_out, void* stream) {
+  return fp8_quantize_impl(x, x8, B, S, H, d, transpose, amax, descale, amax_out, stream, false);
+}
+
+int attn_fp8_quantize_e5m2(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
+                           float* descale, float* amax_out, void* stream) {
+  return fp8_quantize_impl(x, x8, B, S, H, d, transpose, amax, descale, amax_out, stream, true);
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,
@@ -622,6 +632,123 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* d
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("fp8 forward kernel launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+size_t attn_bwd_fp8_workspace_size(int B, int S_q, int H_q) {
+  if (B < 0 || S_q < 0 || H_q <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H_q * ((static_cast<size_t>(S_q) + 127) / 128 * 128);
+  return 2 * round256(rows * sizeof(float));
+}
+
+int attn_bwd_fp8(const void* q8, const void* k8, const void* v8, const void* do8, const void* qt8, const void* kt8,
+                 const void* dot8, const float* descale_q, const float* descale_k, const float* descale_v,
+                 const float* descale_do, const void* o, const float* lse, const float* ds_amax, float* ds_amax_out,
+                 void* dq, void* dk, void* dv, float* d_offset, int B, int S_q, int S_kv, int H_q, int H_kv, int d,
+                 float scale, int causal, int window, int softmax_type, const float* softmax_offset, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  int st = check_common(B, S_q, S_kv, H_q, H_kv, d, d, causal, window, softmax_type, softmax_offset);
+  if (st != ATTN_OK) return st;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (softmax_type == ATTN_SOFTMAX_LEARNABLE && !d_offset) return ATTN_ERR_INVALID_ARG;
+  if (!descale_q || !descale_k || !descale_v || !descale_do || !ds_amax) return ATTN_ERR_INVALID_ARG;
+  if (ds_amax_out && ds_amax_out == ds_amax) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(descale_q) & 3u) || (reinterpret_cast<uintptr_t>(descale_k) & 3u) ||
+      (reinterpret_cast<uintptr_t>(descale_v) & 3u) || (reinterpret_cast<uintptr_t>(descale_do) & 3u) ||
+      (reinterpret_cast<uintptr_t>(ds_amax) & 3u) || (reinterpret_cast<uintptr_t>(ds_amax_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(d_offset) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0 || (S_q == 0 && S_kv == 0)) {
+    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (ds_amax_out && cudaMemsetAsync(ds_amax_out, 0, sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if ((S_q > 0 && (!q8 || !qt8 || !do8 || !dot8 || !o || !lse || !dq)) ||
+      (S_kv > 0 && (!k8 || !kt8 || !v8 || !dk || !dv)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(do8) || !aligned16(qt8) ||
+      !aligned16(kt8) || !aligned16(dot8) || !aligned16(o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_bwd_fp8_workspace_size(B, S_q, H_q);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  int* err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  // this call's max |dS| is taken with atomic maxima from zero (0 when nothing is visible)
+  if (ds_amax_out && cudaMemsetAsync(ds_amax_out, 0, sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (S_q == 0) {  // no query row sees a key: dK = dV = 0
+    if (cudaMemsetAsync(dk, 0, (size_t)B * S_kv * H_kv * d * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, (size_t)B * S_kv * H_kv * d * 2, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (d_offset && cudaMemsetAsync(d_offset, 0, sizeof(float) * H_q, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  sdpa::BwdParams p;
+  p.B = B; p.S_q = S_q; p.S_kv = S_kv; p.H_q = H_q; p.H_kv = H_kv; p.G = H_q / H_kv;
+  p.scale = resolve_scale(scale, d);
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.window = window < 0 ? -1 : window;
+  p.softmax_type = softmax_type;
+  p.S_pad = (S_q + 127) / 128 * 128;
+  p.offset = softmax_offset;
+  p.seq_q = nullptr;
+  p.seq_kv = nullptr;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = nullptr;
+  p.lse = lse;
+  p.nlse2 = reinterpret_cast<float*>(ws);
+  p.Dsum = reinterpret_cast<float*>(ws + need / 2);
+  p.d_offset = d_offset;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.ns = 1;
+  p.dk_part = nullptr;
+  p.dv_part = nullptr;
+  p.dq_acc = nullptr;
+  p.err = err;
+  p.do8 = static_cast<const uint8_t*>(do8);
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.descale_do = descale_do;
+  p.ds_amax = ds_amax;
+  p.ds_amax_out = ds_amax_out;
+  const int n_pre = 1 + (softmax_type == ATTN_SOFTMAX_LEARNABLE ? 1 : 0);
+  if (timed(ATTN_KERNEL_BWD_PREPROCESS, n_pre, s, [&] { return sdpa::launch_bwd_preprocess_fp8(d, p, s); }) != 0) {
+    set_error("fp8 backward preprocess launch", cudaGetLastError());
+    return ATTN_ERR_CUDA;
+  }
+  if (S_kv == 0) {  // every row is empty: O = 0 so D = 0 and dQ = 0
+    if (cudaMemsetAsync(dq, 0, (size_t)B * S_q * H_q * d * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  const int tq_row = attn_fp8_vt_row_bytes(S_q), tk_row = attn_fp8_vt_row_bytes(S_kv);
+  CUtensorMap tq64, tdo64, tq128, tdo128, tk, tv, tqt, tdot, tkt;
+  if (!sdpa::make_bshd_map_e4m3(&tq64, q8, B, S_q, H_q, d, 64) ||
+      !sdpa::make_bshd_map_e4m3(&tdo64, do8, B, S_q, H_q, d, 64) ||
+      !sdpa::make_bshd_map_e4m3(&tq128, q8, B, S_q, H_q, d, 128) ||
+      !sdpa::make_bshd_map_e4m3(&tdo128, do8, B, S_q, H_q, d, 128) ||
+      !sdpa::make_bshd_map_e4m3(&tk, k8, B, S_kv, H_kv, d, 128) ||
+      !sdpa::make_bshd_map_e4m3(&tv, v8, B, S_kv, H_kv, d, 128) ||
+      !sdpa::make_t_map_fp8(&tqt, qt8, B, S_q, tq_row, H_q, d, 64) ||
+      !sdpa::make_t_map_fp8(&tdot, dot8, B, S_q, tq_row, H_q, d, 64) ||
+      !sdpa::make_t_map_fp8(&tkt, kt8, B, S_kv, tk_row, H_kv, d, 128)) {
+    set_error("cuTensorMapEncodeTiled (fp8 backward operands)");
+    return ATTN_ERR_CUDA;
+  }
+  int rc = timed(ATTN_KERNEL_BWD_KV, 1, s,
+                 [&] { return sdpa::launch_bwd_kv_fp8(d, tq64, tk, tv, tdo64, tqt, tdot, p, s); });
+  if (rc == 0)
+    rc = timed(ATTN_KERNEL_BWD_Q, 1, s, [&] { return sdpa::launch_bwd_q_fp8(d, tq128, tk, tv, tdo128, tkt, p, s); });
+  if (rc == -2) return ATTN_ERR_UNSUPPORTED;
+  if (rc != 0) {
+    set_error("fp8 backward kernel launch", cudaGetLastError());
     return ATTN_ERR_CUDA;
   }
   return ATTN_OK;

@@ -44,8 +44,9 @@ int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t 
 // x8 = E4M3(x * scale), scale = 448 / amax[0] (1 if amax is 0 or not finite),
 // descale[0] = 1 / scale.  transpose: x [B, S, H, d] -> x8 [B, H, d, S_pad].
 // amax_out (may be null): receives max |x| of this tensor, recorded during the cast.
+// e5m2: E5M2 codes with scale = 57344 / amax instead.
 int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, float* amax_out, cudaStream_t stream);
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2 = false);
 
 struct BwdParams {
   int B, S_q, S_kv, H_q, H_kv, G;
@@ -81,6 +82,16 @@ struct BwdParams {
   const unsigned long long* rng = nullptr;
   unsigned drop_t = 0;
   float drop_scale = 1.f;
+  // FP8 backward: the E5M2 dO codes (for D), the per-tensor descales (device scalars), the
+  // dS scaling statistic (device scalar: scale = 57344 / *ds_amax) and where this step's
+  // max |dS| is recorded (may be null)
+  const uint8_t* do8 = nullptr;
+  const float* descale_q = nullptr;
+  const float* descale_k = nullptr;
+  const float* descale_v = nullptr;
+  const float* descale_do = nullptr;
+  const float* ds_amax = nullptr;
+  float* ds_amax_out = nullptr;
 };
 
 int launch_bwd_preprocess(int d_v, const BwdParams& p, cudaStream_t stream);
@@ -119,6 +130,20 @@ int launch_bwd_kv_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtens
                           bool fuse_dq, cudaStream_t stream);
 int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+
+// FP8 backward (E4M3 Q, K, V; E5M2 dO), d_qk = d_v = d in {64, 128}, full-length batches:
+// the preprocess (D from the dequantised dO8 and the bf16 O), the kv-stationary kernel (dK,
+// dV) and the query-stationary kernel (dQ).  Maps: tq8/tk8/tv8/tdo8 natural BSHD codes
+// (boxes of the whole head dim x 64 rows for Q/dO, x 128 rows for K/V); tqt8/tdot8 the
+// transposed Q / dO codes [B, H_q, d, S_pad] (boxes of 64 queries x d); tkt8 the transposed
+// K codes [B, H_kv, d, S_pad] (boxes of 128 keys x d); tq8_128/tdo8_128 the natural Q/dO
+// with 128-row boxes for the dQ kernel.
+int launch_bwd_preprocess_fp8(int d, const BwdParams& p, cudaStream_t stream);
+int launch_bwd_kv_fp8(int d, const CUtensorMap& tq8, const CUtensorMap& tk8, const CUtensorMap& tv8,
+                      const CUtensorMap& tdo8, const CUtensorMap& tqt8, const CUtensorMap& tdot8, const BwdParams& p,
+                      cudaStream_t stream);
+int launch_bwd_q_fp8(int d, const CUtensorMap& tq8_128, const CUtensorMap& tk8, const CUtensorMap& tv8,
+                     const CUtensorMap& tdo8_128, const CUtensorMap& tkt8, const BwdParams& p, cudaStream_t stream);
 
 // One warp waits on an mbarrier nobody arrives at: after the wait limit it records
 // kErrTimeoutBase + site in *err and returns (the failure path, without a fault).

@@ -1,4 +1,6 @@
-// fp8_quant.cu -- per-tensor E4M3 quantisation of the FP8 forward's inputs.
+// fp8_quant.cu -- per-tensor FP8 quantisation: E4M3 for the FP8 forward's inputs and
+// the backward's Q, K, V; E5M2 for the backward's dO (the hybrid recipe: gradients in
+// E5M2, with max finite 57344 in place of 448 below).
 //
 // Source: "Speed up attention on GPU with cuDNN and TransformerEngine", step 10,
 // section "Inspect the FP8 path": the forward takes E4M3 tensors whose per-tensor
@@ -57,16 +59,24 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__
   block_amax(m, amax_bits);
 }
 
+// E5: the E5M2 format (else E4M3).
+template <bool E5>
 __device__ __forceinline__ float scale_of(const float* amax) {
   const float a = *amax;
-  return (a > 0.f && a <= 3.402823466e38f) ? __fdiv_rn(448.f, a) : 1.f;
+  return (a > 0.f && a <= 3.402823466e38f) ? __fdiv_rn(E5 ? 57344.f : 448.f, a) : 1.f;
 }
 
+template <bool E5>
+__device__ __forceinline__ uint32_t pack4(float a, float b, float c, float d) {
+  return E5 ? pack_e5m2x4(a, b, c, d) : pack_e4m3x4(a, b, c, d);
+}
+
+template <bool E5>
 __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict__ x8, const __nv_bfloat16* __restrict__ x,
                                                         uint2* __restrict__ out8, uint8_t* __restrict__ out, size_t n,
                                                         const float* __restrict__ amax, float* __restrict__ descale,
                                                         unsigned* __restrict__ amax_out) {
-  const float sc = scale_of(amax);
+  const float sc = scale_of<E5>(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
   const size_t n8 = n / 8;
   unsigned m = 0;
@@ -77,17 +87,17 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
 #pragma unroll
       for (int q = 0; q < 4; ++q) m = max(m, max(abs_bits(bf16_lo(ws[q])), abs_bits(bf16_hi(ws[q]))));
     }
-    const uint32_t lo = pack_e4m3x4(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
-                                    __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
-    const uint32_t hi = pack_e4m3x4(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
-                                    __fmul_rn(bf16_lo(w.w), sc), __fmul_rn(bf16_hi(w.w), sc));
+    const uint32_t lo = pack4<E5>(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
+                                  __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
+    const uint32_t hi = pack4<E5>(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
+                                  __fmul_rn(bf16_lo(w.w), sc), __fmul_rn(bf16_hi(w.w), sc));
     out8[t] = make_uint2(lo, hi);
   }
   if (blockIdx.x == 0)
     for (size_t t = n8 * 8 + threadIdx.x; t < n; t += blockDim.x) {
       const float xv = __bfloat162float(x[t]);
       m = max(m, abs_bits(xv));
-      out[t] = (uint8_t)(pack_e4m3x4(__fmul_rn(xv, sc), 0.f, 0.f, 0.f) & 0xFFu);
+      out[t] = (uint8_t)(pack4<E5>(__fmul_rn(xv, sc), 0.f, 0.f, 0.f) & 0xFFu);
     }
   block_amax(m, amax_out);
 }
@@ -97,14 +107,14 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
 // row (key-major) in shared memory.  Phase 2 gives each thread 4 head dims x 16 keys:
 // sixteen 4-byte reads, 4 x 4 byte transposes with byte permutes, and one 16-byte
 // store per head dim into V^T (keys past S are zeros; keys past S_pad are not written).
-template <int D>
+template <int D, bool E5>
 __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ out,
                                                           int S, int H, int S_pad, const float* __restrict__ amax,
                                                           float* __restrict__ descale, unsigned* __restrict__ amax_out) {
   constexpr int KT = 128;          // keys per tile
   constexpr int ROW = D + 4;       // bytes per key row in shared memory (4-byte aligned, skews the banks)
   __shared__ __align__(16) uint8_t tile[KT * ROW];
-  const float sc = scale_of(amax);
+  const float sc = scale_of<E5>(amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *descale = __fdiv_rn(1.f, sc);
   const int n_tiles = (S_pad + KT - 1) / KT;
   const int kt = blockIdx.x % n_tiles, bh = blockIdx.x / n_tiles;
@@ -119,10 +129,10 @@ __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* _
     if (key < S) w = __ldcs(reinterpret_cast<const uint4*>(x + (((size_t)b * S + key) * H + h) * D + d0));
     m = max(m, max(max(abs_bits(bf16_lo(w.x)), abs_bits(bf16_hi(w.x))), max(abs_bits(bf16_lo(w.y)), abs_bits(bf16_hi(w.y)))));
     m = max(m, max(max(abs_bits(bf16_lo(w.z)), abs_bits(bf16_hi(w.z))), max(abs_bits(bf16_lo(w.w)), abs_bits(bf16_hi(w.w)))));
-    const uint32_t lo = pack_e4m3x4(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
-                                    __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
-    const uint32_t hi = pack_e4m3x4(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
-                                    __fmul_rn(bf16_lo(w.w), sc), __fmul_rn(bf16_hi(w.w), sc));
+    const uint32_t lo = pack4<E5>(__fmul_rn(bf16_lo(w.x), sc), __fmul_rn(bf16_hi(w.x), sc),
+                                  __fmul_rn(bf16_lo(w.y), sc), __fmul_rn(bf16_hi(w.y), sc));
+    const uint32_t hi = pack4<E5>(__fmul_rn(bf16_lo(w.z), sc), __fmul_rn(bf16_hi(w.z), sc),
+                                  __fmul_rn(bf16_lo(w.w), sc), __fmul_rn(bf16_hi(w.w), sc));
     uint32_t* dst = reinterpret_cast<uint32_t*>(tile + kk * ROW + d0);
     dst[0] = lo;
     dst[1] = hi;
@@ -169,25 +179,32 @@ int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t 
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, float* amax_out, cudaStream_t stream) {
+template <bool E5>
+static int quantize_t(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
+                      const float* amax, float* descale, unsigned* ao, cudaStream_t stream) {
   const size_t n = (size_t)B * S * H * d;
-  unsigned* ao = reinterpret_cast<unsigned*>(amax_out);
-  if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return -1;
   if (!transpose) {
-    fp8_quant_kernel<<<grid_for(n / 8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), x,
-                                                          reinterpret_cast<uint2*>(x8), x8, n, amax, descale, ao);
+    fp8_quant_kernel<E5><<<grid_for(n / 8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), x,
+                                                              reinterpret_cast<uint2*>(x8), x8, n, amax, descale, ao);
   } else {
     const long long blocks = (long long)((S_pad + 127) / 128) * H * B;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
     if (d == 128)
-      fp8_quant_t_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
+      fp8_quant_t_kernel<128, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
     else if (d == 64)
-      fp8_quant_t_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
+      fp8_quant_t_kernel<64, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
     else
       return -2;
   }
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2) {
+  unsigned* ao = reinterpret_cast<unsigned*>(amax_out);
+  if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return -1;
+  return e5m2 ? quantize_t<true>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream)
+              : quantize_t<false>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream);
 }
 
 }  // namespace sdpa

@@ -237,6 +237,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// kind::f8f6f4 with A and B each E4M3 (format code 0) or E5M2 (code 1), fp32
+// accumulation, both operands K-major.
+enum F8Fmt : uint32_t { kF8E4M3 = 0, kF8E5M2 = 1 };
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, F8Fmt a, F8Fmt b) {
+  return (1u << 4) | ((uint32_t)a << 7) | ((uint32_t)b << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05.mma (cta_group::1, kind::f16).  Issued by one thread.
 // ---------------------------------------------------------------------------
@@ -408,6 +416,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// Four fp32 values as E5M2 bytes (round to nearest even, saturating to +-57344), `a`
+// in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e5m2x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E5M2);
   return lo | (hi << 16);
 }
 

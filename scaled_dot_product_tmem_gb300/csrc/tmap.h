@@ -89,20 +89,25 @@ inline bool make_bshd_map_e4m3(CUtensorMap* m, const void* base, int B, int S, i
   return r == CUDA_SUCCESS;
 }
 
-// The transposed E4M3 V [B, H, D, S_pad] (keys innermost, rows S_pad bytes apart)
-// as (s, d, h, b) with a box of 128 keys x D rows x 1 x 1, 128-byte swizzle; keys
-// at or past S read as zeros.
-inline bool make_vt_map_e4m3(CUtensorMap* m, const void* base, int B, int S, int S_pad, int H, int D) {
+// A transposed 8-bit tensor [B, H, D, S_pad] (the sequence innermost, rows S_pad bytes
+// apart) as (s, d, h, b) with a box of `box_seq` (64 or 128) positions x D rows x 1 x 1,
+// swizzled by the box's row length (64- or 128-byte); positions at or past S read as zeros.
+inline bool make_t_map_fp8(CUtensorMap* m, const void* base, int B, int S, int S_pad, int H, int D, int box_seq) {
   PFN_encodeTiled enc = get_encode_tiled();
-  if (!enc || S_pad % 16 != 0 || S_pad < S) return false;
+  if (!enc || S_pad % 16 != 0 || S_pad < S || (box_seq != 64 && box_seq != 128)) return false;
   cuuint64_t dims[4] = {(cuuint64_t)S, (cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)S_pad, (cuuint64_t)D * S_pad, (cuuint64_t)H * D * S_pad};
-  cuuint32_t box[4] = {128, (cuuint32_t)D, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_seq, (cuuint32_t)D, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, box_seq == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The transposed E4M3 V of the FP8 forward: boxes of 128 keys x D rows.
+inline bool make_vt_map_e4m3(CUtensorMap* m, const void* base, int B, int S, int S_pad, int H, int D) {
+  return make_t_map_fp8(m, base, B, S, S_pad, H, D, 128);
 }
 
 // A row-major bf16 matrix [rows, cols] as a 2-D TMA tensor with a 64 x box_rows

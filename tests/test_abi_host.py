@@ -191,3 +191,37 @@ def test_dropout_argument_validation(lib):
         assert call(1.0 - 2.0 ** -18, P) == INVALID   # rounds to t = 65536: everything dropped
         assert call(0.1, None) == INVALID             # a drop probability needs the rng state
         assert call(0.1, MIS4) == MISALIGNED
+
+
+def test_fp8_backward_argument_validation(lib):
+    """attn_bwd_fp8 and attn_fp8_quantize_e5m2 reject bad arguments before any device
+    work; the workspace is two fp32 rows per (b, h) of S_q rounded up to 128."""
+    lib.attn_bwd_fp8_workspace_size.restype = ctypes.c_size_t
+    assert lib.attn_bwd_fp8_workspace_size(2, 100, 4) == 2 * 2 * 4 * 128 * 4
+    assert lib.attn_bwd_fp8_workspace_size(1, 1, 1) == 2 * 512
+    assert lib.attn_bwd_fp8_workspace_size(-1, 1, 1) == 0
+
+    def b8(q=P, dsq=P, dsa=P, dsout=None, doff=None, B=1, Sq=64, Skv=64, Hq=4, Hkv=2, d=128, st=0, off=None,
+           ws=P, wsb=1 << 20):
+        return lib.attn_bwd_fp8(q, P, P, P, P, P, P, dsq, P, P, P, P, P, dsa, dsout, P, P, P, doff, B, Sq, Skv, Hq,
+                                Hkv, d, ctypes.c_float(0.0), 1, -1, st, off, ws, ctypes.c_size_t(wsb), None)
+
+    assert b8(d=96) == UNSUPPORTED and b8(d=192) == UNSUPPORTED   # d = 64 or 128
+    assert b8(Hq=3) == INVALID
+    assert b8(dsq=None) == INVALID                      # descales are required
+    assert b8(dsa=None) == INVALID                      # so is the dS scaling statistic
+    assert b8(dsout=P) == INVALID                       # ds_amax_out may not alias ds_amax
+    assert b8(dsout=ctypes.c_void_p(0x10022)) == MISALIGNED
+    assert b8(st=2, off=P, doff=None) == INVALID        # learnable sinks need d_offset
+    assert b8(q=MIS) == MISALIGNED
+    assert b8(q=None) == INVALID
+    assert b8(B=0) == OK                                # nothing to launch
+
+    def qz(x=P, x8=P, B=1, S=64, H=2, d=128, t=0, amax=P, desc=P, aout=None):
+        return lib.attn_fp8_quantize_e5m2(x, x8, B, S, H, d, t, amax, desc, aout, None)
+
+    assert qz(d=96, t=1) == UNSUPPORTED
+    assert qz(d=12) == INVALID
+    assert qz(desc=None) == INVALID
+    assert qz(x=MIS) == MISALIGNED
+    assert qz(B=0) == OK
