@@ -7,7 +7,11 @@ One step = attn_fwd + attn_bwd (every step of the hot path) over one batch of
 synthetic BSHD bf16 inputs already resident in HBM.  The ``fp8_fwd_*`` workloads
 time the E4M3 forward instead: one step = the per-tensor E4M3 casts of Q, K and V
 (delayed scaling: the scale from the previous step's amax, this step's amax
-recorded during the cast) + attn_fwd_fp8, counted in forward FLOPs.  The default
+recorded during the cast) + attn_fwd_fp8, counted in forward FLOPs.  The
+``fp8_train_*`` workloads time an FP8 training step: the E4M3 casts of Q, K, V and
+the E5M2 casts of dO (BSHD and transposed, delayed scaling), attn_fwd_fp8 and
+attn_bwd_fp8 (dS scaled by the previous step's max |dS|), counted in forward +
+backward FLOPs.  The default
 workload is causal GQA at S=8192 (B=4, H_q=32, H_kv=8, d=128, vanilla softmax),
 the point at which the method's target is stated.  FLOPs count only unmasked
 (query, key) pairs: forward 2(d_qk + d_v) per pair, backward 2(3 d_qk + 2 d_v) per
@@ -41,20 +45,23 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, unmasked FLOPs) and % of GB300 BF16 peak"
 METRIC_FP8 = "attention fwd TFLOP/s (E4M3 Q/K/V with per-tensor scales, bf16 O; unmasked FLOPs)"
+METRIC_FP8_TRAIN = ("attention fwd+bwd TFLOP/s (E4M3 Q/K/V, E5M2 dO and dS, per-tensor delayed scaling; "
+                    "unmasked FLOPs)")
 FP8_PER_BF16 = 2.0  # nominal dense E4M3 / bf16 tensor throughput (4.5 / 2.25 PFLOP/s)
 NOMINAL_BF16_TFLOPS = 2250.0
 L2_BYTES = 129 * 1024 * 1024
 
 
 def _w(name, B, S, Hq, Hkv, dqk, dv, causal, window, st, scale, seed, desc, lens=None, fp8=False, bias=None,
-       dropout=0.0):
+       dropout=0.0, fp8_train=False):
     """A workload; `lens` (one length per batch entry, same for queries and keys) makes
     it a padded batch run through the varlen entry points; `fp8` makes it the E4M3
-    forward; `bias` = (Bb, Hb) adds a bf16 [Bb, Hb, S, S] bias (attn_fwd_bias /
-    attn_bwd_bias, with dbias); `dropout` = p runs attn_fwd_dropout / attn_bwd_dropout
-    with the rng state DROPOUT_RNG."""
+    forward, `fp8_train` the FP8 forward + backward step; `bias` = (Bb, Hb) adds a bf16
+    [Bb, Hb, S, S] bias (attn_fwd_bias / attn_bwd_bias, with dbias); `dropout` = p runs
+    attn_fwd_dropout / attn_bwd_dropout with the rng state DROPOUT_RNG."""
     return dict(name=name, B=B, S=S, Hq=Hq, Hkv=Hkv, dqk=dqk, dv=dv, causal=causal, window=window, st=st,
-                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8, bias=bias, dropout=dropout)
+                scale=scale, seed=seed, desc=desc, lens=lens, fp8=fp8 or fp8_train, fp8_train=fp8_train, bias=bias,
+                dropout=dropout)
 
 
 DROPOUT_RNG = (0x5EED_2024_0001, 0)  # (seed, offset) of the dropout workloads
@@ -90,6 +97,14 @@ WORKLOADS["fp8_fwd_mha_b4_s2048_d64"] = _w(
 WORKLOADS["fp8_fwd_gqa_b4_s8192_d128"] = _w(
     "fp8_fwd_gqa_b4_s8192_d128", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 42,
     "E4M3 forward: B=4, S=8192, H_q=32, H_kv=8, d=128, causal", fp8=True)
+# FP8 training step (forward + backward) at the causal GQA S=8192 point.
+WORKLOADS["fp8_train_gqa_b4_s8192_d128"] = _w(
+    "fp8_train_gqa_b4_s8192_d128", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 43,
+    "FP8 training step (E4M3 Q/K/V, E5M2 dO/dS): B=4, S=8192, H_q=32, H_kv=8, d=128, causal", fp8_train=True)
+# The same step at B=1: the small case its kernels are profiled on (inputs above L2, < 1 GB held).
+WORKLOADS["fp8_train_gqa_b1_s8192_d128"] = _w(
+    "fp8_train_gqa_b1_s8192_d128", 1, 8192, 32, 8, 128, 128, True, -1, 0, None, 44,
+    "FP8 training step (E4M3 Q/K/V, E5M2 dO/dS): B=1, S=8192, H_q=32, H_kv=8, d=128, causal", fp8_train=True)
 # Additive bias, one [S, S] plane per query head shared by the batch (dbias sums the batch).
 WORKLOADS["bias_gqa_b2_s4096"] = _w(
     "bias_gqa_b2_s4096", 2, 4096, 32, 8, 128, 128, True, -1, 0, None, 8,
@@ -127,7 +142,7 @@ def total_pairs(wl):
 def flops(wl, part="total"):
     n = wl["Hq"] * total_pairs(wl)
     fwd = n * 2 * (wl["dqk"] + wl["dv"])
-    bwd = 0 if wl.get("fp8") else n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
+    bwd = 0 if wl.get("fp8") and not wl.get("fp8_train") else n * 2 * (3 * wl["dqk"] + 2 * wl["dv"])
     return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd}[part]
 
 
@@ -141,12 +156,20 @@ def kernel_flops(wl, cls, fused):
 
 
 def fp8_cast_bytes(wl):
-    """Bytes the three E4M3 casts of one step must move: read bf16 Q, K, V (2 B per
-    element) and write their E4M3 codes (1 B; V's rows padded to 16 keys)."""
+    """Bytes the FP8 casts of one step must move, read bf16 (2 B per element) and write
+    codes (1 B; transposed rows padded to 16): Q, K (BSHD) and V (transposed) for the
+    forward; for a training step also Q^T, K^T, V (BSHD) and dO, dO^T."""
     B, S, Hq, Hkv, d = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"]
+    Sp = (S + 15) // 16 * 16
     nq, nk = B * S * Hq * d, B * S * Hkv * d
-    nv_out = B * Hkv * d * ((S + 15) // 16 * 16)
-    return 2 * (nq + 2 * nk) + nq + nk + nv_out
+    nqt, nkt = B * Hq * d * Sp, B * Hkv * d * Sp
+    fwd = 2 * (nq + 2 * nk) + nq + nk + nkt
+    if not wl.get("fp8_train"):
+        return fwd
+    return fwd + 2 * (nq + 2 * nk) + nqt + nkt + nk + 2 * (2 * nq) + nq + nqt
+
+def fp8_cast_launches(wl):
+    return 8 if wl.get("fp8_train") else 3
 
 
 def recorded_traffic(wl, kernel):
@@ -253,8 +276,13 @@ def run_oracle_unit(wl, x, b, h):
         q8, _, dq = fp8.quantize(x["q"][b:b + 1, :, h:h + 1].float().numpy(), amax=amax["q"])
         k8, _, dk = fp8.quantize(x["k"][b:b + 1, :, g:g + 1].float().numpy(), amax=amax["k"])
         v8, _, dv = fp8.quantize(x["v"][b:b + 1, :, g:g + 1].float().numpy(), amax=amax["v"])
-        fp8.attention_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=wl["causal"], window=wl["window"],
-                              softmax_type=wl["st"], scale=wl["scale"])
+        f = fp8.attention_fwd_fp8(q8, k8, v8, dq, dk, dv, causal=wl["causal"], window=wl["window"],
+                                  softmax_type=wl["st"], scale=wl["scale"])
+        if wl.get("fp8_train"):
+            a_do = x.setdefault("_amax_do", np.float32(x["dout"].float().abs().max()))
+            do8, _, ddo = fp8.quantize(x["dout"][b:b + 1, :, h:h + 1].float().numpy(), amax=a_do, fmt="e5m2")
+            fp8.attention_bwd_fp8(q8, k8, v8, do8, dq, dk, dv, ddo, f["o"], f["lse"], 1.0, causal=wl["causal"],
+                                  window=wl["window"], softmax_type=wl["st"], scale=wl["scale"])
         return
     L = wl["lens"][b] if wl.get("lens") else wl["S"]  # a padded entry computes on its own rows
     q = x["q"][b:b + 1, :L, h:h + 1].double().numpy()
@@ -276,7 +304,8 @@ def run_oracle_unit(wl, x, b, h):
 def unit_flops(wl, b=None):
     """FLOPs of one (batch, query head) unit: of entry b, or the workload's average."""
     if b is not None and wl.get("lens"):
-        per = 2 * (wl["dqk"] + wl["dv"]) + (0 if wl.get("fp8") else 2 * (3 * wl["dqk"] + 2 * wl["dv"]))
+        per = 2 * (wl["dqk"] + wl["dv"]) + (0 if wl.get("fp8") and not wl.get("fp8_train")
+                                           else 2 * (3 * wl["dqk"] + 2 * wl["dv"]))
         return n_pairs(wl["lens"][b], wl["causal"], wl["window"]) * per
     return flops(wl) / (wl["B"] * wl["Hq"])
 
@@ -305,8 +334,20 @@ def cpu_baseline(wl, x, budget_s=12.0):
     return {"value": work / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{done} of {len(units)} (batch, query head) units of the workload, "
-                      f"{'E4M3 quantisation + fwd' if wl.get('fp8') else 'fwd+bwd'} in fp64 "
+                      f"{oracle_step_desc(wl)} in fp64 "
                       f"({dt:.1f} s); TFLOP/s counts the same unmasked FLOPs as the GPU number"}
+
+
+def oracle_step_desc(wl):
+    if wl.get("fp8_train"):
+        return "FP8 quantisation + fwd + FP8 bwd"
+    return "E4M3 quantisation + fwd" if wl.get("fp8") else "fwd+bwd"
+
+
+def metric_of(wl):
+    if wl.get("fp8_train"):
+        return METRIC_FP8_TRAIN
+    return METRIC_FP8 if wl.get("fp8") else METRIC
 
 
 # ----------------------------------------------------------------------------- arms
@@ -330,7 +371,10 @@ def bench_config(wl, world, det):
     fp8 = bool(wl.get("fp8"))
     return {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
             "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
-            **({"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + attn_fwd_fp8"}
+            **({"step": "E4M3 casts of Q, K, V and E5M2 casts of dO, BSHD and transposed (delayed scaling, "
+                        "amax recorded in the cast) + attn_fwd_fp8 + attn_bwd_fp8 (dS scaled by the previous "
+                        "step's max |dS|)"} if wl.get("fp8_train") else
+               {"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + attn_fwd_fp8"}
                if fp8 else {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
             "l2": "flushed between timed steps (258 MB write outside the timed span)",
             **({"seq_lens": wl["lens"]} if wl.get("lens") else {}),
@@ -361,9 +405,9 @@ def reference_arm(args, wl, world, rank):
     dt = time.perf_counter() - t0
     value = work / dt / 1e12
     sample = (f"each step = one (batch, query head) unit of the workload, "
-              f"{'E4M3 quantisation + fwd' if wl.get('fp8') else 'fwd+bwd'} in fp64 "
+              f"{oracle_step_desc(wl)} in fp64 "
               f"({unit_flops(wl) / 1e9:.2f} GFLOP)")
-    line = {"metric": METRIC_FP8 if wl.get("fp8") else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+    line = {"metric": metric_of(wl), "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": bench_config(wl, 1, uses_deterministic(wl, args)),
@@ -377,29 +421,57 @@ def reference_arm(args, wl, world, rank):
 
 def _step_fns_fp8(sdpa, wl, dev, x):
     """E4M3 forward step: cast Q, K (BSHD) and V (transposed) with the scales of the
-    previous step's amax while recording this step's, then attn_fwd_fp8."""
+    previous step's amax while recording this step's, then attn_fwd_fp8.  A training
+    step (fp8_train) also casts Q^T, K^T and V (E4M3) and dO, dO^T (E5M2) the same way
+    and runs attn_bwd_fp8 with dS scaled by the previous step's max |dS|."""
     import torch
+    train = bool(wl.get("fp8_train"))
     B, S, Hq, Hkv, d = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"]
-    t = {n: x[n].to(dev) for n in ("q", "k", "v")}
+    Sp = sdpa.attn_fp8_vt_row_bytes(S)
+    t = {n: x[n].to(dev) for n in (("q", "k", "v", "dout") if train else ("q", "k", "v"))}
     f32 = lambda: torch.empty(1, dtype=torch.float32, device=dev)
     amax = {n: [f32(), f32()] for n in t}          # [previous step's, this step's]
     desc = {n: f32() for n in t}
     for n in t:
         sdpa.attn_fp8_amax(t[n], amax[n][0])      # the history before the first step
-    x8 = {"q": torch.empty((B, S, Hq, d), dtype=torch.uint8, device=dev),
-          "k": torch.empty((B, S, Hkv, d), dtype=torch.uint8, device=dev),
-          "v": torch.empty((B, Hkv, d, sdpa.attn_fp8_vt_row_bytes(S)), dtype=torch.uint8, device=dev)}
+    u8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=dev)
+    x8 = {"q": u8(B, S, Hq, d), "k": u8(B, S, Hkv, d), "vt": u8(B, Hkv, d, Sp)}
+    # (tensor, code buffer, transposed, E5M2): the first cast of a tensor records its amax
+    casts = [("q", "q", False, False), ("k", "k", False, False), ("v", "vt", True, False)]
+    if train:
+        x8.update(qt=u8(B, Hq, d, Sp), kt=u8(B, Hkv, d, Sp), v=u8(B, S, Hkv, d), do=u8(B, S, Hq, d),
+                  dot=u8(B, Hq, d, Sp))
+        casts += [("q", "qt", True, False), ("k", "kt", True, False), ("v", "v", False, False),
+                  ("dout", "do", False, True), ("dout", "dot", True, True)]
     o = torch.empty((B, S, Hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], scale=wl["scale"] or 0.0)
+    outs = (o,)
+    if train:
+        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        ds_amax = [f32(), f32()]
+        ds_amax[0].fill_(1.0)                      # the history before the first step
+        ws = torch.empty(max(sdpa.attn_bwd_fp8_workspace_size(B, S, Hq), 256), dtype=torch.uint8, device=dev)
+        outs = (o, dq, dk, dv)
 
     def step():
-        for n in ("q", "k", "v"):
-            sdpa.attn_fp8_quantize(t[n], x8[n], amax[n][0], desc[n], transpose=(n == "v"), amax_out=amax[n][1])
+        seen = set()
+        for n, buf, tr, e5 in casts:
+            quant = sdpa.attn_fp8_quantize_e5m2 if e5 else sdpa.attn_fp8_quantize
+            quant(t[n], x8[buf], amax[n][0], desc[n], transpose=tr, amax_out=None if n in seen else amax[n][1])
+            seen.add(n)
+        for n in t:
             amax[n].reverse()                      # this step's amax scales the next step
-        sdpa.attn_fwd_fp8(x8["q"], x8["k"], x8["v"], desc["q"], desc["k"], desc["v"], o, lse, **kw)
+        sdpa.attn_fwd_fp8(x8["q"], x8["k"], x8["vt"], desc["q"], desc["k"], desc["v"], o, lse, **kw)
+        if train:
+            # the step's scales were applied above, so desc[] holds them; the amax lists were
+            # swapped, so [1] is the history that scaled this step and [0] this step's record
+            sdpa.attn_bwd_fp8(x8["q"], x8["k"], x8["v"], x8["do"], x8["qt"], x8["kt"], x8["dot"], desc["q"],
+                              desc["k"], desc["v"], desc["dout"], o, lse, ds_amax[0], dq, dk, dv, None,
+                              ds_amax_out=ds_amax[1], workspace=ws, **kw)
+            ds_amax.reverse()
 
-    return step, t, (o,)
+    return step, t, outs
 
 
 def _step_fns(sdpa, wl, dev, det, x):
@@ -573,24 +645,26 @@ def ours_arm(args, wl, world, rank, local):
     dms, dn = kt[dom]
     if dom == "fp8_quantize":  # a stream: bytes, against the measured copy bandwidth
         bound, unit = "hbm", "GB/s"
-        achieved = fp8_cast_bytes(wl) / 3 / (dms / dn / 1e3) / 1e9 if dn else 0.0
+        achieved = fp8_cast_bytes(wl) / fp8_cast_launches(wl) / (dms / dn / 1e3) / 1e9 if dn else 0.0
         peak = float(peaks["hbm_gbs"])
         peak_desc = f"hbm_gbs from {peak_src}"
     else:
         bound, unit = "tensor", "TFLOP/s"
-        dflops = kernel_flops(wl, dom, fused=not det)
+        dflops = kernel_flops(wl, dom, fused=not det and not wl.get("fp8_train"))
         achieved = dflops / (dms / dn / 1e3) / 1e12 if dn else 0.0
         peak = float(peaks["bf16_tflops"]) * (FP8_PER_BF16 if fp8 else 1.0)
         peak_desc = (f"bf16_tflops (burst) from {peak_src} x {FP8_PER_BF16} (nominal E4M3/bf16 ratio)"
                      if fp8 else f"bf16_tflops (burst) from {peak_src}")
-    launches = sum(v[1] for v in kt.values())
-    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps,
+    split_steps = min(args.steps, 10)   # the per-kernel pass (measure's split_steps)
+    per_step = sum(v[1] for v in kt.values()) / split_steps
+    launches = int(round(per_step * args.steps))  # the timed pass runs the same launches per step
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / split_steps,
                    "share": v[0] / sum(u[0] for u in kt.values())}
                for k, v in kt.items() if v[1]}
-    line = {"metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+    line = {"metric": metric_of(wl), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": ("e4m3/e5m2" if wl.get("fp8_train") else "e4m3") if fp8 else "bf16", "data": "synthetic",
             "config": bench_config(wl, world, det),
             "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             **({"pct_of_nominal_fp8_peak": 100.0 * value / world / (FP8_PER_BF16 * NOMINAL_BF16_TFLOPS)}

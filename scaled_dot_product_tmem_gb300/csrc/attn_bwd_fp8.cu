@@ -15,7 +15,12 @@
 //   query-stationary kernel (one CTA per (b, h, 128 queries)):
 //     S = Q K^T and dP = dO V^T from the natural codes; dS~ (E5M2) in TMEM;
 //     dQ += dS~ K with K read from its transposed copy [B, H_kv, d, S_pad].
-// The descales of the codes fold into the score scale, into dP and into the epilogues.
+// The descales of the codes fold into the score scale, into dP and into the epilogues, and
+// the two code scales into the per-row values the preprocess stores: with
+//   l' = -LSE log2(e) + 8 and D' = -D s / 2^8 (s the dS scale),
+// a thread forms 2^8 P = 2^(S scale log2(e) + l') (the E4M3 operand as it stands) and
+// s dS = 2^8 P (dP s / 2^8 + D') (the E5M2 operand as it stands) with one fma, one ex2, one
+// more fma and one multiply per element, the fmas and multiplies two lanes at a time.
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
@@ -44,8 +49,9 @@ __device__ __forceinline__ uint64_t desc_rows(uint32_t saddr, int row) {
   return row == 128 ? smem_desc_sw128(saddr, 16, 1024) : smem_desc_sw64(saddr, 16, 512);
 }
 
-// Preprocess: D = descale_do * sum_d E5M2(dO8) O (fp32) and nlse2 = -LSE log2(e) into the
-// padded [B, H_q, S_pad] rows (D = 0, nlse2 = -inf past S_q), one block per 64 rows.
+// Preprocess: D' = -D s / 2^8 with D = descale_do * sum_d E5M2(dO8) O (fp32) and
+// l' = -LSE log2(e) + 8 into the padded [B, H_q, S_pad] rows (D' = 0, l' = -inf past S_q),
+// one block per 64 rows.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_fp8_kernel(const BwdParams p) {
   constexpr int TPR = D / 8, RPP = 256 / TPR, TILE = 64, NR = TILE / RPP;
@@ -53,6 +59,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_fp8_kernel(const BwdParams
   const int i0 = blockIdx.x * TILE, h = blockIdx.y, b = blockIdx.z;
   const int sub = threadIdx.x % TPR;
   const float dsc = *p.descale_do;
+  const float neg_s8 = -e5m2_scale_of(p.ds_amax) * (1.f / kPScale);  // -s / 2^8 (exact)
   uint4 a[NR];
   uint2 g[NR];
 #pragma unroll
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_fp8_kernel(const BwdParams
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0) dsum[r] = acc * dsc;
+    if (sub == 0) dsum[r] = (acc * dsc) * neg_s8;
   }
   __syncthreads();
   if (threadIdx.x < TILE) {
@@ -90,14 +97,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_fp8_kernel(const BwdParams
     const bool real = i < p.S_q;
     p.Dsum[bh * p.S_pad + i] = real ? dsum[threadIdx.x] : 0.f;
     const float l = real ? p.lse[bh * p.S_q + i] : -INFINITY;
-    p.nlse2[bh * p.S_pad + i] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+    p.nlse2[bh * p.S_pad + i] = l == -INFINITY ? -INFINITY : fmaf(-l, kLog2e, 8.f);
   }
 }
 
-// d offset_h = -sum_{b,i} exp(offset_h - LSE) D, as in the bf16 backward (fixed order).
+// d offset_h = -sum_{b,i} exp(offset_h - LSE) D = (2^8 / s) sum_{b,i} 2^(c log2(e) + l' - 8) D',
+// as in the bf16 backward (fixed order).
 __global__ void __launch_bounds__(256) bwd_doffset_fp8_kernel(const BwdParams p) {
   const int h = blockIdx.x;
-  const float c2 = p.offset[h] * kLog2e;
+  const float c2 = fmaf(p.offset[h], kLog2e, -8.f);
   float acc = 0.f;
   for (int b = 0; b < p.B; ++b) {
     const float* nl2 = p.nlse2 + ((size_t)b * p.H_q + h) * p.S_pad;
@@ -112,7 +120,7 @@ __global__ void __launch_bounds__(256) bwd_doffset_fp8_kernel(const BwdParams p)
   if (threadIdx.x == 0) {
     float s = 0.f;
     for (int w = 0; w < 8; ++w) s += part[w];
-    p.d_offset[h] = -s;
+    p.d_offset[h] = s * __fdiv_rn(kPScale, e5m2_scale_of(p.ds_amax));
   }
 }
 
@@ -142,14 +150,16 @@ struct KvF8Cfg {
   static constexpr int L_STAGE = 2 * BQ * 4;
   static constexpr int STAGE_TX = 2 * Q_TILE + 2 * T_TILE + L_STAGE;
   static constexpr int OFF_BAR = OFF_L + NQ * L_STAGE;
-  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, mma_done, dv_done[2], dk_done
-  static constexpr int NBAR = 1 + 2 * NQ + 10;
+  // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready[2], p_ready[2], ds_ready[2], mma_done, dv_done[2],
+  // dk_done[2]
+  static constexpr int NBAR = 1 + 2 * NQ + 13;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
   static constexpr int THREADS = 352;
-  static constexpr int COL_S0 = 0, COL_S1 = 64, COL_DP = 128, COL_DV = 192, COL_DK = 192 + D;
-  static_assert(COL_DK + D <= 512, "TMEM budget");
+  // S^T and dP^T double-buffered (slot = step & 1); P~^T and dS~^T overwrite them in place
+  static constexpr int COL_S0 = 0, COL_S1 = 64, COL_DP0 = 128, COL_DV = 192, COL_DK = 192 + D, COL_DP1 = 192 + 2 * D;
+  static_assert(COL_DP1 + 64 <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -168,13 +178,13 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NQ;
-  uint64_t* s_ready = q_empty + C::NQ;  // [2]
-  uint64_t* dp_ready = s_ready + 2;
-  uint64_t* p_ready = s_ready + 3;      // [2]
-  uint64_t* ds_ready = s_ready + 5;
-  uint64_t* mma_done = s_ready + 6;
-  uint64_t* dv_done = s_ready + 7;      // [2]
-  uint64_t* dk_done = s_ready + 9;
+  uint64_t* s_ready = q_empty + C::NQ;  // [2] per slot
+  uint64_t* dp_ready = s_ready + 2;     // [2]
+  uint64_t* p_ready = s_ready + 4;      // [2]
+  uint64_t* ds_ready = s_ready + 6;     // [2]
+  uint64_t* mma_done = s_ready + 8;
+  uint64_t* dv_done = s_ready + 9;      // [2]
+  uint64_t* dk_done = s_ready + 11;     // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -197,16 +207,15 @@ __global__ void __launch_bounds__(352, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NQ; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
-    mbar_init(&s_ready[0], 1);
-    mbar_init(&s_ready[1], 1);
-    mbar_init(dp_ready, 1);
-    mbar_init(&p_ready[0], 256);
-    mbar_init(&p_ready[1], 256);
-    mbar_init(ds_ready, 256);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_ready[k], 1);
+      mbar_init(&dp_ready[k], 1);
+      mbar_init(&p_ready[k], 256);
+      mbar_init(&ds_ready[k], 256);
+      mbar_init(&dv_done[k], 1);
+      mbar_init(&dk_done[k], 1);
+    }
     mbar_init(mma_done, 2);
-    mbar_init(&dv_done[0], 1);
-    mbar_init(&dv_done[1], 1);
-    mbar_init(dk_done, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -276,14 +285,16 @@ __global__ void __launch_bounds__(352, 1)
           for (int kk = 0; kk < D / 32; ++kk)
             mma_ss_f8_warp(colS, desc_add(dK0, kk * 32), desc_add(dq, kk * 32), idS, kk > 0);
           mma_commit_warp(&s_ready[slot]);
-          if (s > 0) ok = mbar_wait_warp(dk_done, (s - 1) & 1, err, kF8DkDone);
+          // dP^T(s) reuses the slot of dP^T(s - 2): dK(s - 2) must have read its dS~^T
+          if (s >= 2) ok = mbar_wait_warp(&dk_done[slot], ((s >> 1) - 1) & 1, err, kF8DkDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t ddo = desc_rows(smem_u32(smem + C::OFF_DO + st * C::Q_TILE), D);
+          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8_warp(tmem + C::COL_DP, desc_add(dV0, kk * 32), desc_add(ddo, kk * 32), idP, kk > 0);
-          mma_commit_warp(dp_ready);
+            mma_ss_f8_warp(colP, desc_add(dV0, kk * 32), desc_add(ddo, kk * 32), idP, kk > 0);
+          mma_commit_warp(&dp_ready[slot]);
         }
       } else {
         for (int s = 0; s < nsteps && ok; ++s) {
@@ -300,16 +311,16 @@ __global__ void __launch_bounds__(352, 1)
           for (int kk = 0; kk < C::BQ / 32; ++kk)
             mma_ts_f8_warp(tmem + C::COL_DV, colS + 32 * kk, desc_add(ddot, kk * 32), idV, (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dv_done[slot]);
-          ok = mbar_wait_warp(ds_ready, s & 1, err, kF8DS);
+          ok = mbar_wait_warp(&ds_ready[slot], (s >> 1) & 1, err, kF8DS);
           if (!ok) break;
           tc_fence_after();
-          // dK += dS~^T Q: A = dS~^T in TMEM over the dP columns, B = Q^T
+          // dK += dS~^T Q: A = dS~^T in TMEM over the slot's dP columns, B = Q^T
           const uint64_t dqt = desc_rows(smem_u32(smem + C::OFF_QT + st * C::T_TILE), 64);
+          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 32; ++kk)
-            mma_ts_f8_warp(tmem + C::COL_DK, tmem + C::COL_DP + 32 * kk, desc_add(dqt, kk * 32), idK,
-                           (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_warp(dk_done);
+            mma_ts_f8_warp(tmem + C::COL_DK, colP + 32 * kk, desc_add(dqt, kk * 32), idK, (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_warp(&dk_done[slot]);
           mma_commit_warp(&q_empty[st]);  // the stage's S / dP products completed before P~ / dS~ existed
         }
       }
@@ -323,9 +334,10 @@ __global__ void __launch_bounds__(352, 1)
     const int key = n0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2 * (*p.descale_q) * (*p.descale_k);
-    const float dsc = (*p.descale_do) * (*p.descale_v);
     const float s_ds = e5m2_scale_of(p.ds_amax);
-    float amax = 0.f;
+    const float dsc = (*p.descale_do) * (*p.descale_v) * (s_ds * (1.f / kPScale));  // dP -> dP s / 2^8
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), dsc2 = f2_pack(dsc, dsc);
+    float amax = 0.f;  // of s dS
     bool ok = true;
     for (int s = 0; s < nsteps && ok; ++s) {
       const int st = s % C::NQ;
@@ -334,10 +346,11 @@ __global__ void __launch_bounds__(352, 1)
       const float* dd = l2 + C::BQ;
       const int slot = s & 1;
       const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
+      const uint32_t colP = slot ? C::COL_DP1 : C::COL_DP0;
       ok = mbar_wait_warp(&s_ready[slot], (s >> 1) & 1, err, kF8S);
       if (!ok) break;
       tc_fence_after();
-      float pr[32];
+      float pr[32];  // 2^8 P
       {
         uint32_t rr[32];
         tmem_ld32(lane_addr + colS + 32 * w, rr);
@@ -346,7 +359,13 @@ __global__ void __launch_bounds__(352, 1)
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c] = ex2(fmaf(__uint_as_float(rr[c]), sl2, lv[c]));
+        for (int c = 0; c < 32; c += 2) {
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2,
+                           f2_pack(lv[c], lv[c + 1])), xa, xb);
+          pr[c] = ex2(xa);
+          pr[c + 1] = ex2(xb);
+        }
       }
       if (!tile_fully_visible<false>(mask, q0, C::BQ, n0, C::BN)) {
         int vlo, vhi;
@@ -360,41 +379,40 @@ __global__ void __launch_bounds__(352, 1)
       {  // P~^T: E4M3(2^8 P), 4 queries per TMEM column, over this warpgroup's own S columns
         uint32_t p8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p8[q] = pack_e4m3x4(pr[4 * q] * kPScale, pr[4 * q + 1] * kPScale, pr[4 * q + 2] * kPScale,
-                              pr[4 * q + 3] * kPScale);
+        for (int q = 0; q < 8; ++q) p8[q] = pack_e4m3x4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
         tmem_st8(lane_addr + colS + 32 * w, p8);
         tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(&p_ready[slot]);
-      ok = mbar_wait_warp(dp_ready, s & 1, err, kF8DP);
+      ok = mbar_wait_warp(&dp_ready[slot], (s >> 1) & 1, err, kF8DP);
       if (!ok) break;
       tc_fence_after();
       {
         uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
+        tmem_ld32(lane_addr + colP + 32 * w, rr);
         float dv4[32];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
         tmem_ld_wait();
-        float ds[32];
+        float ds[32];  // s dS = 2^8 P (dP s / 2^8 + D')
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          ds[c] = pr[c] * fmaf(__uint_as_float(rr[c]), dsc, -dv4[c]);  // dS = P (dP - D)
-          amax = fmaxf(amax, fabsf(ds[c]));
+        for (int c = 0; c < 32; c += 2) {
+          const uint64_t t = f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), dsc2,
+                                    f2_pack(dv4[c], dv4[c + 1]));
+          f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]), t), ds[c], ds[c + 1]);
+          amax = fmax3(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
         }
         uint32_t d8[8];  // dS~^T: E5M2(s dS), over this warpgroup's own dP columns
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d8[q] = pack_e5m2x4(ds[4 * q] * s_ds, ds[4 * q + 1] * s_ds, ds[4 * q + 2] * s_ds, ds[4 * q + 3] * s_ds);
-        tmem_st8(lane_addr + C::COL_DP + 32 * w, d8);
+        for (int q = 0; q < 8; ++q) d8[q] = pack_e5m2x4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
+        tmem_st8(lane_addr + colP + 32 * w, d8);
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive(&ds_ready[slot]);
     }
-    record_amax(amax, p.ds_amax_out);
+    record_amax(__fdiv_rn(amax, s_ds), p.ds_amax_out);
     // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
     bool have = false;
     if (ok && nsteps > 0) {
@@ -453,14 +471,15 @@ struct QF8Cfg {
   static constexpr int OFF_V = OFF_K + NK * TILE;
   static constexpr int OFF_KT = OFF_V + NK * TILE;
   static constexpr int OFF_BAR = OFF_KT + NK * TILE;
-  // q_full, k_full[NK], k_empty[NK], s_ready, dp_ready, ds_ready, mma_done, s_free, dq_done
-  static constexpr int NBAR = 1 + 2 * NK + 6;
+  // q_full, k_full[NK], k_empty[NK], s_ready, dp_ready[2], ds_ready[2], mma_done, s_free, dq_done[2]
+  static constexpr int NBAR = 1 + 2 * NK + 9;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;
   static constexpr int THREADS = 352;
-  static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256;
-  static_assert(COL_DQ + D <= 512, "TMEM budget");
+  // dP double-buffered (slot = kv tile & 1); dS~ overwrites it in place
+  static constexpr int COL_S = 0, COL_DP0 = 128, COL_DQ = 256, COL_DP1 = 384;
+  static_assert(COL_DQ + D <= COL_DP1 && COL_DP1 + 128 <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -479,11 +498,11 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* k_full = bars + 1;
   uint64_t* k_empty = k_full + C::NK;
   uint64_t* s_ready = k_empty + C::NK;
-  uint64_t* dp_ready = s_ready + 1;
-  uint64_t* ds_ready = s_ready + 2;
-  uint64_t* mma_done = s_ready + 3;
-  uint64_t* s_free = s_ready + 4;
-  uint64_t* dq_done = s_ready + 5;
+  uint64_t* dp_ready = s_ready + 1;  // [2] per slot
+  uint64_t* ds_ready = s_ready + 3;  // [2]
+  uint64_t* mma_done = s_ready + 5;
+  uint64_t* s_free = s_ready + 6;
+  uint64_t* dq_done = s_ready + 7;   // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -505,11 +524,13 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     mbar_init(s_ready, 1);
-    mbar_init(dp_ready, 1);
-    mbar_init(ds_ready, 256);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&dp_ready[k], 1);
+      mbar_init(&ds_ready[k], 256);
+      mbar_init(&dq_done[k], 1);
+    }
     mbar_init(mma_done, 2);
     mbar_init(s_free, 256);
-    mbar_init(dq_done, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -569,29 +590,33 @@ __global__ void __launch_bounds__(352, 1)
           for (int kk = 0; kk < D / 32; ++kk)
             mma_ss_f8_warp(tmem + C::COL_S, desc_add(dQ0, kk * 32), desc_add(dKa, kk * 32), idS, kk > 0);
           mma_commit_warp(s_ready);
-          if (n > 0) ok = mbar_wait_warp(dq_done, (n - 1) & 1, err, kF8QDqDone);
+          // dP(n) reuses the slot of dP(n - 2): dQ(n - 2) must have read its dS~
+          const int slot = n & 1;
+          if (n >= 2) ok = mbar_wait_warp(&dq_done[slot], ((n >> 1) - 1) & 1, err, kF8QDqDone);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8_warp(tmem + C::COL_DP, desc_add(dDO0, kk * 32), desc_add(dVa, kk * 32), idP, kk > 0);
-          mma_commit_warp(dp_ready);
+            mma_ss_f8_warp(colP, desc_add(dDO0, kk * 32), desc_add(dVa, kk * 32), idP, kk > 0);
+          mma_commit_warp(&dp_ready[slot]);
         }
       } else {
         for (int n = 0; n < nj && ok; ++n) {
-          const int sk = n % C::NK;
+          const int sk = n % C::NK, slot = n & 1;
           ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kF8QKFull) &&
-               mbar_wait_warp(ds_ready, n & 1, err, kF8QDS);
+               mbar_wait_warp(&ds_ready[slot], (n >> 1) & 1, err, kF8QDS);
           if (!ok) break;
           tc_fence_after();
           // dS~ of keys 32 kk .. 32 kk + 31: warpgroup kk / 2 stored its 64 keys 4 per column from
-          // COL_DP + 64 (kk / 2)
+          // the slot's dP column + 64 (kk / 2)
           const uint64_t dKT = desc_rows(smem_u32(smem + C::OFF_KT + sk * C::TILE), 128);
+          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 32; ++kk)
-            mma_ts_f8_warp(tmem + C::COL_DQ, tmem + C::COL_DP + (kk / 2) * 64 + (kk % 2) * 8, desc_add(dKT, kk * 32),
-                           idQ, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_warp(dq_done);
+            mma_ts_f8_warp(tmem + C::COL_DQ, colP + (kk / 2) * 64 + (kk % 2) * 8, desc_add(dKT, kk * 32), idQ,
+                           (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_warp(&dq_done[slot]);
           mma_commit_warp(&k_empty[sk]);  // S(n) / dP(n) (issuer A) completed before dS~(n) existed
         }
       }
@@ -605,14 +630,16 @@ __global__ void __launch_bounds__(352, 1)
     const int i = m0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2 * (*p.descale_q) * (*p.descale_k);
-    const float dsc = (*p.descale_do) * (*p.descale_v);
     const float s_ds = e5m2_scale_of(p.ds_amax);
-    float nl2row = -INFINITY, drow = 0.f;
+    const float dsc = (*p.descale_do) * (*p.descale_v) * (s_ds * (1.f / kPScale));  // dP -> dP s / 2^8
+    float nl2row = -INFINITY, drow = 0.f;  // l' and D' of the row
     if (i < p.S_q) {
       const size_t ri = ((size_t)b * p.H_q + h) * p.S_pad + i;
       nl2row = p.nlse2[ri];
       drow = p.Dsum[ri];
     }
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2row, nl2row);
+    const uint64_t dsc2 = f2_pack(dsc, dsc), dr2 = f2_pack(drow, drow);
     bool ok = true;
     for (int n = 0; n < nj && ok; ++n) {
       const int k0 = (jlo + n) * C::BN + 64 * w;
@@ -620,7 +647,7 @@ __global__ void __launch_bounds__(352, 1)
       if (!ok) break;
       tc_fence_after();
       const bool full = tile_fully_visible<false>(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
-      float pr[64];
+      float pr[64];  // 2^8 P
       {
         uint32_t ra[32], rb[32];
         tmem_ld32(lane_addr + C::COL_S + 64 * w, ra);
@@ -629,9 +656,14 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_before();
         mbar_arrive(s_free);  // S is in registers: the next S may be written
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pr[c] = ex2(fmaf(__uint_as_float(ra[c]), sl2, nl2row));
-          pr[32 + c] = ex2(fmaf(__uint_as_float(rb[c]), sl2, nl2row));
+        for (int c = 0; c < 32; c += 2) {
+          float xa, xb, xc, xd;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2x2), xa, xb);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, nl2x2), xc, xd);
+          pr[c] = ex2(xa);
+          pr[c + 1] = ex2(xb);
+          pr[32 + c] = ex2(xc);
+          pr[33 + c] = ex2(xd);
         }
       }
       if (!full) {
@@ -640,27 +672,30 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
       }
-      ok = mbar_wait_warp(dp_ready, n & 1, err, kF8QDP);
+      const int slot = n & 1;
+      const uint32_t colP = slot ? C::COL_DP1 : C::COL_DP0;
+      ok = mbar_wait_warp(&dp_ready[slot], (n >> 1) & 1, err, kF8QDP);
       if (!ok) break;
       tc_fence_after();
       uint32_t d8[16];  // dS~: E5M2(s dS) of this row's 64 keys, 4 per TMEM column
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 64 * w + c0, rr);
+        tmem_ld32(lane_addr + colP + 64 * w + c0, rr);
         tmem_ld_wait();
-        float ds[32];
+        float ds[32];  // s dS = 2^8 P (dP s / 2^8 + D')
 #pragma unroll
-        for (int c = 0; c < 32; ++c) ds[c] = pr[c0 + c] * fmaf(__uint_as_float(rr[c]), dsc, -drow);
+        for (int c = 0; c < 32; c += 2) {
+          const uint64_t t = f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), dsc2, dr2);
+          f2_unpack(f2_mul(f2_pack(pr[c0 + c], pr[c0 + c + 1]), t), ds[c], ds[c + 1]);
+        }
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d8[c0 / 4 + q] = pack_e5m2x4(ds[4 * q] * s_ds, ds[4 * q + 1] * s_ds, ds[4 * q + 2] * s_ds,
-                                       ds[4 * q + 3] * s_ds);
+        for (int q = 0; q < 8; ++q) d8[c0 / 4 + q] = pack_e5m2x4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
       }
-      tmem_st16(lane_addr + C::COL_DP + 64 * w, d8);
+      tmem_st16(lane_addr + colP + 64 * w, d8);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive(&ds_ready[slot]);
     }
     // epilogue: dQ = scale * descale_k / s * acc; warpgroup w writes head dims [w D/2, (w+1) D/2)
     bool have = false;

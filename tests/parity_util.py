@@ -182,8 +182,9 @@ def fp8_bwd_bounds(q8, k8, v8, do8, descale_q, descale_k, descale_v, descale_do,
     value may move by at most the larger of their distances from round(x) (zero where
     both ends round alike).  Error model (fp32 unit roundoff 2^-24):
       S     = scale q.k:  fp8_acc_rel(d) scale sum_d |q k| + 2^-22 |S|  (descale product)
-      exponent (natural units): e_S + 2^-23 (|S| + |LSE|), then ex2: 2^-21 relative,
-            so e_P = P (e_exp + 2^-21) 1.01;
+      exponent (natural units): e_S + 2^-23 (|S| + |LSE| + 8) (the kernel adds log2 of
+            the code scale 2^8 inside it), then ex2: 2^-21 relative, so
+            e_P = P (e_exp + 2^-21) 1.01;
       dP    = dO.v:  fp8_acc_rel(d) sum_d |dO v| + 2^-22 |dP|;
       D     = dO.O in fp32 over d terms:  d 2^-24 sum_d |dO O| + 2^-23 |D|;
       dS    = P (dP - D):  |dP - D| e_P + P (e_dP + e_D) + 2^-23 |dS|.
@@ -241,7 +242,7 @@ def fp8_bwd_bounds(q8, k8, v8, do8, descale_q, descale_k, descale_v, descale_do,
             Sabs = sc * np.abs(q[b, :, h, :]) @ np.abs(k[b, :, g, :]).T
             m = vis & ok
             P = np.where(m, np.exp(np.where(m, S, 0.0) - Lf), 0.0)
-            e_exp = acc_d * Sabs + 2.0 ** -22 * np.abs(S) + 2.0 ** -23 * (np.abs(S) + np.abs(Lf))
+            e_exp = acc_d * Sabs + 2.0 ** -22 * np.abs(S) + 2.0 ** -23 * (np.abs(S) + np.abs(Lf) + 8.0)
             e_P = np.where(m, P * (e_exp + 2.0 ** -21) * 1.01, 0.0)
             x = P * fp8.P_SCALE
             ex = e_P * fp8.P_SCALE

@@ -287,9 +287,10 @@ def test_fp8_backward_sampled_positions_match_the_full_result(causal, window):
 
 def _emulate_fp8_bwd_kernel(codes, o, lse, ds_amax, causal, window, scale):
     """The FP8 backward in the kernel's fp32 arithmetic: S and dP as fp32 sums of the
-    codes' products, P = 2^(S sl2 - LSE log2 e) in fp32, D = fp32 sum of dO8 O times
-    descale, dS = P (dP dsc - D), the two roundings of the fp32 values, the output
-    sums scaled by the descales and rounded to bf16."""
+    codes' products; per row l' = -LSE log2(e) + 8 and D' = -D s / 2^8 (D = fp32 sum of
+    dO8 O times descale); 2^8 P = 2^(S sl2 + l') and s dS = 2^8 P (dP dsc' + D') with
+    dsc' = descale_do descale_v s / 2^8, each rounded to fp32; the two roundings of those
+    fp32 values; the output sums scaled by the descales and rounded to bf16."""
     f32 = np.float32
     q8, k8, v8, do8, dsq, dsk, dsv, dsdo = codes
     q, k, v = (fp8.e4m3_decode(c).astype(f32) for c in (q8, k8, v8))
@@ -299,8 +300,9 @@ def _emulate_fp8_bwd_kernel(codes, o, lse, ds_amax, causal, window, scale):
     sc = f32(scale)
     log2e = f32(1.4426950408889634)
     sl2 = f32(f32(f32(sc * log2e) * f32(dsq)) * f32(dsk))
-    dsc = f32(f32(dsdo) * f32(dsv))
     s_ds = fp8.scale_from_amax(ds_amax, "e5m2")
+    s8 = f32(s_ds / f32(256))
+    dsc = f32(f32(f32(dsdo) * f32(dsv)) * s8)
     i, j = np.arange(Sq)[:, None], np.arange(Skv)[None, :]
     vis = np.ones((Sq, Skv), dtype=bool)
     if causal:
@@ -311,13 +313,14 @@ def _emulate_fp8_bwd_kernel(codes, o, lse, ds_amax, causal, window, scale):
     for b in range(B):
         for h in range(Hq):
             g = h // G
-            nl2 = (-np.asarray(lse[b, h], dtype=f32) * log2e).astype(f32)[:, None]
-            P = np.exp2(((q[b, :, h] @ k[b, :, g].T).astype(f32) * sl2 + nl2).astype(f32)).astype(f32)
-            P = np.where(vis, P, f32(0))
-            Pt = fp8.e4m3_decode(fp8.e4m3_encode((P * f32(256)).astype(f32)))
+            lp = (-np.asarray(lse[b, h], dtype=f32) * log2e + f32(8)).astype(f32)[:, None]
+            P8 = np.exp2(((q[b, :, h] @ k[b, :, g].T).astype(f32) * sl2 + lp).astype(f32)).astype(f32)
+            P8 = np.where(vis, P8, f32(0))
+            Pt = fp8.e4m3_decode(fp8.e4m3_encode(P8))
             D = (np.sum(do[b, :, h] * np.asarray(o[b, :, h], dtype=f32), axis=1, dtype=f32) * f32(dsdo)).astype(f32)
-            dS = (P * ((do[b, :, h] @ v[b, :, g].T).astype(f32) * dsc - D[:, None])).astype(f32)
-            St = fp8.e5m2_decode(fp8.e5m2_encode((dS * s_ds).astype(f32)))
+            Dp = (D * -s8).astype(f32)
+            t = ((do[b, :, h] @ v[b, :, g].T).astype(f32) * dsc + Dp[:, None]).astype(f32)
+            St = fp8.e5m2_decode(fp8.e5m2_encode((P8 * t).astype(f32)))
             dv[b, :, g] += (Pt.T @ do[b, :, h]) * float(dsdo) / 256
             dk[b, :, g] += (St.T @ q[b, :, h]) * float(sc * dsq / s_ds)
             dq[b, :, h] = (St @ k[b, :, g]) * float(sc * dsk / s_ds)
