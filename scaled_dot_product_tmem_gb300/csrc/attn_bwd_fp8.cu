@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(352, 1)
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_ready[k], 1);
       mbar_init(&dp_ready[k], 1);
-      mbar_init(&p_ready[k], 256);
-      mbar_init(&ds_ready[k], 256);
+      mbar_init(&p_ready[k], 128);  // one warpgroup per slot
+      mbar_init(&ds_ready[k], 128);
       mbar_init(&dv_done[k], 1);
       mbar_init(&dk_done[k], 1);
     }
@@ -304,22 +304,22 @@ __global__ void __launch_bounds__(352, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
-          // dV += P~^T dO: A = P~^T in TMEM (queries 32 kk .. 32 kk + 31 at colS + 32 kk, 4 per
+          // dV += P~^T dO: A = P~^T in TMEM (queries 32 kk .. 32 kk + 31 at colS + 8 kk, 4 per
           // column), B = dO^T (d rows x 64 queries, K-major over the queries)
           const uint64_t ddot = desc_rows(smem_u32(smem + C::OFF_DOT + st * C::T_TILE), 64);
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 32; ++kk)
-            mma_ts_f8_warp(tmem + C::COL_DV, colS + 32 * kk, desc_add(ddot, kk * 32), idV, (s > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_f8_warp(tmem + C::COL_DV, colS + 8 * kk, desc_add(ddot, kk * 32), idV, (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dv_done[slot]);
           ok = mbar_wait_warp(&ds_ready[slot], (s >> 1) & 1, err, kF8DS);
           if (!ok) break;
           tc_fence_after();
-          // dK += dS~^T Q: A = dS~^T in TMEM over the slot's dP columns, B = Q^T
+          // dK += dS~^T Q: A = dS~^T in TMEM over the slot's first dP columns, B = Q^T
           const uint64_t dqt = desc_rows(smem_u32(smem + C::OFF_QT + st * C::T_TILE), 64);
           const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 32; ++kk)
-            mma_ts_f8_warp(tmem + C::COL_DK, colP + 32 * kk, desc_add(dqt, kk * 32), idK, (s > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_f8_warp(tmem + C::COL_DK, colP + 8 * kk, desc_add(dqt, kk * 32), idK, (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dk_done[slot]);
           mma_commit_warp(&q_empty[st]);  // the stage's S / dP products completed before P~ / dS~ existed
         }
@@ -329,89 +329,106 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ P / dS warpgroups (thread = key)
-    const int w = warp / 4;  // which 32 query columns of the 64
+    // Ping-pong: warpgroup w takes the steps s = w, w + 2, ... (TMEM slot w), all 64 queries of
+    // each, so one warpgroup computes while the other waits for its products.
+    const int w = warp / 4;
     const int r = (warp % 4) * 32 + lane;
     const int key = n0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const uint32_t colS = lane_addr + (w ? C::COL_S1 : C::COL_S0);
+    const uint32_t colP = lane_addr + (w ? C::COL_DP1 : C::COL_DP0);
     const float sl2 = p.scale_log2 * (*p.descale_q) * (*p.descale_k);
     const float s_ds = e5m2_scale_of(p.ds_amax);
     const float dsc = (*p.descale_do) * (*p.descale_v) * (s_ds * (1.f / kPScale));  // dP -> dP s / 2^8
     const uint64_t sl2x2 = f2_pack(sl2, sl2), dsc2 = f2_pack(dsc, dsc);
-    float amax = 0.f;  // of s dS
+    float am[4] = {0.f, 0.f, 0.f, 0.f};  // max |s dS|, four independent chains
     bool ok = true;
-    for (int s = 0; s < nsteps && ok; ++s) {
+    for (int s = w; s < nsteps && ok; s += 2) {
       const int st = s % C::NQ;
       const int q0 = (ilo + s % nq) * C::BQ;
-      const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
+      const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE);
       const float* dd = l2 + C::BQ;
-      const int slot = s & 1;
-      const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
-      const uint32_t colP = slot ? C::COL_DP1 : C::COL_DP0;
-      ok = mbar_wait_warp(&s_ready[slot], (s >> 1) & 1, err, kF8S);
+      const uint32_t ph = (s >> 1) & 1;
+      ok = mbar_wait_warp(&s_ready[w], ph, err, kF8S);
       if (!ok) break;
       tc_fence_after();
-      float pr[32];  // 2^8 P
+      float pr[64];  // 2^8 P of the step's 64 queries
       {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + colS + 32 * w, rr);
-        float lv[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
+        uint32_t ra[32], rb[32];
+        tmem_ld32(colS, ra);
+        tmem_ld32(colS + 32, rb);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float xa, xb;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2,
-                           f2_pack(lv[c], lv[c + 1])), xa, xb);
-          pr[c] = ex2(xa);
-          pr[c + 1] = ex2(xb);
+        for (int c = 0; c < 32; c += 4) {
+          const float4 la = *reinterpret_cast<const float4*>(&l2[c]);
+          const float4 lb = *reinterpret_cast<const float4*>(&l2[32 + c]);
+          float x[8];
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, f2_pack(la.x, la.y)),
+                    x[0], x[1]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(ra[c + 2]), __uint_as_float(ra[c + 3])), sl2x2, f2_pack(la.z, la.w)),
+                    x[2], x[3]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), sl2x2, f2_pack(lb.x, lb.y)),
+                    x[4], x[5]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rb[c + 2]), __uint_as_float(rb[c + 3])), sl2x2, f2_pack(lb.z, lb.w)),
+                    x[6], x[7]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pr[c + e] = ex2(x[e]);
+            pr[32 + c + e] = ex2(x[4 + e]);
+          }
         }
       }
       if (!tile_fully_visible<false>(mask, q0, C::BQ, n0, C::BN)) {
         int vlo, vhi;
         visible_rows<false>(mask, key, &vlo, &vhi);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int qq = q0 + 32 * w + c;
-          pr[c] = (qq >= vlo && qq <= vhi) ? pr[c] : 0.f;
-        }
+        for (int c = 0; c < 64; ++c) pr[c] = (q0 + c >= vlo && q0 + c <= vhi) ? pr[c] : 0.f;
       }
-      {  // P~^T: E4M3(2^8 P), 4 queries per TMEM column, over this warpgroup's own S columns
-        uint32_t p8[8];
+      {  // P~^T: E4M3(2^8 P), 4 queries per TMEM column, over the slot's first 16 S^T columns
+        uint32_t p8[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) p8[q] = pack_e4m3x4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
-        tmem_st8(lane_addr + colS + 32 * w, p8);
+        for (int q = 0; q < 16; ++q) p8[q] = pack_e4m3x4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
+        tmem_st16(colS, p8);
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&p_ready[slot]);
-      ok = mbar_wait_warp(&dp_ready[slot], (s >> 1) & 1, err, kF8DP);
+      mbar_arrive(&p_ready[w]);
+      ok = mbar_wait_warp(&dp_ready[w], ph, err, kF8DP);
       if (!ok) break;
       tc_fence_after();
       {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + colP + 32 * w, rr);
-        float dv4[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
+        uint32_t ra[32], rb[32];
+        tmem_ld32(colP, ra);
+        tmem_ld32(colP + 32, rb);
         tmem_ld_wait();
-        float ds[32];  // s dS = 2^8 P (dP s / 2^8 + D')
+        uint32_t d8[16];  // dS~^T: E5M2(s dS), over the slot's first 16 dP^T columns
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const uint64_t t = f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), dsc2,
-                                    f2_pack(dv4[c], dv4[c + 1]));
-          f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]), t), ds[c], ds[c + 1]);
-          amax = fmax3(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+        for (int c = 0; c < 32; c += 4) {
+          const float4 da = *reinterpret_cast<const float4*>(&dd[c]);
+          const float4 db = *reinterpret_cast<const float4*>(&dd[32 + c]);
+          float y[8];  // s dS = 2^8 P (dP s / 2^8 + D')
+          const uint64_t t0 = f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), dsc2, f2_pack(da.x, da.y));
+          const uint64_t t1 = f2_fma(f2_pack(__uint_as_float(ra[c + 2]), __uint_as_float(ra[c + 3])), dsc2, f2_pack(da.z, da.w));
+          const uint64_t t2 = f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), dsc2, f2_pack(db.x, db.y));
+          const uint64_t t3 = f2_fma(f2_pack(__uint_as_float(rb[c + 2]), __uint_as_float(rb[c + 3])), dsc2, f2_pack(db.z, db.w));
+          f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]), t0), y[0], y[1]);
+          f2_unpack(f2_mul(f2_pack(pr[c + 2], pr[c + 3]), t1), y[2], y[3]);
+          f2_unpack(f2_mul(f2_pack(pr[32 + c], pr[33 + c]), t2), y[4], y[5]);
+          f2_unpack(f2_mul(f2_pack(pr[34 + c], pr[35 + c]), t3), y[6], y[7]);
+          am[0] = fmax3(am[0], fabsf(y[0]), fabsf(y[1]));
+          am[1] = fmax3(am[1], fabsf(y[2]), fabsf(y[3]));
+          am[2] = fmax3(am[2], fabsf(y[4]), fabsf(y[5]));
+          am[3] = fmax3(am[3], fabsf(y[6]), fabsf(y[7]));
+          d8[c / 4] = pack_e5m2x4(y[0], y[1], y[2], y[3]);
+          d8[8 + c / 4] = pack_e5m2x4(y[4], y[5], y[6], y[7]);
         }
-        uint32_t d8[8];  // dS~^T: E5M2(s dS), over this warpgroup's own dP columns
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d8[q] = pack_e5m2x4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
-        tmem_st8(lane_addr + colP + 32 * w, d8);
+        tmem_st16(colP, d8);
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&ds_ready[slot]);
+      mbar_arrive(&ds_ready[w]);
     }
+    const float amax = fmaxf(fmax3(am[0], am[1], am[2]), am[3]);
     record_amax(__fdiv_rn(amax, s_ds), p.ds_amax_out);
     // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
     bool have = false;
