@@ -729,23 +729,27 @@ int attn_bwd_fp8(const void* q8, const void* k8, const void* v8, const void* do8
     return ATTN_OK;
   }
   const int tq_row = attn_fp8_vt_row_bytes(S_q), tk_row = attn_fp8_vt_row_bytes(S_kv);
-  CUtensorMap tq64, tdo64, tq128, tdo128, tk, tv, tqt, tdot, tkt;
+  // kv kernel: 64-query Q / dO tiles, 128-key K / V tiles; dQ kernel: 128-row Q / dO tiles,
+  // 64-key K / V / K^T tiles
+  CUtensorMap tq64, tdo64, tq128, tdo128, tk, tv, tk64, tv64, tqt, tdot, tkt;
   if (!sdpa::make_bshd_map_e4m3(&tq64, q8, B, S_q, H_q, d, 64) ||
       !sdpa::make_bshd_map_e4m3(&tdo64, do8, B, S_q, H_q, d, 64) ||
       !sdpa::make_bshd_map_e4m3(&tq128, q8, B, S_q, H_q, d, 128) ||
       !sdpa::make_bshd_map_e4m3(&tdo128, do8, B, S_q, H_q, d, 128) ||
       !sdpa::make_bshd_map_e4m3(&tk, k8, B, S_kv, H_kv, d, 128) ||
       !sdpa::make_bshd_map_e4m3(&tv, v8, B, S_kv, H_kv, d, 128) ||
+      !sdpa::make_bshd_map_e4m3(&tk64, k8, B, S_kv, H_kv, d, 64) ||
+      !sdpa::make_bshd_map_e4m3(&tv64, v8, B, S_kv, H_kv, d, 64) ||
       !sdpa::make_t_map_fp8(&tqt, qt8, B, S_q, tq_row, H_q, d, 64) ||
       !sdpa::make_t_map_fp8(&tdot, dot8, B, S_q, tq_row, H_q, d, 64) ||
-      !sdpa::make_t_map_fp8(&tkt, kt8, B, S_kv, tk_row, H_kv, d, 128)) {
+      !sdpa::make_t_map_fp8(&tkt, kt8, B, S_kv, tk_row, H_kv, d, 64)) {
     set_error("cuTensorMapEncodeTiled (fp8 backward operands)");
     return ATTN_ERR_CUDA;
   }
   int rc = timed(ATTN_KERNEL_BWD_KV, 1, s,
                  [&] { return sdpa::launch_bwd_kv_fp8(d, tq64, tk, tv, tdo64, tqt, tdot, p, s); });
   if (rc == 0)
-    rc = timed(ATTN_KERNEL_BWD_Q, 1, s, [&] { return sdpa::launch_bwd_q_fp8(d, tq128, tk, tv, tdo128, tkt, p, s); });
+    rc = timed(ATTN_KERNEL_BWD_Q, 1, s, [&] { return sdpa::launch_bwd_q_fp8(d, tq128, tk64, tv64, tdo128, tkt, p, s); });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
     set_error("fp8 backward kernel launch", cudaGetLastError());

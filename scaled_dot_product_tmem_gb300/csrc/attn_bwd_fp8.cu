@@ -12,7 +12,7 @@
 //     S^T = K Q^T and dP^T = V dO^T from the natural codes; P~^T (E4M3) and dS~^T (E5M2)
 //     written to TMEM, 4 per column; dV += P~^T dO and dK += dS~^T Q with dO and Q read
 //     from their transposed copies [B, H_q, d, S_pad] (queries innermost);
-//   query-stationary kernel (one CTA per (b, h, 128 queries)):
+//   query-stationary kernel (one CTA per (b, h, 128 queries), 64 keys per step):
 //     S = Q K^T and dP = dO V^T from the natural codes; dS~ (E5M2) in TMEM;
 //     dQ += dS~ K with K read from its transposed copy [B, H_kv, d, S_pad].
 // The descales of the codes fold into the score scale, into dP and into the epilogues, and
@@ -480,27 +480,28 @@ __global__ void __launch_bounds__(352, 1)
 // =============================================================================
 template <int D>
 struct QF8Cfg {
-  static constexpr int BM = 128, BN = 128;
-  static constexpr int TILE = 128 * D;  // Q / dO (128 rows), K / V (128 keys), K^T (d rows x 128 keys)
-  static constexpr int NK = 2;
-  static constexpr int OFF_Q = 0, OFF_DO = TILE;
-  static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + NK * TILE;
-  static constexpr int OFF_KT = OFF_V + NK * TILE;
-  static constexpr int OFF_BAR = OFF_KT + NK * TILE;
-  // q_full, k_full[NK], k_empty[NK], s_ready, dp_ready[2], ds_ready[2], mma_done, s_free, dq_done[2]
+  static constexpr int BM = 128, BN = 64;
+  static constexpr int Q_TILE = BM * D;  // Q / dO codes, 128 rows x d bytes
+  static constexpr int K_TILE = BN * D;  // K / V codes (64 keys x d bytes); K^T (d rows x 64 keys)
+  static constexpr int NK = 4;
+  static constexpr int OFF_Q = 0, OFF_DO = Q_TILE;
+  static constexpr int OFF_K = 2 * Q_TILE;
+  static constexpr int OFF_V = OFF_K + NK * K_TILE;
+  static constexpr int OFF_KT = OFF_V + NK * K_TILE;
+  static constexpr int OFF_BAR = OFF_KT + NK * K_TILE;
+  // q_full, k_full[NK], k_empty[NK], s_ready[2], dp_ready[2], ds_ready[2], dq_done[2], mma_done
   static constexpr int NBAR = 1 + 2 * NK + 9;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;
   static constexpr int THREADS = 352;
-  // dP double-buffered (slot = kv tile & 1); dS~ overwrites it in place
-  static constexpr int COL_S = 0, COL_DP0 = 128, COL_DQ = 256, COL_DP1 = 384;
-  static_assert(COL_DQ + D <= COL_DP1 && COL_DP1 + 128 <= 512, "TMEM budget");
+  // S and dP double-buffered (slot = kv tile & 1); dS~ overwrites the slot's first dP columns
+  static constexpr int COL_S0 = 0, COL_S1 = 64, COL_DP0 = 128, COL_DP1 = 192, COL_DQ = 256;
+  static_assert(COL_DQ + D <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum QF8Site { kF8QQ = 0x70, kF8QKFull, kF8QKEmpty, kF8QS, kF8QDP, kF8QDS, kF8QDone, kF8QDrain, kF8QSFree, kF8QDqDone };
+enum QF8Site { kF8QQ = 0x70, kF8QKFull, kF8QKEmpty, kF8QS, kF8QDP, kF8QDS, kF8QDone, kF8QDrain, kF8QDqDone };
 
 template <int D>
 __global__ void __launch_bounds__(352, 1)
@@ -514,12 +515,11 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* k_empty = k_full + C::NK;
-  uint64_t* s_ready = k_empty + C::NK;
-  uint64_t* dp_ready = s_ready + 1;  // [2] per slot
-  uint64_t* ds_ready = s_ready + 3;  // [2]
-  uint64_t* mma_done = s_ready + 5;
-  uint64_t* s_free = s_ready + 6;
-  uint64_t* dq_done = s_ready + 7;   // [2]
+  uint64_t* s_ready = k_empty + C::NK;  // [2] per slot
+  uint64_t* dp_ready = s_ready + 2;     // [2]
+  uint64_t* ds_ready = s_ready + 4;     // [2]
+  uint64_t* dq_done = s_ready + 6;      // [2]
+  uint64_t* mma_done = s_ready + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -540,14 +540,13 @@ __global__ void __launch_bounds__(352, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
-    mbar_init(s_ready, 1);
     for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_ready[k], 1);
       mbar_init(&dp_ready[k], 1);
-      mbar_init(&ds_ready[k], 256);
+      mbar_init(&ds_ready[k], 128);  // one warpgroup per slot
       mbar_init(&dq_done[k], 1);
     }
     mbar_init(mma_done, 2);
-    mbar_init(s_free, 256);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -567,16 +566,16 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmKT);
-      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
       tma_load_4d(smem + C::OFF_Q, &tmQ, q_full, 0, h, m0, b);
       tma_load_4d(smem + C::OFF_DO, &tmDO, q_full, 0, h, m0, b);
       for (int n = 0; n < nj; ++n) {
-        const int j = jlo + n, sk = n % C::NK;
+        const int j0 = (jlo + n) * C::BN, sk = n % C::NK;
         if (!mbar_wait(&k_empty[sk], ((n / C::NK) & 1) ^ 1, err, kF8QKEmpty)) break;
-        mbar_arrive_expect_tx(&k_full[sk], 3 * C::TILE);
-        tma_load_4d(smem + C::OFF_K + sk * C::TILE, &tmK, &k_full[sk], 0, hk, j * C::BN, b);
-        tma_load_4d(smem + C::OFF_V + sk * C::TILE, &tmV, &k_full[sk], 0, hk, j * C::BN, b);
-        tma_load_4d(smem + C::OFF_KT + sk * C::TILE, &tmKT, &k_full[sk], j * C::BN, 0, hk, b);
+        mbar_arrive_expect_tx(&k_full[sk], 3 * C::K_TILE);
+        tma_load_4d(smem + C::OFF_K + sk * C::K_TILE, &tmK, &k_full[sk], 0, hk, j0, b);
+        tma_load_4d(smem + C::OFF_V + sk * C::K_TILE, &tmV, &k_full[sk], 0, hk, j0, b);
+        tma_load_4d(smem + C::OFF_KT + sk * C::K_TILE, &tmKT, &k_full[sk], j0, 0, hk, b);
       }
       mbar_wait(q_full, 0, err, kF8QDrain);
       for (int s = 0; s < C::NK && s < nj; ++s) {
@@ -585,34 +584,32 @@ __global__ void __launch_bounds__(352, 1)
       }
     }
   } else if (warp == 8 || warp == 10) {
-    //   A (warp 8):  S(n) = Q K_n^T, dP(n) = dO V_n^T
-    //   B (warp 10): dQ += dS~(n) K_n (K read as K^T, d rows x 128 keys)
+    //   A (warp 8):  S(n) = Q K_n^T and dP(n) = dO V_n^T into slot n & 1
+    //   B (warp 10): dQ += dS~(n) K_n (K read as K^T, d rows x 64 keys)
     if (nj > 0) {
-      constexpr uint32_t idS = idesc_f8_f32(128, 128, kF8E4M3, kF8E4M3);
-      constexpr uint32_t idP = idesc_f8_f32(128, 128, kF8E5M2, kF8E4M3);
+      constexpr uint32_t idS = idesc_f8_f32(128, C::BN, kF8E4M3, kF8E4M3);
+      constexpr uint32_t idP = idesc_f8_f32(128, C::BN, kF8E5M2, kF8E4M3);
       constexpr uint32_t idQ = idesc_f8_f32(128, D, kF8E5M2, kF8E4M3);
       bool ok = mbar_wait_warp(q_full, 0, err, kF8QQ);
       if (warp == 8) {
         const uint64_t dQ0 = desc_rows(smem_u32(smem + C::OFF_Q), D);
         const uint64_t dDO0 = desc_rows(smem_u32(smem + C::OFF_DO), D);
         for (int n = 0; n < nj && ok; ++n) {
-          const int sk = n % C::NK;
+          const int sk = n % C::NK, slot = n & 1;
           ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kF8QKFull);
-          if (ok && n > 0) ok = mbar_wait_warp(s_free, (n - 1) & 1, err, kF8QSFree);
+          // the slot's S and dP were last used by tile n - 2, whose dQ product read its dS~
+          // after the compute warps had taken S(n - 2) and dP(n - 2) into registers
+          if (ok && n >= 2) ok = mbar_wait_warp(&dq_done[slot], ((n >> 1) - 1) & 1, err, kF8QDqDone);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t dKa = desc_rows(smem_u32(smem + C::OFF_K + sk * C::TILE), D);
-          const uint64_t dVa = desc_rows(smem_u32(smem + C::OFF_V + sk * C::TILE), D);
+          const uint64_t dKa = desc_rows(smem_u32(smem + C::OFF_K + sk * C::K_TILE), D);
+          const uint64_t dVa = desc_rows(smem_u32(smem + C::OFF_V + sk * C::K_TILE), D);
+          const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
+          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8_warp(tmem + C::COL_S, desc_add(dQ0, kk * 32), desc_add(dKa, kk * 32), idS, kk > 0);
-          mma_commit_warp(s_ready);
-          // dP(n) reuses the slot of dP(n - 2): dQ(n - 2) must have read its dS~
-          const int slot = n & 1;
-          if (n >= 2) ok = mbar_wait_warp(&dq_done[slot], ((n >> 1) - 1) & 1, err, kF8QDqDone);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
+            mma_ss_f8_warp(colS, desc_add(dQ0, kk * 32), desc_add(dKa, kk * 32), idS, kk > 0);
+          mma_commit_warp(&s_ready[slot]);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
             mma_ss_f8_warp(colP, desc_add(dDO0, kk * 32), desc_add(dVa, kk * 32), idP, kk > 0);
@@ -625,14 +622,12 @@ __global__ void __launch_bounds__(352, 1)
                mbar_wait_warp(&ds_ready[slot], (n >> 1) & 1, err, kF8QDS);
           if (!ok) break;
           tc_fence_after();
-          // dS~ of keys 32 kk .. 32 kk + 31: warpgroup kk / 2 stored its 64 keys 4 per column from
-          // the slot's dP column + 64 (kk / 2)
-          const uint64_t dKT = desc_rows(smem_u32(smem + C::OFF_KT + sk * C::TILE), 128);
+          // dS~ of keys 32 kk .. 32 kk + 31 at the slot's dP column + 8 kk (4 keys per column)
+          const uint64_t dKT = desc_rows(smem_u32(smem + C::OFF_KT + sk * C::K_TILE), 64);
           const uint32_t colP = tmem + (slot ? C::COL_DP1 : C::COL_DP0);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 32; ++kk)
-            mma_ts_f8_warp(tmem + C::COL_DQ, colP + (kk / 2) * 64 + (kk % 2) * 8, desc_add(dKT, kk * 32), idQ,
-                           (n > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_f8_warp(tmem + C::COL_DQ, colP + 8 * kk, desc_add(dKT, kk * 32), idQ, (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dq_done[slot]);
           mma_commit_warp(&k_empty[sk]);  // S(n) / dP(n) (issuer A) completed before dS~(n) existed
         }
@@ -642,10 +637,13 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ dS warpgroups: thread = query row
-    const int w = warp / 4;  // keys 64w .. 64w+63 of each kv tile
+    // Ping-pong: warpgroup w takes the kv tiles n = w, w + 2, ... (TMEM slot w), all 64 keys of each.
+    const int w = warp / 4;
     const int r = (warp % 4) * 32 + lane;
     const int i = m0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const uint32_t colS = lane_addr + (w ? C::COL_S1 : C::COL_S0);
+    const uint32_t colP = lane_addr + (w ? C::COL_DP1 : C::COL_DP0);
     const float sl2 = p.scale_log2 * (*p.descale_q) * (*p.descale_k);
     const float s_ds = e5m2_scale_of(p.ds_amax);
     const float dsc = (*p.descale_do) * (*p.descale_v) * (s_ds * (1.f / kPScale));  // dP -> dP s / 2^8
@@ -658,20 +656,18 @@ __global__ void __launch_bounds__(352, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2row, nl2row);
     const uint64_t dsc2 = f2_pack(dsc, dsc), dr2 = f2_pack(drow, drow);
     bool ok = true;
-    for (int n = 0; n < nj && ok; ++n) {
-      const int k0 = (jlo + n) * C::BN + 64 * w;
-      ok = mbar_wait_warp(s_ready, n & 1, err, kF8QS);
+    for (int n = w; n < nj && ok; n += 2) {
+      const int k0 = (jlo + n) * C::BN;
+      const uint32_t ph = (n >> 1) & 1;
+      ok = mbar_wait_warp(&s_ready[w], ph, err, kF8QS);
       if (!ok) break;
       tc_fence_after();
-      const bool full = tile_fully_visible<false>(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
-      float pr[64];  // 2^8 P
+      float pr[64];  // 2^8 P of the row's 64 keys
       {
         uint32_t ra[32], rb[32];
-        tmem_ld32(lane_addr + C::COL_S + 64 * w, ra);
-        tmem_ld32(lane_addr + C::COL_S + 64 * w + 32, rb);
+        tmem_ld32(colS, ra);
+        tmem_ld32(colS + 32, rb);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(s_free);  // S is in registers: the next S may be written
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float xa, xb, xc, xd;
@@ -683,36 +679,40 @@ __global__ void __launch_bounds__(352, 1)
           pr[33 + c] = ex2(xd);
         }
       }
-      if (!full) {
+      if (!tile_fully_visible<false>(mask, m0, C::BM, k0, C::BN)) {
         int vlo, vhi;
         visible_keys<false>(mask, i, &vlo, &vhi);
 #pragma unroll
         for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
       }
-      const int slot = n & 1;
-      const uint32_t colP = slot ? C::COL_DP1 : C::COL_DP0;
-      ok = mbar_wait_warp(&dp_ready[slot], (n >> 1) & 1, err, kF8QDP);
+      ok = mbar_wait_warp(&dp_ready[w], ph, err, kF8QDP);
       if (!ok) break;
       tc_fence_after();
-      uint32_t d8[16];  // dS~: E5M2(s dS) of this row's 64 keys, 4 per TMEM column
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + colP + 64 * w + c0, rr);
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(colP, ra);
+        tmem_ld32(colP + 32, rb);
         tmem_ld_wait();
-        float ds[32];  // s dS = 2^8 P (dP s / 2^8 + D')
+        uint32_t d8[16];  // dS~: E5M2(s dS) of the row's 64 keys, 4 per TMEM column
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const uint64_t t = f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), dsc2, dr2);
-          f2_unpack(f2_mul(f2_pack(pr[c0 + c], pr[c0 + c + 1]), t), ds[c], ds[c + 1]);
+        for (int c = 0; c < 32; c += 4) {
+          float y[8];  // s dS = 2^8 P (dP s / 2^8 + D')
+          f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]),
+                           f2_fma(f2_pack(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), dsc2, dr2)), y[0], y[1]);
+          f2_unpack(f2_mul(f2_pack(pr[c + 2], pr[c + 3]),
+                           f2_fma(f2_pack(__uint_as_float(ra[c + 2]), __uint_as_float(ra[c + 3])), dsc2, dr2)), y[2], y[3]);
+          f2_unpack(f2_mul(f2_pack(pr[32 + c], pr[33 + c]),
+                           f2_fma(f2_pack(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), dsc2, dr2)), y[4], y[5]);
+          f2_unpack(f2_mul(f2_pack(pr[34 + c], pr[35 + c]),
+                           f2_fma(f2_pack(__uint_as_float(rb[c + 2]), __uint_as_float(rb[c + 3])), dsc2, dr2)), y[6], y[7]);
+          d8[c / 4] = pack_e5m2x4(y[0], y[1], y[2], y[3]);
+          d8[8 + c / 4] = pack_e5m2x4(y[4], y[5], y[6], y[7]);
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d8[c0 / 4 + q] = pack_e5m2x4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
+        tmem_st16(colP, d8);
+        tmem_st_wait();
       }
-      tmem_st16(lane_addr + colP + 64 * w, d8);
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ds_ready[slot]);
+      mbar_arrive(&ds_ready[w]);
     }
     // epilogue: dQ = scale * descale_k / s * acc; warpgroup w writes head dims [w D/2, (w+1) D/2)
     bool have = false;

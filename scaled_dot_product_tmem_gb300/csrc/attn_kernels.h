@@ -134,10 +134,10 @@ int launch_bwd_q_dropout(int d_qk, int d_v, const CUtensorMap& tq, const CUtenso
 // FP8 backward (E4M3 Q, K, V; E5M2 dO), d_qk = d_v = d in {64, 128}, full-length batches:
 // the preprocess (D from the dequantised dO8 and the bf16 O), the kv-stationary kernel (dK,
 // dV) and the query-stationary kernel (dQ).  Maps: tq8/tk8/tv8/tdo8 natural BSHD codes
-// (boxes of the whole head dim x 64 rows for Q/dO, x 128 rows for K/V); tqt8/tdot8 the
-// transposed Q / dO codes [B, H_q, d, S_pad] (boxes of 64 queries x d); tkt8 the transposed
-// K codes [B, H_kv, d, S_pad] (boxes of 128 keys x d); tq8_128/tdo8_128 the natural Q/dO
-// with 128-row boxes for the dQ kernel.
+// (boxes of the whole head dim x 64 rows for Q/dO, x 128 rows for K/V in the kv kernel, x 64
+// rows for K/V in the dQ kernel); tqt8/tdot8 the transposed Q / dO codes [B, H_q, d, S_pad]
+// (boxes of 64 queries x d); tkt8 the transposed K codes [B, H_kv, d, S_pad] (boxes of 64
+// keys x d); tq8_128/tdo8_128 the natural Q/dO with 128-row boxes for the dQ kernel.
 int launch_bwd_preprocess_fp8(int d, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_kv_fp8(int d, const CUtensorMap& tq8, const CUtensorMap& tk8, const CUtensorMap& tv8,
                       const CUtensorMap& tdo8, const CUtensorMap& tqt8, const CUtensorMap& tdot8, const BwdParams& p,
