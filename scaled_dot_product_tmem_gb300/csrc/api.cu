@@ -274,10 +274,17 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.bias_sb = bsb;
   p.bias_sh = bsh;
+  // head dims up to 128 stage the bias tiles by TMA when the rows are whole 16-byte units
+  CUtensorMap tb;
+  p.bias_tma = bias && d_qk <= 128 && S_kv > 0 && S_kv % 8 == 0 ? 1 : 0;
+  if (p.bias_tma && !sdpa::make_bias_map_sw128(&tb, bias, bias_B, bias_H, S_q, S_kv)) {
+    set_error("cuTensorMapEncodeTiled (bias)");
+    return ATTN_ERR_CUDA;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = timed(ATTN_KERNEL_FWD, 1, s, [&] {
     return p.drop_t ? sdpa::launch_attn_fwd_dropout(d_qk, d_v, tq, tk, tv, p, s)
-                    : sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s);
+                    : sdpa::launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, s, p.bias_tma ? &tb : nullptr);
   });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {

@@ -7,15 +7,17 @@
 
 namespace sdpa {
 
+// The forward's two staged bias tiles take 64 KB of shared memory: at d = 128 one V stage
+// makes room for them.
 int launch_attn_fwd_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, cudaStream_t stream) {
+                         const FwdParams& p, cudaStream_t stream, const CUtensorMap* tb) {
   const bool vl = p.seq_q || p.seq_kv;
   if (d_qk == 128 && d_v == 128)
-    return vl ? launch_fwd_t<128, 128, 2, 2, true, false, true>(tq, tk, tv, p, stream)
-              : launch_fwd_t<128, 128, 2, 2, false, false, true>(tq, tk, tv, p, stream);
+    return vl ? launch_fwd_t<128, 128, 2, 1, true, false, true>(tq, tk, tv, p, stream, tb)
+              : launch_fwd_t<128, 128, 2, 1, false, false, true>(tq, tk, tv, p, stream, tb);
   if (d_qk == 64 && d_v == 64)
-    return vl ? launch_fwd_t<64, 64, 4, 4, true, false, true>(tq, tk, tv, p, stream)
-              : launch_fwd_t<64, 64, 4, 4, false, false, true>(tq, tk, tv, p, stream);
+    return vl ? launch_fwd_t<64, 64, 4, 4, true, false, true>(tq, tk, tv, p, stream, tb)
+              : launch_fwd_t<64, 64, 4, 4, false, false, true>(tq, tk, tv, p, stream, tb);
   if (d_qk == 192 && d_v == 128)
     return vl ? launch_fwd_t<192, 128, 2, 1, true, false, true>(tq, tk, tv, p, stream)
               : launch_fwd_t<192, 128, 2, 1, false, false, true>(tq, tk, tv, p, stream);

@@ -17,8 +17,8 @@ static int launch_attn_fwd_vl(int d_qk, int d_v, const CUtensorMap& tq, const CU
 }
 
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                    const FwdParams& p, cudaStream_t stream) {
-  if (p.bias) return launch_attn_fwd_bias(d_qk, d_v, tq, tk, tv, p, stream);  // attn_bias.cu
+                    const FwdParams& p, cudaStream_t stream, const CUtensorMap* tb) {
+  if (p.bias) return launch_attn_fwd_bias(d_qk, d_v, tq, tk, tv, p, stream, tb);  // attn_bias.cu
   // padded batches get the instantiation with the per-entry lengths and row tests
   return (p.seq_q || p.seq_kv) ? launch_attn_fwd_vl<true>(d_qk, d_v, tq, tk, tv, p, stream)
                                : launch_attn_fwd_vl<false>(d_qk, d_v, tq, tk, tv, p, stream);

@@ -54,7 +54,8 @@
 
 namespace sdpa {
 
-template <int D_QK, int D_V, int NK, int NV, bool F8 = false>
+// BT: the bias tiles of the two query tiles are staged in shared memory by TMA.
+template <int D_QK, int D_V, int NK, int NV, bool F8 = false, bool BT = false>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   // bf16: boxes of 64 head dims (one 128-byte swizzle row each); E4M3: one box of
@@ -68,10 +69,14 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
   static constexpr int OFF_V = OFF_K + NK * K_STAGE;
-  static constexpr int OFF_BAR = OFF_V + NV * V_STAGE;
+  // bias tile of one query tile: 128 rows x 128 keys bf16, as two 64-key boxes with
+  // 128-byte swizzle (row r's 16-byte chunk c at chunk c ^ (r % 8) of its 128-byte row)
+  static constexpr int B_BOX = 128 * 128, B_TILE = 2 * B_BOX;
+  static constexpr int OFF_B = OFF_V + NV * V_STAGE;
+  static constexpr int OFF_BAR = OFF_B + (BT ? 2 * B_TILE : 0);
   // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready[2], p_ready[2], o_done[2], mma_done,
-  // q_empty
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 8;
+  // q_empty, then (BT) b_full[2], b_empty[2]
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 8 + (BT ? 4 : 0);
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_TMEM_SLOT + 16 + 1024;
   // at least 117 KB so that one CTA per SM holds the 512 TMEM columns
@@ -116,13 +121,20 @@ __device__ __forceinline__ FwdTile fwd_tile(const FwdParams& p, int nqb, int wi)
   return T;
 }
 
-enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain };
+enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteS, kSiteP, kSiteO, kSiteDrain,
+               kSiteBFull, kSiteBEmpty };
+
+// Bias tiles staged by TMA for head dims up to 128 (the MLA dims keep the per-row loads).
+template <int D_QK, bool BIAS>
+constexpr bool fwd_bias_staged() { return BIAS && D_QK <= 128; }
 
 template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false, bool BIAS = false, bool DROP = false>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D_QK, D_V, NK, NV, F8>;
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                    const FwdParams p) {
+  constexpr bool BT = fwd_bias_staged<D_QK, BIAS>();
+  using C = FwdCfg<D_QK, D_V, NK, NV, F8, BT>;
   static_assert(!DROP || (!F8 && !BIAS && !VL), "dropout: full-length bf16 batches without a bias");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -137,7 +149,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* o_done = p_ready + 2;
   uint64_t* mma_done = o_done + 2;
   uint64_t* q_empty = mma_done + 1;
+  [[maybe_unused]] uint64_t* b_full = q_empty + 1;  // [2] (BT)
+  [[maybe_unused]] uint64_t* b_empty = b_full + 2;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+  // the bias tiles are staged only when the rows are whole 16-byte units (S_kv % 8 == 0)
+  [[maybe_unused]] const bool b_tma = BT && p.bias_tma;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nqb = (p.S_q + 2 * C::BM - 1) / (2 * C::BM);
@@ -154,6 +170,12 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_done, 1);
+    if constexpr (BT) {
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(&b_full[t], 1);
+        mbar_init(&b_empty[t], C::BM);
+      }
+    }
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -174,7 +196,9 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      if (b_tma) tma_prefetch_desc(&tmB);
       int n = 0, nw = 0;  // kv stages loaded, Q tiles loaded
+      [[maybe_unused]] int nb[2] = {0, 0};  // bias tiles loaded per query tile
       bool ok = true;
       for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
         const FwdTile T = fwd_tile<C::BM, C::BN, VL>(p, nqb, wi);
@@ -198,6 +222,27 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < C::QCH; ++c)
             tma_load_4d(smem + C::OFF_K + sk * C::K_STAGE + c * C::CHUNK, &tmK, &k_full[sk], c * 64, T.hk,
                         j * C::BN, T.b);
+          if constexpr (BT) {
+            // each query tile's bias tile for kv tile j, once its softmax has read the last one
+            // (ahead of V(j), which is only needed after that softmax); the next one is
+            // prefetched into L2 meanwhile
+            const int hb = p.bias_sh ? T.h : 0, bb = p.bias_sb ? T.b : 0;
+#pragma unroll
+            for (int t = 0; t < 2 && b_tma; ++t) {
+              if (!T.active[t] || j < T.jlo[t] || j > T.jhi[t]) continue;
+              ok = mbar_wait(&b_empty[t], (nb[t] & 1) ^ 1, err, kSiteBEmpty);
+              if (!ok) break;
+              const int r0 = T.m0 + t * C::BM;
+              mbar_arrive_expect_tx(&b_full[t], C::B_TILE);
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_4d(smem + C::OFF_B + t * C::B_TILE + hf * C::B_BOX, &tmB, &b_full[t], j * C::BN + 64 * hf,
+                            r0, hb, bb);
+              if (j < T.jhi[t])
+                for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_4d(&tmB, (j + 1) * C::BN + 64 * hf, r0, hb, bb);
+              ++nb[t];
+            }
+          }
+          if (!ok) break;
           ok = mbar_wait(&v_empty[sv], ((n / NV) & 1) ^ 1, err, kSiteVEmpty);
           if (!ok) break;
           mbar_arrive_expect_tx(&v_full[sv], C::V_STAGE);
@@ -220,6 +265,9 @@ __global__ void __launch_bounds__(320, 1)
         const int last = s + ((n - 1 - s) / NV) * NV;
         mbar_wait(&v_full[s], (last / NV) & 1, err, kSiteDrain);
       }
+      if constexpr (BT)
+        for (int t = 0; t < 2; ++t)
+          if (nb[t] > 0) mbar_wait(&b_full[t], (nb[t] - 1) & 1, err, kSiteDrain);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
@@ -339,6 +387,8 @@ __global__ void __launch_bounds__(320, 1)
     const float sx = BIAS ? 1.f : sl2;
     const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
+    [[maybe_unused]] int nbc = 0;  // bias tiles consumed (BT)
+    [[maybe_unused]] const uint8_t* btile = smem + C::OFF_B + t * C::B_TILE + r * 128;  // this row, first box
     bool ok = true;
     for (int wi = blockIdx.x; wi < n_work && ok; wi += gridDim.x) {
       const FwdTile T = fwd_tile<C::BM, C::BN, VL>(p, nqb, wi);
@@ -369,6 +419,16 @@ __global__ void __launch_bounds__(320, 1)
               keep[q] = dropout_row_span16(drop, b, h, i, j * C::BN + 32 * q) |
                         (dropout_row_span16(drop, b, h, i, j * C::BN + 32 * q + 16) << 16);
           }
+          if (BIAS && !b_tma) {
+            // this row's bias for the next kv tile (and, on the first, this one) into L2
+            // while the scores are computed, so the loads below do not wait on DRAM
+            for (int jj = (it == 0 ? j : j + 1); jj <= min(j + 1, my_jhi); ++jj) {
+              const int ka = jj * C::BN, kz = min(ka + C::BN, p.S_kv) - 1;
+              prefetch_l2(brow + ka);
+              prefetch_l2(brow + min(ka + 64, kz));
+              prefetch_l2(brow + kz);
+            }
+          }
           ok = mbar_wait_warp(&s_ready[t], sc & 1, err, kSiteS);
           ++sc;
           if (!ok) break;
@@ -387,23 +447,44 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(rr[c]);
           }
           const int k0 = j * C::BN;
+          if constexpr (BT) {
+            if (b_tma) {
+              ok = mbar_wait_warp(&b_full[t], nbc & 1, err, kSiteBFull);
+              ++nbc;
+              if (!ok) break;
+            }
+          }
           if constexpr (BIAS) {
+            const uint64_t sl2x2b = f2_pack(sl2, sl2), l2e2b = f2_pack(kLog2e, kLog2e);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float m = -INFINITY;
 #pragma unroll
               for (int e8 = 0; e8 < 4; ++e8) {
                 float bv[8];
-                load_bias8(brow, k0 + 32 * q + 8 * e8, p.S_kv, bias_vec, bv);
+                if (b_tma) {  // chunk (32 q + 8 e8) / 8 of the row: box q / 2, chunk 4 (q % 2) + e8 of 8
+                  const uint4 w = *reinterpret_cast<const uint4*>(
+                      btile + (q / 2) * C::B_BOX + (((4 * (q % 2) + e8) ^ (r & 7)) << 4));
+                  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  float& x = s[32 * q + 8 * e8 + e];
-                  x = fmaf(bv[e], kLog2e, x * sl2);
-                  m = fmaxf(m, x);
+                  for (int u = 0; u < 4; ++u) {
+                    bv[2 * u] = __uint_as_float(ws[u] << 16);
+                    bv[2 * u + 1] = __uint_as_float(ws[u] & 0xFFFF0000u);
+                  }
+                } else {
+                  load_bias8(brow, k0 + 32 * q + 8 * e8, p.S_kv, bias_vec, bv);
+                }
+                // t = s sl2 + bias log2(e), two keys per paired multiply and fma
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  float* x = &s[32 * q + 8 * e8 + e];
+                  f2_unpack(f2_fma(f2_pack(x[0], x[1]), sl2x2b, f2_mul(f2_pack(bv[e], bv[e + 1]), l2e2b)), x[0], x[1]);
+                  m = fmax3(m, x[0], x[1]);
                 }
               }
               cmax[q] = m;
             }
+            if (b_tma) mbar_arrive(&b_empty[t]);  // the tile's bias is in registers
           }
           if (!tile_fully_visible<VL>(mask, m0 + t * C::BM, C::BM, k0, C::BN)) {
             // the keys this row sees form one interval [vlo, vhi], so a chunk whose two
@@ -540,8 +621,8 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D_QK, int D_V, int NK, int NV, bool VL, bool F8 = false, bool BIAS = false, bool DROP = false>
 inline int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                        cudaStream_t stream) {
-  using C = FwdCfg<D_QK, D_V, NK, NV, F8>;
+                        cudaStream_t stream, const CUtensorMap* tb = nullptr) {
+  using C = FwdCfg<D_QK, D_V, NK, NV, F8, fwd_bias_staged<D_QK, BIAS>()>;
   auto kern = attn_fwd_kernel<D_QK, D_V, NK, NV, VL, F8, BIAS, DROP>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -558,7 +639,7 @@ inline int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   }
   const long long n_work = (long long)((p.S_q + 2 * C::BM - 1) / (2 * C::BM)) * p.H_q * p.B;
   const unsigned grid = (unsigned)(n_work < n_sm ? n_work : n_sm);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tb ? *tb : tq, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -25,6 +25,7 @@ struct FwdParams {
   // (0 along a broadcast dim)
   const __nv_bfloat16* bias = nullptr;
   long long bias_sb = 0, bias_sh = 0;
+  int bias_tma = 0;  // head dims <= 128: the bias tiles are staged by TMA (S_kv % 8 == 0)
   // attention dropout (drop_t > 0): rng = device [seed, offset] (the Philox key), drop
   // threshold t (16-bit uniforms below it are dropped), kept values scaled by drop_scale
   const unsigned long long* rng = nullptr;
@@ -34,8 +35,9 @@ struct FwdParams {
 
 // Returns 0 on a successful launch, -2 for an unsupported (d_qk, d_v), -1 on a
 // CUDA launch error.
+// tb: the bias map (boxes of 64 keys x 128 rows, 128-byte swizzle) when p.bias_tma, else null.
 int launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                    const FwdParams& p, cudaStream_t stream);
+                    const FwdParams& p, cudaStream_t stream, const CUtensorMap* tb = nullptr);
 // E4M3 forward, d_qk = d_v = d in {64, 128}; tvt maps V^T [B, H_kv, d, S_kv_pad].
 int launch_attn_fwd_fp8(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                         const FwdParams& p, cudaStream_t stream);
@@ -114,7 +116,7 @@ bool bwd_kv_supports_fused_dq(int d_qk, int d_v);
 // Bias instantiations (full-length or padded batches, bf16; (d_qk, d_v) in {(64, 64),
 // (128, 128), (192, 128)}; the fused dQ for 64 and 128): the same contracts as above.
 int launch_attn_fwd_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, cudaStream_t stream);
+                         const FwdParams& p, cudaStream_t stream, const CUtensorMap* tb);
 int launch_bwd_kv_bias(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tb, const BwdParams& p,
                        bool fuse_dq, cudaStream_t stream);

@@ -73,6 +73,22 @@ inline bool make_bias_map(CUtensorMap* m, const void* base, int Bb, int Hb, int 
   return r == CUDA_SUCCESS;
 }
 
+// The same bias as boxes of 64 keys (128 bytes) x 128 query rows with 128-byte swizzle:
+// row r's 16-byte chunk c lands at chunk c ^ (r % 8) of its 128-byte row, so a warp that
+// reads one chunk of 32 consecutive rows touches every bank once per 8 rows.
+inline bool make_bias_map_sw128(CUtensorMap* m, const void* base, int Bb, int Hb, int S_q, int S_kv) {
+  PFN_encodeTiled enc = get_encode_tiled();
+  if (!enc || S_kv % 8 != 0) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)S_kv, (cuuint64_t)S_q, (cuuint64_t)Hb, (cuuint64_t)Bb};
+  cuuint64_t strides[3] = {(cuuint64_t)S_kv * 2, (cuuint64_t)S_q * S_kv * 2, (cuuint64_t)Hb * S_q * S_kv * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // An E4M3 BSHD tensor [B, S, H, D] (D = 64 or 128 bytes per row) as a 4-D TMA
 // tensor (d, h, s, b) with a box of the whole head dim x 1 head x `box_rows` rows
 // x 1 batch, swizzled by the row length (128-byte or 64-byte swizzle).
