@@ -173,25 +173,23 @@ def fp8_cast_launches(wl):
 
 
 def recorded_traffic(wl, kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
-    that summary is for another workload or the kernel sources changed since."""
+    """DRAM bytes per launch of `kernel` from the committed ncu record of this workload,
+    or None when there is none or the kernel sources it names changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "kernel_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    kernels = d.get("kernels", {}) if d.get("workload") == wl["name"] else \
-        d.get("other_workloads", {}).get(wl["name"], {})
-    if kernel not in kernels:
+        rec = json.load(f).get("workloads", {}).get(wl["name"])
+    if not rec or kernel not in rec.get("kernels", {}):
         return None
     h = hashlib.sha256()
-    for s in d["sources"]:
-        with open(os.path.join(ROOT, s), "rb") as f:
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
             h.update(f.read())
-    if h.hexdigest() != d["sources_sha256"]:
+    if h.hexdigest() != rec["sources_sha256"]:
         return None
-    k = kernels[kernel]
+    k = rec["kernels"][kernel]
     return k["dram_bytes_read"] + k["dram_bytes_write"]
 
 
