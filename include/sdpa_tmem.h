@@ -102,7 +102,8 @@ size_t attn_bwd_workspace_size(int B, int S_q, int S_kv, int H_q, int H_kv, int 
  * (fp32, summed over batch and rows; NULL is allowed for the other types and is
  * then not written; for them a non-NULL d_offset receives zeros).
  * deterministic != 0: bitwise-reproducible results (dQ by a query-stationary
- * recompute pass); 0: dQ may be accumulated with fp32 atomics where supported.
+ * recompute pass); 0: dQ accumulated with fp32 reductions for (d_qk, d_v) = (64, 64)
+ * and (128, 128); the other head dims take the deterministic path either way.
  * workspace: device scratch of at least attn_bwd_workspace_size() bytes.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
