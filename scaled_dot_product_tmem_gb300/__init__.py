@@ -605,26 +605,44 @@ def sdpa_backward(q, k, v, o, dout, lse, *, causal=True, window=-1, softmax_type
 
 
 class SDPAFunction(torch.autograd.Function):
-    """autograd wrapper: forward/backward both run in the library's kernels."""
+    """autograd wrapper: forward and backward both run in the library's kernels (the
+    plain, padded-batch, bias and dropout entry points, chosen by the arguments)."""
 
     @staticmethod
-    def forward(ctx, q, k, v, softmax_offset, causal, window, softmax_type, scale, deterministic):
-        o, lse = sdpa_forward(q, k, v, causal=causal, window=window, softmax_type=softmax_type,
-                              softmax_offset=softmax_offset, scale=scale)
-        ctx.save_for_backward(q, k, v, o, lse, softmax_offset)
-        ctx.cfg = (causal, window, softmax_type, scale, deterministic)
+    def forward(ctx, q, k, v, softmax_offset, bias, causal, window, softmax_type, scale, deterministic,
+                seq_lens_q, seq_lens_kv, dropout_p, rng_state):
+        kw = dict(causal=causal, window=window, softmax_type=softmax_type, scale=scale, seq_lens_q=seq_lens_q,
+                  seq_lens_kv=seq_lens_kv, dropout_p=dropout_p, rng_state=rng_state)
+        o, lse = sdpa_forward(q, k, v, softmax_offset=softmax_offset, bias=bias, **kw)
+        ctx.save_for_backward(q, k, v, o, lse, softmax_offset, bias)
+        ctx.kw = dict(kw, deterministic=deterministic)
         return o
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, o, lse, off = ctx.saved_tensors
-        causal, window, st, scale, det = ctx.cfg
-        dq, dk, dv, d_off = sdpa_backward(q, k, v, o, dout.contiguous(), lse, causal=causal, window=window,
-                                          softmax_type=st, softmax_offset=off, scale=scale, deterministic=det)
-        return dq, dk, dv, d_off, None, None, None, None, None
+        q, k, v, o, lse, off, bias = ctx.saved_tensors
+        res = sdpa_backward(q, k, v, o, dout.contiguous(), lse, softmax_offset=off, bias=bias, **ctx.kw)
+        dq, dk, dv, d_off = res[:4]
+        dbias = None
+        if bias is not None and ctx.needs_input_grad[4]:
+            dbias = res[4] if bias.dtype == torch.float32 else res[4].to(bias.dtype)  # autograd wants bias's dtype
+        return dq, dk, dv, d_off, dbias, None, None, None, None, None, None, None, None, None
+
+
+def new_rng_state(device=None):
+    """A fresh dropout rng_state: a CUDA int64 [seed, offset] with a seed drawn from
+    torch's default generator and offset 0."""
+    seed = int(torch.randint(0, 2 ** 62, (1,)).item())
+    return torch.tensor([seed, 0], dtype=torch.int64, device=device or "cuda")
 
 
 def attention(q, k, v, softmax_offset=None, *, causal=True, window=-1, softmax_type=VANILLA, scale=0.0,
-              deterministic=True):
-    """Differentiable fused attention (q, k, v and the learnable offset receive gradients)."""
-    return SDPAFunction.apply(q, k, v, softmax_offset, causal, window, softmax_type, scale, deterministic)
+              deterministic=True, bias=None, seq_lens_q=None, seq_lens_kv=None, dropout_p=0.0, rng_state=None):
+    """Differentiable fused attention. q, k, v, the learnable offset and the bias receive
+    gradients. seq_lens_q / seq_lens_kv (int32 [B] on the device) make it a padded batch;
+    dropout_p > 0 applies attention dropout with rng_state (a fresh one when None; the
+    backward regenerates the same decisions from it)."""
+    if dropout_p and rng_state is None:
+        rng_state = new_rng_state(q.device)
+    return SDPAFunction.apply(q, k, v, softmax_offset, bias, causal, window, softmax_type, scale, deterministic,
+                              seq_lens_q, seq_lens_kv, dropout_p, rng_state)
