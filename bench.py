@@ -158,18 +158,19 @@ def kernel_flops(wl, cls, fused):
 def fp8_cast_bytes(wl):
     """Bytes the FP8 casts of one step must move, read bf16 (2 B per element) and write
     codes (1 B; transposed rows padded to 16): Q, K (BSHD) and V (transposed) for the
-    forward; for a training step also Q^T, K^T, V (BSHD) and dO, dO^T."""
+    forward; a training step reads Q, K, V and dO once each and writes both layouts of
+    all four (dO in E5M2)."""
     B, S, Hq, Hkv, d = wl["B"], wl["S"], wl["Hq"], wl["Hkv"], wl["dqk"]
     Sp = (S + 15) // 16 * 16
     nq, nk = B * S * Hq * d, B * S * Hkv * d
     nqt, nkt = B * Hq * d * Sp, B * Hkv * d * Sp
-    fwd = 2 * (nq + 2 * nk) + nq + nk + nkt
     if not wl.get("fp8_train"):
-        return fwd
-    return fwd + 2 * (nq + 2 * nk) + nqt + nkt + nk + 2 * (2 * nq) + nq + nqt
+        return 2 * (nq + 2 * nk) + nq + nk + nkt
+    return 2 * (2 * nq + 2 * nk) + 2 * (nq + nqt) + 2 * (nk + nkt)
+
 
 def fp8_cast_launches(wl):
-    return 8 if wl.get("fp8_train") else 3
+    return 4 if wl.get("fp8_train") else 3
 
 
 def recorded_traffic(wl, kernel):
@@ -369,9 +370,9 @@ def bench_config(wl, world, det):
     fp8 = bool(wl.get("fp8"))
     return {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["S"],
             "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
-            **({"step": "E4M3 casts of Q, K, V and E5M2 casts of dO, BSHD and transposed (delayed scaling, "
-                        "amax recorded in the cast) + attn_fwd_fp8 + attn_bwd_fp8 (dS scaled by the previous "
-                        "step's max |dS|)"} if wl.get("fp8_train") else
+            **({"step": "E4M3 casts of Q, K, V and an E5M2 cast of dO, each writing BSHD and transposed "
+                        "codes from one read (delayed scaling, amax recorded in the cast) + attn_fwd_fp8 + "
+                        "attn_bwd_fp8 (dS scaled by the previous step's max |dS|)"} if wl.get("fp8_train") else
                {"step": "E4M3 casts of Q, K, V (delayed scaling, amax recorded in the cast) + attn_fwd_fp8"}
                if fp8 else {"bwd_path": "deterministic (query-stationary dQ)" if det else "fp32 atomic dQ"}),
             "l2": "flushed between timed steps (258 MB write outside the timed span)",
@@ -434,13 +435,13 @@ def _step_fns_fp8(sdpa, wl, dev, x):
         sdpa.attn_fp8_amax(t[n], amax[n][0])      # the history before the first step
     u8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=dev)
     x8 = {"q": u8(B, S, Hq, d), "k": u8(B, S, Hkv, d), "vt": u8(B, Hkv, d, Sp)}
-    # (tensor, code buffer, transposed, E5M2): the first cast of a tensor records its amax
-    casts = [("q", "q", False, False), ("k", "k", False, False), ("v", "vt", True, False)]
-    if train:
+    # (tensor, code buffer, transposed, E5M2, BSHD buffer written by the same pass or None)
+    casts = [("q", "q", False, False, None), ("k", "k", False, False, None), ("v", "vt", True, False, None)]
+    if train:  # every tensor in both layouts from one read
         x8.update(qt=u8(B, Hq, d, Sp), kt=u8(B, Hkv, d, Sp), v=u8(B, S, Hkv, d), do=u8(B, S, Hq, d),
                   dot=u8(B, Hq, d, Sp))
-        casts += [("q", "qt", True, False), ("k", "kt", True, False), ("v", "v", False, False),
-                  ("dout", "do", False, True), ("dout", "dot", True, True)]
+        casts = [("q", "qt", True, False, "q"), ("k", "kt", True, False, "k"), ("v", "vt", True, False, "v"),
+                 ("dout", "dot", True, True, "do")]
     o = torch.empty((B, S, Hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     kw = dict(causal=wl["causal"], window=wl["window"], softmax_type=wl["st"], scale=wl["scale"] or 0.0)
@@ -453,11 +454,13 @@ def _step_fns_fp8(sdpa, wl, dev, x):
         outs = (o, dq, dk, dv)
 
     def step():
-        seen = set()
-        for n, buf, tr, e5 in casts:
-            quant = sdpa.attn_fp8_quantize_e5m2 if e5 else sdpa.attn_fp8_quantize
-            quant(t[n], x8[buf], amax[n][0], desc[n], transpose=tr, amax_out=None if n in seen else amax[n][1])
-            seen.add(n)
+        for n, buf, tr, e5, nat in casts:
+            if nat is not None:
+                sdpa.attn_fp8_quantize_both(t[n], x8[nat], x8[buf], amax[n][0], desc[n], e5m2=e5,
+                                            amax_out=amax[n][1])
+            else:
+                quant = sdpa.attn_fp8_quantize_e5m2 if e5 else sdpa.attn_fp8_quantize
+                quant(t[n], x8[buf], amax[n][0], desc[n], transpose=tr, amax_out=amax[n][1])
         for n in t:
             amax[n].reverse()                      # this step's amax scales the next step
         sdpa.attn_fwd_fp8(x8["q"], x8["k"], x8["vt"], desc["q"], desc["k"], desc["v"], o, lse, **kw)

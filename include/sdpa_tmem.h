@@ -350,6 +350,15 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* d
  */
 int attn_fp8_quantize_e5m2(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
                            float* descale, float* amax_out, void* stream);
+/*
+ * attn_fp8_quantize_both: both layouts of one cast from a single read of x: x8 [B, S, H, d]
+ * (BSHD) and x8t [B, H, d, attn_fp8_vt_row_bytes(S)] (transposed), E4M3 (e5m2 = 0) or E5M2
+ * (e5m2 != 0), with the same codes, scale, descale and amax_out as the two separate calls
+ * of attn_fp8_quantize / attn_fp8_quantize_e5m2.  d = 64 or 128; x8 and x8t distinct and
+ * 16-byte aligned.  Errors as attn_fp8_quantize.
+ */
+int attn_fp8_quantize_both(const void* x, void* x8, void* x8t, int B, int S, int H, int d, int e5m2,
+                           const float* amax, float* descale, float* amax_out, void* stream);
 size_t attn_bwd_fp8_workspace_size(int B, int S_q, int H_q);
 int attn_bwd_fp8(const void* q8, const void* k8, const void* v8, const void* do8, const void* qt8, const void* kt8,
                  const void* dot8, const float* descale_q, const float* descale_k, const float* descale_v,

@@ -103,6 +103,8 @@ def _load():
     lib.attn_bwd_dropout.restype = i
     lib.attn_fp8_quantize_e5m2.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.attn_fp8_quantize_e5m2.restype = i
+    lib.attn_fp8_quantize_both.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.attn_fp8_quantize_both.restype = i
     lib.attn_bwd_fp8_workspace_size.argtypes = [i, i, i]
     lib.attn_bwd_fp8_workspace_size.restype = sz
     lib.attn_bwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
@@ -426,6 +428,43 @@ def attn_fp8_quantize_e5m2(x, x8, amax, descale, *, transpose=False, amax_out=No
     _fp8_quantize("attn_fp8_quantize_e5m2", x, x8, amax, descale, transpose, amax_out, stream)
 
 
+def attn_fp8_quantize_both(x, x8, x8t, amax, descale, *, e5m2=False, amax_out=None, stream=None):
+    """One read of x, both layouts: x8 BSHD [B,S,H,d] and x8t [B,H,d,S_pad] (uint8), E4M3 or
+    (e5m2=True) E5M2, with the same codes as the two separate casts."""
+    _check(x, "x", torch.bfloat16, 4)
+    _check(x8, "x8", torch.uint8, 4)
+    _check(x8t, "x8t", torch.uint8, 4)
+    _check(amax, "amax", torch.float32, 1)
+    _check(descale, "descale", torch.float32, 1)
+    B, S, H, d = x.shape
+    if tuple(x8.shape) != (B, S, H, d):
+        raise ValueError(f"x8 must have shape {(B, S, H, d)}, got {tuple(x8.shape)}")
+    want = (B, H, d, attn_fp8_vt_row_bytes(S))
+    if tuple(x8t.shape) != want:
+        raise ValueError(f"x8t must have shape {want}, got {tuple(x8t.shape)}")
+    if amax_out is not None:
+        _check(amax_out, "amax_out", torch.float32, 1)
+    st = _load().attn_fp8_quantize_both(_ptr(x), _ptr(x8), _ptr(x8t), B, S, H, d, int(bool(e5m2)), _ptr(amax),
+                                        _ptr(descale), _ptr(amax_out), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fp8_quantize_both")
+
+
+def fp8_quantize_both(x, *, amax=None, amax_out=None, fmt="e4m3", stream=None):
+    """fp8_quantize in both layouts from one read: returns (x8, x8t, amax, descale)."""
+    if fmt not in ("e4m3", "e5m2"):
+        raise ValueError(f"fmt must be 'e4m3' or 'e5m2', got {fmt!r}")
+    B, S, H, d = x.shape
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+        attn_fp8_amax(x, amax, stream=stream)
+    x8 = torch.empty((B, S, H, d), dtype=torch.uint8, device=x.device)
+    x8t = torch.empty((B, H, d, attn_fp8_vt_row_bytes(S)), dtype=torch.uint8, device=x.device)
+    descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    attn_fp8_quantize_both(x, x8, x8t, amax, descale, e5m2=(fmt == "e5m2"), amax_out=amax_out, stream=stream)
+    return x8, x8t, amax, descale
+
+
 def attn_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, *, causal=True, window=-1,
                  softmax_type=VANILLA, softmax_offset=None, scale=0.0, stream=None):
     """E4M3 forward into preallocated o [B,S_q,H_q,d] bf16 and lse [B,H_q,S_q] fp32.
@@ -546,13 +585,10 @@ def sdpa_backward_fp8(q, k, v, o, dout, lse, *, ds_amax=None, ds_amax_out=None, 
     dS scaling statistic (fp32 [1] device tensor, e.g. the max of an amax history);
     None runs the backward twice, the first time only to record this step's max |dS|.
     Returns (dq, dk, dv, d_offset)."""
-    q8, aq, sq = fp8_quantize(q, stream=stream)
-    k8, ak, sk = fp8_quantize(k, stream=stream)
+    q8, qt8, _, sq = fp8_quantize_both(q, stream=stream)
+    k8, kt8, _, sk = fp8_quantize_both(k, stream=stream)
     v8, _, sv = fp8_quantize(v, stream=stream)
-    do8, ado, sdo = fp8_quantize(dout, fmt="e5m2", stream=stream)
-    qt8, _, _ = fp8_quantize(q, transpose=True, amax=aq, stream=stream)
-    kt8, _, _ = fp8_quantize(k, transpose=True, amax=ak, stream=stream)
-    dot8, _, _ = fp8_quantize(dout, transpose=True, amax=ado, fmt="e5m2", stream=stream)
+    do8, dot8, _, sdo = fp8_quantize_both(dout, fmt="e5m2", stream=stream)
     B, S_q, H_q, d = q.shape
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)

@@ -558,11 +558,12 @@ int attn_fp8_amax(const void* x, size_t n, float* amax, void* stream) {
 }
 
 static int fp8_quantize_impl(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
-                             float* descale, float* amax_out, void* stream, bool e5m2) {
+                             float* descale, float* amax_out, void* stream, bool e5m2, void* x8_nat = nullptr) {
   if (B < 0 || S < 0 || H <= 0 || d <= 0 || d % 8 != 0 || !amax || !descale) return ATTN_ERR_INVALID_ARG;
   if (transpose && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((size_t)B * S * H * d > 0 && (!x || !x8)) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
+  if (x8_nat && (x8_nat == x8 || !transpose)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x8) || !aligned16(x8_nat) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
       (reinterpret_cast<uintptr_t>(descale) & 3u) || (reinterpret_cast<uintptr_t>(amax_out) & 3u))
     return ATTN_ERR_MISALIGNED;
   if (amax_out && (amax_out == amax || amax_out == descale)) return ATTN_ERR_INVALID_ARG;
@@ -570,7 +571,8 @@ static int fp8_quantize_impl(const void* x, void* x8, int B, int S, int H, int d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int rc = timed(ATTN_KERNEL_FP8_QUANT, 1, s, [&] {
     return sdpa::launch_fp8_quantize(static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(x8), B, S, H, d,
-                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, amax_out, s, e5m2);
+                                     transpose != 0, attn_fp8_vt_row_bytes(S), amax, descale, amax_out, s, e5m2,
+                                     static_cast<uint8_t*>(x8_nat));
   });
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) {
@@ -588,6 +590,12 @@ int attn_fp8_quantize(const void* x, void* x8, int B, int S, int H, int d, int t
 int attn_fp8_quantize_e5m2(const void* x, void* x8, int B, int S, int H, int d, int transpose, const float* amax,
                            float* descale, float* amax_out, void* stream) {
   return fp8_quantize_impl(x, x8, B, S, H, d, transpose, amax, descale, amax_out, stream, true);
+}
+
+int attn_fp8_quantize_both(const void* x, void* x8, void* x8t, int B, int S, int H, int d, int e5m2,
+                           const float* amax, float* descale, float* amax_out, void* stream) {
+  if ((size_t)B * S * H * d > 0 && !x8) return ATTN_ERR_INVALID_ARG;
+  return fp8_quantize_impl(x, x8t, B, S, H, d, 1, amax, descale, amax_out, stream, e5m2 != 0, x8);
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* descale_q, const float* descale_k,

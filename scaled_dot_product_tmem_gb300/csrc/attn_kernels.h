@@ -46,9 +46,11 @@ int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t 
 // x8 = E4M3(x * scale), scale = 448 / amax[0] (1 if amax is 0 or not finite),
 // descale[0] = 1 / scale.  transpose: x [B, S, H, d] -> x8 [B, H, d, S_pad].
 // amax_out (may be null): receives max |x| of this tensor, recorded during the cast.
-// e5m2: E5M2 codes with scale = 57344 / amax instead.
+// e5m2: E5M2 codes with scale = 57344 / amax instead.  x8_nat (transpose only, may be
+// null): the same codes in x's BSHD layout as well, from the same read of x.
 int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2 = false);
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2 = false,
+                        uint8_t* x8_nat = nullptr);
 
 struct BwdParams {
   int B, S_q, S_kv, H_q, H_kv, G;

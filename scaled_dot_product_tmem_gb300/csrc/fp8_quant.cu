@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint4* __restrict_
 // row (key-major) in shared memory.  Phase 2 gives each thread 4 head dims x 16 keys:
 // sixteen 4-byte reads, 4 x 4 byte transposes with byte permutes, and one 16-byte
 // store per head dim into V^T (keys past S are zeros; keys past S_pad are not written).
+// out_nat (may be null): the same codes in the input's own BSHD layout, written in phase 1,
+// so one read of x gives both layouts.
 template <int D, bool E5>
 __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ out,
                                                           int S, int H, int S_pad, const float* __restrict__ amax,
-                                                          float* __restrict__ descale, unsigned* __restrict__ amax_out) {
+                                                          float* __restrict__ descale, unsigned* __restrict__ amax_out,
+                                                          uint8_t* __restrict__ out_nat) {
   constexpr int KT = 128;          // keys per tile
   constexpr int ROW = D + 4;       // bytes per key row in shared memory (4-byte aligned, skews the banks)
   __shared__ __align__(16) uint8_t tile[KT * ROW];
@@ -136,6 +139,8 @@ __global__ void __launch_bounds__(256) fp8_quant_t_kernel(const __nv_bfloat16* _
     uint32_t* dst = reinterpret_cast<uint32_t*>(tile + kk * ROW + d0);
     dst[0] = lo;
     dst[1] = hi;
+    if (out_nat && key < S)
+      *reinterpret_cast<uint2*>(out_nat + (((size_t)b * S + key) * H + h) * D + d0) = make_uint2(lo, hi);
   }
   block_amax(m, amax_out);
   __syncthreads();
@@ -181,7 +186,7 @@ int launch_fp8_amax(const __nv_bfloat16* x, size_t n, float* amax, cudaStream_t 
 
 template <bool E5>
 static int quantize_t(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                      const float* amax, float* descale, unsigned* ao, cudaStream_t stream) {
+                      const float* amax, float* descale, unsigned* ao, cudaStream_t stream, uint8_t* x8_nat) {
   const size_t n = (size_t)B * S * H * d;
   if (!transpose) {
     fp8_quant_kernel<E5><<<grid_for(n / 8), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), x,
@@ -190,9 +195,9 @@ static int quantize_t(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, 
     const long long blocks = (long long)((S_pad + 127) / 128) * H * B;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
     if (d == 128)
-      fp8_quant_t_kernel<128, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
+      fp8_quant_t_kernel<128, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao, x8_nat);
     else if (d == 64)
-      fp8_quant_t_kernel<64, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao);
+      fp8_quant_t_kernel<64, E5><<<(unsigned)blocks, 256, 0, stream>>>(x, x8, S, H, S_pad, amax, descale, ao, x8_nat);
     else
       return -2;
   }
@@ -200,11 +205,13 @@ static int quantize_t(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, 
 }
 
 int launch_fp8_quantize(const __nv_bfloat16* x, uint8_t* x8, int B, int S, int H, int d, bool transpose, int S_pad,
-                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2) {
+                        const float* amax, float* descale, float* amax_out, cudaStream_t stream, bool e5m2,
+                        uint8_t* x8_nat) {
   unsigned* ao = reinterpret_cast<unsigned*>(amax_out);
   if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return -1;
-  return e5m2 ? quantize_t<true>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream)
-              : quantize_t<false>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream);
+  if (x8_nat && !transpose) return -2;
+  return e5m2 ? quantize_t<true>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream, x8_nat)
+              : quantize_t<false>(x, x8, B, S, H, d, transpose, S_pad, amax, descale, ao, stream, x8_nat);
 }
 
 }  // namespace sdpa

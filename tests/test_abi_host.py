@@ -225,3 +225,18 @@ def test_fp8_backward_argument_validation(lib):
     assert qz(desc=None) == INVALID
     assert qz(x=MIS) == MISALIGNED
     assert qz(B=0) == OK
+
+
+def test_fp8_quantize_both_argument_validation(lib):
+    """attn_fp8_quantize_both needs two distinct outputs and the transposed layout's head
+    dims (64 or 128)."""
+    Q = ctypes.c_void_p(0x20000)
+
+    def qb(x=P, x8=P, x8t=Q, B=1, S=64, H=2, d=128, e5=0, amax=P, desc=ctypes.c_void_p(0x30000)):
+        return lib.attn_fp8_quantize_both(x, x8, x8t, B, S, H, d, e5, amax, desc, None, None)
+
+    assert qb(x8t=P) == INVALID                         # the two layouts may not share a buffer
+    assert qb(x8=None) == INVALID
+    assert qb(d=96) == UNSUPPORTED
+    assert qb(x8=MIS) == MISALIGNED
+    assert qb(B=0) == OK

@@ -76,6 +76,29 @@ def test_quantize_with_a_given_amax_and_saturation(transpose):
     assert rec.item() == float(np.abs(x.float().numpy()).max())
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("shape", [(2, 200, 3, 64), (1, 77, 2, 128)])
+def test_quantize_both_layouts_in_one_pass(shape, fmt):
+    """attn_fp8_quantize_both writes the BSHD and the transposed codes from one read: both
+    equal the oracle's casts, with the same descale and the tensor's amax recorded."""
+    sdpa = _sdpa()
+    B, S, H, d = shape
+    x = make_inputs(Shape(B, S, S, H, H, d, d), 13)["q"] * 2.0
+    rec = torch.full((1,), 7.0, dtype=torch.float32, device="cuda")
+    x8, x8t, amax, descale = sdpa.fp8_quantize_both(x.cuda(), fmt=fmt, amax_out=rec)
+    torch.cuda.synchronize()
+    _check_device()
+    xf = x.float().numpy()
+    codes, a_ref, d_ref = fp8.quantize(xf, fmt=fmt)
+    codes_t, _, _ = fp8.quantize(xf, fmt=fmt, transpose=True)
+    assert amax.item() == a_ref and descale.item() == d_ref
+    assert rec.item() == float(np.abs(xf).max())
+    assert np.array_equal(x8.cpu().numpy(), codes)
+    got_t = x8t.cpu().numpy()
+    assert not got_t[..., S:].any()
+    assert np.array_equal(got_t[..., :S], codes_t)
+
+
 def _oracle_fp8(x, *, causal, window, softmax_type, scale, rows=None):
     """The oracle's own quantisation of the bf16 inputs, then the exact forward of the
     dequantised tensors and the P-rounding bound."""
