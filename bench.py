@@ -101,6 +101,11 @@ WORKLOADS["fp8_fwd_gqa_b4_s8192_d128"] = _w(
 WORKLOADS["fp8_train_gqa_b4_s8192_d128"] = _w(
     "fp8_train_gqa_b4_s8192_d128", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 43,
     "FP8 training step (E4M3 Q/K/V, E5M2 dO/dS): B=4, S=8192, H_q=32, H_kv=8, d=128, causal", fp8_train=True)
+# The same step at the FP8 example's shape (MHA, d = 64).
+WORKLOADS["fp8_train_mha_b4_s2048_d64"] = _w(
+    "fp8_train_mha_b4_s2048_d64", 4, 2048, 8, 8, 64, 64, True, -1, 0, None, 46,
+    "FP8 training step (E4M3 Q/K/V, E5M2 dO/dS): B=4, S=2048, H=8 (MHA), d=64, causal (the FP8 example's shape)",
+    fp8_train=True)
 # The same step at B=1: the small case its kernels are profiled on (inputs above L2, < 1 GB held).
 WORKLOADS["fp8_train_gqa_b1_s8192_d128"] = _w(
     "fp8_train_gqa_b1_s8192_d128", 1, 8192, 32, 8, 128, 128, True, -1, 0, None, 44,

@@ -190,14 +190,16 @@ def test_fp8_backward_is_deterministic():
         assert np.array_equal(a[n], b[n]), n
 
 
-# The FP8 training shape: causal GQA at S = 8192, d = 128 (B = 4, 32 query heads, 8
+# The FP8 training shapes: causal GQA at S = 8192, d = 128 (B = 4, 32 query heads, 8
 # kv heads), checked on one kv-head group: every query head's dQ on sampled rows and
-# the group's dK, dV on sampled keys.  The checked unit gets the oracle's forward;
+# the group's dK, dV on sampled keys; and the FP8 example's MHA shape, on all rows.  The checked unit gets the oracle's forward;
 # every other unit gets the GPU's FP8 forward (its outputs do not reach the checked
 # unit's gradients).
 FULL = [
     ("fp8_gqa_b4_s8192_d128", Shape(4, 8192, 8192, 32, 8, 128, 128), 43, (1, 6),
      np.r_[0:48, 2040:2056, 5000:5016, 8160:8192], np.r_[0:32, 4096:4112, 8176:8192]),
+    # the FP8 example's shape (MHA, d = 64), every row and key of one (batch, head)
+    ("fp8_mha_b4_s2048_d64", Shape(4, 2048, 2048, 8, 8, 64, 64), 45, (3, 5), np.arange(2048), np.arange(2048)),
 ]
 
 
