@@ -131,6 +131,24 @@ def test_fp8_backward_parity(case):
         assert np.all(got["d_offset"] == 0.0)
 
 
+@pytest.mark.parametrize("stat", [0.0, float("inf"), float("nan")], ids=["zero", "inf", "nan"])
+def test_fp8_backward_degenerate_ds_statistic(stat):
+    """A dS statistic that is 0 or not finite (no history yet, or an overflowed one) scales
+    dS by 1, on both sides, and the call still records this step's max |dS|."""
+    shape = Shape(1, 160, 160, 2, 1, 64, 64)
+    x = make_inputs(shape, 611)
+    kw = dict(causal=True, window=-1, softmax_type=VANILLA, offset=None, scale=None)
+    c = _oracle_inputs(x)
+    o, lse = _fwd(c, **kw)
+    codes = (c["q"], c["k"], c["v"], c["dout"], c["s_q"], c["s_k"], c["s_v"], c["s_dout"])
+    on, ln = o.double().numpy(), lse.double().numpy()
+    ref = fp8.attention_bwd_fp8(*codes, on, ln, np.float32(stat), **kw)
+    bnd = fp8_bwd_bounds(*codes, on, ln, np.float32(stat), **kw)
+    got = _gpu_bwd(c, o, lse, stat, **kw)
+    check_fp8_bwd(got, ref, bnd, f"stat {stat}")
+    assert abs(got["amax"][0] - ref["amax_ds"]) <= bnd["amax_ds"] + 2.0 ** -24 * ref["amax_ds"]
+
+
 def test_fp8_backward_empty_sides():
     """No keys: dQ = 0 (every row is empty, so D = 0 and nothing flows); no queries:
     dK = dV = 0; the recorded max |dS| is 0 either way."""
