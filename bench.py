@@ -178,15 +178,17 @@ def fp8_cast_launches(wl):
     return 4 if wl.get("fp8_train") else 3
 
 
-def recorded_traffic(wl, kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu record of this workload,
-    or None when there is none or the kernel sources it names changed since."""
+def recorded_traffic(wl, kernel, det=False):
+    """DRAM bytes per launch of `kernel` from the committed ncu record of this workload
+    (the deterministic backward's kernels have records of their own), or None when there
+    is none or the kernel sources it names changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "kernel_traffic.json")
     if not os.path.exists(p):
         return None
+    key = wl["name"] + (":deterministic" if det and not wl.get("fp8") else "")
     with open(p) as f:
-        rec = json.load(f).get("workloads", {}).get(wl["name"])
+        rec = json.load(f).get("workloads", {}).get(key)
     if not rec or kernel not in rec.get("kernels", {}):
         return None
     h = hashlib.sha256()
@@ -678,7 +680,7 @@ def ours_arm(args, wl, world, rank, local):
             "fwd_tflop": flops(wl, "fwd") / 1e12, "bwd_tflop": flops(wl, "bwd") / 1e12,
             "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "peak_source": peak_desc,
-                         "traffic": recorded_traffic(wl, dom), "traffic_unit": "bytes per launch (ncu DRAM read+write)"},
+                         "traffic": recorded_traffic(wl, dom, det), "traffic_unit": "bytes per launch (ncu DRAM read+write)"},
             "kernels": kernels,
             "kernel_split": f"a second pass of {min(args.steps, 10)} steps with CUDA events around every launch",
             "gpu_launches": launches,

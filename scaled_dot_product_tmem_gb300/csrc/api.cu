@@ -453,7 +453,17 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     set_error("cuTensorMapEncodeTiled (bias)");
     return ATTN_ERR_CUDA;
   }
+  // the query-stationary dQ kernel's maps (128-row boxes); the deterministic path's kv
+  // kernel uses them too where its 128-row-step form applies
+  CUtensorMap tq128 = tq, tdo128 = tdo;
+  if (!fused && (!sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
+                 !sdpa::make_bshd_map(&tdo128, dout, B, S_q, H_q, d_v, 128))) {
+    set_error("cuTensorMapEncodeTiled (backward operands, 128 rows)");
+    return ATTN_ERR_CUDA;
+  }
+  const bool wide = !fused && !bias && !p.drop_t && sdpa::bwd_kv_wide_supported(d_qk, d_v);
   int rc = timed(ATTN_KERNEL_BWD_KV, 1, s, [&] {
+    if (wide) return sdpa::launch_bwd_kv_wide(d_qk, d_v, tq128, tk, tv, tdo128, p, s);
     return p.drop_t ? sdpa::launch_bwd_kv_dropout(d_qk, d_v, tq, tk, tv, tdo, tdq, tb, p, fused, s)
                     : sdpa::launch_bwd_kv(d_qk, d_v, tq, tk, tv, tdo, tdq, tb, p, fused, s);
   });
@@ -473,10 +483,6 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
       return ATTN_ERR_CUDA;
     }
   } else {
-    CUtensorMap tq128, tdo128;
-    if (!sdpa::make_bshd_map(&tq128, q, B, S_q, H_q, d_qk, 128) ||
-        !sdpa::make_bshd_map(&tdo128, dout, B, S_q, H_q, d_v, 128))
-      return ATTN_ERR_CUDA;
     rc = timed(ATTN_KERNEL_BWD_Q, 1, s, [&] {
       return p.drop_t ? sdpa::launch_bwd_q_dropout(d_qk, d_v, tq128, tk, tv, tdo128, p, s)
                       : sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);

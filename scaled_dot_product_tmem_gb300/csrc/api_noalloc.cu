@@ -179,7 +179,10 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
     snprintf(g_msg, sizeof(g_msg), "attn_bwd_noalloc: cuTensorMapEncodeTiled failed");
     return ATTN_ERR_CUDA;
   }
-  int rc = sdpa::launch_bwd_kv(d_qk, d_v, tq64, tk, tv, tdo64, tq64, tq64, p, false, s);
+  // the same kv kernel as attn_bwd's deterministic path
+  int rc = sdpa::bwd_kv_wide_supported(d_qk, d_v)
+               ? sdpa::launch_bwd_kv_wide(d_qk, d_v, tq128, tk, tv, tdo128, p, s)
+               : sdpa::launch_bwd_kv(d_qk, d_v, tq64, tk, tv, tdo64, tq64, tq64, p, false, s);
   if (rc == -2) return ATTN_ERR_UNSUPPORTED;
   if (rc != 0) return launch_failed("backward kv kernel launch");
   rc = sdpa::launch_bwd_q(d_qk, d_v, tq128, tk, tv, tdo128, p, s);

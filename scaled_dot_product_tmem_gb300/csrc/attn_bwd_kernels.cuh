@@ -579,17 +579,20 @@ struct QCfg {
   static constexpr int OFF_K = OFF_DO + VCH * CHUNK;
   static constexpr int OFF_V = OFF_K + NK * QCH * CHUNK;
   static constexpr int OFF_BAR = OFF_V + NV * VCH * CHUNK;
-  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready, ds_ready, mma_done,
-  // s_free, dq_done
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 6;
+  // dP^T slots: two where TMEM has room beside dQ (d_qk <= 128), so that dP(n+1) runs
+  // while dS(n) is formed and dQ(n) reads it; one at d_qk = 192
+  static constexpr int DPB = D_QK <= 128 ? 2 : 1;
+  // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready[DPB],
+  // ds_ready[DPB], mma_done, s_free, dq_done[DPB]
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 3 + 3 * DPB;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
   static constexpr int THREADS = 352;
   // dS (bf16) is written over the dP columns, so the next S can be computed as soon
-  // as the dS warps have loaded the current S.
-  static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256;
-  static_assert(COL_DQ + D_QK <= 512, "TMEM budget");
+  // as the dS warps have loaded the current S.  Tile n uses dP slot n % DPB.
+  static constexpr int COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DP1 = COL_DQ + D_QK;
+  static_assert(COL_DQ + D_QK + (DPB - 1) * 128 <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -611,11 +614,11 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* v_full = k_empty + C::NK;
   uint64_t* v_empty = v_full + C::NV;
   uint64_t* s_ready = v_empty + C::NV;
-  uint64_t* dp_ready = s_ready + 1;
-  uint64_t* ds_ready = s_ready + 2;
-  uint64_t* mma_done = s_ready + 3;
-  uint64_t* s_free = s_ready + 4;
-  uint64_t* dq_done = s_ready + 5;
+  uint64_t* dp_ready = s_ready + 1;         // [DPB], per dP slot
+  uint64_t* ds_ready = dp_ready + C::DPB;   // [DPB]
+  uint64_t* mma_done = ds_ready + C::DPB;
+  uint64_t* s_free = mma_done + 1;
+  uint64_t* dq_done = s_free + 1;           // [DPB]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -643,11 +646,13 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < C::NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     mbar_init(s_ready, 1);
-    mbar_init(dp_ready, 1);
-    mbar_init(ds_ready, 256);
+    for (int d = 0; d < C::DPB; ++d) {
+      mbar_init(&dp_ready[d], 1);
+      mbar_init(&ds_ready[d], 256);
+      mbar_init(&dq_done[d], 1);
+    }
     mbar_init(mma_done, 2);
     mbar_init(s_free, 256);
-    mbar_init(dq_done, 1);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -693,10 +698,12 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
-    //   A (warp 8):  S(n) = Q K_n^T, dP(n) = dO V_n^T
+    //   A (warp 8):  S(n) = Q K_n^T, dP(n) = dO V_n^T into dP slot n % DPB
     //   B (warp 10): dQ += dS(n) K_n
-    // S(n+1) waits for the dS warps to have loaded S(n) (s_free); dP(n+1) waits
-    // for dQ(n), which reads dS(n) from the dP columns (dq_done).
+    // S(n+1) waits for the dS warps to have loaded S(n) (s_free); dP(n) waits for
+    // dQ(n - DPB), which read dS(n - DPB) from the same slot (dq_done of that slot).
+    // Every per-slot barrier completes once per use of its slot, and a slot's next use
+    // depends on the waiter having seen the previous one, so no phase is skipped.
     if (nj > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idDQ = idesc_bf16_f32(128, D_QK, false, true);
@@ -719,31 +726,36 @@ __global__ void __launch_bounds__(352, 1)
             mma_ss_warp(tmem + C::COL_S, desc_add(dQ0, off), desc_add(dKa, off), idS, kk > 0);
           }
           mma_commit_warp(s_ready);
+          const int ds = n % C::DPB;
           ok = mbar_wait_warp(&v_full[sv], (n / C::NV) & 1, err, kQVFull);
-          if (ok && n > 0) ok = mbar_wait_warp(dq_done, (n - 1) & 1, err, kQDqDone);
+          if (ok && n >= C::DPB) ok = mbar_wait_warp(&dq_done[ds], ((n / C::DPB) - 1) & 1, err, kQDqDone);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t colP = tmem + (ds ? C::COL_DP1 : C::COL_DP);
 #pragma unroll
           for (int kk = 0; kk < D_V / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-            mma_ss_warp(tmem + C::COL_DP, desc_add(dDO0, off), desc_add(dVa, off), idS, kk > 0);
+            mma_ss_warp(colP, desc_add(dDO0, off), desc_add(dVa, off), idS, kk > 0);
           }
-          mma_commit_warp(dp_ready);
+          mma_commit_warp(&dp_ready[ds]);
           mma_commit_warp(&v_empty[sv]);
         }
       } else {
         for (int n = 0; n < nj && ok; ++n) {
           const int sk = n % C::NK;
           const uint64_t dKmn = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, C::CHUNK, 1024);
-          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull) && mbar_wait_warp(ds_ready, n & 1, err, kQDS);
+          const int ds = n % C::DPB;
+          ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull) &&
+               mbar_wait_warp(&ds_ready[ds], (n / C::DPB) & 1, err, kQDS);
           if (!ok) break;
           tc_fence_after();
-          // dQ += dS K   (dS bf16 over the dP columns: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
+          // dQ += dS K   (dS bf16 over the slot's dP columns: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
+          const uint32_t colP = tmem + (ds ? C::COL_DP1 : C::COL_DP);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts_warp(tmem + C::COL_DQ, tmem + C::COL_DP + (kk / 4) * 64 + (kk % 4) * 8, desc_add(dKmn, kk * 2048),
+            mma_ts_warp(tmem + C::COL_DQ, colP + (kk / 4) * 64 + (kk % 4) * 8, desc_add(dKmn, kk * 2048),
                    idDQ, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_warp(dq_done);
+          mma_commit_warp(&dq_done[ds]);
           mma_commit_warp(&k_empty[sk]);  // S(n) (issuer A) completed before dS(n) existed
         }
       }
@@ -832,14 +844,16 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
       }
-      ok = mbar_wait_warp(dp_ready, n & 1, err, kQDP);
+      const int ds = n % C::DPB;
+      const uint32_t colP = ds ? C::COL_DP1 : C::COL_DP;
+      ok = mbar_wait_warp(&dp_ready[ds], (n / C::DPB) & 1, err, kQDP);
       if (!ok) break;
       tc_fence_after();
       const uint64_t drow2 = f2_pack(drow, drow);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 64 * w + c0, rr);
+        tmem_ld32(lane_addr + colP + 64 * w + c0, rr);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -859,11 +873,11 @@ __global__ void __launch_bounds__(352, 1)
           }
           pk[c] = pack_bf16x2(a, bq);
         }
-        tmem_st16(lane_addr + C::COL_DP + 64 * w + c0 / 2, pk);
+        tmem_st16(lane_addr + colP + 64 * w + c0 / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive(&ds_ready[ds]);
     }
     // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2)
     bool have = false;

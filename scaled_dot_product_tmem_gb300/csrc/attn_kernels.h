@@ -110,6 +110,12 @@ int launch_bwd_kv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& t
 int bwd_kv_head_splits(int B, int S_kv, int H_kv, int G);
 // ns > 1: dK, dV (bf16) = the sum of the ns fp32 partial slices, in slice order.
 int launch_bwd_kv_combine(int d_qk, int d_v, const BwdParams& p, cudaStream_t stream);
+// dK/dV only, with 128-row query steps (the deterministic path's kv kernel where it
+// applies): d_qk = d_v in {64, 128}, no bias, no dropout; tq128/tdo128 have boxes of 64
+// columns x 128 rows.  -2 when not applicable (the 64-row kernel is used then).
+bool bwd_kv_wide_supported(int d_qk, int d_v);
+int launch_bwd_kv_wide(int d_qk, int d_v, const CUtensorMap& tq128, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo128, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_q(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 int launch_bwd_dq_convert(int d_qk, const BwdParams& p, cudaStream_t stream);
