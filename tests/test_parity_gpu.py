@@ -110,13 +110,23 @@ def test_empty_problem_is_a_noop():
     assert torch.all(dk == 0) and torch.all(dv == 0)
 
 
-def test_deterministic_bwd_is_bitwise_reproducible():
+@pytest.mark.parametrize("shape, lens", [
+    (Shape(2, 333, 333, 8, 2, 128, 128), None),
+    (Shape(3, 260, 260, 8, 1, 64, 64), [260, 131, 7]),   # d = 64, MQA, padded batch
+], ids=["d128_gqa_window", "d64_mqa_padded"])
+def test_deterministic_bwd_is_bitwise_reproducible(shape, lens):
+    """Two deterministic backward calls give the same bits.  Both cases have small kv
+    grids, so the query heads of a group are split across CTAs and the fp32 partial
+    slices are combined in slice order."""
     import scaled_dot_product_tmem_gb300 as sdpa
-    x = make_inputs(Shape(2, 333, 333, 8, 2, 128, 128), 7, learnable_offset=True)
+    x = make_inputs(shape, 7, learnable_offset=True)
     dev = torch.device("cuda")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     off = x["offset"].to(dev)
     kw = dict(causal=True, window=150, softmax_type=LEARNABLE, softmax_offset=off)
+    if lens is not None:
+        lt = torch.tensor(lens, dtype=torch.int32, device=dev)
+        kw.update(seq_lens_q=lt, seq_lens_kv=lt)
     o, lse = sdpa.sdpa_forward(q, k, v, **kw)
     a = sdpa.sdpa_backward(q, k, v, o, do, lse, deterministic=True, **kw)
     b = sdpa.sdpa_backward(q, k, v, o, do, lse, deterministic=True, **kw)
