@@ -65,10 +65,10 @@ struct KvCfg {
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, dq_ready, dq_free,
-  // mma_done, dv_done[2], dk_done.  Barriers of the double-buffered S slot are per slot: with
-  // two slots the P/dS warps can finish step s+1's P before issuer B has waited for step s's,
-  // and a single barrier would then complete two phases before B looks.
-  static constexpr int NBAR = 1 + 2 * NQ + 12;
+  // mma_done, dv_done[2], dk_done, kv_empty, acc_free, fin.  Barriers of the double-buffered S
+  // slot are per slot: with two slots the P/dS warps can finish step s+1's P before issuer B
+  // has waited for step s's, and a single barrier would then complete two phases before B looks.
+  static constexpr int NBAR = 1 + 2 * NQ + 15;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
@@ -89,9 +89,11 @@ struct KvCfg {
 constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's block order
 
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
-              kKvDvDone, kKvDkDone };
+              kKvDvDone, kKvDkDone, kKvEmpty, kKvAccFree };
 
-template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false, bool DROP = false>
+// PERSIST: the CTAs take every gridDim-th tile; otherwise the grid has one CTA per tile
+// and the tile loops below run once (the cross-tile barriers compile away).
+template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false, bool DROP = false, bool PERSIST = false>
 __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -114,30 +116,49 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   uint64_t* mma_done = s_ready + 8;
   uint64_t* dv_done = s_ready + 9;      // [2], per S slot
   uint64_t* dk_done = s_ready + 11;
+  uint64_t* kv_empty = s_ready + 12;    // a tile's K/V readers are done: the next K/V may load
+  uint64_t* acc_free = s_ready + 13;    // the epilogue has read dV/dK: the next tile may overwrite them
+  uint64_t* fin = s_ready + 14;         // every MMA issued, before TMEM is released
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order: groups (b, kv head) in chunks of kKvChunk; within a chunk, kv tile
-  // by kv tile (tile 0, the most work when causal, first) and group by group.  Blocks
-  // start in index order, so the long blocks of every chunk start early while the
-  // chunk's queries stay few enough to be shared in L2.
+  // Work tiles: (b, kv head, head split) groups in chunks of kKvChunk; within a chunk,
+  // kv tile by kv tile (tile 0, the most work when causal, first) and group by group,
+  // so a chunk's long tiles start early while its queries stay few enough to be shared
+  // in L2.  The CTAs are persistent (at most one per SM) and take every gridDim-th
+  // tile, so a tile's K/V load and first products overlap the previous tile's epilogue.
+  // Every role walks the same tiles and numbers the steps of all its tiles in one
+  // sequence g, which indexes the stages, slots and barrier phases.
   const int n_kv = (p.S_kv + C::BN - 1) / C::BN;
   const int n_gr = p.H_kv * p.B * p.ns;  // group = (b, kv head, head split)
+  const int n_tiles = n_kv * n_gr;
   const int per_chunk = kKvChunk * n_kv;
-  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
-  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
-  const int g = chunk * kKvChunk + within % csize;
-  const int split = g % p.ns, hk = (g / p.ns) % p.H_kv, b = g / (p.ns * p.H_kv);
-  const int Gs = p.G / p.ns;               // query heads this CTA walks
-  const int h0 = hk * p.G + split * Gs;    // the first of them
-  const int n0 = (within / csize) * C::BN;
-  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
-                                      p.window}
-                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
-  int ilo = 0, ihi = -1;
-  const bool any_q = q_tile_range(mask, n0, n0 + C::BN - 1, C::BQ, &ilo, &ihi);
-  const int nq = any_q ? ihi - ilo + 1 : 0;
-  const int nsteps = nq * Gs;
+  const int Gs = p.G / p.ns;  // query heads a tile walks
+  // tile stride of the loops: past the last tile after one pass without PERSIST
+  const int tstride = PERSIST ? (int)gridDim.x : n_tiles;
+  struct Tile {
+    int b, hk, split, h0, n0, ilo, nq, nsteps;
+    MaskSpec mask;
+  };
+  auto tile_of = [&](int ti) {
+    Tile t;
+    const int chunk = ti / per_chunk, within = ti % per_chunk;
+    const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
+    const int g = chunk * kKvChunk + within % csize;
+    t.split = g % p.ns;
+    t.hk = (g / p.ns) % p.H_kv;
+    t.b = g / (p.ns * p.H_kv);
+    t.h0 = t.hk * p.G + t.split * Gs;  // the first query head the tile walks
+    t.n0 = (within / csize) * C::BN;
+    t.mask = VL ? MaskSpec{entry_len(p.seq_q, t.b, p.S_q), entry_len(p.seq_kv, t.b, p.S_kv), p.causal, p.window}
+                : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
+    int ihi = -1;
+    t.ilo = 0;
+    const bool any_q = q_tile_range(t.mask, t.n0, t.n0 + C::BN - 1, C::BQ, &t.ilo, &ihi);
+    t.nq = any_q ? ihi - t.ilo + 1 : 0;
+    t.nsteps = t.nq * Gs;
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -154,6 +175,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     mbar_init(&dv_done[0], 1);
     mbar_init(&dv_done[1], 1);
     mbar_init(dk_done, 1);
+    mbar_init(kv_empty, FUSE_DQ ? 2 : 1);  // issuer A (S, dP) and, with the fused dQ, issuer B (K^T dS^T)
+    mbar_init(acc_free, 256);
+    mbar_init(fin, 2);
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -168,66 +192,92 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nsteps > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      const bool btma = BIAS && p.bias_tma;  // this stage also brings the step's bias tile
-      if (btma) tma_prefetch_desc(&tmB);
-      mbar_arrive_expect_tx(kv_full, (C::QCH + C::VCH) * C::KCHUNK);
-      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_K + c * C::KCHUNK, &tmK, kv_full, c * 64, hk, n0, b);
-      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_V + c * C::KCHUNK, &tmV, kv_full, c * 64, hk, n0, b);
-      for (int s = 0; s < nsteps; ++s) {
-        const int st = s % C::NQ;
-        if (!mbar_wait(&q_empty[st], ((s / C::NQ) & 1) ^ 1, err, kKvQEmpty)) break;
-        const int h = h0 + s / nq;
-        const int q0 = (ilo + s % nq) * C::BQ;
-        mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE + (btma ? C::B_STAGE : 0));
-        if (btma)  // rows past S_q and keys past S_kv come in as zeros
-          tma_load_4d(smem + C::OFF_B + st * C::B_STAGE, &tmB, &q_full[st], n0, q0, p.bias_sh ? h : 0,
-                      p.bias_sb ? b : 0);
+    if (lane == 0) {
+      const bool btma = BIAS && p.bias_tma;  // each stage also brings the step's bias tile
+      bool ok = true, first = true;
+      int g0 = 0, ne = 0;  // steps and non-empty tiles so far
+      for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {
+        const Tile t = tile_of(ti);
+        if (t.nsteps == 0) continue;
+        if (first) {
+          tma_prefetch_desc(&tmQ);
+          tma_prefetch_desc(&tmK);
+          tma_prefetch_desc(&tmV);
+          tma_prefetch_desc(&tmDO);
+          if (btma) tma_prefetch_desc(&tmB);
+          first = false;
+        }
+        // K/V of this tile replace the previous tile's once its S, dP (and dQ^T) products are done
+        if (PERSIST && ne > 0 && !mbar_wait(kv_empty, (ne - 1) & 1, err, kKvEmpty)) break;
+        mbar_arrive_expect_tx(kv_full, (C::QCH + C::VCH) * C::KCHUNK);
         for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(smem + C::OFF_Q + st * C::Q_STAGE + c * C::QCHUNK, &tmQ, &q_full[st], c * 64, h, q0, b);
+          tma_load_4d(smem + C::OFF_K + c * C::KCHUNK, &tmK, kv_full, c * 64, t.hk, t.n0, t.b);
         for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::OFF_DO + st * C::DO_STAGE + c * C::QCHUNK, &tmDO, &q_full[st], c * 64, h, q0, b);
-        const size_t row = ((size_t)b * p.H_q + h) * p.S_pad + q0;
-        bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.nlse2 + row, C::BQ * 4, &q_full[st]);
-        bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
+          tma_load_4d(smem + C::OFF_V + c * C::KCHUNK, &tmV, kv_full, c * 64, t.hk, t.n0, t.b);
+        for (int s = 0; s < t.nsteps; ++s) {
+          const int g = g0 + s, st = g % C::NQ;
+          if (!mbar_wait(&q_empty[st], ((g / C::NQ) & 1) ^ 1, err, kKvQEmpty)) {
+            ok = false;
+            break;
+          }
+          const int h = t.h0 + s / t.nq;
+          const int q0 = (t.ilo + s % t.nq) * C::BQ;
+          mbar_arrive_expect_tx(&q_full[st], C::Q_STAGE + C::DO_STAGE + C::L_STAGE + (btma ? C::B_STAGE : 0));
+          if (btma)  // rows past S_q and keys past S_kv come in as zeros
+            tma_load_4d(smem + C::OFF_B + st * C::B_STAGE, &tmB, &q_full[st], t.n0, q0, p.bias_sh ? h : 0,
+                        p.bias_sb ? t.b : 0);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(smem + C::OFF_Q + st * C::Q_STAGE + c * C::QCHUNK, &tmQ, &q_full[st], c * 64, h, q0, t.b);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::OFF_DO + st * C::DO_STAGE + c * C::QCHUNK, &tmDO, &q_full[st], c * 64, h, q0,
+                        t.b);
+          const size_t row = ((size_t)t.b * p.H_q + h) * p.S_pad + q0;
+          bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.nlse2 + row, C::BQ * 4, &q_full[st]);
+          bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
+        }
+        g0 += t.nsteps;
+        ++ne;
       }
-      mbar_wait(kv_full, 0, err, kKvDrain);
-      for (int s = 0; s < C::NQ && s < nsteps; ++s) {
-        const int last = s + ((nsteps - 1 - s) / C::NQ) * C::NQ;
-        mbar_wait(&q_full[s], (last / C::NQ) & 1, err, kKvDrain);
+      // every copy this warp started must land before the CTA may exit
+      if (ne > 0) mbar_wait(kv_full, (ne - 1) & 1, err, kKvDrain);
+      for (int st = 0; st < C::NQ && st < g0; ++st) {
+        const int last = st + ((g0 - 1 - st) / C::NQ) * C::NQ;
+        mbar_wait(&q_full[st], (last / C::NQ) & 1, err, kKvDrain);
       }
     }
   } else if (warp == 8 || warp == C::MMA_B_WARP) {
     // ------------------------------------------------------------ MMA issuers
     // Two issuing warps, because one cannot issue tcgen05.mma fast enough to
     // keep the tensor core busy with these 64-wide tiles:
-    //   A (warp 8):  S^T(s) = K Q_s^T, dP^T(s) = V dO_s^T
-    //   B:           dV += P^T(s) dO_s, dK += dS^T(s) Q_s, [dQ^T(s) = K^T dS^T(s)]
+    //   A (warp 8):  S^T(g) = K Q_g^T, dP^T(g) = V dO_g^T
+    //   B:           dV += P^T(g) dO_g, dK += dS^T(g) Q_g, [dQ^T(g) = K^T dS^T(g)]
     // MMAs of different warps are not ordered, so A waits for B's dv_done
-    // before S(s) overwrites the columns that held P(s-1), and for B's dk_done(s-1)
-    // before dP(s) overwrites the columns that held dS(s-1).
-    if (nsteps > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
-      constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
-      constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
-      constexpr uint32_t idDK = idesc_bf16_f32(128, D_QK, false, true);
-      constexpr uint32_t idDQ = idesc_bf16_f32(128, C::BQ, true, true);
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait_warp(kv_full, 0, err, kKvFull);
+    // before S(g) overwrites the columns that held P(g-1), and for B's dk_done(g-1)
+    // before dP(g) overwrites the columns that held dS(g-1).  Across tiles, B's first
+    // dV and dK of a tile wait for the epilogue to have read the previous tile's sums.
+    constexpr uint32_t idS = idesc_bf16_f32(128, C::BQ, false, false);
+    constexpr uint32_t idDV = idesc_bf16_f32(128, D_V, false, true);
+    constexpr uint32_t idDK = idesc_bf16_f32(128, D_QK, false, true);
+    constexpr uint32_t idDQ = idesc_bf16_f32(128, C::BQ, true, true);
+    const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+    const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+    bool ok = true;
+    int g0 = 0, ne = 0;
+    for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {  // whole warp; elect.sync picks the lane
+      const Tile t = tile_of(ti);
+      if (t.nsteps == 0) continue;
+      // K/V of the tile: read by A's products and, with the fused dQ, by B's K^T dS^T.  Only
+      // the warps that read them wait (a wait nothing gates could see a later phase complete).
+      if (warp == 8 || FUSE_DQ) ok = mbar_wait_warp(kv_full, ne & 1, err, kKvFull);
       if (warp == 8) {
         const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);  // K as K-major A of S^T
         const uint64_t dV0 = smem_desc_sw128(sV, 16, 1024);  // V as K-major A of dP^T
-        for (int s = 0; s < nsteps && ok; ++s) {
-          const int st = s % C::NQ;
-          const int slot = s & 1;
-          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull);
-          // slot reuse: P^T(s-2) in this slot must have been read by dV(s-2)
-          if (ok && s >= 2) ok = mbar_wait_warp(&dv_done[slot], ((s >> 1) - 1) & 1, err, kKvDvDone);
+        for (int s = 0; s < t.nsteps && ok; ++s) {
+          const int g = g0 + s, st = g % C::NQ, slot = g & 1;
+          ok = mbar_wait_warp(&q_full[st], (g / C::NQ) & 1, err, kKvQFull);
+          // slot reuse: P^T(g-2) in this slot must have been read by dV(g-2)
+          if (ok && g >= 2) ok = mbar_wait_warp(&dv_done[slot], ((g >> 1) - 1) & 1, err, kKvDvDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dq = smem_desc_sw128(sQ + st * C::Q_STAGE, 16, 1024);
@@ -235,49 +285,52 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
 #pragma unroll
           for (int kk = 0; kk < D_QK / 16; ++kk)
             mma_ss_warp(colS, desc_add(dK0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
-                   desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
+                        desc_add(dq, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
           mma_commit_warp(&s_ready[slot]);
-          if (s > 0) ok = mbar_wait_warp(dk_done, (s - 1) & 1, err, kKvDkDone);
+          if (g > 0) ok = mbar_wait_warp(dk_done, (g - 1) & 1, err, kKvDkDone);
           if (!ok) break;
           tc_fence_after();
           const uint64_t ddo = smem_desc_sw128(sDO + st * C::DO_STAGE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D_V / 16; ++kk)
             mma_ss_warp(tmem + C::COL_DP, desc_add(dV0, (kk / 4) * C::KCHUNK + (kk % 4) * 32),
-                   desc_add(ddo, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
+                        desc_add(ddo, (kk / 4) * C::QCHUNK + (kk % 4) * 32), idS, kk > 0);
           mma_commit_warp(dp_ready);
         }
+        if constexpr (PERSIST) mma_commit_warp(kv_empty);  // the tile's S and dP products have read K and V
       } else {
         const uint64_t dKt0 = smem_desc_sw128(sK, C::KCHUNK, 1024);   // K as MN-major A of dQ^T
         const uint64_t dDS0 = smem_desc_sw128(sDS, C::KCHUNK, 1024);  // dS^T as MN-major B of dQ^T
-        for (int s = 0; s < nsteps && ok; ++s) {
-          const int st = s % C::NQ;
+        for (int s = 0; s < t.nsteps && ok; ++s) {
+          const int g = g0 + s, st = g % C::NQ, slot = g & 1;
           const uint64_t ddo_mn = smem_desc_sw128(sDO + st * C::DO_STAGE, C::QCHUNK, 1024);  // dO, MN-major B of dV
           const uint64_t dq_mn = smem_desc_sw128(sQ + st * C::Q_STAGE, C::QCHUNK, 1024);     // Q, MN-major B of dK
-          ok = mbar_wait_warp(&q_full[st], (s / C::NQ) & 1, err, kKvQFull) && mbar_wait_warp(&p_ready[s & 1], (s >> 1) & 1, err, kKvP);
+          ok = mbar_wait_warp(&q_full[st], (g / C::NQ) & 1, err, kKvQFull) &&
+               mbar_wait_warp(&p_ready[slot], (g >> 1) & 1, err, kKvP);
+          // the first dV of a tile overwrites the sums the previous tile's epilogue reads
+          if (PERSIST && ok && s == 0 && ne > 0) ok = mbar_wait_warp(acc_free, (ne - 1) & 1, err, kKvAccFree);
           if (!ok) break;
           tc_fence_after();
-          const int slot = s & 1;
           const uint32_t colS = tmem + (slot ? C::COL_S1 : C::COL_S0);
           // dV += P^T dO   (P^T bf16 in the slot: q 0-31 at cols 0-15, q 32-63 at cols 32-47)
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
             mma_ts_warp(tmem + C::COL_DV, colS + (kk / 2) * 32 + (kk % 2) * 8, desc_add(ddo_mn, kk * 2048), idDV,
-                   (s > 0 || kk > 0) ? 1u : 0u);
+                        (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dv_done[slot]);
-          ok = mbar_wait_warp(ds_ready, s & 1, err, kKvDS);
+          ok = mbar_wait_warp(ds_ready, g & 1, err, kKvDS);
           if (!ok) break;
           tc_fence_after();
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8, desc_add(dq_mn, kk * 2048),
-                   idDK, (s > 0 || kk > 0) ? 1u : 0u);
-          // dS^T(s) in TMEM is consumed once dK(s) completes: issuer A may write dP(s+1).
+            mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + (kk / 2) * 32 + (kk % 2) * 8,
+                        desc_add(dq_mn, kk * 2048), idDK, (s > 0 || kk > 0) ? 1u : 0u);
+          // dS^T(g) in TMEM is consumed once dK(g) completes: issuer A may write dP(g+1).
           // (dQ^T reads dS^T from shared memory, double-buffered, so it does not gate dP.)
           mma_commit_warp(dk_done);
           if constexpr (FUSE_DQ) {
-            ok = mbar_wait_warp(dq_free, (s & 1) ^ 1, err, kKvDQFree);
+            ok = mbar_wait_warp(dq_free, (g & 1) ^ 1, err, kKvDQFree);
             if (!ok) break;
             tc_fence_after();
             // dQ^T = K^T dS^T: A = K (MN-major, M = d), B = dS^T from shared memory (MN-major, N = q)
@@ -287,203 +340,223 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
               mma_ss_warp(tmem + C::COL_DQ, desc_add(dKt0, kk * 2048), desc_add(dDS, kk * 2048), idDQ, kk > 0);
             mma_commit_warp(dq_ready);
           }
-          // The stage's S/dP MMAs (issuer A) completed before P(s)/dS(s) existed.
+          // The stage's S/dP MMAs (issuer A) completed before P(g)/dS(g) existed.
           mma_commit_warp(&q_empty[st]);
         }
+        if constexpr (FUSE_DQ && PERSIST) mma_commit_warp(kv_empty);  // the tile's dQ^T products have read K
       }
-      // Every MMA of both issuers must be complete before TMEM is released.
+      // the tile's dV/dK sums are complete once both issuers' MMAs are
       mma_commit_warp(mma_done);
-      mbar_wait_warp(mma_done, 0, err, kKvDone);
+      g0 += t.nsteps;
+      ++ne;
     }
+    // Every MMA of both issuers must be complete before TMEM is released.
+    mma_commit_warp(fin);
+    mbar_wait_warp(fin, 0, err, kKvDone);
   } else if (warp < 8) {
     // ------------------------------------------------------------ P / dS warpgroups
     const int w = warp / 4;  // which 32 query columns of the 64
     const int r = (warp % 4) * 32 + lane;
-    const int key = n0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2;
-    // bias: this thread's key column of the bias plane (keys past S_kv read key 0; their P is 0)
-    const int bkey = key < p.S_kv ? key : 0;
     [[maybe_unused]] DropState drop{};
     if constexpr (DROP) drop = DropState{p.rng[0], p.rng[1], p.drop_t};
     bool ok = true;
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int st = s % C::NQ;
-      const int q0 = (ilo + s % nq) * C::BQ;
-      [[maybe_unused]] const long long bplane = BIAS ? b * p.bias_sb + (h0 + s / nq) * p.bias_sh : 0;
-      const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
-      const float* dd = l2 + C::BQ;
-      const int slot = s & 1;
-      const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
-      // dropout: keep bits of this key for the step's 32 query rows (bit c: row q0 + 32 w + c),
-      // generated while the step's scores are still being computed
-      [[maybe_unused]] uint32_t keep = 0u;
-      if constexpr (DROP)
-        keep = dropout_key_span16(drop, b, h0 + s / nq, key, q0 + 32 * w) |
-               (dropout_key_span16(drop, b, h0 + s / nq, key, q0 + 32 * w + 16) << 16);
-      ok = mbar_wait_warp(&s_ready[slot], (s >> 1) & 1, err, kKvS);
-      if (!ok) break;
-      tc_fence_after();
-      float pr[32];
-      {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + colS + 32 * w, rr);
-        float lv[32];  // -LSE * log2(e) of the 32 queries
+    int g0 = 0, ne = 0;
+    for (int ti = blockIdx.x; ti < n_tiles; ti += tstride) {
+      const Tile t = tile_of(ti);
+      const int key = t.n0 + r;
+      // bias: this thread's key column of the bias plane (keys past S_kv read key 0; their P is 0)
+      [[maybe_unused]] const int bkey = key < p.S_kv ? key : 0;
+      for (int s = 0; s < t.nsteps && ok; ++s) {
+        const int g = g0 + s, st = g % C::NQ;
+        const int q0 = (t.ilo + s % t.nq) * C::BQ;
+        [[maybe_unused]] const long long bplane = BIAS ? t.b * p.bias_sb + (t.h0 + s / t.nq) * p.bias_sh : 0;
+        const float* l2 = reinterpret_cast<const float*>(smem + C::OFF_L + st * C::L_STAGE) + 32 * w;
+        const float* dd = l2 + C::BQ;
+        const int slot = g & 1;
+        const uint32_t colS = slot ? C::COL_S1 : C::COL_S0;
+        // dropout: keep bits of this key for the step's 32 query rows (bit c: row q0 + 32 w + c),
+        // generated while the step's scores are still being computed
+        [[maybe_unused]] uint32_t keep = 0u;
+        if constexpr (DROP)
+          keep = dropout_key_span16(drop, t.b, t.h0 + s / t.nq, key, q0 + 32 * w) |
+                 (dropout_key_span16(drop, t.b, t.h0 + s / t.nq, key, q0 + 32 * w + 16) << 16);
+        ok = mbar_wait_warp(&s_ready[slot], (g >> 1) & 1, err, kKvS);
+        if (!ok) break;
+        tc_fence_after();
+        float pr[32];
+        {
+          uint32_t rr[32];
+          tmem_ld32(lane_addr + colS + 32 * w, rr);
+          float lv[32];  // -LSE * log2(e) of the 32 queries
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
-        if constexpr (BIAS) {  // + bias * log2(e) (queries past S_q read 0; their P is 0)
-          if (p.bias_tma) {  // this thread's key column of the staged tile [64 q][128 keys]
-            const unsigned short* bt =
-                reinterpret_cast<const unsigned short*>(smem + C::OFF_B + st * C::B_STAGE) + 32 * w * C::BN + r;
+          for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&lv[c]) = *reinterpret_cast<const float4*>(&l2[c]);
+          if constexpr (BIAS) {  // + bias * log2(e) (queries past S_q read 0; their P is 0)
+            if (p.bias_tma) {  // this thread's key column of the staged tile [64 q][128 keys]
+              const unsigned short* bt =
+                  reinterpret_cast<const unsigned short*>(smem + C::OFF_B + st * C::B_STAGE) + 32 * w * C::BN + r;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) lv[c] = fmaf(bf16_bits_to_float(bt[c * C::BN]), kLog2e, lv[c]);
-          } else {
-            const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
+              for (int c = 0; c < 32; ++c) lv[c] = fmaf(bf16_bits_to_float(bt[c * C::BN]), kLog2e, lv[c]);
+            } else {
+              const unsigned short* bcol = reinterpret_cast<const unsigned short*>(p.bias + bplane) + bkey;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int qq = q0 + 32 * w + c;
-              const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
-              lv[c] = fmaf(bv, kLog2e, lv[c]);
+              for (int c = 0; c < 32; ++c) {
+                const int qq = q0 + 32 * w + c;
+                const float bv = qq < p.S_q ? bf16_bits_to_float(__ldg(bcol + (size_t)qq * p.S_kv)) : 0.f;
+                lv[c] = fmaf(bv, kLog2e, lv[c]);
+              }
             }
           }
-        }
-        tmem_ld_wait();
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float xa, xb;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2, f2_pack(lv[c], lv[c + 1])),
-                    xa, xb);
-          pr[c] = ex2(xa);
-          pr[c + 1] = ex2(xb);
-        }
-      }
-      if (!tile_fully_visible<VL>(mask, q0, C::BQ, n0, C::BN)) {
-        int vlo, vhi;  // the query rows that see this thread's key
-        visible_rows<VL>(mask, key, &vlo, &vhi);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int qq = q0 + 32 * w + c;
-          pr[c] = (qq >= vlo && qq <= vhi) ? pr[c] : 0.f;
-        }
-      }
-      {
-        uint32_t pk[16];  // P^T for dV: dropped entries are 0 (the 1/(1-p) scale is in dV's epilogue)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          if constexpr (DROP)
-            pk[c] = pack_bf16x2(((keep >> (2 * c)) & 1u) ? pr[2 * c] : 0.f,
-                                ((keep >> (2 * c)) & 2u) ? pr[2 * c + 1] : 0.f);
-          else
-            pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
-        }
-        tmem_st16(lane_addr + colS + 32 * w, pk);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(&p_ready[slot]);
-      ok = mbar_wait_warp(dp_ready, s & 1, err, kKvDP);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dsk[16];
-      {
-        uint32_t rr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
-        float dv4[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          // dS = P (dP - D), paired; with dropout dS = P (M dP - D), M = 0 or 1/(1-p)
-          float a, bq;
-          if constexpr (DROP) {
-            const float za = ((keep >> (2 * c)) & 1u) ? p.drop_scale : 0.f;
-            const float zb = ((keep >> (2 * c)) & 2u) ? p.drop_scale : 0.f;
-            f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
-                             f2_fma(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
-                                    f2_pack(za, zb), f2_pack(-dv4[2 * c], -dv4[2 * c + 1]))),
-                      a, bq);
-          } else {
-            f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
-                             f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
-                                    f2_pack(dv4[2 * c], dv4[2 * c + 1]))),
-                      a, bq);
-          }
-          dsk[c] = pack_bf16x2(a, bq);
-          if constexpr (BIAS) {  // dbias = dS, summed with fp32 atomics over the (b, h) sharing it
-            if (p.dbias && key < p.S_kv) {
-              const int qq = q0 + 32 * w + 2 * c;
-              float* dcol = p.dbias + bplane + key;
-              if (qq < p.S_q) atomicAdd(dcol + (size_t)qq * p.S_kv, a);
-              if (qq + 1 < p.S_q) atomicAdd(dcol + (size_t)(qq + 1) * p.S_kv, bq);
-            }
-          }
-        }
-      }
-      tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
-      if constexpr (FUSE_DQ) {
-        // dS^T row r, query columns 32w..32w+31 -> 16-byte chunks 4w..4w+3 (128-byte swizzle)
-        uint8_t* rowp = smem + C::OFF_DS + slot * C::DS_BUF + r * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = (4 * w + k) ^ (r & 7);
-          *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-              make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_ready);
-    }
-    // ------------------------------------------------------------ epilogue: dV (w = 0), dK (w = 1)
-    bool have = false;
-    if (ok && nsteps > 0) {
-      have = mbar_wait_warp(mma_done, 0, err, kKvDone);
-      tc_fence_after();
-    }
-    {
-      const bool row_ok = key < p.S_kv;  // all lanes load TMEM; only real keys store
-      const int krow = row_ok ? key : 0;
-      const int ncols = w == 0 ? D_V : D_QK;
-      const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
-      const float mul = w == 0 ? (DROP ? p.drop_scale : 1.f) : p.scale;
-      const size_t row = ((size_t)b * p.S_kv + krow) * p.H_kv + hk;
-      __nv_bfloat16* dst = w == 0 ? p.dv + row * D_V : p.dk + row * D_QK;
-      // with head splits this CTA's sum is one fp32 partial slice
-      float* part = p.ns == 1 ? nullptr
-                              : (w == 0 ? p.dv_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_V
-                                        : p.dk_part + ((size_t)split * p.B * p.S_kv * p.H_kv + row) * D_QK);
-#pragma unroll 1
-      for (int c0 = 0; c0 < ncols; c0 += 32) {
-        uint32_t rr[32];
-        if (have) {
-          tmem_ld32(lane_addr + col0 + c0, rr);
           tmem_ld_wait();
-        } else {
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) rr[c] = 0u;
-        }
-        if (part) {
-          if (row_ok) {
-            float4* f4 = reinterpret_cast<float4*>(part + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              f4[q] = make_float4(__uint_as_float(rr[4 * q]) * mul, __uint_as_float(rr[4 * q + 1]) * mul,
-                                  __uint_as_float(rr[4 * q + 2]) * mul, __uint_as_float(rr[4 * q + 3]) * mul);
+          for (int c = 0; c < 32; c += 2) {
+            float xa, xb;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c]), __uint_as_float(rr[c + 1])), sl2x2,
+                             f2_pack(lv[c], lv[c + 1])),
+                      xa, xb);
+            pr[c] = ex2(xa);
+            pr[c + 1] = ex2(xb);
           }
-          continue;
         }
-        uint32_t pw[16];
+        if (!tile_fully_visible<VL>(t.mask, q0, C::BQ, t.n0, C::BN)) {
+          int vlo, vhi;  // the query rows that see this thread's key
+          visible_rows<VL>(t.mask, key, &vlo, &vhi);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * mul, __uint_as_float(rr[2 * c + 1]) * mul);
-        if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          for (int c = 0; c < 32; ++c) {
+            const int qq = q0 + 32 * w + c;
+            pr[c] = (qq >= vlo && qq <= vhi) ? pr[c] : 0.f;
+          }
         }
+        {
+          uint32_t pk[16];  // P^T for dV: dropped entries are 0 (the 1/(1-p) scale is in dV's epilogue)
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if constexpr (DROP)
+              pk[c] = pack_bf16x2(((keep >> (2 * c)) & 1u) ? pr[2 * c] : 0.f,
+                                  ((keep >> (2 * c)) & 2u) ? pr[2 * c + 1] : 0.f);
+            else
+              pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+          }
+          tmem_st16(lane_addr + colS + 32 * w, pk);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&p_ready[slot]);
+        ok = mbar_wait_warp(dp_ready, g & 1, err, kKvDP);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dsk[16];
+        {
+          uint32_t rr[32];
+          tmem_ld32(lane_addr + C::COL_DP + 32 * w, rr);
+          float dv4[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(&dv4[c]) = *reinterpret_cast<const float4*>(&dd[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            // dS = P (dP - D), paired; with dropout dS = P (M dP - D), M = 0 or 1/(1-p)
+            float a, bq;
+            if constexpr (DROP) {
+              const float za = ((keep >> (2 * c)) & 1u) ? p.drop_scale : 0.f;
+              const float zb = ((keep >> (2 * c)) & 2u) ? p.drop_scale : 0.f;
+              f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
+                               f2_fma(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
+                                      f2_pack(za, zb), f2_pack(-dv4[2 * c], -dv4[2 * c + 1]))),
+                        a, bq);
+            } else {
+              f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
+                               f2_sub(f2_pack(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])),
+                                      f2_pack(dv4[2 * c], dv4[2 * c + 1]))),
+                        a, bq);
+            }
+            dsk[c] = pack_bf16x2(a, bq);
+            if constexpr (BIAS) {  // dbias = dS, summed with fp32 atomics over the (b, h) sharing it
+              if (p.dbias && key < p.S_kv) {
+                const int qq = q0 + 32 * w + 2 * c;
+                float* dcol = p.dbias + bplane + key;
+                if (qq < p.S_q) atomicAdd(dcol + (size_t)qq * p.S_kv, a);
+                if (qq + 1 < p.S_q) atomicAdd(dcol + (size_t)(qq + 1) * p.S_kv, bq);
+              }
+            }
+          }
+        }
+        tmem_st16(lane_addr + C::COL_DP + 32 * w, dsk);
+        if constexpr (FUSE_DQ) {
+          // dS^T row r, query columns 32w..32w+31 -> 16-byte chunks 4w..4w+3 (128-byte swizzle)
+          uint8_t* rowp = smem + C::OFF_DS + slot * C::DS_BUF + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int chunk = (4 * w + k) ^ (r & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_ready);
+      }
+      // ---------------------------------------------------------- epilogue: dV (w = 0), dK (w = 1)
+      // A tile no query sees (nsteps = 0) writes zero rows and touches neither TMEM nor a barrier.
+      bool have = false;
+      if (ok && t.nsteps > 0) {
+        have = mbar_wait_warp(mma_done, ne & 1, err, kKvDone);
+        tc_fence_after();
+      }
+      {
+        const bool row_ok = key < p.S_kv;  // all lanes load TMEM; only real keys store
+        const int krow = row_ok ? key : 0;
+        const int ncols = w == 0 ? D_V : D_QK;
+        const int col0 = w == 0 ? C::COL_DV : C::COL_DK;
+        const float mul = w == 0 ? (DROP ? p.drop_scale : 1.f) : p.scale;
+        const size_t row = ((size_t)t.b * p.S_kv + krow) * p.H_kv + t.hk;
+        __nv_bfloat16* dst = w == 0 ? p.dv + row * D_V : p.dk + row * D_QK;
+        // with head splits this tile's sum is one fp32 partial slice
+        float* part = p.ns == 1 ? nullptr
+                                : (w == 0 ? p.dv_part + ((size_t)t.split * p.B * p.S_kv * p.H_kv + row) * D_V
+                                          : p.dk_part + ((size_t)t.split * p.B * p.S_kv * p.H_kv + row) * D_QK);
+#pragma unroll 1
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          uint32_t rr[32];
+          if (have) {
+            tmem_ld32(lane_addr + col0 + c0, rr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) rr[c] = 0u;
+          }
+          if (part) {
+            if (row_ok) {
+              float4* f4 = reinterpret_cast<float4*>(part + c0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                f4[q] = make_float4(__uint_as_float(rr[4 * q]) * mul, __uint_as_float(rr[4 * q + 1]) * mul,
+                                    __uint_as_float(rr[4 * q + 2]) * mul, __uint_as_float(rr[4 * q + 3]) * mul);
+            }
+            continue;
+          }
+          uint32_t pw[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pw[c] = pack_bf16x2(__uint_as_float(rr[2 * c]) * mul, __uint_as_float(rr[2 * c + 1]) * mul);
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          }
+        }
+      }
+      if (t.nsteps > 0) {
+        // the sums are in registers or stored: issuer B may start the next tile's dV and dK
+        if constexpr (PERSIST) {
+          tc_fence_before();
+          mbar_arrive(acc_free);
+        }
+        g0 += t.nsteps;
+        ++ne;
       }
     }
   } else if (FUSE_DQ && warp >= 10 && warp < 14) {
@@ -496,33 +569,41 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     float* stage = reinterpret_cast<float*>(smem + C::OFF_DQS);
     if (tid_d == 0) tma_prefetch_desc(&tmDQ);
-    for (int s = 0; s < nsteps; ++s) {
-      const bool got = mbar_wait(dq_ready, s & 1, err, kKvDQReady);
-      if (!bar_red_and(1, 128, got)) break;  // uniform over the 128 drain threads
-      tc_fence_after();
-      const int h = h0 + s / nq;
-      const int q0 = (ilo + s % nq) * C::BQ;
-      uint32_t ra[32], rb[32];
-      tmem_ld32(lane_addr + C::COL_DQ, ra);
-      tmem_ld32(lane_addr + C::COL_DQ + 32, rb);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(dq_free);  // the TMEM columns may be overwritten now
-      if (tid_d == 0) bulk_wait_read_all();  // previous tile has left shared memory
-      named_bar_sync(1, 128);
-      if (d < D_QK) {  // lanes past d_qk hold the unused rows of the M = 128 product
+    bool ok = true;
+    int g0 = 0;
+    for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {
+      const Tile t = tile_of(ti);
+      for (int s = 0; s < t.nsteps; ++s) {
+        const int g = g0 + s;
+        const bool got = mbar_wait(dq_ready, g & 1, err, kKvDQReady);
+        ok = bar_red_and(1, 128, got);  // uniform over the 128 drain threads
+        if (!ok) break;
+        tc_fence_after();
+        const int h = t.h0 + s / t.nq;
+        const int q0 = (t.ilo + s % t.nq) * C::BQ;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(lane_addr + C::COL_DQ, ra);
+        tmem_ld32(lane_addr + C::COL_DQ + 32, rb);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(dq_free);  // the TMEM columns may be overwritten now
+        if (tid_d == 0) bulk_wait_read_all();  // previous tile has left shared memory
+        named_bar_sync(1, 128);
+        if (d < D_QK) {  // lanes past d_qk hold the unused rows of the M = 128 product
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          stage[c * D_QK + d] = __uint_as_float(ra[c]);
-          stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
+          for (int c = 0; c < 32; ++c) {
+            stage[c * D_QK + d] = __uint_as_float(ra[c]);
+            stage[(32 + c) * D_QK + d] = __uint_as_float(rb[c]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid_d == 0) {
+          tma_reduce_add_4d(&tmDQ, stage, 0, h, q0, t.b);
+          bulk_commit_group();
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tid_d == 0) {
-        tma_reduce_add_4d(&tmDQ, stage, 0, h, q0, b);
-        bulk_commit_group();
-      }
+      g0 += t.nsteps;
     }
     if (tid_d == 0) bulk_wait_all();
   }
@@ -553,14 +634,36 @@ inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   } else if constexpr (KV == KernVariant::kBias) {
     if (!p.bias) return -2;
     kern = vl ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true, true> : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, true>;
-  } else {
+  }
+  const long long tiles = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
+  if (tiles <= 0 || tiles > 0x7fffffffLL) return -2;
+  // One CTA per tile lets the hardware balance tiles of unequal length (causal tiles
+  // differ by up to the whole sequence).  When every tile is short (at most 16 steps)
+  // and there are many of them, the fixed cost of a CTA (TMEM allocation, the K/V load,
+  // the first products, the dK/dV epilogue) is a large share of its time, and persistent
+  // CTAs, one per SM taking every gridDim-th tile, overlap it with the next tile's work
+  // (the plain fused-dQ kernels of full-length batches with d_qk = d_v).
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+      return -1;
+  }
+  bool persist = false;
+  if constexpr (KV == KernVariant::kPlain) {
     if (p.bias) return -2;
-    kern = vl ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true> : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
+    const long long max_steps = (long long)(p.G / p.ns) * ((p.S_q + C::BQ - 1) / C::BQ);
+    if constexpr (D_QK == D_V && FUSE) persist = !vl && max_steps <= 16 && tiles >= 4LL * n_sm;
+    if (persist) {
+      if constexpr (D_QK == D_V && FUSE) kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, false, false, true>;
+    } else {
+      kern = vl ? attn_bwd_kv_kernel<D_QK, D_V, FUSE, true> : attn_bwd_kv_kernel<D_QK, D_V, FUSE, false>;
+    }
   }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  const long long blocks = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
-  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tb, p);
+  const unsigned grid = (unsigned)(persist ? n_sm : tiles);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, tb, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -10,7 +10,8 @@ import torch
 
 import oracle
 from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
-from parity_util import Shape, check_d_offset_bound, compare, gpu_run, make_inputs, oracle_run
+from parity_util import (Shape, check_d_offset_bound, compare, gpu_run, gpu_slice, make_inputs, oracle_run,
+                         slice_group)
 
 pytestmark = pytest.mark.gpu
 
@@ -108,6 +109,33 @@ def test_empty_problem_is_a_noop():
     dq, dk, dv, _ = sdpa.sdpa_backward(q, k, k, o, o, lse)
     torch.cuda.synchronize()
     assert torch.all(dk == 0) and torch.all(dv == 0)
+
+
+# Grids of many short tiles run the fused-dQ kv kernel with persistent CTAs (at most 16
+# steps per tile and at least four tiles per SM); these cases take that path.
+PERSIST_CASES = [
+    # name, shape, causal, window, softmax type
+    ("mha_ragged_d64_learnable", Shape(16, 300, 300, 40, 40, 64, 64), True, -1, LEARNABLE),
+    ("mha_d128_window", Shape(8, 520, 520, 24, 24, 128, 128), True, 200, OFF_BY_ONE),
+    # S_q < S_kv, causal: the kv tiles past the last query row see no query (empty tiles)
+    ("mha_empty_tiles", Shape(8, 100, 300, 32, 32, 64, 64), True, -1, VANILLA),
+]
+
+
+@pytest.mark.parametrize("case", PERSIST_CASES, ids=[c[0] for c in PERSIST_CASES])
+def test_persistent_kv_tiles_match_oracle(case):
+    """The fused-dQ path on grids of many short tiles, against the oracle on sampled
+    (batch, head) units; with S_q < S_kv, the keys no query sees get zero gradients."""
+    name, shape, causal, window, st = case
+    x = make_inputs(shape, 31, learnable_offset=True)
+    kw = dict(causal=causal, window=window, softmax_type=st, scale=None)
+    gpu = gpu_run(x, deterministic=False, **kw)
+    for b, g in ((0, 0), (shape.B - 1, shape.H_kv - 1)):
+        ref = oracle_run(slice_group(x, b, g, 1), **kw)
+        ref.pop("d_offset", None)
+        compare(gpu_slice(gpu, b, g, 1), ref, f"{name} unit (b={b}, h={g})")
+    if name == "mha_empty_tiles":
+        assert np.all(gpu["dk"][:, 100:] == 0) and np.all(gpu["dv"][:, 100:] == 0)
 
 
 @pytest.mark.parametrize("shape, lens", [
