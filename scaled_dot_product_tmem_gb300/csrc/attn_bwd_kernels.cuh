@@ -65,10 +65,11 @@ struct KvCfg {
   static constexpr int DQS_BYTES = FUSE_DQ ? BQ * D_QK * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, q_full[NQ], q_empty[NQ], s_ready[2], dp_ready, p_ready[2], ds_ready, dq_ready, dq_free,
-  // mma_done, dv_done[2], dk_done, kv_empty, acc_free, fin.  Barriers of the double-buffered S
-  // slot are per slot: with two slots the P/dS warps can finish step s+1's P before issuer B
-  // has waited for step s's, and a single barrier would then complete two phases before B looks.
-  static constexpr int NBAR = 1 + 2 * NQ + 15;
+  // mma_done, dv_done[2], dk_done, kv_empty, acc_free, fin, tile_full[2], tile_empty[2].  Barriers
+  // of the double-buffered S slot are per slot: with two slots the P/dS warps can finish step
+  // s+1's P before issuer B has waited for step s's, and a single barrier would then complete
+  // two phases before B looks.  The tile index ring (two ints) sits beside the TMEM address.
+  static constexpr int NBAR = 1 + 2 * NQ + 19;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int MMA_B_WARP = FUSE_DQ ? 14 : 10;  // second MMA issuer
@@ -89,10 +90,11 @@ struct KvCfg {
 constexpr int kKvChunk = 8;  // (b, kv head) groups per chunk of the kv kernel's block order
 
 enum KvSite { kKvFull = 0x20, kKvQFull, kKvQEmpty, kKvS, kKvDP, kKvP, kKvDS, kKvDQReady, kKvDQFree, kKvDone, kKvDrain,
-              kKvDvDone, kKvDkDone, kKvEmpty, kKvAccFree };
+              kKvDvDone, kKvDkDone, kKvEmpty, kKvAccFree, kKvTile };
 
-// PERSIST: the CTAs take every gridDim-th tile; otherwise the grid has one CTA per tile
-// and the tile loops below run once (the cross-tile barriers compile away).
+// PERSIST: the CTAs take tiles from a counter in global memory until it runs out; otherwise
+// the grid has one CTA per tile and the tile loops below run once (the cross-tile barriers
+// compile away).
 template <int D_QK, int D_V, bool FUSE_DQ, bool VL, bool BIAS = false, bool DROP = false, bool PERSIST = false>
 __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -119,23 +121,26 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   uint64_t* kv_empty = s_ready + 12;    // a tile's K/V readers are done: the next K/V may load
   uint64_t* acc_free = s_ready + 13;    // the epilogue has read dV/dK: the next tile may overwrite them
   uint64_t* fin = s_ready + 14;         // every MMA issued, before TMEM is released
+  uint64_t* tile_full = s_ready + 15;   // [2] PERSIST: the producer has published the next tile
+  uint64_t* tile_empty = s_ready + 17;  // [2] PERSIST: every role has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_TMEM_SLOT + 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Work tiles: (b, kv head, head split) groups in chunks of kKvChunk; within a chunk,
   // kv tile by kv tile (tile 0, the most work when causal, first) and group by group,
   // so a chunk's long tiles start early while its queries stay few enough to be shared
-  // in L2.  The CTAs are persistent (at most one per SM) and take every gridDim-th
-  // tile, so a tile's K/V load and first products overlap the previous tile's epilogue.
-  // Every role walks the same tiles and numbers the steps of all its tiles in one
-  // sequence g, which indexes the stages, slots and barrier phases.
+  // in L2.  Persistent CTAs (PERSIST, at most one per SM) take the tiles in that order
+  // from a counter, as an SM would take blocks, so a tile's K/V load and first products
+  // overlap the previous tile's epilogue; the producer takes each index and publishes
+  // it to the other roles through a two-slot ring.  Every role walks the same tiles and
+  // numbers the steps of all its tiles in one sequence g, which indexes the stages,
+  // slots and barrier phases.
   const int n_kv = (p.S_kv + C::BN - 1) / C::BN;
   const int n_gr = p.H_kv * p.B * p.ns;  // group = (b, kv head, head split)
   const int n_tiles = n_kv * n_gr;
   const int per_chunk = kKvChunk * n_kv;
   const int Gs = p.G / p.ns;  // query heads a tile walks
-  // tile stride of the loops: past the last tile after one pass without PERSIST
-  const int tstride = PERSIST ? (int)gridDim.x : n_tiles;
   struct Tile {
     int b, hk, split, h0, n0, ilo, nq, nsteps;
     MaskSpec mask;
@@ -159,6 +164,25 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     t.nsteps = t.nq * Gs;
     return t;
   };
+  // Tile k of this CTA for the roles other than the producer: without PERSIST the CTA's
+  // own tile, then none; with it, slot k % 2 of the ring once the producer has published
+  // it.  whole_warp: the warp waits together and its lane 0 arrives for it.
+  auto take_tile = [&](int k, bool whole_warp) -> int {
+    if constexpr (!PERSIST) {
+      return k == 0 ? (int)blockIdx.x : n_tiles;
+    } else {
+      const int slot = k & 1;
+      if (!mbar_wait_warp(&tile_full[slot], (k >> 1) & 1, p.err, kKvTile)) return n_tiles;
+      const int ti = ring[slot];
+      if (whole_warp) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&tile_empty[slot]);
+      } else {
+        mbar_arrive(&tile_empty[slot]);
+      }
+      return ti;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -178,6 +202,10 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     mbar_init(kv_empty, FUSE_DQ ? 2 : 1);  // issuer A (S, dP) and, with the fused dQ, issuer B (K^T dS^T)
     mbar_init(acc_free, 256);
     mbar_init(fin, 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tile_full[i], 1);
+      mbar_init(&tile_empty[i], 2 + 256 + (FUSE_DQ ? 128 : 0));  // the two issuers (one lane each), P/dS and drain threads
+    }
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -196,9 +224,24 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
       const bool btma = BIAS && p.bias_tma;  // each stage also brings the step's bias tile
       bool ok = true, first = true;
       int g0 = 0, ne = 0;  // steps and non-empty tiles so far
-      for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {
+      int ti_next = 0;     // PERSIST: the tile taken for the next iteration
+      for (int k = 0;; ++k) {
+        int ti;
+        if constexpr (PERSIST) {  // publish tile k in ring slot k % 2 once every role has read tile k - 2
+          const int slot = k & 1;
+          if (k >= 2 && !mbar_wait(&tile_empty[slot], ((k >> 1) - 1) & 1, err, kKvTile)) break;
+          ti = k == 0 ? atomicAdd(p.tile_counter, 1) : ti_next;
+          ring[slot] = ti;
+          mbar_arrive(&tile_full[slot]);
+        } else {
+          ti = k == 0 ? (int)blockIdx.x : n_tiles;
+        }
+        if (ti >= n_tiles || !ok) break;
         const Tile t = tile_of(ti);
-        if (t.nsteps == 0) continue;
+        if (t.nsteps == 0) {
+          if constexpr (PERSIST) ti_next = atomicAdd(p.tile_counter, 1);
+          continue;
+        }
         if (first) {
           tma_prefetch_desc(&tmQ);
           tma_prefetch_desc(&tmK);
@@ -235,6 +278,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
           bulk_load(smem + C::OFF_L + st * C::L_STAGE, p.nlse2 + row, C::BQ * 4, &q_full[st]);
           bulk_load(smem + C::OFF_L + st * C::L_STAGE + C::BQ * 4, p.Dsum + row, C::BQ * 4, &q_full[st]);
         }
+        // the next tile is taken once this one's loads are issued: late enough that the
+        // counter still balances the last tiles, early enough to hide the atomic
+        if constexpr (PERSIST) ti_next = atomicAdd(p.tile_counter, 1);
         g0 += t.nsteps;
         ++ne;
       }
@@ -264,7 +310,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     const uint32_t sDS = smem_u32(smem + C::OFF_DS);
     bool ok = true;
     int g0 = 0, ne = 0;
-    for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {  // whole warp; elect.sync picks the lane
+    for (int k = 0;; ++k) {  // whole warp; elect.sync picks the lane
+      const int ti = take_tile(k, true);
+      if (ti >= n_tiles || !ok) break;
       const Tile t = tile_of(ti);
       if (t.nsteps == 0) continue;
       // K/V of the tile: read by A's products and, with the fused dQ, by B's K^T dS^T.  Only
@@ -363,7 +411,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     if constexpr (DROP) drop = DropState{p.rng[0], p.rng[1], p.drop_t};
     bool ok = true;
     int g0 = 0, ne = 0;
-    for (int ti = blockIdx.x; ti < n_tiles; ti += tstride) {
+    for (int k = 0;; ++k) {
+      const int ti = take_tile(k, false);
+      if (ti >= n_tiles) break;
       const Tile t = tile_of(ti);
       const int key = t.n0 + r;
       // bias: this thread's key column of the bias plane (keys past S_kv read key 0; their P is 0)
@@ -571,7 +621,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     if (tid_d == 0) tma_prefetch_desc(&tmDQ);
     bool ok = true;
     int g0 = 0;
-    for (int ti = blockIdx.x; ti < n_tiles && ok; ti += tstride) {
+    for (int k = 0;; ++k) {
+      const int ti = take_tile(k, false);
+      if (ti >= n_tiles || !ok) break;
       const Tile t = tile_of(ti);
       for (int s = 0; s < t.nsteps; ++s) {
         const int g = g0 + s;
@@ -637,12 +689,13 @@ inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   }
   const long long tiles = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
   if (tiles <= 0 || tiles > 0x7fffffffLL) return -2;
-  // One CTA per tile lets the hardware balance tiles of unequal length (causal tiles
-  // differ by up to the whole sequence).  When every tile is short (at most 16 steps)
-  // and there are many of them, the fixed cost of a CTA (TMEM allocation, the K/V load,
-  // the first products, the dK/dV epilogue) is a large share of its time, and persistent
-  // CTAs, one per SM taking every gridDim-th tile, overlap it with the next tile's work
-  // (the plain fused-dQ kernels of full-length batches with d_qk = d_v).
+  // The plain fused-dQ kernels of full-length batches with d_qk = d_v run persistent
+  // CTAs, one per SM, when there are more tiles than SMs and every tile is short (at most
+  // 32 steps): a CTA's fixed costs (TMEM allocation, the K/V load, the first products, the
+  // dK/dV epilogue) are then a large share of a tile, and persistent CTAs overlap them
+  // with the neighbouring tiles' work; the tile counter hands out tiles in the
+  // heaviest-first order as SMs free up, as the hardware does with blocks.  With longer
+  // tiles the persistent kernel measured about 4 % slower, so those keep one CTA per tile.
   static int n_sm = 0;
   if (n_sm == 0) {
     int dev = 0;
@@ -654,7 +707,7 @@ inline int launch_kv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if constexpr (KV == KernVariant::kPlain) {
     if (p.bias) return -2;
     const long long max_steps = (long long)(p.G / p.ns) * ((p.S_q + C::BQ - 1) / C::BQ);
-    if constexpr (D_QK == D_V && FUSE) persist = !vl && max_steps <= 16 && tiles >= 4LL * n_sm;
+    if constexpr (D_QK == D_V && FUSE) persist = !vl && p.tile_counter && tiles > n_sm && max_steps <= 32;
     if (persist) {
       if constexpr (D_QK == D_V && FUSE) kern = attn_bwd_kv_kernel<D_QK, D_V, FUSE, false, false, false, true>;
     } else {

@@ -77,7 +77,7 @@ def test_bwd_workspace_and_validation(lib):
     atom = sdpa.attn_bwd_workspace_size(4, 2048, 2048, 32, 8, 128, 128, False)
     rows = 4 * 32 * 2048
     assert det == 2 * rows * 4                          # lse2 + D, fp32
-    assert atom == det + 4 * 2048 * 32 * 128 * 4        # + fp32 dQ accumulator
+    assert atom == det + 4 * 2048 * 32 * 128 * 4 + 256  # + fp32 dQ accumulator, tile counter
     # B=1, S=100, H_kv=2: 2 kv CTAs, so the 2 query heads of each group go to 2 CTAs
     # and the workspace adds 2 fp32 partial slices of dK and dV
     part = 2 * 1 * 100 * 2 * 64 * 4
