@@ -74,9 +74,9 @@ WsLayout ws_layout(int B, int S_q, int S_kv, int H_q, int H_kv, int d_qk, int d_
   w.ns = S_q > 0 && S_kv > 0 ? sdpa::bwd_kv_head_splits(B, S_kv, H_kv, H_q / H_kv) : 1;
   const size_t kv_rows = static_cast<size_t>(w.ns > 1 ? w.ns : 0) * B * S_kv * H_kv;
   w.dv_part = w.dk_part + round256(kv_rows * d_qk * sizeof(float));
-  // the fused-dQ path's tile counter for the persistent kv kernel
+  // tile counters of the persistent kv and dQ kernels
   w.counter = w.dv_part + round256(kv_rows * d_v * sizeof(float));
-  w.total = w.counter + (need_dq_acc ? 256 : 0);
+  w.total = w.counter + 256;
   return w;
 }
 
@@ -412,7 +412,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.dq_acc = fused ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
-  p.tile_counter = fused ? reinterpret_cast<int*>(ws + w.counter) : nullptr;
+  p.tile_counter = reinterpret_cast<int*>(ws + w.counter);
+  p.tile_counter_q = reinterpret_cast<int*>(ws + w.counter) + 1;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.bias_sb = bsb;
   p.bias_sh = bsh;

@@ -43,8 +43,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   constexpr int TILE = 64;
   __shared__ float dsum[TILE];
   const int i0 = blockIdx.x * TILE, h = blockIdx.y, b = blockIdx.z;
-  // the kv kernel that follows on this stream takes its tiles from this counter
-  if (p.tile_counter && blockIdx.x == 0 && h == 0 && b == 0 && threadIdx.x == 0) *p.tile_counter = 0;
+  // the kv and dQ kernels that follow on this stream take their tiles from these counters
+  if (blockIdx.x == 0 && h == 0 && b == 0 && threadIdx.x == 0) {
+    if (p.tile_counter) *p.tile_counter = 0;
+    if (p.tile_counter_q) *p.tile_counter_q = 0;
+  }
   const int Lq = entry_len(p.seq_q, b, p.S_q);  // rows past it are padding, like rows past S_q
   const int sub = threadIdx.x % TPR;
   constexpr int NR = TILE / RPP;  // rows per thread

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     mbar_init(ds_ready, 256);
     mbar_init(dq_ready, 1);
     mbar_init(dq_free, 128);
-    mbar_init(mma_done, 2);
+    mbar_init(mma_done, 1);  // issuer B, once per tile: it alone writes the dV/dK sums
     mbar_init(&dv_done[0], 1);
     mbar_init(&dv_done[1], 1);
     mbar_init(dk_done, 1);
@@ -393,8 +393,10 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
         }
         if constexpr (FUSE_DQ && PERSIST) mma_commit_warp(kv_empty);  // the tile's dQ^T products have read K
       }
-      // the tile's dV/dK sums are complete once both issuers' MMAs are
-      mma_commit_warp(mma_done);
+      // The tile's dV/dK sums are complete once B's MMAs are; B alone writes them.  (With
+      // both issuers arriving, A could finish the next tile's products first and complete
+      // the phase early.)
+      if (warp == C::MMA_B_WARP) mma_commit_warp(mma_done);
       g0 += t.nsteps;
       ++ne;
     }
@@ -739,8 +741,9 @@ struct QCfg {
   // while dS(n) is formed and dQ(n) reads it; one at d_qk = 192
   static constexpr int DPB = D_QK <= 128 ? 2 : 1;
   // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_ready, dp_ready[DPB],
-  // ds_ready[DPB], mma_done, s_free, dq_done[DPB]
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 3 + 3 * DPB;
+  // ds_ready[DPB], mma_done, s_free, dq_done[DPB], qo_empty, acc_free, fin, tile_full[2],
+  // tile_empty[2]; the tile index ring (two ints) sits beside the TMEM address
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 3 + 3 * DPB + 7;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_RAW = OFF_TMEM_SLOT + 16 + 1024;
   static constexpr int SMEM = SMEM_RAW > 117 * 1024 ? SMEM_RAW : 117 * 1024;  // one CTA per SM
@@ -752,9 +755,13 @@ struct QCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone };
+enum QSite { kQQ = 0x40, kQKFull, kQKEmpty, kQVFull, kQVEmpty, kQS, kQDP, kQDS, kQDone, kQDrain, kQSFree, kQDqDone,
+             kQQEmpty, kQAccFree, kQTile };
 
-template <int D_QK, int D_V, bool VL, bool BIAS = false, bool DROP = false>
+// PERSIST: the CTAs (one per SM) take tiles from a counter in global memory, as the
+// persistent kv kernels do; otherwise the grid has one CTA per tile and the tile loops
+// run once (the cross-tile barriers compile away).
+template <int D_QK, int D_V, bool VL, bool BIAS = false, bool DROP = false, bool PERSIST = false>
 __global__ void __launch_bounds__(352, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -775,27 +782,62 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* mma_done = ds_ready + C::DPB;
   uint64_t* s_free = mma_done + 1;
   uint64_t* dq_done = s_free + 1;           // [DPB]
+  uint64_t* qo_empty = dq_done + C::DPB;    // a tile's Q/dO readers are done: the next Q/dO may load
+  uint64_t* acc_free = qo_empty + 1;        // the epilogue has read dQ: the next tile may overwrite it
+  uint64_t* fin = acc_free + 1;             // every MMA issued, before TMEM is released
+  uint64_t* tile_full = fin + 1;            // [2] PERSIST: the producer has published the next tile
+  uint64_t* tile_empty = tile_full + 2;     // [2] PERSIST: every role has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_TMEM_SLOT + 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order as in the kv kernel: (b, head) groups in chunks of kKvChunk (heads of a
+  // Tiles in the kv kernel's order: (b, head) groups in chunks of kKvChunk (heads of a
   // chunk share K and V in L2), within a chunk query tile by query tile, the tile with
-  // the most kv tiles (the last one when causal) first.
+  // the most kv tiles (the last one when causal) first.  Every role walks the same tiles
+  // and numbers the kv tiles of all of them in one sequence n (stages, barrier phases).
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
   const int n_gr = p.H_q * p.B;
+  const int n_tiles = n_qt * n_gr;
   const int per_chunk = kKvChunk * n_qt;
-  const int chunk = (int)blockIdx.x / per_chunk, within = (int)blockIdx.x % per_chunk;
-  const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
-  const int g = chunk * kKvChunk + within % csize;
-  const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
-  const int h = g % p.H_q, b = g / p.H_q, hk = h / p.G;
-  const int m0 = qt * C::BM;
-  const MaskSpec mask = VL ? MaskSpec{entry_len(p.seq_q, b, p.S_q), entry_len(p.seq_kv, b, p.S_kv), p.causal,
-                                      p.window}
-                           : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
-  int jlo = 1, jhi = 0;
-  const bool active = kv_tile_range(mask, m0, m0 + C::BM - 1, C::BN, &jlo, &jhi);
-  const int nj = active ? jhi - jlo + 1 : 0;
+  struct Tile {
+    int b, h, hk, m0, jlo, nj;
+    MaskSpec mask;
+  };
+  auto tile_of = [&](int ti) {
+    Tile t;
+    const int chunk = ti / per_chunk, within = ti % per_chunk;
+    const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
+    const int g = chunk * kKvChunk + within % csize;
+    const int qt = p.causal ? n_qt - 1 - within / csize : within / csize;
+    t.h = g % p.H_q;
+    t.b = g / p.H_q;
+    t.hk = t.h / p.G;
+    t.m0 = qt * C::BM;
+    t.mask = VL ? MaskSpec{entry_len(p.seq_q, t.b, p.S_q), entry_len(p.seq_kv, t.b, p.S_kv), p.causal, p.window}
+                : MaskSpec{p.S_q, p.S_kv, p.causal, p.window};
+    int jhi = 0;
+    t.jlo = 1;
+    const bool active = kv_tile_range(t.mask, t.m0, t.m0 + C::BM - 1, C::BN, &t.jlo, &jhi);
+    t.nj = active ? jhi - t.jlo + 1 : 0;
+    return t;
+  };
+  // Tile k of this CTA for the roles other than the producer (see the fused-dQ kv kernel).
+  auto take_tile = [&](int k, bool whole_warp) -> int {
+    if constexpr (!PERSIST) {
+      return k == 0 ? (int)blockIdx.x : n_tiles;
+    } else {
+      const int slot = k & 1;
+      if (!mbar_wait_warp(&tile_full[slot], (k >> 1) & 1, p.err, kQTile)) return n_tiles;
+      const int ti = ring[slot];
+      if (whole_warp) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&tile_empty[slot]);
+      } else {
+        mbar_arrive(&tile_empty[slot]);
+      }
+      return ti;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -807,8 +849,15 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&ds_ready[d], 256);
       mbar_init(&dq_done[d], 1);
     }
-    mbar_init(mma_done, 2);
+    mbar_init(mma_done, 1);  // issuer B, once per tile: it alone writes the dQ sum
     mbar_init(s_free, 256);
+    mbar_init(qo_empty, 1);   // issuer A's S and dP read Q and dO
+    mbar_init(acc_free, 256);
+    mbar_init(fin, 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tile_full[i], 1);
+      mbar_init(&tile_empty[i], 2 + 256);  // the two issuers (one lane each) and the dS threads
+    }
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -822,33 +871,72 @@ __global__ void __launch_bounds__(352, 1)
   int* err = p.err;
 
   if (warp == 9) {
-    if (lane == 0 && nj > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(q_full, (C::QCH + C::VCH) * C::CHUNK);
-      for (int c = 0; c < C::QCH; ++c) tma_load_4d(smem + C::OFF_Q + c * C::CHUNK, &tmQ, q_full, c * 64, h, m0, b);
-      for (int c = 0; c < C::VCH; ++c) tma_load_4d(smem + C::OFF_DO + c * C::CHUNK, &tmDO, q_full, c * 64, h, m0, b);
-      for (int n = 0; n < nj; ++n) {
-        const int j = jlo + n;
-        const int sk = n % C::NK, sv = n % C::NV;
-        if (!mbar_wait(&k_empty[sk], ((n / C::NK) & 1) ^ 1, err, kQKEmpty)) break;
-        mbar_arrive_expect_tx(&k_full[sk], C::QCH * C::CHUNK);
+    if (lane == 0) {
+      bool ok = true, first = true;
+      int n0 = 0, ne = 0, ti_next = 0;  // kv tiles and non-empty tiles so far
+      for (int k = 0;; ++k) {
+        int ti;
+        if constexpr (PERSIST) {  // publish tile k once every role has read tile k - 2
+          const int slot = k & 1;
+          if (k >= 2 && !mbar_wait(&tile_empty[slot], ((k >> 1) - 1) & 1, err, kQTile)) break;
+          ti = k == 0 ? atomicAdd(p.tile_counter_q, 1) : ti_next;
+          ring[slot] = ti;
+          mbar_arrive(&tile_full[slot]);
+        } else {
+          ti = k == 0 ? (int)blockIdx.x : n_tiles;
+        }
+        if (ti >= n_tiles || !ok) break;
+        const Tile t = tile_of(ti);
+        if (t.nj == 0) {
+          if constexpr (PERSIST) ti_next = atomicAdd(p.tile_counter_q, 1);
+          continue;
+        }
+        if (first) {
+          tma_prefetch_desc(&tmQ);
+          tma_prefetch_desc(&tmK);
+          tma_prefetch_desc(&tmV);
+          tma_prefetch_desc(&tmDO);
+          first = false;
+        }
+        // Q/dO of this tile replace the previous tile's once its S and dP products are done
+        if (PERSIST && ne > 0 && !mbar_wait(qo_empty, (ne - 1) & 1, err, kQQEmpty)) break;
+        mbar_arrive_expect_tx(q_full, (C::QCH + C::VCH) * C::CHUNK);
         for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(smem + C::OFF_K + (sk * C::QCH + c) * C::CHUNK, &tmK, &k_full[sk], c * 64, hk, j * C::BN, b);
-        if (!mbar_wait(&v_empty[sv], ((n / C::NV) & 1) ^ 1, err, kQVEmpty)) break;
-        mbar_arrive_expect_tx(&v_full[sv], C::VCH * C::CHUNK);
+          tma_load_4d(smem + C::OFF_Q + c * C::CHUNK, &tmQ, q_full, c * 64, t.h, t.m0, t.b);
         for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::OFF_V + (sv * C::VCH + c) * C::CHUNK, &tmV, &v_full[sv], c * 64, hk, j * C::BN, b);
+          tma_load_4d(smem + C::OFF_DO + c * C::CHUNK, &tmDO, q_full, c * 64, t.h, t.m0, t.b);
+        for (int j0 = 0; j0 < t.nj; ++j0) {
+          const int n = n0 + j0, j = t.jlo + j0;
+          const int sk = n % C::NK, sv = n % C::NV;
+          if (!mbar_wait(&k_empty[sk], ((n / C::NK) & 1) ^ 1, err, kQKEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[sk], C::QCH * C::CHUNK);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(smem + C::OFF_K + (sk * C::QCH + c) * C::CHUNK, &tmK, &k_full[sk], c * 64, t.hk, j * C::BN,
+                        t.b);
+          if (!mbar_wait(&v_empty[sv], ((n / C::NV) & 1) ^ 1, err, kQVEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[sv], C::VCH * C::CHUNK);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::OFF_V + (sv * C::VCH + c) * C::CHUNK, &tmV, &v_full[sv], c * 64, t.hk, j * C::BN,
+                        t.b);
+        }
+        if constexpr (PERSIST) ti_next = atomicAdd(p.tile_counter_q, 1);
+        n0 += t.nj;
+        ++ne;
       }
-      mbar_wait(q_full, 0, err, kQDrain);
-      for (int s = 0; s < C::NK && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / C::NK) * C::NK;
+      // every copy this warp started must land before the CTA may exit
+      if (ne > 0) mbar_wait(q_full, (ne - 1) & 1, err, kQDrain);
+      for (int s = 0; s < C::NK && s < n0; ++s) {
+        const int last = s + ((n0 - 1 - s) / C::NK) * C::NK;
         mbar_wait(&k_full[s], (last / C::NK) & 1, err, kQDrain);
       }
-      for (int s = 0; s < C::NV && s < nj; ++s) {
-        const int last = s + ((nj - 1 - s) / C::NV) * C::NV;
+      for (int s = 0; s < C::NV && s < n0; ++s) {
+        const int last = s + ((n0 - 1 - s) / C::NV) * C::NV;
         mbar_wait(&v_full[s], (last / C::NV) & 1, err, kQDrain);
       }
     }
@@ -860,15 +948,25 @@ __global__ void __launch_bounds__(352, 1)
     // dQ(n - DPB), which read dS(n - DPB) from the same slot (dq_done of that slot).
     // Every per-slot barrier completes once per use of its slot, and a slot's next use
     // depends on the waiter having seen the previous one, so no phase is skipped.
-    if (nj > 0) {  // whole warp runs the loop; elect.sync picks the issuing lane
+    {  // whole warp runs the loops; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idDQ = idesc_bf16_f32(128, D_QK, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      bool ok = mbar_wait_warp(q_full, 0, err, kQQ);
+      bool ok = true;
+      int n0 = 0, ne = 0;
+      for (int k = 0;; ++k) {
+      const int ti = take_tile(k, true);
+      if (ti >= n_tiles || !ok) break;
+      const Tile t = tile_of(ti);
+      if (t.nj == 0) continue;
       if (warp == 8) {
+        // Q and dO of the tile: only A's products read them (a wait nothing gates could
+        // see a later phase complete)
+        ok = mbar_wait_warp(q_full, ne & 1, err, kQQ);
         const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
-        for (int n = 0; n < nj && ok; ++n) {
+        for (int j0 = 0; j0 < t.nj && ok; ++j0) {
+          const int n = n0 + j0;
           const int sk = n % C::NK, sv = n % C::NV;
           const uint64_t dKa = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, 16, 1024);
           const uint64_t dVa = smem_desc_sw128(sV + sv * C::VCH * C::CHUNK, 16, 1024);
@@ -896,13 +994,17 @@ __global__ void __launch_bounds__(352, 1)
           mma_commit_warp(&dp_ready[ds]);
           mma_commit_warp(&v_empty[sv]);
         }
+        if constexpr (PERSIST) mma_commit_warp(qo_empty);  // the tile's S and dP products have read Q and dO
       } else {
-        for (int n = 0; n < nj && ok; ++n) {
+        for (int j0 = 0; j0 < t.nj && ok; ++j0) {
+          const int n = n0 + j0;
           const int sk = n % C::NK;
           const uint64_t dKmn = smem_desc_sw128(sK + sk * C::QCH * C::CHUNK, C::CHUNK, 1024);
           const int ds = n % C::DPB;
           ok = mbar_wait_warp(&k_full[sk], (n / C::NK) & 1, err, kQKFull) &&
                mbar_wait_warp(&ds_ready[ds], (n / C::DPB) & 1, err, kQDS);
+          // the first dQ of a tile overwrites the sum the previous tile's epilogue reads
+          if (PERSIST && ok && j0 == 0 && ne > 0) ok = mbar_wait_warp(acc_free, (ne - 1) & 1, err, kQAccFree);
           if (!ok) break;
           tc_fence_after();
           // dQ += dS K   (dS bf16 over the slot's dP columns: keys 0-63 at cols 0-31, keys 64-127 at cols 64-95)
@@ -910,23 +1012,41 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
             mma_ts_warp(tmem + C::COL_DQ, colP + (kk / 4) * 64 + (kk % 4) * 8, desc_add(dKmn, kk * 2048),
-                   idDQ, (n > 0 || kk > 0) ? 1u : 0u);
+                   idDQ, (j0 > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(&dq_done[ds]);
           mma_commit_warp(&k_empty[sk]);  // S(n) (issuer A) completed before dS(n) existed
         }
       }
-      mma_commit_warp(mma_done);
-      mbar_wait_warp(mma_done, 0, err, kQDone);
+      // The tile's dQ sum is complete once B's MMAs are; B alone writes it.  (With both
+      // issuers arriving, A could finish the next tile's products first and complete the
+      // phase early.)
+      if (warp == 10) mma_commit_warp(mma_done);
+      n0 += t.nj;
+      ++ne;
+      }
+      // Every MMA of both issuers must be complete before TMEM is released.
+      mma_commit_warp(fin);
+      mbar_wait_warp(fin, 0, err, kQDone);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ dS warpgroups: thread = query row
     const int w = warp / 4;  // keys 64w .. 64w+63 of each kv tile
     const int r = (warp % 4) * 32 + lane;
-    const int i = m0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const float sl2 = p.scale_log2;
+    [[maybe_unused]] const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
+    [[maybe_unused]] DropState drop{};
+    if constexpr (DROP) drop = DropState{p.rng[0], p.rng[1], p.drop_t};
+    bool ok = true;
+    int n0 = 0, ne = 0;
+    for (int k = 0;; ++k) {
+    const int ti = take_tile(k, false);
+    if (ti >= n_tiles) break;
+    const Tile t = tile_of(ti);
+    const int b = t.b, h = t.h;
+    const int i = t.m0 + r;
     float nl2row = -INFINITY, drow = 0.f;
-    if (i < p.S_q) {
+    if (i < p.S_q && t.nj > 0) {
       const size_t ri = ((size_t)b * p.H_q + h) * p.S_pad + i;
       nl2row = p.nlse2[ri];
       drow = p.Dsum[ri];
@@ -934,12 +1054,9 @@ __global__ void __launch_bounds__(352, 1)
     // bias: this row of the bias plane (rows past S_q read row S_q - 1; their P is 0)
     [[maybe_unused]] const __nv_bfloat16* brow =
         BIAS ? p.bias + b * p.bias_sb + h * p.bias_sh + (size_t)min(i, p.S_q - 1) * p.S_kv : nullptr;
-    [[maybe_unused]] const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
-    [[maybe_unused]] DropState drop{};
-    if constexpr (DROP) drop = DropState{p.rng[0], p.rng[1], p.drop_t};
-    bool ok = true;
-    for (int n = 0; n < nj && ok; ++n) {
-      const int k0 = (jlo + n) * C::BN + 64 * w;
+    for (int j0 = 0; j0 < t.nj && ok; ++j0) {
+      const int n = n0 + j0;
+      const int k0 = (t.jlo + j0) * C::BN + 64 * w;
       // dropout: keep bits of this row for keys k0 .. k0 + 63 (bit c of keep[q]: key k0 + 32 q + c),
       // generated while the tile's scores are still being computed
       [[maybe_unused]] uint32_t keep[2] = {0u, 0u};
@@ -952,7 +1069,7 @@ __global__ void __launch_bounds__(352, 1)
       ok = mbar_wait_warp(s_ready, n & 1, err, kQS);
       if (!ok) break;
       tc_fence_after();
-      const bool full = tile_fully_visible<VL>(mask, m0, C::BM, (jlo + n) * C::BN, C::BN);
+      const bool full = tile_fully_visible<VL>(t.mask, t.m0, C::BM, (t.jlo + j0) * C::BN, C::BN);
       float pr[64];
       {
         uint32_t ra[32], rb[32];
@@ -996,7 +1113,7 @@ __global__ void __launch_bounds__(352, 1)
       }
       if (!full) {  // this row sees keys [vlo, vhi]: two compares per key
         int vlo, vhi;
-        visible_keys<VL>(mask, i, &vlo, &vhi);
+        visible_keys<VL>(t.mask, i, &vlo, &vhi);
 #pragma unroll
         for (int c = 0; c < 64; ++c) pr[c] = (k0 + c >= vlo && k0 + c <= vhi) ? pr[c] : 0.f;
       }
@@ -1035,10 +1152,11 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_before();
       mbar_arrive(&ds_ready[ds]);
     }
-    // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2)
+    // epilogue: dQ = scale * acc; warpgroup w writes head-dim columns [w*D_QK/2, (w+1)*D_QK/2).
+    // A tile whose rows see no key (nj = 0) writes zeros and touches neither TMEM nor a barrier.
     bool have = false;
-    if (ok && nj > 0) {
-      have = mbar_wait_warp(mma_done, 0, err, kQDone);
+    if (ok && t.nj > 0) {
+      have = mbar_wait_warp(mma_done, ne & 1, err, kQDone);
       tc_fence_after();
     }
     {
@@ -1066,6 +1184,15 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
     }
+    if (t.nj > 0) {
+      if constexpr (PERSIST) {  // the sum is read: issuer B may start the next tile's dQ
+        tc_fence_before();
+        mbar_arrive(acc_free);
+      }
+      n0 += t.nj;
+      ++ne;
+    }
+    }
   }
 
   tc_fence_before();
@@ -1083,6 +1210,16 @@ inline int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   using C = QCfg<D_QK, D_V>;
   const bool vl = p.seq_q || p.seq_kv;  // padded batches: per-entry lengths and row tests
   decltype(&attn_bwd_q_kernel<D_QK, D_V, false>) kern;
+  const long long tiles = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
+  if (tiles <= 0 || tiles > 0x7fffffffLL) return -2;
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+      return -1;
+  }
+  bool persist = false;
   if constexpr (KV == KernVariant::kDrop) {  // dropout: full-length batches without a bias
     if (vl || p.bias) return -2;
     kern = attn_bwd_q_kernel<D_QK, D_V, false, false, true>;
@@ -1091,12 +1228,21 @@ inline int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     kern = vl ? attn_bwd_q_kernel<D_QK, D_V, true, true> : attn_bwd_q_kernel<D_QK, D_V, false, true>;
   } else {
     if (p.bias) return -2;
-    kern = vl ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
+    // Persistent CTAs (one per SM, tiles from the counter) for the plain kernels of
+    // full-length batches with d_qk = d_v when every tile is short: at most 8 kv tiles,
+    // so a CTA's fixed costs (the Q/dO load, the first products, the dQ epilogue) are a
+    // large share of a tile's time.
+    const long long max_kv = (p.S_kv + C::BN - 1) / C::BN;
+    if constexpr (D_QK == D_V) persist = !vl && p.tile_counter_q && tiles > n_sm && max_kv <= 8;
+    if (persist) {
+      if constexpr (D_QK == D_V) kern = attn_bwd_q_kernel<D_QK, D_V, false, false, false, true>;
+    } else {
+      kern = vl ? attn_bwd_q_kernel<D_QK, D_V, true> : attn_bwd_q_kernel<D_QK, D_V, false>;
+    }
   }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
-  const long long blocks = (long long)((p.S_q + C::BM - 1) / C::BM) * p.H_q * p.B;
-  if (blocks <= 0 || blocks > 0x7fffffffLL) return -2;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  const unsigned grid = (unsigned)(persist ? n_sm : tiles);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

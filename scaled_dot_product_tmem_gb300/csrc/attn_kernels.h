@@ -74,7 +74,10 @@ struct BwdParams {
   float* dk_part;             // ns > 1: [ns, B, S_kv, H_kv, d_qk] fp32 partial dK (scaled), one slice per split
   float* dv_part;             // ns > 1: [ns, B, S_kv, H_kv, d_v] fp32 partial dV
   float* dq_acc;              // [B, S_q, H_q, d_qk] fp32 workspace (atomic dQ path) or null
-  int* tile_counter = nullptr;  // fused-dQ path: next tile of the persistent kv kernel (the preprocess zeroes it)
+  // next tile of the persistent kv kernel and of the persistent dQ kernel (workspace ints
+  // the preprocess zeroes; null: those kernels run one CTA per tile)
+  int* tile_counter = nullptr;
+  int* tile_counter_q = nullptr;
   int* err;
   // additive bias [Bb, Hb, S_q, S_kv] (bf16) or null, with the element strides of batch
   // and head (0 along a broadcast dim); dbias: fp32, same shape and strides, zeroed by

@@ -76,18 +76,18 @@ def test_bwd_workspace_and_validation(lib):
     det = sdpa.attn_bwd_workspace_size(4, 2048, 2048, 32, 8, 128, 128, True)
     atom = sdpa.attn_bwd_workspace_size(4, 2048, 2048, 32, 8, 128, 128, False)
     rows = 4 * 32 * 2048
-    assert det == 2 * rows * 4                          # lse2 + D, fp32
-    assert atom == det + 4 * 2048 * 32 * 128 * 4 + 256  # + fp32 dQ accumulator, tile counter
+    assert det == 2 * rows * 4 + 256                    # lse2 + D (fp32), tile counters
+    assert atom == det + 4 * 2048 * 32 * 128 * 4        # + fp32 dQ accumulator
     # B=1, S=100, H_kv=2: 2 kv CTAs, so the 2 query heads of each group go to 2 CTAs
     # and the workspace adds 2 fp32 partial slices of dK and dV
     part = 2 * 1 * 100 * 2 * 64 * 4
-    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4 + 2 * part
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 2, 64, 64, True) == 2 * 4 * 128 * 4 + 2 * part + 256
     # MQA at 32,768 tokens: 256 kv CTAs (under 3 per SM) -> 4 splits, 1024 CTAs
     mqa = sdpa.attn_bwd_workspace_size(4, 8192, 8192, 32, 1, 128, 128, True)
-    assert mqa == 2 * 4 * 32 * 8192 * 4 + 2 * 4 * (4 * 8192 * 1 * 128 * 4)
+    assert mqa == 2 * 4 * 32 * 8192 * 4 + 2 * 4 * (4 * 8192 * 1 * 128 * 4) + 256
     # GQA B=4 S=2048 H_kv=8: 512 CTAs, no split (checked above: det has no partials)
     # MHA has no head loop to split
-    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 4, 64, 64, True) == 2 * 4 * 128 * 4
+    assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 4, 64, 64, True) == 2 * 4 * 128 * 4 + 256
     assert sdpa.attn_bwd_workspace_size(1, 100, 100, 4, 3, 64, 64, True) == 0
 
     def bwd(ws=P, ws_bytes=1 << 30, q=P, Hq=4, Hkv=2, st=0, doff=None, off=None, window=-1, causal=1):

@@ -111,8 +111,8 @@ def test_empty_problem_is_a_noop():
     assert torch.all(dk == 0) and torch.all(dv == 0)
 
 
-# Grids of many short tiles run the fused-dQ kv kernel with persistent CTAs (at most 16
-# steps per tile and at least four tiles per SM); these cases take that path.
+# Grids of many short tiles run the backward kernels with persistent CTAs (more tiles
+# than SMs, each of a few steps); these cases take that path.
 PERSIST_CASES = [
     # name, shape, causal, window, softmax type
     ("mha_ragged_d64_learnable", Shape(16, 300, 300, 40, 40, 64, 64), True, -1, LEARNABLE),
@@ -122,14 +122,16 @@ PERSIST_CASES = [
 ]
 
 
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused_dq", "det"])
 @pytest.mark.parametrize("case", PERSIST_CASES, ids=[c[0] for c in PERSIST_CASES])
-def test_persistent_kv_tiles_match_oracle(case):
-    """The fused-dQ path on grids of many short tiles, against the oracle on sampled
-    (batch, head) units; with S_q < S_kv, the keys no query sees get zero gradients."""
+def test_persistent_kv_tiles_match_oracle(case, deterministic):
+    """Both backward paths on grids of many short tiles (persistent CTAs in the kv and
+    dQ kernels), against the oracle on sampled (batch, head) units; with S_q < S_kv, the
+    keys no query sees get zero gradients."""
     name, shape, causal, window, st = case
     x = make_inputs(shape, 31, learnable_offset=True)
     kw = dict(causal=causal, window=window, softmax_type=st, scale=None)
-    gpu = gpu_run(x, deterministic=False, **kw)
+    gpu = gpu_run(x, deterministic=deterministic, **kw)
     for b, g in ((0, 0), (shape.B - 1, shape.H_kv - 1)):
         ref = oracle_run(slice_group(x, b, g, 1), **kw)
         ref.pop("d_offset", None)

@@ -8,9 +8,12 @@ failure has already run every other test.  It calls the entry point through the 
 ABI three times in a row with different shapes, so each later call runs on an array
 that still holds the previous call's contents, and checks:
   * against attn_bwd with deterministic != 0: bitwise equal where attn_bwd also walks
-    every query head of a kv group in one CTA (no head split: the same kernels on the
+    every query head of a kv group in one CTA (no head split: the same arithmetic on the
     same inputs), within the gradient tolerance where attn_bwd splits the heads (its
-    partial dK/dV slices add in another fp32 order);
+    partial dK/dV slices add in another fp32 order).  On grids of many short tiles
+    attn_bwd runs persistent CTAs that take their tiles from a counter, and this entry
+    point (no counter in its scratch) one CTA per tile: the bitwise comparison then also
+    checks the persistent kernels' tile hand-over;
   * against the fp64 oracle on the first shape, with the tolerances of every other
     parity test.
 """
@@ -84,9 +87,30 @@ def test_no_alloc_backward_three_calls_in_a_row():
     assert not _splits(shape)
     _run_both(sdpa, lib, shape, 202, sdpa.VANILLA, -1)
     # third call: GQA with 512 kv CTAs (no split), off-by-one sink: bitwise equal to attn_bwd
+    # (whose dQ kernel runs persistent CTAs here)
     shape = Shape(16, 512, 512, 16, 8, 64, 64)
     assert not _splits(shape)
     _run_both(sdpa, lib, shape, 203, sdpa.OFF_BY_ONE, -1)
+    # fourth call: MHA d = 128 at S = 512, where attn_bwd's kv and dQ kernels both run
+    # persistent CTAs and the last kv tile of each sequence is a single step
+    shape = Shape(16, 512, 512, 16, 16, 128, 128)
+    assert not _splits(shape)
+    _run_both(sdpa, lib, shape, 204, sdpa.VANILLA, -1)
+
+
+def test_persistent_deterministic_backward_repeats_bitwise():
+    """Two deterministic backward calls on a grid of many one- and two-step tiles, where
+    the kv and dQ kernels hand tiles out through a counter, give the same bits."""
+    import scaled_dot_product_tmem_gb300 as sdpa
+    dev = torch.device("cuda")
+    x = make_inputs(Shape(32, 384, 384, 16, 16, 128, 128), 205)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = sdpa.sdpa_forward(q, k, v, causal=True)
+    a = sdpa.sdpa_backward(q, k, v, o, do, lse, causal=True, deterministic=True)
+    b = sdpa.sdpa_backward(q, k, v, o, do, lse, causal=True, deterministic=True)
+    torch.cuda.synchronize()
+    for ta, tb in zip(a[:3], b[:3]):
+        assert torch.equal(ta, tb)
 
 
 def test_no_alloc_rejects_problems_beyond_its_array():
