@@ -118,7 +118,7 @@ WORKLOADS["bias_gqa_b2_s4096"] = _w(
 # Attention dropout p = 0.1 on the target point and on the GQA + SWA training shape.
 WORKLOADS["dropout_gqa_b4_s8192"] = _w(
     "dropout_gqa_b4_s8192", 4, 8192, 32, 8, 128, 128, True, -1, 0, None, 1000 + 8192 + 8,
-    "attention dropout p=0.1 (Philox4x64-10 decisions): B=4, S=8192, H_q=32, H_kv=8, d=128, causal", dropout=0.1)
+    "attention dropout p=0.1 (Philox4x32-10 decisions): B=4, S=8192, H_q=32, H_kv=8, d=128, causal", dropout=0.1)
 WORKLOADS["dropout_gqa_swa_b4_s2048"] = _w(
     "dropout_gqa_swa_b4_s2048", 4, 2048, 32, 8, 128, 128, True, 1024, 0, None, 1,
     "attention dropout p=0.1 on the GQA + SWA training shape: B=4, S=2048, H_q=32, H_kv=8, d=128, causal, "

@@ -204,9 +204,10 @@ const char* attn_bwd_noalloc_message(void);
  * while LSE (and p_sink) are those of the undropped softmax.  The backward uses
  *   dS_ij = P_ij (M_ij dO_i . v_j - D_i),   D_i = dO_i . O_i,   dV_j = sum_i P_ij M_ij dO_i.
  * The decisions come from a counter-based generator, so the backward regenerates
- * them: Philox4x64-10 (Salmon et al., SC'11) keyed by rng_state = (seed, offset);
- * pair (b, h, i, j) uses the counter (j / 4, i / 4, h, b), output word i % 4, 16-bit
- * field j % 4 as a uniform u in [0, 65536), and is kept iff u >= t.
+ * them: Philox4x32-10 (Salmon et al., SC'11).  With rng_state = (seed, offset), the key
+ * is the seed (low 32 bits, high 32 bits); pair (b, h, i, j) uses the counter
+ * (j / 2, i / 4, 65536 b + h, offset mod 2^32), output word i % 4, 16-bit field j % 2
+ * as a uniform u in [0, 65536), and is kept iff u >= t.
  *
  * dropout_p: drop probability in [0, 1), realised as t / 65536 with
  *   t = floor(dropout_p * 65536 + 1/2) (from the float value); t = 0 runs the plain
@@ -214,7 +215,9 @@ const char* attn_bwd_noalloc_message(void);
  *   ATTN_ERR_INVALID_ARG.
  * rng_state: DEVICE pointer to two uint64 values, seed then offset, 8-byte aligned,
  *   read by the kernels when they run (so a caller can advance the offset in place
- *   between steps).  Pass the same state to the forward and the backward of a step.
+ *   between steps).  Only the offset's low 32 bits are used: offsets that differ by a
+ *   multiple of 2^32 give the same decisions.  Pass the same state to the forward and
+ *   the backward of a step.
  * Otherwise as attn_fwd / attn_bwd (same workspace as attn_bwd).  Supported: full-length
  * batches, no bias, (d_qk, d_v) in {(64, 64), (128, 128), (192, 128)}; other head dims
  * return ATTN_ERR_UNSUPPORTED.

@@ -63,8 +63,9 @@ def _load():
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, i, d, i, i, i, dp, dp, i, i, i, u64, u64, i, i,
                                    dp, dp, dp, dp, dp, dp]
         lib.oracle_bwd.restype = ctypes.c_int
-        lib.oracle_philox4x64_10.argtypes = [ctypes.POINTER(u64), ctypes.POINTER(u64), ctypes.POINTER(u64)]
-        lib.oracle_philox4x64_10.restype = None
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        lib.oracle_philox4x32_10.restype = None
         lib.oracle_dropout_keep.argtypes = [i, i, i, i, i, u64, u64, ctypes.POINTER(ctypes.c_ubyte)]
         lib.oracle_dropout_keep.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
@@ -104,13 +105,13 @@ def dropout_threshold(p: float) -> int:
     return t
 
 
-def philox4x64_10(counter, key):
-    """Philox4x64-10 of one 4 x 64-bit counter under a 2 x 64-bit key (four uint64 words)."""
-    c = (ctypes.c_uint64 * 4)(*[int(x) & (2 ** 64 - 1) for x in counter])
-    k = (ctypes.c_uint64 * 2)(*[int(x) & (2 ** 64 - 1) for x in key])
-    out = (ctypes.c_uint64 * 4)()
-    _load().oracle_philox4x64_10(c, k, out)
-    return np.array(list(out), dtype=np.uint64)
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of one 4 x 32-bit counter under a 2 x 32-bit key (four uint32 words)."""
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in counter])
+    k = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    out = (ctypes.c_uint32 * 4)()
+    _load().oracle_philox4x32_10(c, k, out)
+    return np.array(list(out), dtype=np.uint32)
 
 
 def dropout_keep(b, h, Sq, Skv, p, rng_state):

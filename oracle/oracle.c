@@ -58,12 +58,13 @@
  * probability 1 - p and scaled by 1/(1 - p), or dropped to 0; the normaliser, LSE and
  * p_sink are those of the undropped softmax.  The keep decisions come from a
  * counter-based generator, so the backward regenerates them from the same state:
- *   - Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
- *     as 1, 2, 3", SC'11): ten rounds on a 4 x 64-bit counter with a 2 x 64-bit key;
- *   - key = (seed, offset) = the rng_state; counter of pair (b, h, i, j) =
- *     (j / 4, i / 4, h, b);
- *   - the call yields four 64-bit words; pair (i, j) takes word i % 4 and, within it,
- *     the 16-bit field j % 4 (bits 16 (j % 4) .. 16 (j % 4) + 15), a uniform u in
+ *   - Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ *     as 1, 2, 3", SC'11): ten rounds on a 4 x 32-bit counter with a 2 x 32-bit key;
+ *   - the rng_state is (seed, offset), two 64-bit words.  The key is the seed (low
+ *     word first); the counter of pair (b, h, i, j) is
+ *     (j / 2, i / 4, 65536 b + h, offset mod 2^32), so b and h are below 65536;
+ *   - the call yields four 32-bit words; pair (i, j) takes word i % 4 and, within it,
+ *     the 16-bit field j % 2 (bits 16 (j % 2) .. 16 (j % 2) + 15), a uniform u in
  *     [0, 65536);
  *   - the drop probability is realised as t / 65536 with t = floor(p * 65536 + 1/2);
  *     the pair is kept iff u >= t, and a kept P is multiplied by 65536 / (65536 - t).
@@ -103,21 +104,21 @@ static const double* bias_plane(const double* bias, int Bb, int Hb, int b, int h
 }
 
 /*
- * Philox4x64-10 (SC'11 paper cited above).  One round maps the counter
+ * Philox4x32-10 (SC'11 paper cited above).  One round maps the counter
  * (c0, c1, c2, c3) with key (k0, k1) to
  *   (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)),
- * hi/lo the upper/lower 64 bits of the 128-bit product; between rounds the key is
+ * hi/lo the upper/lower 32 bits of the 64-bit product; between rounds the key is
  * bumped by the Weyl constants (W0, W1).  Ten rounds, the first with the key itself.
  */
-void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
     for (int r = 0; r < 10; r++) {
         if (r > 0) { k0 += W0; k1 += W1; }
-        unsigned __int128 p0 = (unsigned __int128)M0 * c0, p1 = (unsigned __int128)M1 * c2;
-        uint64_t n0 = (uint64_t)(p1 >> 64) ^ c1 ^ k0, n1 = (uint64_t)p1;
-        uint64_t n2 = (uint64_t)(p0 >> 64) ^ c3 ^ k1, n3 = (uint64_t)p0;
+        uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
         c0 = n0; c1 = n1; c2 = n2; c3 = n3;
     }
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
@@ -128,12 +129,13 @@ void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t
  * from (0 for a whole problem): the decisions are those of (b + b0, h + h0). */
 typedef struct { int t; uint64_t seed, offset; int b0, h0; } dropout_t;
 
-/* The 16-bit uniform of pair (b, h, i, j) (see the header). */
+/* The 16-bit uniform of pair (b, h, i, j) (see the header); b, h < 65536. */
 static unsigned dropout_u16(const dropout_t* d, int b, int h, int i, int j) {
-    uint64_t ctr[4] = {(uint64_t)(j / 4), (uint64_t)(i / 4), (uint64_t)h, (uint64_t)b};
-    uint64_t key[2] = {d->seed, d->offset}, w[4];
-    oracle_philox4x64_10(ctr, key, w);
-    return (unsigned)((w[i % 4] >> (16 * (j % 4))) & 0xFFFFu);
+    uint32_t ctr[4] = {(uint32_t)(j / 2), (uint32_t)(i / 4), (uint32_t)b * 65536u + (uint32_t)h,
+                       (uint32_t)d->offset};
+    uint32_t key[2] = {(uint32_t)d->seed, (uint32_t)(d->seed >> 32)}, w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    return (w[i % 4] >> (16 * (j % 2))) & 0xFFFFu;
 }
 
 /* M_ij: 65536 / (65536 - t) if the pair is kept, 0 if dropped; 1 without dropout. */
@@ -145,7 +147,7 @@ static double dropout_mult(const dropout_t* d, int b, int h, int i, int j) {
 /* The keep decisions of one (b, h) as bytes [Sq * Skv] (1 kept, 0 dropped), for tests. */
 int oracle_dropout_keep(int b, int h, int Sq, int Skv, int t, uint64_t seed, uint64_t offset,
                         unsigned char* keep) {
-    if (t < 0 || t > 65535) return -1;
+    if (t < 0 || t > 65535 || b < 0 || b > 65535 || h < 0 || h > 65535) return -1;
     dropout_t d = {t, seed, offset, 0, 0};
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < Sq; i++)
@@ -215,6 +217,7 @@ int oracle_fwd(const double* q, const double* k, const double* v,
                double* o, double* lse, double* psink, double* rowsum) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
     if (drop_t < 0 || drop_t > 65535 || drop_b0 < 0 || drop_h0 < 0) return -1;
+    if (drop_t > 0 && ((long)drop_b0 + B > 65536 || (long)drop_h0 + Hq > 65536)) return -1;
     dropout_t drop = {drop_t, seed, offset_rng, drop_b0, drop_h0};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;
@@ -270,6 +273,7 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                double* dq, double* dk, double* dvout, double* d_offset, double* Dout, double* dbias) {
     if (B < 0 || Sq < 0 || Skv < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return -1;
     if (drop_t < 0 || drop_t > 65535 || drop_b0 < 0 || drop_h0 < 0) return -1;
+    if (drop_t > 0 && ((long)drop_b0 + B > 65536 || (long)drop_h0 + Hq > 65536)) return -1;
     dropout_t drop = {drop_t, seed, offset_rng, drop_b0, drop_h0};
     if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq))) return -1;
     if (softmax_type == ORACLE_LEARNABLE && !offset) return -1;

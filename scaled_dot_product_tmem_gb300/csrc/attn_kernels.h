@@ -26,7 +26,7 @@ struct FwdParams {
   const __nv_bfloat16* bias = nullptr;
   long long bias_sb = 0, bias_sh = 0;
   int bias_tma = 0;  // head dims <= 128: the bias tiles are staged by TMA (S_kv % 8 == 0)
-  // attention dropout (drop_t > 0): rng = device [seed, offset] (the Philox key), drop
+  // attention dropout (drop_t > 0): rng = device [seed, offset] (the Philox key and counter), drop
   // threshold t (16-bit uniforms below it are dropped), kept values scaled by drop_scale
   const unsigned long long* rng = nullptr;
   unsigned drop_t = 0;

@@ -63,12 +63,15 @@ def rel_l2(a, ref):
     return num / den if den > 0 else num
 
 
-def compare(gpu, ref, what=""):
-    """Assert every tolerance; return a dict of the measured errors."""
+def compare(gpu, ref, what="", o_scale=1.0):
+    """Assert every tolerance; return a dict of the measured errors.  o_scale multiplies
+    the O bound: under attention dropout O is 1/(1 - p) times a sum of the same kind as
+    the plain path's O (kept probabilities times values), so its bf16 errors scale by
+    that factor (see dropout_o_scale)."""
     errs = {}
     assert gpu["o"].shape == ref["o"].shape
     errs["o"] = float(np.abs(gpu["o"] - ref["o"]).max()) if ref["o"].size else 0.0
-    assert errs["o"] <= TOL_O, f"{what}: O max-abs {errs['o']}"
+    assert errs["o"] <= TOL_O * o_scale, f"{what}: O max-abs {errs['o']} (bound {TOL_O * o_scale})"
     fin = np.isfinite(ref["lse"])
     assert np.array_equal(fin, np.isfinite(gpu["lse"])), f"{what}: LSE finiteness differs"
     assert np.all(gpu["lse"][~fin] == ref["lse"][~fin]), f"{what}: infinite LSE differs"
@@ -82,10 +85,22 @@ def compare(gpu, ref, what=""):
     return errs
 
 
+def dropout_o_scale(p):
+    """The O bound's factor under dropout probability p: the kept-value multiplier
+    65536 / (65536 - t), t = floor(65536 p + 1/2).  O_i = s sum_j P_ij keep_ij v_j: the sum
+    is a sub-convex combination of value rows, as the plain O is, and the kernel applies
+    s in fp32 before the one bf16 rounding of O, so every error term of O is s times the
+    plain path's.  The relative-L2 gradient bounds are scale-free and LSE is the undropped
+    one, so neither changes."""
+    t = int(np.floor(p * 65536.0 + 0.5))
+    return 65536.0 / (65536.0 - t)
+
+
 BF16_U = 2.0 ** -8  # unit roundoff of bf16 (8 significant bits)
 
 
-def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0):
+def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0, dropout_p=0.0, rng_state=None,
+                   dropout_origin=(0, 0)):
     """Tolerance for the learnable sink's d_offset, from the rounding the design imposes.
 
     d_offset_h = -sum_{b,i} p_i D_i, with p_i = exp(o_h - LSE_i) and D_i = dO_i . O_i.
@@ -110,6 +125,13 @@ def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0):
     (scale, offset and bias times 2) on v^2 gives sum_j P'_ij v_jd^2, with
     P'_ij = P_ij^2 e^{2 LSE_i - LSE'_i}.
 
+    With attention dropout (dropout_p, rng_state, dropout_origin as the oracle takes
+    them) O_i = s sum_j P_ij M_ij v_j, M the keep decisions and s = 1/(1 - p) the kept
+    multiplier.  The kernel rounds the kept P to bf16 and applies s in fp32 before the
+    output rounding, so the P term becomes s^2 sum_j P_ij^2 M_ij v_jd^2.  The doubled-logit
+    forward with the same decisions returns s sum_j P'_ij M_ij v_jd^2, one factor s short.
+    D, p_sink and the exact d_offset come from the oracle with the same dropout.
+
     `gpu` holds the kernel's stored O ("o") and LSE ("lse").  Returns
       (exact d_offset, tolerance, the formula in fp64 on the stored O, kernel tolerance).
     The kernel tolerance is the deterministic part alone.  The last two isolate the
@@ -118,6 +140,10 @@ def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0):
     xd = {n: t.double().numpy() for n, t in x.items()}
     sc = oracle.default_scale(xd["q"].shape[-1]) if scale is None else float(scale)
     kw = dict(causal=causal, window=window, softmax_type=oracle.LEARNABLE, offset=xd["offset"], scale=sc)
+    drop_s = 1.0
+    if dropout_p > 0.0:
+        kw.update(dropout_p=dropout_p, rng_state=rng_state, dropout_origin=dropout_origin)
+        drop_s = dropout_o_scale(dropout_p)
     kw2 = dict(kw, offset=2.0 * xd["offset"], scale=2.0 * sc)
     if bias is not None:
         kw["bias"] = bias
@@ -128,7 +154,7 @@ def d_offset_bound(x, gpu, *, causal, window, scale, bias=None, sigmas=6.0):
     with np.errstate(invalid="ignore"):
         w = np.exp(f2["lse"] - 2.0 * f["lse"])                       # [B, H_q, S_q]
     w = np.where(np.isfinite(w), w, 0.0)
-    p2v2 = f2["o"] * np.transpose(w, (0, 2, 1))[..., None]          # sum_j P_ij^2 v_jd^2
+    p2v2 = drop_s * f2["o"] * np.transpose(w, (0, 2, 1))[..., None]  # (s^2) sum_j P_ij^2 (M_ij) v_jd^2
     var_o = BF16_U ** 2 / 3.0 * (f["o"] ** 2 + p2v2)
     dO = xd["dout"]
     var_d = np.einsum("bshd,bshd->bhs", dO ** 2, var_o)

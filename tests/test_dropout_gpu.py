@@ -10,7 +10,8 @@ Two kinds of check:
         M_id - mean_j M_ij.
     All three are compared with oracle.dropout_keep, and the keep rate is held to
     binomial bounds;
-  * parity of O, LSE, dQ, dK, dV and d_offset with the oracle at the stated tolerances,
+  * parity of O, LSE, dQ, dK, dV and d_offset with the oracle at the stated tolerances
+    (the O bound times the kept-value multiplier 1/(1 - p), see dropout_o_scale),
     for p in {0.1, 0.5}, on both dQ paths, the sink types, GQA, windows, MLA dims and
     ragged sizes, and that a fixed rng_state is bitwise reproducible.
 """
@@ -20,7 +21,7 @@ import torch
 
 import oracle
 from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
-from parity_util import compare, rel_l2
+from parity_util import check_d_offset_bound, compare, dropout_o_scale, rel_l2
 from scaled_dot_product_tmem_gb300.inputs import Shape, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -159,7 +160,18 @@ def test_dropout_parity(case, p, det):
     name, shape, causal, window, st, scale = case
     x = make_inputs(shape, 900 + CASES.index(case), learnable_offset=True)
     kw = dict(causal=causal, window=window, st=st, scale=scale, p=p)
-    compare(_gpu(x, det=det, **kw), _ref(x, **kw), f"{name} p={p}")
+    _check(x, _gpu(x, det=det, **kw), _ref(x, **kw), f"{name} p={p}", kw)
+
+
+def _check(x, gpu, ref, what, kw):
+    """compare() at the dropout O bound.  The learnable sink's d_offset is held to the
+    derived bound (parity_util.d_offset_bound, with the same dropout), as for the other
+    cases whose d_offset terms cancel."""
+    if "d_offset" in ref:
+        ref = {n: a for n, a in ref.items() if n != "d_offset"}
+        check_d_offset_bound(x, gpu, what, causal=kw["causal"], window=kw["window"], scale=kw["scale"],
+                             dropout_p=kw["p"], rng_state=RNG)
+    compare({n: a for n, a in gpu.items() if n != "d_offset"}, ref, what, o_scale=dropout_o_scale(kw["p"]))
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5])
@@ -168,7 +180,7 @@ def test_dropout_parity_mla(p):
     shape = Shape(1, 257, 257, 2, 2, 192, 128)
     x = make_inputs(shape, 950, learnable_offset=True)
     kw = dict(causal=True, window=-1, st=LEARNABLE, scale=1 / np.sqrt(192), p=p)
-    compare(_gpu(x, det=True, **kw), _ref(x, **kw), f"mla p={p}")
+    _check(x, _gpu(x, det=True, **kw), _ref(x, **kw), f"mla p={p}", kw)
 
 
 def test_fixed_rng_state_is_reproducible_and_offset_changes_the_result():
@@ -218,4 +230,4 @@ def test_dropout_full_size_sampled():
     for b, g in ((0, 0), (3, 7)):
         # a unit takes the decisions of its own (b, h) in the full problem
         ref = _ref(slice_group(x, b, g, G), origin=(b, g * G), **kw)
-        compare(gpu_slice(gpu, b, g, G), ref, f"dropout unit (b={b}, g={g})")
+        compare(gpu_slice(gpu, b, g, G), ref, f"dropout unit (b={b}, g={g})", o_scale=dropout_o_scale(kw["p"]))

@@ -4,11 +4,13 @@
 offers `attention_dropout`.  The sequence diagrams of "[JAX] Add support for sink
 attention in JAX #2225" show the fused forward returning an rng_state that the fused
 backward takes.  The oracle reads this as a counter-based generator,
-Philox4x64-10 (Salmon et al., SC'11).  The generator is keyed by rng_state =
-(seed, offset), and its 16-bit fields decide each (query, key) pair.  These tests
-pin the oracle against things it does not compute itself:
-  * the generator against numpy's Philox bit generator, a library implementation of
-    the same published algorithm;
+Philox4x32-10 (Salmon et al., SC'11).  The generator is keyed by the seed of
+rng_state = (seed, offset), and its 16-bit fields decide each (query, key) pair.
+These tests pin the oracle against things it does not compute itself:
+  * the generator against the known-answer vectors published with the Random123
+    library (the SC'11 paper's reference implementation), and against Triton's
+    `tl.philox`, a library implementation of the same algorithm, run by Triton's CPU
+    interpreter;
   * the keep rate against binomial bounds;
   * p = 0 against the plain oracle;
   * the dropped forward and backward against torch autograd in fp64 on the same keep
@@ -16,6 +18,11 @@ pin the oracle against things it does not compute itself:
   * the gradients against central differences on tiny inputs (the decisions are fixed
     by the seed, so the function is smooth).
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -24,25 +31,93 @@ import oracle
 from oracle import LEARNABLE, OFF_BY_ONE, VANILLA
 from scaled_dot_product_tmem_gb300.inputs import Shape, make_inputs
 
-U64 = 2 ** 64 - 1
+U32 = 2 ** 32 - 1
 
 
 def _inp(shape, seed):
     return {k: x.double().numpy() for k, x in make_inputs(shape, seed, learnable_offset=True).items()}
 
 
-@pytest.mark.parametrize("counter,key", [
-    ((1, 0, 0, 0), (0, 0)),
-    ((7, 3, 2, 1), (12345, 678)),
-    ((2 ** 40 + 5, 2 ** 63, U64, 17), (U64, 2 ** 62 + 11)),
-    ((123456789, 987654321, 31, 4), (0x243F6A8885A308D3, 0x13198A2E03707344)),
-])
-def test_philox_matches_numpy_bit_generator(counter, key):
-    """numpy's Philox increments its counter before each block, so the block numpy
-    produces from counter c - 1 is the Philox of c (c0 >= 1 here: no carry)."""
-    start = np.array([counter[0] - 1, *counter[1:]], dtype=np.uint64)
-    ref = np.random.Philox(counter=start, key=np.array(key, dtype=np.uint64)).random_raw(4)
-    np.testing.assert_array_equal(oracle.philox4x64_10(counter, key), ref.astype(np.uint64))
+# Philox4x32-10 known-answer vectors of the Random123 distribution (counter, key, output)
+KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((U32, U32, U32, U32), (U32, U32), (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("counter,key,expected", KAT)
+def test_philox_known_answers(counter, key, expected):
+    np.testing.assert_array_equal(oracle.philox4x32_10(counter, key), np.array(expected, dtype=np.uint32))
+
+
+_TRITON_PHILOX = """
+import json, sys
+import torch, triton, triton.language as tl
+
+@triton.jit
+def philox_kernel(seed_ptr, ctr_ptr, out_ptr, N: tl.constexpr):
+    n = tl.arange(0, N)
+    seed = tl.load(seed_ptr + n)
+    a, b, c, d = tl.philox(seed, tl.load(ctr_ptr + 4 * n), tl.load(ctr_ptr + 4 * n + 1),
+                           tl.load(ctr_ptr + 4 * n + 2), tl.load(ctr_ptr + 4 * n + 3), 10)
+    tl.store(out_ptr + 4 * n, a)
+    tl.store(out_ptr + 4 * n + 1, b)
+    tl.store(out_ptr + 4 * n + 2, c)
+    tl.store(out_ptr + 4 * n + 3, d)
+
+args = json.loads(sys.stdin.read())
+n = len(args["seeds"])
+out = torch.zeros(4 * n, dtype=torch.int32)
+philox_kernel[(1,)](torch.tensor(args["seeds"], dtype=torch.int64), torch.tensor(args["ctr"], dtype=torch.int32),
+                    out, N=n)
+print(json.dumps(out.tolist()))
+"""
+
+
+def test_philox_matches_triton_library_generator():
+    """Triton's tl.philox(seed, c0, c1, c2, c3) is Philox4x32-10 with the key (low,
+    high) 32 bits of a 64-bit seed.  Its CPU interpreter (TRITON_INTERPRET=1, set
+    before Triton is imported, so in a child process) runs it without a GPU."""
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(20240607)
+    n = 16
+    ctr = rng.integers(0, 2 ** 32, size=(n, 4), dtype=np.uint64)
+    ctr[0] = (5, 0, 0, 0)
+    ctr[1] = (U32, 17, 2 ** 31, 123456789)
+    key = rng.integers(0, 2 ** 32, size=(n, 2), dtype=np.uint64)
+    key[0] = (0, 0)
+    key[1] = (U32, U32)
+    # signed carriers of the same bits: the seed as int64, the counters as int32 (32-bit
+    # counters select the 4 x 32-bit generator in tl.philox)
+    seeds = [int(np.uint64(k0) | (np.uint64(k1) << np.uint64(32))) - (2 ** 64 if k1 >= 2 ** 31 else 0)
+             for k0, k1 in key]
+    ctr32 = [int(x) - (2 ** 32 if x >= 2 ** 31 else 0) for x in ctr.ravel()]
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    res = subprocess.run([sys.executable, "-c", _TRITON_PHILOX], input=json.dumps({"seeds": seeds,
+                         "ctr": ctr32}), capture_output=True, text=True, env=env,
+                         timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    ref = np.array(json.loads(res.stdout.strip().splitlines()[-1]), dtype=np.int64).reshape(n, 4) & U32
+    for m in range(n):
+        np.testing.assert_array_equal(oracle.philox4x32_10(ctr[m], key[m]).astype(np.int64), ref[m])
+
+
+def test_decisions_follow_the_stated_counter_layout():
+    """Pair (b, h, i, j) reads the 16-bit field j % 2 of word i % 4 of the call with
+    counter (j / 2, i / 4, 65536 b + h, offset mod 2^32) under the key (seed low, high)."""
+    seed, off, b, h, t = 0x0123456789ABCDEF, 2 ** 32 + 9, 3, 65535, 30000
+    keep = oracle.dropout_keep(b, h, 9, 7, t / 65536.0, (seed, off))
+    for i in range(9):
+        for j in range(7):
+            w = oracle.philox4x32_10((j // 2, i // 4, 65536 * b + h, off & U32), (seed & U32, seed >> 32))
+            assert keep[i, j] == (((int(w[i % 4]) >> (16 * (j % 2))) & 0xFFFF) >= t)
+    # the offset counts modulo 2^32; batch entries and heads are below 65536
+    np.testing.assert_array_equal(keep, oracle.dropout_keep(b, h, 9, 7, t / 65536.0, (seed, off + 2 ** 33)))
+    for bad in ((65536, 0), (0, 65536)):
+        with pytest.raises(ValueError):
+            oracle.dropout_keep(*bad, 4, 4, 0.5, (1, 2))
 
 
 def test_threshold_rule():
