@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
   // Work tiles: (b, kv head, head split) groups in chunks of kKvChunk; within a chunk,
   // kv tile by kv tile (tile 0, the most work when causal, first) and group by group,
   // so a chunk's long tiles start early while its queries stay few enough to be shared
-  // in L2.  Persistent CTAs (PERSIST, at most one per SM) take the tiles in that order
+  // in L2.  With a bias broadcast over the batch, b is the innermost group index: the
+  // batch entries of one (kv head, kv tile) then run side by side, in step, and their
+  // reductions into the same dbias lines meet in L2.  Persistent CTAs (PERSIST, at most one per SM) take the tiles in that order
   // from a counter, as an SM would take blocks, so a tile's K/V load and first products
   // overlap the previous tile's epilogue; the producer takes each index and publishes
   // it to the other roles through a two-slot ring.  Every role walks the same tiles and
@@ -150,9 +152,15 @@ __global__ void __launch_bounds__(FUSE_DQ ? 480 : 352, 1)
     const int chunk = ti / per_chunk, within = ti % per_chunk;
     const int csize = min(kKvChunk, n_gr - chunk * kKvChunk);
     const int g = chunk * kKvChunk + within % csize;
-    t.split = g % p.ns;
-    t.hk = (g / p.ns) % p.H_kv;
-    t.b = g / (p.ns * p.H_kv);
+    if (BIAS && p.bias_sb == 0) {
+      t.b = g % p.B;
+      t.split = (g / p.B) % p.ns;
+      t.hk = g / (p.B * p.ns);
+    } else {
+      t.split = g % p.ns;
+      t.hk = (g / p.ns) % p.H_kv;
+      t.b = g / (p.ns * p.H_kv);
+    }
     t.h0 = t.hk * p.G + t.split * Gs;  // the first query head the tile walks
     t.n0 = (within / csize) * C::BN;
     t.mask = VL ? MaskSpec{entry_len(p.seq_q, t.b, p.S_q), entry_len(p.seq_kv, t.b, p.S_kv), p.causal, p.window}
