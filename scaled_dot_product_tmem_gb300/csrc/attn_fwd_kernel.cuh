@@ -382,9 +382,9 @@ __global__ void __launch_bounds__(320, 1)
     const float o_mul = F8 ? *p.descale_v : (DROP ? p.drop_scale : 1.f);
     [[maybe_unused]] DropState drop{};
     if constexpr (DROP) drop = DropState{p.rng[0], p.rng[1], p.drop_t};
-    // with a bias the scores are turned into log2-unit logits before the max, so the
-    // max and the exponent then take them as they are
-    const float sx = BIAS ? 1.f : sl2;
+    // with a bias the scores become s + bias / scale before the max; the max and the
+    // exponent then scale them by scale log2(e) as without one
+    const float sx = sl2;
     const bool bias_vec = BIAS && (p.S_kv % 8 == 0);
     int sc = 0, od = 0;  // s_ready / o_done phases consumed
     [[maybe_unused]] int nbc = 0;  // bias tiles consumed (BT)
@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
           if constexpr (BIAS) {
-            const uint64_t sl2x2b = f2_pack(sl2, sl2), l2e2b = f2_pack(kLog2e, kLog2e);
+            const float rsc = kLog2e / sl2;  // 1 / scale
+            const uint64_t rs2 = f2_pack(rsc, rsc);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float m = -INFINITY;
@@ -474,11 +475,12 @@ __global__ void __launch_bounds__(320, 1)
                 } else {
                   load_bias8(brow, k0 + 32 * q + 8 * e8, p.S_kv, bias_vec, bv);
                 }
-                // t = s sl2 + bias log2(e), two keys per paired multiply and fma
+                // y = s + bias / scale (so y scale log2(e) = s scale log2(e) + bias log2(e)),
+                // two keys per paired fma
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                   float* x = &s[32 * q + 8 * e8 + e];
-                  f2_unpack(f2_fma(f2_pack(x[0], x[1]), sl2x2b, f2_mul(f2_pack(bv[e], bv[e + 1]), l2e2b)), x[0], x[1]);
+                  f2_unpack(f2_fma(f2_pack(bv[e], bv[e + 1]), rs2, f2_pack(x[0], x[1])), x[0], x[1]);
                   m = fmax3(m, x[0], x[1]);
                 }
               }
