@@ -1237,11 +1237,12 @@ inline int launch_q_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   } else {
     if (p.bias) return -2;
     // Persistent CTAs (one per SM, tiles from the counter) for the plain kernels of
-    // full-length batches with d_qk = d_v when every tile is short: at most 8 kv tiles,
-    // so a CTA's fixed costs (the Q/dO load, the first products, the dQ epilogue) are a
-    // large share of a tile's time.
+    // full-length batches with d_qk = d_v when every tile has at most 32 kv tiles: a
+    // CTA's fixed costs (the Q/dO load, the first products, the dQ epilogue) then
+    // overlap the previous tile.  Measured faster up to 32 kv tiles (S <= 4096), level
+    // at 64.
     const long long max_kv = (p.S_kv + C::BN - 1) / C::BN;
-    if constexpr (D_QK == D_V) persist = !vl && p.tile_counter_q && tiles > n_sm && max_kv <= 8;
+    if constexpr (D_QK == D_V) persist = !vl && p.tile_counter_q && tiles > n_sm && max_kv <= 32;
     if (persist) {
       if constexpr (D_QK == D_V) kern = attn_bwd_q_kernel<D_QK, D_V, false, false, false, true>;
     } else {

@@ -515,8 +515,9 @@ static int launch_kvw_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const bool vl = p.seq_q || p.seq_kv;
   const long long tiles = (long long)((p.S_kv + C::BN - 1) / C::BN) * p.H_kv * p.B * p.ns;
   if (tiles <= 0 || tiles > 0x7fffffffLL) return -2;
-  // Persistent CTAs (one per SM, tiles from the counter) when every tile is short: at
-  // most 8 steps of 128 rows, the same rows as the fused-dQ kernel's 32 steps of 64.
+  // Persistent CTAs (one per SM, tiles from the counter) when every tile has at most 32
+  // steps of 128 rows: measured faster up to 32 (MHA at S <= 4096), slower at 128 and
+  // 256 (GQA at S = 4096 and 8192).
   static int n_sm = 0;
   if (n_sm == 0) {
     int dev = 0;
@@ -525,7 +526,7 @@ static int launch_kvw_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       return -1;
   }
   const long long max_steps = (long long)(p.G / p.ns) * ((p.S_q + C::BQ - 1) / C::BQ);
-  const bool persist = !vl && p.tile_counter && tiles > n_sm && max_steps <= 8;
+  const bool persist = !vl && p.tile_counter && tiles > n_sm && max_steps <= 32;
   auto kern = persist ? attn_bwd_kvw_kernel<D_QK, D_V, false, true>
                       : (vl ? attn_bwd_kvw_kernel<D_QK, D_V, true> : attn_bwd_kvw_kernel<D_QK, D_V, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;

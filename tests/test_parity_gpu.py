@@ -119,6 +119,11 @@ PERSIST_CASES = [
     ("mha_d128_window", Shape(8, 520, 520, 24, 24, 128, 128), True, 200, OFF_BY_ONE),
     # S_q < S_kv, causal: the kv tiles past the last query row see no query (empty tiles)
     ("mha_empty_tiles", Shape(8, 100, 300, 32, 32, 64, 64), True, -1, VANILLA),
+    # longer tiles with a ragged tail: 24 steps of 128 rows per kv tile and 24 kv tiles per
+    # query tile, inside the deterministic kernels' persistence bound (32 of each)
+    ("mha_long_tiles", Shape(2, 3000, 3000, 40, 40, 128, 128), True, -1, VANILLA),
+    # GQA, d = 64, a window: the dQ kernel's tiles (20 kv tiles) persistent
+    ("gqa_d64_window_q_tiles", Shape(2, 2500, 2500, 32, 8, 64, 64), True, 700, OFF_BY_ONE),
 ]
 
 
@@ -132,10 +137,11 @@ def test_persistent_kv_tiles_match_oracle(case, deterministic):
     x = make_inputs(shape, 31, learnable_offset=True)
     kw = dict(causal=causal, window=window, softmax_type=st, scale=None)
     gpu = gpu_run(x, deterministic=deterministic, **kw)
+    G = shape.H_q // shape.H_kv
     for b, g in ((0, 0), (shape.B - 1, shape.H_kv - 1)):
-        ref = oracle_run(slice_group(x, b, g, 1), **kw)
+        ref = oracle_run(slice_group(x, b, g, G), **kw)
         ref.pop("d_offset", None)
-        compare(gpu_slice(gpu, b, g, 1), ref, f"{name} unit (b={b}, h={g})")
+        compare(gpu_slice(gpu, b, g, G), ref, f"{name} unit (b={b}, kv head {g})")
     if name == "mha_empty_tiles":
         assert np.all(gpu["dk"][:, 100:] == 0) and np.all(gpu["dv"][:, 100:] == 0)
 
