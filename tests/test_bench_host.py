@@ -36,6 +36,29 @@ def test_traffic_only_for_its_workload():
     assert bench.recorded_traffic(bench.WORKLOADS["mla_b2_s4096"], "bwd_kv") is None
 
 
+def test_traffic_record_is_dropped_once_its_sources_change(tmp_path, monkeypatch):
+    """roofline.traffic comes from an ncu record only while the kernel sources it names
+    still hash to the record's sha256; the deterministic path reads its own record."""
+    import hashlib
+    src = tmp_path / "kern.cu"
+    src.write_text("__global__ void k() {}\n")
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()
+    rec = {"sources": ["kern.cu"], "sources_sha256": digest,
+           "kernels": {"bwd_kv": {"dram_bytes_read": 300, "dram_bytes_write": 45}}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "kernel_traffic.json").write_text(json.dumps(
+        {"workloads": {"w": rec, "w:deterministic": dict(rec, kernels={"bwd_kv": {"dram_bytes_read": 7,
+                                                                               "dram_bytes_write": 1}})}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    wl = {"name": "w"}
+    assert bench.recorded_traffic(wl, "bwd_kv") == 345
+    assert bench.recorded_traffic(wl, "bwd_kv", det=True) == 8
+    assert bench.recorded_traffic(wl, "fwd") is None
+    src.write_text("__global__ void k() { }\n")
+    assert bench.recorded_traffic(wl, "bwd_kv") is None
+    assert bench.recorded_traffic(wl, "bwd_kv", det=True) is None
+
+
 def test_reference_arm_prints_one_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
                           "tiny_gqa_swa", "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
