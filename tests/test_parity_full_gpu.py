@@ -25,8 +25,14 @@ FULL = [
      [(0, 0), (63, 31)]),
     ("sweep_s512_gqa", Shape(64, 512, 512, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 512 + 8, [(5, 3)]),
     ("sweep_s512_mqa", Shape(64, 512, 512, 32, 1, 128, 128), True, -1, VANILLA, None, 1000 + 512 + 1, [(9, 0)]),
+    # S = 1024 MHA: both backward paths run persistent CTAs (tiles of 16 steps / 8 kv tiles)
+    ("sweep_s1024_mha", Shape(32, 1024, 1024, 32, 32, 128, 128), True, -1, VANILLA, None, 1000 + 1024 + 32,
+     [(0, 0), (31, 17)]),
     ("sweep_s2048_gqa", Shape(16, 2048, 2048, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 2048 + 8,
      [(15, 2)]),
+    # S = 4096 MHA: the deterministic path's persistent kernels at their 32-step bound
+    ("sweep_s4096_mha", Shape(8, 4096, 4096, 32, 32, 128, 128), True, -1, VANILLA, None, 1000 + 4096 + 32,
+     [(7, 30)]),
     ("sweep_s8192_gqa", Shape(4, 8192, 8192, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 8192 + 8, [(1, 5)]),
     ("sweep_s16384_gqa", Shape(2, 16384, 16384, 32, 8, 128, 128), True, -1, VANILLA, None, 1000 + 16384 + 8,
      [(1, 6)]),
