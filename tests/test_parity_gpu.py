@@ -124,6 +124,8 @@ PERSIST_CASES = [
     ("mha_long_tiles", Shape(2, 3000, 3000, 40, 40, 128, 128), True, -1, VANILLA),
     # GQA, d = 64, a window: the dQ kernel's tiles (20 kv tiles) persistent
     ("gqa_d64_window_q_tiles", Shape(2, 2500, 2500, 32, 8, 64, 64), True, 700, OFF_BY_ONE),
+    # non-causal and rectangular: every tile has the same length, S_q != S_kv
+    ("mha_d64_noncausal_rect", Shape(12, 200, 264, 32, 32, 64, 64), False, -1, LEARNABLE),
 ]
 
 
