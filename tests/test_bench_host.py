@@ -69,6 +69,9 @@ def test_reference_arm_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["dtype"] == "f64"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the same config keys as the GPU arm's line, so the two lines compare the same workload
+    assert d["config"] == bench.bench_config(bench.WORKLOADS["tiny_gqa_swa"], 1, False)
+    assert d["higher_is_better"] is True and d["unit"] == "TFLOP/s"
 
 
 def _rank(rank, world, port, q):
